@@ -1,0 +1,392 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix.
+
+Each test checks the oracle against something other than itself: numbers the
+pages print (tests/golden/), exact rational arithmetic, closed forms,
+invariants, and library routines for the special cases that reduce to them.
+All run on CPU.
+"""
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle as O
+
+
+def f16(v):
+    return np.asarray(v, dtype=np.float16)
+
+
+# ---------------------------------------------------------------------------
+# "What actually happens when you quantize a KV cache", section 3 steps 3-5
+# ---------------------------------------------------------------------------
+
+def test_worked_int4_group(golden):
+    kv, rows = golden("kvq_worked_group_int4.txt")
+    x = f16([float(r[1]) for r in rows])
+    res = O.quantize_groups(x, kv["bits"], kv["group_size"])
+    s = float(res["scale"][0])
+    # min / max / range as printed (inputs are fp16-rounded, 3-decimal agreement)
+    xd = x.astype(np.float64)
+    assert abs(xd.min() - kv["min"]) < 5e-4
+    assert abs(xd.max() - kv["max"]) < 5e-4
+    # scale: range/15 = 0.07667, stored as fp16 (rounded up: within one fp16 ulp)
+    assert abs(s - kv["scale"]) < 1e-4
+    assert s >= (xd.max() - xd.min()) / 15
+    assert abs(-xd.min() / s - kv["neg_min_over_scale"]) < 5e-3
+    assert float(res["zero"][0]) == kv["zero"]
+    # per-channel table: round column, code column, bits column
+    for i, r in enumerate(rows):
+        assert abs(float(x[i]) / s - float(r[2])) < 1e-2
+        assert int(np.rint(np.float32(x[i]) / np.float32(s))) == int(r[3])
+        assert int(res["codes"][i]) == int(r[4])
+        assert format(int(res["codes"][i]), "04b") == r[5]
+    xh = O.dequantize(res["codes"], res["scale"], res["zero"], 8)
+    # the page decodes with the exact s = range/15; the stored fp16 s is at most
+    # one fp16 ulp away, so x_hat may differ by |q - z| ulp plus the page's
+    # 4-decimal rounding
+    ulp = float(np.spacing(res["scale"][0]))
+    for i, r in enumerate(rows):
+        tol = abs(int(r[4]) - kv["zero"]) * ulp + 5e-5
+        assert abs(xh[i] - float(r[6])) <= tol
+        assert abs((xh[i] - xd[i]) - float(r[7])) <= tol + 5e-4   # x was rounded to fp16
+    assert np.abs(xh - xd).max() <= kv["error_bound"]
+    assert np.abs(xh - xd).max() <= s / 2
+
+
+def test_worked_group_packed_bytes(golden):
+    """Two codes per byte, even channel in the low nibble (step 5): the bytes
+    are read off the page's bits column, odd channel's bits first."""
+    kv, rows = golden("kvq_worked_group_int4.txt")
+    expect = [int(rows[2 * i + 1][5] + rows[2 * i][5], 2) for i in range(4)]
+    codes = np.array([int(r[4]) for r in rows], dtype=np.uint8)
+    packed = O.pack_codes(codes, 4)
+    assert list(packed) == expect
+    assert list(O.unpack_codes(packed, 4, 8)) == list(codes)
+    x = f16([float(r[1]) for r in rows])
+    res = O.quantize_groups(x, 4, 8)
+    assert list(O.pack_codes(res["codes"], 4)) == expect
+
+
+def test_outlier_group(golden):
+    kv, _ = golden("kvq_outlier_group_int4.txt")
+    x = f16(kv["values"])
+    res = O.quantize_groups(x, kv["bits"], kv["group_size"])
+    s = float(res["scale"][0])
+    assert abs(s - kv["scale"]) < 1e-3
+    assert abs(15 * s - kv["range"]) < 0.01
+    assert float(res["zero"][0]) == kv["zero"]
+    xh = O.dequantize(res["codes"], res["scale"], res["zero"], 8)
+    assert int((xh[:7] == 0.0).sum()) == kv["erased_channels"]
+    assert abs(xh[7] - 4.80) <= s / 2
+
+
+def test_asymmetric_step_finer_than_symmetric(golden):
+    kv, _ = golden("kvq_symmetric_vs_asymmetric.txt")
+    wk, rows = golden("kvq_worked_group_int4.txt")
+    x = f16([float(r[1]) for r in rows])
+    s = float(O.quantize_groups(x, 4, 8)["scale"][0])
+    assert abs(s - kv["asymmetric_scale"]) < 1e-4
+    assert abs(1 - s / kv["symmetric_scale"] - kv["finer_fraction"]) < 0.01
+
+
+# ---------------------------------------------------------------------------
+# Closed forms and exact arithmetic
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_exact_grid_roundtrip(bits):
+    """Values on an exactly representable grid spanning 2^b - 1 steps are
+    reproduced exactly, with the codes equal to the grid indices."""
+    qmax = (1 << bits) - 1
+    step = 2.0 ** -6
+    rng = np.random.default_rng(7)
+    for offset in (-100, -3, 0, 17, qmax // 2):
+        idx = np.concatenate([[0, qmax], rng.integers(0, qmax + 1, size=6)])
+        x = f16((idx - offset) * step)
+        res = O.quantize_groups(x, bits, 8)
+        assert float(res["scale"][0]) == step
+        assert float(res["zero"][0]) == offset
+        assert list(res["codes"]) == list(idx)
+        assert np.array_equal(O.dequantize(res["codes"], res["scale"], res["zero"], 8),
+                              x.astype(np.float64))
+
+
+def _exact_codes(x16, bits, s16):
+    """Rational-arithmetic codes for one group (Python round() is half-even)."""
+    qmax = (1 << bits) - 1
+    xs = [Fraction(float(v)) for v in x16]
+    s = Fraction(float(s16))
+    z = round(-min(xs) / s)
+    z = max(-O.ZERO_LIMIT, min(O.ZERO_LIMIT, z))
+    return [max(0, min(qmax, round(v / s) + z)) for v in xs], z
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_fp32_decisions_equal_exact_rounding(bits):
+    """The fp32 x/s and -min/s decisions give the codes exact arithmetic gives."""
+    rng = np.random.default_rng(11 + bits)
+    groups = []
+    for _ in range(600):
+        scale = 10.0 ** rng.uniform(-3, 2)
+        center = rng.normal() * scale * rng.choice([0.0, 1.0, 20.0])
+        groups.append(rng.normal(size=8) * scale + center)
+    # exact ties x/s = k + 1/2 with s = 2^-4
+    base = np.array([0.0, 15.0, 2.5, 3.5, 4.5, 0.5, 1.5, 14.5]) * 2.0 ** -4
+    groups.append(base if bits == 4 else np.concatenate([[0.0, 255.0], base[2:] * 16]) * 2.0 ** -4)
+    x16 = f16(np.stack(groups))
+    res = O.quantize_groups(x16, bits, 8)
+    for i in range(x16.shape[0]):
+        codes, z = _exact_codes(x16[i], bits, res["scale"][i, 0])
+        assert list(res["codes"][i]) == codes, i
+        assert float(res["zero"][i, 0]) == z
+
+
+def test_ties_round_half_even():
+    x = f16(np.array([0.0, 15.0, 2.5, 3.5, 4.5, 0.5, 1.5, 14.5]) * 2.0 ** -4)
+    res = O.quantize_groups(x, 4, 8)
+    assert float(res["scale"][0]) == 2.0 ** -4
+    assert list(res["codes"]) == [0, 15, 2, 4, 4, 0, 2, 14]
+
+
+def test_fp16_round_up_is_smallest_upper_bound():
+    rng = np.random.default_rng(3)
+    d = np.concatenate([10.0 ** rng.uniform(-9, 4.5, size=20000),
+                        np.array([0.0, 2.0 ** -24, 1.0, 65504.0, 2.0 ** -14])])
+    h = O.fp16_round_up(d)
+    hd = h.astype(np.float64)
+    assert np.all(hd >= d)
+    below = np.nextafter(h, np.float16(-np.inf)).astype(np.float64)
+    assert np.all((below < d) | (hd == 0.0))
+    exact = f16(rng.normal(size=1000)).astype(np.float64)
+    assert np.array_equal(O.fp16_round_up(np.abs(exact)).astype(np.float64), np.abs(exact))
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+@pytest.mark.parametrize("g", [8, 16, 32, 64, 128])
+def test_roundtrip_error_bound(bits, g):
+    """|x - x_hat| <= s/2 for every element of every unflagged group
+    ("What actually happens when you quantize a KV cache", section 4)."""
+    rng = np.random.default_rng(bits * 1000 + g)
+    D = 128 if g <= 128 else g
+    rows = [rng.normal(size=(64, D)),
+            rng.normal(size=(16, D)) * 10.0 ** rng.uniform(-4, 2, size=(16, 1)),
+            np.abs(rng.normal(size=(16, D))) + 3.0,         # all-positive groups
+            -np.abs(rng.normal(size=(16, D))) - 0.5,        # all-negative groups
+            rng.standard_cauchy(size=(16, D)).clip(-6e4, 6e4)]
+    x16 = f16(np.concatenate(rows))
+    res = O.quantize_groups(x16, bits, g)
+    ok = res["flags"] == 0
+    xh = O.dequantize(res["codes"], res["scale"], res["zero"], g)
+    err = np.abs(xh - x16.astype(np.float64)).reshape(x16.shape[0], D // g, g).max(-1)
+    half = res["scale"].astype(np.float64) / 2
+    assert ok.mean() > 0.9
+    assert np.all(err[ok] <= half[ok])
+
+
+def test_degenerate_constant_groups():
+    vals = [0.0, -0.0, 1.5, -2.25, 6e-8, -6e-8, 65504.0, -65504.0]
+    x16 = f16(np.repeat(np.array(vals)[:, None], 8, axis=1))
+    res = O.quantize_groups(x16, 4, 8)
+    assert np.all(res["codes"] == 0)
+    assert np.all(res["flags"] == 0)
+    xh = O.dequantize(res["codes"], res["scale"], res["zero"], 8)
+    assert np.array_equal(xh, x16.astype(np.float64))
+
+
+def test_zero_point_outside_fp16_integers_is_clamped_and_flagged():
+    x16 = f16([[1000.0, 1000.5, 1000.0, 1000.0, 1000.0, 1000.5, 1000.0, 1000.0]])
+    res = O.quantize_groups(x16, 4, 8)
+    assert res["flags"][0, 0] == O.ZERO_CLAMPED
+    assert float(res["zero"][0, 0]) == -O.ZERO_LIMIT
+
+
+def test_nonfinite_group_is_zeroed_and_flagged():
+    x16 = f16([[1.0, np.inf, 0.0, 0.5, 0.25, 0.0, 0.0, 0.0],
+               [1.0, 2.0, 3.0, 4.0, 5.0, 6.0, 7.0, 8.0]])
+    res = O.quantize_groups(x16, 4, 8)
+    assert res["flags"][0, 0] == O.NONFINITE and res["flags"][1, 0] == 0
+    assert float(res["scale"][0, 0]) == 0.0 and float(res["zero"][0, 0]) == 0.0
+    assert np.all(res["codes"][0] == 0)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_pack_unpack_identity(bits):
+    rng = np.random.default_rng(5)
+    codes = rng.integers(0, 1 << bits, size=(7, 64), dtype=np.uint8)
+    packed = O.pack_codes(codes, bits)
+    assert packed.shape[-1] == 64 * bits // 8
+    assert np.array_equal(O.unpack_codes(packed, bits, 64), codes)
+
+
+# ---------------------------------------------------------------------------
+# Byte accounting
+# ---------------------------------------------------------------------------
+
+def test_fp16_cache_sizes(golden):
+    _, rows = golden("fp16_cache_sizes.txt")
+    assert len(rows) >= 10
+    for r in rows:
+        layers, kvh, hd, nbytes, tokens, expect, tol = map(int, r[2:9])
+        assert nbytes == 2
+        got = O.kv_cache_bytes(layers, kvh, hd, tokens, 16)
+        assert abs(got - expect) <= tol, r[1]
+
+
+def test_quantized_byte_accounting(golden):
+    kv, rows = golden("kvq_byte_accounting.txt")
+    L, H, D = kv["layers"], kv["kv_heads"], kv["head_dim"]
+    assert O.kv_cache_bytes(1, H, D, 1, 16) == kv["fp16_bytes_per_token_per_layer"]
+    # one 128-channel group record: 64 B of codes + 4 B header
+    assert O.kv_cache_bytes(1, 1, 128, 1, 4, 128) // 2 == kv["group128_record_bytes"]
+    assert O.kv_cache_bytes(1, 1, 128, 1, 16) // 2 == kv["group128_fp16_bytes"]
+    fp16 = O.kv_cache_bytes(L, H, D, 1, 16)
+    int4 = O.kv_cache_bytes(L, H, D, 1, 4, 128)
+    assert fp16 == kv["fp16_element_bytes_per_token"] == kv["fp16_total_per_token_kib"] * 1024
+    groups = 2 * L * H * (D // 128)
+    assert groups == kv["int4_g128_header_groups_per_token"]
+    assert groups * 4 == kv["int4_g128_header_bytes_per_token"]
+    assert int4 - groups * 4 == kv["int4_g128_element_bytes_per_token"]
+    assert int4 == kv["int4_g128_total_per_token_kib"] * 1024
+    T = kv["seq_tokens"]
+    assert O.kv_cache_bytes(L, H, D, T, 16) == kv["fp16_seq_gib"] * 2 ** 30
+    assert O.kv_cache_bytes(L, H, D, T, 4, 128) == kv["int4_g128_seq_mib"] * 2 ** 20
+    for r in rows:
+        g, hdr_bits, eff_bits, ratio = int(r[1]), float(r[2]), float(r[3]), float(r[4])
+        per_tok = O.kv_cache_bytes(L, H, D, 1, 4, g)
+        values = 2 * L * H * D
+        assert abs(per_tok * 8 / values - eff_bits) < 1e-9
+        assert abs(per_tok * 8 / values - 4 - hdr_bits) < 1e-9
+        assert abs(fp16 / per_tok - ratio) < 0.005
+
+
+# ---------------------------------------------------------------------------
+# Attention: cached decode vs recompute, batching, GQA, split merge
+# ---------------------------------------------------------------------------
+
+def _toy_model(d, vocab, seed):
+    rng = np.random.default_rng(seed)
+    E = rng.normal(size=(vocab, d))
+    Wq, Wk, Wv, Wo = (rng.normal(size=(d, d)) * 0.1 for _ in range(4))
+    Wlm = rng.normal(size=(d, vocab)) * 0.1
+    return E, Wq, Wk, Wv, Wo, Wlm
+
+
+def test_append_then_attend_work_counters(golden):
+    """Naive re-forward vs prefill+decode through the oracle's attention:
+    same tokens, and the page's work counters -- which hold only if each
+    decode step scores every cached row including the one just appended."""
+    kv, _ = golden("decode_work_counters.txt")
+    d, vocab = 16, 64
+    E, Wq, Wk, Wv, Wo, Wlm = _toy_model(d, vocab, 0)
+    scale = 1.0 / np.sqrt(d)
+    prompt = [5, 9, 2, 41][:kv["prompt_tokens"]]
+    n_new = kv["new_tokens"]
+
+    work = {"proj": 0, "scores": 0}
+
+    def forward(tokens):
+        x = E[tokens]
+        work["proj"] += 3 * len(tokens)
+        work["scores"] += len(tokens) ** 2
+        ctx = O.full_causal(x @ Wq, x @ Wk, x @ Wv, scale)
+        return (ctx @ Wo) @ Wlm
+
+    tokens = list(prompt)
+    for _ in range(n_new):
+        tokens.append(int(np.argmax(forward(tokens)[-1])))
+    naive_tokens, naive = tokens, dict(work)
+
+    work = {"proj": 0, "scores": 0}
+    x = E[prompt]
+    cache_k, cache_v = x @ Wk, x @ Wv
+    work["proj"] += 3 * len(prompt)
+    work["scores"] += len(prompt) ** 2
+    logits = ((O.full_causal(x @ Wq, cache_k, cache_v, scale) @ Wo) @ Wlm)[-1]
+    tokens = list(prompt)
+    for _ in range(n_new):
+        nxt = int(np.argmax(logits))
+        tokens.append(nxt)
+        e = E[nxt]
+        q, k, v = e @ Wq, e @ Wk, e @ Wv
+        work["proj"] += 3
+        cache_k = np.vstack([cache_k, k])
+        cache_v = np.vstack([cache_v, v])
+        work["scores"] += cache_k.shape[0]
+        ctx = O.attend(q[None], cache_k, cache_v, scale)[0]
+        logits = (ctx @ Wo) @ Wlm
+    cached = dict(work)
+
+    assert tokens == naive_tokens
+    assert naive == {"proj": kv["naive_proj"], "scores": kv["naive_scores"]}
+    assert cached == {"proj": kv["cached_proj"], "scores": kv["cached_scores"]}
+
+
+@pytest.mark.parametrize("T,D", [(1, 4), (5, 8), (16, 8), (9, 3)])
+def test_decode_row_equals_full_causal_last_row(T, D):
+    rng = np.random.default_rng(T * 31 + D)
+    Q, K, V = (rng.normal(size=(T, D)) for _ in range(3))
+    scale = 1.0 / np.sqrt(D)
+    full = O.full_causal(Q, K, V, scale)
+    for t in range(1, T + 1):
+        row = O.attend(Q[t - 1:t], K[:t], V[:t], scale)[0]
+        assert np.abs(row - full[t - 1]).max() <= 1e-12
+
+
+def test_batch_equals_solo_runs():
+    rng = np.random.default_rng(2)
+    B, Hq, Hkv, D, Lmax = 3, 4, 2, 8, 12
+    q = rng.normal(size=(B, Hq, D))
+    K = rng.normal(size=(B, Hkv, Lmax, D))
+    V = rng.normal(size=(B, Hkv, Lmax, D))
+    lens = [12, 1, 7]
+    batched = O.decode_attention(q, K, V, lens)
+    for b in range(B):
+        solo = O.decode_attention(q[b:b + 1], K[b:b + 1], V[b:b + 1], [lens[b]])
+        assert np.array_equal(batched[b], solo[0])
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(4, 4), (4, 1), (8, 2), (14, 2)])
+def test_gqa_matches_sdpa_enable_gqa(Hq, Hkv):
+    """Special case reducing to a library routine: PyTorch's fp64 CPU
+    scaled_dot_product_attention with enable_gqa, the call the batched
+    decode step of "Serving many users at once" makes."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(Hq * 10 + Hkv)
+    B, D, L = 2, 16, 9
+    q = rng.normal(size=(B, Hq, D))
+    K = rng.normal(size=(B, Hkv, L, D))
+    V = rng.normal(size=(B, Hkv, L, D))
+    ours = O.decode_attention(q, K, V, [L] * B)
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q)[:, :, None, :], torch.from_numpy(K), torch.from_numpy(V),
+        enable_gqa=True)[:, :, 0, :].numpy()
+    assert np.abs(ours - ref).max() <= 1e-12
+
+
+def test_textbook_softmax_special_case():
+    """G = 1: softmax(q K^T / sqrt(d)) V with scipy's softmax."""
+    special = pytest.importorskip("scipy.special")
+    rng = np.random.default_rng(9)
+    q, K, V = rng.normal(size=(1, 32)), rng.normal(size=(40, 32)), rng.normal(size=(40, 32))
+    ref = special.softmax(K @ q[0] / np.sqrt(32)) @ V
+    assert np.abs(O.attend(q, K, V, 1 / np.sqrt(32))[0] - ref).max() <= 1e-12
+
+
+@pytest.mark.parametrize("S", [1, 2, 3, 7])
+def test_split_merge_equals_single_pass(S):
+    rng = np.random.default_rng(S)
+    G, D, L = 3, 16, 50
+    q, K, V = rng.normal(size=(G, D)), rng.normal(size=(L, D)) * 3, rng.normal(size=(L, D))
+    scale = 1 / 4
+    cuts = np.sort(rng.integers(0, L + 1, size=S - 1))
+    bounds = [0, *cuts.tolist(), L]          # partitions may contain empty slices
+    parts = [O.attend_partial(q, K[a:b], V[a:b], scale) for a, b in zip(bounds[:-1], bounds[1:])]
+    assert np.abs(O.lse_merge(parts) - O.attend(q, K, V, scale)).max() <= 1e-12
+
+
+def test_empty_cache_gives_zeros():
+    q = np.ones((2, 4))
+    assert np.array_equal(O.attend(q, np.zeros((0, 4)), np.zeros((0, 4)), 0.5), np.zeros((2, 4)))
+    parts = [O.attend_partial(q, np.zeros((0, 4)), np.zeros((0, 4)), 0.5)] * 3
+    assert np.array_equal(O.lse_merge(parts), np.zeros((2, 4)))
