@@ -1,0 +1,476 @@
+#!/usr/bin/env python
+"""Decode-step benchmark of the quantized KV-cache library on one node.
+
+One step = for every layer's cache: kvq_append of one new K/V token per
+sequence, then kvq_decode_attn over the whole cache (the new row included).
+Workload (7B-class MHA layer): batch 8, 4096 cached tokens per sequence,
+32 query = 32 KV heads, head_dim 128, INT4 group-32 cache, 32 distinct layer
+caches per step (5.4 GB working set, far above the 129 MB L2).
+
+value      tokens/s, one token = one sequence through one attention layer
+           (B x layers per step), device-timed with CUDA events over a
+           CUDA-graph replay of the step, inputs resident in HBM.
+e2e        the same metric with every step's q/k/v copied from pinned host
+           memory and the outputs copied back inside the timed region.
+roofline   algorithmic bytes of one kvq_decode_attn call (codes + scales +
+           zeros + q + out) / its average duration (events around each call).
+cpu_baseline  the CPU oracle timed on a bounded sample (one sequence, all
+           heads, one layer per step) on this host.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kvq|reference]
+Under torchrun (N > 1) each rank runs its own replica of the workload on its
+own GPU (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn tokens/s and achieved KV HBM GB/s (% of GB300 peak), 1 GPU"
+UNIT = "tokens/s"
+WORKLOAD = "mha7b"
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def rank_info():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def workload_config(w, bits, layers):
+    return {
+        "workload": f"{w.name}: batch {w.batch} x {w.ctx[0]} cached tokens (+1 appended), "
+                    f"{w.num_q_heads} q / {w.num_kv_heads} kv heads, head_dim {w.head_dim}, "
+                    f"{'fp16' if bits == 16 else f'INT{bits} group {w.group_size}'} dense cache, "
+                    f"{layers} layer caches per step",
+        "batch": w.batch,
+        "context": w.ctx[0] + 1,
+        "num_q_heads": w.num_q_heads,
+        "num_kv_heads": w.num_kv_heads,
+        "head_dim": w.head_dim,
+        "cache_bits": bits,
+        "group_size": w.group_size if bits != 16 else None,
+        "layers_per_step": layers,
+        "token": "one sequence through one attention layer (append + decode attention)",
+        "l2": "inputs larger than L2: every step walks all layer caches",
+    }
+
+
+def decode_bytes(w, bits, rows):
+    """Algorithmic bytes of one decode call: codes + scale/zero + q + out."""
+    D = w.head_dim
+    per_row = D * bits // 8 + (0 if bits == 16 else 4 * (D // w.group_size))
+    kv = 2 * w.batch * w.num_kv_heads * rows * per_row
+    return kv + 2 * w.batch * w.num_q_heads * D * 2
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.dev = device_index
+
+    def start(self):
+        try:
+            import torch
+            ident = None
+            try:
+                ident = "GPU-" + str(torch.cuda.get_device_properties(self.dev).uuid)
+            except Exception:
+                ident = str(self.dev)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", ident, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline and reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_sample_setup(w, bits, seed, kv=None):
+    """Host inputs for one sequence (all KV heads) and its oracle-quantized
+    context.  kv: optional (k_ctx, v_ctx, k_new, v_new, q) fp16 numpy arrays."""
+    import numpy as np
+    import oracle as O
+    from quantized_kv_decode_gb300 import synth
+    if kv is None:
+        rng = synth.rng_for(seed)
+        outl = synth.outlier_channels(rng, w.num_kv_heads, w.head_dim)
+        k, v = synth.host_kv(rng, 1, w.ctx[0], w.num_kv_heads, w.head_dim, outl)
+        kn, vn = synth.host_kv(rng, 1, 1, w.num_kv_heads, w.head_dim, outl)
+        q = synth.host_q(rng, 1, w.num_q_heads, w.head_dim)
+        kv = (k, v, kn, vn, q)
+    k, v, kn, vn, q = kv
+    ctx = [O.quantize_groups(np.transpose(x, (0, 2, 1, 3)), bits, w.group_size) for x in (k, v)]
+    return dict(ctx=ctx, new=(kn, vn), q=q)
+
+
+def oracle_step(w, bits, s):
+    """The oracle's decode step for the sampled sequence: quantize the new
+    token, dequantize the cache, attend."""
+    import numpy as np
+    import oracle as O
+    hats = []
+    for r, new in zip(s["ctx"], s["new"]):
+        n = O.quantize_groups(np.transpose(new, (0, 2, 1, 3)), bits, w.group_size)
+        codes = np.concatenate([r["codes"], n["codes"]], axis=2)
+        scale = np.concatenate([r["scale"], n["scale"]], axis=2)
+        zero = np.concatenate([r["zero"], n["zero"]], axis=2)
+        hats.append(O.dequantize(codes, scale, zero, w.group_size))
+    return O.decode_attention(s["q"], hats[0], hats[1], [w.ctx[0] + 1])
+
+
+def time_oracle(w, bits, s, steps, warmup):
+    for _ in range(warmup):
+        oracle_step(w, bits, s)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle_step(w, bits, s)
+    return (time.perf_counter() - t0) / steps
+
+
+def run_reference(args):
+    rank, world, _ = rank_info()
+    if rank != 0:
+        return
+    from quantized_kv_decode_gb300 import synth
+    w = synth.WORKLOADS[WORKLOAD]
+    bits = 4
+    s = oracle_sample_setup(w, bits, w.seed)
+    t = time_oracle(w, bits, s, args.steps, args.warmup)
+    value = 1.0 / t
+    sample = (f"one sequence ({w.num_q_heads} heads, {w.ctx[0] + 1} rows) through one layer "
+              f"per step; context pre-quantized by the oracle before timing")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w, bits, 1),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def build_layers(w, bits, layers, dev, seed, torch, K, synth):
+    """Populate one cache per layer with device-drawn fp16 K/V; per-layer
+    step inputs q, k_new, v_new."""
+    import numpy as np
+    cap = ((w.ctx[0] + 1 + 15) // 16) * 16
+    desc = K.make_desc(bits, w.group_size if bits != 16 else 0, w.num_kv_heads, w.head_dim,
+                       K.KVQ_DENSE, cap)
+    zeros = torch.zeros(w.batch, dtype=torch.int32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    caches, qs, kns, vns, host_slices = [], [], [], [], None
+    for l in range(layers):
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(seed * 100003 + l)
+        outl = synth.outlier_channels(np.random.default_rng(seed * 100003 + l), w.num_kv_heads,
+                                      w.head_dim)
+        k, v = synth.device_kv(gen, w.batch, w.ctx[0], w.num_kv_heads, w.head_dim, outl, dev)
+        kn, vn = synth.device_kv(gen, w.batch, 1, w.num_kv_heads, w.head_dim, outl, dev)
+        q = torch.randn((w.batch, w.num_q_heads, w.head_dim), generator=gen, device=dev).half()
+        cache = K.KVCache.allocate(desc, w.batch, dev)
+        K.kvq_append(cache, k, v, zeros, status)
+        if l == 0:
+            host_slices = (k[:1].cpu().numpy(), v[:1].cpu().numpy(), kn[:1].cpu().numpy(),
+                           vn[:1].cpu().numpy(), q[:1].cpu().numpy())
+        del k, v
+        caches.append(cache)
+        qs.append(q)
+        kns.append(kn)
+        vns.append(vn)
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"populate flagged status {int(status.item()):#x}")
+    return desc, caches, qs, kns, vns, host_slices
+
+
+def run_gpu_arm(args):
+    import numpy as np
+    import torch
+
+    rank, world, local = rank_info()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    from quantized_kv_decode_gb300 import build as kbuild
+    kbuild.build()
+    import quantized_kv_decode_gb300 as K
+    from quantized_kv_decode_gb300 import synth
+
+    w = synth.WORKLOADS[WORKLOAD]
+    bits = 4
+    layers = args.layers or w.layers
+    rows = w.ctx[0] + 1
+    seed = w.seed + 7919 * rank
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+
+    results = {}
+    for fmt in ((bits, 16) if args.fp16_comparator else (bits,)):
+        desc, caches, qs, kns, vns, host_slices = build_layers(
+            w, fmt, layers, dev, seed, torch, K, synth)
+        stream = torch.cuda.Stream(device=dev)
+        lens_before = torch.full((w.batch,), w.ctx[0], dtype=torch.int32, device=dev)
+        lens = lens_before + 1
+        splits = K.kvq_decode_num_splits(desc, w.batch, w.num_q_heads, rows, 0)
+        ws_bytes = K.kvq_decode_workspace_size(desc, w.batch, w.num_q_heads, rows, 0)
+        ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        outs = [torch.empty_like(q) for q in qs]
+
+        def step(s):
+            for l in range(layers):
+                K.kvq_append(caches[l], kns[l], vns[l], lens_before, status, stream=s)
+                K.kvq_decode_attn(caches[l], qs[l], lens, rows, outs[l], ws, status, stream=s)
+
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                step(stream)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step(stream)
+        torch.cuda.synchronize()
+
+        with torch.cuda.stream(stream):
+            for _ in range(max(args.warmup, 3)):
+                graph.replay()
+        torch.cuda.synchronize()
+        barrier()
+
+        clocks = ClockSampler(dev.index)
+        if fmt == bits:
+            clocks.start()
+            time.sleep(0.3)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(args.steps):
+                graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        ms_total = max_over_ranks(e0.elapsed_time(e1))
+        clk = clocks.stop() if fmt == bits else None
+
+        # per-call duration of kvq_decode_attn, events on the launching stream
+        evs = []
+        with torch.cuda.stream(stream):
+            for rep in range(3):
+                for l in range(layers):
+                    a = torch.cuda.Event(enable_timing=True)
+                    b = torch.cuda.Event(enable_timing=True)
+                    K.kvq_append(caches[l], kns[l], vns[l], lens_before, status, stream=stream)
+                    a.record(stream)
+                    K.kvq_decode_attn(caches[l], qs[l], lens, rows, outs[l], ws, status,
+                                      stream=stream)
+                    b.record(stream)
+                    evs.append((a, b))
+        torch.cuda.synchronize()
+        call_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        if int(status.item()) != 0:
+            raise RuntimeError(f"device status {int(status.item()):#x}")
+
+        # end to end: inputs from pinned host memory, outputs back, per step
+        h_q = [q.cpu().pin_memory() for q in qs]
+        h_k = [k.cpu().pin_memory() for k in kns]
+        h_v = [v.cpu().pin_memory() for v in vns]
+        h_o = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
+        h2d = sum(t.numel() * t.element_size() for t in h_q + h_k + h_v)
+        d2h = sum(t.numel() * t.element_size() for t in h_o)
+
+        def e2e_step():
+            for l in range(layers):
+                qs[l].copy_(h_q[l], non_blocking=True)
+                kns[l].copy_(h_k[l], non_blocking=True)
+                vns[l].copy_(h_v[l], non_blocking=True)
+            graph.replay()
+            for l in range(layers):
+                h_o[l].copy_(outs[l], non_blocking=True)
+
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        f0 = torch.cuda.Event(enable_timing=True)
+        f1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            f0.record(stream)
+            for _ in range(args.steps):
+                e2e_step()
+            f1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e2e_ms = max_over_ranks(f0.elapsed_time(f1))
+
+        tokens = world * w.batch * layers * args.steps
+        results[fmt] = dict(
+            value=tokens / (ms_total / 1e3), ms_per_step=ms_total / args.steps,
+            e2e=tokens / (e2e_ms / 1e3), h2d=h2d, d2h=d2h, call_ms=call_ms, splits=splits,
+            bytes=decode_bytes(w, fmt, rows), clocks=clk, host_slices=host_slices,
+            out0=outs[0][:1].float().cpu().numpy(),
+            launches=args.steps * layers * (2 + (1 if splits > 1 else 0)))
+        del caches, graph
+        torch.cuda.empty_cache()
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    r = results[bits]
+    peak, peak_kind = measured_peaks()
+    achieved = r["bytes"] / (r["call_ms"] / 1e3) / 1e9
+    traffic = load_profiled_traffic()
+    line = {
+        "metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": r["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": dict(workload_config(w, bits, layers), splits=r["splits"],
+                       parallelism=f"replicas x{world}" if world > 1 else "single GPU"),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": traffic,
+                     "kernel": "kvq_decode_attn (decode kernel + split merge)",
+                     "bytes_per_launch": r["bytes"], "avg_launch_us": r["call_ms"] * 1e3},
+        "e2e": {"value": r["e2e"], "unit": UNIT, "h2d_bytes_per_step": r["h2d"],
+                "d2h_bytes_per_step": r["d2h"]},
+        "gpu_launches": r["launches"],
+        "clocks": r["clocks"],
+    }
+    if 16 in results:
+        f = results[16]
+        line["fp16_cache"] = {
+            "value": f["value"], "unit": UNIT, "ms_per_step": f["ms_per_step"],
+            "achieved_gbs": f["bytes"] / (f["call_ms"] / 1e3) / 1e9,
+            "bytes_per_launch": f["bytes"], "avg_launch_us": f["call_ms"] * 1e3,
+            "speedup_int4_vs_fp16": r["value"] / f["value"]}
+    if world == 1 and not args.no_cpu_baseline:
+        s = oracle_sample_setup(w, bits, None, kv=r["host_slices"])
+        ref = oracle_step(w, bits, s)
+        got = r["out0"]
+        err = float(np.abs(got - ref).max())
+        rel = float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+        t = time_oracle(w, bits, s, args.cpu_steps, 1)
+        line["cpu_baseline"] = {
+            "value": 1.0 / t, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"one sequence of layer 0 ({w.num_q_heads} heads, {rows} rows) per step, "
+                      f"{args.cpu_steps} steps; context pre-quantized by the oracle"}
+        line["parity_sample"] = {"max_abs": err, "rel_l2": rel,
+                                 "what": "layer 0, sequence 0, all heads vs the oracle"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def load_profiled_traffic():
+    """DRAM bytes per launch of the decode kernel from the committed ncu
+    summary, or None when no capture matches the current kernel."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d.get(WORKLOAD)
+    except Exception:
+        return None
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
+    ap.add_argument("--layers", type=int, default=0)
+    ap.add_argument("--cpu-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fp16-comparator", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,201 @@
+/*
+ * kvq.h -- C ABI of the quantized KV-cache decode-attention library.
+ *
+ * The library implements the decode hot path of a transformer whose KV cache
+ * is stored as group-wise asymmetric INT4/INT8 codes:
+ *
+ *   kvq_append       quantize new K/V vectors into the cache
+ *                    ("What actually happens when you quantize a KV cache",
+ *                    section 3 steps 2-5 and section 4: per group s =
+ *                    (max-min)/(2^b-1), z = round(-min/s), q = clamp(round(x/s)
+ *                    + z, 0, 2^b-1); two INT4 codes per byte, even channel in
+ *                    the low nibble; fp16 scale and zero kept in their own
+ *                    contiguous arrays);
+ *   kvq_decode_attn  one decode row per query head over every cached token of
+ *                    its sequence, the token just appended included
+ *                    ("Quantization & inference optimisation", "Prefill, then
+ *                    decode": append, then attend without a mask; "Serving
+ *                    many users at once", batched decode_step with per-user
+ *                    lengths and grouped-query heads), reading the codes and
+ *                    dequantizing x_hat = (q - z) * s in registers
+ *                    ("What actually happens ...", section 6).
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers marked "device" are CUDA device memory owned by the caller; the
+ *     library never allocates, frees or retains them.  Arrays must be
+ *     16-byte aligned.  fp16 data is passed as uint16_t (IEEE binary16 bits).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Work is enqueued asynchronously; nothing synchronizes.
+ *   - Errors that the host can see (bad sizes, null pointers, unsupported
+ *     shapes, too small a workspace) are returned synchronously and nothing
+ *     is launched.  A failed launch returns KVQ_ERR_CUDA.
+ *   - Errors that only the data reveals (a length beyond the cache, a bad
+ *     block-table entry, a group the format cannot store) are OR-ed as
+ *     KVQ_FLAG_* bits into *dev_status (a device uint32_t, may be NULL) and
+ *     the offending unit is skipped as documented per call; read the word
+ *     after the stream has synchronized.  No kernel traps or waits.
+ *
+ * Cache layouts (one instance for K, one for V; the same shapes for both):
+ *   row_bytes = head_dim * bits / 8;  groups = head_dim / group_size
+ *   DENSE  codes  [batch][num_kv_heads][capacity][row_bytes]       uint8
+ *          scale  [batch][num_kv_heads][capacity][groups]          fp16
+ *          zero   same shape as scale
+ *          token p of sequence b lives in slot p (0 <= p < capacity).
+ *   PAGED  codes  [num_pages][num_kv_heads][page_size][row_bytes]   uint8
+ *          scale, zero  [num_pages][num_kv_heads][page_size][groups]
+ *          block_table [batch][max_blocks_per_seq] int32 (device);
+ *          token p of sequence b lives in page block_table[b][p / page_size]
+ *          at offset p % page_size.  Pages may be shared by sequences.
+ *   bits == 16 stores the fp16 vectors themselves in the codes arrays
+ *   (row_bytes = 2 * head_dim) and uses no scale/zero arrays.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misaligned array      */
+  KVQ_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. head_dim 512) */
+  KVQ_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required    */
+  KVQ_ERR_CUDA = 4          /* a CUDA runtime call or launch failed          */
+} kvq_status;
+
+/* Bits OR-ed into the caller's device status word. */
+#define KVQ_FLAG_SEQ_LEN      0x1u /* position/length outside the cache        */
+#define KVQ_FLAG_BLOCK_TABLE  0x2u /* block-table entry outside [0,num_pages)  */
+#define KVQ_FLAG_ZERO_CLAMPED 0x4u /* zero-point outside +-2048, clamped       */
+#define KVQ_FLAG_NONFINITE    0x8u /* group held inf/NaN, stored as zeros      */
+
+typedef enum { KVQ_DENSE = 0, KVQ_PAGED = 1 } kvq_layout;
+
+typedef struct {
+  int32_t bits;               /* 4 or 8 (quantized), 16 (fp16 cache)          */
+  int32_t group_size;         /* channels per group, multiple of 8, divides
+                                 head_dim; ignored when bits == 16            */
+  int32_t num_kv_heads;       /* >= 1                                          */
+  int32_t head_dim;           /* 64, 128 or 256                                */
+  int32_t layout;             /* kvq_layout                                    */
+  int32_t capacity;           /* DENSE: token slots per sequence;
+                                 PAGED: tokens per page (multiple of 8)        */
+  int32_t num_pages;          /* PAGED only: pages in the pool                 */
+  int32_t max_blocks_per_seq; /* PAGED only: row length of block_table         */
+} kvq_cache_desc;
+
+typedef struct {              /* all device pointers, caller-owned             */
+  void* k_codes;
+  void* v_codes;
+  uint16_t* k_scale;
+  uint16_t* k_zero;
+  uint16_t* v_scale;
+  uint16_t* v_zero;
+  const int32_t* block_table; /* PAGED only                                    */
+} kvq_cache;
+
+/*
+ * Bytes of K+V cache that `tokens` positions of ONE sequence occupy in one
+ * layer: 2 * num_kv_heads * tokens * (row_bytes + 4 * groups), i.e. codes
+ * plus a 4-byte fp16 scale+zero header per group ("What actually happens
+ * when you quantize a KV cache", section 5; for bits == 16 the header is
+ * absent and this is 2 * kv_heads * head_dim * 2 bytes per token, the
+ * formula of "Quantization & inference optimisation", "What the cache
+ * costs").  Host arithmetic only.  Returns 0 for an invalid descriptor.
+ */
+size_t kvq_cache_bytes(const kvq_cache_desc* desc, int64_t tokens);
+
+/*
+ * Allocation sizes for one layer's cache: *codes_bytes for each of k_codes
+ * and v_codes, *header_bytes for each of k_scale, k_zero, v_scale, v_zero
+ * (0 when bits == 16).  DENSE sizes cover `batch` sequences of `capacity`
+ * slots; PAGED sizes cover num_pages pages (`batch` is ignored).
+ */
+kvq_status kvq_cache_array_bytes(const kvq_cache_desc* desc, int32_t batch,
+                                 size_t* codes_bytes, size_t* header_bytes);
+
+/*
+ * Quantize num_new new K and V vectors per sequence into the cache.
+ *
+ *   k_new, v_new     device fp16 [batch][num_new][num_kv_heads][head_dim]
+ *   seq_lens_before  device int32 [batch]: tokens already cached; token t of
+ *                    sequence b is written at position seq_lens_before[b]+t.
+ *   dev_status       device uint32 (may be NULL)
+ *
+ * Per group of group_size consecutive channels of one vector: min and max;
+ * s = fp16 rounded up from (max-min)/(2^bits-1) computed in fp64; z =
+ * round-half-even(-min/s) in fp32, stored as an fp16 integer; codes
+ * clamp(round-half-even(x/s) + z, 0, 2^bits-1) in fp32.  A constant group
+ * stores s = |min| (1 if min == 0) so that it decodes exactly.  A zero-point
+ * beyond +-2048 is clamped and flags KVQ_FLAG_ZERO_CLAMPED; a group with
+ * inf/NaN is stored as s = z = 0, codes 0, and flags KVQ_FLAG_NONFINITE.
+ * A position outside the cache (or an unmapped page) flags SEQ_LEN /
+ * BLOCK_TABLE and that vector is not written.  Lengths are not modified:
+ * the caller passes seq_lens_before + num_new to kvq_decode_attn.
+ */
+kvq_status kvq_append(const kvq_cache_desc* desc, const kvq_cache* cache,
+                      int32_t batch, int32_t num_new,
+                      const uint16_t* k_new, const uint16_t* v_new,
+                      const int32_t* seq_lens_before, uint32_t* dev_status,
+                      void* stream);
+
+/*
+ * Number of context splits kvq_decode_attn uses.  num_splits > 0 is taken
+ * as given (capped so that every split holds at least one token tile);
+ * num_splits == 0 lets the library choose from the SM count of the current
+ * device (needs a device; returns 0 if none is available).
+ */
+int32_t kvq_decode_num_splits(const kvq_cache_desc* desc, int32_t batch,
+                              int32_t num_q_heads, int32_t max_seq_len,
+                              int32_t num_splits);
+
+/*
+ * Workspace bytes kvq_decode_attn needs for these arguments (0 when the
+ * work runs in one split).  Same num_splits convention as above.
+ */
+size_t kvq_decode_workspace_size(const kvq_cache_desc* desc, int32_t batch,
+                                 int32_t num_q_heads, int32_t max_seq_len,
+                                 int32_t num_splits);
+
+/*
+ * Decode attention for one new query per sequence and query head.
+ *
+ *   q            device fp16 [batch][num_q_heads][head_dim]
+ *   seq_lens     device int32 [batch]: cached tokens to attend over, the one
+ *                just appended included.  0 gives a zero output row.
+ *   max_seq_len  host upper bound on every seq_lens[b]; sizes the splits.
+ *   num_splits   0 = library choice, else the split count (see above).
+ *   softmax_scale  0 -> 1/sqrt(head_dim).
+ *   out          device fp16 [batch][num_q_heads][head_dim]
+ *   workspace    device scratch of kvq_decode_workspace_size() bytes
+ *                (may be NULL when that size is 0); contents need no init.
+ *
+ * num_q_heads must be a multiple of num_kv_heads; query head h reads KV head
+ * h / (num_q_heads / num_kv_heads).  For each (b, h):
+ *   out = softmax(scale * q . k_hat_j) weighted sum of v_hat_j, j < seq_lens[b]
+ * with k_hat = (q_k - z) * s dequantized in registers, fp32 accumulation,
+ * an online softmax over token tiles and, when split, a log-sum-exp merge of
+ * the per-split partials.  A length below 0 or above min(max_seq_len,
+ * cache capacity) flags KVQ_FLAG_SEQ_LEN and yields a zero row; a token whose
+ * page is unmapped flags KVQ_FLAG_BLOCK_TABLE and is left out.
+ */
+kvq_status kvq_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache,
+                           int32_t batch, int32_t num_q_heads,
+                           const uint16_t* q, const int32_t* seq_lens,
+                           int32_t max_seq_len, int32_t num_splits,
+                           float softmax_scale, uint16_t* out,
+                           void* workspace, size_t workspace_bytes,
+                           uint32_t* dev_status, void* stream);
+
+/* Static, human-readable name of a status code. */
+const char* kvq_status_string(kvq_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

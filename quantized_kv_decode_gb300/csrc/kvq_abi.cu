@@ -1,0 +1,267 @@
+// Host side of the C ABI declared in include/kvq.h: argument validation,
+// cache geometry, split selection, workspace carving and kernel dispatch.
+// No function here allocates memory or synchronizes a stream.
+#include <math.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "kvq_internal.cuh"
+
+namespace kvq {
+
+namespace {
+
+constexpr size_t kAlign = 16;
+
+bool aligned(const void* p) { return ((uintptr_t)p % kAlign) == 0; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Validates a cache descriptor; fills `g` on success.
+kvq_status check_desc(const kvq_cache_desc* d, CacheGeom* g) {
+  if (!d) return KVQ_ERR_INVALID_ARG;
+  if (d->bits != 4 && d->bits != 8 && d->bits != 16) return KVQ_ERR_INVALID_ARG;
+  if (d->head_dim <= 0 || d->head_dim % 8 || d->num_kv_heads <= 0) return KVQ_ERR_INVALID_ARG;
+  if (d->bits != 16) {
+    if (d->group_size < 8 || d->group_size % 8 || d->head_dim % d->group_size)
+      return KVQ_ERR_INVALID_ARG;
+  }
+  if (d->layout == KVQ_DENSE) {
+    if (d->capacity <= 0) return KVQ_ERR_INVALID_ARG;
+  } else if (d->layout == KVQ_PAGED) {
+    if (d->capacity <= 0 || d->capacity % 8 || d->num_pages <= 0 || d->max_blocks_per_seq <= 0)
+      return KVQ_ERR_INVALID_ARG;
+    if ((int64_t)d->capacity * d->max_blocks_per_seq > INT32_MAX) return KVQ_ERR_INVALID_ARG;
+  } else {
+    return KVQ_ERR_INVALID_ARG;
+  }
+  if (g) {
+    g->bits = d->bits;
+    g->D = d->head_dim;
+    g->g = (d->bits == 16) ? d->head_dim : d->group_size;
+    g->ngroups = (d->bits == 16) ? 0 : d->head_dim / d->group_size;
+    g->row_bytes = d->head_dim * d->bits / 8;
+    g->Hkv = d->num_kv_heads;
+    g->layout = d->layout;
+    g->slots = d->capacity;
+    g->num_pages = d->layout == KVQ_PAGED ? d->num_pages : 0;
+    g->max_blocks = d->layout == KVQ_PAGED ? d->max_blocks_per_seq : 0;
+    g->block_table = nullptr;
+  }
+  // the kernels are built for these head sizes; byte accounting takes any
+  if (d->head_dim != 64 && d->head_dim != 128 && d->head_dim != 256) return KVQ_ERR_UNSUPPORTED;
+  return KVQ_OK;
+}
+
+kvq_status check_cache(const kvq_cache_desc* d, const kvq_cache* c) {
+  if (!c || !c->k_codes || !c->v_codes) return KVQ_ERR_INVALID_ARG;
+  if (!aligned(c->k_codes) || !aligned(c->v_codes)) return KVQ_ERR_INVALID_ARG;
+  if (d->bits != 16) {
+    if (!c->k_scale || !c->k_zero || !c->v_scale || !c->v_zero) return KVQ_ERR_INVALID_ARG;
+    if (!aligned(c->k_scale) || !aligned(c->k_zero) || !aligned(c->v_scale) || !aligned(c->v_zero))
+      return KVQ_ERR_INVALID_ARG;
+  }
+  if (d->layout == KVQ_PAGED && (!c->block_table || !aligned(c->block_table)))
+    return KVQ_ERR_INVALID_ARG;
+  return KVQ_OK;
+}
+
+int sm_count() {
+  static int cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev < 0 || dev >= 64) return 0;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+// Split count: explicit requests are honoured up to one chunk-aligned tile per
+// split; the automatic choice aims at ~4 CTAs per SM while keeping every split
+// at least 256 tokens long.
+int32_t choose_splits(int64_t units, int64_t max_len, int32_t requested) {
+  const int64_t max_splits = std::max<int64_t>(1, ceil_div(std::max<int64_t>(max_len, 1), kChunkAlign));
+  int64_t s;
+  if (requested > 0) {
+    s = requested;
+  } else {
+    const int sms = sm_count();
+    if (sms <= 0) return 0;
+    const int64_t target = 4LL * sms;
+    s = ceil_div(target, std::max<int64_t>(units, 1));
+    s = std::min<int64_t>(s, std::max<int64_t>(1, ceil_div(max_len, 256)));
+  }
+  s = std::max<int64_t>(1, std::min<int64_t>(s, max_splits));
+  // splits cover chunk-aligned ranges; drop splits that would be empty
+  const int64_t chunk = ceil_div(ceil_div(std::max<int64_t>(max_len, 1), s), kChunkAlign) * kChunkAlign;
+  s = ceil_div(std::max<int64_t>(max_len, 1), chunk);
+  return (int32_t)std::min<int64_t>(s, INT32_MAX);
+}
+
+int32_t split_chunk(int64_t max_len, int32_t splits) {
+  return (int32_t)(ceil_div(ceil_div(std::max<int64_t>(max_len, 1), splits), kChunkAlign) * kChunkAlign);
+}
+
+kvq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
+
+}  // namespace
+
+size_t workspace_bytes(int64_t batch, int64_t Hq, int64_t D, int64_t splits) {
+  if (splits <= 1) return 0;
+  const size_t o = (size_t)(batch * Hq * splits * D) * sizeof(float);
+  const size_t ml = (size_t)(batch * Hq * splits * 2) * sizeof(float);
+  return ((o + 255) & ~(size_t)255) + ml;
+}
+
+void workspace_carve(void* ws, int64_t batch, int64_t Hq, int64_t D, int64_t splits,
+                     float** ws_o, float** ws_ml) {
+  const size_t o = (size_t)(batch * Hq * splits * D) * sizeof(float);
+  *ws_o = reinterpret_cast<float*>(ws);
+  *ws_ml = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + ((o + 255) & ~(size_t)255));
+}
+
+}  // namespace kvq
+
+using namespace kvq;
+
+extern "C" {
+
+size_t kvq_cache_bytes(const kvq_cache_desc* desc, int64_t tokens) {
+  CacheGeom g;
+  if (check_desc(desc, &g) == KVQ_ERR_INVALID_ARG || tokens < 0) return 0;
+  const int64_t per_vector = g.row_bytes + (g.bits == 16 ? 0 : 4LL * g.ngroups);
+  return (size_t)(2LL * g.Hkv * tokens * per_vector);
+}
+
+kvq_status kvq_cache_array_bytes(const kvq_cache_desc* desc, int32_t batch,
+                                 size_t* codes_bytes, size_t* header_bytes) {
+  CacheGeom g;
+  const kvq_status st = check_desc(desc, &g);
+  if (st != KVQ_OK) return st;
+  if (!codes_bytes || !header_bytes) return KVQ_ERR_INVALID_ARG;
+  int64_t rows;
+  if (g.layout == KVQ_DENSE) {
+    if (batch < 0) return KVQ_ERR_INVALID_ARG;
+    rows = (int64_t)batch * g.Hkv * g.slots;
+  } else {
+    rows = (int64_t)g.num_pages * g.Hkv * g.slots;
+  }
+  *codes_bytes = (size_t)(rows * g.row_bytes);
+  *header_bytes = g.bits == 16 ? 0 : (size_t)(rows * g.ngroups * 2);
+  return KVQ_OK;
+}
+
+kvq_status kvq_append(const kvq_cache_desc* desc, const kvq_cache* cache, int32_t batch,
+                      int32_t num_new, const uint16_t* k_new, const uint16_t* v_new,
+                      const int32_t* seq_lens_before, uint32_t* dev_status, void* stream) {
+  AppendParams p;
+  kvq_status st = check_desc(desc, &p.geom);
+  if (st != KVQ_OK) return st;
+  if ((st = check_cache(desc, cache)) != KVQ_OK) return st;
+  if (batch < 0 || num_new < 0) return KVQ_ERR_INVALID_ARG;
+  if (batch == 0 || num_new == 0) return KVQ_OK;
+  if (!k_new || !v_new || !seq_lens_before) return KVQ_ERR_INVALID_ARG;
+  if (!aligned(k_new) || !aligned(v_new) || !aligned(seq_lens_before)) return KVQ_ERR_INVALID_ARG;
+  p.geom.block_table = cache->block_table;
+  p.codes[0] = reinterpret_cast<uint8_t*>(cache->k_codes);
+  p.codes[1] = reinterpret_cast<uint8_t*>(cache->v_codes);
+  p.scale[0] = reinterpret_cast<__half*>(cache->k_scale);
+  p.scale[1] = reinterpret_cast<__half*>(cache->v_scale);
+  p.zero[0] = reinterpret_cast<__half*>(cache->k_zero);
+  p.zero[1] = reinterpret_cast<__half*>(cache->v_zero);
+  p.src[0] = reinterpret_cast<const __half*>(k_new);
+  p.src[1] = reinterpret_cast<const __half*>(v_new);
+  p.seq_lens_before = seq_lens_before;
+  p.status = dev_status;
+  p.batch = batch;
+  p.num_new = num_new;
+  return from_cuda(launch_append(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int32_t kvq_decode_num_splits(const kvq_cache_desc* desc, int32_t batch, int32_t num_q_heads,
+                              int32_t max_seq_len, int32_t num_splits) {
+  CacheGeom g;
+  if (check_desc(desc, &g) != KVQ_OK || batch < 0 || num_q_heads <= 0 || max_seq_len < 0)
+    return 0;
+  return choose_splits((int64_t)batch * g.Hkv, max_seq_len, num_splits);
+}
+
+size_t kvq_decode_workspace_size(const kvq_cache_desc* desc, int32_t batch, int32_t num_q_heads,
+                                 int32_t max_seq_len, int32_t num_splits) {
+  const int32_t s = kvq_decode_num_splits(desc, batch, num_q_heads, max_seq_len, num_splits);
+  if (s <= 1) return 0;
+  return workspace_bytes(batch, num_q_heads, desc->head_dim, s);
+}
+
+kvq_status kvq_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache, int32_t batch,
+                           int32_t num_q_heads, const uint16_t* q, const int32_t* seq_lens,
+                           int32_t max_seq_len, int32_t num_splits, float softmax_scale,
+                           uint16_t* out, void* workspace, size_t workspace_size,
+                           uint32_t* dev_status, void* stream) {
+  DecodeParams p;
+  kvq_status st = check_desc(desc, &p.geom);
+  if (st != KVQ_OK) return st;
+  if ((st = check_cache(desc, cache)) != KVQ_OK) return st;
+  if (batch < 0 || num_q_heads <= 0 || max_seq_len < 0 || num_splits < 0)
+    return KVQ_ERR_INVALID_ARG;
+  if (num_q_heads % desc->num_kv_heads) return KVQ_ERR_INVALID_ARG;
+  if (!(softmax_scale >= 0.f) || isinf(softmax_scale)) return KVQ_ERR_INVALID_ARG;
+  if (batch == 0) return KVQ_OK;
+  if (!q || !seq_lens || !out) return KVQ_ERR_INVALID_ARG;
+  if (!aligned(q) || !aligned(out) || !aligned(seq_lens)) return KVQ_ERR_INVALID_ARG;
+  const int G = num_q_heads / desc->num_kv_heads;
+  if (G > kMaxGroupHeads) return KVQ_ERR_UNSUPPORTED;
+
+  const int32_t splits = choose_splits((int64_t)batch * desc->num_kv_heads, max_seq_len, num_splits);
+  if (splits <= 0) return KVQ_ERR_CUDA;
+  const size_t need = workspace_bytes(batch, num_q_heads, desc->head_dim, splits);
+  if (need > 0 && (!workspace || workspace_size < need || !aligned(workspace)))
+    return KVQ_ERR_WORKSPACE;
+
+  p.geom.block_table = cache->block_table;
+  p.codes[0] = reinterpret_cast<const uint8_t*>(cache->k_codes);
+  p.codes[1] = reinterpret_cast<const uint8_t*>(cache->v_codes);
+  p.scale[0] = reinterpret_cast<const __half*>(cache->k_scale);
+  p.scale[1] = reinterpret_cast<const __half*>(cache->v_scale);
+  p.zero[0] = reinterpret_cast<const __half*>(cache->k_zero);
+  p.zero[1] = reinterpret_cast<const __half*>(cache->v_zero);
+  p.q = reinterpret_cast<const __half*>(q);
+  p.seq_lens = seq_lens;
+  p.out = reinterpret_cast<__half*>(out);
+  p.ws_o = nullptr;
+  p.ws_ml = nullptr;
+  if (splits > 1) workspace_carve(workspace, batch, num_q_heads, desc->head_dim, splits, &p.ws_o, &p.ws_ml);
+  p.status = dev_status;
+  p.batch = batch;
+  p.Hq = num_q_heads;
+  p.G = G;
+  p.splits = splits;
+  p.chunk = split_chunk(max_seq_len, splits);
+  const int64_t cap = desc->layout == KVQ_DENSE ? (int64_t)desc->capacity
+                                                 : (int64_t)desc->capacity * desc->max_blocks_per_seq;
+  p.len_limit = (int32_t)std::min<int64_t>(cap, max_seq_len);
+  const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)desc->head_dim);
+  p.scale_log2 = scale * 1.4426950408889634f;
+
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_decode_generic(p, s);
+  if (e == cudaSuccess && splits > 1) e = launch_merge(p, s);
+  return from_cuda(e);
+}
+
+const char* kvq_status_string(kvq_status status) {
+  switch (status) {
+    case KVQ_OK: return "KVQ_OK";
+    case KVQ_ERR_INVALID_ARG: return "KVQ_ERR_INVALID_ARG: invalid argument";
+    case KVQ_ERR_UNSUPPORTED: return "KVQ_ERR_UNSUPPORTED: shape not supported";
+    case KVQ_ERR_WORKSPACE: return "KVQ_ERR_WORKSPACE: workspace missing or too small";
+    case KVQ_ERR_CUDA: return "KVQ_ERR_CUDA: CUDA runtime error";
+  }
+  return "KVQ_ERR_UNKNOWN";
+}
+
+}  // extern "C"

@@ -1,0 +1,238 @@
+// Generic split-K decode attention (CUDA cores) and the log-sum-exp merge.
+//
+// The generic kernel covers every shape the ABI accepts (INT4/INT8/fp16
+// caches, any group size, head_dim 64/128/256, up to 16 query heads per KV
+// head, dense or paged).  It keeps the plain structure of the decode step of
+// "Quantization & inference optimisation" ("Prefill, then decode": scores =
+// K q / sqrt(d), softmax, weighted V) in tiles of 64 tokens with an online
+// softmax, dequantizing x_hat = (q - z) * s element by element in fp32
+// ("What actually happens when you quantize a KV cache", section 3 step 3).
+// The tensor-core kernel in kvq_decode_mma.cu is the fast path for the
+// common shapes; both write the same partials, merged by merge_kernel.
+//
+// Work unit: one CTA per (split, KV head, sequence); the split covers
+// tokens [split*chunk, min(len, (split+1)*chunk)).  Scores and softmax
+// statistics are kept in the log2 domain (scores pre-multiplied by log2 e)
+// so that exp2f serves both the kernel and the merge.
+#include "kvq_internal.cuh"
+
+namespace kvq {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int kTile = 64;
+
+template <int BITS>
+__device__ __forceinline__ float dequant(const uint8_t* codes, const __half* scale,
+                                         const __half* zero, const CacheGeom& c,
+                                         long long row, int d) {
+  if constexpr (BITS == 16) {
+    return __half2float(reinterpret_cast<const __half*>(codes + row * c.row_bytes)[d]);
+  } else {
+    const uint8_t* r = codes + row * c.row_bytes;
+    float q;
+    if constexpr (BITS == 4) {
+      const uint8_t byte = r[d >> 1];
+      q = (float)((d & 1) ? (byte >> 4) : (byte & 15));
+    } else {
+      q = (float)r[d];
+    }
+    const long long h = row * c.ngroups + d / c.g;
+    return (q - __half2float(zero[h])) * __half2float(scale[h]);
+  }
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kThreads) decode_generic_kernel(const DecodeParams p) {
+  extern __shared__ float smem[];
+  const CacheGeom& c = p.geom;
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int G = p.G, D = c.D;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+  float* q_s = smem;                  // [G][D]
+  float* o_s = q_s + G * D;           // [G][D]
+  float* p_s = o_s + G * D;           // [G][kTile] scores, then probabilities
+  float* m_s = p_s + G * kTile;       // [G]
+  float* l_s = m_s + G;               // [G]
+  float* a_s = l_s + G;               // [G]
+  long long* row_s = reinterpret_cast<long long*>(a_s + ((G + 1) & ~1));  // [kTile]
+
+  int L = p.seq_lens[b];
+  const bool bad_len = (L < 0 || L > p.len_limit);
+  if (bad_len) {
+    if (tid == 0 && split == 0 && kvh == 0 && p.status) atomicOr(p.status, KVQ_FLAG_SEQ_LEN);
+    L = 0;
+  }
+  const int t0 = split * p.chunk;
+  const int t1 = min(L, t0 + p.chunk);
+  if (p.splits > 1 && t0 >= L) return;  // the merge reads splits < ceil(L / chunk) only
+
+  const __half* qg = p.q + ((long long)b * p.Hq + (long long)kvh * G) * D;
+  for (int i = tid; i < G * D; i += kThreads) {
+    q_s[i] = __half2float(qg[i]);
+    o_s[i] = 0.f;
+  }
+  if (tid < G) {
+    m_s[tid] = -INFINITY;
+    l_s[tid] = 0.f;
+  }
+  __syncthreads();
+
+  for (int ts = t0; ts < t1; ts += kTile) {
+    const int n = min(kTile, t1 - ts);
+
+    // scores: one warp per token, lanes across channels
+    for (int j = warp; j < n; j += kThreads / 32) {
+      const long long row = token_row(c, b, kvh, ts + j);
+      float part[kMaxGroupHeads];
+#pragma unroll
+      for (int h = 0; h < kMaxGroupHeads; ++h) part[h] = 0.f;
+      if (row >= 0) {
+        for (int d = lane; d < D; d += 32) {
+          const float k = dequant<BITS>(p.codes[0], p.scale[0], p.zero[0], c, row, d);
+#pragma unroll
+          for (int h = 0; h < kMaxGroupHeads; ++h)
+            if (h < G) part[h] = fmaf(q_s[h * D + d], k, part[h]);
+        }
+      }
+#pragma unroll
+      for (int h = 0; h < kMaxGroupHeads; ++h) {
+        if (h < G) {
+          float v = part[h];
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+          if (lane == 0) p_s[h * kTile + j] = (row >= 0) ? v * p.scale_log2 : -INFINITY;
+        }
+      }
+      if (lane == 0) {
+        row_s[j] = row;
+        if (row < 0 && p.status) atomicOr(p.status, KVQ_FLAG_BLOCK_TABLE);
+      }
+    }
+    __syncthreads();
+
+    // online softmax update, one thread per query head
+    if (tid < G) {
+      float* ps = p_s + tid * kTile;
+      float mt = -INFINITY;
+      for (int j = 0; j < n; ++j) mt = fmaxf(mt, ps[j]);
+      const float m_old = m_s[tid];
+      const float m_new = fmaxf(m_old, mt);
+      float alpha = 1.f, lsum = 0.f;
+      if (m_new == -INFINITY) {
+        for (int j = 0; j < n; ++j) ps[j] = 0.f;
+      } else {
+        alpha = exp2f(m_old - m_new);
+        for (int j = 0; j < n; ++j) {
+          const float e = exp2f(ps[j] - m_new);
+          ps[j] = e;
+          lsum += e;
+        }
+      }
+      m_s[tid] = m_new;
+      l_s[tid] = l_s[tid] * alpha + lsum;
+      a_s[tid] = alpha;
+    }
+    __syncthreads();
+
+    // weighted V: each thread owns (head, channel) outputs
+    for (int i = tid; i < G * D; i += kThreads) {
+      const int h = i / D, d = i - h * D;
+      float acc = o_s[i] * a_s[h];
+      const float* ps = p_s + h * kTile;
+      for (int j = 0; j < n; ++j) {
+        const long long row = row_s[j];
+        if (row < 0) continue;
+        acc = fmaf(ps[j], dequant<BITS>(p.codes[1], p.scale[1], p.zero[1], c, row, d), acc);
+      }
+      o_s[i] = acc;
+    }
+    __syncthreads();
+  }
+
+  const long long hq0 = (long long)b * p.Hq + (long long)kvh * G;
+  if (p.splits == 1) {
+    for (int i = tid; i < G * D; i += kThreads) {
+      const int h = i / D;
+      const float l = l_s[h];
+      p.out[hq0 * D + i] = __float2half_rn(l > 0.f ? o_s[i] / l : 0.f);
+    }
+  } else {
+    for (int i = tid; i < G * D; i += kThreads) {
+      const int h = i / D, d = i - h * D;
+      p.ws_o[((hq0 + h) * p.splits + split) * D + d] = o_s[i];
+    }
+    if (tid < G) {
+      float* ml = p.ws_ml + ((hq0 + tid) * p.splits + split) * 2;
+      ml[0] = m_s[tid];
+      ml[1] = l_s[tid];
+    }
+  }
+}
+
+// out[b][h] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s over the splits
+// that hold tokens of sequence b; one warp per (b, h), lanes across channels.
+__global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long rowid = (long long)blockIdx.x * 4 + warp;  // b * Hq + h
+  if (rowid >= (long long)p.batch * p.Hq) return;
+  const int b = (int)(rowid / p.Hq);
+  const int D = p.geom.D;
+  const int L = p.seq_lens[b];
+  const int nv = (L <= 0 || L > p.len_limit) ? 0 : (L + p.chunk - 1) / p.chunk;
+  const float* ml = p.ws_ml + rowid * p.splits * 2;
+  float M = -INFINITY;
+  for (int s = 0; s < nv; ++s) M = fmaxf(M, ml[2 * s]);
+  __half* out = p.out + rowid * D;
+  if (M == -INFINITY) {
+    for (int d = lane; d < D; d += 32) out[d] = __float2half_rn(0.f);
+    return;
+  }
+  float den = 0.f;
+  for (int s = 0; s < nv; ++s) den = fmaf(exp2f(ml[2 * s] - M), ml[2 * s + 1], den);
+  const float inv = 1.f / den;
+  const float* o = p.ws_o + rowid * p.splits * D;
+  for (int d = lane; d < D; d += 32) {
+    float num = 0.f;
+    for (int s = 0; s < nv; ++s) num = fmaf(exp2f(ml[2 * s] - M), o[(long long)s * D + d], num);
+    out[d] = __float2half_rn(num * inv);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_generic(const DecodeParams& p, cudaStream_t stream) {
+  const int G = p.G, D = p.geom.D;
+  const size_t smem = sizeof(float) * (2 * G * D + G * kTile + 3 * G + 1) +
+                      sizeof(long long) * (kTile + 1);
+  const dim3 grid(p.splits, p.geom.Hkv, p.batch);
+  cudaError_t e = cudaSuccess;
+  switch (p.geom.bits) {
+    case 4:
+      e = cudaFuncSetAttribute(decode_generic_kernel<4>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess) decode_generic_kernel<4><<<grid, kThreads, smem, stream>>>(p);
+      break;
+    case 8:
+      e = cudaFuncSetAttribute(decode_generic_kernel<8>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess) decode_generic_kernel<8><<<grid, kThreads, smem, stream>>>(p);
+      break;
+    default:
+      e = cudaFuncSetAttribute(decode_generic_kernel<16>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess) decode_generic_kernel<16><<<grid, kThreads, smem, stream>>>(p);
+      break;
+  }
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream) {
+  const long long rows = (long long)p.batch * p.Hq;
+  merge_kernel<<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

@@ -1,0 +1,90 @@
+// Internal declarations shared by the CUDA translation units of libkvq.
+// Nothing here is part of the public ABI (include/kvq.h).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kvq.h"
+
+namespace kvq {
+
+// Token tile of the generic decode kernel and the alignment of split chunks:
+// every split except the last covers a multiple of this many tokens.
+constexpr int kChunkAlign = 64;
+constexpr int kMaxGroupHeads = 16;  // query heads per KV head handled per CTA
+
+// Geometry of one cache (K and V share it).
+struct CacheGeom {
+  int32_t bits;        // 4, 8 or 16
+  int32_t D;           // head_dim
+  int32_t g;           // group size (channels per scale/zero)
+  int32_t ngroups;     // D / g (0 when bits == 16)
+  int32_t row_bytes;   // bytes of codes per token row
+  int32_t Hkv;
+  int32_t layout;      // KVQ_DENSE / KVQ_PAGED
+  int32_t slots;       // dense: capacity; paged: page size
+  int32_t num_pages;   // paged only
+  int32_t max_blocks;  // paged only
+  const int32_t* block_table;
+};
+
+// Row index of token `pos` of sequence `b`, KV head `kvh`, into the
+// [..][row_bytes] codes array and the [..][ngroups] header arrays;
+// -1 when the block table maps the token to no valid page.
+__device__ __forceinline__ long long token_row(const CacheGeom& c, int b, int kvh,
+                                               int pos) {
+  if (c.layout == KVQ_DENSE) {
+    return ((long long)b * c.Hkv + kvh) * c.slots + pos;
+  }
+  const int blk = pos / c.slots;
+  const int off = pos - blk * c.slots;
+  const int page = __ldg(c.block_table + (long long)b * c.max_blocks + blk);
+  if (page < 0 || page >= c.num_pages) return -1;
+  return ((long long)page * c.Hkv + kvh) * c.slots + off;
+}
+
+struct AppendParams {
+  CacheGeom geom;
+  uint8_t* codes[2];     // K, V
+  __half* scale[2];
+  __half* zero[2];
+  const __half* src[2];  // k_new, v_new: [batch][num_new][Hkv][D]
+  const int32_t* seq_lens_before;
+  uint32_t* status;
+  int32_t batch;
+  int32_t num_new;
+};
+
+struct DecodeParams {
+  CacheGeom geom;
+  const uint8_t* codes[2];  // K, V
+  const __half* scale[2];
+  const __half* zero[2];
+  const __half* q;          // [batch][Hq][D]
+  const int32_t* seq_lens;  // [batch]
+  __half* out;              // [batch][Hq][D]
+  float* ws_o;              // [batch][Hq][splits][D]     (splits > 1)
+  float* ws_ml;             // [batch][Hq][splits][2]      (splits > 1)
+  uint32_t* status;
+  int32_t batch;
+  int32_t Hq;
+  int32_t G;                // Hq / Hkv
+  int32_t splits;
+  int32_t chunk;            // tokens per split (multiple of kChunkAlign)
+  int32_t len_limit;        // largest valid seq_len
+  float scale_log2;         // softmax scale * log2(e)
+};
+
+// Launchers (return a CUDA error code; the caller maps it to kvq_status).
+cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
+cudaError_t launch_decode_generic(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream);
+
+// Size of the workspace for `splits` splits (0 when splits == 1).
+size_t workspace_bytes(int64_t batch, int64_t Hq, int64_t D, int64_t splits);
+void workspace_carve(void* ws, int64_t batch, int64_t Hq, int64_t D, int64_t splits,
+                     float** ws_o, float** ws_ml);
+
+}  // namespace kvq

@@ -1,0 +1,140 @@
+"""CPU tests of the C ABI boundary: the library loads, exports every function
+include/kvq.h declares, and its host-side arithmetic and validation behave
+as documented.  Nothing here launches a kernel."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests.conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "kvq.h")
+
+
+@pytest.fixture(scope="module")
+def K():
+    from quantized_kv_decode_gb300 import build
+    build.build()
+    import quantized_kv_decode_gb300 as K
+    K.lib()
+    return K
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ("kvq_append", "kvq_decode_attn", "kvq_cache_bytes", "kvq_decode_workspace_size",
+              "kvq_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(K):
+    lib = ctypes.CDLL(K._lib.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing
+    # the binding declares the same set, with the header's names
+    assert sorted(K._lib.SIGNATURES) == declared_functions()
+
+
+def test_status_strings(K):
+    for st in range(5):
+        assert K.kvq_status_string(st).startswith("KVQ_")
+
+
+def test_cache_bytes_against_page_figures(K, golden):
+    """kvq_cache_bytes restates the pages' per-token byte counts."""
+    _, rows = golden("fp16_cache_sizes.txt")
+    for r in rows:
+        layers, kvh, hd, nbytes, tokens, expect, tol = map(int, r[2:9])
+        desc = K.make_desc(16, 0, kvh, hd, K.KVQ_DENSE, 1)
+        assert abs(layers * K.kvq_cache_bytes(desc, tokens) - expect) <= tol, r[1]
+    kv, grp = golden("kvq_byte_accounting.txt")
+    L, H, D = kv["layers"], kv["kv_heads"], kv["head_dim"]
+    per_tok = L * K.kvq_cache_bytes(K.make_desc(4, 128, H, D, K.KVQ_DENSE, 1), 1)
+    assert per_tok == kv["int4_g128_total_per_token_kib"] * 1024
+    seq = L * K.kvq_cache_bytes(K.make_desc(4, 128, H, D, K.KVQ_DENSE, 1), kv["seq_tokens"])
+    assert seq == kv["int4_g128_seq_mib"] * 2 ** 20
+    for r in grp:
+        g, eff_bits = int(r[1]), float(r[3])
+        b = L * K.kvq_cache_bytes(K.make_desc(4, g, H, D, K.KVQ_DENSE, 1), 1)
+        assert abs(b * 8 / (2 * L * H * D) - eff_bits) < 1e-9
+
+
+def test_cache_array_bytes(K):
+    d = K.make_desc(4, 32, 8, 128, K.KVQ_DENSE, 4112)
+    codes, hdr = K.kvq_cache_array_bytes(d, 8)
+    assert codes == 8 * 8 * 4112 * 64 and hdr == 8 * 8 * 4112 * 4 * 2
+    p = K.make_desc(8, 64, 2, 64, K.KVQ_PAGED, 16, 1000, 257)
+    codes, hdr = K.kvq_cache_array_bytes(p, 0)
+    assert codes == 1000 * 2 * 16 * 64 and hdr == 1000 * 2 * 16 * 1 * 2
+    f = K.make_desc(16, 0, 4, 256, K.KVQ_DENSE, 10)
+    assert K.kvq_cache_array_bytes(f, 3) == (3 * 4 * 10 * 512, 0)
+
+
+@pytest.mark.parametrize("field,value", [
+    ("bits", 5), ("bits", 2), ("group_size", 12), ("group_size", 0), ("group_size", 48),
+    ("num_kv_heads", 0), ("layout", 3), ("capacity", 0), ("head_dim", 100)])
+def test_invalid_descriptor_rejected(K, field, value):
+    d = K.make_desc(4, 32, 8, 128, K.KVQ_DENSE, 64)
+    setattr(d, field, value)
+    with pytest.raises(K.KVQError) as e:
+        K.kvq_cache_array_bytes(d, 1)
+    assert e.value.status == K.KVQ_ERR_INVALID_ARG
+    assert K.kvq_cache_bytes(d, 1) == 0
+
+
+def test_unsupported_head_dim(K):
+    d = K.make_desc(4, 32, 8, 512, K.KVQ_DENSE, 64)
+    with pytest.raises(K.KVQError) as e:
+        K.kvq_cache_array_bytes(d, 1)
+    assert e.value.status == K.KVQ_ERR_UNSUPPORTED
+    assert K.kvq_cache_bytes(d, 1) == 2 * 8 * (256 + 4 * 16)
+
+
+def test_append_and_decode_validate_before_launch(K):
+    """Host-visible errors return synchronously, before any CUDA call."""
+    from ctypes import byref
+    lib = K.lib()
+    d = K.make_desc(4, 32, 2, 128, K.KVQ_DENSE, 64)
+    empty = K.kvq_cache()
+    assert lib.kvq_append(byref(d), byref(empty), 1, 1, 16, 16, 16, None, None) == K.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_append(None, byref(empty), 1, 1, 16, 16, 16, None, None) == K.KVQ_ERR_INVALID_ARG
+    fake = K.kvq_cache(16, 32, 48, 64, 80, 96, None)
+    # null inputs
+    assert lib.kvq_append(byref(d), byref(fake), 1, 1, None, 16, 16, None, None) == K.KVQ_ERR_INVALID_ARG
+    # misaligned input
+    assert lib.kvq_append(byref(d), byref(fake), 1, 1, 18, 16, 16, None, None) == K.KVQ_ERR_INVALID_ARG
+    # nothing to do is not an error
+    assert lib.kvq_append(byref(d), byref(fake), 0, 1, None, None, None, None, None) == K.KVQ_OK
+    # heads not a multiple of the KV heads
+    assert lib.kvq_decode_attn(byref(d), byref(fake), 1, 3, 16, 16, 64, 1, 0.0, 16, None, 0,
+                               None, None) == K.KVQ_ERR_INVALID_ARG
+    # too many query heads per KV head for the kernels
+    assert lib.kvq_decode_attn(byref(d), byref(fake), 1, 2 * 17, 16, 16, 64, 1, 0.0, 16, None,
+                               0, None, None) == K.KVQ_ERR_UNSUPPORTED
+    # explicit split count needs a workspace
+    assert lib.kvq_decode_attn(byref(d), byref(fake), 1, 2, 16, 16, 640, 4, 0.0, 16, None, 0,
+                               None, None) == K.KVQ_ERR_WORKSPACE
+    # negative scale
+    assert lib.kvq_decode_attn(byref(d), byref(fake), 1, 2, 16, 16, 64, 1, -1.0, 16, None, 0,
+                               None, None) == K.KVQ_ERR_INVALID_ARG
+    # paged without a block table
+    p = K.make_desc(4, 32, 2, 128, K.KVQ_PAGED, 16, 10, 4)
+    assert lib.kvq_append(byref(p), byref(fake), 1, 1, 16, 16, 16, None, None) == K.KVQ_ERR_INVALID_ARG
+
+
+def test_explicit_split_counts(K):
+    d = K.make_desc(4, 32, 32, 128, K.KVQ_DENSE, 4112)
+    assert K.kvq_decode_num_splits(d, 8, 32, 4097, 1) == 1
+    assert K.kvq_decode_num_splits(d, 8, 32, 4097, 7) == 7
+    # never more splits than 64-token tiles
+    assert K.kvq_decode_num_splits(d, 8, 32, 100, 50) == 2
+    assert K.kvq_decode_workspace_size(d, 8, 32, 4097, 1) == 0
+    ws = K.kvq_decode_workspace_size(d, 8, 32, 4097, 4)
+    assert ws >= 8 * 32 * 4 * (128 + 2) * 4

@@ -1,0 +1,111 @@
+"""GPU parity of kvq_decode_attn against the oracle on the same codes.
+
+Tolerance (stated for fp32 accumulation): max |gpu - oracle| <= 2e-3 and
+||gpu - oracle||_2 / ||oracle||_2 <= 1e-3 over all outputs of a case.
+"""
+import numpy as np
+import pytest
+
+from quantized_kv_decode_gb300 import synth
+from tests._cases import Case, assert_close, make_inputs, oracle_step, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(c, num_splits=0, repeat=1):
+    inp = make_inputs(c)
+    run = run_gpu(c, inp, num_splits=num_splits, repeat=repeat)
+    ref, _ = oracle_step(c, inp)
+    assert run["status"] == 0
+    assert_close(run["out"], ref)
+    return run, ref
+
+
+def test_tiny_workload():
+    """1 sequence, 4 heads = 4 KV heads, head_dim 128, context 256, INT4 group 8,
+    seed 0: one decode step (the new token makes 257 rows)."""
+    w = synth.WORKLOADS["tiny"]
+    c = Case(B=w.batch, Hq=w.num_q_heads, Hkv=w.num_kv_heads, D=w.head_dim, bits=4,
+             g=w.group_size, lens=np.array([w.ctx[0]]), seed=w.seed)
+    for s in (0, 1, 2, 5):
+        _check(c, num_splits=s)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 7, 64])
+def test_mha_int4_g32_splits(splits):
+    c = Case(B=2, Hq=4, Hkv=4, D=128, bits=4, g=32, lens=np.array([700, 451]), seed=11)
+    _check(c, num_splits=splits)
+
+
+@pytest.mark.parametrize("bits,g,D,Hq,Hkv", [
+    (4, 64, 128, 8, 2), (4, 32, 128, 8, 2), (8, 32, 128, 8, 2), (4, 32, 64, 14, 2),
+    (4, 128, 256, 4, 1), (8, 8, 64, 2, 2), (4, 16, 128, 16, 1), (16, 0, 128, 8, 2)])
+def test_gqa_ragged(bits, g, D, Hq, Hkv):
+    rng = np.random.default_rng(bits + g + D + Hq)
+    lens = rng.integers(1, 900, size=3)
+    lens[0] = 0                                  # a sequence whose only row is the new token
+    c = Case(B=3, Hq=Hq, Hkv=Hkv, D=D, bits=bits, g=g, lens=lens, seed=int(lens.sum()))
+    for s in (0, 1, 3):
+        _check(c, num_splits=s)
+
+
+@pytest.mark.parametrize("ps", [8, 16, 64])
+def test_paged_matches_oracle_and_dense(ps):
+    lens = np.array([130, 1, 64, 47, 300])
+    dense = Case(B=5, Hq=14, Hkv=2, D=64, bits=4, g=32, lens=lens, seed=21)
+    paged = Case(B=5, Hq=14, Hkv=2, D=64, bits=4, g=32, lens=lens, seed=21, layout="paged",
+                 page_size=ps)
+    rd, _ = _check(dense, num_splits=2)
+    rp, _ = _check(paged, num_splits=2)
+    assert np.array_equal(rd["out"].view(np.uint16), rp["out"].view(np.uint16))
+
+
+def test_long_int8_and_int4():
+    for bits in (8, 4):
+        c = Case(B=1, Hq=8, Hkv=2, D=128, bits=bits, g=32, lens=np.array([5000]), seed=31)
+        _check(c, num_splits=0)
+
+
+def test_deterministic_run_to_run():
+    c = Case(B=2, Hq=8, Hkv=2, D=128, bits=4, g=64, lens=np.array([1000, 777]), seed=41)
+    run, _ = _check(c, num_splits=5, repeat=3)
+    for o in run["outs"][1:]:
+        assert np.array_equal(o.view(np.uint16), run["outs"][0].view(np.uint16))
+
+
+def test_bad_lengths_flag_and_zero_rows():
+    import torch
+    import quantized_kv_decode_gb300 as K
+    c = Case(B=3, Hq=4, Hkv=2, D=64, bits=4, g=32, lens=np.array([10, 20, 30]), seed=51)
+    inp = make_inputs(c)
+    run = run_gpu(c, inp)
+    cache = run["cache"]
+    q = torch.from_numpy(inp["q"]).cuda()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for splits in (1, 3):
+        lens = torch.tensor([11, 10 ** 6, -4], dtype=torch.int32, device="cuda")
+        out = K.kvq_decode_attn(cache, q, lens, 31, dev_status=st, num_splits=splits)
+        torch.cuda.synchronize()
+        assert int(st.item()) & K.KVQ_FLAG_SEQ_LEN
+        o = out.cpu().numpy()
+        assert not o[1].any() and not o[2].any()
+        assert np.array_equal(o[0].view(np.uint16), run["out"][0].view(np.uint16))
+
+
+def test_unmapped_page_flags_block_table():
+    import torch
+    import quantized_kv_decode_gb300 as K
+    c = Case(B=2, Hq=4, Hkv=2, D=64, bits=4, g=32, lens=np.array([40, 40]), seed=61,
+             layout="paged", page_size=16)
+    inp = make_inputs(c)
+    run = run_gpu(c, inp)
+    cache = run["cache"]
+    cache.block_table[1, 1] = -7                 # sequence 1 loses its second page
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lens = torch.tensor([41, 41], dtype=torch.int32, device="cuda")
+    out = K.kvq_decode_attn(cache, torch.from_numpy(inp["q"]).cuda(), lens, 41, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == K.KVQ_FLAG_BLOCK_TABLE
+    o = out.cpu().numpy()
+    assert np.array_equal(o[0].view(np.uint16), run["out"][0].view(np.uint16))
+    assert np.isfinite(o[1].astype(np.float32)).all()
