@@ -133,7 +133,8 @@ def quantize_groups(x16: np.ndarray, bits: int, group_size: int) -> dict:
     flags = np.where(clamped, ZERO_CLAMPED, 0).astype(np.uint32)
     flags = np.where(finite, flags, NONFINITE).astype(np.uint32)
     s16 = np.where(finite, s16, np.float16(0.0)).astype(np.float16)
-    z = np.where(finite, z, 0.0)
+    # z is an integer code: store it without a sign on zero (rint(-0.3) is -0.0)
+    z = np.where(finite, z, 0.0) + 0.0
     q = np.where(finite[..., None], q, 0.0)
 
     return {

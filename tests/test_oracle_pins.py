@@ -201,6 +201,20 @@ def test_zero_point_outside_fp16_integers_is_clamped_and_flagged():
     assert float(res["zero"][0, 0]) == -O.ZERO_LIMIT
 
 
+def test_zero_point_is_an_integer_without_signed_zero():
+    """z is the integer code that decodes to ~0.0 ("What actually happens when
+    you quantize a KV cache", section 3 step 3): -min/s in (-1/2, 0) rounds to
+    the integer 0, stored as +0."""
+    x16 = f16([[0.01, 0.5, 0.6, 0.7, 0.8, 0.9, 1.0, 1.1],
+               [-0.01, -0.5, -0.6, -0.7, -0.8, -0.9, -1.0, -0.02]])
+    res = O.quantize_groups(x16, 4, 8)
+    assert int(res["zero"][0, 0].view(np.uint16)) == 0
+    assert not np.any(res["zero"].view(np.uint16) == 0x8000)
+    rng = np.random.default_rng(1)
+    many = f16(np.abs(rng.normal(size=(2000, 8))) + rng.uniform(0, 3, size=(2000, 1)))
+    assert not np.any(O.quantize_groups(many, 4, 8)["zero"].view(np.uint16) == 0x8000)
+
+
 def test_nonfinite_group_is_zeroed_and_flagged():
     x16 = f16([[1.0, np.inf, 0.0, 0.5, 0.25, 0.0, 0.0, 0.0],
                [1.0, 2.0, 3.0, 4.0, 5.0, 6.0, 7.0, 8.0]])
