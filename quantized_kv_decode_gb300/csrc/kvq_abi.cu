@@ -248,7 +248,15 @@ kvq_status kvq_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache, i
   p.scale_log2 = scale * 1.4426950408889634f;
 
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_decode_generic(p, s);
+  cudaError_t e = cudaSuccess;
+  bool handled = false;
+  if (desc->bits != 16 && G <= 8) {
+    int gp = 1;
+    while (gp < G) gp <<= 1;
+    if (desc->bits == 4) e = launch_decode_fast_int4(p, gp, s, &handled);
+    else e = launch_decode_fast_int8(p, gp, s, &handled);
+  }
+  if (!handled) e = launch_decode_generic(p, s);
   if (e == cudaSuccess && splits > 1) e = launch_merge(p, s);
   return from_cuda(e);
 }

@@ -1,0 +1,516 @@
+// Tensor-core split-K decode attention over INT4/INT8 caches (sm_103a).
+//
+// What it computes is the decode step of "Quantization & inference
+// optimisation" ("Prefill, then decode": scores = K q / sqrt(d), softmax,
+// weighted V over every cached row), with the keys and values read as
+// group-wise codes and dequantized x_hat = (q - z) * s in registers
+// ("What actually happens when you quantize a KV cache", sections 3-4 and 6).
+//
+// Structure (one CTA per (split, KV head, sequence); kFastWarps warps):
+//  * Each warp streams its own 32-token tiles through a private cp.async
+//    pipeline (16-byte chunks, zero-filled past the end of the sequence or
+//    for unmapped pages) into shared memory whose code rows are padded by
+//    16 bytes, which makes every ldmatrix below free of bank conflicts.
+//  * Scores, mma.m16n8k16 (fp16 in, fp32 accumulate): A = q, one row per
+//    (group, head) pair, holding that head's channels of that group only;
+//    B = the raw codes of 8 tokens (integers 0..2^b-1, exact in fp16),
+//    converted from packed nibbles/bytes with two LOP3 + one HSUB2/HFMA2 per
+//    code pair.  Row (g, h) of the accumulator is sum_{d in g} q_h[d] c[d];
+//    the epilogue forms s_g (sum - z_g sum_{d in g} q_h[d]) in fp32 and adds
+//    the groups with warp shuffles.
+//  * Online softmax per 32-token tile (log2 domain), rescaling only when a
+//    running maximum grows.
+//  * Weighted V, mma.m16n8k16: A = V codes transposed (ldmatrix.trans puts
+//    two tokens of one channel in each register), B = p * s_g per token and
+//    group (fp16); the zero-points enter through one extra mma per group
+//    whose A rows hold z_g per token, subtracted once at the end.
+//  * The warps' (m, l, o) are merged in shared memory; the CTA writes the
+//    final row (one split) or its partial for the merge kernel.
+#pragma once
+
+#include "kvq_internal.cuh"
+
+namespace kvq {
+namespace fast {
+
+constexpr int kWarps = 4;
+constexpr int kTT = 32;  // tokens per warp tile
+
+template <int BITS, int D, int NG, int GP>
+struct Cfg {
+  static constexpr int ROWB = D * BITS / 8;       // code bytes per token row
+  static constexpr int ROWS = ROWB + 16;          // padded shared-memory row stride
+  static constexpr int CHUNKS = ROWB / 16;        // 16-byte chunks per row
+  static constexpr int GSZ = D / NG;              // channels per group
+  static constexpr int DPC = 128 / BITS;          // channels per 16-byte chunk
+  static constexpr int KB = D / 16;               // k-blocks of the score mma
+  static constexpr int MT = D / 16;               // m-tiles of the V mma
+  static constexpr int HDRB = NG * 2;             // header bytes per token
+  static constexpr int CODE_TILE = kTT * ROWS;
+  static constexpr int HDR_TILE = kTT * HDRB;
+  static constexpr int STAGE = 2 * CODE_TILE + 4 * HDR_TILE;
+  static constexpr int STAGES = (kWarps * 4 * STAGE <= 110 * 1024) ? 4 : 3;
+  static constexpr int NGL = (NG < 8 / GP) ? NG : 8 / GP;  // groups in accumulator rows 0..7
+  static constexpr bool HI = NG * GP > 8;                   // rows 8..15 in use
+  static_assert(BITS == 4 || BITS == 8, "bits");
+  static_assert(GSZ % DPC == 0, "a 16-byte chunk must lie inside one group");
+  static_assert(NG * GP <= 16, "groups x padded heads must fit 16 rows");
+  static_assert(HDRB == 4 || HDRB == 8 || HDRB == 16, "header row size");
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_small(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], %2, %3;\n" ::"r"(dst), "l"(src), "n"(N),
+               "r"(valid ? N : 0)
+               : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t a, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(a)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x2(uint32_t a, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n"
+               : "=r"(r0), "=r"(r1)
+               : "r"(a)
+               : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t a, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(a)
+               : "memory");
+}
+
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
+__device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
+
+// fp16 bit patterns: 1024, 1/16, -64 in both halves
+constexpr uint32_t kH1024 = 0x64006400u;
+constexpr uint32_t kH1_16 = 0x2C002C00u;
+constexpr uint32_t kHm64 = 0xD400D400u;
+
+// Eight 4-bit codes of one 32-bit word (code k in bits 4k..4k+3) to four
+// fp16 pairs: o[0] = (c0, c4), o[1] = (c1, c5), o[2] = (c2, c6), o[3] = (c3, c7).
+// (0x6400 | c) is the fp16 value 1024 + c; (0x6400 | 16c) is 1024 + 16c.
+__device__ __forceinline__ void nib8_to_h2(uint32_t w, uint32_t (&o)[4]) {
+  const uint32_t w2 = w >> 8;
+  const uint32_t a = (w & 0x000F000Fu) | kH1024;
+  const uint32_t b = (w & 0x00F000F0u) | kH1024;
+  const uint32_t c = (w2 & 0x000F000Fu) | kH1024;
+  const uint32_t d = (w2 & 0x00F000F0u) | kH1024;
+  o[0] = h2_as_u32(__hsub2(u32_as_h2(a), u32_as_h2(kH1024)));
+  o[1] = h2_as_u32(__hfma2(u32_as_h2(b), u32_as_h2(kH1_16), u32_as_h2(kHm64)));
+  o[2] = h2_as_u32(__hsub2(u32_as_h2(c), u32_as_h2(kH1024)));
+  o[3] = h2_as_u32(__hfma2(u32_as_h2(d), u32_as_h2(kH1_16), u32_as_h2(kHm64)));
+}
+
+// Four 8-bit codes (byte k = code k) to fp16 pairs per the selectors:
+// sel 0x4140 -> (c0, c1), 0x4342 -> (c2, c3), 0x4240 -> (c0, c2), 0x4341 -> (c1, c3).
+template <uint32_t SEL>
+__device__ __forceinline__ uint32_t byte2_to_h2(uint32_t w) {
+  const uint32_t x = __byte_perm(w, 0x64646464u, SEL);
+  return h2_as_u32(__hsub2(u32_as_h2(x), u32_as_h2(kH1024)));
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  return h2_as_u32(__floats2half2_rn(lo, hi));
+}
+
+__device__ __forceinline__ uint32_t pack_halves(__half lo, __half hi) {
+  return h2_as_u32(__halves2half2(lo, hi));
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+
+template <int BITS, int D, int NG, int GP>
+__global__ void __launch_bounds__(kWarps * 32, 2) decode_fast_kernel(const DecodeParams p) {
+  using C = Cfg<BITS, D, NG, GP>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  const CacheGeom& geo = p.geom;
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int G = p.G;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int rho = lane >> 2, j = lane & 3;
+
+  int L = p.seq_lens[b];
+  if (L < 0 || L > p.len_limit) {
+    if (threadIdx.x == 0 && split == 0 && kvh == 0 && p.status) atomicOr(p.status, KVQ_FLAG_SEQ_LEN);
+    L = 0;
+  }
+  const int t0 = split * p.chunk;
+  const int t1 = min(L, t0 + p.chunk);
+  if (p.splits > 1 && t0 >= L) return;  // the merge reads splits < ceil(L / chunk) only
+
+  // shared memory: [q fp16 G x D][warp pipelines][tile masks]
+  __half* q_s = reinterpret_cast<__half*>(smem);
+  uint8_t* pipe = smem + ((GP * D * 2 + 127) / 128) * 128;
+  uint32_t* mask_s = reinterpret_cast<uint32_t*>(pipe + kWarps * C::STAGES * C::STAGE);
+  uint8_t* wpipe = pipe + warp * C::STAGES * C::STAGE;
+
+  const __half* qg = p.q + ((long long)b * p.Hq + (long long)kvh * G) * D;
+  for (int i = threadIdx.x; i < GP * D; i += kWarps * 32)
+    q_s[i] = (i < G * D) ? qg[i] : __float2half_rn(0.f);
+  __syncthreads();
+
+  // ---- score-mma A fragments: row r <-> (group r / GP, head r % GP) ----
+  const int g_lo = rho / GP, h_row = rho % GP;
+  const int g_hi = g_lo + 8 / GP;
+  const bool row_ok = h_row < G;
+  uint32_t qa[C::KB][4];
+#pragma unroll
+  for (int kb = 0; kb < C::KB; ++kb) {
+    const int grp = (16 * kb) / C::GSZ;
+    int dk[4];  // channel of k-slots 2j, 2j+1, 2j+8, 2j+9
+    if constexpr (BITS == 4) {
+      const int base = 32 * (kb >> 1) + 8 * j + 2 * (kb & 1);
+      dk[0] = base; dk[1] = base + 4; dk[2] = base + 1; dk[3] = base + 5;
+    } else {
+      const int base = 16 * kb + 4 * j;
+      dk[0] = base; dk[1] = base + 1; dk[2] = base + 2; dk[3] = base + 3;
+    }
+    const __half* qh = q_s + h_row * D;
+    const bool lo = row_ok && g_lo == grp;
+    const bool hi = C::HI && row_ok && g_hi == grp;
+    const uint32_t v01 = pack_halves(qh[dk[0]], qh[dk[1]]);
+    const uint32_t v23 = pack_halves(qh[dk[2]], qh[dk[3]]);
+    qa[kb][0] = lo ? v01 : 0u;
+    qa[kb][1] = hi ? v01 : 0u;
+    qa[kb][2] = lo ? v23 : 0u;
+    qa[kb][3] = hi ? v23 : 0u;
+  }
+  float qs_lo = 0.f, qs_hi = 0.f;  // sum of q_h over the row's group
+  if (row_ok && g_lo < NG)
+    for (int d = g_lo * C::GSZ; d < (g_lo + 1) * C::GSZ; ++d) qs_lo += __half2float(q_s[h_row * D + d]);
+  if (C::HI && row_ok && g_hi < NG)
+    for (int d = g_hi * C::GSZ; d < (g_hi + 1) * C::GSZ; ++d) qs_hi += __half2float(q_s[h_row * D + d]);
+  const int g_lo_c = min(g_lo, NG - 1), g_hi_c = min(g_hi, NG - 1);
+
+  // ---- running state ----
+  float o[C::MT][4];
+#pragma unroll
+  for (int m = 0; m < C::MT; ++m) o[m][0] = o[m][1] = o[m][2] = o[m][3] = 0.f;
+  float cz[4] = {0.f, 0.f, 0.f, 0.f};  // zero-point correction rows (group, head)
+  float m_run = -INFINITY, l_run = 0.f;
+
+  // ---- this warp's tiles ----
+  const int ntiles = (t1 > t0) ? (t1 - t0 + kTT - 1) / kTT : 0;
+  const int nmine = (ntiles > warp) ? (ntiles - warp + kWarps - 1) / kWarps : 0;
+  const uint8_t* kc_g = p.codes[0];
+  const uint8_t* vc_g = p.codes[1];
+  const uint8_t* ks_g = reinterpret_cast<const uint8_t*>(p.scale[0]);
+  const uint8_t* kz_g = reinterpret_cast<const uint8_t*>(p.zero[0]);
+  const uint8_t* vs_g = reinterpret_cast<const uint8_t*>(p.scale[1]);
+  const uint8_t* vz_g = reinterpret_cast<const uint8_t*>(p.zero[1]);
+
+  auto issue = [&](int it) {
+    const int stage = it % C::STAGES;
+    if (it < nmine) {
+      const int start = t0 + (warp + it * kWarps) * kTT;
+      const int n = min(kTT, t1 - start);
+      long long row = -1;
+      if (lane < n) {
+        row = token_row(geo, b, kvh, start + lane);
+        if (row < 0 && p.status) atomicOr(p.status, KVQ_FLAG_BLOCK_TABLE);
+      }
+      const unsigned bad = __ballot_sync(0xffffffffu, row < 0);
+      if (lane == 0) mask_s[warp * C::STAGES + stage] = bad;
+      uint8_t* st = wpipe + stage * C::STAGE;
+      const uint32_t kc_s = smem_u32(st), vc_s = kc_s + C::CODE_TILE;
+      const uint32_t hd_s = vc_s + C::CODE_TILE;
+#pragma unroll
+      for (int k = 0; k < C::CHUNKS; ++k) {
+        const int c = lane + 32 * k;
+        const int tok = c / C::CHUNKS, part = c % C::CHUNKS;
+        const long long r = __shfl_sync(0xffffffffu, row, tok);
+        const bool ok = r >= 0;
+        const long long off = (ok ? r : 0) * C::ROWB + part * 16;
+        const uint32_t dst = tok * C::ROWS + part * 16;
+        cp_async16(kc_s + dst, kc_g + off, ok);
+        cp_async16(vc_s + dst, vc_g + off, ok);
+      }
+      const bool ok = row >= 0;
+      const long long hoff = (ok ? row : 0) * C::HDRB;
+      const uint32_t hdst = hd_s + lane * C::HDRB;
+      cp_async_small<C::HDRB>(hdst, ks_g + hoff, ok);
+      cp_async_small<C::HDRB>(hdst + C::HDR_TILE, kz_g + hoff, ok);
+      cp_async_small<C::HDRB>(hdst + 2 * C::HDR_TILE, vs_g + hoff, ok);
+      cp_async_small<C::HDRB>(hdst + 3 * C::HDR_TILE, vz_g + hoff, ok);
+    }
+    cp_async_commit();  // one group per slot, empty past the end
+  };
+
+#pragma unroll
+  for (int s = 0; s < C::STAGES - 1; ++s) issue(s);
+
+  for (int it = 0; it < nmine; ++it) {
+    cp_async_wait<C::STAGES - 2>();
+    __syncwarp();
+    const int stage = it % C::STAGES;
+    const uint8_t* st = wpipe + stage * C::STAGE;
+    const uint32_t kc_s = smem_u32(st), vc_s = kc_s + C::CODE_TILE;
+    const __half* ks_s = reinterpret_cast<const __half*>(st + 2 * C::CODE_TILE);
+    const __half* kz_s = ks_s + kTT * NG;
+    const __half* vs_s = kz_s + kTT * NG;
+    const __half* vz_s = vs_s + kTT * NG;
+    const unsigned bad = mask_s[warp * C::STAGES + stage];
+
+    // ---------------- scores: 4 n-tiles of 8 tokens ----------------
+    float sc[4][2];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      uint32_t w[C::CHUNKS];
+      const uint32_t rowaddr = kc_s + (8 * nt + (lane & 7)) * C::ROWS;
+      if constexpr (C::CHUNKS == 2) {
+        ldsm_x2(rowaddr + ((lane >> 3) & 1) * 16, w[0], w[1]);
+      } else {
+#pragma unroll
+        for (int c4 = 0; c4 < C::CHUNKS; c4 += 4)
+          ldsm_x4(rowaddr + (c4 + (lane >> 3)) * 16, w[c4], w[c4 + 1], w[c4 + 2], w[c4 + 3]);
+      }
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int c = 0; c < C::CHUNKS; ++c) {
+        if constexpr (BITS == 4) {
+          uint32_t h[4];
+          nib8_to_h2(w[c], h);
+          mma16816(acc, qa[2 * c][0], qa[2 * c][1], qa[2 * c][2], qa[2 * c][3], h[0], h[1]);
+          mma16816(acc, qa[2 * c + 1][0], qa[2 * c + 1][1], qa[2 * c + 1][2], qa[2 * c + 1][3],
+                   h[2], h[3]);
+        } else {
+          const uint32_t h01 = byte2_to_h2<0x4140>(w[c]);
+          const uint32_t h23 = byte2_to_h2<0x4342>(w[c]);
+          mma16816(acc, qa[c][0], qa[c][1], qa[c][2], qa[c][3], h01, h23);
+        }
+      }
+      // group epilogue: row (g, h) holds sum_{d in g} q_h[d] code[d]
+      const int ta = 8 * nt + 2 * j, tb = ta + 1;
+      float va = __half2float(ks_s[ta * NG + g_lo_c]) *
+                 fmaf(-__half2float(kz_s[ta * NG + g_lo_c]), qs_lo, acc[0]);
+      float vb = __half2float(ks_s[tb * NG + g_lo_c]) *
+                 fmaf(-__half2float(kz_s[tb * NG + g_lo_c]), qs_lo, acc[1]);
+      if constexpr (C::HI) {
+        va = fmaf(__half2float(ks_s[ta * NG + g_hi_c]),
+                  fmaf(-__half2float(kz_s[ta * NG + g_hi_c]), qs_hi, acc[2]), va);
+        vb = fmaf(__half2float(ks_s[tb * NG + g_hi_c]),
+                  fmaf(-__half2float(kz_s[tb * NG + g_hi_c]), qs_hi, acc[3]), vb);
+      }
+#pragma unroll
+      for (int s = 0; (1 << s) < C::NGL; ++s) {
+        va += __shfl_xor_sync(0xffffffffu, va, 4 * GP << s);
+        vb += __shfl_xor_sync(0xffffffffu, vb, 4 * GP << s);
+      }
+      const bool head_ok = rho < G;
+      sc[nt][0] = (head_ok && !((bad >> ta) & 1u)) ? va * p.scale_log2 : -INFINITY;
+      sc[nt][1] = (head_ok && !((bad >> tb) & 1u)) ? vb * p.scale_log2 : -INFINITY;
+    }
+
+    // ---------------- online softmax over the tile ----------------
+    float mt = sc[0][0];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) mt = fmaxf(mt, fmaxf(sc[nt][0], sc[nt][1]));
+    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+    const float m_new = fmaxf(m_run, mt);
+    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+    if (__any_sync(0xffffffffu, m_new > m_run)) {
+      const float alpha = exp2f(m_run - m_use);
+      l_run *= alpha;
+      const float a0 = __shfl_sync(0xffffffffu, alpha, (2 * j) << 2);
+      const float a1 = __shfl_sync(0xffffffffu, alpha, (2 * j + 1) << 2);
+#pragma unroll
+      for (int m = 0; m < C::MT; ++m) {
+        o[m][0] *= a0; o[m][1] *= a1; o[m][2] *= a0; o[m][3] *= a1;
+      }
+      cz[0] *= a0; cz[1] *= a1; cz[2] *= a0; cz[3] *= a1;
+    }
+    m_run = m_new;
+    float pr[4][2];
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+      pr[nt][0] = exp2f(sc[nt][0] - m_use);
+      pr[nt][1] = exp2f(sc[nt][1] - m_use);
+      l_run += pr[nt][0] + pr[nt][1];
+    }
+
+    // ---------------- weighted V: 2 k-steps of 16 tokens ----------------
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+      const int tk = 16 * ks + 2 * j;  // this lane's tokens: tk, tk+1, tk+8, tk+9
+      const uint32_t plo = pack_h2(pr[2 * ks][0], pr[2 * ks][1]);
+      const uint32_t phi = pack_h2(pr[2 * ks + 1][0], pr[2 * ks + 1][1]);
+      uint32_t bg[NG][2];
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        const uint32_t slo = pack_halves(vs_s[tk * NG + g], vs_s[(tk + 1) * NG + g]);
+        const uint32_t shi = pack_halves(vs_s[(tk + 8) * NG + g], vs_s[(tk + 9) * NG + g]);
+        bg[g][0] = h2_as_u32(__hmul2(u32_as_h2(plo), u32_as_h2(slo)));
+        bg[g][1] = h2_as_u32(__hmul2(u32_as_h2(phi), u32_as_h2(shi)));
+      }
+      // V codes, transposed: per chunk, lo = tokens 0-7 of the k-step, hi = tokens 8-15
+#pragma unroll
+      for (int c = 0; c < C::CHUNKS; c += 2) {
+        uint32_t xlo0, xhi0, xlo1, xhi1;
+        const int m = lane >> 3;
+        const int tok = 16 * ks + ((m & 1) << 3) + (lane & 7);
+        ldsm_x4_t(vc_s + tok * C::ROWS + (c + (m >> 1)) * 16, xlo0, xhi0, xlo1, xhi1);
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const uint32_t xlo = cc ? xlo1 : xlo0, xhi = cc ? xhi1 : xhi0;
+          const int chunk = c + cc;
+          const int g = (chunk * C::DPC) / C::GSZ;
+          if constexpr (BITS == 4) {
+            uint32_t lo[4], hi[4];
+            nib8_to_h2(xlo, lo);
+            nib8_to_h2(xhi, hi);
+            // channel of lo[e] = chunk*32 + 4*rho + e; m-tile (chunk, pp) rows: e = 2pp, 2pp+1
+            mma16816(o[2 * chunk], lo[0], lo[1], hi[0], hi[1], bg[g][0], bg[g][1]);
+            mma16816(o[2 * chunk + 1], lo[2], lo[3], hi[2], hi[3], bg[g][0], bg[g][1]);
+          } else {
+            const uint32_t l0 = byte2_to_h2<0x4240>(xlo), l1 = byte2_to_h2<0x4341>(xlo);
+            const uint32_t h0 = byte2_to_h2<0x4240>(xhi), h1 = byte2_to_h2<0x4341>(xhi);
+            mma16816(o[chunk], l0, l1, h0, h1, bg[g][0], bg[g][1]);
+          }
+        }
+      }
+      // zero-points: rows = groups, A[g][token] = z_g(token)
+      const int gz = min(rho, NG - 1);
+      const uint32_t zlo = pack_halves(vz_s[tk * NG + gz], vz_s[(tk + 1) * NG + gz]);
+      const uint32_t zhi = pack_halves(vz_s[(tk + 8) * NG + gz], vz_s[(tk + 9) * NG + gz]);
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        const bool mine = rho == g;
+        mma16816(cz, mine ? zlo : 0u, 0u, mine ? zhi : 0u, 0u, bg[g][0], bg[g][1]);
+      }
+    }
+    __syncwarp();
+    issue(it + C::STAGES - 1);
+  }
+  cp_async_wait<0>();
+
+  // ---------------- finish this warp: l, zero-point correction ----------------
+  l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+  l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+  // o[channel][head] -= cz[group(channel)][head]; cz row g lives in lanes 4g + j
+  float corr[NG][2];
+#pragma unroll
+  for (int g = 0; g < NG; ++g) {
+    corr[g][0] = __shfl_sync(0xffffffffu, cz[0], (g << 2) + j);
+    corr[g][1] = __shfl_sync(0xffffffffu, cz[1], (g << 2) + j);
+  }
+  __syncthreads();  // every warp is done with its pipeline: reuse it for the merge
+
+  float* red = reinterpret_cast<float*>(pipe);                 // [warps][GP][D] o
+  float* ml = red + kWarps * GP * D;                            // [warps][GP][2]
+#pragma unroll
+  for (int m = 0; m < C::MT; ++m) {
+    int d0;
+    if constexpr (BITS == 4) d0 = 32 * (m >> 1) + 4 * rho + 2 * (m & 1);
+    else d0 = 16 * m + 2 * rho;
+    const int g = d0 / C::GSZ;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int h = 2 * j + e;
+      if (h < GP) {
+        float* dst = red + (warp * GP + h) * D;
+        dst[d0] = o[m][e] - corr[g][e];
+        dst[d0 + 1] = o[m][2 + e] - corr[g][e];
+      }
+    }
+  }
+  if (j == 0 && rho < GP) {
+    ml[(warp * GP + rho) * 2] = m_run;
+    ml[(warp * GP + rho) * 2 + 1] = l_run;
+  }
+  __syncthreads();
+
+  const long long hq0 = (long long)b * p.Hq + (long long)kvh * G;
+  for (int i = threadIdx.x; i < G * D; i += kWarps * 32) {
+    const int h = i / D, d = i - h * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w2 = 0; w2 < kWarps; ++w2) M = fmaxf(M, ml[(w2 * GP + h) * 2]);
+    float num = 0.f, den = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w2 = 0; w2 < kWarps; ++w2) {
+        const float f = exp2f(ml[(w2 * GP + h) * 2] - M);
+        num = fmaf(f, red[(w2 * GP + h) * D + d], num);
+        den = fmaf(f, ml[(w2 * GP + h) * 2 + 1], den);
+      }
+    }
+    if (p.splits == 1) {
+      p.out[hq0 * D + i] = __float2half_rn(den > 0.f ? num / den : 0.f);
+    } else {
+      p.ws_o[((hq0 + h) * p.splits + split) * D + d] = num;
+      if (d == 0) {
+        float* mlo = p.ws_ml + ((hq0 + h) * p.splits + split) * 2;
+        mlo[0] = M;
+        mlo[1] = den;
+      }
+    }
+  }
+}
+
+template <int BITS, int D, int NG, int GP>
+size_t fast_smem_bytes() {
+  using C = Cfg<BITS, D, NG, GP>;
+  const size_t pipe = (size_t)kWarps * C::STAGES * C::STAGE;
+  const size_t merge = (size_t)kWarps * GP * (D + 2) * sizeof(float);
+  return ((GP * D * 2 + 127) / 128) * 128 + (pipe > merge ? pipe : merge) +
+         kWarps * C::STAGES * sizeof(uint32_t);
+}
+
+template <int BITS, int D, int NG, int GP>
+cudaError_t launch_fast_inst(const DecodeParams& p, cudaStream_t stream) {
+  const size_t smem = fast_smem_bytes<BITS, D, NG, GP>();
+  cudaError_t e = cudaFuncSetAttribute(decode_fast_kernel<BITS, D, NG, GP>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const dim3 grid(p.splits, p.geom.Hkv, p.batch);
+  decode_fast_kernel<BITS, D, NG, GP><<<grid, kWarps * 32, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace fast
+}  // namespace kvq

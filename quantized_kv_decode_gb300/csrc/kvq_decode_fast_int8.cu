@@ -1,0 +1,32 @@
+// Instantiations of the tensor-core decode kernel for INT8 caches.
+#include "kvq_decode_fast.cuh"
+
+namespace kvq {
+
+template <int D, int NG>
+static cudaError_t by_gp8(const DecodeParams& p, int gp, cudaStream_t s, bool* handled) {
+  *handled = true;
+  switch (gp) {
+    case 1: return fast::launch_fast_inst<8, D, NG, 1>(p, s);
+    case 2: return fast::launch_fast_inst<8, D, NG, 2>(p, s);
+    case 4: if constexpr (NG * 4 <= 16) return fast::launch_fast_inst<8, D, NG, 4>(p, s);
+            break;
+    case 8: if constexpr (NG * 8 <= 16) return fast::launch_fast_inst<8, D, NG, 8>(p, s);
+            break;
+  }
+  *handled = false;
+  return cudaSuccess;
+}
+
+cudaError_t launch_decode_fast_int8(const DecodeParams& p, int gp, cudaStream_t s, bool* handled) {
+  *handled = false;
+  const int D = p.geom.D, NG = p.geom.ngroups;
+  if (D == 128 && NG == 2) return by_gp8<128, 2>(p, gp, s, handled);
+  if (D == 128 && NG == 4) return by_gp8<128, 4>(p, gp, s, handled);
+  if (D == 128 && NG == 8) return by_gp8<128, 8>(p, gp, s, handled);
+  if (D == 64 && NG == 2) return by_gp8<64, 2>(p, gp, s, handled);
+  if (D == 64 && NG == 4) return by_gp8<64, 4>(p, gp, s, handled);
+  return cudaSuccess;
+}
+
+}  // namespace kvq
