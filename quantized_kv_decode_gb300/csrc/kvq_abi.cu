@@ -80,30 +80,90 @@ int sm_count() {
   return cached[dev];
 }
 
-// Split count: explicit requests are honoured up to one chunk-aligned tile per
-// split; the automatic choice aims at ~4 CTAs per SM while keeping every split
-// at least 256 tokens long.
-int32_t choose_splits(int64_t units, int64_t max_len, int32_t requested) {
-  const int64_t max_splits = std::max<int64_t>(1, ceil_div(std::max<int64_t>(max_len, 1), kChunkAlign));
-  int64_t s;
-  if (requested > 0) {
-    s = requested;
-  } else {
-    const int sms = sm_count();
-    if (sms <= 0) return 0;
-    const int64_t target = 4LL * sms;
-    s = ceil_div(target, std::max<int64_t>(units, 1));
-    s = std::min<int64_t>(s, std::max<int64_t>(1, ceil_div(max_len, 256)));
-  }
-  s = std::max<int64_t>(1, std::min<int64_t>(s, max_splits));
-  // splits cover chunk-aligned ranges; drop splits that would be empty
-  const int64_t chunk = ceil_div(ceil_div(std::max<int64_t>(max_len, 1), s), kChunkAlign) * kChunkAlign;
-  s = ceil_div(std::max<int64_t>(max_len, 1), chunk);
-  return (int32_t)std::min<int64_t>(s, INT32_MAX);
-}
-
 int32_t split_chunk(int64_t max_len, int32_t splits) {
   return (int32_t)(ceil_div(ceil_div(std::max<int64_t>(max_len, 1), splits), kChunkAlign) * kChunkAlign);
+}
+
+// Fixed cost of one CTA (prologue, pipeline fill, partial write) expressed in
+// tokens of streaming work; used to weigh more splits against fewer.
+constexpr int64_t kCtaOverheadTokens = 128;
+
+// Split count.  Explicit requests are honoured up to one chunk-aligned tile
+// per split and need no device.  The automatic choice models the launch as
+// waves of equal CTAs over (SMs x CTAs per SM) slots and minimises
+// waves x (tokens per CTA + fixed CTA cost), with at least 256 tokens per split.
+int32_t choose_splits(int64_t units, int64_t max_len, int32_t requested, int ctas_per_sm) {
+  const int64_t L = std::max<int64_t>(max_len, 1);
+  const int64_t max_splits = ceil_div(L, kChunkAlign);
+  int64_t s;
+  if (requested > 0) {
+    s = std::min<int64_t>(requested, max_splits);
+  } else {
+    const int sms = sm_count();
+    if (sms <= 0 || ctas_per_sm <= 0) return 0;
+    const int64_t slots = (int64_t)sms * ctas_per_sm;
+    const int64_t s_cap = std::max<int64_t>(1, std::min<int64_t>(ceil_div(L, 256), 256));
+    int64_t best = 1;
+    double best_cost = 1e300;
+    for (int64_t c = 1; c <= s_cap; ++c) {
+      const int64_t chunk = split_chunk(L, (int32_t)c);
+      const int64_t eff = ceil_div(L, chunk);
+      const int64_t waves = ceil_div(std::max<int64_t>(units, 1) * eff, slots);
+      const double cost = (double)waves * (double)(chunk + kCtaOverheadTokens);
+      if (cost < best_cost * 0.999) {
+        best_cost = cost;
+        best = eff;
+      }
+    }
+    s = best;
+  }
+  s = std::max<int64_t>(1, s);
+  // splits cover chunk-aligned ranges; drop splits that would be empty
+  return (int32_t)ceil_div(L, split_chunk(L, (int32_t)s));
+}
+
+// Which decode kernel runs for a descriptor and query-head count: the
+// tensor-core kernel when an instantiation exists, else the generic one.
+struct Plan {
+  bool fast = false;
+  int gp = 1;
+  int32_t splits = 0;
+};
+
+kvq_status make_plan(const kvq_cache_desc* desc, const CacheGeom& geom, int32_t batch,
+                     int32_t num_q_heads, int32_t max_seq_len, int32_t requested, Plan* plan) {
+  const int G = num_q_heads / desc->num_kv_heads;
+  int occ = 0;
+  plan->fast = false;
+  if (desc->bits != 16 && G <= 8) {
+    int gp = 1;
+    while (gp < G) gp <<= 1;
+    plan->gp = gp;
+    if (requested > 0) {
+      plan->splits = choose_splits((int64_t)batch * desc->num_kv_heads, max_seq_len, requested, 0);
+      return KVQ_OK;
+    }
+    DecodeParams probe{};
+    probe.geom = geom;
+    probe.G = G;
+    bool handled = false;
+    cudaError_t e = desc->bits == 4 ? launch_decode_fast_int4(probe, gp, nullptr, &handled, &occ)
+                                    : launch_decode_fast_int8(probe, gp, nullptr, &handled, &occ);
+    if (handled && e != cudaSuccess) return KVQ_ERR_CUDA;
+    plan->fast = handled;
+  }
+  if (requested > 0) {
+    plan->splits = choose_splits((int64_t)batch * desc->num_kv_heads, max_seq_len, requested, 0);
+    return KVQ_OK;
+  }
+  if (!plan->fast) {
+    DecodeParams probe{};
+    probe.geom = geom;
+    probe.G = G;
+    occ = generic_ctas_per_sm(probe);
+  }
+  plan->splits = choose_splits((int64_t)batch * desc->num_kv_heads, max_seq_len, 0, occ);
+  return plan->splits > 0 ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
 kvq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
@@ -185,9 +245,12 @@ kvq_status kvq_append(const kvq_cache_desc* desc, const kvq_cache* cache, int32_
 int32_t kvq_decode_num_splits(const kvq_cache_desc* desc, int32_t batch, int32_t num_q_heads,
                               int32_t max_seq_len, int32_t num_splits) {
   CacheGeom g;
-  if (check_desc(desc, &g) != KVQ_OK || batch < 0 || num_q_heads <= 0 || max_seq_len < 0)
+  if (check_desc(desc, &g) != KVQ_OK || batch < 0 || num_q_heads <= 0 || max_seq_len < 0 ||
+      num_splits < 0 || num_q_heads % desc->num_kv_heads)
     return 0;
-  return choose_splits((int64_t)batch * g.Hkv, max_seq_len, num_splits);
+  Plan plan;
+  if (make_plan(desc, g, batch, num_q_heads, max_seq_len, num_splits, &plan) != KVQ_OK) return 0;
+  return plan.splits;
 }
 
 size_t kvq_decode_workspace_size(const kvq_cache_desc* desc, int32_t batch, int32_t num_q_heads,
@@ -216,8 +279,10 @@ kvq_status kvq_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache, i
   const int G = num_q_heads / desc->num_kv_heads;
   if (G > kMaxGroupHeads) return KVQ_ERR_UNSUPPORTED;
 
-  const int32_t splits = choose_splits((int64_t)batch * desc->num_kv_heads, max_seq_len, num_splits);
-  if (splits <= 0) return KVQ_ERR_CUDA;
+  Plan plan;
+  if ((st = make_plan(desc, p.geom, batch, num_q_heads, max_seq_len, num_splits, &plan)) != KVQ_OK)
+    return st;
+  const int32_t splits = plan.splits;
   const size_t need = workspace_bytes(batch, num_q_heads, desc->head_dim, splits);
   if (need > 0 && (!workspace || workspace_size < need || !aligned(workspace)))
     return KVQ_ERR_WORKSPACE;
@@ -251,10 +316,8 @@ kvq_status kvq_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache, i
   cudaError_t e = cudaSuccess;
   bool handled = false;
   if (desc->bits != 16 && G <= 8) {
-    int gp = 1;
-    while (gp < G) gp <<= 1;
-    if (desc->bits == 4) e = launch_decode_fast_int4(p, gp, s, &handled);
-    else e = launch_decode_fast_int8(p, gp, s, &handled);
+    if (desc->bits == 4) e = launch_decode_fast_int4(p, plan.gp, s, &handled, nullptr);
+    else e = launch_decode_fast_int8(p, plan.gp, s, &handled, nullptr);
   }
   if (!handled) e = launch_decode_generic(p, s);
   if (e == cudaSuccess && splits > 1) e = launch_merge(p, s);

@@ -49,7 +49,10 @@ struct Cfg {
   static constexpr int CODE_TILE = kTT * ROWS;
   static constexpr int HDR_TILE = kTT * HDRB;
   static constexpr int STAGE = 2 * CODE_TILE + 4 * HDR_TILE;
-  static constexpr int STAGES = (kWarps * 4 * STAGE <= 110 * 1024) ? 4 : 3;
+  static constexpr int STAGES = (kWarps * 3 * STAGE <= 72 * 1024) ? 3 : 2;
+  // per-warp scratch of the header pass: fp32 K scale*log2e/sqrt-scale and
+  // zero, fp16 V scale and zero, each [group][token]
+  static constexpr int XHDR = kTT * NG * (4 + 4 + 2 + 2);
   static constexpr int NGL = (NG < 8 / GP) ? NG : 8 / GP;  // groups in accumulator rows 0..7
   static constexpr bool HI = NG * GP > 8;                   // rows 8..15 in use
   static_assert(BITS == 4 || BITS == 8, "bits");
@@ -128,15 +131,22 @@ constexpr uint32_t kH1024 = 0x64006400u;
 constexpr uint32_t kH1_16 = 0x2C002C00u;
 constexpr uint32_t kHm64 = 0xD400D400u;
 
+// (a & b) | c in one LOP3
+__device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;\n" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+
 // Eight 4-bit codes of one 32-bit word (code k in bits 4k..4k+3) to four
 // fp16 pairs: o[0] = (c0, c4), o[1] = (c1, c5), o[2] = (c2, c6), o[3] = (c3, c7).
 // (0x6400 | c) is the fp16 value 1024 + c; (0x6400 | 16c) is 1024 + 16c.
 __device__ __forceinline__ void nib8_to_h2(uint32_t w, uint32_t (&o)[4]) {
   const uint32_t w2 = w >> 8;
-  const uint32_t a = (w & 0x000F000Fu) | kH1024;
-  const uint32_t b = (w & 0x00F000F0u) | kH1024;
-  const uint32_t c = (w2 & 0x000F000Fu) | kH1024;
-  const uint32_t d = (w2 & 0x00F000F0u) | kH1024;
+  const uint32_t a = and_or(w, 0x000F000Fu, kH1024);
+  const uint32_t b = and_or(w, 0x00F000F0u, kH1024);
+  const uint32_t c = and_or(w2, 0x000F000Fu, kH1024);
+  const uint32_t d = and_or(w2, 0x00F000F0u, kH1024);
   o[0] = h2_as_u32(__hsub2(u32_as_h2(a), u32_as_h2(kH1024)));
   o[1] = h2_as_u32(__hfma2(u32_as_h2(b), u32_as_h2(kH1_16), u32_as_h2(kHm64)));
   o[2] = h2_as_u32(__hsub2(u32_as_h2(c), u32_as_h2(kH1024)));
@@ -163,8 +173,13 @@ __device__ __forceinline__ uint32_t pack_halves(__half lo, __half hi) {
 // The kernel
 // ---------------------------------------------------------------------------
 
+// Threshold (log2 units) by which a head's tile maximum may exceed the
+// reference maximum before the accumulators are rescaled; probabilities are
+// bounded by 2^kSlack.
+constexpr float kSlack = 4.f;
+
 template <int BITS, int D, int NG, int GP>
-__global__ void __launch_bounds__(kWarps * 32, 2) decode_fast_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const DecodeParams p) {
   using C = Cfg<BITS, D, NG, GP>;
   extern __shared__ __align__(128) uint8_t smem[];
   const CacheGeom& geo = p.geom;
@@ -182,11 +197,16 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_fast_kernel(const Decod
   const int t1 = min(L, t0 + p.chunk);
   if (p.splits > 1 && t0 >= L) return;  // the merge reads splits < ceil(L / chunk) only
 
-  // shared memory: [q fp16 G x D][warp pipelines][tile masks]
+  // shared memory: [q fp16 GP x D][per warp: stages, header scratch][tile masks]
   __half* q_s = reinterpret_cast<__half*>(smem);
   uint8_t* pipe = smem + ((GP * D * 2 + 127) / 128) * 128;
-  uint32_t* mask_s = reinterpret_cast<uint32_t*>(pipe + kWarps * C::STAGES * C::STAGE);
-  uint8_t* wpipe = pipe + warp * C::STAGES * C::STAGE;
+  constexpr int WARP_BYTES = C::STAGES * C::STAGE + C::XHDR;
+  uint32_t* mask_s = reinterpret_cast<uint32_t*>(pipe + kWarps * WARP_BYTES);
+  uint8_t* wpipe = pipe + warp * WARP_BYTES;
+  float* ksx = reinterpret_cast<float*>(wpipe + C::STAGES * C::STAGE);  // [NG][kTT] s*scale
+  float* kzx = ksx + NG * kTT;                                          // [NG][kTT] z
+  __half* vsx = reinterpret_cast<__half*>(kzx + NG * kTT);              // [NG][kTT]
+  __half* vzx = vsx + NG * kTT;                                         // [NG][kTT]
 
   const __half* qg = p.q + ((long long)b * p.Hq + (long long)kvh * G) * D;
   for (int i = threadIdx.x; i < GP * D; i += kWarps * 32)
@@ -225,13 +245,14 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_fast_kernel(const Decod
   if (C::HI && row_ok && g_hi < NG)
     for (int d = g_hi * C::GSZ; d < (g_hi + 1) * C::GSZ; ++d) qs_hi += __half2float(q_s[h_row * D + d]);
   const int g_lo_c = min(g_lo, NG - 1), g_hi_c = min(g_hi, NG - 1);
+  const bool head_ok = rho < G;
 
   // ---- running state ----
   float o[C::MT][4];
 #pragma unroll
   for (int m = 0; m < C::MT; ++m) o[m][0] = o[m][1] = o[m][2] = o[m][3] = 0.f;
   float cz[4] = {0.f, 0.f, 0.f, 0.f};  // zero-point correction rows (group, head)
-  float m_run = -INFINITY, l_run = 0.f;
+  float m_ref = -INFINITY, l_run = 0.f;
 
   // ---- this warp's tiles ----
   const int ntiles = (t1 > t0) ? (t1 - t0 + kTT - 1) / kTT : 0;
@@ -242,15 +263,17 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_fast_kernel(const Decod
   const uint8_t* kz_g = reinterpret_cast<const uint8_t*>(p.zero[0]);
   const uint8_t* vs_g = reinterpret_cast<const uint8_t*>(p.scale[1]);
   const uint8_t* vz_g = reinterpret_cast<const uint8_t*>(p.zero[1]);
+  const bool dense = geo.layout == KVQ_DENSE;
+  const long long slab_row = ((long long)b * geo.Hkv + kvh) * geo.slots;  // dense only
 
   auto issue = [&](int it) {
     const int stage = it % C::STAGES;
     if (it < nmine) {
       const int start = t0 + (warp + it * kWarps) * kTT;
       const int n = min(kTT, t1 - start);
-      long long row = -1;
+      long long row = -1;  // this lane's token
       if (lane < n) {
-        row = token_row(geo, b, kvh, start + lane);
+        row = dense ? slab_row + start + lane : token_row(geo, b, kvh, start + lane);
         if (row < 0 && p.status) atomicOr(p.status, KVQ_FLAG_BLOCK_TABLE);
       }
       const unsigned bad = __ballot_sync(0xffffffffu, row < 0);
@@ -258,19 +281,33 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_fast_kernel(const Decod
       uint8_t* st = wpipe + stage * C::STAGE;
       const uint32_t kc_s = smem_u32(st), vc_s = kc_s + C::CODE_TILE;
       const uint32_t hd_s = vc_s + C::CODE_TILE;
+      if (dense) {
+        const long long base = (slab_row + start) * C::ROWB;
 #pragma unroll
-      for (int k = 0; k < C::CHUNKS; ++k) {
-        const int c = lane + 32 * k;
-        const int tok = c / C::CHUNKS, part = c % C::CHUNKS;
-        const long long r = __shfl_sync(0xffffffffu, row, tok);
-        const bool ok = r >= 0;
-        const long long off = (ok ? r : 0) * C::ROWB + part * 16;
-        const uint32_t dst = tok * C::ROWS + part * 16;
-        cp_async16(kc_s + dst, kc_g + off, ok);
-        cp_async16(vc_s + dst, vc_g + off, ok);
+        for (int k = 0; k < C::CHUNKS; ++k) {
+          const int c = lane + 32 * k;
+          const int tok = c / C::CHUNKS, part = c % C::CHUNKS;
+          const bool ok = tok < n;
+          const long long off = ok ? base + tok * C::ROWB + part * 16 : 0;
+          const uint32_t dst = tok * C::ROWS + part * 16;
+          cp_async16(kc_s + dst, kc_g + off, ok);
+          cp_async16(vc_s + dst, vc_g + off, ok);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < C::CHUNKS; ++k) {
+          const int c = lane + 32 * k;
+          const int tok = c / C::CHUNKS, part = c % C::CHUNKS;
+          const long long r = __shfl_sync(0xffffffffu, row, tok);
+          const bool ok = r >= 0;
+          const long long off = ok ? r * C::ROWB + part * 16 : 0;
+          const uint32_t dst = tok * C::ROWS + part * 16;
+          cp_async16(kc_s + dst, kc_g + off, ok);
+          cp_async16(vc_s + dst, vc_g + off, ok);
+        }
       }
       const bool ok = row >= 0;
-      const long long hoff = (ok ? row : 0) * C::HDRB;
+      const long long hoff = ok ? row * C::HDRB : 0;
       const uint32_t hdst = hd_s + lane * C::HDRB;
       cp_async_small<C::HDRB>(hdst, ks_g + hoff, ok);
       cp_async_small<C::HDRB>(hdst + C::HDR_TILE, kz_g + hoff, ok);
@@ -289,11 +326,28 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_fast_kernel(const Decod
     const int stage = it % C::STAGES;
     const uint8_t* st = wpipe + stage * C::STAGE;
     const uint32_t kc_s = smem_u32(st), vc_s = kc_s + C::CODE_TILE;
-    const __half* ks_s = reinterpret_cast<const __half*>(st + 2 * C::CODE_TILE);
-    const __half* kz_s = ks_s + kTT * NG;
-    const __half* vs_s = kz_s + kTT * NG;
-    const __half* vz_s = vs_s + kTT * NG;
     const unsigned bad = mask_s[warp * C::STAGES + stage];
+
+    // ---- header pass: lane = token; [token][group] fp16 -> [group][token] ----
+    {
+      const __half* hsrc = reinterpret_cast<const __half*>(st + 2 * C::CODE_TILE) + lane * NG;
+      __half hk[NG], hz[NG], hv[NG], hw[NG];
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        hk[g] = hsrc[g];
+        hz[g] = hsrc[g + kTT * NG];
+        hv[g] = hsrc[g + 2 * kTT * NG];
+        hw[g] = hsrc[g + 3 * kTT * NG];
+      }
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        ksx[g * kTT + lane] = __half2float(hk[g]) * p.scale_log2;
+        kzx[g * kTT + lane] = __half2float(hz[g]);
+        vsx[g * kTT + lane] = hv[g];
+        vzx[g * kTT + lane] = hw[g];
+      }
+    }
+    __syncwarp();
 
     // ---------------- scores: 4 n-tiles of 8 tokens ----------------
     float sc[4][2];
@@ -323,26 +377,25 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_fast_kernel(const Decod
           mma16816(acc, qa[c][0], qa[c][1], qa[c][2], qa[c][3], h01, h23);
         }
       }
-      // group epilogue: row (g, h) holds sum_{d in g} q_h[d] code[d]
-      const int ta = 8 * nt + 2 * j, tb = ta + 1;
-      float va = __half2float(ks_s[ta * NG + g_lo_c]) *
-                 fmaf(-__half2float(kz_s[ta * NG + g_lo_c]), qs_lo, acc[0]);
-      float vb = __half2float(ks_s[tb * NG + g_lo_c]) *
-                 fmaf(-__half2float(kz_s[tb * NG + g_lo_c]), qs_lo, acc[1]);
+      // group epilogue: row (g, h) holds sum_{d in g} q_h[d] code[d]; scale in log2 units
+      const int ta = 8 * nt + 2 * j;
+      const float2 s_lo = *reinterpret_cast<const float2*>(ksx + g_lo_c * kTT + ta);
+      const float2 z_lo = *reinterpret_cast<const float2*>(kzx + g_lo_c * kTT + ta);
+      float va = s_lo.x * fmaf(-z_lo.x, qs_lo, acc[0]);
+      float vb = s_lo.y * fmaf(-z_lo.y, qs_lo, acc[1]);
       if constexpr (C::HI) {
-        va = fmaf(__half2float(ks_s[ta * NG + g_hi_c]),
-                  fmaf(-__half2float(kz_s[ta * NG + g_hi_c]), qs_hi, acc[2]), va);
-        vb = fmaf(__half2float(ks_s[tb * NG + g_hi_c]),
-                  fmaf(-__half2float(kz_s[tb * NG + g_hi_c]), qs_hi, acc[3]), vb);
+        const float2 s_hi = *reinterpret_cast<const float2*>(ksx + g_hi_c * kTT + ta);
+        const float2 z_hi = *reinterpret_cast<const float2*>(kzx + g_hi_c * kTT + ta);
+        va = fmaf(s_hi.x, fmaf(-z_hi.x, qs_hi, acc[2]), va);
+        vb = fmaf(s_hi.y, fmaf(-z_hi.y, qs_hi, acc[3]), vb);
       }
 #pragma unroll
       for (int s = 0; (1 << s) < C::NGL; ++s) {
         va += __shfl_xor_sync(0xffffffffu, va, 4 * GP << s);
         vb += __shfl_xor_sync(0xffffffffu, vb, 4 * GP << s);
       }
-      const bool head_ok = rho < G;
-      sc[nt][0] = (head_ok && !((bad >> ta) & 1u)) ? va * p.scale_log2 : -INFINITY;
-      sc[nt][1] = (head_ok && !((bad >> tb) & 1u)) ? vb * p.scale_log2 : -INFINITY;
+      sc[nt][0] = (head_ok && !((bad >> ta) & 1u)) ? va : -INFINITY;
+      sc[nt][1] = (head_ok && !((bad >> (ta + 1)) & 1u)) ? vb : -INFINITY;
     }
 
     // ---------------- online softmax over the tile ----------------
@@ -351,10 +404,11 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_fast_kernel(const Decod
     for (int nt = 0; nt < 4; ++nt) mt = fmaxf(mt, fmaxf(sc[nt][0], sc[nt][1]));
     mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
     mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
-    const float m_new = fmaxf(m_run, mt);
-    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-    if (__any_sync(0xffffffffu, m_new > m_run)) {
-      const float alpha = exp2f(m_run - m_use);
+    // move the reference maximum only when this tile exceeds it by kSlack
+    const bool need = mt > m_ref + kSlack;
+    const float m_next = need ? mt : m_ref;
+    if (__any_sync(0xffffffffu, need)) {
+      const float alpha = exp2f(m_ref - m_next);  // 0 on the first live tile, 1 if unchanged
       l_run *= alpha;
       const float a0 = __shfl_sync(0xffffffffu, alpha, (2 * j) << 2);
       const float a1 = __shfl_sync(0xffffffffu, alpha, (2 * j + 1) << 2);
@@ -364,7 +418,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_fast_kernel(const Decod
       }
       cz[0] *= a0; cz[1] *= a1; cz[2] *= a0; cz[3] *= a1;
     }
-    m_run = m_new;
+    m_ref = m_next;
+    const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
     float pr[4][2];
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
@@ -382,8 +437,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_fast_kernel(const Decod
       uint32_t bg[NG][2];
 #pragma unroll
       for (int g = 0; g < NG; ++g) {
-        const uint32_t slo = pack_halves(vs_s[tk * NG + g], vs_s[(tk + 1) * NG + g]);
-        const uint32_t shi = pack_halves(vs_s[(tk + 8) * NG + g], vs_s[(tk + 9) * NG + g]);
+        const uint32_t slo = *reinterpret_cast<const uint32_t*>(vsx + g * kTT + tk);
+        const uint32_t shi = *reinterpret_cast<const uint32_t*>(vsx + g * kTT + tk + 8);
         bg[g][0] = h2_as_u32(__hmul2(u32_as_h2(plo), u32_as_h2(slo)));
         bg[g][1] = h2_as_u32(__hmul2(u32_as_h2(phi), u32_as_h2(shi)));
       }
@@ -415,8 +470,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_fast_kernel(const Decod
       }
       // zero-points: rows = groups, A[g][token] = z_g(token)
       const int gz = min(rho, NG - 1);
-      const uint32_t zlo = pack_halves(vz_s[tk * NG + gz], vz_s[(tk + 1) * NG + gz]);
-      const uint32_t zhi = pack_halves(vz_s[(tk + 8) * NG + gz], vz_s[(tk + 9) * NG + gz]);
+      const uint32_t zlo = *reinterpret_cast<const uint32_t*>(vzx + gz * kTT + tk);
+      const uint32_t zhi = *reinterpret_cast<const uint32_t*>(vzx + gz * kTT + tk + 8);
 #pragma unroll
       for (int g = 0; g < NG; ++g) {
         const bool mine = rho == g;
@@ -459,7 +514,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_fast_kernel(const Decod
     }
   }
   if (j == 0 && rho < GP) {
-    ml[(warp * GP + rho) * 2] = m_run;
+    ml[(warp * GP + rho) * 2] = m_ref;
     ml[(warp * GP + rho) * 2 + 1] = l_run;
   }
   __syncthreads();
@@ -495,18 +550,24 @@ __global__ void __launch_bounds__(kWarps * 32, 2) decode_fast_kernel(const Decod
 template <int BITS, int D, int NG, int GP>
 size_t fast_smem_bytes() {
   using C = Cfg<BITS, D, NG, GP>;
-  const size_t pipe = (size_t)kWarps * C::STAGES * C::STAGE;
+  const size_t pipe = (size_t)kWarps * (C::STAGES * C::STAGE + C::XHDR);
   const size_t merge = (size_t)kWarps * GP * (D + 2) * sizeof(float);
   return ((GP * D * 2 + 127) / 128) * 128 + (pipe > merge ? pipe : merge) +
          kWarps * C::STAGES * sizeof(uint32_t);
 }
 
+// Launches the instantiation, or with ctas_per_sm != nullptr only reports
+// how many of its CTAs fit on one SM.
 template <int BITS, int D, int NG, int GP>
-cudaError_t launch_fast_inst(const DecodeParams& p, cudaStream_t stream) {
+cudaError_t launch_fast_inst(const DecodeParams& p, cudaStream_t stream, int* ctas_per_sm) {
   const size_t smem = fast_smem_bytes<BITS, D, NG, GP>();
   cudaError_t e = cudaFuncSetAttribute(decode_fast_kernel<BITS, D, NG, GP>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
+  if (ctas_per_sm) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        ctas_per_sm, decode_fast_kernel<BITS, D, NG, GP>, kWarps * 32, smem);
+  }
   const dim3 grid(p.splits, p.geom.Hkv, p.batch);
   decode_fast_kernel<BITS, D, NG, GP><<<grid, kWarps * 32, smem, stream>>>(p);
   return cudaGetLastError();

@@ -7,7 +7,7 @@
 // K q / sqrt(d), softmax, weighted V) in tiles of 64 tokens with an online
 // softmax, dequantizing x_hat = (q - z) * s element by element in fp32
 // ("What actually happens when you quantize a KV cache", section 3 step 3).
-// The tensor-core kernel in kvq_decode_mma.cu is the fast path for the
+// The tensor-core kernel (kvq_decode_fast.cuh) is the fast path for the
 // common shapes; both write the same partials, merged by merge_kernel.
 //
 // Work unit: one CTA per (split, KV head, sequence); the split covers
@@ -172,32 +172,29 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(const DecodePa
 }
 
 // out[b][h] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s over the splits
-// that hold tokens of sequence b; one warp per (b, h), lanes across channels.
-__global__ void __launch_bounds__(128) merge_kernel(const DecodeParams p) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long rowid = (long long)blockIdx.x * 4 + warp;  // b * Hq + h
-  if (rowid >= (long long)p.batch * p.Hq) return;
+// that hold tokens of sequence b.  One CTA per (b, h), one thread per
+// channel; the loop rescales as it goes so that every load is independent.
+__global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
+  const long long rowid = blockIdx.x;  // b * Hq + h
   const int b = (int)(rowid / p.Hq);
   const int D = p.geom.D;
+  const int d = threadIdx.x;
   const int L = p.seq_lens[b];
   const int nv = (L <= 0 || L > p.len_limit) ? 0 : (L + p.chunk - 1) / p.chunk;
   const float* ml = p.ws_ml + rowid * p.splits * 2;
-  float M = -INFINITY;
-  for (int s = 0; s < nv; ++s) M = fmaxf(M, ml[2 * s]);
-  __half* out = p.out + rowid * D;
-  if (M == -INFINITY) {
-    for (int d = lane; d < D; d += 32) out[d] = __float2half_rn(0.f);
-    return;
+  const float* o = p.ws_o + rowid * p.splits * D + d;
+  float M = -INFINITY, num = 0.f, den = 0.f;
+#pragma unroll 4
+  for (int s = 0; s < nv; ++s) {
+    const float m = ml[2 * s], l = ml[2 * s + 1], x = o[(long long)s * D];
+    if (m == -INFINITY) continue;
+    const float Mn = fmaxf(M, m);
+    const float a = exp2f(M - Mn), f = exp2f(m - Mn);
+    num = fmaf(f, x, num * a);
+    den = fmaf(f, l, den * a);
+    M = Mn;
   }
-  float den = 0.f;
-  for (int s = 0; s < nv; ++s) den = fmaf(exp2f(ml[2 * s] - M), ml[2 * s + 1], den);
-  const float inv = 1.f / den;
-  const float* o = p.ws_o + rowid * p.splits * D;
-  for (int d = lane; d < D; d += 32) {
-    float num = 0.f;
-    for (int s = 0; s < nv; ++s) num = fmaf(exp2f(ml[2 * s] - M), o[(long long)s * D + d], num);
-    out[d] = __float2half_rn(num * inv);
-  }
+  if (d < D) p.out[rowid * D + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
 }
 
 }  // namespace
@@ -231,8 +228,22 @@ cudaError_t launch_decode_generic(const DecodeParams& p, cudaStream_t stream) {
 
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream) {
   const long long rows = (long long)p.batch * p.Hq;
-  merge_kernel<<<(unsigned)((rows + 3) / 4), 128, 0, stream>>>(p);
+  merge_kernel<<<(unsigned)rows, p.geom.D, 0, stream>>>(p);
   return cudaGetLastError();
+}
+
+int generic_ctas_per_sm(const DecodeParams& p) {
+  const int G = p.G, D = p.geom.D;
+  const size_t smem = sizeof(float) * (2 * G * D + G * kTile + 3 * G + 1) +
+                      sizeof(long long) * (kTile + 1);
+  int n = 0;
+  cudaError_t e = cudaErrorInvalidValue;
+  switch (p.geom.bits) {
+    case 4: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_generic_kernel<4>, kThreads, smem); break;
+    case 8: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_generic_kernel<8>, kThreads, smem); break;
+    default: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_generic_kernel<16>, kThreads, smem); break;
+  }
+  return (e == cudaSuccess && n > 0) ? n : 1;
 }
 
 }  // namespace kvq

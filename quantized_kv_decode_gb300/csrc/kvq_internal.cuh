@@ -83,8 +83,12 @@ cudaError_t launch_decode_generic(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream);
 // Tensor-core kernel for INT4/INT8 caches; *handled is false when the shape
 // (head_dim, groups, padded heads per KV head `gp`) has no instantiation.
-cudaError_t launch_decode_fast_int4(const DecodeParams& p, int gp, cudaStream_t s, bool* handled);
-cudaError_t launch_decode_fast_int8(const DecodeParams& p, int gp, cudaStream_t s, bool* handled);
+// With occ != nullptr nothing is launched: *occ receives the CTAs per SM.
+cudaError_t launch_decode_fast_int4(const DecodeParams& p, int gp, cudaStream_t s, bool* handled,
+                                    int* occ);
+cudaError_t launch_decode_fast_int8(const DecodeParams& p, int gp, cudaStream_t s, bool* handled,
+                                    int* occ);
+int generic_ctas_per_sm(const DecodeParams& p);
 
 // Size of the workspace for `splits` splits (0 when splits == 1).
 size_t workspace_bytes(int64_t batch, int64_t Hq, int64_t D, int64_t splits);

@@ -78,7 +78,13 @@ def test_append_edge_groups(bits):
     ]
     # one KV head per row; head_dim 64 holds the 8-value group 8 times over
     x = np.tile(np.array(rows, dtype=np.float16).reshape(1, 1, len(rows), 8), (1, 1, 1, 8))
-    _append_direct(x, bits, 8, 0)
+    # the all-negative group [-9, -8] has -min/s ~ 9 * 255 > 2048 at 8 bits: the
+    # zero-point is clamped and flagged on both sides
+    import quantized_kv_decode_gb300 as K
+    flags = O.quantize_groups(np.transpose(x, (0, 2, 1, 3)), bits, 8)["flags"]
+    expect = K.KVQ_FLAG_ZERO_CLAMPED if np.any(flags & O.ZERO_CLAMPED) else 0
+    assert expect == (K.KVQ_FLAG_ZERO_CLAMPED if bits == 8 else 0)
+    _append_direct(x, bits, 8, expect)
 
 
 def test_append_flags_zero_clamped_and_nonfinite():
@@ -88,7 +94,9 @@ def test_append_flags_zero_clamped_and_nonfinite():
     x[0, 0, 1, 16:24] = np.nan
     import quantized_kv_decode_gb300 as K
     ref = _append_direct(x, 4, 8, K.KVQ_FLAG_ZERO_CLAMPED | K.KVQ_FLAG_NONFINITE)
-    assert ref["flags"][0, 0, 0] == O.ZERO_CLAMPED and ref["flags"][0, 1, 1] == O.NONFINITE
+    # flags are [B][Hkv][T][groups]
+    assert ref["flags"][0, 0, 0, 0] == O.ZERO_CLAMPED
+    assert ref["flags"][0, 1, 0, 1] == O.NONFINITE and ref["flags"][0, 1, 0, 2] == O.NONFINITE
 
 
 def test_append_randomized_wide_ranges():
