@@ -39,26 +39,39 @@ constexpr int kTT = 32;  // tokens per warp tile
 template <int BITS, int D, int NG, int GP>
 struct Cfg {
   static constexpr int ROWB = D * BITS / 8;       // code bytes per token row
-  static constexpr int ROWS = ROWB + 16;          // padded shared-memory row stride
   static constexpr int CHUNKS = ROWB / 16;        // 16-byte chunks per row
+  static constexpr int RPL = 128 / ROWB;          // token rows per 128-byte line
   static constexpr int GSZ = D / NG;              // channels per group
   static constexpr int DPC = 128 / BITS;          // channels per 16-byte chunk
   static constexpr int KB = D / 16;               // k-blocks of the score mma
   static constexpr int MT = D / 16;               // m-tiles of the V mma
   static constexpr int HDRB = NG * 2;             // header bytes per token
-  static constexpr int CODE_TILE = kTT * ROWS;
+  static constexpr int CODE_TILE = kTT * ROWB;
   static constexpr int HDR_TILE = kTT * HDRB;
   static constexpr int STAGE = 2 * CODE_TILE + 4 * HDR_TILE;
-  static constexpr int STAGES = (kWarps * 3 * STAGE <= 72 * 1024) ? 3 : 2;
-  // per-warp scratch of the header pass: fp32 K scale*log2e/sqrt-scale and
-  // zero, fp16 V scale and zero, each [group][token]
-  static constexpr int XHDR = kTT * NG * (4 + 4 + 2 + 2);
+  // per-warp scratch of the header pass, each [group][token]: fp32 K scale
+  // (times the softmax scale in log2 units), fp32 K zero, fp16 V scale and
+  // zero; then fp32 [token] additive mask (0 or -inf) and a row of -inf
+  static constexpr int XHDR = kTT * NG * (4 + 4 + 2 + 2) + 2 * kTT * 4;
+  // three stages when a CTA then still fits three times on an SM
+  static constexpr int STAGES = (kWarps * (3 * STAGE + XHDR) <= 72 * 1024) ? 3 : 2;
+  static constexpr int WARP_BYTES = STAGES * STAGE + XHDR;
+  // CTAs per SM the shared memory allows; the register budget follows it
+  static constexpr int MIN_CTAS = (kWarps * WARP_BYTES <= 72 * 1024) ? 3 : 2;
   static constexpr int NGL = (NG < 8 / GP) ? NG : 8 / GP;  // groups in accumulator rows 0..7
   static constexpr bool HI = NG * GP > 8;                   // rows 8..15 in use
   static_assert(BITS == 4 || BITS == 8, "bits");
+  static_assert(ROWB == 32 || ROWB == 64 || ROWB == 128, "code row size");
   static_assert(GSZ % DPC == 0, "a 16-byte chunk must lie inside one group");
   static_assert(NG * GP <= 16, "groups x padded heads must fit 16 rows");
   static_assert(HDRB == 4 || HDRB == 8 || HDRB == 16, "header row size");
+
+  // Shared-memory byte offset of 16-byte chunk c of token row t: chunk slots
+  // are XOR-swizzled by the row's position so that the 8 rows an ldmatrix
+  // reads at one chunk index fall in 8 different 16-byte bank groups.
+  __device__ static __forceinline__ uint32_t at(int t, int c) {
+    return (uint32_t)(t * ROWB + ((c ^ ((t / RPL) & (CHUNKS - 1))) << 4));
+  }
 };
 
 // ---------------------------------------------------------------------------
@@ -116,8 +129,7 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t a, uint32_t& r0, uint32_t& r1
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -153,6 +165,20 @@ __device__ __forceinline__ void nib8_to_h2(uint32_t w, uint32_t (&o)[4]) {
   o[3] = h2_as_u32(__hfma2(u32_as_h2(d), u32_as_h2(kH1_16), u32_as_h2(kHm64)));
 }
 
+__device__ __forceinline__ void nib8_to_h2_biased(uint32_t w, uint32_t (&o)[4]) {
+  const uint32_t w2 = w >> 8;
+  o[0] = and_or(w, 0x000F000Fu, kH1024);
+  o[1] = and_or(w, 0x00F000F0u, kH1024);
+  o[2] = and_or(w2, 0x000F000Fu, kH1024);
+  o[3] = and_or(w2, 0x00F000F0u, kH1024);
+}
+
+// Four 8-bit codes (byte k = code k) to fp16 pairs 1024 + c (score side).
+template <uint32_t SEL>
+__device__ __forceinline__ uint32_t byte2_to_h2_biased(uint32_t w) {
+  return __byte_perm(w, 0x64646464u, SEL);
+}
+
 // Four 8-bit codes (byte k = code k) to fp16 pairs per the selectors:
 // sel 0x4140 -> (c0, c1), 0x4342 -> (c2, c3), 0x4240 -> (c0, c2), 0x4341 -> (c1, c3).
 template <uint32_t SEL>
@@ -160,6 +186,19 @@ __device__ __forceinline__ uint32_t byte2_to_h2(uint32_t w) {
   const uint32_t x = __byte_perm(w, 0x64646464u, SEL);
   return h2_as_u32(__hsub2(u32_as_h2(x), u32_as_h2(kH1024)));
 }
+
+// 2^x by the SFU (flush-to-zero; 2^-inf = 0)
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Score-side code conversion: the +1024 offset stays in (it is removed
+// exactly by the accumulator's starting value), and the x16 of the odd
+// nibbles is undone by q/16 in the matching A slots.
+// o[0] = (1024+c0, 1024+c4), o[1] = (1024+16c1, 1024+16c5), o[2], o[3] likewise.
+__device__ __forceinline__ void nib8_to_h2_biased(uint32_t w, uint32_t (&o)[4]);
 
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   return h2_as_u32(__floats2half2_rn(lo, hi));
@@ -179,7 +218,8 @@ __device__ __forceinline__ uint32_t pack_halves(__half lo, __half hi) {
 constexpr float kSlack = 4.f;
 
 template <int BITS, int D, int NG, int GP>
-__global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
+    decode_fast_kernel(const DecodeParams p) {
   using C = Cfg<BITS, D, NG, GP>;
   extern __shared__ __align__(128) uint8_t smem[];
   const CacheGeom& geo = p.geom;
@@ -200,17 +240,19 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const Decod
   // shared memory: [q fp16 GP x D][per warp: stages, header scratch][tile masks]
   __half* q_s = reinterpret_cast<__half*>(smem);
   uint8_t* pipe = smem + ((GP * D * 2 + 127) / 128) * 128;
-  constexpr int WARP_BYTES = C::STAGES * C::STAGE + C::XHDR;
-  uint32_t* mask_s = reinterpret_cast<uint32_t*>(pipe + kWarps * WARP_BYTES);
-  uint8_t* wpipe = pipe + warp * WARP_BYTES;
-  float* ksx = reinterpret_cast<float*>(wpipe + C::STAGES * C::STAGE);  // [NG][kTT] s*scale
-  float* kzx = ksx + NG * kTT;                                          // [NG][kTT] z
+  uint32_t* mask_s = reinterpret_cast<uint32_t*>(pipe + kWarps * C::WARP_BYTES);
+  uint8_t* wpipe = pipe + warp * C::WARP_BYTES;
+  float* ksx = reinterpret_cast<float*>(wpipe + C::STAGES * C::STAGE);  // [NG][kTT]
+  float* kzx = ksx + NG * kTT;                                          // [NG][kTT]
   __half* vsx = reinterpret_cast<__half*>(kzx + NG * kTT);              // [NG][kTT]
   __half* vzx = vsx + NG * kTT;                                         // [NG][kTT]
+  float* madd = reinterpret_cast<float*>(vzx + NG * kTT);               // [kTT]
+  float* ninf = madd + kTT;                                             // [kTT]
 
   const __half* qg = p.q + ((long long)b * p.Hq + (long long)kvh * G) * D;
   for (int i = threadIdx.x; i < GP * D; i += kWarps * 32)
     q_s[i] = (i < G * D) ? qg[i] : __float2half_rn(0.f);
+  ninf[lane] = -INFINITY;
   __syncthreads();
 
   // ---- score-mma A fragments: row r <-> (group r / GP, head r % GP) ----
@@ -233,25 +275,44 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const Decod
     const bool lo = row_ok && g_lo == grp;
     const bool hi = C::HI && row_ok && g_hi == grp;
     const uint32_t v01 = pack_halves(qh[dk[0]], qh[dk[1]]);
-    const uint32_t v23 = pack_halves(qh[dk[2]], qh[dk[3]]);
+    uint32_t v23 = pack_halves(qh[dk[2]], qh[dk[3]]);
+    if constexpr (BITS == 4)  // slots 2j+8, 2j+9 meet the odd nibbles, held as 16c
+      v23 = h2_as_u32(__hmul2(u32_as_h2(v23), u32_as_h2(kH1_16)));
     qa[kb][0] = lo ? v01 : 0u;
     qa[kb][1] = hi ? v01 : 0u;
     qa[kb][2] = lo ? v23 : 0u;
     qa[kb][3] = hi ? v23 : 0u;
   }
-  float qs_lo = 0.f, qs_hi = 0.f;  // sum of q_h over the row's group
-  if (row_ok && g_lo < NG)
-    for (int d = g_lo * C::GSZ; d < (g_lo + 1) * C::GSZ; ++d) qs_lo += __half2float(q_s[h_row * D + d]);
-  if (C::HI && row_ok && g_hi < NG)
-    for (int d = g_hi * C::GSZ; d < (g_hi + 1) * C::GSZ; ++d) qs_hi += __half2float(q_s[h_row * D + d]);
+  // Per row (g, h): the sum of q_h over group g, and the offset that the
+  // biased codes add, 1024 * (sum of the row's A entries); both by the same
+  // mma against constant codes.
+  float qs_lo, qs_hi, off_lo, off_hi;
+  {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float bia[4] = {0.f, 0.f, 0.f, 0.f};
+    constexpr uint32_t kOnes = 0x3C003C00u;   // fp16 (1, 1)
+    constexpr uint32_t kSixteen = 0x4C004C00u;  // fp16 (16, 16)
+#pragma unroll
+    for (int kb = 0; kb < C::KB; ++kb) {
+      mma16816(acc, qa[kb][0], qa[kb][1], qa[kb][2], qa[kb][3], kOnes,
+               BITS == 4 ? kSixteen : kOnes);
+      mma16816(bia, qa[kb][0], qa[kb][1], qa[kb][2], qa[kb][3], kH1024, kH1024);
+    }
+    qs_lo = acc[0];
+    qs_hi = acc[2];
+    off_lo = bia[0];
+    off_hi = bia[2];
+  }
   const int g_lo_c = min(g_lo, NG - 1), g_hi_c = min(g_hi, NG - 1);
-  const bool head_ok = rho < G;
+  // lanes whose row holds no live head read a row of -inf as their token mask
+  const float* mrow = (rho < G) ? madd : ninf;
 
   // ---- running state ----
   float o[C::MT][4];
 #pragma unroll
   for (int m = 0; m < C::MT; ++m) o[m][0] = o[m][1] = o[m][2] = o[m][3] = 0.f;
-  float cz[4] = {0.f, 0.f, 0.f, 0.f};  // zero-point correction rows (group, head)
+  float cz0[4] = {0.f, 0.f, 0.f, 0.f};  // zero-point correction rows (group, head),
+  float cz1[4] = {0.f, 0.f, 0.f, 0.f};  // even and odd groups in separate chains
   float m_ref = -INFINITY, l_run = 0.f;
 
   // ---- this warp's tiles ----
@@ -265,6 +326,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const Decod
   const uint8_t* vz_g = reinterpret_cast<const uint8_t*>(p.zero[1]);
   const bool dense = geo.layout == KVQ_DENSE;
   const long long slab_row = ((long long)b * geo.Hkv + kvh) * geo.slots;  // dense only
+  const uint32_t wpipe_s = smem_u32(wpipe);
 
   auto issue = [&](int it) {
     const int stage = it % C::STAGES;
@@ -278,33 +340,20 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const Decod
       }
       const unsigned bad = __ballot_sync(0xffffffffu, row < 0);
       if (lane == 0) mask_s[warp * C::STAGES + stage] = bad;
-      uint8_t* st = wpipe + stage * C::STAGE;
-      const uint32_t kc_s = smem_u32(st), vc_s = kc_s + C::CODE_TILE;
+      const uint32_t kc_s = wpipe_s + stage * C::STAGE, vc_s = kc_s + C::CODE_TILE;
       const uint32_t hd_s = vc_s + C::CODE_TILE;
-      if (dense) {
-        const long long base = (slab_row + start) * C::ROWB;
 #pragma unroll
-        for (int k = 0; k < C::CHUNKS; ++k) {
-          const int c = lane + 32 * k;
-          const int tok = c / C::CHUNKS, part = c % C::CHUNKS;
-          const bool ok = tok < n;
-          const long long off = ok ? base + tok * C::ROWB + part * 16 : 0;
-          const uint32_t dst = tok * C::ROWS + part * 16;
-          cp_async16(kc_s + dst, kc_g + off, ok);
-          cp_async16(vc_s + dst, vc_g + off, ok);
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < C::CHUNKS; ++k) {
-          const int c = lane + 32 * k;
-          const int tok = c / C::CHUNKS, part = c % C::CHUNKS;
-          const long long r = __shfl_sync(0xffffffffu, row, tok);
-          const bool ok = r >= 0;
-          const long long off = ok ? r * C::ROWB + part * 16 : 0;
-          const uint32_t dst = tok * C::ROWS + part * 16;
-          cp_async16(kc_s + dst, kc_g + off, ok);
-          cp_async16(vc_s + dst, vc_g + off, ok);
-        }
+      for (int k = 0; k < C::CHUNKS; ++k) {
+        const int c = lane + 32 * k;
+        const int tok = c / C::CHUNKS, part = c % C::CHUNKS;
+        long long r;
+        if (dense) r = (tok < n) ? slab_row + start + tok : -1;
+        else r = __shfl_sync(0xffffffffu, row, tok);
+        const bool ok = r >= 0;
+        const long long off = ok ? r * C::ROWB + part * 16 : 0;
+        const uint32_t dst = C::at(tok, part);
+        cp_async16(kc_s + dst, kc_g + off, ok);
+        cp_async16(vc_s + dst, vc_g + off, ok);
       }
       const bool ok = row >= 0;
       const long long hoff = ok ? row * C::HDRB : 0;
@@ -320,25 +369,30 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const Decod
 #pragma unroll
   for (int s = 0; s < C::STAGES - 1; ++s) issue(s);
 
+  int stage = 0;
   for (int it = 0; it < nmine; ++it) {
     cp_async_wait<C::STAGES - 2>();
     __syncwarp();
-    const int stage = it % C::STAGES;
     const uint8_t* st = wpipe + stage * C::STAGE;
-    const uint32_t kc_s = smem_u32(st), vc_s = kc_s + C::CODE_TILE;
-    const unsigned bad = mask_s[warp * C::STAGES + stage];
+    const uint32_t kc_s = wpipe_s + stage * C::STAGE, vc_s = kc_s + C::CODE_TILE;
 
     // ---- header pass: lane = token; [token][group] fp16 -> [group][token] ----
     {
-      const __half* hsrc = reinterpret_cast<const __half*>(st + 2 * C::CODE_TILE) + lane * NG;
+      const uint8_t* hsrc = st + 2 * C::CODE_TILE + lane * C::HDRB;
       __half hk[NG], hz[NG], hv[NG], hw[NG];
-#pragma unroll
-      for (int g = 0; g < NG; ++g) {
-        hk[g] = hsrc[g];
-        hz[g] = hsrc[g + kTT * NG];
-        hv[g] = hsrc[g + 2 * kTT * NG];
-        hw[g] = hsrc[g + 3 * kTT * NG];
-      }
+      auto load_row = [&](const uint8_t* src, __half (&dst)[NG]) {
+        if constexpr (NG == 2) {
+          *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(src);
+        } else if constexpr (NG == 4) {
+          *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(src);
+        } else {
+          *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+        }
+      };
+      load_row(hsrc, hk);
+      load_row(hsrc + C::HDR_TILE, hz);
+      load_row(hsrc + 2 * C::HDR_TILE, hv);
+      load_row(hsrc + 3 * C::HDR_TILE, hw);
 #pragma unroll
       for (int g = 0; g < NG; ++g) {
         ksx[g * kTT + lane] = __half2float(hk[g]) * p.scale_log2;
@@ -346,56 +400,75 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const Decod
         vsx[g * kTT + lane] = hv[g];
         vzx[g * kTT + lane] = hw[g];
       }
+      const unsigned bad = mask_s[warp * C::STAGES + stage];
+      madd[lane] = ((bad >> lane) & 1u) ? -INFINITY : 0.f;
     }
     __syncwarp();
 
-    // ---------------- scores: 4 n-tiles of 8 tokens ----------------
+    // ---------------- scores: 4 n-tiles of 8 tokens, two at a time ----------------
     float sc[4][2];
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      uint32_t w[C::CHUNKS];
-      const uint32_t rowaddr = kc_s + (8 * nt + (lane & 7)) * C::ROWS;
-      if constexpr (C::CHUNKS == 2) {
-        ldsm_x2(rowaddr + ((lane >> 3) & 1) * 16, w[0], w[1]);
-      } else {
+    for (int np = 0; np < 2; ++np) {
+      uint32_t w[2][C::CHUNKS];
 #pragma unroll
-        for (int c4 = 0; c4 < C::CHUNKS; c4 += 4)
-          ldsm_x4(rowaddr + (c4 + (lane >> 3)) * 16, w[c4], w[c4 + 1], w[c4 + 2], w[c4 + 3]);
+      for (int u = 0; u < 2; ++u) {
+        const int tok = 8 * (2 * np + u) + (lane & 7);
+        if constexpr (C::CHUNKS == 2) {
+          ldsm_x2(kc_s + C::at(tok, (lane >> 3) & 1), w[u][0], w[u][1]);
+        } else {
+#pragma unroll
+          for (int c4 = 0; c4 < C::CHUNKS; c4 += 4)
+            ldsm_x4(kc_s + C::at(tok, c4 + (lane >> 3)), w[u][c4], w[u][c4 + 1], w[u][c4 + 2],
+                    w[u][c4 + 3]);
+        }
       }
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      // the accumulators start at minus the offset of the biased codes
+      float acc[2][4] = {{-off_lo, -off_lo, -off_hi, -off_hi}, {-off_lo, -off_lo, -off_hi, -off_hi}};
 #pragma unroll
       for (int c = 0; c < C::CHUNKS; ++c) {
         if constexpr (BITS == 4) {
-          uint32_t h[4];
-          nib8_to_h2(w[c], h);
-          mma16816(acc, qa[2 * c][0], qa[2 * c][1], qa[2 * c][2], qa[2 * c][3], h[0], h[1]);
-          mma16816(acc, qa[2 * c + 1][0], qa[2 * c + 1][1], qa[2 * c + 1][2], qa[2 * c + 1][3],
-                   h[2], h[3]);
+          uint32_t h0[4], h1[4];
+          nib8_to_h2_biased(w[0][c], h0);
+          nib8_to_h2_biased(w[1][c], h1);
+          mma16816(acc[0], qa[2 * c][0], qa[2 * c][1], qa[2 * c][2], qa[2 * c][3], h0[0], h0[1]);
+          mma16816(acc[1], qa[2 * c][0], qa[2 * c][1], qa[2 * c][2], qa[2 * c][3], h1[0], h1[1]);
+          mma16816(acc[0], qa[2 * c + 1][0], qa[2 * c + 1][1], qa[2 * c + 1][2],
+                   qa[2 * c + 1][3], h0[2], h0[3]);
+          mma16816(acc[1], qa[2 * c + 1][0], qa[2 * c + 1][1], qa[2 * c + 1][2],
+                   qa[2 * c + 1][3], h1[2], h1[3]);
         } else {
-          const uint32_t h01 = byte2_to_h2<0x4140>(w[c]);
-          const uint32_t h23 = byte2_to_h2<0x4342>(w[c]);
-          mma16816(acc, qa[c][0], qa[c][1], qa[c][2], qa[c][3], h01, h23);
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const uint32_t h01 = byte2_to_h2_biased<0x4140>(w[u][c]);
+            const uint32_t h23 = byte2_to_h2_biased<0x4342>(w[u][c]);
+            mma16816(acc[u], qa[c][0], qa[c][1], qa[c][2], qa[c][3], h01, h23);
+          }
         }
       }
-      // group epilogue: row (g, h) holds sum_{d in g} q_h[d] code[d]; scale in log2 units
-      const int ta = 8 * nt + 2 * j;
-      const float2 s_lo = *reinterpret_cast<const float2*>(ksx + g_lo_c * kTT + ta);
-      const float2 z_lo = *reinterpret_cast<const float2*>(kzx + g_lo_c * kTT + ta);
-      float va = s_lo.x * fmaf(-z_lo.x, qs_lo, acc[0]);
-      float vb = s_lo.y * fmaf(-z_lo.y, qs_lo, acc[1]);
-      if constexpr (C::HI) {
-        const float2 s_hi = *reinterpret_cast<const float2*>(ksx + g_hi_c * kTT + ta);
-        const float2 z_hi = *reinterpret_cast<const float2*>(kzx + g_hi_c * kTT + ta);
-        va = fmaf(s_hi.x, fmaf(-z_hi.x, qs_hi, acc[2]), va);
-        vb = fmaf(s_hi.y, fmaf(-z_hi.y, qs_hi, acc[3]), vb);
-      }
+      // group epilogue: row (g, h) holds sum_{d in g} q_h[d] code[d]; log2 units
 #pragma unroll
-      for (int s = 0; (1 << s) < C::NGL; ++s) {
-        va += __shfl_xor_sync(0xffffffffu, va, 4 * GP << s);
-        vb += __shfl_xor_sync(0xffffffffu, vb, 4 * GP << s);
+      for (int u = 0; u < 2; ++u) {
+        const int nt = 2 * np + u;
+        const int ta = 8 * nt + 2 * j;
+        const float2 s_lo = *reinterpret_cast<const float2*>(ksx + g_lo_c * kTT + ta);
+        const float2 z_lo = *reinterpret_cast<const float2*>(kzx + g_lo_c * kTT + ta);
+        const float2 mk = *reinterpret_cast<const float2*>(mrow + ta);
+        float va = s_lo.x * fmaf(-z_lo.x, qs_lo, acc[u][0]);
+        float vb = s_lo.y * fmaf(-z_lo.y, qs_lo, acc[u][1]);
+        if constexpr (C::HI) {
+          const float2 s_hi = *reinterpret_cast<const float2*>(ksx + g_hi_c * kTT + ta);
+          const float2 z_hi = *reinterpret_cast<const float2*>(kzx + g_hi_c * kTT + ta);
+          va = fmaf(s_hi.x, fmaf(-z_hi.x, qs_hi, acc[u][2]), va);
+          vb = fmaf(s_hi.y, fmaf(-z_hi.y, qs_hi, acc[u][3]), vb);
+        }
+#pragma unroll
+        for (int s = 0; (1 << s) < C::NGL; ++s) {
+          va += __shfl_xor_sync(0xffffffffu, va, 4 * GP << s);
+          vb += __shfl_xor_sync(0xffffffffu, vb, 4 * GP << s);
+        }
+        sc[nt][0] = va + mk.x;
+        sc[nt][1] = vb + mk.y;
       }
-      sc[nt][0] = (head_ok && !((bad >> ta) & 1u)) ? va : -INFINITY;
-      sc[nt][1] = (head_ok && !((bad >> (ta + 1)) & 1u)) ? vb : -INFINITY;
     }
 
     // ---------------- online softmax over the tile ----------------
@@ -408,7 +481,8 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const Decod
     const bool need = mt > m_ref + kSlack;
     const float m_next = need ? mt : m_ref;
     if (__any_sync(0xffffffffu, need)) {
-      const float alpha = exp2f(m_ref - m_next);  // 0 on the first live tile, 1 if unchanged
+      // 0 on the first live tile; lanes that keep their reference scale by 1
+      const float alpha = need ? ex2(m_ref - m_next) : 1.f;
       l_run *= alpha;
       const float a0 = __shfl_sync(0xffffffffu, alpha, (2 * j) << 2);
       const float a1 = __shfl_sync(0xffffffffu, alpha, (2 * j + 1) << 2);
@@ -416,15 +490,16 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const Decod
       for (int m = 0; m < C::MT; ++m) {
         o[m][0] *= a0; o[m][1] *= a1; o[m][2] *= a0; o[m][3] *= a1;
       }
-      cz[0] *= a0; cz[1] *= a1; cz[2] *= a0; cz[3] *= a1;
+      cz0[0] *= a0; cz0[1] *= a1; cz0[2] *= a0; cz0[3] *= a1;
+      cz1[0] *= a0; cz1[1] *= a1; cz1[2] *= a0; cz1[3] *= a1;
     }
     m_ref = m_next;
     const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
     float pr[4][2];
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
-      pr[nt][0] = exp2f(sc[nt][0] - m_use);
-      pr[nt][1] = exp2f(sc[nt][1] - m_use);
+      pr[nt][0] = ex2(sc[nt][0] - m_use);
+      pr[nt][1] = ex2(sc[nt][1] - m_use);
       l_run += pr[nt][0] + pr[nt][1];
     }
 
@@ -448,7 +523,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const Decod
         uint32_t xlo0, xhi0, xlo1, xhi1;
         const int m = lane >> 3;
         const int tok = 16 * ks + ((m & 1) << 3) + (lane & 7);
-        ldsm_x4_t(vc_s + tok * C::ROWS + (c + (m >> 1)) * 16, xlo0, xhi0, xlo1, xhi1);
+        ldsm_x4_t(vc_s + C::at(tok, c + (m >> 1)), xlo0, xhi0, xlo1, xhi1);
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const uint32_t xlo = cc ? xlo1 : xlo0, xhi = cc ? xhi1 : xhi0;
@@ -475,11 +550,13 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const Decod
 #pragma unroll
       for (int g = 0; g < NG; ++g) {
         const bool mine = rho == g;
-        mma16816(cz, mine ? zlo : 0u, 0u, mine ? zhi : 0u, 0u, bg[g][0], bg[g][1]);
+        if (g & 1) mma16816(cz1, mine ? zlo : 0u, 0u, mine ? zhi : 0u, 0u, bg[g][0], bg[g][1]);
+        else mma16816(cz0, mine ? zlo : 0u, 0u, mine ? zhi : 0u, 0u, bg[g][0], bg[g][1]);
       }
     }
     __syncwarp();
     issue(it + C::STAGES - 1);
+    stage = (stage + 1 == C::STAGES) ? 0 : stage + 1;
   }
   cp_async_wait<0>();
 
@@ -490,8 +567,8 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const Decod
   float corr[NG][2];
 #pragma unroll
   for (int g = 0; g < NG; ++g) {
-    corr[g][0] = __shfl_sync(0xffffffffu, cz[0], (g << 2) + j);
-    corr[g][1] = __shfl_sync(0xffffffffu, cz[1], (g << 2) + j);
+    corr[g][0] = __shfl_sync(0xffffffffu, cz0[0] + cz1[0], (g << 2) + j);
+    corr[g][1] = __shfl_sync(0xffffffffu, cz0[1] + cz1[1], (g << 2) + j);
   }
   __syncthreads();  // every warp is done with its pipeline: reuse it for the merge
 
@@ -550,7 +627,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3) decode_fast_kernel(const Decod
 template <int BITS, int D, int NG, int GP>
 size_t fast_smem_bytes() {
   using C = Cfg<BITS, D, NG, GP>;
-  const size_t pipe = (size_t)kWarps * (C::STAGES * C::STAGE + C::XHDR);
+  const size_t pipe = (size_t)kWarps * C::WARP_BYTES;
   const size_t merge = (size_t)kWarps * GP * (D + 2) * sizeof(float);
   return ((GP * D * 2 + 127) / 128) * 128 + (pipe > merge ? pipe : merge) +
          kWarps * C::STAGES * sizeof(uint32_t);
