@@ -58,6 +58,7 @@ struct Cfg {
   static constexpr int WARP_BYTES = STAGES * STAGE + XHDR;
   // CTAs per SM the shared memory allows; the register budget follows it
   static constexpr int MIN_CTAS = (kWarps * WARP_BYTES <= 72 * 1024) ? 3 : 2;
+  static constexpr int NTV = (NG * GP + 7) / 8;           // V-mma n-tiles: columns (group, head)
   static constexpr int NGL = (NG < 8 / GP) ? NG : 8 / GP;  // groups in accumulator rows 0..7
   static constexpr bool HI = NG * GP > 8;                   // rows 8..15 in use
   static_assert(BITS == 4 || BITS == 8, "bits");
@@ -304,15 +305,23 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
     off_hi = bia[2];
   }
   const int g_lo_c = min(g_lo, NG - 1), g_hi_c = min(g_hi, NG - 1);
-  // lanes whose row holds no live head read a row of -inf as their token mask
-  const float* mrow = (rho < G) ? madd : ninf;
+  // After the group sum, lane rho holds the scores of head rho % GP; lanes of
+  // a head beyond G read a row of -inf as their token mask.
+  const int h_lane = rho % GP;
+  const float* mrow = (h_lane < G) ? madd : ninf;
+  // V-mma B columns of this lane, per n-tile t: (group (8t + rho) / GP, head h_lane)
+  int gcol[C::NTV];
+#pragma unroll
+  for (int t = 0; t < C::NTV; ++t) gcol[t] = (8 * t + rho) / GP;
 
   // ---- running state ----
   float o[C::MT][4];
 #pragma unroll
   for (int m = 0; m < C::MT; ++m) o[m][0] = o[m][1] = o[m][2] = o[m][3] = 0.f;
-  float cz0[4] = {0.f, 0.f, 0.f, 0.f};  // zero-point correction rows (group, head),
-  float cz1[4] = {0.f, 0.f, 0.f, 0.f};  // even and odd groups in separate chains
+  float cz[C::NTV][4];  // zero-point terms: rows = groups r, columns = (group, head)
+#pragma unroll
+  for (int t = 0; t < C::NTV; ++t) cz[t][0] = cz[t][1] = cz[t][2] = cz[t][3] = 0.f;
+  bool bt_bad = false;  // an unmapped page was met (flagged once at the end)
   float m_ref = -INFINITY, l_run = 0.f;
 
   // ---- this warp's tiles ----
@@ -328,33 +337,48 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
   const long long slab_row = ((long long)b * geo.Hkv + kvh) * geo.slots;  // dense only
   const uint32_t wpipe_s = smem_u32(wpipe);
 
-  auto issue = [&](int it) {
+  // issues tile `it` into its stage; returns true when a page was unmapped
+  auto issue = [&](int it) -> bool {
     const int stage = it % C::STAGES;
+    bool unmapped = false;
     if (it < nmine) {
       const int start = t0 + (warp + it * kWarps) * kTT;
       const int n = min(kTT, t1 - start);
       long long row = -1;  // this lane's token
-      if (lane < n) {
-        row = dense ? slab_row + start + lane : token_row(geo, b, kvh, start + lane);
-        if (row < 0 && p.status) atomicOr(p.status, KVQ_FLAG_BLOCK_TABLE);
+      const uint32_t kc_s = wpipe_s + stage * C::STAGE, vc_s = kc_s + C::CODE_TILE;
+      const uint32_t hd_s = vc_s + C::CODE_TILE;
+      if (dense) {
+        if (lane < n) row = slab_row + start + lane;
+        const long long base = (slab_row + start) * C::ROWB;
+#pragma unroll
+        for (int k = 0; k < C::CHUNKS; ++k) {
+          const int c = lane + 32 * k;
+          const int tok = c / C::CHUNKS, part = c % C::CHUNKS;
+          const bool ok = tok < n;
+          const long long off = ok ? base + tok * C::ROWB + part * 16 : 0;
+          const uint32_t dst = C::at(tok, part);
+          cp_async16(kc_s + dst, kc_g + off, ok);
+          cp_async16(vc_s + dst, vc_g + off, ok);
+        }
+      } else {
+        if (lane < n) {
+          row = token_row(geo, b, kvh, start + lane);
+          unmapped = row < 0;
+        }
+#pragma unroll
+        for (int k = 0; k < C::CHUNKS; ++k) {
+          const int c = lane + 32 * k;
+          const int tok = c / C::CHUNKS, part = c % C::CHUNKS;
+          const long long r = __shfl_sync(0xffffffffu, row, tok);
+          const bool ok = r >= 0;
+          const long long off = ok ? r * C::ROWB + part * 16 : 0;
+          const uint32_t dst = C::at(tok, part);
+          cp_async16(kc_s + dst, kc_g + off, ok);
+          cp_async16(vc_s + dst, vc_g + off, ok);
+        }
       }
       const unsigned bad = __ballot_sync(0xffffffffu, row < 0);
       if (lane == 0) mask_s[warp * C::STAGES + stage] = bad;
-      const uint32_t kc_s = wpipe_s + stage * C::STAGE, vc_s = kc_s + C::CODE_TILE;
-      const uint32_t hd_s = vc_s + C::CODE_TILE;
-#pragma unroll
-      for (int k = 0; k < C::CHUNKS; ++k) {
-        const int c = lane + 32 * k;
-        const int tok = c / C::CHUNKS, part = c % C::CHUNKS;
-        long long r;
-        if (dense) r = (tok < n) ? slab_row + start + tok : -1;
-        else r = __shfl_sync(0xffffffffu, row, tok);
-        const bool ok = r >= 0;
-        const long long off = ok ? r * C::ROWB + part * 16 : 0;
-        const uint32_t dst = C::at(tok, part);
-        cp_async16(kc_s + dst, kc_g + off, ok);
-        cp_async16(vc_s + dst, vc_g + off, ok);
-      }
       const bool ok = row >= 0;
       const long long hoff = ok ? row * C::HDRB : 0;
       const uint32_t hdst = hd_s + lane * C::HDRB;
@@ -364,10 +388,11 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
       cp_async_small<C::HDRB>(hdst + 3 * C::HDR_TILE, vz_g + hoff, ok);
     }
     cp_async_commit();  // one group per slot, empty past the end
+    return unmapped;
   };
 
 #pragma unroll
-  for (int s = 0; s < C::STAGES - 1; ++s) issue(s);
+  for (int s = 0; s < C::STAGES - 1; ++s) bt_bad |= issue(s);
 
   int stage = 0;
   for (int it = 0; it < nmine; ++it) {
@@ -379,26 +404,29 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
     // ---- header pass: lane = token; [token][group] fp16 -> [group][token] ----
     {
       const uint8_t* hsrc = st + 2 * C::CODE_TILE + lane * C::HDRB;
-      __half hk[NG], hz[NG], hv[NG], hw[NG];
-      auto load_row = [&](const uint8_t* src, __half (&dst)[NG]) {
+      uint32_t r[4][NG / 2];  // K scale, K zero, V scale, V zero: two halves per word
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        const uint8_t* src = hsrc + a * C::HDR_TILE;
         if constexpr (NG == 2) {
-          *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(src);
+          r[a][0] = *reinterpret_cast<const uint32_t*>(src);
         } else if constexpr (NG == 4) {
-          *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(src);
+          const uint2 v = *reinterpret_cast<const uint2*>(src);
+          r[a][0] = v.x; r[a][1] = v.y;
         } else {
-          *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+          const uint4 v = *reinterpret_cast<const uint4*>(src);
+          r[a][0] = v.x; r[a][1] = v.y; r[a][2] = v.z; r[a][3] = v.w;
         }
-      };
-      load_row(hsrc, hk);
-      load_row(hsrc + C::HDR_TILE, hz);
-      load_row(hsrc + 2 * C::HDR_TILE, hv);
-      load_row(hsrc + 3 * C::HDR_TILE, hw);
+      }
 #pragma unroll
       for (int g = 0; g < NG; ++g) {
-        ksx[g * kTT + lane] = __half2float(hk[g]) * p.scale_log2;
-        kzx[g * kTT + lane] = __half2float(hz[g]);
-        vsx[g * kTT + lane] = hv[g];
-        vzx[g * kTT + lane] = hw[g];
+        const int sh = (g & 1) * 16;
+        const unsigned short uk = (unsigned short)(r[0][g / 2] >> sh);
+        const unsigned short uz = (unsigned short)(r[1][g / 2] >> sh);
+        ksx[g * kTT + lane] = __half2float(__ushort_as_half(uk)) * p.scale_log2;
+        kzx[g * kTT + lane] = __half2float(__ushort_as_half(uz));
+        reinterpret_cast<unsigned short*>(vsx)[g * kTT + lane] = (unsigned short)(r[2][g / 2] >> sh);
+        reinterpret_cast<unsigned short*>(vzx)[g * kTT + lane] = (unsigned short)(r[3][g / 2] >> sh);
       }
       const unsigned bad = mask_s[warp * C::STAGES + stage];
       madd[lane] = ((bad >> lane) & 1u) ? -INFINITY : 0.f;
@@ -484,14 +512,17 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
       // 0 on the first live tile; lanes that keep their reference scale by 1
       const float alpha = need ? ex2(m_ref - m_next) : 1.f;
       l_run *= alpha;
-      const float a0 = __shfl_sync(0xffffffffu, alpha, (2 * j) << 2);
-      const float a1 = __shfl_sync(0xffffffffu, alpha, (2 * j + 1) << 2);
+      // V columns 2j, 2j+1 (of any n-tile) belong to heads (2j) % GP, (2j+1) % GP
+      const float a0 = __shfl_sync(0xffffffffu, alpha, ((2 * j) % GP) << 2);
+      const float a1 = __shfl_sync(0xffffffffu, alpha, ((2 * j + 1) % GP) << 2);
 #pragma unroll
       for (int m = 0; m < C::MT; ++m) {
         o[m][0] *= a0; o[m][1] *= a1; o[m][2] *= a0; o[m][3] *= a1;
       }
-      cz0[0] *= a0; cz0[1] *= a1; cz0[2] *= a0; cz0[3] *= a1;
-      cz1[0] *= a0; cz1[1] *= a1; cz1[2] *= a0; cz1[3] *= a1;
+#pragma unroll
+      for (int t = 0; t < C::NTV; ++t) {
+        cz[t][0] *= a0; cz[t][1] *= a1; cz[t][2] *= a0; cz[t][3] *= a1;
+      }
     }
     m_ref = m_next;
     const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
@@ -509,13 +540,16 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
       const int tk = 16 * ks + 2 * j;  // this lane's tokens: tk, tk+1, tk+8, tk+9
       const uint32_t plo = pack_h2(pr[2 * ks][0], pr[2 * ks][1]);
       const uint32_t phi = pack_h2(pr[2 * ks + 1][0], pr[2 * ks + 1][1]);
-      uint32_t bg[NG][2];
+      // B[token][(g, h)] = p_h(token) * s_g(token); this lane's column per n-tile
+      uint32_t bt[C::NTV][2];
 #pragma unroll
-      for (int g = 0; g < NG; ++g) {
+      for (int t = 0; t < C::NTV; ++t) {
+        const int g = min(gcol[t], NG - 1);
         const uint32_t slo = *reinterpret_cast<const uint32_t*>(vsx + g * kTT + tk);
         const uint32_t shi = *reinterpret_cast<const uint32_t*>(vsx + g * kTT + tk + 8);
-        bg[g][0] = h2_as_u32(__hmul2(u32_as_h2(plo), u32_as_h2(slo)));
-        bg[g][1] = h2_as_u32(__hmul2(u32_as_h2(phi), u32_as_h2(shi)));
+        const bool live = gcol[t] < NG;
+        bt[t][0] = live ? h2_as_u32(__hmul2(u32_as_h2(plo), u32_as_h2(slo))) : 0u;
+        bt[t][1] = live ? h2_as_u32(__hmul2(u32_as_h2(phi), u32_as_h2(shi))) : 0u;
       }
       // V codes, transposed: per chunk, lo = tokens 0-7 of the k-step, hi = tokens 8-15
 #pragma unroll
@@ -528,48 +562,39 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
         for (int cc = 0; cc < 2; ++cc) {
           const uint32_t xlo = cc ? xlo1 : xlo0, xhi = cc ? xhi1 : xhi0;
           const int chunk = c + cc;
-          const int g = (chunk * C::DPC) / C::GSZ;
+          const int t = ((chunk * C::DPC) / C::GSZ) * GP / 8;  // n-tile of the chunk's group
           if constexpr (BITS == 4) {
             uint32_t lo[4], hi[4];
             nib8_to_h2(xlo, lo);
             nib8_to_h2(xhi, hi);
             // channel of lo[e] = chunk*32 + 4*rho + e; m-tile (chunk, pp) rows: e = 2pp, 2pp+1
-            mma16816(o[2 * chunk], lo[0], lo[1], hi[0], hi[1], bg[g][0], bg[g][1]);
-            mma16816(o[2 * chunk + 1], lo[2], lo[3], hi[2], hi[3], bg[g][0], bg[g][1]);
+            mma16816(o[2 * chunk], lo[0], lo[1], hi[0], hi[1], bt[t][0], bt[t][1]);
+            mma16816(o[2 * chunk + 1], lo[2], lo[3], hi[2], hi[3], bt[t][0], bt[t][1]);
           } else {
             const uint32_t l0 = byte2_to_h2<0x4240>(xlo), l1 = byte2_to_h2<0x4341>(xlo);
             const uint32_t h0 = byte2_to_h2<0x4240>(xhi), h1 = byte2_to_h2<0x4341>(xhi);
-            mma16816(o[chunk], l0, l1, h0, h1, bg[g][0], bg[g][1]);
+            mma16816(o[chunk], l0, l1, h0, h1, bt[t][0], bt[t][1]);
           }
         }
       }
-      // zero-points: rows = groups, A[g][token] = z_g(token)
+      // zero-points: A rows = groups r, A[r][token] = z_r(token); the entries
+      // with r equal to the column's group are the ones used
       const int gz = min(rho, NG - 1);
-      const uint32_t zlo = *reinterpret_cast<const uint32_t*>(vzx + gz * kTT + tk);
-      const uint32_t zhi = *reinterpret_cast<const uint32_t*>(vzx + gz * kTT + tk + 8);
+      const uint32_t zlo = rho < NG ? *reinterpret_cast<const uint32_t*>(vzx + gz * kTT + tk) : 0u;
+      const uint32_t zhi = rho < NG ? *reinterpret_cast<const uint32_t*>(vzx + gz * kTT + tk + 8) : 0u;
 #pragma unroll
-      for (int g = 0; g < NG; ++g) {
-        const bool mine = rho == g;
-        if (g & 1) mma16816(cz1, mine ? zlo : 0u, 0u, mine ? zhi : 0u, 0u, bg[g][0], bg[g][1]);
-        else mma16816(cz0, mine ? zlo : 0u, 0u, mine ? zhi : 0u, 0u, bg[g][0], bg[g][1]);
-      }
+      for (int t = 0; t < C::NTV; ++t) mma16816(cz[t], zlo, 0u, zhi, 0u, bt[t][0], bt[t][1]);
     }
     __syncwarp();
-    issue(it + C::STAGES - 1);
+    bt_bad |= issue(it + C::STAGES - 1);
     stage = (stage + 1 == C::STAGES) ? 0 : stage + 1;
   }
   cp_async_wait<0>();
 
   // ---------------- finish this warp: l, zero-point correction ----------------
+  if (bt_bad && p.status) atomicOr(p.status, KVQ_FLAG_BLOCK_TABLE);
   l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
   l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
-  // o[channel][head] -= cz[group(channel)][head]; cz row g lives in lanes 4g + j
-  float corr[NG][2];
-#pragma unroll
-  for (int g = 0; g < NG; ++g) {
-    corr[g][0] = __shfl_sync(0xffffffffu, cz0[0] + cz1[0], (g << 2) + j);
-    corr[g][1] = __shfl_sync(0xffffffffu, cz0[1] + cz1[1], (g << 2) + j);
-  }
   __syncthreads();  // every warp is done with its pipeline: reuse it for the merge
 
   float* red = reinterpret_cast<float*>(pipe);                 // [warps][GP][D] o
@@ -579,14 +604,20 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
     int d0;
     if constexpr (BITS == 4) d0 = 32 * (m >> 1) + 4 * rho + 2 * (m & 1);
     else d0 = 16 * m + 2 * rho;
-    const int g = d0 / C::GSZ;
+    const int g = ((BITS == 4 ? (m >> 1) : m) * C::DPC) / C::GSZ;  // group of the m-tile's chunk
+    const int t = g * GP / 8;
+    // o[channel][(g, h)] -= cz[g][(g, h)]: row g of the correction lives in lanes 4g + j
+    const float corr0 = __shfl_sync(0xffffffffu, cz[t][0], (g << 2) + j);
+    const float corr1 = __shfl_sync(0xffffffffu, cz[t][1], (g << 2) + j);
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      const int h = 2 * j + e;
-      if (h < GP) {
+      const int col = 8 * t + 2 * j + e;  // (group col / GP, head col % GP)
+      const int h = col % GP;
+      if (col / GP == g && h < G) {
+        const float corr = e ? corr1 : corr0;
         float* dst = red + (warp * GP + h) * D;
-        dst[d0] = o[m][e] - corr[g][e];
-        dst[d0 + 1] = o[m][2 + e] - corr[g][e];
+        dst[d0] = o[m][e] - corr;
+        dst[d0 + 1] = o[m][2 + e] - corr;
       }
     }
   }
