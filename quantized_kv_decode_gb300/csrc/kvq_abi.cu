@@ -84,9 +84,10 @@ int32_t split_chunk(int64_t max_len, int32_t splits) {
   return (int32_t)(ceil_div(ceil_div(std::max<int64_t>(max_len, 1), splits), kChunkAlign) * kChunkAlign);
 }
 
-// Fixed cost of one CTA (prologue, pipeline fill, partial write) expressed in
-// tokens of streaming work; used to weigh more splits against fewer.
-constexpr int64_t kCtaOverheadTokens = 128;
+// Fixed cost of one CTA (prologue, pipeline fill, partial write and merge)
+// expressed in tokens of streaming work; used to weigh more splits against
+// fewer (fitted to split sweeps of the tensor-core kernel on GB300).
+constexpr int64_t kCtaOverheadTokens = 1024;
 
 // Split count.  Explicit requests are honoured up to one chunk-aligned tile
 // per split and need no device.  The automatic choice models the launch as

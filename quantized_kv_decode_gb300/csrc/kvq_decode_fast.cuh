@@ -49,10 +49,13 @@ struct Cfg {
   static constexpr int CODE_TILE = kTT * ROWB;
   static constexpr int HDR_TILE = kTT * HDRB;
   static constexpr int STAGE = 2 * CODE_TILE + 4 * HDR_TILE;
-  // per-warp scratch of the header pass, each [group][token]: fp32 K scale
-  // (times the softmax scale in log2 units), fp32 K zero, fp16 V scale and
-  // zero; then fp32 [token] additive mask (0 or -inf) and a row of -inf
-  static constexpr int XHDR = kTT * NG * (4 + 4 + 2 + 2) + 2 * kTT * 4;
+  // per-warp scratch of the header pass, rows [group] of [token] entries
+  // padded so that lanes reading different groups hit different banks:
+  // fp32 K (scale * softmax scale in log2 units, zero) pairs, fp16 V scale,
+  // fp16 V zero; then an fp32 [token] additive mask (0 or -inf)
+  static constexpr int KROW = kTT + 8;            // float2 entries per K row
+  static constexpr int VROW = kTT + 8;            // half entries per V row
+  static constexpr int XHDR = NG * KROW * 8 + 2 * NG * VROW * 2 + kTT * 4;
   // three stages when a CTA then still fits three times on an SM
   static constexpr int STAGES = (kWarps * (3 * STAGE + XHDR) <= 72 * 1024) ? 3 : 2;
   static constexpr int WARP_BYTES = STAGES * STAGE + XHDR;
@@ -243,17 +246,14 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
   uint8_t* pipe = smem + ((GP * D * 2 + 127) / 128) * 128;
   uint32_t* mask_s = reinterpret_cast<uint32_t*>(pipe + kWarps * C::WARP_BYTES);
   uint8_t* wpipe = pipe + warp * C::WARP_BYTES;
-  float* ksx = reinterpret_cast<float*>(wpipe + C::STAGES * C::STAGE);  // [NG][kTT]
-  float* kzx = ksx + NG * kTT;                                          // [NG][kTT]
-  __half* vsx = reinterpret_cast<__half*>(kzx + NG * kTT);              // [NG][kTT]
-  __half* vzx = vsx + NG * kTT;                                         // [NG][kTT]
-  float* madd = reinterpret_cast<float*>(vzx + NG * kTT);               // [kTT]
-  float* ninf = madd + kTT;                                             // [kTT]
+  float2* ksz = reinterpret_cast<float2*>(wpipe + C::STAGES * C::STAGE);  // [NG][KROW]
+  __half* vsx = reinterpret_cast<__half*>(ksz + NG * C::KROW);            // [NG][VROW]
+  __half* vzx = vsx + NG * C::VROW;                                       // [NG][VROW]
+  float* madd = reinterpret_cast<float*>(vzx + NG * C::VROW);             // [kTT]
 
   const __half* qg = p.q + ((long long)b * p.Hq + (long long)kvh * G) * D;
   for (int i = threadIdx.x; i < GP * D; i += kWarps * 32)
     q_s[i] = (i < G * D) ? qg[i] : __float2half_rn(0.f);
-  ninf[lane] = -INFINITY;
   __syncthreads();
 
   // ---- score-mma A fragments: row r <-> (group r / GP, head r % GP) ----
@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
   // After the group sum, lane rho holds the scores of head rho % GP; lanes of
   // a head beyond G read a row of -inf as their token mask.
   const int h_lane = rho % GP;
-  const float* mrow = (h_lane < G) ? madd : ninf;
+  const float hmask = (h_lane < G) ? 0.f : -INFINITY;
   // V-mma B columns of this lane, per n-tile t: (group (8t + rho) / GP, head h_lane)
   int gcol[C::NTV];
 #pragma unroll
@@ -400,6 +400,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
     __syncwarp();
     const uint8_t* st = wpipe + stage * C::STAGE;
     const uint32_t kc_s = wpipe_s + stage * C::STAGE, vc_s = kc_s + C::CODE_TILE;
+    const unsigned bad = mask_s[warp * C::STAGES + stage];  // tokens not to attend to
 
     // ---- header pass: lane = token; [token][group] fp16 -> [group][token] ----
     {
@@ -423,12 +424,11 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
         const int sh = (g & 1) * 16;
         const unsigned short uk = (unsigned short)(r[0][g / 2] >> sh);
         const unsigned short uz = (unsigned short)(r[1][g / 2] >> sh);
-        ksx[g * kTT + lane] = __half2float(__ushort_as_half(uk)) * p.scale_log2;
-        kzx[g * kTT + lane] = __half2float(__ushort_as_half(uz));
-        reinterpret_cast<unsigned short*>(vsx)[g * kTT + lane] = (unsigned short)(r[2][g / 2] >> sh);
-        reinterpret_cast<unsigned short*>(vzx)[g * kTT + lane] = (unsigned short)(r[3][g / 2] >> sh);
+        ksz[g * C::KROW + lane] = make_float2(__half2float(__ushort_as_half(uk)) * p.scale_log2,
+                                              __half2float(__ushort_as_half(uz)));
+        reinterpret_cast<unsigned short*>(vsx)[g * C::VROW + lane] = (unsigned short)(r[2][g / 2] >> sh);
+        reinterpret_cast<unsigned short*>(vzx)[g * C::VROW + lane] = (unsigned short)(r[3][g / 2] >> sh);
       }
-      const unsigned bad = mask_s[warp * C::STAGES + stage];
       madd[lane] = ((bad >> lane) & 1u) ? -INFINITY : 0.f;
     }
     __syncwarp();
@@ -478,24 +478,27 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
       for (int u = 0; u < 2; ++u) {
         const int nt = 2 * np + u;
         const int ta = 8 * nt + 2 * j;
-        const float2 s_lo = *reinterpret_cast<const float2*>(ksx + g_lo_c * kTT + ta);
-        const float2 z_lo = *reinterpret_cast<const float2*>(kzx + g_lo_c * kTT + ta);
-        const float2 mk = *reinterpret_cast<const float2*>(mrow + ta);
-        float va = s_lo.x * fmaf(-z_lo.x, qs_lo, acc[u][0]);
-        float vb = s_lo.y * fmaf(-z_lo.y, qs_lo, acc[u][1]);
+        // (s*scale, z) of tokens ta and ta+1 in one 16-byte load
+        const float4 szl = *reinterpret_cast<const float4*>(ksz + g_lo_c * C::KROW + ta);
+        float va = szl.x * fmaf(-szl.y, qs_lo, acc[u][0]);
+        float vb = szl.z * fmaf(-szl.w, qs_lo, acc[u][1]);
         if constexpr (C::HI) {
-          const float2 s_hi = *reinterpret_cast<const float2*>(ksx + g_hi_c * kTT + ta);
-          const float2 z_hi = *reinterpret_cast<const float2*>(kzx + g_hi_c * kTT + ta);
-          va = fmaf(s_hi.x, fmaf(-z_hi.x, qs_hi, acc[u][2]), va);
-          vb = fmaf(s_hi.y, fmaf(-z_hi.y, qs_hi, acc[u][3]), vb);
+          const float4 szh = *reinterpret_cast<const float4*>(ksz + g_hi_c * C::KROW + ta);
+          va = fmaf(szh.x, fmaf(-szh.y, qs_hi, acc[u][2]), va);
+          vb = fmaf(szh.z, fmaf(-szh.w, qs_hi, acc[u][3]), vb);
         }
 #pragma unroll
         for (int s = 0; (1 << s) < C::NGL; ++s) {
           va += __shfl_xor_sync(0xffffffffu, va, 4 * GP << s);
           vb += __shfl_xor_sync(0xffffffffu, vb, 4 * GP << s);
         }
-        sc[nt][0] = va + mk.x;
-        sc[nt][1] = vb + mk.y;
+        if (bad) {  // warp-uniform: only partial tiles and unmapped pages pay for the mask
+          const float2 mk = *reinterpret_cast<const float2*>(madd + ta);
+          va += mk.x;
+          vb += mk.y;
+        }
+        sc[nt][0] = va + hmask;
+        sc[nt][1] = vb + hmask;
       }
     }
 
@@ -545,8 +548,8 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
 #pragma unroll
       for (int t = 0; t < C::NTV; ++t) {
         const int g = min(gcol[t], NG - 1);
-        const uint32_t slo = *reinterpret_cast<const uint32_t*>(vsx + g * kTT + tk);
-        const uint32_t shi = *reinterpret_cast<const uint32_t*>(vsx + g * kTT + tk + 8);
+        const uint32_t slo = *reinterpret_cast<const uint32_t*>(vsx + g * C::VROW + tk);
+        const uint32_t shi = *reinterpret_cast<const uint32_t*>(vsx + g * C::VROW + tk + 8);
         const bool live = gcol[t] < NG;
         bt[t][0] = live ? h2_as_u32(__hmul2(u32_as_h2(plo), u32_as_h2(slo))) : 0u;
         bt[t][1] = live ? h2_as_u32(__hmul2(u32_as_h2(phi), u32_as_h2(shi))) : 0u;
@@ -580,8 +583,8 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
       // zero-points: A rows = groups r, A[r][token] = z_r(token); the entries
       // with r equal to the column's group are the ones used
       const int gz = min(rho, NG - 1);
-      const uint32_t zlo = rho < NG ? *reinterpret_cast<const uint32_t*>(vzx + gz * kTT + tk) : 0u;
-      const uint32_t zhi = rho < NG ? *reinterpret_cast<const uint32_t*>(vzx + gz * kTT + tk + 8) : 0u;
+      const uint32_t zlo = rho < NG ? *reinterpret_cast<const uint32_t*>(vzx + gz * C::VROW + tk) : 0u;
+      const uint32_t zhi = rho < NG ? *reinterpret_cast<const uint32_t*>(vzx + gz * C::VROW + tk + 8) : 0u;
 #pragma unroll
       for (int t = 0; t < C::NTV; ++t) mma16816(cz[t], zlo, 0u, zhi, 0u, bt[t][0], bt[t][1]);
     }
