@@ -331,21 +331,24 @@ def run_gpu_arm(args):
         ms_total = max_over_ranks(e0.elapsed_time(e1))
         clk = clocks.stop() if fmt == bits else None
 
-        # per-call duration of kvq_decode_attn, events on the launching stream
-        evs = []
-        with torch.cuda.stream(stream):
-            for rep in range(3):
-                for l in range(layers):
-                    a = torch.cuda.Event(enable_timing=True)
-                    b = torch.cuda.Event(enable_timing=True)
-                    K.kvq_append(caches[l], kns[l], vns[l], lens_before, status, stream=stream)
-                    a.record(stream)
-                    K.kvq_decode_attn(caches[l], qs[l], lens, rows, outs[l], ws, status,
-                                      stream=stream)
-                    b.record(stream)
-                    evs.append((a, b))
+        # per-call duration of kvq_decode_attn (decode kernel + merge): a graph of
+        # every layer's decode call back to back, timed with events on its stream
+        dgraph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(dgraph, stream=stream):
+            for l in range(layers):
+                K.kvq_decode_attn(caches[l], qs[l], lens, rows, outs[l], ws, status, stream=stream)
         torch.cuda.synchronize()
-        call_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+        reps = max(3, args.steps // 2)
+        d0 = torch.cuda.Event(enable_timing=True)
+        d1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            dgraph.replay()
+            d0.record(stream)
+            for _ in range(reps):
+                dgraph.replay()
+            d1.record(stream)
+        torch.cuda.synchronize()
+        call_ms = d0.elapsed_time(d1) / (reps * layers)
         if int(status.item()) != 0:
             raise RuntimeError(f"device status {int(status.item()):#x}")
 
@@ -389,7 +392,7 @@ def run_gpu_arm(args):
             bytes=decode_bytes(w, fmt, rows), clocks=clk, host_slices=host_slices,
             out0=outs[0][:1].float().cpu().numpy(),
             launches=args.steps * layers * (2 + (1 if splits > 1 else 0)))
-        del caches, graph
+        del caches, graph, dgraph
         torch.cuda.empty_cache()
 
     if rank != 0:

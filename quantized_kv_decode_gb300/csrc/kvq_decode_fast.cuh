@@ -56,11 +56,14 @@ struct Cfg {
   static constexpr int KROW = kTT + 8;            // float2 entries per K row
   static constexpr int VROW = kTT + 8;            // half entries per V row
   static constexpr int XHDR = NG * KROW * 8 + 2 * NG * VROW * 2 + kTT * 4;
-  // three stages when a CTA then still fits three times on an SM
-  static constexpr int STAGES = (kWarps * (3 * STAGE + XHDR) <= 72 * 1024) ? 3 : 2;
-  static constexpr int WARP_BYTES = STAGES * STAGE + XHDR;
-  // CTAs per SM the shared memory allows; the register budget follows it
-  static constexpr int MIN_CTAS = (kWarps * WARP_BYTES <= 72 * 1024) ? 3 : 2;
+  // Two CTAs per SM; as many stages (2..5) as then fit.  The header scratch
+  // is double-buffered because tile i+1's scores are formed while tile i's
+  // values are still being read.
+  static constexpr int BUDGET = 110 * 1024 / kWarps;  // shared bytes per warp
+  static constexpr int STAGES_FIT = (BUDGET - 2 * XHDR) / STAGE;
+  static constexpr int STAGES = STAGES_FIT > 5 ? 5 : (STAGES_FIT < 2 ? 2 : STAGES_FIT);
+  static constexpr int WARP_BYTES = STAGES * STAGE + 2 * XHDR;
+  static constexpr int MIN_CTAS = 2;
   static constexpr int NTV = (NG * GP + 7) / 8;           // V-mma n-tiles: columns (group, head)
   static constexpr int NGL = (NG < 8 / GP) ? NG : 8 / GP;  // groups in accumulator rows 0..7
   static constexpr bool HI = NG * GP > 8;                   // rows 8..15 in use
@@ -246,10 +249,13 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
   uint8_t* pipe = smem + ((GP * D * 2 + 127) / 128) * 128;
   uint32_t* mask_s = reinterpret_cast<uint32_t*>(pipe + kWarps * C::WARP_BYTES);
   uint8_t* wpipe = pipe + warp * C::WARP_BYTES;
-  float2* ksz = reinterpret_cast<float2*>(wpipe + C::STAGES * C::STAGE);  // [NG][KROW]
-  __half* vsx = reinterpret_cast<__half*>(ksz + NG * C::KROW);            // [NG][VROW]
-  __half* vzx = vsx + NG * C::VROW;                                       // [NG][VROW]
-  float* madd = reinterpret_cast<float*>(vzx + NG * C::VROW);             // [kTT]
+  // header scratch buffer `buf` (0/1): K (s*scale, z) [NG][KROW], V scale
+  // [NG][VROW], V zero [NG][VROW], token mask [kTT]
+  uint8_t* xbase = wpipe + C::STAGES * C::STAGE;
+  auto ksz_of = [&](int buf) { return reinterpret_cast<float2*>(xbase + buf * C::XHDR); };
+  auto vsx_of = [&](int buf) { return reinterpret_cast<__half*>(ksz_of(buf) + NG * C::KROW); };
+  auto vzx_of = [&](int buf) { return vsx_of(buf) + NG * C::VROW; };
+  auto madd_of = [&](int buf) { return reinterpret_cast<float*>(vzx_of(buf) + NG * C::VROW); };
 
   const __half* qg = p.q + ((long long)b * p.Hq + (long long)kvh * G) * D;
   for (int i = threadIdx.x; i < GP * D; i += kWarps * 32)
@@ -391,50 +397,45 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
     return unmapped;
   };
 
+  // ---- one tile's steps ----
+  // header pass: lane = token; [token][group] fp16 -> [group][token] scratch
+  auto header = [&](int stg, int buf, unsigned bad) {
+    const uint8_t* hsrc = wpipe + stg * C::STAGE + 2 * C::CODE_TILE + lane * C::HDRB;
+    uint32_t r[4][NG / 2];  // K scale, K zero, V scale, V zero: two halves per word
 #pragma unroll
-  for (int s = 0; s < C::STAGES - 1; ++s) bt_bad |= issue(s);
-
-  int stage = 0;
-  for (int it = 0; it < nmine; ++it) {
-    cp_async_wait<C::STAGES - 2>();
-    __syncwarp();
-    const uint8_t* st = wpipe + stage * C::STAGE;
-    const uint32_t kc_s = wpipe_s + stage * C::STAGE, vc_s = kc_s + C::CODE_TILE;
-    const unsigned bad = mask_s[warp * C::STAGES + stage];  // tokens not to attend to
-
-    // ---- header pass: lane = token; [token][group] fp16 -> [group][token] ----
-    {
-      const uint8_t* hsrc = st + 2 * C::CODE_TILE + lane * C::HDRB;
-      uint32_t r[4][NG / 2];  // K scale, K zero, V scale, V zero: two halves per word
-#pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        const uint8_t* src = hsrc + a * C::HDR_TILE;
-        if constexpr (NG == 2) {
-          r[a][0] = *reinterpret_cast<const uint32_t*>(src);
-        } else if constexpr (NG == 4) {
-          const uint2 v = *reinterpret_cast<const uint2*>(src);
-          r[a][0] = v.x; r[a][1] = v.y;
-        } else {
-          const uint4 v = *reinterpret_cast<const uint4*>(src);
-          r[a][0] = v.x; r[a][1] = v.y; r[a][2] = v.z; r[a][3] = v.w;
-        }
+    for (int a = 0; a < 4; ++a) {
+      const uint8_t* src = hsrc + a * C::HDR_TILE;
+      if constexpr (NG == 2) {
+        r[a][0] = *reinterpret_cast<const uint32_t*>(src);
+      } else if constexpr (NG == 4) {
+        const uint2 v = *reinterpret_cast<const uint2*>(src);
+        r[a][0] = v.x; r[a][1] = v.y;
+      } else {
+        const uint4 v = *reinterpret_cast<const uint4*>(src);
+        r[a][0] = v.x; r[a][1] = v.y; r[a][2] = v.z; r[a][3] = v.w;
       }
-#pragma unroll
-      for (int g = 0; g < NG; ++g) {
-        const int sh = (g & 1) * 16;
-        const unsigned short uk = (unsigned short)(r[0][g / 2] >> sh);
-        const unsigned short uz = (unsigned short)(r[1][g / 2] >> sh);
-        ksz[g * C::KROW + lane] = make_float2(__half2float(__ushort_as_half(uk)) * p.scale_log2,
-                                              __half2float(__ushort_as_half(uz)));
-        reinterpret_cast<unsigned short*>(vsx)[g * C::VROW + lane] = (unsigned short)(r[2][g / 2] >> sh);
-        reinterpret_cast<unsigned short*>(vzx)[g * C::VROW + lane] = (unsigned short)(r[3][g / 2] >> sh);
-      }
-      madd[lane] = ((bad >> lane) & 1u) ? -INFINITY : 0.f;
     }
-    __syncwarp();
+    float2* ksz = ksz_of(buf);
+    unsigned short* vs = reinterpret_cast<unsigned short*>(vsx_of(buf));
+    unsigned short* vz = reinterpret_cast<unsigned short*>(vzx_of(buf));
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      const int sh = (g & 1) * 16;
+      const unsigned short uk = (unsigned short)(r[0][g / 2] >> sh);
+      const unsigned short uz = (unsigned short)(r[1][g / 2] >> sh);
+      ksz[g * C::KROW + lane] = make_float2(__half2float(__ushort_as_half(uk)) * p.scale_log2,
+                                            __half2float(__ushort_as_half(uz)));
+      vs[g * C::VROW + lane] = (unsigned short)(r[2][g / 2] >> sh);
+      vz[g * C::VROW + lane] = (unsigned short)(r[3][g / 2] >> sh);
+    }
+    madd_of(buf)[lane] = ((bad >> lane) & 1u) ? -INFINITY : 0.f;
+  };
 
-    // ---------------- scores: 4 n-tiles of 8 tokens, two at a time ----------------
-    float sc[4][2];
+  // scores of the tile's 4 n-tiles of 8 tokens (log2 units, masked)
+  auto scores = [&](int stg, int buf, unsigned bad, float (&sc)[4][2]) {
+    const uint32_t kc_s = wpipe_s + stg * C::STAGE;
+    const float2* ksz = ksz_of(buf);
+    const float* madd = madd_of(buf);
 #pragma unroll
     for (int np = 0; np < 2; ++np) {
       uint32_t w[2][C::CHUNKS];
@@ -473,7 +474,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
           }
         }
       }
-      // group epilogue: row (g, h) holds sum_{d in g} q_h[d] code[d]; log2 units
+      // group epilogue: row (g, h) holds sum_{d in g} q_h[d] code[d]
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         const int nt = 2 * np + u;
@@ -488,9 +489,9 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
           vb = fmaf(szh.z, fmaf(-szh.w, qs_hi, acc[u][3]), vb);
         }
 #pragma unroll
-        for (int s = 0; (1 << s) < C::NGL; ++s) {
-          va += __shfl_xor_sync(0xffffffffu, va, 4 * GP << s);
-          vb += __shfl_xor_sync(0xffffffffu, vb, 4 * GP << s);
+        for (int s2 = 0; (1 << s2) < C::NGL; ++s2) {
+          va += __shfl_xor_sync(0xffffffffu, va, 4 * GP << s2);
+          vb += __shfl_xor_sync(0xffffffffu, vb, 4 * GP << s2);
         }
         if (bad) {  // warp-uniform: only partial tiles and unmapped pages pay for the mask
           const float2 mk = *reinterpret_cast<const float2*>(madd + ta);
@@ -501,8 +502,11 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
         sc[nt][1] = vb + hmask;
       }
     }
+  };
 
-    // ---------------- online softmax over the tile ----------------
+  // online softmax over the tile; pp = fp16 probabilities of this lane's tokens
+  // (tk, tk+1 | tk+8, tk+9 for k-steps 0 and 1)
+  auto softmax = [&](const float (&sc)[4][2], uint32_t (&pp)[4]) {
     float mt = sc[0][0];
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) mt = fmaxf(mt, fmaxf(sc[nt][0], sc[nt][1]));
@@ -536,13 +540,19 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
       pr[nt][1] = ex2(sc[nt][1] - m_use);
       l_run += pr[nt][0] + pr[nt][1];
     }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) pp[k] = pack_h2(pr[k][0], pr[k][1]);
+  };
 
-    // ---------------- weighted V: 2 k-steps of 16 tokens ----------------
+  // weighted V of the tile: 2 k-steps of 16 tokens
+  auto weighted_v = [&](int stg, int buf, const uint32_t (&pp)[4]) {
+    const uint32_t vc_s = wpipe_s + stg * C::STAGE + C::CODE_TILE;
+    const __half* vsx = vsx_of(buf);
+    const __half* vzx = vzx_of(buf);
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
       const int tk = 16 * ks + 2 * j;  // this lane's tokens: tk, tk+1, tk+8, tk+9
-      const uint32_t plo = pack_h2(pr[2 * ks][0], pr[2 * ks][1]);
-      const uint32_t phi = pack_h2(pr[2 * ks + 1][0], pr[2 * ks + 1][1]);
+      const uint32_t plo = pp[2 * ks], phi = pp[2 * ks + 1];
       // B[token][(g, h)] = p_h(token) * s_g(token); this lane's column per n-tile
       uint32_t bt[C::NTV][2];
 #pragma unroll
@@ -588,9 +598,42 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
 #pragma unroll
       for (int t = 0; t < C::NTV; ++t) mma16816(cz[t], zlo, 0u, zhi, 0u, bt[t][0], bt[t][1]);
     }
+  };
+
+  // ---- software-pipelined loop: tile i+1's scores overlap tile i's values ----
+  // Tile k lives in stage k % STAGES; one commit group per tile.
+#pragma unroll
+  for (int s2 = 0; s2 < C::STAGES; ++s2) bt_bad |= issue(s2);
+
+  uint32_t pp[4] = {0u, 0u, 0u, 0u};
+  if (nmine > 0) {
+    cp_async_wait<C::STAGES - 1>();  // tile 0
     __syncwarp();
-    bt_bad |= issue(it + C::STAGES - 1);
-    stage = (stage + 1 == C::STAGES) ? 0 : stage + 1;
+    const unsigned bad0 = mask_s[warp * C::STAGES];
+    header(0, 0, bad0);
+    __syncwarp();
+    float sc[4][2];
+    scores(0, 0, bad0, sc);
+    softmax(sc, pp);
+  }
+  int stage = 0;
+  for (int it = 0; it < nmine; ++it) {
+    const int nstage = (stage + 1 == C::STAGES) ? 0 : stage + 1;
+    const bool more = it + 1 < nmine;
+    float scn[4][2];
+    if (more) {
+      cp_async_wait<C::STAGES - 2>();  // tile it+1
+      __syncwarp();
+      const unsigned badn = mask_s[warp * C::STAGES + nstage];
+      header(nstage, (it + 1) & 1, badn);
+      __syncwarp();
+      scores(nstage, (it + 1) & 1, badn, scn);
+    }
+    weighted_v(stage, it & 1, pp);
+    if (more) softmax(scn, pp);
+    __syncwarp();
+    bt_bad |= issue(it + C::STAGES);  // into the stage tile it has just left
+    stage = nstage;
   }
   cp_async_wait<0>();
 
