@@ -115,23 +115,20 @@ __device__ __forceinline__ void ldsm_x4(uint32_t a, uint32_t& r0, uint32_t& r1, 
                                         uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(a)
-               : "memory");
+               : "r"(a));
 }
 
 __device__ __forceinline__ void ldsm_x2(uint32_t a, uint32_t& r0, uint32_t& r1) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];\n"
                : "=r"(r0), "=r"(r1)
-               : "r"(a)
-               : "memory");
+               : "r"(a));
 }
 
 __device__ __forceinline__ void ldsm_x4_t(uint32_t a, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                           uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-               : "r"(a)
-               : "memory");
+               : "r"(a));
 }
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -617,24 +614,23 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
     softmax(sc, pp);
   }
   int stage = 0;
-  for (int it = 0; it < nmine; ++it) {
+  // steady state, branch-free so that the two tiles' work can interleave
+  for (int it = 0; it + 1 < nmine; ++it) {
     const int nstage = (stage + 1 == C::STAGES) ? 0 : stage + 1;
-    const bool more = it + 1 < nmine;
     float scn[4][2];
-    if (more) {
-      cp_async_wait<C::STAGES - 2>();  // tile it+1
-      __syncwarp();
-      const unsigned badn = mask_s[warp * C::STAGES + nstage];
-      header(nstage, (it + 1) & 1, badn);
-      __syncwarp();
-      scores(nstage, (it + 1) & 1, badn, scn);
-    }
+    cp_async_wait<C::STAGES - 2>();  // tile it+1
+    __syncwarp();
+    const unsigned badn = mask_s[warp * C::STAGES + nstage];
+    header(nstage, (it + 1) & 1, badn);
+    __syncwarp();
+    scores(nstage, (it + 1) & 1, badn, scn);
     weighted_v(stage, it & 1, pp);
-    if (more) softmax(scn, pp);
+    softmax(scn, pp);
     __syncwarp();
     bt_bad |= issue(it + C::STAGES);  // into the stage tile it has just left
     stage = nstage;
   }
+  if (nmine > 0) weighted_v(stage, (nmine - 1) & 1, pp);  // the last tile's values
   cp_async_wait<0>();
 
   // ---------------- finish this warp: l, zero-point correction ----------------
