@@ -128,56 +128,43 @@ int32_t choose_splits(int64_t units, int64_t max_len, int32_t requested, int cta
 struct Plan {
   bool fast = false;
   int gp = 1;
-  int32_t splits = 0;  // generic kernel: context splits; tensor-core kernel: CTAs
-  size_t workspace = 0;
+  int32_t splits = 0;
 };
 
 kvq_status make_plan(const kvq_cache_desc* desc, const CacheGeom& geom, int32_t batch,
                      int32_t num_q_heads, int32_t max_seq_len, int32_t requested, Plan* plan) {
   const int G = num_q_heads / desc->num_kv_heads;
-  const int64_t units = (int64_t)batch * desc->num_kv_heads;
+  int occ = 0;
   plan->fast = false;
   if (desc->bits != 16 && G <= 8) {
     int gp = 1;
     while (gp < G) gp <<= 1;
     plan->gp = gp;
+    if (requested > 0) {
+      plan->splits = choose_splits((int64_t)batch * desc->num_kv_heads, max_seq_len, requested, 0);
+      return KVQ_OK;
+    }
     DecodeParams probe{};
     probe.geom = geom;
     probe.G = G;
     bool handled = false;
-    int occ = requested > 0 ? -1 : 0;  // explicit counts need no device
     cudaError_t e = desc->bits == 4 ? launch_decode_fast_int4(probe, gp, nullptr, &handled, &occ)
                                     : launch_decode_fast_int8(probe, gp, nullptr, &handled, &occ);
-    if (handled) {
-      if (e != cudaSuccess) return KVQ_ERR_CUDA;
-      plan->fast = true;
-      // CTAs the tile stream is balanced over: one wave, no more warps than tiles
-      int64_t ctas;
-      if (requested > 0) {
-        ctas = requested;
-      } else {
-        const int sms = sm_count();
-        if (sms <= 0 || occ <= 0) return KVQ_ERR_CUDA;
-        const int64_t tiles = units * ceil_div(std::max<int64_t>(max_seq_len, 1), kFastTile);
-        ctas = std::min<int64_t>((int64_t)sms * occ, ceil_div(tiles, kFastWarps));
-      }
-      ctas = std::max<int64_t>(1, std::min<int64_t>(ctas, INT32_MAX / kFastWarps));
-      plan->splits = (int32_t)ctas;
-      plan->workspace = fast_workspace_bytes(ctas, G, desc->head_dim);
-      return KVQ_OK;
-    }
+    if (handled && e != cudaSuccess) return KVQ_ERR_CUDA;
+    plan->fast = handled;
   }
   if (requested > 0) {
-    plan->splits = choose_splits(units, max_seq_len, requested, 0);
-  } else {
+    plan->splits = choose_splits((int64_t)batch * desc->num_kv_heads, max_seq_len, requested, 0);
+    return KVQ_OK;
+  }
+  if (!plan->fast) {
     DecodeParams probe{};
     probe.geom = geom;
     probe.G = G;
-    plan->splits = choose_splits(units, max_seq_len, 0, generic_ctas_per_sm(probe));
-    if (plan->splits <= 0) return KVQ_ERR_CUDA;
+    occ = generic_ctas_per_sm(probe);
   }
-  plan->workspace = workspace_bytes(batch, num_q_heads, desc->head_dim, plan->splits);
-  return KVQ_OK;
+  plan->splits = choose_splits((int64_t)batch * desc->num_kv_heads, max_seq_len, 0, occ);
+  return plan->splits > 0 ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
 kvq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
@@ -189,21 +176,6 @@ size_t workspace_bytes(int64_t batch, int64_t Hq, int64_t D, int64_t splits) {
   const size_t o = (size_t)(batch * Hq * splits * D) * sizeof(float);
   const size_t ml = (size_t)(batch * Hq * splits * 2) * sizeof(float);
   return ((o + 255) & ~(size_t)255) + ml;
-}
-
-size_t fast_workspace_bytes(int64_t ctas, int64_t G, int64_t D) {
-  const int64_t slots = 2 * ctas * kFastWarps;
-  const size_t o = (size_t)(slots * G * D) * sizeof(float);
-  const size_t ml = (size_t)(slots * G * 2) * sizeof(float);
-  return ((o + 255) & ~(size_t)255) + ml;
-}
-
-void fast_workspace_carve(void* ws, int64_t ctas, int64_t G, int64_t D, float** ws_o,
-                          float** ws_ml) {
-  const int64_t slots = 2 * ctas * kFastWarps;
-  const size_t o = (size_t)(slots * G * D) * sizeof(float);
-  *ws_o = reinterpret_cast<float*>(ws);
-  *ws_ml = reinterpret_cast<float*>(reinterpret_cast<char*>(ws) + ((o + 255) & ~(size_t)255));
 }
 
 void workspace_carve(void* ws, int64_t batch, int64_t Hq, int64_t D, int64_t splits,
@@ -284,13 +256,9 @@ int32_t kvq_decode_num_splits(const kvq_cache_desc* desc, int32_t batch, int32_t
 
 size_t kvq_decode_workspace_size(const kvq_cache_desc* desc, int32_t batch, int32_t num_q_heads,
                                  int32_t max_seq_len, int32_t num_splits) {
-  CacheGeom g;
-  if (check_desc(desc, &g) != KVQ_OK || batch < 0 || num_q_heads <= 0 || max_seq_len < 0 ||
-      num_splits < 0 || num_q_heads % desc->num_kv_heads)
-    return 0;
-  Plan plan;
-  if (make_plan(desc, g, batch, num_q_heads, max_seq_len, num_splits, &plan) != KVQ_OK) return 0;
-  return plan.workspace;
+  const int32_t s = kvq_decode_num_splits(desc, batch, num_q_heads, max_seq_len, num_splits);
+  if (s <= 1) return 0;
+  return workspace_bytes(batch, num_q_heads, desc->head_dim, s);
 }
 
 kvq_status kvq_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache, int32_t batch,
@@ -316,7 +284,7 @@ kvq_status kvq_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache, i
   if ((st = make_plan(desc, p.geom, batch, num_q_heads, max_seq_len, num_splits, &plan)) != KVQ_OK)
     return st;
   const int32_t splits = plan.splits;
-  const size_t need = plan.workspace;
+  const size_t need = workspace_bytes(batch, num_q_heads, desc->head_dim, splits);
   if (need > 0 && (!workspace || workspace_size < need || !aligned(workspace)))
     return KVQ_ERR_WORKSPACE;
 
@@ -332,19 +300,13 @@ kvq_status kvq_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache, i
   p.out = reinterpret_cast<__half*>(out);
   p.ws_o = nullptr;
   p.ws_ml = nullptr;
-  p.ctas = 0;
-  if (plan.fast) {
-    p.ctas = splits;
-    fast_workspace_carve(workspace, splits, G, desc->head_dim, &p.ws_o, &p.ws_ml);
-  } else if (splits > 1) {
-    workspace_carve(workspace, batch, num_q_heads, desc->head_dim, splits, &p.ws_o, &p.ws_ml);
-  }
+  if (splits > 1) workspace_carve(workspace, batch, num_q_heads, desc->head_dim, splits, &p.ws_o, &p.ws_ml);
   p.status = dev_status;
   p.batch = batch;
   p.Hq = num_q_heads;
   p.G = G;
-  p.splits = plan.fast ? 1 : splits;
-  p.chunk = split_chunk(max_seq_len, p.splits);
+  p.splits = splits;
+  p.chunk = split_chunk(max_seq_len, splits);
   const int64_t cap = desc->layout == KVQ_DENSE ? (int64_t)desc->capacity
                                                  : (int64_t)desc->capacity * desc->max_blocks_per_seq;
   p.len_limit = (int32_t)std::min<int64_t>(cap, max_seq_len);
@@ -353,15 +315,13 @@ kvq_status kvq_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache, i
 
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
-  if (plan.fast) {
-    bool handled = false;
+  bool handled = false;
+  if (desc->bits != 16 && G <= 8) {
     if (desc->bits == 4) e = launch_decode_fast_int4(p, plan.gp, s, &handled, nullptr);
     else e = launch_decode_fast_int8(p, plan.gp, s, &handled, nullptr);
-    if (!handled) return KVQ_ERR_UNSUPPORTED;
-  } else {
-    e = launch_decode_generic(p, s);
-    if (e == cudaSuccess && splits > 1) e = launch_merge(p, s);
   }
+  if (!handled) e = launch_decode_generic(p, s);
+  if (e == cudaSuccess && splits > 1) e = launch_merge(p, s);
   return from_cuda(e);
 }
 

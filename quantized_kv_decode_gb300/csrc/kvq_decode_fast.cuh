@@ -33,8 +33,8 @@
 namespace kvq {
 namespace fast {
 
-constexpr int kWarps = kFastWarps;
-constexpr int kTT = kFastTile;  // tokens per warp tile
+constexpr int kWarps = 4;
+constexpr int kTT = 32;  // tokens per warp tile
 
 template <int BITS, int D, int NG, int GP>
 struct Cfg {
@@ -60,11 +60,9 @@ struct Cfg {
   // is double-buffered because tile i+1's scores are formed while tile i's
   // values are still being read.
   static constexpr int BUDGET = 110 * 1024 / kWarps;  // shared bytes per warp
-  static constexpr int STAGES_FIT = (BUDGET - 2 * XHDR - ((GP * D * 2 + 127) / 128) * 128 - 128) / STAGE;
+  static constexpr int STAGES_FIT = (BUDGET - 2 * XHDR) / STAGE;
   static constexpr int STAGES = STAGES_FIT > 5 ? 5 : (STAGES_FIT < 2 ? 2 : STAGES_FIT);
-  static constexpr int QBYTES = ((GP * D * 2 + 127) / 128) * 128;  // staged q of a unit
-  // per warp: [q][stages][2 header scratch buffers][stage masks]
-  static constexpr int WARP_BYTES = QBYTES + STAGES * STAGE + 2 * XHDR + 128;
+  static constexpr int WARP_BYTES = STAGES * STAGE + 2 * XHDR;
   static constexpr int MIN_CTAS = 2;
   static constexpr int NTV = (NG * GP + 7) / 8;           // V-mma n-tiles: columns (group, head)
   static constexpr int NGL = (NG < 8 / GP) ? NG : 8 / GP;  // groups in accumulator rows 0..7
@@ -223,180 +221,80 @@ __device__ __forceinline__ uint32_t pack_halves(__half lo, __half hi) {
 // bounded by 2^kSlack.
 constexpr float kSlack = 4.f;
 
-// Position in the stream of 32-token tiles: all tiles of (sequence 0, KV head
-// 0), then (0, 1), ..., (1, 0), ...; sequences with no tiles are skipped.
-struct TileCursor {
-  int b;          // sequence
-  int kvh;        // KV head
-  int tin;        // tile within the unit
-  int T;          // tiles of sequence b
-  long long ub;   // index of the unit's first tile in the stream
-  __device__ __forceinline__ void next_unit(const DecodeParams& p) {
-    ub += T;
-    tin = 0;
-    if (++kvh == p.geom.Hkv) {
-      kvh = 0;
-      do {
-        ++b;
-        T = 0;
-        if (b < p.batch) {
-          const int L = __ldg(p.seq_lens + b);
-          T = (L < 0 || L > p.len_limit) ? 0 : (L + kTT - 1) / kTT;
-        }
-      } while (b < p.batch && T == 0);
-    }
-  }
-  __device__ __forceinline__ void advance(const DecodeParams& p) {
-    if (++tin == T) {
-      --tin;
-      next_unit(p);
-    }
-  }
-};
-
-// Warp w of W owns stream tiles [w * total / W, (w + 1) * total / W).
-__device__ __forceinline__ long long range_start(long long w, long long W, long long total) {
-  return w * total / W;
-}
-
 template <int BITS, int D, int NG, int GP>
 __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
     decode_fast_kernel(const DecodeParams p) {
   using C = Cfg<BITS, D, NG, GP>;
   extern __shared__ __align__(128) uint8_t smem[];
   const CacheGeom& geo = p.geom;
-  const int G = p.G, Hkv = geo.Hkv;
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int G = p.G;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int rho = lane >> 2, j = lane & 3;
-  const long long W = (long long)gridDim.x * kWarps;
-  const long long wid = (long long)blockIdx.x * kWarps + warp;
 
-  // ---- this warp's share of the tile stream ----
-  // tiles of sequence b: ceil(len / 32), none for an invalid length (the merge
-  // kernel flags those and writes their zero rows)
-  long long total = 0;
-  for (int b0 = 0; b0 < p.batch; b0 += 32) {
-    int T = 0;
-    if (b0 + lane < p.batch) {
-      const int L = __ldg(p.seq_lens + b0 + lane);
-      T = (L < 0 || L > p.len_limit) ? 0 : (L + kTT - 1) / kTT;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) T += __shfl_xor_sync(0xffffffffu, T, o);
-    total += (long long)T * Hkv;
+  int L = p.seq_lens[b];
+  if (L < 0 || L > p.len_limit) {
+    if (threadIdx.x == 0 && split == 0 && kvh == 0 && p.status) atomicOr(p.status, KVQ_FLAG_SEQ_LEN);
+    L = 0;
   }
-  const long long X0 = range_start(wid, W, total), X1 = range_start(wid + 1, W, total);
-  const int nmine = (int)(X1 - X0);
-  if (nmine <= 0) return;
+  const int t0 = split * p.chunk;
+  const int t1 = min(L, t0 + p.chunk);
+  if (p.splits > 1 && t0 >= L) return;  // the merge reads splits < ceil(L / chunk) only
 
-  // cursor at tile X0: the sequence whose prefix range holds it
-  TileCursor cur;
-  {
-    long long pre = 0;
-    int b_hit = -1;
-    for (int b0 = 0; b0 < p.batch && b_hit < 0; b0 += 32) {
-      int T = 0;
-      if (b0 + lane < p.batch) {
-        const int L = __ldg(p.seq_lens + b0 + lane);
-        T = (L < 0 || L > p.len_limit) ? 0 : (L + kTT - 1) / kTT;
-      }
-      long long incl = (long long)T * Hkv;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const long long v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      const unsigned hit = __ballot_sync(0xffffffffu, pre + incl > X0);
-      if (hit) {
-        const int l = __ffs(hit) - 1;
-        const long long excl = __shfl_sync(0xffffffffu, incl, l) - (long long)__shfl_sync(0xffffffffu, T, l) * Hkv;
-        b_hit = b0 + l;
-        cur.b = b_hit;
-        cur.T = __shfl_sync(0xffffffffu, T, l);
-        const long long off = X0 - (pre + excl);
-        cur.kvh = (int)(off / cur.T);
-        cur.tin = (int)(off % cur.T);
-        cur.ub = pre + excl + (long long)cur.kvh * cur.T;
-      } else {
-        pre += __shfl_sync(0xffffffffu, incl, 31);
-      }
-    }
-  }
-
-  // ---- per-warp shared memory ----
-  uint8_t* wbase = smem + warp * C::WARP_BYTES;
-  __half* q_s = reinterpret_cast<__half*>(wbase);
-  uint8_t* wpipe = wbase + C::QBYTES;
-  uint8_t* xbase = wpipe + C::STAGES * C::STAGE;
-  uint32_t* mask_s = reinterpret_cast<uint32_t*>(xbase + 2 * C::XHDR);
-  const uint32_t wpipe_s = smem_u32(wpipe);
+  // shared memory: [q fp16 GP x D][per warp: stages, header scratch][tile masks]
+  __half* q_s = reinterpret_cast<__half*>(smem);
+  uint8_t* pipe = smem + ((GP * D * 2 + 127) / 128) * 128;
+  uint32_t* mask_s = reinterpret_cast<uint32_t*>(pipe + kWarps * C::WARP_BYTES);
+  uint8_t* wpipe = pipe + warp * C::WARP_BYTES;
   // header scratch buffer `buf` (0/1): K (s*scale, z) [NG][KROW], V scale
   // [NG][VROW], V zero [NG][VROW], token mask [kTT]
+  uint8_t* xbase = wpipe + C::STAGES * C::STAGE;
   auto ksz_of = [&](int buf) { return reinterpret_cast<float2*>(xbase + buf * C::XHDR); };
   auto vsx_of = [&](int buf) { return reinterpret_cast<__half*>(ksz_of(buf) + NG * C::KROW); };
   auto vzx_of = [&](int buf) { return vsx_of(buf) + NG * C::VROW; };
   auto madd_of = [&](int buf) { return reinterpret_cast<float*>(vzx_of(buf) + NG * C::VROW); };
 
-  // ---- lane roles ----
-  // score-mma rows: r <-> (group r / GP, head r % GP); after the group sum
-  // lane rho holds the scores of head rho % GP
+  const __half* qg = p.q + ((long long)b * p.Hq + (long long)kvh * G) * D;
+  for (int i = threadIdx.x; i < GP * D; i += kWarps * 32)
+    q_s[i] = (i < G * D) ? qg[i] : __float2half_rn(0.f);
+  __syncthreads();
+
+  // ---- score-mma A fragments: row r <-> (group r / GP, head r % GP) ----
   const int g_lo = rho / GP, h_row = rho % GP;
   const int g_hi = g_lo + 8 / GP;
   const bool row_ok = h_row < G;
-  const int g_lo_c = min(g_lo, NG - 1), g_hi_c = min(g_hi, NG - 1);
-  const float hmask = (h_row < G) ? 0.f : -INFINITY;
-  // V-mma B columns of this lane, per n-tile t: (group (8t + rho) / GP, head rho % GP)
-  int gcol[C::NTV];
-#pragma unroll
-  for (int t = 0; t < C::NTV; ++t) gcol[t] = (8 * t + rho) / GP;
-
-  // ---- per-unit state ----
   uint32_t qa[C::KB][4];
-  float qs_lo = 0.f, qs_hi = 0.f, off_lo = 0.f, off_hi = 0.f;
-  float o[C::MT][4];
-  float cz[C::NTV][4];  // zero-point terms: rows = groups r, columns = (group, head)
-  float m_ref = -INFINITY, l_run = 0.f;
-
-  // load q of the cursor's unit, build the score-mma A fragments, reset the
-  // accumulators
-  auto begin_unit = [&](const TileCursor& u) {
-    const __half* qg = p.q + ((long long)u.b * p.Hq + (long long)u.kvh * G) * D;
-    for (int i = lane * 8; i < GP * D; i += 256) {
-      uint4 v = make_uint4(0u, 0u, 0u, 0u);
-      if (i < G * D) v = *reinterpret_cast<const uint4*>(qg + i);
-      *reinterpret_cast<uint4*>(q_s + i) = v;
-    }
-    __syncwarp();
 #pragma unroll
-    for (int kb = 0; kb < C::KB; ++kb) {
-      const int grp = (16 * kb) / C::GSZ;
-      int dk[4];  // channel of k-slots 2j, 2j+1, 2j+8, 2j+9
-      if constexpr (BITS == 4) {
-        const int base = 32 * (kb >> 1) + 8 * j + 2 * (kb & 1);
-        dk[0] = base; dk[1] = base + 4; dk[2] = base + 1; dk[3] = base + 5;
-      } else {
-        const int base = 16 * kb + 4 * j;
-        dk[0] = base; dk[1] = base + 1; dk[2] = base + 2; dk[3] = base + 3;
-      }
-      const __half* qh = q_s + h_row * D;
-      const bool lo = row_ok && g_lo == grp;
-      const bool hi = C::HI && row_ok && g_hi == grp;
-      const uint32_t v01 = pack_halves(qh[dk[0]], qh[dk[1]]);
-      uint32_t v23 = pack_halves(qh[dk[2]], qh[dk[3]]);
-      if constexpr (BITS == 4)  // slots 2j+8, 2j+9 meet the odd nibbles, held as 16c
-        v23 = h2_as_u32(__hmul2(u32_as_h2(v23), u32_as_h2(kH1_16)));
-      qa[kb][0] = lo ? v01 : 0u;
-      qa[kb][1] = hi ? v01 : 0u;
-      qa[kb][2] = lo ? v23 : 0u;
-      qa[kb][3] = hi ? v23 : 0u;
+  for (int kb = 0; kb < C::KB; ++kb) {
+    const int grp = (16 * kb) / C::GSZ;
+    int dk[4];  // channel of k-slots 2j, 2j+1, 2j+8, 2j+9
+    if constexpr (BITS == 4) {
+      const int base = 32 * (kb >> 1) + 8 * j + 2 * (kb & 1);
+      dk[0] = base; dk[1] = base + 4; dk[2] = base + 1; dk[3] = base + 5;
+    } else {
+      const int base = 16 * kb + 4 * j;
+      dk[0] = base; dk[1] = base + 1; dk[2] = base + 2; dk[3] = base + 3;
     }
-    __syncwarp();
-    // Per row (g, h): the sum of q_h over group g, and the offset that the
-    // biased codes add, 1024 * (sum of the row's A entries); both by the same
-    // mma against constant codes.
+    const __half* qh = q_s + h_row * D;
+    const bool lo = row_ok && g_lo == grp;
+    const bool hi = C::HI && row_ok && g_hi == grp;
+    const uint32_t v01 = pack_halves(qh[dk[0]], qh[dk[1]]);
+    uint32_t v23 = pack_halves(qh[dk[2]], qh[dk[3]]);
+    if constexpr (BITS == 4)  // slots 2j+8, 2j+9 meet the odd nibbles, held as 16c
+      v23 = h2_as_u32(__hmul2(u32_as_h2(v23), u32_as_h2(kH1_16)));
+    qa[kb][0] = lo ? v01 : 0u;
+    qa[kb][1] = hi ? v01 : 0u;
+    qa[kb][2] = lo ? v23 : 0u;
+    qa[kb][3] = hi ? v23 : 0u;
+  }
+  // Per row (g, h): the sum of q_h over group g, and the offset that the
+  // biased codes add, 1024 * (sum of the row's A entries); both by the same
+  // mma against constant codes.
+  float qs_lo, qs_hi, off_lo, off_hi;
+  {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float bia[4] = {0.f, 0.f, 0.f, 0.f};
-    constexpr uint32_t kOnes = 0x3C003C00u;     // fp16 (1, 1)
+    constexpr uint32_t kOnes = 0x3C003C00u;   // fp16 (1, 1)
     constexpr uint32_t kSixteen = 0x4C004C00u;  // fp16 (16, 16)
 #pragma unroll
     for (int kb = 0; kb < C::KB; ++kb) {
@@ -408,60 +306,30 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
     qs_hi = acc[2];
     off_lo = bia[0];
     off_hi = bia[2];
+  }
+  const int g_lo_c = min(g_lo, NG - 1), g_hi_c = min(g_hi, NG - 1);
+  // After the group sum, lane rho holds the scores of head rho % GP; lanes of
+  // a head beyond G read a row of -inf as their token mask.
+  const int h_lane = rho % GP;
+  const float hmask = (h_lane < G) ? 0.f : -INFINITY;
+  // V-mma B columns of this lane, per n-tile t: (group (8t + rho) / GP, head h_lane)
+  int gcol[C::NTV];
 #pragma unroll
-    for (int m = 0; m < C::MT; ++m) o[m][0] = o[m][1] = o[m][2] = o[m][3] = 0.f;
-#pragma unroll
-    for (int t = 0; t < C::NTV; ++t) cz[t][0] = cz[t][1] = cz[t][2] = cz[t][3] = 0.f;
-    m_ref = -INFINITY;
-    l_run = 0.f;
-  };
+  for (int t = 0; t < C::NTV; ++t) gcol[t] = (8 * t + rho) / GP;
 
-  // finish the cursor's unit: the final rows when the whole unit lies in this
-  // warp's range, else a partial in slot 2w (unit began before the range) or
-  // 2w + 1 (unit continues after it)
-  auto end_unit = [&](const TileCursor& u) {
-    float l = l_run;
-    l += __shfl_xor_sync(0xffffffffu, l, 1);
-    l += __shfl_xor_sync(0xffffffffu, l, 2);
-    const bool whole = u.ub >= X0 && u.ub + u.T <= X1;
-    // columns 2j, 2j+1 of any V n-tile belong to heads (2j) % GP, (2j+1) % GP
-    const float l0 = __shfl_sync(0xffffffffu, l, ((2 * j) % GP) << 2);
-    const float l1 = __shfl_sync(0xffffffffu, l, ((2 * j + 1) % GP) << 2);
-    const long long hq0 = (long long)u.b * p.Hq + (long long)u.kvh * G;
-    const long long slot = 2 * wid + (u.ub < X0 ? 0 : 1);
+  // ---- running state ----
+  float o[C::MT][4];
 #pragma unroll
-    for (int m = 0; m < C::MT; ++m) {
-      int d0;
-      if constexpr (BITS == 4) d0 = 32 * (m >> 1) + 4 * rho + 2 * (m & 1);
-      else d0 = 16 * m + 2 * rho;
-      const int g = ((BITS == 4 ? (m >> 1) : m) * C::DPC) / C::GSZ;  // group of the m-tile
-      const int t = g * GP / 8;
-      // o[channel][(g, h)] -= cz[g][(g, h)]: row g of the correction lives in lanes 4g + j
-      const float corr0 = __shfl_sync(0xffffffffu, cz[t][0], (g << 2) + j);
-      const float corr1 = __shfl_sync(0xffffffffu, cz[t][1], (g << 2) + j);
+  for (int m = 0; m < C::MT; ++m) o[m][0] = o[m][1] = o[m][2] = o[m][3] = 0.f;
+  float cz[C::NTV][4];  // zero-point terms: rows = groups r, columns = (group, head)
 #pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int col = 8 * t + 2 * j + e;  // (group col / GP, head col % GP)
-        const int h = col % GP;
-        if (col / GP == g && h < G) {
-          const float corr = e ? corr1 : corr0;
-          const float x0 = o[m][e] - corr, x1 = o[m][2 + e] - corr;
-          if (whole) {
-            const float lh = e ? l1 : l0;
-            const float inv = lh > 0.f ? 1.f / lh : 0.f;
-            *reinterpret_cast<__half2*>(p.out + (hq0 + h) * D + d0) =
-                __floats2half2_rn(x0 * inv, x1 * inv);
-          } else {
-            *reinterpret_cast<float2*>(p.ws_o + (slot * G + h) * D + d0) = make_float2(x0, x1);
-          }
-        }
-      }
-    }
-    if (!whole && j == 0 && rho < G)
-      *reinterpret_cast<float2*>(p.ws_ml + (slot * G + rho) * 2) = make_float2(m_ref, l);
-  };
+  for (int t = 0; t < C::NTV; ++t) cz[t][0] = cz[t][1] = cz[t][2] = cz[t][3] = 0.f;
+  bool bt_bad = false;  // an unmapped page was met (flagged once at the end)
+  float m_ref = -INFINITY, l_run = 0.f;
 
-  // ---- tile issue (cp.async into stage it % STAGES) ----
+  // ---- this warp's tiles ----
+  const int ntiles = (t1 > t0) ? (t1 - t0 + kTT - 1) / kTT : 0;
+  const int nmine = (ntiles > warp) ? (ntiles - warp + kWarps - 1) / kWarps : 0;
   const uint8_t* kc_g = p.codes[0];
   const uint8_t* vc_g = p.codes[1];
   const uint8_t* ks_g = reinterpret_cast<const uint8_t*>(p.scale[0]);
@@ -469,24 +337,22 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
   const uint8_t* vs_g = reinterpret_cast<const uint8_t*>(p.scale[1]);
   const uint8_t* vz_g = reinterpret_cast<const uint8_t*>(p.zero[1]);
   const bool dense = geo.layout == KVQ_DENSE;
-  bool bt_bad = false;  // an unmapped page was met (flagged once at the end)
-  TileCursor icur = cur;  // the tile the next issue fetches
+  const long long slab_row = ((long long)b * geo.Hkv + kvh) * geo.slots;  // dense only
+  const uint32_t wpipe_s = smem_u32(wpipe);
 
-  // issues tile `it` of this warp (at icur) and moves icur on
+  // issues tile `it` into its stage; returns true when a page was unmapped
   auto issue = [&](int it) -> bool {
     const int stage = it % C::STAGES;
     bool unmapped = false;
     if (it < nmine) {
-      const int L = __ldg(p.seq_lens + icur.b);
-      const int start = icur.tin * kTT;
-      const int n = min(kTT, L - start);
+      const int start = t0 + (warp + it * kWarps) * kTT;
+      const int n = min(kTT, t1 - start);
       long long row = -1;  // this lane's token
       const uint32_t kc_s = wpipe_s + stage * C::STAGE, vc_s = kc_s + C::CODE_TILE;
       const uint32_t hd_s = vc_s + C::CODE_TILE;
       if (dense) {
-        const long long slab_row = ((long long)icur.b * Hkv + icur.kvh) * geo.slots + start;
-        if (lane < n) row = slab_row + lane;
-        const long long base = slab_row * C::ROWB;
+        if (lane < n) row = slab_row + start + lane;
+        const long long base = (slab_row + start) * C::ROWB;
 #pragma unroll
         for (int k = 0; k < C::CHUNKS; ++k) {
           const int c = lane + 32 * k;
@@ -499,7 +365,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
         }
       } else {
         if (lane < n) {
-          row = token_row(geo, icur.b, icur.kvh, start + lane);
+          row = token_row(geo, b, kvh, start + lane);
           unmapped = row < 0;
         }
 #pragma unroll
@@ -515,7 +381,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
         }
       }
       const unsigned bad = __ballot_sync(0xffffffffu, row < 0);
-      if (lane == 0) mask_s[stage] = bad;
+      if (lane == 0) mask_s[warp * C::STAGES + stage] = bad;
       const bool ok = row >= 0;
       const long long hoff = ok ? row * C::HDRB : 0;
       const uint32_t hdst = hd_s + lane * C::HDRB;
@@ -523,7 +389,6 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
       cp_async_small<C::HDRB>(hdst + C::HDR_TILE, kz_g + hoff, ok);
       cp_async_small<C::HDRB>(hdst + 2 * C::HDR_TILE, vs_g + hoff, ok);
       cp_async_small<C::HDRB>(hdst + 3 * C::HDR_TILE, vz_g + hoff, ok);
-      icur.advance(p);
     }
     cp_async_commit();  // one group per slot, empty past the end
     return unmapped;
@@ -733,16 +598,15 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
   };
 
   // ---- software-pipelined loop: tile i+1's scores overlap tile i's values ----
-  // Tile k of this warp lives in stage k % STAGES; one commit group per tile.
+  // Tile k lives in stage k % STAGES; one commit group per tile.
 #pragma unroll
   for (int s2 = 0; s2 < C::STAGES; ++s2) bt_bad |= issue(s2);
 
   uint32_t pp[4] = {0u, 0u, 0u, 0u};
-  begin_unit(cur);
-  {
+  if (nmine > 0) {
     cp_async_wait<C::STAGES - 1>();  // tile 0
     __syncwarp();
-    const unsigned bad0 = mask_s[0];
+    const unsigned bad0 = mask_s[warp * C::STAGES];
     header(0, 0, bad0);
     __syncwarp();
     float sc[4][2];
@@ -750,61 +614,102 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
     softmax(sc, pp);
   }
   int stage = 0;
-  for (int it = 0; it < nmine; ++it) {
+  // steady state, branch-free so that the two tiles' work can interleave
+  for (int it = 0; it + 1 < nmine; ++it) {
     const int nstage = (stage + 1 == C::STAGES) ? 0 : stage + 1;
-    const bool last = it + 1 == nmine;
-    if (!last && cur.tin + 1 < cur.T) {
-      // tile it+1 continues this unit: its scores overlap tile it's values
-      float scn[4][2];
-      cp_async_wait<C::STAGES - 2>();  // tile it+1
-      __syncwarp();
-      const unsigned badn = mask_s[nstage];
-      header(nstage, (it + 1) & 1, badn);
-      __syncwarp();
-      scores(nstage, (it + 1) & 1, badn, scn);
-      weighted_v(stage, it & 1, pp);
-      softmax(scn, pp);
-      ++cur.tin;
-    } else {
-      weighted_v(stage, it & 1, pp);
-      end_unit(cur);
-      if (!last) {
-        cur.next_unit(p);
-        begin_unit(cur);
-        float scn[4][2];
-        cp_async_wait<C::STAGES - 2>();  // tile it+1
-        __syncwarp();
-        const unsigned badn = mask_s[nstage];
-        header(nstage, (it + 1) & 1, badn);
-        __syncwarp();
-        scores(nstage, (it + 1) & 1, badn, scn);
-        softmax(scn, pp);
-      }
-    }
+    float scn[4][2];
+    cp_async_wait<C::STAGES - 2>();  // tile it+1
+    __syncwarp();
+    const unsigned badn = mask_s[warp * C::STAGES + nstage];
+    header(nstage, (it + 1) & 1, badn);
+    __syncwarp();
+    scores(nstage, (it + 1) & 1, badn, scn);
+    weighted_v(stage, it & 1, pp);
+    softmax(scn, pp);
     __syncwarp();
     bt_bad |= issue(it + C::STAGES);  // into the stage tile it has just left
     stage = nstage;
   }
+  if (nmine > 0) weighted_v(stage, (nmine - 1) & 1, pp);  // the last tile's values
   cp_async_wait<0>();
+
+  // ---------------- finish this warp: l, zero-point correction ----------------
   if (bt_bad && p.status) atomicOr(p.status, KVQ_FLAG_BLOCK_TABLE);
+  l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
+  l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
+  __syncthreads();  // every warp is done with its pipeline: reuse it for the merge
+
+  float* red = reinterpret_cast<float*>(pipe);                 // [warps][GP][D] o
+  float* ml = red + kWarps * GP * D;                            // [warps][GP][2]
+#pragma unroll
+  for (int m = 0; m < C::MT; ++m) {
+    int d0;
+    if constexpr (BITS == 4) d0 = 32 * (m >> 1) + 4 * rho + 2 * (m & 1);
+    else d0 = 16 * m + 2 * rho;
+    const int g = ((BITS == 4 ? (m >> 1) : m) * C::DPC) / C::GSZ;  // group of the m-tile's chunk
+    const int t = g * GP / 8;
+    // o[channel][(g, h)] -= cz[g][(g, h)]: row g of the correction lives in lanes 4g + j
+    const float corr0 = __shfl_sync(0xffffffffu, cz[t][0], (g << 2) + j);
+    const float corr1 = __shfl_sync(0xffffffffu, cz[t][1], (g << 2) + j);
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int col = 8 * t + 2 * j + e;  // (group col / GP, head col % GP)
+      const int h = col % GP;
+      if (col / GP == g && h < G) {
+        const float corr = e ? corr1 : corr0;
+        float* dst = red + (warp * GP + h) * D;
+        dst[d0] = o[m][e] - corr;
+        dst[d0 + 1] = o[m][2 + e] - corr;
+      }
+    }
+  }
+  if (j == 0 && rho < GP) {
+    ml[(warp * GP + rho) * 2] = m_ref;
+    ml[(warp * GP + rho) * 2 + 1] = l_run;
+  }
+  __syncthreads();
+
+  const long long hq0 = (long long)b * p.Hq + (long long)kvh * G;
+  for (int i = threadIdx.x; i < G * D; i += kWarps * 32) {
+    const int h = i / D, d = i - h * D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w2 = 0; w2 < kWarps; ++w2) M = fmaxf(M, ml[(w2 * GP + h) * 2]);
+    float num = 0.f, den = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w2 = 0; w2 < kWarps; ++w2) {
+        const float f = exp2f(ml[(w2 * GP + h) * 2] - M);
+        num = fmaf(f, red[(w2 * GP + h) * D + d], num);
+        den = fmaf(f, ml[(w2 * GP + h) * 2 + 1], den);
+      }
+    }
+    if (p.splits == 1) {
+      p.out[hq0 * D + i] = __float2half_rn(den > 0.f ? num / den : 0.f);
+    } else {
+      p.ws_o[((hq0 + h) * p.splits + split) * D + d] = num;
+      if (d == 0) {
+        float* mlo = p.ws_ml + ((hq0 + h) * p.splits + split) * 2;
+        mlo[0] = M;
+        mlo[1] = den;
+      }
+    }
+  }
 }
 
 template <int BITS, int D, int NG, int GP>
 size_t fast_smem_bytes() {
   using C = Cfg<BITS, D, NG, GP>;
-  return (size_t)kWarps * C::WARP_BYTES;
+  const size_t pipe = (size_t)kWarps * C::WARP_BYTES;
+  const size_t merge = (size_t)kWarps * GP * (D + 2) * sizeof(float);
+  return ((GP * D * 2 + 127) / 128) * 128 + (pipe > merge ? pipe : merge) +
+         kWarps * C::STAGES * sizeof(uint32_t);
 }
 
-// Launches the instantiation over p.ctas CTAs.  With ctas_per_sm != nullptr
-// nothing is launched: *ctas_per_sm receives how many CTAs fit on one SM, or,
-// when it holds -1 on entry, is set to 0 without any CUDA call (a check that
-// the instantiation exists).
+// Launches the instantiation, or with ctas_per_sm != nullptr only reports
+// how many of its CTAs fit on one SM.
 template <int BITS, int D, int NG, int GP>
 cudaError_t launch_fast_inst(const DecodeParams& p, cudaStream_t stream, int* ctas_per_sm) {
-  if (ctas_per_sm && *ctas_per_sm == -1) {
-    *ctas_per_sm = 0;
-    return cudaSuccess;
-  }
   const size_t smem = fast_smem_bytes<BITS, D, NG, GP>();
   cudaError_t e = cudaFuncSetAttribute(decode_fast_kernel<BITS, D, NG, GP>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -813,10 +718,9 @@ cudaError_t launch_fast_inst(const DecodeParams& p, cudaStream_t stream, int* ct
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
         ctas_per_sm, decode_fast_kernel<BITS, D, NG, GP>, kWarps * 32, smem);
   }
-  decode_fast_kernel<BITS, D, NG, GP><<<p.ctas, kWarps * 32, smem, stream>>>(p);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  return launch_merge_balanced(p, stream);
+  const dim3 grid(p.splits, p.geom.Hkv, p.batch);
+  decode_fast_kernel<BITS, D, NG, GP><<<grid, kWarps * 32, smem, stream>>>(p);
+  return cudaGetLastError();
 }
 
 }  // namespace fast

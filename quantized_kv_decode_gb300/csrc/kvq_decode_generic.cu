@@ -197,77 +197,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
   if (d < D) p.out[rowid * D + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
 }
 
-// Merge for the tensor-core kernel.  Its warps own equal ranges of the stream
-// of 32-token tiles (all tiles of unit (0, 0), then (0, 1), ...); a unit
-// whose tiles span several warps left one partial per warp: slot 2w + 1 in
-// the warp where it begins (its last segment there), slot 2w in every later
-// warp (their first segment).  One CTA per unit; units held by a single warp
-// were finished by that warp.  Empty and invalid sequences get zero rows here.
-__global__ void __launch_bounds__(128) merge_balanced_kernel(const DecodeParams p) {
-  const int unit = blockIdx.x;  // b * Hkv + kvh
-  const int Hkv = p.geom.Hkv, D = p.geom.D, G = p.G;
-  const int b = unit / Hkv, kvh = unit - (unit / Hkv) * Hkv;
-  __shared__ long long red[2][4];
-  long long before = 0, total = 0;
-  for (int i = threadIdx.x; i < p.batch; i += 128) {
-    const int L = p.seq_lens[i];
-    const long long T = (L < 0 || L > p.len_limit) ? 0 : (L + kFastTile - 1) / kFastTile;
-    total += T;
-    if (i < b) before += T;
-  }
-  for (int o = 16; o > 0; o >>= 1) {
-    before += __shfl_xor_sync(0xffffffffu, before, o);
-    total += __shfl_xor_sync(0xffffffffu, total, o);
-  }
-  if ((threadIdx.x & 31) == 0) {
-    red[0][threadIdx.x >> 5] = before;
-    red[1][threadIdx.x >> 5] = total;
-  }
-  __syncthreads();
-  before = (red[0][0] + red[0][1] + red[0][2] + red[0][3]) * Hkv;
-  total = (red[1][0] + red[1][1] + red[1][2] + red[1][3]) * Hkv;
-
-  const int L = p.seq_lens[b];
-  const bool bad = L < 0 || L > p.len_limit;
-  if (bad && kvh == 0 && threadIdx.x == 0 && p.status) atomicOr(p.status, KVQ_FLAG_SEQ_LEN);
-  const long long T = bad ? 0 : (L + kFastTile - 1) / kFastTile;
-  const long long hq0 = (long long)b * p.Hq + (long long)kvh * G;
-  if (T == 0) {
-    for (int i = threadIdx.x; i < G * D; i += 128) p.out[hq0 * D + i] = __float2half_rn(0.f);
-    return;
-  }
-  const long long W = (long long)p.ctas * kFastWarps;
-  const long long U0 = before + kvh * T, U1 = U0 + T;
-  // warp holding tile x: the last w with w * total / W <= x
-  const long long w0 = ((U0 + 1) * W - 1) / total;
-  const long long w1 = (U1 * W - 1) / total;
-  if (w0 == w1) return;
-  for (int i = threadIdx.x; i < G * D; i += 128) {
-    const int h = i / D, d = i - h * D;
-    float M = -INFINITY, num = 0.f, den = 0.f;
-    for (long long w = w0; w <= w1; ++w) {
-      const long long Xw = w * total / W, Xn = (w + 1) * total / W;
-      if (Xn == Xw) continue;  // a warp with no tiles
-      const long long slot = 2 * w + (U0 < Xw ? 0 : 1);
-      const float m = p.ws_ml[(slot * G + h) * 2], l = p.ws_ml[(slot * G + h) * 2 + 1];
-      const float x = p.ws_o[(slot * G + h) * D + d];
-      if (m == -INFINITY) continue;
-      const float Mn = fmaxf(M, m);
-      const float a = exp2f(M - Mn), f = exp2f(m - Mn);
-      num = fmaf(f, x, num * a);
-      den = fmaf(f, l, den * a);
-      M = Mn;
-    }
-    p.out[hq0 * D + i] = __float2half_rn(den > 0.f ? num / den : 0.f);
-  }
-}
-
 }  // namespace
-
-cudaError_t launch_merge_balanced(const DecodeParams& p, cudaStream_t stream) {
-  merge_balanced_kernel<<<(unsigned)(p.batch * p.geom.Hkv), 128, 0, stream>>>(p);
-  return cudaGetLastError();
-}
 
 cudaError_t launch_decode_generic(const DecodeParams& p, cudaStream_t stream) {
   const int G = p.G, D = p.geom.D;

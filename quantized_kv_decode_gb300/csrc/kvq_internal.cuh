@@ -75,7 +75,6 @@ struct DecodeParams {
   int32_t chunk;            // tokens per split (multiple of kChunkAlign)
   int32_t len_limit;        // largest valid seq_len
   float scale_log2;         // softmax scale * log2(e)
-  int32_t ctas;             // tensor-core kernel: CTAs the tile stream is balanced over
 };
 
 // Launchers (return a CUDA error code; the caller maps it to kvq_status).
@@ -90,19 +89,6 @@ cudaError_t launch_decode_fast_int4(const DecodeParams& p, int gp, cudaStream_t 
 cudaError_t launch_decode_fast_int8(const DecodeParams& p, int gp, cudaStream_t s, bool* handled,
                                     int* occ);
 int generic_ctas_per_sm(const DecodeParams& p);
-// Combines the per-warp partials of the tensor-core kernel for the
-// (sequence, KV head) units split between warps, and writes zero rows for
-// empty or invalid sequences.
-cudaError_t launch_merge_balanced(const DecodeParams& p, cudaStream_t stream);
-
-// Warps per CTA of the tensor-core kernel and tokens per warp tile.
-constexpr int kFastWarps = 4;
-constexpr int kFastTile = 32;
-// Workspace of the tensor-core kernel over `ctas` CTAs: two partial slots per
-// warp, each G x (D + 2) floats.
-size_t fast_workspace_bytes(int64_t ctas, int64_t G, int64_t D);
-void fast_workspace_carve(void* ws, int64_t ctas, int64_t G, int64_t D, float** ws_o,
-                          float** ws_ml);
 
 // Size of the workspace for `splits` splits (0 when splits == 1).
 size_t workspace_bytes(int64_t batch, int64_t Hq, int64_t D, int64_t splits);

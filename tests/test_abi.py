@@ -130,19 +130,11 @@ def test_append_and_decode_validate_before_launch(K):
 
 
 def test_explicit_split_counts(K):
-    """Explicit counts need no device.  Generic kernel (fp16 cache): context
-    splits, at most one per 64-token tile, no workspace for one split.
-    Tensor-core kernel (INT4): CTAs the tile stream is balanced over, two
-    partial slots of G x (D + 2) floats per warp (4 warps per CTA)."""
-    f = K.make_desc(16, 0, 32, 128, K.KVQ_DENSE, 4112)
-    assert K.kvq_decode_num_splits(f, 8, 32, 4097, 1) == 1
-    assert K.kvq_decode_num_splits(f, 8, 32, 4097, 7) == 7
-    assert K.kvq_decode_num_splits(f, 8, 32, 100, 50) == 2
-    assert K.kvq_decode_workspace_size(f, 8, 32, 4097, 1) == 0
-    assert K.kvq_decode_workspace_size(f, 8, 32, 4097, 4) >= 8 * 32 * 4 * (128 + 2) * 4
     d = K.make_desc(4, 32, 32, 128, K.KVQ_DENSE, 4112)
     assert K.kvq_decode_num_splits(d, 8, 32, 4097, 1) == 1
     assert K.kvq_decode_num_splits(d, 8, 32, 4097, 7) == 7
-    assert K.kvq_decode_workspace_size(d, 8, 32, 4097, 3) >= 2 * 3 * 4 * 1 * (128 + 2) * 4
-    g = K.make_desc(4, 64, 8, 128, K.KVQ_DENSE, 4112)     # 4 query heads per KV head
-    assert K.kvq_decode_workspace_size(g, 8, 32, 4097, 3) >= 2 * 3 * 4 * 4 * (128 + 2) * 4
+    # never more splits than 64-token tiles
+    assert K.kvq_decode_num_splits(d, 8, 32, 100, 50) == 2
+    assert K.kvq_decode_workspace_size(d, 8, 32, 4097, 1) == 0
+    ws = K.kvq_decode_workspace_size(d, 8, 32, 4097, 4)
+    assert ws >= 8 * 32 * 4 * (128 + 2) * 4
