@@ -1,16 +1,21 @@
 // Quantize-on-append kernel.
 //
-// One thread owns one group of `g` consecutive channels of one new K or V
-// vector ("What actually happens when you quantize a KV cache", section 3
-// steps 2-5 and section 4): it scans the group for min and max, derives the
-// fp16 scale and the integer zero-point, encodes every channel and packs two
-// INT4 codes per byte with the even channel in the low nibble.  Consecutive
-// threads own consecutive groups of the same vector, so the fp16 reads, the
-// code writes and the header writes are all contiguous across a warp.
+// Each group of `g` consecutive channels of one new K or V vector is encoded
+// as in "What actually happens when you quantize a KV cache" (section 3 steps
+// 2-5 and section 4): min and max over the group, an fp16 scale and integer
+// zero-point, codes clamp(round(x/s) + z, 0, 2^b - 1), and two INT4 codes per
+// byte with the even channel in the low nibble.
+//
+// One thread owns 8 channels (one 16-byte load); the g/8 threads of a group
+// are adjacent lanes of one warp and combine their min/max with shuffles, so
+// every lane runs a short chain (this matters most for the one-token append
+// of a decode step, where there are few groups).  Reads, code writes and
+// header writes are contiguous across a warp.
 //
 // Arithmetic (fixed so that codes are reproducible bit for bit):
 //   range = max - min            fp64 (exact for two fp16 values)
-//   s     = fp16 rounded toward +inf of range / (2^b - 1), fp64 quotient
+//   s     = the smallest fp16 with s * (2^b - 1) >= range (range / (2^b - 1)
+//           rounded toward +inf): an fp32 estimate, then exact fp64 checks
 //   z     = rint(-min / s)       fp32 IEEE division, round half to even
 //   q     = clamp(rint(x / s) + z, 0, 2^b - 1)
 // The file is compiled without fast-math: '/' here must stay div.rn.
@@ -19,9 +24,25 @@
 namespace kvq {
 namespace {
 
-__device__ __forceinline__ __half half_round_up(double d) {
+__device__ __forceinline__ unsigned short half_bits_up(unsigned short h) {   // h >= 0 finite
+  return (unsigned short)(h + 1);
+}
+__device__ __forceinline__ unsigned short half_bits_down(unsigned short h) { // h > 0
+  return (unsigned short)(h - 1);
+}
+__device__ __forceinline__ double half_bits_value(unsigned short h) {
+  return (double)__half2float(__ushort_as_half(h));
+}
+
+// smallest fp16 s > 0 with s * qmax >= range, for 0 < range <= 2 * 65504
+__device__ __forceinline__ __half scale_round_up(double range, int qmax) {
   unsigned short h;
-  asm("cvt.rp.f16.f64 %0, %1;" : "=h"(h) : "d"(d));
+  const float est = (float)range / (float)qmax;
+  asm("cvt.rp.f16.f32 %0, %1;" : "=h"(h) : "f"(est));
+  // the estimate is within one fp16 step of the answer; settle it exactly
+  // (h * qmax is exact in fp64: 11-bit significand times an 8-bit integer)
+  if (half_bits_value(h) * qmax < range) h = half_bits_up(h);
+  if (h > 1 && half_bits_value(half_bits_down(h)) * qmax >= range) h = half_bits_down(h);
   return __ushort_as_half(h);
 }
 
@@ -29,13 +50,14 @@ template <int BITS>
 __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
   const CacheGeom& c = p.geom;
   const int which = blockIdx.y;  // 0: K, 1: V
-  const int units_per_row = (BITS == 16) ? c.D / 8 : c.ngroups;
-  const long long n_units = (long long)p.batch * p.num_new * c.Hkv * units_per_row;
+  const int chunks = c.D / 8;    // 8-channel chunks per vector
+  const long long n_units = (long long)p.batch * p.num_new * c.Hkv * chunks;
   const long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (u >= n_units) return;
+  const bool live = u < n_units;
+  const long long uu = live ? u : 0;
 
-  const int grp = (int)(u % units_per_row);
-  long long r = u / units_per_row;
+  const int ch = (int)(uu % chunks);
+  long long r = uu / chunks;
   const int kvh = (int)(r % c.Hkv);
   r /= c.Hkv;
   const int t = (int)(r % p.num_new);
@@ -51,35 +73,44 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
     row = token_row(c, b, kvh, pos);
     if (row < 0) flags |= KVQ_FLAG_BLOCK_TABLE;
   }
-  if (row < 0) {
-    if (p.status) atomicOr(p.status, flags);
-    return;
-  }
-
   const __half* src = p.src[which] + (((long long)b * p.num_new + t) * c.Hkv + kvh) * c.D;
 
   if constexpr (BITS == 16) {
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + grp);
-    *reinterpret_cast<uint4*>(p.codes[which] + row * c.row_bytes + grp * 16) = v;
+    if (!live) return;
+    if (row < 0) {
+      if (ch == 0 && p.status) atomicOr(p.status, flags);
+      return;
+    }
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + ch);
+    *reinterpret_cast<uint4*>(p.codes[which] + row * c.row_bytes + ch * 16) = v;
     return;
   } else {
     constexpr int QMAX = (1 << BITS) - 1;
-    const int g = c.g;
-    const uint4* gsrc = reinterpret_cast<const uint4*>(src + (long long)grp * g);
+    const int tpg = c.g / 8;          // threads per group: 1, 2, 4, ..., 32
+    const int sub = ch % tpg;          // this thread's place in its group
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (live) v = __ldg(reinterpret_cast<const uint4*>(src) + ch);
+    const __half* h = reinterpret_cast<const __half*>(&v);
 
-    // pass 1: min, max, finiteness
     float mn = INFINITY, mx = -INFINITY;
     bool finite = true;
-    for (int i = 0; i < g / 8; ++i) {
-      const uint4 v = __ldg(gsrc + i);
-      const __half2* h2 = reinterpret_cast<const __half2*>(&v);
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const float2 f = __half22float2(h2[k]);
-        finite = finite && isfinite(f.x) && isfinite(f.y);
-        mn = fminf(mn, fminf(f.x, f.y));
-        mx = fmaxf(mx, fmaxf(f.x, f.y));
-      }
+    for (int k = 0; k < 8; ++k) {
+      const float f = __half2float(h[k]);
+      finite = finite && isfinite(f);
+      mn = fminf(mn, f);
+      mx = fmaxf(mx, f);
+    }
+    // combine over the group's adjacent lanes (groups never straddle a warp)
+    for (int o = 1; o < tpg; o <<= 1) {
+      mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      finite = (__shfl_xor_sync(0xffffffffu, (int)finite, o) != 0) && finite;
+    }
+    if (!live) return;
+    if (row < 0) {
+      if (ch == 0 && p.status) atomicOr(p.status, flags);
+      return;
     }
 
     __half s_h = __ushort_as_half(0);
@@ -93,7 +124,7 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
         // constant group: s = |min| (1 for an all-zero group) decodes exactly
         s_h = __float2half_rn(mn == 0.f ? 1.f : fabsf(mn));
       } else {
-        s_h = half_round_up(range / (double)QMAX);
+        s_h = scale_round_up(range, QMAX);
       }
       sf = __half2float(s_h);
       zf = rintf(__fdiv_rn(-mn, sf));
@@ -104,36 +135,33 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
       z_h = __int2half_rn((int)zf);  // an integer of magnitude <= 2048: exact, +0 for 0
     }
 
-    // pass 2: encode and pack, 8 channels (one 16-byte load) at a time
-    uint8_t* dst = p.codes[which] + row * c.row_bytes + (long long)grp * g * BITS / 8;
-    for (int i = 0; i < g / 8; ++i) {
-      const uint4 v = __ldg(gsrc + i);
-      const __half* h = reinterpret_cast<const __half*>(&v);
-      uint32_t w0 = 0, w1 = 0;
+    uint32_t w0 = 0, w1 = 0;
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        uint32_t q = 0;
-        if (finite) {
-          const float tq = rintf(__fdiv_rn(__half2float(h[k]), sf)) + zf;
-          q = (uint32_t)fminf(fmaxf(tq, 0.f), (float)QMAX);
-        }
-        if constexpr (BITS == 4) {
-          w0 |= q << (4 * k);  // channel 2m -> low nibble of byte m
-        } else {
-          if (k < 4) w0 |= q << (8 * k);
-          else       w1 |= q << (8 * (k - 4));
-        }
+    for (int k = 0; k < 8; ++k) {
+      uint32_t q = 0;
+      if (finite) {
+        const float tq = rintf(__fdiv_rn(__half2float(h[k]), sf)) + zf;
+        q = (uint32_t)fminf(fmaxf(tq, 0.f), (float)QMAX);
       }
       if constexpr (BITS == 4) {
-        *reinterpret_cast<uint32_t*>(dst + i * 4) = w0;
+        w0 |= q << (4 * k);  // channel 2m -> low nibble of byte m
       } else {
-        *reinterpret_cast<uint2*>(dst + i * 8) = make_uint2(w0, w1);
+        if (k < 4) w0 |= q << (8 * k);
+        else       w1 |= q << (8 * (k - 4));
       }
     }
-    const long long h_idx = row * c.ngroups + grp;
-    p.scale[which][h_idx] = s_h;
-    p.zero[which][h_idx] = z_h;
-    if (flags && p.status) atomicOr(p.status, flags);
+    uint8_t* dst = p.codes[which] + row * c.row_bytes + (long long)ch * 8 * BITS / 8;
+    if constexpr (BITS == 4) {
+      *reinterpret_cast<uint32_t*>(dst) = w0;
+    } else {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);
+    }
+    if (sub == 0) {
+      const long long h_idx = row * c.ngroups + ch / tpg;
+      p.scale[which][h_idx] = s_h;
+      p.zero[which][h_idx] = z_h;
+      if (flags && p.status) atomicOr(p.status, flags);
+    }
   }
 }
 
@@ -141,8 +169,7 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
   const CacheGeom& c = p.geom;
-  const int units_per_row = (c.bits == 16) ? c.D / 8 : c.ngroups;
-  const long long n_units = (long long)p.batch * p.num_new * c.Hkv * units_per_row;
+  const long long n_units = (long long)p.batch * p.num_new * c.Hkv * (c.D / 8);
   if (n_units == 0) return cudaSuccess;
   const dim3 block(256);
   const dim3 grid((unsigned)((n_units + 255) / 256), 2);
