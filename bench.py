@@ -276,11 +276,7 @@ def run_gpu_arm(args):
             torch.distributed.barrier()
 
     def max_over_ranks(x):
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max_over_ranks(x, world, dev)
 
     results = {}
     for fmt in ((bits, 16) if args.fp16_comparator else (bits,)):
@@ -385,10 +381,11 @@ def run_gpu_arm(args):
         barrier()
         e2e_ms = max_over_ranks(f0.elapsed_time(f1))
 
-        tokens = world * w.batch * layers * args.steps
+        tokens = w.batch * layers * args.steps  # per rank
         results[fmt] = dict(
-            value=tokens / (ms_total / 1e3), ms_per_step=ms_total / args.steps,
-            e2e=tokens / (e2e_ms / 1e3), h2d=h2d, d2h=d2h, call_ms=call_ms, splits=splits,
+            value=job_throughput(tokens, world, ms_total), ms_per_step=ms_total / args.steps,
+            e2e=job_throughput(tokens, world, e2e_ms), h2d=h2d, d2h=d2h, call_ms=call_ms,
+            splits=splits,
             bytes=decode_bytes(w, fmt, rows), clocks=clk, host_slices=host_slices,
             out0=outs[0][:1].float().cpu().numpy(),
             launches=args.steps * layers * (2 + (1 if splits > 1 else 0)))
@@ -446,14 +443,33 @@ def run_gpu_arm(args):
         torch.distributed.destroy_process_group()
 
 
+def reduce_max_over_ranks(x, world, device):
+    """The largest of every rank's x (the job's time is its slowest rank's)."""
+    if world == 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_rank, world, ms_max):
+    """Whole-job tokens/s: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank / (ms_max / 1e3)
+
+
 def load_profiled_traffic():
     """DRAM bytes per launch of the decode kernel from the committed ncu
-    summary, or None when no capture matches the current kernel."""
+    summary, or None when the kernel source changed since that capture."""
+    import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            d = json.load(f)
-        return d.get(WORKLOAD)
+            d = json.load(f)[WORKLOAD]
+        with open(os.path.join(ROOT, d["kernel_source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != d["kernel_sha256"]:
+                return None
+        return int(d["dram_bytes_per_launch"])
     except Exception:
         return None
 
