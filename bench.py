@@ -1,8 +1,10 @@
 #!/usr/bin/env python
 """Decode-step benchmark of the quantized KV-cache library on one node.
 
-One step = for every layer's cache: kvq_append of one new K/V token per
-sequence, then kvq_decode_attn over the whole cache (the new row included).
+One step = for every layer's cache: one kvq_append_decode_attn call, which
+quantizes one new K/V token per sequence into the cache and attends over the
+whole cache, the new row included (--separate-append: kvq_append then
+kvq_decode_attn, the same work in two launches).
 Workload (7B-class MHA layer): batch 8, 4096 cached tokens per sequence,
 32 query = 32 KV heads, head_dim 128, INT4 group-32 cache, 32 distinct layer
 caches per step (5.4 GB working set, far above the 129 MB L2).
@@ -12,8 +14,9 @@ value      tokens/s, one token = one sequence through one attention layer
            CUDA-graph replay of the step, inputs resident in HBM.
 e2e        the same metric with every step's q/k/v copied from pinned host
            memory and the outputs copied back inside the timed region.
-roofline   algorithmic bytes of one kvq_decode_attn call (codes + scales +
-           zeros + q + out) / its average duration (events around each call).
+roofline   algorithmic bytes of one step call (cache rows read, the new row
+           written, k/v/q in, out) / its average duration, from events around
+           a CUDA graph of every layer's call back to back.
 cpu_baseline  the CPU oracle timed on a bounded sample (one sequence, all
            heads, one layer per step) on this host.
 
@@ -74,11 +77,15 @@ def workload_config(w, bits, layers):
     }
 
 
-def decode_bytes(w, bits, rows):
-    """Algorithmic bytes of one decode call: codes + scale/zero + q + out."""
+def decode_bytes(w, bits, rows, fused=True):
+    """Algorithmic bytes of one step call.  Decode alone: `rows` cache rows
+    (codes + scale/zero, K and V) read, q read, out written.  Fused append:
+    rows - 1 cache rows read, the new row written, the new fp16 K/V read."""
     D = w.head_dim
     per_row = D * bits // 8 + (0 if bits == 16 else 4 * (D // w.group_size))
     kv = 2 * w.batch * w.num_kv_heads * rows * per_row
+    if fused:
+        kv += 2 * w.batch * w.num_kv_heads * D * 2
     return kv + 2 * w.batch * w.num_q_heads * D * 2
 
 
@@ -291,10 +298,21 @@ def run_gpu_arm(args):
         status = torch.zeros(1, dtype=torch.int32, device=dev)
         outs = [torch.empty_like(q) for q in qs]
 
+        kn1 = [k[:, 0] for k in kns]   # [B][Hkv][D] views of the step's new K/V
+        vn1 = [v[:, 0] for v in vns]
+
+        def call(l, s):
+            if args.separate_append:
+                K.kvq_decode_attn(caches[l], qs[l], lens, rows, outs[l], ws, status, stream=s)
+            else:
+                K.kvq_append_decode_attn(caches[l], kn1[l], vn1[l], qs[l], lens_before, rows,
+                                         outs[l], ws, status, stream=s)
+
         def step(s):
             for l in range(layers):
-                K.kvq_append(caches[l], kns[l], vns[l], lens_before, status, stream=s)
-                K.kvq_decode_attn(caches[l], qs[l], lens, rows, outs[l], ws, status, stream=s)
+                if args.separate_append:
+                    K.kvq_append(caches[l], kns[l], vns[l], lens_before, status, stream=s)
+                call(l, s)
 
         with torch.cuda.stream(stream):
             for _ in range(2):
@@ -327,12 +345,13 @@ def run_gpu_arm(args):
         ms_total = max_over_ranks(e0.elapsed_time(e1))
         clk = clocks.stop() if fmt == bits else None
 
-        # per-call duration of kvq_decode_attn (decode kernel + merge): a graph of
-        # every layer's decode call back to back, timed with events on its stream
+        # per-call duration of the step call (kernel + split merge): a graph of
+        # every layer's call back to back, timed with events on its stream
+        # (repeating a fused call re-writes the same row with the same codes)
         dgraph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(dgraph, stream=stream):
             for l in range(layers):
-                K.kvq_decode_attn(caches[l], qs[l], lens, rows, outs[l], ws, status, stream=stream)
+                call(l, stream)
         torch.cuda.synchronize()
         reps = max(3, args.steps // 2)
         d0 = torch.cuda.Event(enable_timing=True)
@@ -386,9 +405,10 @@ def run_gpu_arm(args):
             value=job_throughput(tokens, world, ms_total), ms_per_step=ms_total / args.steps,
             e2e=job_throughput(tokens, world, e2e_ms), h2d=h2d, d2h=d2h, call_ms=call_ms,
             splits=splits,
-            bytes=decode_bytes(w, fmt, rows), clocks=clk, host_slices=host_slices,
-            out0=outs[0][:1].float().cpu().numpy(),
-            launches=args.steps * layers * (2 + (1 if splits > 1 else 0)))
+            bytes=decode_bytes(w, fmt, rows, not args.separate_append), clocks=clk,
+            host_slices=host_slices, out0=outs[0][:1].float().cpu().numpy(),
+            launches=args.steps * layers * ((2 if args.separate_append else 1) +
+                                            (1 if splits > 1 else 0)))
         del caches, graph, dgraph
         torch.cuda.empty_cache()
 
@@ -411,7 +431,8 @@ def run_gpu_arm(args):
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "traffic": traffic,
-                     "kernel": "kvq_decode_attn (decode kernel + split merge)",
+                     "kernel": ("kvq_decode_attn" if args.separate_append else
+                                "kvq_append_decode_attn") + " (decode kernel + split merge)",
                      "bytes_per_launch": r["bytes"], "avg_launch_us": r["call_ms"] * 1e3},
         "e2e": {"value": r["e2e"], "unit": UNIT, "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"]},
@@ -459,16 +480,18 @@ def job_throughput(tokens_per_rank, world, ms_max):
 
 
 def load_profiled_traffic():
-    """DRAM bytes per launch of the decode kernel from the committed ncu
-    summary, or None when the kernel source changed since that capture."""
+    """DRAM bytes per launch of the step kernel from the committed ncu
+    summary, or None when any of the kernel's sources changed since that
+    capture."""
     import hashlib
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)[WORKLOAD]
-        with open(os.path.join(ROOT, d["kernel_source"]), "rb") as f:
-            if hashlib.sha256(f.read()).hexdigest() != d["kernel_sha256"]:
-                return None
+        for src, digest in d["kernel_sources"].items():
+            with open(os.path.join(ROOT, src), "rb") as f:
+                if hashlib.sha256(f.read()).hexdigest() != digest:
+                    return None
         return int(d["dram_bytes_per_launch"])
     except Exception:
         return None
@@ -484,6 +507,8 @@ def main():
     ap.add_argument("--cpu-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fp16-comparator", action="store_true")
+    ap.add_argument("--separate-append", action="store_true",
+                    help="append and attend in two calls instead of the fused call")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -191,6 +191,38 @@ kvq_status kvq_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache,
                            void* workspace, size_t workspace_bytes,
                            uint32_t* dev_status, void* stream);
 
+/*
+ * One decode step in one call: kvq_append of one token per sequence followed
+ * by kvq_decode_attn over the lengths seq_lens_before + 1 ("What actually
+ * happens when you quantize a KV cache", section 3: the new K/V vectors are
+ * quantized on arrival and attention then reads the quantized cache, the new
+ * token included).
+ *
+ *   k_new, v_new     device fp16 [batch][num_kv_heads][head_dim]
+ *   seq_lens_before  device int32 [batch]: tokens cached before this step; the
+ *                    new token is written at position seq_lens_before[b] and
+ *                    seq_lens_before[b] + 1 tokens are attended.
+ *   max_seq_len      host upper bound on every seq_lens_before[b] + 1.
+ *   the rest         as for kvq_decode_attn (same workspace size for the same
+ *                    batch, num_q_heads, max_seq_len and num_splits).
+ *
+ * Cache contents, out and the status flags are those of kvq_append (num_new =
+ * 1) followed by kvq_decode_attn: the codes, scales and zero-points written
+ * are bit-identical, and so is out.  For bits 4 and 8 with at most 8 query
+ * heads per KV head this is one kernel launch (plus the merge when split):
+ * the thread block that owns the new position quantizes it, stores it, and
+ * uses it from shared memory.  Other shapes run the two kernels in sequence.
+ * Lengths are not modified.
+ */
+kvq_status kvq_append_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache,
+                                  int32_t batch, int32_t num_q_heads,
+                                  const uint16_t* k_new, const uint16_t* v_new,
+                                  const uint16_t* q, const int32_t* seq_lens_before,
+                                  int32_t max_seq_len, int32_t num_splits,
+                                  float softmax_scale, uint16_t* out,
+                                  void* workspace, size_t workspace_bytes,
+                                  uint32_t* dev_status, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* kvq_status_string(kvq_status status);
 

@@ -10,7 +10,8 @@ from ._lib import (KVQ_DENSE, KVQ_ERR_CUDA, KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPO
                    kvq_cache, kvq_cache_desc, lib)
 
 __all__ = [
-    "KVCache", "make_desc", "kvq_append", "kvq_decode_attn", "kvq_cache_bytes",
+    "KVCache", "make_desc", "kvq_append", "kvq_decode_attn", "kvq_append_decode_attn",
+    "kvq_cache_bytes",
     "kvq_cache_array_bytes", "kvq_decode_num_splits", "kvq_decode_workspace_size",
     "kvq_status_string", "KVQError", "lib",
 ]

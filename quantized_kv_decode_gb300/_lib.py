@@ -77,6 +77,10 @@ SIGNATURES = {
     "kvq_decode_attn": (c_int32, [POINTER(kvq_cache_desc), POINTER(kvq_cache), c_int32, c_int32,
                                   c_void_p, c_void_p, c_int32, c_int32, c_float, c_void_p,
                                   c_void_p, c_size_t, c_void_p, c_void_p]),
+    "kvq_append_decode_attn": (c_int32, [POINTER(kvq_cache_desc), POINTER(kvq_cache), c_int32,
+                                         c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_int32,
+                                         c_int32, c_float, c_void_p, c_void_p, c_size_t, c_void_p,
+                                         c_void_p]),
     "kvq_status_string": (ctypes.c_char_p, [c_int32]),
 }
 

@@ -157,5 +157,36 @@ def kvq_decode_attn(cache: KVCache, q: torch.Tensor, seq_lens: torch.Tensor, max
     return out
 
 
+def kvq_append_decode_attn(cache: KVCache, k_new: torch.Tensor, v_new: torch.Tensor,
+                           q: torch.Tensor, seq_lens_before: torch.Tensor, max_seq_len: int,
+                           out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+                           dev_status: torch.Tensor | None = None, num_splits: int = 0,
+                           softmax_scale: float = 0.0, stream=None) -> torch.Tensor:
+    """One decode step: append k_new/v_new [B][Hkv][D] at seq_lens_before and
+    attend q [B][Hq][D] over seq_lens_before + 1 tokens; returns out."""
+    _need(q, torch.float16, "q", 3)
+    _need(k_new, torch.float16, "k_new", 3)
+    _need(v_new, torch.float16, "v_new", 3)
+    _need(seq_lens_before, torch.int32, "seq_lens_before", 1)
+    B, Hq, D = q.shape
+    if (D != cache.desc.head_dim or seq_lens_before.numel() != B
+            or tuple(k_new.shape) != (B, cache.desc.num_kv_heads, D)
+            or tuple(v_new.shape) != tuple(k_new.shape)):
+        raise ValueError("shape does not match the cache descriptor")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, torch.float16, "out", 3)
+    need = kvq_decode_workspace_size(cache.desc, B, Hq, max_seq_len, num_splits)
+    if need and (workspace is None or workspace.numel() * workspace.element_size() < need):
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = _lib.lib().kvq_append_decode_attn(
+        byref(cache.desc), byref(cache.ptrs), B, Hq, _ptr(k_new), _ptr(v_new), _ptr(q),
+        _ptr(seq_lens_before), int(max_seq_len), int(num_splits), float(softmax_scale), _ptr(out),
+        _ptr(workspace), ws_bytes, _ptr(dev_status), _stream(stream))
+    _lib.check(st, "kvq_append_decode_attn")
+    return out
+
+
 def default_scale(head_dim: int) -> float:
     return 1.0 / math.sqrt(head_dim)

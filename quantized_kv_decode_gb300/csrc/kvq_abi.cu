@@ -261,12 +261,20 @@ size_t kvq_decode_workspace_size(const kvq_cache_desc* desc, int32_t batch, int3
   return workspace_bytes(batch, num_q_heads, desc->head_dim, s);
 }
 
-kvq_status kvq_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache, int32_t batch,
-                           int32_t num_q_heads, const uint16_t* q, const int32_t* seq_lens,
-                           int32_t max_seq_len, int32_t num_splits, float softmax_scale,
-                           uint16_t* out, void* workspace, size_t workspace_size,
-                           uint32_t* dev_status, void* stream) {
-  DecodeParams p;
+}  // extern "C"
+
+namespace {
+
+// Validation, planning and dispatch shared by the decode entry points.  With
+// lens_before set the new token's K/V are quantized and attended in the same
+// pass (fused append); otherwise seq_lens gives the lengths to attend over.
+kvq_status decode_impl(const kvq_cache_desc* desc, const kvq_cache* cache, int32_t batch,
+                       int32_t num_q_heads, const uint16_t* q, const int32_t* seq_lens,
+                       const int32_t* lens_before, const uint16_t* k_new, const uint16_t* v_new,
+                       int32_t max_seq_len, int32_t num_splits, float softmax_scale,
+                       uint16_t* out, void* workspace, size_t workspace_size,
+                       uint32_t* dev_status, void* stream) {
+  DecodeParams p{};
   kvq_status st = check_desc(desc, &p.geom);
   if (st != KVQ_OK) return st;
   if ((st = check_cache(desc, cache)) != KVQ_OK) return st;
@@ -275,8 +283,12 @@ kvq_status kvq_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache, i
   if (num_q_heads % desc->num_kv_heads) return KVQ_ERR_INVALID_ARG;
   if (!(softmax_scale >= 0.f) || isinf(softmax_scale)) return KVQ_ERR_INVALID_ARG;
   if (batch == 0) return KVQ_OK;
-  if (!q || !seq_lens || !out) return KVQ_ERR_INVALID_ARG;
-  if (!aligned(q) || !aligned(out) || !aligned(seq_lens)) return KVQ_ERR_INVALID_ARG;
+  const bool fused = lens_before != nullptr;
+  if (!q || !out || (!fused && !seq_lens) || (fused && (!k_new || !v_new)))
+    return KVQ_ERR_INVALID_ARG;
+  if (!aligned(q) || !aligned(out)) return KVQ_ERR_INVALID_ARG;
+  if (fused ? (!aligned(lens_before) || !aligned(k_new) || !aligned(v_new)) : !aligned(seq_lens))
+    return KVQ_ERR_INVALID_ARG;
   const int G = num_q_heads / desc->num_kv_heads;
   if (G > kMaxGroupHeads) return KVQ_ERR_UNSUPPORTED;
 
@@ -296,7 +308,10 @@ kvq_status kvq_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache, i
   p.zero[0] = reinterpret_cast<const __half*>(cache->k_zero);
   p.zero[1] = reinterpret_cast<const __half*>(cache->v_zero);
   p.q = reinterpret_cast<const __half*>(q);
-  p.seq_lens = seq_lens;
+  p.seq_lens = fused ? nullptr : seq_lens;
+  p.lens_before = fused ? lens_before : nullptr;
+  p.new_kv[0] = reinterpret_cast<const __half*>(k_new);
+  p.new_kv[1] = reinterpret_cast<const __half*>(v_new);
   p.out = reinterpret_cast<__half*>(out);
   p.ws_o = nullptr;
   p.ws_ml = nullptr;
@@ -320,9 +335,57 @@ kvq_status kvq_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache, i
     if (desc->bits == 4) e = launch_decode_fast_int4(p, plan.gp, s, &handled, nullptr);
     else e = launch_decode_fast_int8(p, plan.gp, s, &handled, nullptr);
   }
-  if (!handled) e = launch_decode_generic(p, s);
+  if (!handled) {
+    if (fused) {
+      // shapes without a fast kernel: the append kernel, then the generic pass
+      AppendParams a{};
+      a.geom = p.geom;
+      a.codes[0] = reinterpret_cast<uint8_t*>(cache->k_codes);
+      a.codes[1] = reinterpret_cast<uint8_t*>(cache->v_codes);
+      a.scale[0] = reinterpret_cast<__half*>(cache->k_scale);
+      a.scale[1] = reinterpret_cast<__half*>(cache->v_scale);
+      a.zero[0] = reinterpret_cast<__half*>(cache->k_zero);
+      a.zero[1] = reinterpret_cast<__half*>(cache->v_zero);
+      a.src[0] = p.new_kv[0];
+      a.src[1] = p.new_kv[1];
+      a.seq_lens_before = lens_before;
+      a.status = dev_status;
+      a.batch = batch;
+      a.num_new = 1;
+      e = launch_append(a, s);
+    }
+    if (e == cudaSuccess) e = launch_decode_generic(p, s);
+  }
   if (e == cudaSuccess && splits > 1) e = launch_merge(p, s);
   return from_cuda(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+kvq_status kvq_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache, int32_t batch,
+                           int32_t num_q_heads, const uint16_t* q, const int32_t* seq_lens,
+                           int32_t max_seq_len, int32_t num_splits, float softmax_scale,
+                           uint16_t* out, void* workspace, size_t workspace_size,
+                           uint32_t* dev_status, void* stream) {
+  return decode_impl(desc, cache, batch, num_q_heads, q, seq_lens, nullptr, nullptr, nullptr,
+                     max_seq_len, num_splits, softmax_scale, out, workspace, workspace_size,
+                     dev_status, stream);
+}
+
+kvq_status kvq_append_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache,
+                                  int32_t batch, int32_t num_q_heads, const uint16_t* k_new,
+                                  const uint16_t* v_new, const uint16_t* q,
+                                  const int32_t* seq_lens_before, int32_t max_seq_len,
+                                  int32_t num_splits, float softmax_scale, uint16_t* out,
+                                  void* workspace, size_t workspace_size, uint32_t* dev_status,
+                                  void* stream) {
+  if (batch > 0 && !seq_lens_before) return KVQ_ERR_INVALID_ARG;
+  if (batch > 0 && (!k_new || !v_new)) return KVQ_ERR_INVALID_ARG;
+  return decode_impl(desc, cache, batch, num_q_heads, q, nullptr, seq_lens_before, k_new, v_new,
+                     max_seq_len, num_splits, softmax_scale, out, workspace, workspace_size,
+                     dev_status, stream);
 }
 
 const char* kvq_status_string(kvq_status status) {

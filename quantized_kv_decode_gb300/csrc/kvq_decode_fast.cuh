@@ -28,7 +28,7 @@
 //    final row (one split) or its partial for the merge kernel.
 #pragma once
 
-#include "kvq_internal.cuh"
+#include "kvq_quant.cuh"
 
 namespace kvq {
 namespace fast {
@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int rho = lane >> 2, j = lane & 3;
 
-  int L = p.seq_lens[b];
+  int L = seq_len_of(p, b);
   if (L < 0 || L > p.len_limit) {
     if (threadIdx.x == 0 && split == 0 && kvh == 0 && p.status) atomicOr(p.status, KVQ_FLAG_SEQ_LEN);
     L = 0;
@@ -241,10 +241,12 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
   const int t1 = min(L, t0 + p.chunk);
   if (p.splits > 1 && t0 >= L) return;  // the merge reads splits < ceil(L / chunk) only
 
-  // shared memory: [q fp16 GP x D][per warp: stages, header scratch][tile masks]
+  // shared memory: [q fp16 GP x D][per warp: stages, header scratch][tile
+  // masks][the appended token: K codes, V codes, 4 header rows (fused only)]
   __half* q_s = reinterpret_cast<__half*>(smem);
   uint8_t* pipe = smem + ((GP * D * 2 + 127) / 128) * 128;
   uint32_t* mask_s = reinterpret_cast<uint32_t*>(pipe + kWarps * C::WARP_BYTES);
+  uint8_t* newtok = pipe + kWarps * C::WARP_BYTES + ((kWarps * C::STAGES * 4 + 15) / 16) * 16;
   uint8_t* wpipe = pipe + warp * C::WARP_BYTES;
   // header scratch buffer `buf` (0/1): K (s*scale, z) [NG][KROW], V scale
   // [NG][VROW], V zero [NG][VROW], token mask [kTT]
@@ -257,7 +259,19 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
   const __half* qg = p.q + ((long long)b * p.Hq + (long long)kvh * G) * D;
   for (int i = threadIdx.x; i < GP * D; i += kWarps * 32)
     q_s[i] = (i < G * D) ? qg[i] : __float2half_rn(0.f);
+
   __syncthreads();
+
+  // Fused append: the warp whose tile holds the new position quantizes the
+  // new K and V vectors (the quantize8 the append kernel runs), stores them
+  // to the cache and keeps them in shared memory, then copies them into its
+  // stage when that tile arrives.  Cache reads of this launch never depend on
+  // the cache write, so nothing orders them.
+  const int pos_new = L - 1;
+  const bool owner_cta = p.lens_before != nullptr && L > 0 && pos_new >= t0 && pos_new < t1;
+  const int new_tile = owner_cta ? (pos_new - t0) / kTT : -1;  // tile index within the CTA
+  const bool owner = owner_cta && (new_tile % kWarps) == warp;  // warp-uniform
+  const int new_it = new_tile / kWarps;                          // ... within the warp's tiles
 
   // ---- score-mma A fragments: row r <-> (group r / GP, head r % GP) ----
   const int g_lo = rho / GP, h_row = rho % GP;
@@ -597,15 +611,78 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
     }
   };
 
+  // fused append: copy the new token into the stage of the tile that holds it
+  auto patch_new = [&](int it_tile, int stg) {
+    if (!owner || it_tile != new_it) return;  // warp-uniform
+    const int r = pos_new - (t0 + new_tile * kTT);
+    uint8_t* st = wpipe + stg * C::STAGE;
+    if (lane < C::CHUNKS) {
+      *reinterpret_cast<uint4*>(st + C::at(r, lane)) =
+          *reinterpret_cast<const uint4*>(newtok + lane * 16);
+    } else if (lane < 2 * C::CHUNKS) {
+      const int c = lane - C::CHUNKS;
+      *reinterpret_cast<uint4*>(st + C::CODE_TILE + C::at(r, c)) =
+          *reinterpret_cast<const uint4*>(newtok + C::ROWB + c * 16);
+    } else if (lane < 2 * C::CHUNKS + 4) {
+      const int a = lane - 2 * C::CHUNKS;  // K scale, K zero, V scale, V zero
+      uint8_t* dst = st + 2 * C::CODE_TILE + a * C::HDR_TILE + r * C::HDRB;
+      const uint8_t* src = newtok + 2 * C::ROWB + a * C::HDRB;
+      if constexpr (C::HDRB == 4) *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(src);
+      else if constexpr (C::HDRB == 8) *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(src);
+      else *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+    }
+    __syncwarp();
+  };
+
   // ---- software-pipelined loop: tile i+1's scores overlap tile i's values ----
   // Tile k lives in stage k % STAGES; one commit group per tile.
 #pragma unroll
   for (int s2 = 0; s2 < C::STAGES; ++s2) bt_bad |= issue(s2);
 
+  // fused append (owner warp only), after its first loads are in flight
+  if (owner) {
+    constexpr int CHV = D / 8;          // 8-channel chunks per vector
+    const int which = lane / CHV;       // 0: K, 1: V, 2+: idle lanes
+    const int ch = lane % CHV;
+    const long long nrow = token_row(geo, b, kvh, pos_new);
+    if (nrow < 0 && lane == 0 && p.status) atomicOr(p.status, KVQ_FLAG_BLOCK_TABLE);
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (which < 2)
+      v = __ldg(reinterpret_cast<const uint4*>(p.new_kv[which] + ((long long)b * geo.Hkv + kvh) * D) + ch);
+    const Quant8 qz = quantize8<BITS>(v, C::GSZ / 8);
+    if (which < 2) {
+      constexpr int CB = BITS;          // code bytes per 8 channels
+      uint8_t* gcodes = const_cast<uint8_t*>(p.codes[which]);
+      if constexpr (BITS == 4) {
+        *reinterpret_cast<uint32_t*>(newtok + which * C::ROWB + ch * CB) = qz.w0;
+        if (nrow >= 0) *reinterpret_cast<uint32_t*>(gcodes + nrow * C::ROWB + ch * CB) = qz.w0;
+      } else {
+        *reinterpret_cast<uint2*>(newtok + which * C::ROWB + ch * CB) = make_uint2(qz.w0, qz.w1);
+        if (nrow >= 0)
+          *reinterpret_cast<uint2*>(gcodes + nrow * C::ROWB + ch * CB) = make_uint2(qz.w0, qz.w1);
+      }
+      const int tpg = C::GSZ / 8;
+      if (ch % tpg == 0) {
+        const int g = ch / tpg;
+        __half* hs = reinterpret_cast<__half*>(newtok + 2 * C::ROWB + (2 * which) * C::HDRB);
+        __half* hz = reinterpret_cast<__half*>(newtok + 2 * C::ROWB + (2 * which + 1) * C::HDRB);
+        hs[g] = qz.s;
+        hz[g] = qz.z;
+        if (nrow >= 0) {
+          const_cast<__half*>(p.scale[which])[nrow * NG + g] = qz.s;
+          const_cast<__half*>(p.zero[which])[nrow * NG + g] = qz.z;
+        }
+        if (qz.flags && p.status) atomicOr(p.status, qz.flags);
+      }
+    }
+    __syncwarp();
+  }
+
   uint32_t pp[4] = {0u, 0u, 0u, 0u};
   if (nmine > 0) {
     cp_async_wait<C::STAGES - 1>();  // tile 0
     __syncwarp();
+    patch_new(0, 0);
     const unsigned bad0 = mask_s[warp * C::STAGES];
     header(0, 0, bad0);
     __syncwarp();
@@ -620,6 +697,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
     float scn[4][2];
     cp_async_wait<C::STAGES - 2>();  // tile it+1
     __syncwarp();
+    patch_new(it + 1, nstage);
     const unsigned badn = mask_s[warp * C::STAGES + nstage];
     header(nstage, (it + 1) & 1, badn);
     __syncwarp();
@@ -701,9 +779,10 @@ template <int BITS, int D, int NG, int GP>
 size_t fast_smem_bytes() {
   using C = Cfg<BITS, D, NG, GP>;
   const size_t pipe = (size_t)kWarps * C::WARP_BYTES;
+  const size_t masks = ((kWarps * C::STAGES * 4 + 15) / 16) * 16;
+  const size_t newtok = 2 * C::ROWB + 4 * C::HDRB;
   const size_t merge = (size_t)kWarps * GP * (D + 2) * sizeof(float);
-  return ((GP * D * 2 + 127) / 128) * 128 + (pipe > merge ? pipe : merge) +
-         kWarps * C::STAGES * sizeof(uint32_t);
+  return ((GP * D * 2 + 127) / 128) * 128 + (pipe > merge ? pipe : merge) + masks + newtok;
 }
 
 // Launches the instantiation, or with ctas_per_sm != nullptr only reports

@@ -58,7 +58,7 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(const DecodePa
   float* a_s = l_s + G;               // [G]
   long long* row_s = reinterpret_cast<long long*>(a_s + ((G + 1) & ~1));  // [kTile]
 
-  int L = p.seq_lens[b];
+  int L = seq_len_of(p, b);
   const bool bad_len = (L < 0 || L > p.len_limit);
   if (bad_len) {
     if (tid == 0 && split == 0 && kvh == 0 && p.status) atomicOr(p.status, KVQ_FLAG_SEQ_LEN);
@@ -179,7 +179,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
   const int b = (int)(rowid / p.Hq);
   const int D = p.geom.D;
   const int d = threadIdx.x;
-  const int L = p.seq_lens[b];
+  const int L = seq_len_of(p, b);
   const int nv = (L <= 0 || L > p.len_limit) ? 0 : (L + p.chunk - 1) / p.chunk;
   const float* ml = p.ws_ml + rowid * p.splits * 2;
   const float* o = p.ws_o + rowid * p.splits * D + d;

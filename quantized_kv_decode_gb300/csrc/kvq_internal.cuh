@@ -75,7 +75,20 @@ struct DecodeParams {
   int32_t chunk;            // tokens per split (multiple of kChunkAlign)
   int32_t len_limit;        // largest valid seq_len
   float scale_log2;         // softmax scale * log2(e)
+  // fused append + decode: lengths before the step and the new token's K/V
+  // ([batch][Hkv][D]); the attended length is lens_before + 1 (seq_lens unused)
+  const int32_t* lens_before;
+  const __half* new_kv[2];
 };
+
+// Tokens to attend over for sequence b (-1 for a length that cannot be formed).
+__device__ __forceinline__ int seq_len_of(const DecodeParams& p, int b) {
+  if (p.lens_before) {
+    const int x = __ldg(p.lens_before + b);
+    return (x < 0 || x == 0x7fffffff) ? -1 : x + 1;
+  }
+  return __ldg(p.seq_lens + b);
+}
 
 // Launchers (return a CUDA error code; the caller maps it to kvq_status).
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);

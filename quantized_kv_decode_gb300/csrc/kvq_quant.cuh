@@ -1,0 +1,117 @@
+// Group-wise asymmetric quantization of fp16 vectors, shared by the append
+// kernel and the fused append + decode path.
+//
+// "What actually happens when you quantize a KV cache", section 3 steps 2-5
+// and section 4: per group of g channels, min and max, an fp16 scale and an
+// integer zero-point, codes clamp(round(x/s) + z, 0, 2^b - 1), two INT4
+// codes per byte with the even channel in the low nibble.
+//
+// Arithmetic (fixed so that codes are reproducible bit for bit):
+//   range = max - min            fp64 (exact for two fp16 values)
+//   s     = the smallest fp16 with s * (2^b - 1) >= range (range / (2^b - 1)
+//           rounded toward +inf): an fp32 estimate, then exact fp64 checks
+//   z     = rint(-min / s)       fp32 IEEE division, round half to even,
+//                                clamped to +-2048 (flagged) and stored as an
+//                                integer (+0, never -0)
+//   q     = clamp(rint(x / s) + z, 0, 2^b - 1)
+//   constant group: s = |min| (1 when min = 0), so every code is 0 and the
+//   value decodes exactly; a group holding inf/NaN: s = z = 0, codes 0, flagged.
+// Translation units including this file must not use fast-math: '/' stays div.rn.
+#pragma once
+
+#include "kvq_internal.cuh"
+
+namespace kvq {
+
+namespace quant_detail {
+
+__device__ __forceinline__ double half_bits_value(unsigned short h) {
+  return (double)__half2float(__ushort_as_half(h));
+}
+
+// smallest fp16 s > 0 with s * qmax >= range, for 0 < range <= 2 * 65504
+__device__ __forceinline__ __half scale_round_up(double range, int qmax) {
+  unsigned short h;
+  const float est = (float)range / (float)qmax;
+  asm("cvt.rp.f16.f32 %0, %1;" : "=h"(h) : "f"(est));
+  // the estimate is within one fp16 step of the answer; settle it exactly
+  // (h * qmax is exact in fp64: 11-bit significand times an 8-bit integer)
+  if (half_bits_value(h) * qmax < range) h = (unsigned short)(h + 1);
+  if (h > 1 && half_bits_value((unsigned short)(h - 1)) * qmax >= range)
+    h = (unsigned short)(h - 1);
+  return __ushort_as_half(h);
+}
+
+}  // namespace quant_detail
+
+// One lane's share of a group: 8 channels.
+struct Quant8 {
+  uint32_t w0, w1;  // packed codes: INT4 -> w0 (4 bytes), INT8 -> w0, w1 (8 bytes)
+  __half s, z;      // the group's scale and zero-point
+  uint32_t flags;   // KVQ_FLAG_ZERO_CLAMPED / KVQ_FLAG_NONFINITE
+};
+
+// Quantizes 8 channels held by this lane; the group is the `tpg` adjacent
+// lanes (tpg = g / 8, a power of two <= 32, groups aligned to tpg lanes).
+// Every lane of the warp must call it (the group min/max uses shuffles).
+template <int BITS>
+__device__ __forceinline__ Quant8 quantize8(const uint4 v, int tpg) {
+  constexpr int QMAX = (1 << BITS) - 1;
+  const __half* h = reinterpret_cast<const __half*>(&v);
+  float mn = INFINITY, mx = -INFINITY;
+  bool finite = true;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float f = __half2float(h[k]);
+    finite = finite && isfinite(f);
+    mn = fminf(mn, f);
+    mx = fmaxf(mx, f);
+  }
+  for (int o = 1; o < tpg; o <<= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    finite = (__shfl_xor_sync(0xffffffffu, (int)finite, o) != 0) && finite;
+  }
+
+  Quant8 r;
+  r.s = __ushort_as_half(0);
+  r.z = __ushort_as_half(0);
+  r.flags = 0;
+  float sf = 0.f, zf = 0.f;
+  if (!finite) {
+    r.flags |= KVQ_FLAG_NONFINITE;
+  } else {
+    const double range = (double)mx - (double)mn;
+    if (range == 0.0) {
+      r.s = __float2half_rn(mn == 0.f ? 1.f : fabsf(mn));
+    } else {
+      r.s = quant_detail::scale_round_up(range, QMAX);
+    }
+    sf = __half2float(r.s);
+    zf = rintf(__fdiv_rn(-mn, sf));
+    if (fabsf(zf) > 2048.f) {
+      r.flags |= KVQ_FLAG_ZERO_CLAMPED;
+      zf = fminf(fmaxf(zf, -2048.f), 2048.f);
+    }
+    r.z = __int2half_rn((int)zf);
+  }
+  r.w0 = 0;
+  r.w1 = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    uint32_t q = 0;
+    if (finite) {
+      const float tq = rintf(__fdiv_rn(__half2float(h[k]), sf)) + zf;
+      q = (uint32_t)fminf(fmaxf(tq, 0.f), (float)QMAX);
+    }
+    if constexpr (BITS == 4) {
+      r.w0 |= q << (4 * k);  // channel 2m -> low nibble of byte m
+    } else {
+      if (k < 4) r.w0 |= q << (8 * k);
+      else       r.w1 |= q << (8 * (k - 4));
+    }
+  }
+  return r;
+}
+
+}  // namespace kvq

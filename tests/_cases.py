@@ -59,7 +59,9 @@ def logical_rows(arr_np, c: Case, table, b, kvh, L):
     return arr_np[pages, kvh, pos % c.page_size]
 
 
-def run_gpu(c: Case, inp, num_splits=0, repeat=1):
+def run_gpu(c: Case, inp, num_splits=0, repeat=1, fused=False):
+    """fused: the step's token is appended by kvq_append_decode_attn in the
+    same call as the attention instead of a separate kvq_append."""
     import torch
     import quantized_kv_decode_gb300 as K
     dev = "cuda"
@@ -77,13 +79,21 @@ def run_gpu(c: Case, inp, num_splits=0, repeat=1):
     K.kvq_append(cache, torch.from_numpy(inp["k_ctx"]).to(dev), torch.from_numpy(inp["v_ctx"]).to(dev),
                  zeros, status)
     lens = torch.from_numpy(c.lens.astype(np.int32)).to(dev)
-    K.kvq_append(cache, torch.from_numpy(inp["k_new"]).to(dev), torch.from_numpy(inp["v_new"]).to(dev),
-                 lens, status)
+    k_new = torch.from_numpy(inp["k_new"]).to(dev)
+    v_new = torch.from_numpy(inp["v_new"]).to(dev)
+    if not fused:
+        K.kvq_append(cache, k_new, v_new, lens, status)
     q = torch.from_numpy(inp["q"]).to(dev)
     outs = []
     for _ in range(repeat):
-        outs.append(K.kvq_decode_attn(cache, q, lens + 1, Lctx + 1, dev_status=status,
-                                      num_splits=num_splits).cpu().numpy())
+        if fused:
+            o = K.kvq_append_decode_attn(cache, k_new[:, 0].contiguous(), v_new[:, 0].contiguous(),
+                                         q, lens, Lctx + 1, dev_status=status,
+                                         num_splits=num_splits)
+        else:
+            o = K.kvq_decode_attn(cache, q, lens + 1, Lctx + 1, dev_status=status,
+                                  num_splits=num_splits)
+        outs.append(o.cpu().numpy())
     torch.cuda.synchronize()
     return dict(out=outs[0], outs=outs, status=int(status.item()), cache=cache, desc=desc)
 
