@@ -223,6 +223,43 @@ kvq_status kvq_append_decode_attn(const kvq_cache_desc* desc, const kvq_cache* c
                                   void* workspace, size_t workspace_bytes,
                                   uint32_t* dev_status, void* stream);
 
+/* Size of the library's own split scratch used by kvq_decode_attn_static_ws. */
+#define KVQ_STATIC_WORKSPACE_BYTES ((size_t)8 << 20)
+
+/*
+ * kvq_decode_attn without a caller workspace: the split partials go to a
+ * static device array of KVQ_STATIC_WORKSPACE_BYTES inside the library.
+ * The pages have no counterpart to this call. It exists for callers that
+ * cannot allocate device memory around a decode call, such as a plugin that
+ * is handed only its input and output buffers, or code whose device
+ * footprint must stay fixed after start-up.
+ *
+ * Arguments, results and status flags are those of kvq_decode_attn. The
+ * workspace is the library's array.
+ *
+ *   - Set-up: the first call on each device, with that device current,
+ *     looks up the array's device address (cudaGetSymbolAddress) and keeps
+ *     it. This may load the library's device code on that device. Make that
+ *     first call before any stream capture.
+ *   - Size limit: when kvq_decode_workspace_size() for the same arguments
+ *     exceeds KVQ_STATIC_WORKSPACE_BYTES, the call returns KVQ_ERR_WORKSPACE
+ *     before any launch. Pass a smaller num_splits, or use kvq_decode_attn.
+ *   - Allocation: none. No cudaMalloc, no cudaFree, no allocating library
+ *     routine.
+ *   - Initial contents: nothing in the array has to start at zero. Each
+ *     call writes every partial it reads.
+ *   - Concurrency: one array serves every call on a device. Calls whose
+ *     kernels can overlap on the GPU race on it and give wrong results. That
+ *     covers calls on different streams without ordering between them, and
+ *     calls from several host threads. Calls on one stream are safe.
+ */
+kvq_status kvq_decode_attn_static_ws(const kvq_cache_desc* desc, const kvq_cache* cache,
+                                     int32_t batch, int32_t num_q_heads,
+                                     const uint16_t* q, const int32_t* seq_lens,
+                                     int32_t max_seq_len, int32_t num_splits,
+                                     float softmax_scale, uint16_t* out,
+                                     uint32_t* dev_status, void* stream);
+
 /* Static, human-readable name of a status code. */
 const char* kvq_status_string(kvq_status status);
 

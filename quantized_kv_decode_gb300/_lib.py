@@ -81,6 +81,9 @@ SIGNATURES = {
                                          c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_int32,
                                          c_int32, c_float, c_void_p, c_void_p, c_size_t, c_void_p,
                                          c_void_p]),
+    "kvq_decode_attn_static_ws": (c_int32, [POINTER(kvq_cache_desc), POINTER(kvq_cache), c_int32,
+                                            c_int32, c_void_p, c_void_p, c_int32, c_int32,
+                                            c_float, c_void_p, c_void_p, c_void_p]),
     "kvq_status_string": (ctypes.c_char_p, [c_int32]),
 }
 

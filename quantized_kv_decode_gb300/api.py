@@ -188,5 +188,25 @@ def kvq_append_decode_attn(cache: KVCache, k_new: torch.Tensor, v_new: torch.Ten
     return out
 
 
+def kvq_decode_attn_static_ws(cache: KVCache, q: torch.Tensor, seq_lens: torch.Tensor,
+                              max_seq_len: int, out: torch.Tensor,
+                              dev_status: torch.Tensor | None = None, num_splits: int = 0,
+                              softmax_scale: float = 0.0, stream=None) -> torch.Tensor:
+    """kvq_decode_attn with the library's static split scratch instead of a
+    workspace; allocates nothing, so `out` must be given.  Calls that can
+    overlap on the GPU share that scratch and race."""
+    _need(q, torch.float16, "q", 3)
+    _need(seq_lens, torch.int32, "seq_lens", 1)
+    _need(out, torch.float16, "out", 3)
+    B, Hq, D = q.shape
+    if D != cache.desc.head_dim or seq_lens.numel() != B or out.shape != q.shape:
+        raise ValueError("shape does not match the cache descriptor")
+    st = _lib.lib().kvq_decode_attn_static_ws(
+        byref(cache.desc), byref(cache.ptrs), B, Hq, _ptr(q), _ptr(seq_lens), int(max_seq_len),
+        int(num_splits), float(softmax_scale), _ptr(out), _ptr(dev_status), _stream(stream))
+    _lib.check(st, "kvq_decode_attn_static_ws")
+    return out
+
+
 def default_scale(head_dim: int) -> float:
     return 1.0 / math.sqrt(head_dim)
