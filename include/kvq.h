@@ -206,13 +206,14 @@ kvq_status kvq_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache,
  *   the rest         as for kvq_decode_attn (same workspace size for the same
  *                    batch, num_q_heads, max_seq_len and num_splits).
  *
- * Cache contents, out and the status flags are those of kvq_append (num_new =
- * 1) followed by kvq_decode_attn: the codes, scales and zero-points written
- * are bit-identical, and so is out.  For bits 4 and 8 with at most 8 query
- * heads per KV head this is one kernel launch (plus the merge when split):
- * the thread block that owns the new position quantizes it, stores it, and
- * uses it from shared memory.  Other shapes run the two kernels in sequence.
- * Lengths are not modified.
+ * Cache contents and status flags are those of kvq_append (num_new = 1)
+ * followed by kvq_decode_attn: the codes, scales and zero-points written are
+ * bit-identical.  out is the same attention; it can differ from the two-call
+ * result in fp32 rounding.  For bits 4 and 8 with at most 8 query heads per
+ * KV head this is one kernel launch (plus the merge when split): the thread
+ * block that owns the new position quantizes the token, stores it, and adds
+ * its dequantized K/V to the attention directly.  Other shapes run the two
+ * kernels in sequence.  Lengths are not modified.
  */
 kvq_status kvq_append_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache,
                                   int32_t batch, int32_t num_q_heads,

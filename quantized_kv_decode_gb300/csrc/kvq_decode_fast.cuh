@@ -6,26 +6,30 @@
 // group-wise codes and dequantized x_hat = (q - z) * s in registers
 // ("What actually happens when you quantize a KV cache", sections 3-4 and 6).
 //
-// Structure (one CTA per (split, KV head, sequence); kFastWarps warps):
+// Structure (one CTA per (split, KV head, sequence); kWarps warps):
 //  * Each warp streams its own 32-token tiles through a private cp.async
 //    pipeline (16-byte chunks, zero-filled past the end of the sequence or
-//    for unmapped pages) into shared memory whose code rows are padded by
-//    16 bytes, which makes every ldmatrix below free of bank conflicts.
+//    for unmapped pages) into shared memory whose code rows are XOR-swizzled
+//    by 16-byte chunk, which makes every ldmatrix below free of bank
+//    conflicts.
 //  * Scores, mma.m16n8k16 (fp16 in, fp32 accumulate): A = q, one row per
 //    (group, head) pair, holding that head's channels of that group only;
-//    B = the raw codes of 8 tokens (integers 0..2^b-1, exact in fp16),
-//    converted from packed nibbles/bytes with two LOP3 + one HSUB2/HFMA2 per
-//    code pair.  Row (g, h) of the accumulator is sum_{d in g} q_h[d] c[d];
-//    the epilogue forms s_g (sum - z_g sum_{d in g} q_h[d]) in fp32 and adds
-//    the groups with warp shuffles.
+//    B = the codes of 8 tokens as fp16 1024 + c (one LOP3 per code pair; the
+//    1024 offset is removed exactly by starting the accumulator at
+//    -1024 * sum(A row)).  Row (g, h) of the accumulator is
+//    sum_{d in g} q_h[d] c[d]; the epilogue forms s_g (sum - z_g sum_{d in g}
+//    q_h[d]) in fp32 and adds the groups with warp shuffles.
 //  * Online softmax per 32-token tile (log2 domain), rescaling only when a
-//    running maximum grows.
+//    head's tile maximum exceeds its reference maximum by kSlack.
 //  * Weighted V, mma.m16n8k16: A = V codes transposed (ldmatrix.trans puts
 //    two tokens of one channel in each register), B = p * s_g per token and
-//    group (fp16); the zero-points enter through one extra mma per group
+//    group (fp16); the zero-points enter through one extra mma per n-tile
 //    whose A rows hold z_g per token, subtracted once at the end.
 //  * The warps' (m, l, o) are merged in shared memory; the CTA writes the
 //    final row (one split) or its partial for the merge kernel.
+//  * Fused append (lens_before set): the CTA holding the new position
+//    quantizes the new K/V in one warp, stores them, and merges the token as
+//    one more partial; its tiles stop before that position.
 #pragma once
 
 #include "kvq_quant.cuh"
@@ -72,6 +76,7 @@ struct Cfg {
   static_assert(GSZ % DPC == 0, "a 16-byte chunk must lie inside one group");
   static_assert(NG * GP <= 16, "groups x padded heads must fit 16 rows");
   static_assert(HDRB == 4 || HDRB == 8 || HDRB == 16, "header row size");
+  static_assert(GP * (D + 2) * 4 <= WARP_BYTES, "the CTA merge reuses the pipeline region");
 
   // Shared-memory byte offset of 16-byte chunk c of token row t: chunk slots
   // are XOR-swizzled by the row's position so that the 8 rows an ldmatrix
@@ -242,11 +247,13 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
   if (p.splits > 1 && t0 >= L) return;  // the merge reads splits < ceil(L / chunk) only
 
   // shared memory: [q fp16 GP x D][per warp: stages, header scratch][tile
-  // masks][the appended token: K codes, V codes, 4 header rows (fused only)]
+  // masks][the appended token's partial: v_hat fp32 [D], scores fp32 [GP]]
   __half* q_s = reinterpret_cast<__half*>(smem);
   uint8_t* pipe = smem + ((GP * D * 2 + 127) / 128) * 128;
   uint32_t* mask_s = reinterpret_cast<uint32_t*>(pipe + kWarps * C::WARP_BYTES);
-  uint8_t* newtok = pipe + kWarps * C::WARP_BYTES + ((kWarps * C::STAGES * 4 + 15) / 16) * 16;
+  float* tok_v = reinterpret_cast<float*>(pipe + kWarps * C::WARP_BYTES +
+                                         ((kWarps * C::STAGES * 4 + 15) / 16) * 16);
+  float* tok_s = tok_v + D;
   uint8_t* wpipe = pipe + warp * C::WARP_BYTES;
   // header scratch buffer `buf` (0/1): K (s*scale, z) [NG][KROW], V scale
   // [NG][VROW], V zero [NG][VROW], token mask [kTT]
@@ -262,16 +269,15 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
 
   __syncthreads();
 
-  // Fused append: the warp whose tile holds the new position quantizes the
-  // new K and V vectors (the quantize8 the append kernel runs), stores them
-  // to the cache and keeps them in shared memory, then copies them into its
-  // stage when that tile arrives.  Cache reads of this launch never depend on
-  // the cache write, so nothing orders them.
+  // Fused append: in the CTA whose range holds the new position, the tiles
+  // stop short of it.  One warp quantizes the new K and V vectors (the
+  // quantize8 the append kernel runs), stores them to the cache, and turns
+  // the dequantized token into a one-token partial (score per head, weight
+  // 1, value v_hat) that the CTA merge adds to the warps' partials.  No read
+  // of this launch touches the new row, so the store needs no ordering.
   const int pos_new = L - 1;
   const bool owner_cta = p.lens_before != nullptr && L > 0 && pos_new >= t0 && pos_new < t1;
-  const int new_tile = owner_cta ? (pos_new - t0) / kTT : -1;  // tile index within the CTA
-  const bool owner = owner_cta && (new_tile % kWarps) == warp;  // warp-uniform
-  const int new_it = new_tile / kWarps;                          // ... within the warp's tiles
+  const int t_end = owner_cta ? t1 - 1 : t1;  // tiles cover [t0, t_end)
 
   // ---- score-mma A fragments: row r <-> (group r / GP, head r % GP) ----
   const int g_lo = rho / GP, h_row = rho % GP;
@@ -342,7 +348,9 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
   float m_ref = -INFINITY, l_run = 0.f;
 
   // ---- this warp's tiles ----
-  const int ntiles = (t1 > t0) ? (t1 - t0 + kTT - 1) / kTT : 0;
+  const int ntiles = (t_end > t0) ? (t_end - t0 + kTT - 1) / kTT : 0;
+  // the appending warp: one with the fewest tiles
+  const bool owner = owner_cta && warp == ntiles % kWarps;  // warp-uniform
   const int nmine = (ntiles > warp) ? (ntiles - warp + kWarps - 1) / kWarps : 0;
   const uint8_t* kc_g = p.codes[0];
   const uint8_t* vc_g = p.codes[1];
@@ -360,7 +368,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
     bool unmapped = false;
     if (it < nmine) {
       const int start = t0 + (warp + it * kWarps) * kTT;
-      const int n = min(kTT, t1 - start);
+      const int n = min(kTT, t_end - start);
       long long row = -1;  // this lane's token
       const uint32_t kc_s = wpipe_s + stage * C::STAGE, vc_s = kc_s + C::CODE_TILE;
       const uint32_t hd_s = vc_s + C::CODE_TILE;
@@ -611,35 +619,12 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
     }
   };
 
-  // fused append: copy the new token into the stage of the tile that holds it
-  auto patch_new = [&](int it_tile, int stg) {
-    if (!owner || it_tile != new_it) return;  // warp-uniform
-    const int r = pos_new - (t0 + new_tile * kTT);
-    uint8_t* st = wpipe + stg * C::STAGE;
-    if (lane < C::CHUNKS) {
-      *reinterpret_cast<uint4*>(st + C::at(r, lane)) =
-          *reinterpret_cast<const uint4*>(newtok + lane * 16);
-    } else if (lane < 2 * C::CHUNKS) {
-      const int c = lane - C::CHUNKS;
-      *reinterpret_cast<uint4*>(st + C::CODE_TILE + C::at(r, c)) =
-          *reinterpret_cast<const uint4*>(newtok + C::ROWB + c * 16);
-    } else if (lane < 2 * C::CHUNKS + 4) {
-      const int a = lane - 2 * C::CHUNKS;  // K scale, K zero, V scale, V zero
-      uint8_t* dst = st + 2 * C::CODE_TILE + a * C::HDR_TILE + r * C::HDRB;
-      const uint8_t* src = newtok + 2 * C::ROWB + a * C::HDRB;
-      if constexpr (C::HDRB == 4) *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(src);
-      else if constexpr (C::HDRB == 8) *reinterpret_cast<uint2*>(dst) = *reinterpret_cast<const uint2*>(src);
-      else *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
-    }
-    __syncwarp();
-  };
-
   // ---- software-pipelined loop: tile i+1's scores overlap tile i's values ----
   // Tile k lives in stage k % STAGES; one commit group per tile.
 #pragma unroll
   for (int s2 = 0; s2 < C::STAGES; ++s2) bt_bad |= issue(s2);
 
-  // fused append (owner warp only), after its first loads are in flight
+  // fused append (one warp of the owning CTA), after its first loads are in flight
   if (owner) {
     constexpr int CHV = D / 8;          // 8-channel chunks per vector
     const int which = lane / CHV;       // 0: K, 1: V, 2+: idle lanes
@@ -650,39 +635,48 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
     if (which < 2)
       v = __ldg(reinterpret_cast<const uint4*>(p.new_kv[which] + ((long long)b * geo.Hkv + kvh) * D) + ch);
     const Quant8 qz = quantize8<BITS>(v, C::GSZ / 8);
-    if (which < 2) {
-      constexpr int CB = BITS;          // code bytes per 8 channels
-      uint8_t* gcodes = const_cast<uint8_t*>(p.codes[which]);
-      if constexpr (BITS == 4) {
-        *reinterpret_cast<uint32_t*>(newtok + which * C::ROWB + ch * CB) = qz.w0;
-        if (nrow >= 0) *reinterpret_cast<uint32_t*>(gcodes + nrow * C::ROWB + ch * CB) = qz.w0;
-      } else {
-        *reinterpret_cast<uint2*>(newtok + which * C::ROWB + ch * CB) = make_uint2(qz.w0, qz.w1);
-        if (nrow >= 0)
-          *reinterpret_cast<uint2*>(gcodes + nrow * C::ROWB + ch * CB) = make_uint2(qz.w0, qz.w1);
-      }
-      const int tpg = C::GSZ / 8;
-      if (ch % tpg == 0) {
-        const int g = ch / tpg;
-        __half* hs = reinterpret_cast<__half*>(newtok + 2 * C::ROWB + (2 * which) * C::HDRB);
-        __half* hz = reinterpret_cast<__half*>(newtok + 2 * C::ROWB + (2 * which + 1) * C::HDRB);
-        hs[g] = qz.s;
-        hz[g] = qz.z;
-        if (nrow >= 0) {
-          const_cast<__half*>(p.scale[which])[nrow * NG + g] = qz.s;
-          const_cast<__half*>(p.zero[which])[nrow * NG + g] = qz.z;
-        }
-        if (qz.flags && p.status) atomicOr(p.status, qz.flags);
+    if (which < 2 && nrow >= 0) {
+      uint8_t* gcodes = const_cast<uint8_t*>(p.codes[which]) + nrow * C::ROWB + ch * BITS;
+      if constexpr (BITS == 4) *reinterpret_cast<uint32_t*>(gcodes) = qz.w0;
+      else *reinterpret_cast<uint2*>(gcodes) = make_uint2(qz.w0, qz.w1);
+      if (ch % (C::GSZ / 8) == 0) {
+        const int g = ch / (C::GSZ / 8);
+        const_cast<__half*>(p.scale[which])[nrow * NG + g] = qz.s;
+        const_cast<__half*>(p.zero[which])[nrow * NG + g] = qz.z;
       }
     }
-    __syncwarp();
+    if (which < 2 && ch % (C::GSZ / 8) == 0 && qz.flags && p.status) atomicOr(p.status, qz.flags);
+    // dequantized channels of this lane: (code - z) * s, exact in fp32
+    const float sf = __half2float(qz.s), zf = __half2float(qz.z);
+    float xh[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t code = BITS == 4 ? (qz.w0 >> (4 * k)) & 0xFu
+                                      : ((k < 4 ? qz.w0 : qz.w1) >> (8 * (k & 3))) & 0xFFu;
+      xh[k] = ((float)code - zf) * sf;
+    }
+    if (which == 1) {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) tok_v[ch * 8 + k] = xh[k];
+    }
+    // scores q_h . k_hat over the K lanes (lanes 0 .. CHV-1), log2 units
+#pragma unroll
+    for (int h = 0; h < GP; ++h) {
+      float part = 0.f;
+      if (which == 0 && h < G) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) part = fmaf(__half2float(q_s[h * D + ch * 8 + k]), xh[k], part);
+      }
+#pragma unroll
+      for (int o2 = 1; o2 < CHV; o2 <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o2);
+      if (lane == 0) tok_s[h] = h < G ? part * p.scale_log2 : -INFINITY;
+    }
   }
 
   uint32_t pp[4] = {0u, 0u, 0u, 0u};
   if (nmine > 0) {
     cp_async_wait<C::STAGES - 1>();  // tile 0
     __syncwarp();
-    patch_new(0, 0);
     const unsigned bad0 = mask_s[warp * C::STAGES];
     header(0, 0, bad0);
     __syncwarp();
@@ -697,7 +691,6 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
     float scn[4][2];
     cp_async_wait<C::STAGES - 2>();  // tile it+1
     __syncwarp();
-    patch_new(it + 1, nstage);
     const unsigned badn = mask_s[warp * C::STAGES + nstage];
     header(nstage, (it + 1) & 1, badn);
     __syncwarp();
@@ -753,6 +746,8 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
     float M = -INFINITY;
 #pragma unroll
     for (int w2 = 0; w2 < kWarps; ++w2) M = fmaxf(M, ml[(w2 * GP + h) * 2]);
+    const float ms = owner_cta ? tok_s[h] : -INFINITY;  // the appended token's partial
+    M = fmaxf(M, ms);
     float num = 0.f, den = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
@@ -760,6 +755,11 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
         const float f = exp2f(ml[(w2 * GP + h) * 2] - M);
         num = fmaf(f, red[(w2 * GP + h) * D + d], num);
         den = fmaf(f, ml[(w2 * GP + h) * 2 + 1], den);
+      }
+      if (owner_cta) {
+        const float f = exp2f(ms - M);
+        num = fmaf(f, tok_v[d], num);
+        den += f;
       }
     }
     if (p.splits == 1) {
@@ -780,7 +780,7 @@ size_t fast_smem_bytes() {
   using C = Cfg<BITS, D, NG, GP>;
   const size_t pipe = (size_t)kWarps * C::WARP_BYTES;
   const size_t masks = ((kWarps * C::STAGES * 4 + 15) / 16) * 16;
-  const size_t newtok = 2 * C::ROWB + 4 * C::HDRB;
+  const size_t newtok = (D + GP) * sizeof(float);
   const size_t merge = (size_t)kWarps * GP * (D + 2) * sizeof(float);
   return ((GP * D * 2 + 127) / 128) * 128 + (pipe > merge ? pipe : merge) + masks + newtok;
 }
