@@ -39,7 +39,8 @@ Readings of points the pages leave open (each is listed in the design doc):
   * a group holding inf/NaN is stored as s = z = 0, codes 0, flagged NONFINITE;
   * decode attention over an empty cache returns zeros.
 
-Pins (tests/test_oracle_pins.py): the worked 8-value INT4 group and the
+Pins (tests/test_oracle_pins.py): the worked 8-value INT4 group, its
+symmetric counterpart and the absmax level count of [SMU], the
 outlier group of [KVQ] section 3, the byte accounting of [KVQ] section 5,
 the FP16 cache sizes of [KVQ]/[QIO]/[GIB]/[CS336]/[SMU], the naive-vs-cached
 work counters of [QIO], brute-force equality of cached decode and full
@@ -141,6 +142,61 @@ def quantize_groups(x16: np.ndarray, bits: int, group_size: int) -> dict:
         "codes": q.astype(np.uint8).reshape(x16.shape),
         "scale": s16,
         "zero": z.astype(np.float16),
+        "flags": flags,
+    }
+
+
+def quantize_groups_symmetric(x16: np.ndarray, bits: int, group_size: int) -> dict:
+    """Group-wise symmetric (absmax) uniform quantization of fp16 vectors.
+
+    [KVQ] section 3, "Why asymmetric? A concrete comparison", sets the
+    asymmetric grid against a zero-centred one whose half-width is the larger
+    of |min| and |max| (s = 0.87 / 7 for the worked group).  [SMU]
+    "Quantization: rounding the weights" writes that quantizer out for any
+    bit width:
+        qmax  = 2^(b-1) - 1
+        scale = max |x| / qmax            (one scale per group, stored as fp16)
+        q     = clamp(round(x / scale), -qmax - 1, qmax)
+        x_hat = q * scale
+
+    Readings (listed in the design doc): the fp16 scale is rounded up (as in the
+    asymmetric quantizer) so that no element is clipped; an all-zero group
+    takes s = 1 (the page's clamp_min(1e-12) scale is not an fp16 value);
+    the signed q is stored as the code q + 2^(b-1), which makes the grid the
+    asymmetric one with the fixed zero-point z = 2^(b-1); a group holding
+    inf/NaN is stored as s = 0, code 2^(b-1) and flagged NONFINITE.
+
+    Returns the dict of quantize_groups; "zero" holds 2^(b-1) everywhere so
+    that dequantize() applies unchanged.
+    """
+    x16 = np.asarray(x16, dtype=np.float16)
+    D = x16.shape[-1]
+    if D % group_size:
+        raise ValueError("group_size must divide the last axis")
+    if not 2 <= bits <= 8:
+        raise ValueError("bits must be in [2, 8]")
+    ng = D // group_size
+    qmax = (1 << (bits - 1)) - 1
+    offset = 1 << (bits - 1)
+    xg = x16.reshape(x16.shape[:-1] + (ng, group_size)).astype(np.float64)
+
+    finite = np.isfinite(xg).all(axis=-1)
+    xg_safe = np.where(finite[..., None], xg, 0.0)
+    a = np.abs(xg_safe).max(axis=-1)                  # exact: |fp16| is an fp16 value
+    s16 = np.where(a == 0.0, np.float16(1.0), fp16_round_up(a / qmax)).astype(np.float16)
+
+    s32 = s16.astype(np.float32)
+    # the integer decision in fp32, as in quantize_groups
+    t = np.rint(xg_safe.astype(np.float32) / s32[..., None]).astype(np.float64)
+    q = np.clip(t, -qmax - 1, qmax)
+    q = np.where(finite[..., None], q, 0.0)
+
+    flags = np.where(finite, 0, NONFINITE).astype(np.uint32)
+    s16 = np.where(finite, s16, np.float16(0.0)).astype(np.float16)
+    return {
+        "codes": (q + offset).astype(np.uint8).reshape(x16.shape),
+        "scale": s16,
+        "zero": np.full(s16.shape, offset, dtype=np.float16),
         "flags": flags,
     }
 
@@ -295,14 +351,17 @@ def decode_attention(q16: np.ndarray, k_hat: np.ndarray, v_hat: np.ndarray,
 # ---------------------------------------------------------------------------
 
 def kv_cache_bytes(layers: int, kv_heads: int, head_dim: int, tokens: int,
-                   bits: int, group_size: int | None = None) -> int:
+                   bits: int, group_size: int | None = None,
+                   symmetric: bool = False) -> int:
     """Bytes of K+V cache for ``tokens`` tokens of one sequence.
 
     FP16 (bits == 16): 2 * layers * kv_heads * head_dim * 2 bytes per token.
     INT4/INT8: packed codes head_dim*bits/8 bytes plus a 4-byte header
-    (fp16 scale + fp16 zero) per group of ``group_size`` channels.
+    (fp16 scale + fp16 zero) per group of ``group_size`` channels; a
+    symmetric group stores the 2-byte scale only ([SMU] keeps a single
+    16-bit scale for each group of 32 values).
     """
     per_vector = head_dim * bits // 8
     if bits != 16:
-        per_vector += 4 * (head_dim // group_size)
+        per_vector += (2 if symmetric else 4) * (head_dim // group_size)
     return 2 * layers * kv_heads * per_vector * tokens

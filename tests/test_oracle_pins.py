@@ -91,6 +91,115 @@ def test_asymmetric_step_finer_than_symmetric(golden):
 
 
 # ---------------------------------------------------------------------------
+# Symmetric (absmax) quantizer: "What actually happens when you quantize a KV
+# cache", section 3 comparison; "Serving many users at once", "Quantization:
+# rounding the weights"
+# ---------------------------------------------------------------------------
+
+def test_symmetric_worked_group(golden):
+    """The worked group under the symmetric grid: s = max(|min|, |max|) / 7 =
+    0.124 as printed, and the asymmetric step is 38 % finer."""
+    kv, _ = golden("kvq_symmetric_vs_asymmetric.txt")
+    _, rows = golden("kvq_worked_group_int4.txt")
+    x = f16([float(r[1]) for r in rows])
+    sym = O.quantize_groups_symmetric(x, 4, 8)
+    s = float(sym["scale"][0])
+    assert abs(s - kv["symmetric_scale"]) < 5e-4
+    a = float(np.abs(x.astype(np.float64)).max())
+    assert a / 7 <= s <= float(np.nextafter(np.float16(a / 7), np.float16(np.inf))) + 1e-12
+    s_asym = float(O.quantize_groups(x, 4, 8)["scale"][0])
+    assert abs(1 - s_asym / s - kv["finer_fraction"]) < 0.01
+    # c2 = 0.87 is the absmax: it lands on the top level 7 (code 15)
+    assert int(sym["codes"][2]) == 15
+    assert float(O.dequantize(sym["codes"], sym["scale"], sym["zero"], 8)[2]) == 7 * s
+
+
+def test_symmetric_levels_match_page(golden):
+    """2^b levels from -2^(b-1) to 2^(b-1)-1 (the page lists -2, -1, 0, 1 for
+    2 bits); qmax = 127 / 7 for 8 / 4 bits; every decoded value is a level
+    times the group's scale."""
+    kv, rows = golden("smu_absmax_levels.txt")
+    assert kv["qmax_8"] == (1 << 7) - 1 and kv["qmax_4"] == (1 << 3) - 1
+    rng = np.random.default_rng(3)
+    for r in rows:
+        bits, levels, lo, hi = int(r[1]), int(r[2]), int(r[3]), int(r[4])
+        assert levels == hi - lo + 1 == 2 ** bits
+        x = f16(rng.standard_normal((64, 32)) * rng.uniform(0.01, 20, (64, 1)))
+        res = O.quantize_groups_symmetric(x, bits, 32)
+        q = res["codes"].astype(np.int64) - (1 << (bits - 1))
+        assert q.min() >= lo and q.max() <= hi
+        # the scale is rounded up, so no element is clipped: |q| <= qmax
+        assert np.abs(q).max() <= hi
+        xh = O.dequantize(res["codes"], res["scale"], res["zero"], 32)
+        s = res["scale"].astype(np.float64)
+        assert np.array_equal(xh, q.reshape(64, 1, 32).astype(np.float64).reshape(64, 32) *
+                              np.repeat(s, 32, axis=-1))
+
+
+def test_symmetric_scale_overhead(golden):
+    """One 2-byte scale per group and no zero-point: 16 bits per 32 values on
+    top of the codes, as the page states."""
+    kv, _ = golden("smu_absmax_levels.txt")
+    for bits in (4, 8):
+        per_tok = O.kv_cache_bytes(1, 1, 128, 1, bits, kv["scale_group"], symmetric=True)
+        codes = 2 * 128 * bits // 8
+        assert (per_tok - codes) * 8 == 2 * (128 // kv["scale_group"]) * kv["scale_bits"]
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_symmetric_nearest_level_brute_force(bits):
+    """Each code is the level nearest x / s (exhaustive over all 2^b levels,
+    ties to even), decided on the fp32 quotient."""
+    rng = np.random.default_rng(bits)
+    x = f16(rng.standard_normal((200, 8)) * rng.uniform(0.05, 5, (200, 1)))
+    res = O.quantize_groups_symmetric(x, bits, 8)
+    half = 1 << (bits - 1)
+    levels = np.arange(-half, half, dtype=np.float64)
+    s32 = res["scale"].astype(np.float32)
+    for i in range(x.shape[0]):
+        t = (x[i].astype(np.float32) / s32[i, 0]).astype(np.float64)
+        for k in range(8):
+            d = np.abs(levels - t[k])
+            best = levels[d == d.min()]
+            want = best[0] if len(best) == 1 else best[np.abs(best % 2) == 0][0]
+            assert int(res["codes"][i, k]) - half == int(want)
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_symmetric_is_odd_and_error_bounded(bits):
+    """q(-x) = -q(x) (the grid is centred at zero; rint is symmetric), and
+    |x - x_hat| <= s/2 (plus the fp32 quotient's rounding) for every element."""
+    rng = np.random.default_rng(10 + bits)
+    x = f16(rng.standard_normal((300, 64)) * rng.uniform(0.001, 100, (300, 1)))
+    half = 1 << (bits - 1)
+    a = O.quantize_groups_symmetric(x, bits, 32)
+    b = O.quantize_groups_symmetric(-x, bits, 32)
+    assert np.array_equal(a["scale"], b["scale"])
+    assert np.array_equal(a["codes"].astype(np.int64) - half, -(b["codes"].astype(np.int64) - half))
+    xh = O.dequantize(a["codes"], a["scale"], a["zero"], 32)
+    s = np.repeat(a["scale"].astype(np.float64), 32, axis=-1)
+    err = np.abs(xh - x.astype(np.float64))
+    assert (err <= s / 2 * (1 + 1e-6) + 1e-12).all()
+
+
+def test_symmetric_special_groups():
+    """All-zero group: s = 1, codes at the offset, decodes to 0.  A group with
+    inf/NaN: s = 0, flagged, decodes to 0.  Other groups are unaffected."""
+    x = np.zeros((3, 16), dtype=np.float16)
+    x[1, :] = np.float16(0.5)
+    x[2, 3] = np.float16(np.inf)
+    x[2, 9] = np.float16(1.0)
+    res = O.quantize_groups_symmetric(x, 4, 8)
+    assert float(res["scale"][0, 0]) == 1.0 and (res["codes"][0] == 8).all()
+    assert res["flags"][2, 0] == O.NONFINITE and float(res["scale"][2, 0]) == 0.0
+    assert res["flags"][2, 1] == 0
+    xh = O.dequantize(res["codes"], res["scale"], res["zero"], 8)
+    assert (xh[0] == 0).all() and (xh[2, :8] == 0).all()
+    assert np.allclose(xh[1], 0.5, atol=float(res["scale"][1, 0]) / 2)
+    assert abs(xh[2, 9] - 1.0) <= float(res["scale"][2, 1]) / 2 and np.isfinite(xh[2, 8:]).all()
+
+
+# ---------------------------------------------------------------------------
 # Closed forms and exact arithmetic
 # ---------------------------------------------------------------------------
 
