@@ -77,12 +77,12 @@ def workload_config(w, bits, layers):
     }
 
 
-def decode_bytes(w, bits, rows, fused=True):
+def decode_bytes(w, bits, rows, fused=True, symmetric=False):
     """Algorithmic bytes of one step call.  Decode alone: `rows` cache rows
     (codes + scale/zero, K and V) read, q read, out written.  Fused append:
     rows - 1 cache rows read, the new row written, the new fp16 K/V read."""
     D = w.head_dim
-    per_row = D * bits // 8 + (0 if bits == 16 else 4 * (D // w.group_size))
+    per_row = D * bits // 8 + (0 if bits == 16 else (2 if symmetric else 4) * (D // w.group_size))
     kv = 2 * w.batch * w.num_kv_heads * rows * per_row
     if fused:
         kv += 2 * w.batch * w.num_kv_heads * D * 2
@@ -221,13 +221,13 @@ def run_reference(args):
 # GPU arm
 # ---------------------------------------------------------------------------
 
-def build_layers(w, bits, layers, dev, seed, torch, K, synth):
+def build_layers(w, bits, layers, dev, seed, torch, K, synth, symmetric=False):
     """Populate one cache per layer with device-drawn fp16 K/V; per-layer
     step inputs q, k_new, v_new."""
     import numpy as np
     cap = ((w.ctx[0] + 1 + 15) // 16) * 16
     desc = K.make_desc(bits, w.group_size if bits != 16 else 0, w.num_kv_heads, w.head_dim,
-                       K.KVQ_DENSE, cap)
+                       K.KVQ_DENSE, cap, symmetric=symmetric)
     zeros = torch.zeros(w.batch, dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     caches, qs, kns, vns, host_slices = [], [], [], [], None
@@ -286,9 +286,16 @@ def run_gpu_arm(args):
         return reduce_max_over_ranks(x, world, dev)
 
     results = {}
-    for fmt in ((bits, 16) if args.fp16_comparator else (bits,)):
+    # formats: the headline asymmetric cache first, then the comparators
+    formats = [(bits, False)]
+    if not args.no_symmetric:
+        formats.append((bits, True))
+    if args.fp16_comparator:
+        formats.append((16, False))
+    for fmt, sym in formats:
         desc, caches, qs, kns, vns, host_slices = build_layers(
-            w, fmt, layers, dev, seed, torch, K, synth)
+            w, fmt, layers, dev, seed, torch, K, synth, symmetric=sym)
+        key = "sym" if sym else fmt
         stream = torch.cuda.Stream(device=dev)
         lens_before = torch.full((w.batch,), w.ctx[0], dtype=torch.int32, device=dev)
         lens = lens_before + 1
@@ -330,7 +337,7 @@ def run_gpu_arm(args):
         barrier()
 
         clocks = ClockSampler(dev.index)
-        if fmt == bits:
+        if key == bits:
             clocks.start()
             time.sleep(0.3)
         e0 = torch.cuda.Event(enable_timing=True)
@@ -343,7 +350,7 @@ def run_gpu_arm(args):
         torch.cuda.synchronize()
         barrier()
         ms_total = max_over_ranks(e0.elapsed_time(e1))
-        clk = clocks.stop() if fmt == bits else None
+        clk = clocks.stop() if key == bits else None
 
         # per-call duration of the step call (kernel + split merge): a graph of
         # every layer's call back to back, timed with events on its stream
@@ -401,11 +408,11 @@ def run_gpu_arm(args):
         e2e_ms = max_over_ranks(f0.elapsed_time(f1))
 
         tokens = w.batch * layers * args.steps  # per rank
-        results[fmt] = dict(
+        results[key] = dict(
             value=job_throughput(tokens, world, ms_total), ms_per_step=ms_total / args.steps,
             e2e=job_throughput(tokens, world, e2e_ms), h2d=h2d, d2h=d2h, call_ms=call_ms,
             splits=splits,
-            bytes=decode_bytes(w, fmt, rows, not args.separate_append), clocks=clk,
+            bytes=decode_bytes(w, fmt, rows, not args.separate_append, sym), clocks=clk,
             host_slices=host_slices, out0=outs[0][:1].float().cpu().numpy(),
             launches=args.steps * layers * ((2 if args.separate_append else 1) +
                                             (1 if splits > 1 else 0)))
@@ -439,6 +446,16 @@ def run_gpu_arm(args):
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
     }
+    if "sym" in results:
+        f = results["sym"]
+        line["symmetric_cache"] = {
+            "value": f["value"], "unit": UNIT, "ms_per_step": f["ms_per_step"],
+            "achieved_gbs": f["bytes"] / (f["call_ms"] / 1e3) / 1e9,
+            "frac": f["bytes"] / (f["call_ms"] / 1e3) / 1e9 / peak,
+            "bytes_per_launch": f["bytes"], "avg_launch_us": f["call_ms"] * 1e3,
+            "e2e": f["e2e"], "speedup_vs_asymmetric": f["value"] / r["value"],
+            "what": "the same step over symmetric INT4 g32 caches (2-byte scale per group, "
+                    "no zero-point)"}
     if 16 in results:
         f = results[16]
         line["fp16_cache"] = {
@@ -507,6 +524,8 @@ def main():
     ap.add_argument("--cpu-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fp16-comparator", action="store_true")
+    ap.add_argument("--no-symmetric", action="store_true",
+                    help="skip the symmetric-cache comparator")
     ap.add_argument("--separate-append", action="store_true",
                     help="append and attend in two calls instead of the fused call")
     args = ap.parse_args()

@@ -48,6 +48,7 @@
  *          at offset p % page_size.  Pages may be shared by sequences.
  *   bits == 16 stores the fp16 vectors themselves in the codes arrays
  *   (row_bytes = 2 * head_dim) and uses no scale/zero arrays.
+ *   symmetric == 1 uses no zero arrays (k_zero and v_zero are ignored).
  */
 #ifndef KVQ_H
 #define KVQ_H
@@ -86,6 +87,9 @@ typedef struct {
                                  PAGED: tokens per page (multiple of 8)        */
   int32_t num_pages;          /* PAGED only: pages in the pool                 */
   int32_t max_blocks_per_seq; /* PAGED only: row length of block_table         */
+  int32_t symmetric;          /* 0: asymmetric, fp16 scale + zero per group;
+                                 1: symmetric, fp16 scale only, codes offset
+                                 by 2^(bits-1); must be 0 when bits == 16     */
 } kvq_cache_desc;
 
 typedef struct {              /* all device pointers, caller-owned             */
@@ -102,18 +106,20 @@ typedef struct {              /* all device pointers, caller-owned             *
  * Bytes of K+V cache that `tokens` positions of ONE sequence occupy in one
  * layer: 2 * num_kv_heads * tokens * (row_bytes + 4 * groups), i.e. codes
  * plus a 4-byte fp16 scale+zero header per group ("What actually happens
- * when you quantize a KV cache", section 5; for bits == 16 the header is
- * absent and this is 2 * kv_heads * head_dim * 2 bytes per token, the
- * formula of "Quantization & inference optimisation", "What the cache
- * costs").  Host arithmetic only.  Returns 0 for an invalid descriptor.
+ * when you quantize a KV cache", section 5; a symmetric cache keeps only the
+ * 2-byte scale; for bits == 16 the header is absent and this is
+ * 2 * kv_heads * head_dim * 2 bytes per token, the formula of
+ * "Quantization & inference optimisation", "What the cache costs").  Host
+ * arithmetic only.  Returns 0 for an invalid descriptor.
  */
 size_t kvq_cache_bytes(const kvq_cache_desc* desc, int64_t tokens);
 
 /*
  * Allocation sizes for one layer's cache: *codes_bytes for each of k_codes
  * and v_codes, *header_bytes for each of k_scale, k_zero, v_scale, v_zero
- * (0 when bits == 16).  DENSE sizes cover `batch` sequences of `capacity`
- * slots; PAGED sizes cover num_pages pages (`batch` is ignored).
+ * (0 when bits == 16; a symmetric cache needs no zero arrays).  DENSE sizes
+ * cover `batch` sequences of `capacity` slots; PAGED sizes cover num_pages
+ * pages (`batch` is ignored).
  */
 kvq_status kvq_cache_array_bytes(const kvq_cache_desc* desc, int32_t batch,
                                  size_t* codes_bytes, size_t* header_bytes);
@@ -136,6 +142,14 @@ kvq_status kvq_cache_array_bytes(const kvq_cache_desc* desc, int32_t batch,
  * A position outside the cache (or an unmapped page) flags SEQ_LEN /
  * BLOCK_TABLE and that vector is not written.  Lengths are not modified:
  * the caller passes seq_lens_before + num_new to kvq_decode_attn.
+ *
+ * Symmetric caches (the zero-centred grid that "What actually happens when
+ * you quantize a KV cache", section 3, compares against; the absmax
+ * quantizer of "Serving many users at once", "Quantization: rounding the
+ * weights"): per group a = max |x|; s = fp16 rounded up from
+ * a/(2^(bits-1)-1) (s = 1 when a == 0); q = clamp(round-half-even(x/s),
+ * -2^(bits-1), 2^(bits-1)-1) in fp32, stored as the code q + 2^(bits-1);
+ * x_hat = (code - 2^(bits-1)) * s.  inf/NaN: s = 0, code 2^(bits-1), flagged.
  */
 kvq_status kvq_append(const kvq_cache_desc* desc, const kvq_cache* cache,
                       int32_t batch, int32_t num_new,

@@ -40,6 +40,7 @@ class kvq_cache_desc(Structure):
         ("capacity", c_int32),
         ("num_pages", c_int32),
         ("max_blocks_per_seq", c_int32),
+        ("symmetric", c_int32),
     ]
 
 

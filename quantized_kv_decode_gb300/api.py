@@ -28,9 +28,9 @@ def _stream(stream) -> int | None:
 
 def make_desc(bits: int, group_size: int, num_kv_heads: int, head_dim: int,
               layout: int = KVQ_DENSE, capacity: int = 0, num_pages: int = 0,
-              max_blocks_per_seq: int = 0) -> kvq_cache_desc:
+              max_blocks_per_seq: int = 0, symmetric: bool = False) -> kvq_cache_desc:
     return kvq_cache_desc(bits, group_size, num_kv_heads, head_dim, layout, capacity,
-                          num_pages, max_blocks_per_seq)
+                          num_pages, max_blocks_per_seq, int(bool(symmetric)))
 
 
 def kvq_cache_bytes(desc: kvq_cache_desc, tokens: int) -> int:
@@ -90,7 +90,8 @@ class KVCache:
         else:
             ng = D // desc.group_size
             hdr = lambda: torch.zeros(lead + (ng,), dtype=torch.float16, device=device)
-        return cls(desc, batch, codes(), codes(), hdr(), hdr(), hdr(), hdr(), block_table)
+        zero = (lambda: None) if desc.symmetric else hdr
+        return cls(desc, batch, codes(), codes(), hdr(), zero(), hdr(), zero(), block_table)
 
     @property
     def ptrs(self) -> kvq_cache:

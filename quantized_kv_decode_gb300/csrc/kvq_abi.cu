@@ -27,6 +27,8 @@ kvq_status check_desc(const kvq_cache_desc* d, CacheGeom* g) {
     if (d->group_size < 8 || d->group_size % 8 || d->head_dim % d->group_size)
       return KVQ_ERR_INVALID_ARG;
   }
+  if (d->symmetric != 0 && d->symmetric != 1) return KVQ_ERR_INVALID_ARG;
+  if (d->symmetric && d->bits == 16) return KVQ_ERR_INVALID_ARG;
   if (d->layout == KVQ_DENSE) {
     if (d->capacity <= 0) return KVQ_ERR_INVALID_ARG;
   } else if (d->layout == KVQ_PAGED) {
@@ -47,6 +49,7 @@ kvq_status check_desc(const kvq_cache_desc* d, CacheGeom* g) {
     g->slots = d->capacity;
     g->num_pages = d->layout == KVQ_PAGED ? d->num_pages : 0;
     g->max_blocks = d->layout == KVQ_PAGED ? d->max_blocks_per_seq : 0;
+    g->sym = d->symmetric;
     g->block_table = nullptr;
   }
   // the kernels are built for these head sizes; byte accounting takes any
@@ -58,8 +61,9 @@ kvq_status check_cache(const kvq_cache_desc* d, const kvq_cache* c) {
   if (!c || !c->k_codes || !c->v_codes) return KVQ_ERR_INVALID_ARG;
   if (!aligned(c->k_codes) || !aligned(c->v_codes)) return KVQ_ERR_INVALID_ARG;
   if (d->bits != 16) {
-    if (!c->k_scale || !c->k_zero || !c->v_scale || !c->v_zero) return KVQ_ERR_INVALID_ARG;
-    if (!aligned(c->k_scale) || !aligned(c->k_zero) || !aligned(c->v_scale) || !aligned(c->v_zero))
+    if (!c->k_scale || !c->v_scale || !aligned(c->k_scale) || !aligned(c->v_scale))
+      return KVQ_ERR_INVALID_ARG;
+    if (!d->symmetric && (!c->k_zero || !c->v_zero || !aligned(c->k_zero) || !aligned(c->v_zero)))
       return KVQ_ERR_INVALID_ARG;
   }
   if (d->layout == KVQ_PAGED && (!c->block_table || !aligned(c->block_table)))
@@ -194,7 +198,7 @@ extern "C" {
 size_t kvq_cache_bytes(const kvq_cache_desc* desc, int64_t tokens) {
   CacheGeom g;
   if (check_desc(desc, &g) == KVQ_ERR_INVALID_ARG || tokens < 0) return 0;
-  const int64_t per_vector = g.row_bytes + (g.bits == 16 ? 0 : 4LL * g.ngroups);
+  const int64_t per_vector = g.row_bytes + (g.bits == 16 ? 0 : (g.sym ? 2LL : 4LL) * g.ngroups);
   return (size_t)(2LL * g.Hkv * tokens * per_vector);
 }
 

@@ -12,7 +12,7 @@
 namespace kvq {
 namespace {
 
-template <int BITS>
+template <int BITS, bool SYM>
 __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
   const CacheGeom& c = p.geom;
   const int which = blockIdx.y;  // 0: K, 1: V
@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
     const int sub = ch % tpg;          // this thread's place in its group
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (live) v = __ldg(reinterpret_cast<const uint4*>(src) + ch);
-    const Quant8 qz = quantize8<BITS>(v, tpg);  // every lane: the group uses shuffles
+    const Quant8 qz = quantize8<BITS, SYM>(v, tpg);  // every lane: the group uses shuffles
     if (!live) return;
     if (row < 0) {
       if (ch == 0 && p.status) atomicOr(p.status, flags);
@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
     if (sub == 0) {
       const long long h_idx = row * c.ngroups + ch / tpg;
       p.scale[which][h_idx] = s_h;
-      p.zero[which][h_idx] = z_h;
+      if constexpr (!SYM) p.zero[which][h_idx] = z_h;
       if (flags && p.status) atomicOr(p.status, flags);
     }
   }
@@ -87,10 +87,12 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
   if (n_units == 0) return cudaSuccess;
   const dim3 block(256);
   const dim3 grid((unsigned)((n_units + 255) / 256), 2);
-  switch (c.bits) {
-    case 4:  append_kernel<4><<<grid, block, 0, stream>>>(p); break;
-    case 8:  append_kernel<8><<<grid, block, 0, stream>>>(p); break;
-    default: append_kernel<16><<<grid, block, 0, stream>>>(p); break;
+  switch (c.bits * 2 + (c.sym ? 1 : 0)) {
+    case 8:  append_kernel<4, false><<<grid, block, 0, stream>>>(p); break;
+    case 9:  append_kernel<4, true><<<grid, block, 0, stream>>>(p); break;
+    case 16: append_kernel<8, false><<<grid, block, 0, stream>>>(p); break;
+    case 17: append_kernel<8, true><<<grid, block, 0, stream>>>(p); break;
+    default: append_kernel<16, false><<<grid, block, 0, stream>>>(p); break;
   }
   return cudaGetLastError();
 }

@@ -226,9 +226,11 @@ __device__ __forceinline__ uint32_t pack_halves(__half lo, __half hi) {
 // bounded by 2^kSlack.
 constexpr float kSlack = 4.f;
 
-template <int BITS, int D, int NG, int GP>
+template <int BITS, int D, int NG, int GP, bool SYM>
 __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
     decode_fast_kernel(const DecodeParams p) {
+  // SYM: symmetric caches, no zero arrays; every zero-point is 2^(BITS-1)
+  constexpr unsigned short kSymZero = BITS == 4 ? 0x4800u : 0x5800u;  // fp16 8, 128
   using C = Cfg<BITS, D, NG, GP>;
   extern __shared__ __align__(128) uint8_t smem[];
   const CacheGeom& geo = p.geom;
@@ -408,9 +410,11 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
       const long long hoff = ok ? row * C::HDRB : 0;
       const uint32_t hdst = hd_s + lane * C::HDRB;
       cp_async_small<C::HDRB>(hdst, ks_g + hoff, ok);
-      cp_async_small<C::HDRB>(hdst + C::HDR_TILE, kz_g + hoff, ok);
       cp_async_small<C::HDRB>(hdst + 2 * C::HDR_TILE, vs_g + hoff, ok);
-      cp_async_small<C::HDRB>(hdst + 3 * C::HDR_TILE, vz_g + hoff, ok);
+      if constexpr (!SYM) {
+        cp_async_small<C::HDRB>(hdst + C::HDR_TILE, kz_g + hoff, ok);
+        cp_async_small<C::HDRB>(hdst + 3 * C::HDR_TILE, vz_g + hoff, ok);
+      }
     }
     cp_async_commit();  // one group per slot, empty past the end
     return unmapped;
@@ -423,6 +427,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
     uint32_t r[4][NG / 2];  // K scale, K zero, V scale, V zero: two halves per word
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
+      if (SYM && (a & 1)) continue;  // no zero rows
       const uint8_t* src = hsrc + a * C::HDR_TILE;
       if constexpr (NG == 2) {
         r[a][0] = *reinterpret_cast<const uint32_t*>(src);
@@ -441,11 +446,11 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
     for (int g = 0; g < NG; ++g) {
       const int sh = (g & 1) * 16;
       const unsigned short uk = (unsigned short)(r[0][g / 2] >> sh);
-      const unsigned short uz = (unsigned short)(r[1][g / 2] >> sh);
+      const unsigned short uz = SYM ? kSymZero : (unsigned short)(r[1][g / 2] >> sh);
       ksz[g * C::KROW + lane] = make_float2(__half2float(__ushort_as_half(uk)) * p.scale_log2,
                                             __half2float(__ushort_as_half(uz)));
       vs[g * C::VROW + lane] = (unsigned short)(r[2][g / 2] >> sh);
-      vz[g * C::VROW + lane] = (unsigned short)(r[3][g / 2] >> sh);
+      vz[g * C::VROW + lane] = SYM ? kSymZero : (unsigned short)(r[3][g / 2] >> sh);
     }
     madd_of(buf)[lane] = ((bad >> lane) & 1u) ? -INFINITY : 0.f;
   };
@@ -634,7 +639,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (which < 2)
       v = __ldg(reinterpret_cast<const uint4*>(p.new_kv[which] + ((long long)b * geo.Hkv + kvh) * D) + ch);
-    const Quant8 qz = quantize8<BITS>(v, C::GSZ / 8);
+    const Quant8 qz = quantize8<BITS, SYM>(v, C::GSZ / 8);
     if (which < 2 && nrow >= 0) {
       uint8_t* gcodes = const_cast<uint8_t*>(p.codes[which]) + nrow * C::ROWB + ch * BITS;
       if constexpr (BITS == 4) *reinterpret_cast<uint32_t*>(gcodes) = qz.w0;
@@ -642,7 +647,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
       if (ch % (C::GSZ / 8) == 0) {
         const int g = ch / (C::GSZ / 8);
         const_cast<__half*>(p.scale[which])[nrow * NG + g] = qz.s;
-        const_cast<__half*>(p.zero[which])[nrow * NG + g] = qz.z;
+        if constexpr (!SYM) const_cast<__half*>(p.zero[which])[nrow * NG + g] = qz.z;
       }
     }
     if (which < 2 && ch % (C::GSZ / 8) == 0 && qz.flags && p.status) atomicOr(p.status, qz.flags);
@@ -787,18 +792,18 @@ size_t fast_smem_bytes() {
 
 // Launches the instantiation, or with ctas_per_sm != nullptr only reports
 // how many of its CTAs fit on one SM.
-template <int BITS, int D, int NG, int GP>
+template <int BITS, int D, int NG, int GP, bool SYM>
 cudaError_t launch_fast_inst(const DecodeParams& p, cudaStream_t stream, int* ctas_per_sm) {
   const size_t smem = fast_smem_bytes<BITS, D, NG, GP>();
-  cudaError_t e = cudaFuncSetAttribute(decode_fast_kernel<BITS, D, NG, GP>,
+  cudaError_t e = cudaFuncSetAttribute(decode_fast_kernel<BITS, D, NG, GP, SYM>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   if (ctas_per_sm) {
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        ctas_per_sm, decode_fast_kernel<BITS, D, NG, GP>, kWarps * 32, smem);
+        ctas_per_sm, decode_fast_kernel<BITS, D, NG, GP, SYM>, kWarps * 32, smem);
   }
   const dim3 grid(p.splits, p.geom.Hkv, p.batch);
-  decode_fast_kernel<BITS, D, NG, GP><<<grid, kWarps * 32, smem, stream>>>(p);
+  decode_fast_kernel<BITS, D, NG, GP, SYM><<<grid, kWarps * 32, smem, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -1,0 +1,33 @@
+// Tensor-core decode kernel instantiations for INT4 caches with symmetric codes
+// (no zero arrays; every zero-point is 2^(bits-1)).
+#include "kvq_decode_fast.cuh"
+
+namespace kvq {
+
+template <int D, int NG>
+static cudaError_t by_gp4(const DecodeParams& p, int gp, cudaStream_t s, bool* handled,
+                          int* occ) {
+  constexpr bool SYM = true;
+  *handled = true;
+  switch (gp) {
+    case 1: return fast::launch_fast_inst<4, D, NG, 1, SYM>(p, s, occ);
+    case 2: return fast::launch_fast_inst<4, D, NG, 2, SYM>(p, s, occ);
+    case 4: return fast::launch_fast_inst<4, D, NG, 4, SYM>(p, s, occ);
+    case 8: if constexpr (NG * 8 <= 16) return fast::launch_fast_inst<4, D, NG, 8, SYM>(p, s, occ);
+            break;
+  }
+  *handled = false;
+  return cudaSuccess;
+}
+
+cudaError_t launch_decode_fast_int4_sym(const DecodeParams& p, int gp, cudaStream_t s,
+                                        bool* handled, int* occ) {
+  *handled = false;
+  const int D = p.geom.D, NG = p.geom.ngroups;
+  if (D == 128 && NG == 2) return by_gp4<128, 2>(p, gp, s, handled, occ);
+  if (D == 128 && NG == 4) return by_gp4<128, 4>(p, gp, s, handled, occ);
+  if (D == 64 && NG == 2) return by_gp4<64, 2>(p, gp, s, handled, occ);
+  return cudaSuccess;
+}
+
+}  // namespace kvq

@@ -38,7 +38,8 @@ __device__ __forceinline__ float dequant(const uint8_t* codes, const __half* sca
       q = (float)r[d];
     }
     const long long h = row * c.ngroups + d / c.g;
-    return (q - __half2float(zero[h])) * __half2float(scale[h]);
+    const float z = c.sym ? (float)(1 << (BITS - 1)) : __half2float(zero[h]);
+    return (q - z) * __half2float(scale[h]);
   }
 }
 

@@ -27,6 +27,7 @@ struct CacheGeom {
   int32_t slots;       // dense: capacity; paged: page size
   int32_t num_pages;   // paged only
   int32_t max_blocks;  // paged only
+  int32_t sym;         // 1: symmetric codes (offset 2^(bits-1)), no zero arrays
   const int32_t* block_table;
 };
 
@@ -99,6 +100,10 @@ cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream);
 // With occ != nullptr nothing is launched: *occ receives the CTAs per SM.
 cudaError_t launch_decode_fast_int4(const DecodeParams& p, int gp, cudaStream_t s, bool* handled,
                                     int* occ);
+cudaError_t launch_decode_fast_int4_sym(const DecodeParams& p, int gp, cudaStream_t s,
+                                        bool* handled, int* occ);
+cudaError_t launch_decode_fast_int8_sym(const DecodeParams& p, int gp, cudaStream_t s,
+                                        bool* handled, int* occ);
 cudaError_t launch_decode_fast_int8(const DecodeParams& p, int gp, cudaStream_t s, bool* handled,
                                     int* occ);
 int generic_ctas_per_sm(const DecodeParams& p);

@@ -54,9 +54,18 @@ struct Quant8 {
 // Quantizes 8 channels held by this lane; the group is the `tpg` adjacent
 // lanes (tpg = g / 8, a power of two <= 32, groups aligned to tpg lanes).
 // Every lane of the warp must call it (the group min/max uses shuffles).
-template <int BITS>
+//
+// SYM selects the symmetric (absmax) grid: the zero-centred grid that "What
+// actually happens when you quantize a KV cache", section 3, compares the
+// asymmetric one against, written out as the absmax quantizer in "Serving
+// many users at once", "Quantization: rounding the weights":
+//   a = max |x|, s = the smallest fp16 with s * (2^(b-1) - 1) >= a
+//   (s = 1 when a = 0), q = clamp(rint(x / s), -2^(b-1), 2^(b-1) - 1),
+//   stored as the code q + 2^(b-1); z is returned as 2^(b-1) and not stored.
+template <int BITS, bool SYM = false>
 __device__ __forceinline__ Quant8 quantize8(const uint4 v, int tpg) {
   constexpr int QMAX = (1 << BITS) - 1;
+  constexpr int HALF = 1 << (BITS - 1);  // symmetric code offset
   const __half* h = reinterpret_cast<const __half*>(&v);
   float mn = INFINITY, mx = -INFINITY;
   bool finite = true;
@@ -77,6 +86,32 @@ __device__ __forceinline__ Quant8 quantize8(const uint4 v, int tpg) {
   r.s = __ushort_as_half(0);
   r.z = __ushort_as_half(0);
   r.flags = 0;
+  r.w0 = 0;
+  r.w1 = 0;
+  if constexpr (SYM) {
+    r.z = __int2half_rn(HALF);
+    float sf = 0.f;
+    if (!finite) {
+      r.flags |= KVQ_FLAG_NONFINITE;
+    } else {
+      const float a = fmaxf(fabsf(mn), fabsf(mx));
+      r.s = (a == 0.f) ? __float2half_rn(1.f) : quant_detail::scale_round_up((double)a, HALF - 1);
+      sf = __half2float(r.s);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      float t = 0.f;
+      if (finite) t = fminf(fmaxf(rintf(__fdiv_rn(__half2float(h[k]), sf)), (float)-HALF), (float)(HALF - 1));
+      const uint32_t q = (uint32_t)(int)(t + (float)HALF);
+      if constexpr (BITS == 4) {
+        r.w0 |= q << (4 * k);
+      } else {
+        if (k < 4) r.w0 |= q << (8 * k);
+        else       r.w1 |= q << (8 * (k - 4));
+      }
+    }
+    return r;
+  }
   float sf = 0.f, zf = 0.f;
   if (!finite) {
     r.flags |= KVQ_FLAG_NONFINITE;
@@ -95,8 +130,6 @@ __device__ __forceinline__ Quant8 quantize8(const uint4 v, int tpg) {
     }
     r.z = __int2half_rn((int)zf);
   }
-  r.w0 = 0;
-  r.w1 = 0;
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     uint32_t q = 0;

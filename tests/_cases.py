@@ -32,6 +32,7 @@ class Case:
     page_size: int = 16
     seed: int = 0
     spare_slots: int = 0      # extra dense capacity beyond max(lens)+1
+    symmetric: bool = False   # absmax codes, scale only
 
 
 def make_inputs(c: Case):
@@ -68,11 +69,11 @@ def run_gpu(c: Case, inp, num_splits=0, repeat=1, fused=False):
     Lctx = inp["Lctx"]
     cap = Lctx + 1 + c.spare_slots
     if c.layout == "dense":
-        desc = K.make_desc(c.bits, c.g, c.Hkv, c.D, K.KVQ_DENSE, cap)
+        desc = K.make_desc(c.bits, c.g, c.Hkv, c.D, K.KVQ_DENSE, cap, symmetric=c.symmetric)
         cache = K.KVCache.allocate(desc, c.B, dev)
     else:
         desc = K.make_desc(c.bits, c.g, c.Hkv, c.D, K.KVQ_PAGED, c.page_size,
-                           inp["num_pages"], inp["table"].shape[1])
+                           inp["num_pages"], inp["table"].shape[1], symmetric=c.symmetric)
         cache = K.KVCache.allocate(desc, c.B, dev, torch.from_numpy(inp["table"]))
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     zeros = torch.zeros(c.B, dtype=torch.int32, device=dev)
@@ -115,7 +116,8 @@ def oracle_step(c: Case, inp):
                 hat[b, :, :L + 1] = rows.astype(np.float64)
                 ref_codes[(which, b)] = dict(raw=rows)
                 continue
-            r = O.quantize_groups(rows, c.bits, c.g)
+            quantize = O.quantize_groups_symmetric if c.symmetric else O.quantize_groups
+            r = quantize(rows, c.bits, c.g)
             hat[b, :, :L + 1] = O.dequantize(r["codes"], r["scale"], r["zero"], c.g)
             ref_codes[(which, b)] = dict(packed=O.pack_codes(r["codes"], c.bits),
                                          scale=r["scale"], zero=r["zero"], flags=r["flags"])
@@ -135,7 +137,11 @@ def gpu_codes(run, c: Case, inp, which, b):
         return out
     out["packed"] = np.stack(rows)
     for name in ("scale", "zero"):
-        t = getattr(cache, f"{which}_{name}").cpu().numpy()
+        arr = getattr(cache, f"{which}_{name}")
+        if arr is None:     # symmetric: the zero-point is the fixed code offset
+            out[name] = np.full_like(out["scale"], 1 << (c.bits - 1))
+            continue
+        t = arr.cpu().numpy()
         out[name] = np.stack([logical_rows(t, c, inp["table"], b, h, L) for h in range(c.Hkv)])
     return out
 

@@ -138,3 +138,23 @@ def test_explicit_split_counts(K):
     assert K.kvq_decode_workspace_size(d, 8, 32, 4097, 1) == 0
     ws = K.kvq_decode_workspace_size(d, 8, 32, 4097, 4)
     assert ws >= 8 * 32 * 4 * (128 + 2) * 4
+
+
+def test_symmetric_descriptor(K):
+    """A symmetric cache keeps a 2-byte scale per group and no zero arrays."""
+    from ctypes import byref
+    d = K.make_desc(4, 32, 8, 128, K.KVQ_DENSE, 64, symmetric=True)
+    assert K.kvq_cache_bytes(d, 1) == 2 * 8 * (64 + 2 * 4)
+    assert K.kvq_cache_array_bytes(d, 2) == (2 * 8 * 64 * 64, 2 * 8 * 64 * 4 * 2)
+    for bad in (K.make_desc(16, 0, 8, 128, K.KVQ_DENSE, 64, symmetric=True),):
+        assert K.kvq_cache_bytes(bad, 1) == 0
+    d2 = K.make_desc(4, 32, 8, 128, K.KVQ_DENSE, 64)
+    d2.symmetric = 2
+    assert K.kvq_cache_bytes(d2, 1) == 0
+    lib = K.lib()
+    no_zero = K.kvq_cache(16, 32, 48, None, 80, None, None)
+    # symmetric: the zero arrays are not needed (batch 0: validated, nothing runs)
+    assert lib.kvq_append(byref(d), byref(no_zero), 0, 1, None, None, None, None, None) == K.KVQ_OK
+    asym = K.make_desc(4, 32, 8, 128, K.KVQ_DENSE, 64)
+    assert lib.kvq_append(byref(asym), byref(no_zero), 0, 1, None, None, None, None,
+                          None) == K.KVQ_ERR_INVALID_ARG
