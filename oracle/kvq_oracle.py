@@ -39,7 +39,9 @@ Readings of points the pages leave open (each is listed in the design doc):
   * a group holding inf/NaN is stored as s = z = 0, codes 0, flagged NONFINITE;
   * decode attention over an empty cache returns zeros.
 
-Pins (tests/test_oracle_pins.py): the worked 8-value INT4 group, its
+Pins (tests/test_oracle_pins.py): the axis-aware cache against the outlier
+group of [KVQ] section 3 and its sink-window cost, the worked 8-value INT4
+group, its
 symmetric counterpart and the absmax level count of [SMU], the
 outlier group of [KVQ] section 3, the byte accounting of [KVQ] section 5,
 the FP16 cache sizes of [KVQ]/[QIO]/[GIB]/[CS336]/[SMU], the naive-vs-cached
@@ -242,6 +244,77 @@ def dequantize(codes: np.ndarray, scale: np.ndarray, zero: np.ndarray,
 def quantize_dequantize(x16: np.ndarray, bits: int, group_size: int) -> np.ndarray:
     r = quantize_groups(x16, bits, group_size)
     return dequantize(r["codes"], r["scale"], r["zero"], group_size)
+
+
+# ---------------------------------------------------------------------------
+# Axis-aware (KIVI-style) cache: [KVQ] section 3 step 7 ("axis choice",
+# "sinks") and section 7
+# ---------------------------------------------------------------------------
+
+def kivi_partition(L: int, sink_tokens: int, g: int) -> tuple[int, int, int]:
+    """Where each of L cached positions lives.
+
+    [KVQ] keeps the first few tokens (attention sinks) in fp16, groups K per
+    channel over runs of consecutive tokens, and keeps the newest tokens that
+    have not yet filled such a run in an fp16 residual window.  Returns
+    (S, nb, r0): sinks are positions [0, S); quantized block j < nb covers
+    [S + j g, S + (j + 1) g); the fp16 residual window is [r0, L), r0 = S + nb g,
+    fewer than g tokens.
+    """
+    S = min(int(sink_tokens), int(L))
+    nb = (int(L) - S) // g
+    return S, nb, S + nb * g
+
+
+def kivi_quantize(k16: np.ndarray, v16: np.ndarray, bits: int, g: int,
+                  sink_tokens: int) -> dict:
+    """Quantize one cache of L tokens the axis-aware way.
+
+    k16, v16: fp16 [..., L, D].  In each quantized block of g tokens, K is
+    grouped per channel: one group is one channel across the block's g
+    tokens, so a hot channel shares its scale only with itself.  V is grouped
+    per token, g consecutive channels of one token, as in quantize_groups.
+    Both use the asymmetric quantizer of quantize_groups (only the grouping
+    axis differs).  Sinks and the residual window stay fp16 (exact).
+
+    Returns k_hat, v_hat (fp64 [..., L, D]) and the stored parts of the
+    blocks: k_codes [..., nb g, D] (unpacked), k_scale / k_zero [..., nb, D],
+    v_codes [..., nb g, D], v_scale / v_zero [..., nb g, D / g], flags of both.
+    """
+    k16 = np.asarray(k16, dtype=np.float16)
+    v16 = np.asarray(v16, dtype=np.float16)
+    L, D = k16.shape[-2], k16.shape[-1]
+    S, nb, r0 = kivi_partition(L, sink_tokens, g)
+    lead = k16.shape[:-2]
+    k_hat = k16.astype(np.float64)
+    v_hat = v16.astype(np.float64)
+    blk_k = k16[..., S:r0, :].reshape(lead + (nb, g, D))
+    # per channel: the group axis is the block's tokens
+    rk = quantize_groups(np.swapaxes(blk_k, -1, -2), bits, g)           # [..., nb, D, g]
+    k_codes = np.swapaxes(rk["codes"], -1, -2).reshape(lead + (nb * g, D))
+    k_hat[..., S:r0, :] = np.swapaxes(
+        dequantize(rk["codes"], rk["scale"], rk["zero"], g), -1, -2).reshape(lead + (nb * g, D))
+    rv = quantize_groups(v16[..., S:r0, :], bits, g)
+    v_hat[..., S:r0, :] = dequantize(rv["codes"], rv["scale"], rv["zero"], g)
+    return {
+        "k_hat": k_hat, "v_hat": v_hat, "S": S, "nb": nb, "r0": r0,
+        "k_codes": k_codes, "k_scale": rk["scale"][..., 0], "k_zero": rk["zero"][..., 0],
+        "k_flags": rk["flags"][..., 0],
+        "v_codes": rv["codes"], "v_scale": rv["scale"], "v_zero": rv["zero"],
+        "v_flags": rv["flags"],
+    }
+
+
+def kivi_cache_bytes(kv_heads: int, head_dim: int, tokens: int, bits: int, g: int,
+                     sink_tokens: int) -> int:
+    """Bytes of one layer's axis-aware cache for one sequence of ``tokens``:
+    fp16 sinks and residual, and for each quantized block g code rows of K
+    and V, a K header of one fp16 scale + zero per channel and a V header of
+    one per group of each token."""
+    S, nb, r0 = kivi_partition(tokens, sink_tokens, g)
+    fp16_rows = S + (tokens - r0)
+    per_block = 2 * g * head_dim * bits // 8 + 4 * head_dim + 4 * g * (head_dim // g)
+    return kv_heads * (2 * 2 * head_dim * fp16_rows + nb * per_block)
 
 
 # ---------------------------------------------------------------------------

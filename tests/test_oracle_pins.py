@@ -200,6 +200,111 @@ def test_symmetric_special_groups():
 
 
 # ---------------------------------------------------------------------------
+# Axis-aware (KIVI-style) cache: "What actually happens when you quantize a KV
+# cache", section 3 step 7 and section 7
+# ---------------------------------------------------------------------------
+
+def _outlier_tokens(golden, n_tok=8, seed=0):
+    """n_tok key vectors shaped like the page's toy group: seven small
+    channels and one hot channel (jittered per token)."""
+    kv, _ = golden("kvq_outlier_group_int4.txt")
+    base = np.array(kv["values"], dtype=np.float64)
+    rng = np.random.default_rng(seed)
+    k = base[None, :] * (1 + 0.5 * rng.uniform(-1, 1, (n_tok, 8)))
+    return kv, f16(k)
+
+
+def test_kivi_per_channel_keys_survive_outlier(golden):
+    """The page's outlier group erases seven of eight channels when K is
+    grouped per token; grouping per channel over the tokens keeps each
+    normal channel within half its own (small) step."""
+    kv, k = _outlier_tokens(golden)
+    per_token = O.quantize_groups(k, 4, 8)
+    xh = O.dequantize(per_token["codes"], per_token["scale"], per_token["zero"], 8)
+    assert ((xh[:, :7] == 0.0).sum(axis=1) == kv["erased_channels"]).all()
+    r = O.kivi_quantize(k, k, 4, 8, sink_tokens=0)
+    assert r["nb"] == 1 and r["S"] == 0 and r["r0"] == 8
+    kd = k.astype(np.float64)
+    err = np.abs(r["k_hat"] - kd)
+    s_ch = r["k_scale"][0].astype(np.float64)                      # one scale per channel
+    assert (err <= s_ch[None, :] / 2 + 1e-12).all()
+    assert (s_ch[:7] < 0.02).all() and s_ch[7] > 0.05              # only the hot channel is coarse
+    assert (r["k_hat"][:, :7] != 0.0).sum() >= 50                  # normal channels not erased
+    assert err[:, :7].max() < 0.2 * np.abs(kd[:, :7]).max()
+
+
+def test_kivi_partition_and_fp16_parts():
+    """Sinks and the residual window are stored exactly; blocks cover whole
+    runs of g tokens after the sinks."""
+    rng = np.random.default_rng(1)
+    g, S = 16, 3
+    for L in (0, 2, 3, 3 + 15, 3 + 16, 3 + 16 * 3 + 5, 200):
+        k = f16(rng.standard_normal((2, L, 32)))
+        v = f16(rng.standard_normal((2, L, 32)))
+        r = O.kivi_quantize(k, v, 4, g, S)
+        S_, nb, r0 = O.kivi_partition(L, S, g)
+        assert (r["S"], r["nb"], r["r0"]) == (S_, nb, r0)
+        assert S_ == min(S, L) and r0 == S_ + nb * g and 0 <= L - r0 < g
+        for part in (slice(0, S_), slice(r0, L)):
+            assert np.array_equal(r["k_hat"][:, part], k[:, part].astype(np.float64))
+            assert np.array_equal(r["v_hat"][:, part], v[:, part].astype(np.float64))
+        if nb:
+            assert not np.array_equal(r["k_hat"][:, S_:r0], k[:, S_:r0].astype(np.float64))
+
+
+def test_kivi_grouping_axes():
+    """Axis checks that a transposed grouping would fail: permuting tokens
+    inside a block permutes K codes and leaves the per-channel K scales
+    alone, while V scales follow their tokens; permuting channels permutes
+    the K scales."""
+    rng = np.random.default_rng(2)
+    g, D = 8, 16
+    k = f16(rng.standard_normal((g, D)) * rng.uniform(0.1, 10, (1, D)))
+    v = f16(rng.standard_normal((g, D)) * rng.uniform(0.1, 10, (g, 1)))
+    r = O.kivi_quantize(k, v, 4, g, 0)
+    perm = rng.permutation(g)
+    rp = O.kivi_quantize(k[perm], v[perm], 4, g, 0)
+    assert np.array_equal(rp["k_scale"], r["k_scale"]) and np.array_equal(rp["k_zero"], r["k_zero"])
+    assert np.array_equal(rp["k_codes"], r["k_codes"][perm])
+    assert np.array_equal(rp["v_scale"], r["v_scale"][perm])
+    cperm = rng.permutation(D)
+    rc = O.kivi_quantize(k[:, cperm], v, 4, g, 0)
+    assert np.array_equal(rc["k_scale"][0], r["k_scale"][0][cperm])
+    # K scale per channel from that channel's range over the block's tokens
+    rngs = k.astype(np.float64).max(0) - k.astype(np.float64).min(0)
+    assert (r["k_scale"][0].astype(np.float64) * 15 >= rngs).all()
+
+
+@pytest.mark.parametrize("bits", [4, 8])
+def test_kivi_error_bound(bits):
+    rng = np.random.default_rng(20 + bits)
+    g, S, L, D = 32, 4, 4 + 32 * 5 + 7, 64
+    k = f16(rng.standard_normal((3, L, D)) * np.where(np.arange(D) % 17 == 0, 10.0, 1.0))
+    v = f16(rng.standard_normal((3, L, D)))
+    r = O.kivi_quantize(k, v, bits, g, S)
+    ks = np.repeat(r["k_scale"].astype(np.float64), g, axis=-2)           # [3][nb g][D]
+    assert (np.abs(r["k_hat"][:, S:r["r0"]] - k[:, S:r["r0"]]) <= ks / 2 + 1e-12).all()
+    vs = np.repeat(r["v_scale"].astype(np.float64), g, axis=-1)
+    assert (np.abs(r["v_hat"][:, S:r["r0"]] - v[:, S:r["r0"]]) <= vs / 2 + 1e-12).all()
+
+
+def test_kivi_fp16_window_cost(golden):
+    """A 128-token fp16 window next to a 4096-token cache costs about 3 % of
+    the fp16 cache; the window bytes do not grow with the context."""
+    kv, _ = golden("kvq_sink_window.txt")
+    acc, _ = golden("kvq_byte_accounting.txt")
+    H, D = acc["kv_heads"], acc["head_dim"]
+    w = kv["window_tokens"]
+    window = O.kivi_cache_bytes(H, D, w, 4, 128, sink_tokens=w)        # all fp16
+    full = O.kv_cache_bytes(1, H, D, kv["ctx_tokens"], 16)
+    assert window == O.kv_cache_bytes(1, H, D, w, 16)
+    assert abs(window / full - kv["window_cost_fraction"]) < 0.005
+    # quantized blocks cost what per-token INT4 costs, with one header per channel
+    q = O.kivi_cache_bytes(H, D, 128, 4, 128, sink_tokens=0)
+    assert q == O.kv_cache_bytes(1, H, D, 128, 4, 128)
+
+
+# ---------------------------------------------------------------------------
 # Closed forms and exact arithmetic
 # ---------------------------------------------------------------------------
 
