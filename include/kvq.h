@@ -49,6 +49,23 @@
  *   bits == 16 stores the fp16 vectors themselves in the codes arrays
  *   (row_bytes = 2 * head_dim) and uses no scale/zero arrays.
  *   symmetric == 1 uses no zero arrays (k_zero and v_zero are ignored).
+ *
+ * Axis-aware caches (k_per_channel == 1; "What actually happens when you
+ * quantize a KV cache", section 3 step 7 and section 7: K grouped per
+ * channel, V per token, the first tokens and the newest ones kept in fp16).
+ * With S = sink_tokens, g = group_size, and L tokens cached:
+ *   positions [0, min(S, L))          fp16 sinks, window slot p;
+ *   block j covers [S + j g, S + (j+1) g), quantized once all g of its
+ *     tokens have arrived: K codes in row p of k_codes with one scale and
+ *     zero per channel for the block, V codes in row p of v_codes with
+ *     per-token groups of g channels as in the default layout;
+ *   the newest L - S - floor((L - S) / g) g tokens (fewer than g) form the
+ *     fp16 residual window, slot S + (p - S) mod g.
+ *   DENSE only; capacity must be a multiple of g and larger than S.
+ *          k_codes, v_codes  [batch][num_kv_heads][capacity][row_bytes]
+ *          k_scale, k_zero   [batch][num_kv_heads][capacity / g][head_dim]
+ *          v_scale, v_zero   [batch][num_kv_heads][capacity][head_dim / g]
+ *          k_window, v_window [batch][num_kv_heads][S + g][head_dim] fp16
  */
 #ifndef KVQ_H
 #define KVQ_H
@@ -90,6 +107,11 @@ typedef struct {
   int32_t symmetric;          /* 0: asymmetric, fp16 scale + zero per group;
                                  1: symmetric, fp16 scale only, codes offset
                                  by 2^(bits-1); must be 0 when bits == 16     */
+  int32_t k_per_channel;      /* 1: axis-aware cache (DENSE, bits 4/8,
+                                 asymmetric): K grouped per channel over
+                                 group_size consecutive tokens, V per token,
+                                 fp16 sinks and residual window (see below)   */
+  int32_t sink_tokens;        /* k_per_channel only: leading tokens kept fp16 */
 } kvq_cache_desc;
 
 typedef struct {              /* all device pointers, caller-owned             */
@@ -100,6 +122,8 @@ typedef struct {              /* all device pointers, caller-owned             *
   uint16_t* v_scale;
   uint16_t* v_zero;
   const int32_t* block_table; /* PAGED only                                    */
+  uint16_t* k_window;         /* k_per_channel only: fp16 sinks + residual     */
+  uint16_t* v_window;
 } kvq_cache;
 
 /*
@@ -113,6 +137,13 @@ typedef struct {              /* all device pointers, caller-owned             *
  * arithmetic only.  Returns 0 for an invalid descriptor.
  */
 size_t kvq_cache_bytes(const kvq_cache_desc* desc, int64_t tokens);
+
+/*
+ * Bytes of each of k_window and v_window for `batch` sequences of an
+ * axis-aware cache (batch * num_kv_heads * (sink_tokens + group_size) *
+ * head_dim * 2); 0 for other caches or an invalid descriptor.
+ */
+size_t kvq_cache_window_bytes(const kvq_cache_desc* desc, int32_t batch);
 
 /*
  * Allocation sizes for one layer's cache: *codes_bytes for each of k_codes
@@ -150,6 +181,13 @@ kvq_status kvq_cache_array_bytes(const kvq_cache_desc* desc, int32_t batch,
  * a/(2^(bits-1)-1) (s = 1 when a == 0); q = clamp(round-half-even(x/s),
  * -2^(bits-1), 2^(bits-1)-1) in fp32, stored as the code q + 2^(bits-1);
  * x_hat = (code - 2^(bits-1)) * s.  inf/NaN: s = 0, code 2^(bits-1), flagged.
+ *
+ * Axis-aware caches: a token at a sink position or in the residual window is
+ * stored as fp16.  When a token completes block j, the block is quantized
+ * from the window and the new tokens: each K channel over the block's g
+ * tokens, and each V token per group of g channels, with the formulas
+ * above.  The tokens that remain in the residual window are then written
+ * to their slots.  One call is two kernel launches, in stream order.
  */
 kvq_status kvq_append(const kvq_cache_desc* desc, const kvq_cache* cache,
                       int32_t batch, int32_t num_new,

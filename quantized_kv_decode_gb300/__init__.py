@@ -12,7 +12,7 @@ from ._lib import (KVQ_DENSE, KVQ_ERR_CUDA, KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPO
 __all__ = [
     "KVCache", "make_desc", "kvq_append", "kvq_decode_attn", "kvq_append_decode_attn",
     "kvq_decode_attn_static_ws", "kvq_cache_bytes",
-    "kvq_cache_array_bytes", "kvq_decode_num_splits", "kvq_decode_workspace_size",
+    "kvq_cache_array_bytes", "kvq_cache_window_bytes", "kvq_decode_num_splits", "kvq_decode_workspace_size",
     "kvq_status_string", "KVQError", "lib",
 ]
 

@@ -41,6 +41,8 @@ class kvq_cache_desc(Structure):
         ("num_pages", c_int32),
         ("max_blocks_per_seq", c_int32),
         ("symmetric", c_int32),
+        ("k_per_channel", c_int32),
+        ("sink_tokens", c_int32),
     ]
 
 
@@ -53,6 +55,8 @@ class kvq_cache(Structure):
         ("v_scale", c_void_p),
         ("v_zero", c_void_p),
         ("block_table", c_void_p),
+        ("k_window", c_void_p),
+        ("v_window", c_void_p),
     ]
 
 
@@ -67,6 +71,7 @@ _lib = None
 # name -> (restype, argtypes): the C declarations of include/kvq.h
 SIGNATURES = {
     "kvq_cache_bytes": (c_size_t, [POINTER(kvq_cache_desc), c_int64]),
+    "kvq_cache_window_bytes": (c_size_t, [POINTER(kvq_cache_desc), c_int32]),
     "kvq_cache_array_bytes": (c_int32, [POINTER(kvq_cache_desc), c_int32,
                                         POINTER(c_size_t), POINTER(c_size_t)]),
     "kvq_append": (c_int32, [POINTER(kvq_cache_desc), POINTER(kvq_cache), c_int32, c_int32,

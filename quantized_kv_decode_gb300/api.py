@@ -28,13 +28,19 @@ def _stream(stream) -> int | None:
 
 def make_desc(bits: int, group_size: int, num_kv_heads: int, head_dim: int,
               layout: int = KVQ_DENSE, capacity: int = 0, num_pages: int = 0,
-              max_blocks_per_seq: int = 0, symmetric: bool = False) -> kvq_cache_desc:
+              max_blocks_per_seq: int = 0, symmetric: bool = False,
+              k_per_channel: bool = False, sink_tokens: int = 0) -> kvq_cache_desc:
     return kvq_cache_desc(bits, group_size, num_kv_heads, head_dim, layout, capacity,
-                          num_pages, max_blocks_per_seq, int(bool(symmetric)))
+                          num_pages, max_blocks_per_seq, int(bool(symmetric)),
+                          int(bool(k_per_channel)), int(sink_tokens))
 
 
 def kvq_cache_bytes(desc: kvq_cache_desc, tokens: int) -> int:
     return int(_lib.lib().kvq_cache_bytes(byref(desc), int(tokens)))
+
+
+def kvq_cache_window_bytes(desc: kvq_cache_desc, batch: int) -> int:
+    return int(_lib.lib().kvq_cache_window_bytes(byref(desc), int(batch)))
 
 
 def kvq_cache_array_bytes(desc: kvq_cache_desc, batch: int) -> tuple[int, int]:
@@ -70,6 +76,8 @@ class KVCache:
     v_scale: torch.Tensor | None
     v_zero: torch.Tensor | None
     block_table: torch.Tensor | None = None
+    k_window: torch.Tensor | None = None
+    v_window: torch.Tensor | None = None
 
     @classmethod
     def allocate(cls, desc: kvq_cache_desc, batch: int, device="cuda",
@@ -91,18 +99,27 @@ class KVCache:
             ng = D // desc.group_size
             hdr = lambda: torch.zeros(lead + (ng,), dtype=torch.float16, device=device)
         zero = (lambda: None) if desc.symmetric else hdr
+        if desc.k_per_channel:
+            # K: one scale + zero per channel for each block of g tokens
+            g = desc.group_size
+            khdr = lambda: torch.zeros((batch, Hkv, desc.capacity // g, D), dtype=torch.float16,
+                                       device=device)
+            win = lambda: torch.zeros((batch, Hkv, desc.sink_tokens + g, D), dtype=torch.float16,
+                                      device=device)
+            return cls(desc, batch, codes(), codes(), khdr(), khdr(), hdr(), hdr(), block_table,
+                       win(), win())
         return cls(desc, batch, codes(), codes(), hdr(), zero(), hdr(), zero(), block_table)
 
     @property
     def ptrs(self) -> kvq_cache:
         return kvq_cache(_ptr(self.k_codes), _ptr(self.v_codes), _ptr(self.k_scale),
                          _ptr(self.k_zero), _ptr(self.v_scale), _ptr(self.v_zero),
-                         _ptr(self.block_table))
+                         _ptr(self.block_table), _ptr(self.k_window), _ptr(self.v_window))
 
     def nbytes(self) -> int:
         return sum(t.numel() * t.element_size() for t in
                    (self.k_codes, self.v_codes, self.k_scale, self.k_zero, self.v_scale,
-                    self.v_zero) if t is not None)
+                    self.v_zero, self.k_window, self.v_window) if t is not None)
 
 
 def _need(t, dtype, name, ndim=None):

@@ -29,6 +29,15 @@ kvq_status check_desc(const kvq_cache_desc* d, CacheGeom* g) {
   }
   if (d->symmetric != 0 && d->symmetric != 1) return KVQ_ERR_INVALID_ARG;
   if (d->symmetric && d->bits == 16) return KVQ_ERR_INVALID_ARG;
+  if (d->k_per_channel != 0 && d->k_per_channel != 1) return KVQ_ERR_INVALID_ARG;
+  if (d->k_per_channel) {
+    if (d->bits == 16 || d->symmetric || d->sink_tokens < 0) return KVQ_ERR_INVALID_ARG;
+    if (d->layout == KVQ_DENSE &&
+        (d->capacity % d->group_size || d->sink_tokens >= d->capacity))
+      return KVQ_ERR_INVALID_ARG;
+  } else if (d->sink_tokens != 0) {
+    return KVQ_ERR_INVALID_ARG;
+  }
   if (d->layout == KVQ_DENSE) {
     if (d->capacity <= 0) return KVQ_ERR_INVALID_ARG;
   } else if (d->layout == KVQ_PAGED) {
@@ -50,10 +59,13 @@ kvq_status check_desc(const kvq_cache_desc* d, CacheGeom* g) {
     g->num_pages = d->layout == KVQ_PAGED ? d->num_pages : 0;
     g->max_blocks = d->layout == KVQ_PAGED ? d->max_blocks_per_seq : 0;
     g->sym = d->symmetric;
+    g->kch = d->k_per_channel;
+    g->sink = d->k_per_channel ? d->sink_tokens : 0;
     g->block_table = nullptr;
   }
   // the kernels are built for these head sizes; byte accounting takes any
   if (d->head_dim != 64 && d->head_dim != 128 && d->head_dim != 256) return KVQ_ERR_UNSUPPORTED;
+  if (d->k_per_channel && d->layout != KVQ_DENSE) return KVQ_ERR_UNSUPPORTED;
   return KVQ_OK;
 }
 
@@ -67,6 +79,9 @@ kvq_status check_cache(const kvq_cache_desc* d, const kvq_cache* c) {
       return KVQ_ERR_INVALID_ARG;
   }
   if (d->layout == KVQ_PAGED && (!c->block_table || !aligned(c->block_table)))
+    return KVQ_ERR_INVALID_ARG;
+  if (d->k_per_channel &&
+      (!c->k_window || !c->v_window || !aligned(c->k_window) || !aligned(c->v_window)))
     return KVQ_ERR_INVALID_ARG;
   return KVQ_OK;
 }
@@ -140,7 +155,7 @@ kvq_status make_plan(const kvq_cache_desc* desc, const CacheGeom& geom, int32_t 
   const int G = num_q_heads / desc->num_kv_heads;
   int occ = 0;
   plan->fast = false;
-  if (desc->bits != 16 && G <= 8) {
+  if (desc->bits != 16 && G <= 8 && !desc->k_per_channel) {
     int gp = 1;
     while (gp < G) gp <<= 1;
     plan->gp = gp;
@@ -198,8 +213,24 @@ extern "C" {
 size_t kvq_cache_bytes(const kvq_cache_desc* desc, int64_t tokens) {
   CacheGeom g;
   if (check_desc(desc, &g) == KVQ_ERR_INVALID_ARG || tokens < 0) return 0;
+  if (g.kch) {
+    // fp16 sinks and residual rows (K and V), then per completed block: g
+    // code rows of K and V, a K scale + zero per channel, a V scale + zero
+    // per group of each token
+    const int64_t S = std::min<int64_t>(g.sink, tokens);
+    const int64_t nb = (tokens - S) / g.g;
+    const int64_t fp16_rows = tokens - nb * g.g;
+    const int64_t per_block = 2LL * g.g * g.row_bytes + 4LL * g.D + 4LL * g.g * g.ngroups;
+    return (size_t)(g.Hkv * (2LL * 2 * g.D * fp16_rows + nb * per_block));
+  }
   const int64_t per_vector = g.row_bytes + (g.bits == 16 ? 0 : (g.sym ? 2LL : 4LL) * g.ngroups);
   return (size_t)(2LL * g.Hkv * tokens * per_vector);
+}
+
+size_t kvq_cache_window_bytes(const kvq_cache_desc* desc, int32_t batch) {
+  CacheGeom g;
+  if (check_desc(desc, &g) == KVQ_ERR_INVALID_ARG || batch < 0 || !g.kch) return 0;
+  return (size_t)batch * g.Hkv * (g.sink + g.g) * g.D * 2;
 }
 
 kvq_status kvq_cache_array_bytes(const kvq_cache_desc* desc, int32_t batch,
@@ -223,7 +254,7 @@ kvq_status kvq_cache_array_bytes(const kvq_cache_desc* desc, int32_t batch,
 kvq_status kvq_append(const kvq_cache_desc* desc, const kvq_cache* cache, int32_t batch,
                       int32_t num_new, const uint16_t* k_new, const uint16_t* v_new,
                       const int32_t* seq_lens_before, uint32_t* dev_status, void* stream) {
-  AppendParams p;
+  AppendParams p{};
   kvq_status st = check_desc(desc, &p.geom);
   if (st != KVQ_OK) return st;
   if ((st = check_cache(desc, cache)) != KVQ_OK) return st;
@@ -240,6 +271,8 @@ kvq_status kvq_append(const kvq_cache_desc* desc, const kvq_cache* cache, int32_
   p.zero[1] = reinterpret_cast<__half*>(cache->v_zero);
   p.src[0] = reinterpret_cast<const __half*>(k_new);
   p.src[1] = reinterpret_cast<const __half*>(v_new);
+  p.window[0] = reinterpret_cast<__half*>(cache->k_window);
+  p.window[1] = reinterpret_cast<__half*>(cache->v_window);
   p.seq_lens_before = seq_lens_before;
   p.status = dev_status;
   p.batch = batch;
@@ -316,6 +349,8 @@ kvq_status decode_impl(const kvq_cache_desc* desc, const kvq_cache* cache, int32
   p.lens_before = fused ? lens_before : nullptr;
   p.new_kv[0] = reinterpret_cast<const __half*>(k_new);
   p.new_kv[1] = reinterpret_cast<const __half*>(v_new);
+  p.window[0] = reinterpret_cast<const __half*>(cache->k_window);
+  p.window[1] = reinterpret_cast<const __half*>(cache->v_window);
   p.out = reinterpret_cast<__half*>(out);
   p.ws_o = nullptr;
   p.ws_ml = nullptr;
@@ -335,7 +370,7 @@ kvq_status decode_impl(const kvq_cache_desc* desc, const kvq_cache* cache, int32
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
   bool handled = false;
-  if (desc->bits != 16 && G <= 8) {
+  if (desc->bits != 16 && G <= 8 && !desc->k_per_channel) {
     if (desc->bits == 4) e = launch_decode_fast_int4(p, plan.gp, s, &handled, nullptr);
     else e = launch_decode_fast_int8(p, plan.gp, s, &handled, nullptr);
   }
@@ -352,6 +387,8 @@ kvq_status decode_impl(const kvq_cache_desc* desc, const kvq_cache* cache, int32
       a.zero[1] = reinterpret_cast<__half*>(cache->v_zero);
       a.src[0] = p.new_kv[0];
       a.src[1] = p.new_kv[1];
+      a.window[0] = reinterpret_cast<__half*>(cache->k_window);
+      a.window[1] = reinterpret_cast<__half*>(cache->v_window);
       a.seq_lens_before = lens_before;
       a.status = dev_status;
       a.batch = batch;

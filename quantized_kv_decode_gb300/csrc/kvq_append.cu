@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
 
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
   const CacheGeom& c = p.geom;
+  if (c.kch) return launch_append_kivi(p, stream);
   const long long n_units = (long long)p.batch * p.num_new * c.Hkv * (c.D / 8);
   if (n_units == 0) return cudaSuccess;
   const dim3 block(256);

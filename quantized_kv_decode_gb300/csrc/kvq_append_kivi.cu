@@ -1,0 +1,166 @@
+// Append into axis-aware caches: K grouped per channel over blocks of g
+// tokens, V per token, fp16 sinks and residual window.
+//
+// "What actually happens when you quantize a KV cache", section 3 step 7
+// ("axis choice": a K group is one channel across consecutive tokens, so a
+// hot channel shares its scale with no other; V keeps per-token groups;
+// per-channel K needs a few tokens buffered until a group fills, kept in an
+// fp16 residual window; "sinks": the first tokens stay fp16) and section 7.
+// The quantizer itself is the asymmetric one of section 3 steps 2-5 and
+// section 4 (group_params / group_encode / quantize8 in kvq_quant.cuh), so a
+// K group here is exactly a per-token group with its axis turned.
+//
+// One append is two launches in stream order:
+//  1. kivi_block_kernel: every block that this append completes is
+//     quantized, reading the tokens already in the residual window and the
+//     new ones;
+//  2. kivi_window_kernel: sink tokens and the tokens left in the (new)
+//     residual window are written to their fp16 slots.  It runs second
+//     because its slots may be the ones launch 1 reads.
+#include "kvq_quant.cuh"
+
+namespace kvq {
+namespace {
+
+constexpr int kBlockThreads = 128;
+
+// fp16 source of token q of sequence b, KV head kvh: the residual window for
+// tokens cached before this append, the caller's input otherwise
+__device__ __forceinline__ const __half* token_src(const AppendParams& p, int which, int b, int kvh,
+                                                   int q, int p0) {
+  const CacheGeom& c = p.geom;
+  if (q < p0) {
+    const long long bh = (long long)b * c.Hkv + kvh;
+    return p.window[which] + (bh * (c.sink + c.g) + c.sink + (q - c.sink) % c.g) * c.D;
+  }
+  return p.src[which] + (((long long)b * p.num_new + (q - p0)) * c.Hkv + kvh) * c.D;
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kBlockThreads) kivi_block_kernel(const AppendParams p) {
+  const CacheGeom& c = p.geom;
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int S = c.sink, g = c.g, D = c.D;
+  const int p0 = __ldg(p.seq_lens_before + b);
+  const int n = p.num_new;
+  if (p0 < 0) return;  // flagged by the window kernel
+  // the block holding the first new token (or block 0), then the next ones
+  const int j = (p0 <= S ? 0 : (p0 - S) / g) + blockIdx.x;
+  const long long start = (long long)S + (long long)j * g;
+  const long long end = start + g - 1;               // last position of the block
+  if (end < p0 || end > (long long)p0 + n - 1) return;  // not completed by this append
+  if (end >= c.slots) {
+    if (threadIdx.x == 0 && p.status) atomicOr(p.status, KVQ_FLAG_SEQ_LEN);
+    return;
+  }
+  const long long bh = (long long)b * c.Hkv + kvh;
+  uint32_t flags = 0;
+
+  // ---- K: one group per channel over the block's g tokens ----
+  constexpr int CPU = BITS == 4 ? 2 : 1;  // channels per code byte
+  for (int u = threadIdx.x; u < D / CPU; u += blockDim.x) {
+    GroupParams gp[CPU];
+#pragma unroll
+    for (int e = 0; e < CPU; ++e) {
+      const int ch = u * CPU + e;
+      float mn = INFINITY, mx = -INFINITY;
+      bool finite = true;
+      for (int t = 0; t < g; ++t) {
+        const float x = __half2float(token_src(p, 0, b, kvh, (int)start + t, p0)[ch]);
+        finite = finite && isfinite(x);
+        mn = fminf(mn, x);
+        mx = fmaxf(mx, x);
+      }
+      gp[e] = group_params<BITS>(mn, mx, finite);
+      flags |= gp[e].flags;
+      const long long hi = (bh * (c.slots / g) + j) * D + ch;
+      p.scale[0][hi] = gp[e].s;
+      p.zero[0][hi] = gp[e].z;
+    }
+    for (int t = 0; t < g; ++t) {
+      const __half* src = token_src(p, 0, b, kvh, (int)start + t, p0);
+      uint32_t byte = 0;
+#pragma unroll
+      for (int e = 0; e < CPU; ++e)
+        byte |= group_encode<BITS>(__half2float(src[u * CPU + e]), gp[e]) << (4 * e);
+      p.codes[0][(bh * c.slots + start + t) * c.row_bytes + u] = (uint8_t)byte;
+    }
+  }
+
+  // ---- V: per-token groups of g channels (quantize8 over 8-channel chunks) ----
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int chv = D / 8;               // chunks per token
+  const int tpw = 32 / chv;            // tokens per warp pass (D <= 256)
+  const int tpg = g / 8;               // lanes per group
+  for (int t0 = warp * tpw; t0 < g; t0 += (blockDim.x / 32) * tpw) {
+    const int t = t0 + lane / chv, ch = lane % chv;  // every lane is live: g % tpw == 0
+    const long long q = start + t;
+    const uint4 v = *(reinterpret_cast<const uint4*>(token_src(p, 1, b, kvh, (int)q, p0)) + ch);
+    const Quant8 qz = quantize8<BITS>(v, tpg);
+    uint8_t* dst = p.codes[1] + (bh * c.slots + q) * c.row_bytes + ch * BITS;
+    if constexpr (BITS == 4) {
+      *reinterpret_cast<uint32_t*>(dst) = qz.w0;
+    } else {
+      *reinterpret_cast<uint2*>(dst) = make_uint2(qz.w0, qz.w1);
+    }
+    if (ch % tpg == 0) {
+      const long long hi = (bh * c.slots + q) * c.ngroups + ch / tpg;
+      p.scale[1][hi] = qz.s;
+      p.zero[1][hi] = qz.z;
+      flags |= qz.flags;
+    }
+  }
+  if (flags && p.status) atomicOr(p.status, flags);
+}
+
+// Sinks and the residual window left after this append: one thread per
+// 16-byte chunk of a new token's K and V.
+__global__ void __launch_bounds__(256) kivi_window_kernel(const AppendParams p) {
+  const CacheGeom& c = p.geom;
+  const int chunks = c.D / 8;
+  const long long units = (long long)p.batch * p.num_new * c.Hkv * chunks;
+  const long long u = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= units) return;
+  const int ch = (int)(u % chunks);
+  long long r = u / chunks;
+  const int kvh = (int)(r % c.Hkv);
+  r /= c.Hkv;
+  const int t = (int)(r % p.num_new);
+  const int b = (int)(r / p.num_new);
+  const int p0 = __ldg(p.seq_lens_before + b);
+  const long long q = (long long)p0 + t;
+  if (p0 < 0 || q >= c.slots) {
+    if (ch == 0 && kvh == 0 && p.status) atomicOr(p.status, KVQ_FLAG_SEQ_LEN);
+    return;
+  }
+  // the cache holds min(p0 + num_new, capacity) tokens after this append
+  const int slot = window_slot(c, (int)min((long long)p0 + p.num_new, (long long)c.slots), (int)q);
+  if (slot < 0) return;  // quantized by the block kernel
+  const long long bh = (long long)b * c.Hkv + kvh;
+  const long long src = (((long long)b * p.num_new + t) * c.Hkv + kvh) * c.D + ch * 8;
+  const long long dst = (bh * (c.sink + c.g) + slot) * c.D + ch * 8;
+#pragma unroll
+  for (int which = 0; which < 2; ++which)
+    *reinterpret_cast<uint4*>(p.window[which] + dst) =
+        *reinterpret_cast<const uint4*>(p.src[which] + src);
+}
+
+}  // namespace
+
+cudaError_t launch_append_kivi(const AppendParams& p, cudaStream_t stream) {
+  const CacheGeom& c = p.geom;
+  if (p.batch == 0 || p.num_new == 0) return cudaSuccess;
+  // blocks one append can complete: the one holding its first token and
+  // every later one it reaches
+  const long long nblk = (long long)(p.num_new + c.g - 1) / c.g + 1;
+  const dim3 grid1((unsigned)nblk, c.Hkv, p.batch);
+  if (c.bits == 4) kivi_block_kernel<4><<<grid1, kBlockThreads, 0, stream>>>(p);
+  else kivi_block_kernel<8><<<grid1, kBlockThreads, 0, stream>>>(p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const long long units = (long long)p.batch * p.num_new * c.Hkv * (c.D / 8);
+  kivi_window_kernel<<<(unsigned)((units + 255) / 256), 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

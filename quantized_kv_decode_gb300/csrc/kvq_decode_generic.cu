@@ -43,6 +43,30 @@ __device__ __forceinline__ float dequant(const uint8_t* codes, const __half* sca
   }
 }
 
+// Channel d of K (which = 0) or V (which = 1) at position pos (cache row
+// `row`) of a sequence of L tokens.  Axis-aware caches read sinks and the
+// residual window as fp16 and K blocks with per-channel headers.
+template <int BITS>
+__device__ __forceinline__ float load_kv(const DecodeParams& p, int which, int b, int kvh, int L,
+                                         int pos, long long row, int d) {
+  const CacheGeom& c = p.geom;
+  if constexpr (BITS != 16) {
+    if (c.kch) {
+      const long long bh = (long long)b * c.Hkv + kvh;
+      const int slot = window_slot(c, L, pos);
+      if (slot >= 0) return __half2float(p.window[which][(bh * (c.sink + c.g) + slot) * c.D + d]);
+      if (which == 0) {
+        const uint8_t* r = p.codes[0] + row * c.row_bytes;
+        const float q = BITS == 4 ? (float)((d & 1) ? (r[d >> 1] >> 4) : (r[d >> 1] & 15))
+                                  : (float)r[d];
+        const long long h = (bh * (c.slots / c.g) + (pos - c.sink) / c.g) * c.D + d;
+        return (q - __half2float(p.zero[0][h])) * __half2float(p.scale[0][h]);
+      }
+    }
+  }
+  return dequant<BITS>(p.codes[which], p.scale[which], p.zero[which], c, row, d);
+}
+
 template <int BITS>
 __global__ void __launch_bounds__(kThreads) decode_generic_kernel(const DecodeParams p) {
   extern __shared__ float smem[];
@@ -91,7 +115,7 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(const DecodePa
       for (int h = 0; h < kMaxGroupHeads; ++h) part[h] = 0.f;
       if (row >= 0) {
         for (int d = lane; d < D; d += 32) {
-          const float k = dequant<BITS>(p.codes[0], p.scale[0], p.zero[0], c, row, d);
+          const float k = load_kv<BITS>(p, 0, b, kvh, L, ts + j, row, d);
 #pragma unroll
           for (int h = 0; h < kMaxGroupHeads; ++h)
             if (h < G) part[h] = fmaf(q_s[h * D + d], k, part[h]);
@@ -145,7 +169,7 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(const DecodePa
       for (int j = 0; j < n; ++j) {
         const long long row = row_s[j];
         if (row < 0) continue;
-        acc = fmaf(ps[j], dequant<BITS>(p.codes[1], p.scale[1], p.zero[1], c, row, d), acc);
+        acc = fmaf(ps[j], load_kv<BITS>(p, 1, b, kvh, L, ts + j, row, d), acc);
       }
       o_s[i] = acc;
     }

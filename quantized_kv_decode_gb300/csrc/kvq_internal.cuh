@@ -28,8 +28,20 @@ struct CacheGeom {
   int32_t num_pages;   // paged only
   int32_t max_blocks;  // paged only
   int32_t sym;         // 1: symmetric codes (offset 2^(bits-1)), no zero arrays
+  int32_t kch;         // 1: axis-aware cache (K per channel, fp16 sinks + residual)
+  int32_t sink;        // axis-aware: fp16 sink tokens
   const int32_t* block_table;
 };
+
+// Axis-aware caches: the window slot of position p, or -1 when p is stored
+// quantized (L = tokens cached).  Sinks [0, min(S, L)), residual window
+// [r0, L) with r0 = S + floor((L - S) / g) g.
+__device__ __forceinline__ int window_slot(const CacheGeom& c, int L, int p) {
+  const int S = min(c.sink, L);
+  if (p < S) return p;
+  const int r0 = S + ((L - S) / c.g) * c.g;
+  return p >= r0 ? c.sink + (p - c.sink) % c.g : -1;
+}
 
 // Row index of token `pos` of sequence `b`, KV head `kvh`, into the
 // [..][row_bytes] codes array and the [..][ngroups] header arrays;
@@ -52,6 +64,7 @@ struct AppendParams {
   __half* scale[2];
   __half* zero[2];
   const __half* src[2];  // k_new, v_new: [batch][num_new][Hkv][D]
+  __half* window[2];     // axis-aware caches: fp16 sinks + residual, K and V
   const int32_t* seq_lens_before;
   uint32_t* status;
   int32_t batch;
@@ -80,6 +93,7 @@ struct DecodeParams {
   // ([batch][Hkv][D]); the attended length is lens_before + 1 (seq_lens unused)
   const int32_t* lens_before;
   const __half* new_kv[2];
+  const __half* window[2];  // axis-aware caches: fp16 sinks + residual, K and V
 };
 
 // Tokens to attend over for sequence b (-1 for a length that cannot be formed).
@@ -93,6 +107,7 @@ __device__ __forceinline__ int seq_len_of(const DecodeParams& p, int b) {
 
 // Launchers (return a CUDA error code; the caller maps it to kvq_status).
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
+cudaError_t launch_append_kivi(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_decode_generic(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream);
 // Tensor-core kernel for INT4/INT8 caches; *handled is false when the shape

@@ -44,6 +44,56 @@ __device__ __forceinline__ __half scale_round_up(double range, int qmax) {
 
 }  // namespace quant_detail
 
+// Parameters of one asymmetric group from its min and max (fp16 values as
+// fp32) and whether all its values were finite.
+struct GroupParams {
+  __half s, z;     // stored scale and zero-point
+  float sf, zf;    // the same as fp32 (zf an integer)
+  uint32_t flags;  // KVQ_FLAG_ZERO_CLAMPED / KVQ_FLAG_NONFINITE
+  bool finite;
+};
+
+template <int BITS>
+__device__ __forceinline__ GroupParams group_params(float mn, float mx, bool finite) {
+  constexpr int QMAX = (1 << BITS) - 1;
+  GroupParams r;
+  r.s = __ushort_as_half(0);
+  r.z = __ushort_as_half(0);
+  r.sf = 0.f;
+  r.zf = 0.f;
+  r.flags = 0;
+  r.finite = finite;
+  if (!finite) {
+    r.flags = KVQ_FLAG_NONFINITE;
+    return r;
+  }
+  const double range = (double)mx - (double)mn;
+  if (range == 0.0) {
+    r.s = __float2half_rn(mn == 0.f ? 1.f : fabsf(mn));
+  } else {
+    r.s = quant_detail::scale_round_up(range, QMAX);
+  }
+  r.sf = __half2float(r.s);
+  float zf = rintf(__fdiv_rn(-mn, r.sf));
+  if (fabsf(zf) > 2048.f) {
+    r.flags |= KVQ_FLAG_ZERO_CLAMPED;
+    zf = fminf(fmaxf(zf, -2048.f), 2048.f);
+  }
+  r.zf = zf;
+  r.z = __int2half_rn((int)zf);
+  return r;
+}
+
+// The code of one value x of a group: clamp(rint(x / s) + z, 0, 2^b - 1);
+// 0 for a non-finite group.
+template <int BITS>
+__device__ __forceinline__ uint32_t group_encode(float x, const GroupParams& gp) {
+  constexpr int QMAX = (1 << BITS) - 1;
+  if (!gp.finite) return 0u;
+  const float tq = rintf(__fdiv_rn(x, gp.sf)) + gp.zf;
+  return (uint32_t)fminf(fmaxf(tq, 0.f), (float)QMAX);
+}
+
 // One lane's share of a group: 8 channels.
 struct Quant8 {
   uint32_t w0, w1;  // packed codes: INT4 -> w0 (4 bytes), INT8 -> w0, w1 (8 bytes)
@@ -64,7 +114,6 @@ struct Quant8 {
 //   stored as the code q + 2^(b-1); z is returned as 2^(b-1) and not stored.
 template <int BITS, bool SYM = false>
 __device__ __forceinline__ Quant8 quantize8(const uint4 v, int tpg) {
-  constexpr int QMAX = (1 << BITS) - 1;
   constexpr int HALF = 1 << (BITS - 1);  // symmetric code offset
   const __half* h = reinterpret_cast<const __half*>(&v);
   float mn = INFINITY, mx = -INFINITY;
@@ -112,31 +161,13 @@ __device__ __forceinline__ Quant8 quantize8(const uint4 v, int tpg) {
     }
     return r;
   }
-  float sf = 0.f, zf = 0.f;
-  if (!finite) {
-    r.flags |= KVQ_FLAG_NONFINITE;
-  } else {
-    const double range = (double)mx - (double)mn;
-    if (range == 0.0) {
-      r.s = __float2half_rn(mn == 0.f ? 1.f : fabsf(mn));
-    } else {
-      r.s = quant_detail::scale_round_up(range, QMAX);
-    }
-    sf = __half2float(r.s);
-    zf = rintf(__fdiv_rn(-mn, sf));
-    if (fabsf(zf) > 2048.f) {
-      r.flags |= KVQ_FLAG_ZERO_CLAMPED;
-      zf = fminf(fmaxf(zf, -2048.f), 2048.f);
-    }
-    r.z = __int2half_rn((int)zf);
-  }
+  const GroupParams gp = group_params<BITS>(mn, mx, finite);
+  r.s = gp.s;
+  r.z = gp.z;
+  r.flags = gp.flags;
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    uint32_t q = 0;
-    if (finite) {
-      const float tq = rintf(__fdiv_rn(__half2float(h[k]), sf)) + zf;
-      q = (uint32_t)fminf(fmaxf(tq, 0.f), (float)QMAX);
-    }
+    const uint32_t q = group_encode<BITS>(__half2float(h[k]), gp);
     if constexpr (BITS == 4) {
       r.w0 |= q << (4 * k);  // channel 2m -> low nibble of byte m
     } else {

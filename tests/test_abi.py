@@ -158,3 +158,24 @@ def test_symmetric_descriptor(K):
     asym = K.make_desc(4, 32, 8, 128, K.KVQ_DENSE, 64)
     assert lib.kvq_append(byref(asym), byref(no_zero), 0, 1, None, None, None, None,
                           None) == K.KVQ_ERR_INVALID_ARG
+
+
+def test_axis_aware_descriptor(K):
+    """Byte accounting of axis-aware caches equals the oracle's, and the
+    descriptor rules are enforced on the host."""
+    import oracle as O
+    for (bits, g, S, D, H) in ((4, 32, 4, 128, 8), (8, 64, 0, 128, 2), (4, 16, 3, 64, 4)):
+        d = K.make_desc(bits, g, H, D, K.KVQ_DENSE, 4 * g, k_per_channel=True, sink_tokens=S)
+        for tokens in (0, 1, S, S + g - 1, S + g, S + 3 * g + 5, 1000):
+            assert K.kvq_cache_bytes(d, tokens) == O.kivi_cache_bytes(H, D, tokens, bits, g, S)
+        assert K.kvq_cache_window_bytes(d, 3) == 3 * H * (S + g) * D * 2
+        codes, hdr = K.kvq_cache_array_bytes(d, 2)
+        assert codes == 2 * H * 4 * g * D * bits // 8 and hdr == 2 * H * 4 * g * (D // g) * 2
+    assert K.kvq_cache_window_bytes(K.make_desc(4, 32, 8, 128, K.KVQ_DENSE, 64), 3) == 0
+    bad = [dict(symmetric=True), dict(sink_tokens=-1), dict(sink_tokens=64)]
+    for kw in bad:
+        d = K.make_desc(4, 32, 8, 128, K.KVQ_DENSE, 64, k_per_channel=True, **kw)
+        assert K.kvq_cache_bytes(d, 1) == 0, kw
+    assert K.kvq_cache_bytes(K.make_desc(4, 32, 8, 128, K.KVQ_DENSE, 48, k_per_channel=True), 1) == 0
+    assert K.kvq_cache_bytes(K.make_desc(16, 0, 8, 128, K.KVQ_DENSE, 64, k_per_channel=True), 1) == 0
+    assert K.kvq_cache_bytes(K.make_desc(4, 32, 8, 128, K.KVQ_DENSE, 64, sink_tokens=2), 1) == 0

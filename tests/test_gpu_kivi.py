@@ -1,0 +1,175 @@
+"""GPU parity of axis-aware (KIVI-style) caches against the oracle.
+
+K is grouped per channel over blocks of g tokens, V per token; the first
+sink tokens and the newest tokens that have not filled a block stay fp16.
+Caches are filled by kvq_append calls of several sizes (one token at a time,
+uneven chunks, everything at once); the stored codes, per-channel K headers,
+per-token V headers and fp16 window must equal oracle.kivi_quantize bit for
+bit, and kvq_decode_attn / kvq_append_decode_attn must match the oracle's
+attention over the dequantized cache within the decode tolerance (max |err|
+<= 2e-3, relative L2 <= 1e-3).
+"""
+import numpy as np
+import pytest
+
+import oracle as O
+from quantized_kv_decode_gb300 import synth
+from tests._cases import assert_close
+
+pytestmark = pytest.mark.gpu
+
+
+def _seq_view(K, cache, b):
+    """A one-sequence view of a dense cache (slices of the batch arrays)."""
+    sl = slice(b, b + 1)
+    return K.KVCache(cache.desc, 1, cache.k_codes[sl], cache.v_codes[sl], cache.k_scale[sl],
+                     cache.k_zero[sl], cache.v_scale[sl], cache.v_zero[sl], None,
+                     cache.k_window[sl], cache.v_window[sl])
+
+
+def _fill(K, cache, k, v, lens, chunks, st):
+    """Append sequence b's first lens[b] tokens in pieces of the given sizes."""
+    import torch
+    for b, L in enumerate(lens):
+        view = _seq_view(K, cache, b)
+        pos, i = 0, 0
+        while pos < L:
+            n = min(chunks[i % len(chunks)], L - pos)
+            K.kvq_append(view, k[b:b + 1, pos:pos + n].contiguous(), v[b:b + 1, pos:pos + n].contiguous(),
+                         torch.tensor([pos], dtype=torch.int32, device="cuda"), st)
+            pos += n
+            i += 1
+
+
+def _compare_cache(cache, k16, v16, lens, bits, g, S):
+    """Stored parts against the oracle, per sequence."""
+    for b, L in enumerate(lens):
+        kk = np.transpose(k16[b, :L], (1, 0, 2))           # [Hkv][L][D]
+        vv = np.transpose(v16[b, :L], (1, 0, 2))
+        r = O.kivi_quantize(kk, vv, bits, g, S)
+        S_, nb, r0 = r["S"], r["nb"], r["r0"]
+        kc = cache.k_codes[b].cpu().numpy()
+        vc = cache.v_codes[b].cpu().numpy()
+        assert np.array_equal(kc[:, S_:r0], O.pack_codes(r["k_codes"], bits)), b
+        assert np.array_equal(vc[:, S_:r0], O.pack_codes(r["v_codes"], bits)), b
+        for name, want in (("k_scale", r["k_scale"]), ("k_zero", r["k_zero"])):
+            got = getattr(cache, name)[b, :, :nb].cpu().numpy()
+            assert np.array_equal(got.view(np.uint16), want.view(np.uint16)), (name, b)
+        for name, want in (("v_scale", r["v_scale"]), ("v_zero", r["v_zero"])):
+            got = getattr(cache, name)[b, :, S_:r0].cpu().numpy()
+            assert np.array_equal(got.view(np.uint16), want.view(np.uint16)), (name, b)
+        kw = cache.k_window[b].cpu().numpy()
+        vw = cache.v_window[b].cpu().numpy()
+        assert np.array_equal(kw[:, :S_].view(np.uint16), kk[:, :S_].view(np.uint16))
+        assert np.array_equal(vw[:, :S_].view(np.uint16), vv[:, :S_].view(np.uint16))
+        for p in range(r0, L):
+            slot = S + (p - S) % g
+            assert np.array_equal(kw[:, slot].view(np.uint16), kk[:, p].view(np.uint16)), (b, p)
+            assert np.array_equal(vw[:, slot].view(np.uint16), vv[:, p].view(np.uint16)), (b, p)
+
+
+def _oracle_out(q16, k16, v16, lens, bits, g, S):
+    B, Hq, D = q16.shape
+    Hkv = k16.shape[2]
+    Lmax = int(max(lens))
+    k_hat = np.zeros((B, Hkv, Lmax, D))
+    v_hat = np.zeros((B, Hkv, Lmax, D))
+    for b, L in enumerate(lens):
+        r = O.kivi_quantize(np.transpose(k16[b, :L], (1, 0, 2)), np.transpose(v16[b, :L], (1, 0, 2)),
+                            bits, g, S)
+        k_hat[b, :, :L] = r["k_hat"]
+        v_hat[b, :, :L] = r["v_hat"]
+    return O.decode_attention(q16, k_hat, v_hat, np.asarray(lens))
+
+
+def _run(bits, g, S, D, Hq, Hkv, lens, chunks, splits=0, seed=0, cap=None):
+    import torch
+    import quantized_kv_decode_gb300 as K
+    B = len(lens)
+    Lmax = int(max(lens))
+    cap = cap or ((Lmax + 1 + g - 1) // g) * g + g
+    rng = synth.rng_for(seed)
+    outl = synth.outlier_channels(rng, Hkv, D)
+    k16, v16 = synth.host_kv(rng, B, Lmax + 1, Hkv, D, outl)
+    q16 = synth.host_q(rng, B, Hq, D)
+    desc = K.make_desc(bits, g, Hkv, D, K.KVQ_DENSE, cap, k_per_channel=True, sink_tokens=S)
+    cache = K.KVCache.allocate(desc, B)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kt, vt = torch.from_numpy(k16).cuda(), torch.from_numpy(v16).cuda()
+    _fill(K, cache, kt, vt, lens, chunks, st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    _compare_cache(cache, k16, v16, lens, bits, g, S)
+    q = torch.from_numpy(q16).cuda()
+    lt = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    out = K.kvq_decode_attn(cache, q, lt, Lmax, dev_status=st, num_splits=splits)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert_close(out.cpu().numpy(), _oracle_out(q16, k16, v16, lens, bits, g, S))
+    return K, cache, k16, v16, q16, kt, vt, q, lt, st
+
+
+@pytest.mark.parametrize("bits,g,S,D,Hq,Hkv", [
+    (4, 32, 4, 128, 8, 2), (8, 32, 0, 128, 4, 4), (4, 64, 16, 128, 4, 1), (4, 16, 1, 64, 14, 2),
+    (8, 128, 8, 128, 2, 2), (4, 32, 3, 256, 4, 2)])
+def test_kivi_append_bit_exact_and_decode(bits, g, S, D, Hq, Hkv):
+    lens = [0, 1, S, S + g - 1, S + g, S + 3 * g + 5, 300]
+    lens = [L for L in lens if L > 0]
+    _run(bits, g, S, D, Hq, Hkv, lens, chunks=[1, 7, 64, 3], seed=bits + g + S + D)
+
+
+@pytest.mark.parametrize("chunks", [[1], [1000], [5, 11, 2]])
+def test_kivi_append_granularity_does_not_matter(chunks):
+    """The same tokens appended one at a time, all at once, or in uneven
+    pieces give the same cache (checked bit-exact against the oracle)."""
+    _run(4, 32, 4, 128, 8, 2, [173, 64, 37], chunks=chunks, seed=77)
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+def test_kivi_fused_step_and_splits(splits):
+    """kvq_append_decode_attn on an axis-aware cache: the step's token lands
+    in the residual window (or completes a block) and is attended."""
+    import torch
+    g, S = 32, 4
+    lens = [S + 2 * g - 1, S + 5, 150]          # the first sequence completes a block
+    K, cache, k16, v16, q16, kt, vt, q, lt, st = _run(4, g, S, 128, 8, 2, lens, [16],
+                                                      splits=splits, seed=5)
+    new_k = torch.stack([kt[b, L] for b, L in enumerate(lens)]).contiguous()   # [B][Hkv][D]
+    new_v = torch.stack([vt[b, L] for b, L in enumerate(lens)]).contiguous()
+    out = K.kvq_append_decode_attn(cache, new_k, new_v, q, lt, max(lens) + 1, dev_status=st,
+                                   num_splits=splits)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    lens1 = [L + 1 for L in lens]
+    _compare_cache(cache, k16, v16, lens1, 4, g, S)
+    assert_close(out.cpu().numpy(), _oracle_out(q16, k16, v16, lens1, 4, g, S))
+
+
+def test_kivi_descriptor_limits():
+    import torch
+    import quantized_kv_decode_gb300 as K
+    paged = K.make_desc(4, 32, 2, 128, K.KVQ_PAGED, 32, 10, 4, k_per_channel=True)
+    with pytest.raises(K.KVQError) as e:
+        K.kvq_cache_array_bytes(paged, 1)
+    assert e.value.status == K.KVQ_ERR_UNSUPPORTED
+    # appending past the capacity flags SEQ_LEN and writes nothing there
+    desc = K.make_desc(4, 32, 2, 128, K.KVQ_DENSE, 64, k_per_channel=True, sink_tokens=4)
+    cache = K.KVCache.allocate(desc, 1)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(3)
+    x = torch.randn((1, 70, 2, 128), generator=gen, device="cuda").half()
+    y = torch.randn((1, 70, 2, 128), generator=gen, device="cuda").half()
+    K.kvq_append(cache, x, y, torch.zeros(1, dtype=torch.int32, device="cuda"), st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == K.KVQ_FLAG_SEQ_LEN
+    # the 64 positions inside the cache hold the first 64 tokens
+    k16, v16 = x.cpu().numpy(), y.cpu().numpy()
+    _compare_cache(cache, k16, v16, [64], 4, 32, 4)
+    q16 = torch.randn((1, 4, 128), generator=gen, device="cuda").half()
+    st.zero_()
+    out = K.kvq_decode_attn(cache, q16, torch.tensor([64], dtype=torch.int32, device="cuda"), 64,
+                            dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert_close(out.cpu().numpy(), _oracle_out(q16.cpu().numpy(), k16, v16, [64], 4, 32, 4))
