@@ -77,6 +77,19 @@ def workload_config(w, bits, layers):
     }
 
 
+def kivi_decode_bytes(w, bits, rows, sink):
+    """Algorithmic bytes of one fused step call on an axis-aware cache of
+    `rows` tokens after the append: quantized rows (codes + V headers), one
+    K scale + zero per channel per block, fp16 sink and residual rows, the
+    new token's K/V (read, then written to the window), q and out."""
+    D, g = w.head_dim, w.group_size
+    nb = (rows - sink) // g
+    quant = nb * g * (2 * D * bits // 8 + 4 * (D // g)) + nb * 4 * D
+    fp16_rows = rows - nb * g
+    kv = w.batch * w.num_kv_heads * (quant + fp16_rows * 2 * D * 2 + 2 * D * 2)
+    return kv + 2 * w.batch * w.num_q_heads * D * 2
+
+
 def decode_bytes(w, bits, rows, fused=True, symmetric=False):
     """Algorithmic bytes of one step call.  Decode alone: `rows` cache rows
     (codes + scale/zero, K and V) read, q read, out written.  Fused append:
@@ -221,13 +234,16 @@ def run_reference(args):
 # GPU arm
 # ---------------------------------------------------------------------------
 
-def build_layers(w, bits, layers, dev, seed, torch, K, synth, symmetric=False):
+def build_layers(w, bits, layers, dev, seed, torch, K, synth, symmetric=False, kivi_sink=None):
     """Populate one cache per layer with device-drawn fp16 K/V; per-layer
-    step inputs q, k_new, v_new."""
+    step inputs q, k_new, v_new.  kivi_sink: an axis-aware cache with that
+    many fp16 sink tokens."""
     import numpy as np
-    cap = ((w.ctx[0] + 1 + 15) // 16) * 16
+    align = w.group_size if kivi_sink is not None else 16
+    cap = ((w.ctx[0] + 1 + align - 1) // align) * align
     desc = K.make_desc(bits, w.group_size if bits != 16 else 0, w.num_kv_heads, w.head_dim,
-                       K.KVQ_DENSE, cap, symmetric=symmetric)
+                       K.KVQ_DENSE, cap, symmetric=symmetric, k_per_channel=kivi_sink is not None,
+                       sink_tokens=kivi_sink or 0)
     zeros = torch.zeros(w.batch, dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     caches, qs, kns, vns, host_slices = [], [], [], [], None
@@ -287,15 +303,18 @@ def run_gpu_arm(args):
 
     results = {}
     # formats: the headline asymmetric cache first, then the comparators
-    formats = [(bits, False)]
+    kivi_sink = 4
+    formats = [(bits, False, None)]
     if not args.no_symmetric:
-        formats.append((bits, True))
+        formats.append((bits, True, None))
+    if not args.no_kivi:
+        formats.append((bits, False, kivi_sink))
     if args.fp16_comparator:
-        formats.append((16, False))
-    for fmt, sym in formats:
+        formats.append((16, False, None))
+    for fmt, sym, ksink in formats:
         desc, caches, qs, kns, vns, host_slices = build_layers(
-            w, fmt, layers, dev, seed, torch, K, synth, symmetric=sym)
-        key = "sym" if sym else fmt
+            w, fmt, layers, dev, seed, torch, K, synth, symmetric=sym, kivi_sink=ksink)
+        key = "sym" if sym else ("kivi" if ksink is not None else fmt)
         stream = torch.cuda.Stream(device=dev)
         lens_before = torch.full((w.batch,), w.ctx[0], dtype=torch.int32, device=dev)
         lens = lens_before + 1
@@ -412,7 +431,8 @@ def run_gpu_arm(args):
             value=job_throughput(tokens, world, ms_total), ms_per_step=ms_total / args.steps,
             e2e=job_throughput(tokens, world, e2e_ms), h2d=h2d, d2h=d2h, call_ms=call_ms,
             splits=splits,
-            bytes=decode_bytes(w, fmt, rows, not args.separate_append, sym), clocks=clk,
+            bytes=(kivi_decode_bytes(w, fmt, rows, ksink) if ksink is not None else
+                   decode_bytes(w, fmt, rows, not args.separate_append, sym)), clocks=clk,
             host_slices=host_slices, out0=outs[0][:1].float().cpu().numpy(),
             launches=args.steps * layers * ((2 if args.separate_append else 1) +
                                             (1 if splits > 1 else 0)))
@@ -456,6 +476,17 @@ def run_gpu_arm(args):
             "e2e": f["e2e"], "speedup_vs_asymmetric": f["value"] / r["value"],
             "what": "the same step over symmetric INT4 g32 caches (2-byte scale per group, "
                     "no zero-point)"}
+    if "kivi" in results:
+        f = results["kivi"]
+        line["kivi_cache"] = {
+            "value": f["value"], "unit": UNIT, "ms_per_step": f["ms_per_step"],
+            "achieved_gbs": f["bytes"] / (f["call_ms"] / 1e3) / 1e9,
+            "frac": f["bytes"] / (f["call_ms"] / 1e3) / 1e9 / peak,
+            "bytes_per_launch": f["bytes"], "avg_launch_us": f["call_ms"] * 1e3,
+            "e2e": f["e2e"], "speedup_vs_asymmetric": f["value"] / r["value"],
+            "what": f"the same step over axis-aware INT4 caches: K per channel over blocks of "
+                    f"{w.group_size} tokens, V per token, {kivi_sink} fp16 sink tokens and the fp16 "
+                    f"residual window; the step call is the append kernels + decode"}
     if 16 in results:
         f = results[16]
         line["fp16_cache"] = {
@@ -526,6 +557,8 @@ def main():
     ap.add_argument("--fp16-comparator", action="store_true")
     ap.add_argument("--no-symmetric", action="store_true",
                     help="skip the symmetric-cache comparator")
+    ap.add_argument("--no-kivi", action="store_true",
+                    help="skip the axis-aware-cache comparator")
     ap.add_argument("--separate-append", action="store_true",
                     help="append and attend in two calls instead of the fused call")
     args = ap.parse_args()

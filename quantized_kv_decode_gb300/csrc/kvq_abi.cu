@@ -155,7 +155,7 @@ kvq_status make_plan(const kvq_cache_desc* desc, const CacheGeom& geom, int32_t 
   const int G = num_q_heads / desc->num_kv_heads;
   int occ = 0;
   plan->fast = false;
-  if (desc->bits != 16 && G <= 8 && !desc->k_per_channel) {
+  if (desc->bits != 16 && G <= 8) {
     int gp = 1;
     while (gp < G) gp <<= 1;
     plan->gp = gp;
@@ -370,31 +370,36 @@ kvq_status decode_impl(const kvq_cache_desc* desc, const kvq_cache* cache, int32
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;
   bool handled = false;
-  if (desc->bits != 16 && G <= 8 && !desc->k_per_channel) {
+  // the fast kernel appends in-launch for per-token caches; axis-aware
+  // caches and shapes without a fast kernel run the append kernels first
+  bool appended = false;
+  auto append_first = [&]() -> cudaError_t {
+    appended = true;
+    AppendParams a{};
+    a.geom = p.geom;
+    a.codes[0] = reinterpret_cast<uint8_t*>(cache->k_codes);
+    a.codes[1] = reinterpret_cast<uint8_t*>(cache->v_codes);
+    a.scale[0] = reinterpret_cast<__half*>(cache->k_scale);
+    a.scale[1] = reinterpret_cast<__half*>(cache->v_scale);
+    a.zero[0] = reinterpret_cast<__half*>(cache->k_zero);
+    a.zero[1] = reinterpret_cast<__half*>(cache->v_zero);
+    a.src[0] = p.new_kv[0];
+    a.src[1] = p.new_kv[1];
+    a.window[0] = reinterpret_cast<__half*>(cache->k_window);
+    a.window[1] = reinterpret_cast<__half*>(cache->v_window);
+    a.seq_lens_before = lens_before;
+    a.status = dev_status;
+    a.batch = batch;
+    a.num_new = 1;
+    return launch_append(a, s);
+  };
+  if (fused && desc->k_per_channel) e = append_first();
+  if (e == cudaSuccess && desc->bits != 16 && G <= 8) {
     if (desc->bits == 4) e = launch_decode_fast_int4(p, plan.gp, s, &handled, nullptr);
     else e = launch_decode_fast_int8(p, plan.gp, s, &handled, nullptr);
   }
-  if (!handled) {
-    if (fused) {
-      // shapes without a fast kernel: the append kernel, then the generic pass
-      AppendParams a{};
-      a.geom = p.geom;
-      a.codes[0] = reinterpret_cast<uint8_t*>(cache->k_codes);
-      a.codes[1] = reinterpret_cast<uint8_t*>(cache->v_codes);
-      a.scale[0] = reinterpret_cast<__half*>(cache->k_scale);
-      a.scale[1] = reinterpret_cast<__half*>(cache->v_scale);
-      a.zero[0] = reinterpret_cast<__half*>(cache->k_zero);
-      a.zero[1] = reinterpret_cast<__half*>(cache->v_zero);
-      a.src[0] = p.new_kv[0];
-      a.src[1] = p.new_kv[1];
-      a.window[0] = reinterpret_cast<__half*>(cache->k_window);
-      a.window[1] = reinterpret_cast<__half*>(cache->v_window);
-      a.seq_lens_before = lens_before;
-      a.status = dev_status;
-      a.batch = batch;
-      a.num_new = 1;
-      e = launch_append(a, s);
-    }
+  if (e == cudaSuccess && !handled) {
+    if (fused && !appended) e = append_first();
     if (e == cudaSuccess) e = launch_decode_generic(p, s);
   }
   if (e == cudaSuccess && splits > 1) e = launch_merge(p, s);

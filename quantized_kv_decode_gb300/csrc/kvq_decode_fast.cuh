@@ -40,7 +40,7 @@ namespace fast {
 constexpr int kWarps = 4;
 constexpr int kTT = 32;  // tokens per warp tile
 
-template <int BITS, int D, int NG, int GP>
+template <int BITS, int D, int NG, int GP, bool KCH = false>
 struct Cfg {
   static constexpr int ROWB = D * BITS / 8;       // code bytes per token row
   static constexpr int CHUNKS = ROWB / 16;        // 16-byte chunks per row
@@ -52,7 +52,10 @@ struct Cfg {
   static constexpr int HDRB = NG * 2;             // header bytes per token
   static constexpr int CODE_TILE = kTT * ROWB;
   static constexpr int HDR_TILE = kTT * HDRB;
-  static constexpr int STAGE = 2 * CODE_TILE + 4 * HDR_TILE;
+  // K header bytes of a stage: per-token scale + zero rows, or (KCH, axis-
+  // aware caches) the tile's block: one fp16 scale and zero per channel
+  static constexpr int KHB = KCH ? 4 * D : 2 * HDR_TILE;
+  static constexpr int STAGE = 2 * CODE_TILE + KHB + 2 * HDR_TILE;
   // per-warp scratch of the header pass, rows [group] of [token] entries
   // padded so that lanes reading different groups hit different banks:
   // fp32 K (scale * softmax scale in log2 units, zero) pairs, fp16 V scale,
@@ -76,7 +79,8 @@ struct Cfg {
   static_assert(GSZ % DPC == 0, "a 16-byte chunk must lie inside one group");
   static_assert(NG * GP <= 16, "groups x padded heads must fit 16 rows");
   static_assert(HDRB == 4 || HDRB == 8 || HDRB == 16, "header row size");
-  static_assert(GP * (D + 2) * 4 <= WARP_BYTES, "the CTA merge reuses the pipeline region");
+  static_assert(2 * GP * (D + 2) * 4 <= WARP_BYTES, "the CTA merge reuses the pipeline region");
+  static_assert(!KCH || NG * KROW * 8 >= 4 * D, "KCH: block header scratch");
 
   // Shared-memory byte offset of 16-byte chunk c of token row t: chunk slots
   // are XOR-swizzled by the row's position so that the 8 rows an ldmatrix
@@ -226,12 +230,12 @@ __device__ __forceinline__ uint32_t pack_halves(__half lo, __half hi) {
 // bounded by 2^kSlack.
 constexpr float kSlack = 4.f;
 
-template <int BITS, int D, int NG, int GP, bool SYM>
-__global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
+template <int BITS, int D, int NG, int GP, bool SYM, bool KCH>
+__global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CTAS)
     decode_fast_kernel(const DecodeParams p) {
   // SYM: symmetric caches, no zero arrays; every zero-point is 2^(BITS-1)
   constexpr unsigned short kSymZero = BITS == 4 ? 0x4800u : 0x5800u;  // fp16 8, 128
-  using C = Cfg<BITS, D, NG, GP>;
+  using C = Cfg<BITS, D, NG, GP, KCH>;
   extern __shared__ __align__(128) uint8_t smem[];
   const CacheGeom& geo = p.geom;
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
@@ -278,28 +282,35 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
   // 1, value v_hat) that the CTA merge adds to the warps' partials.  No read
   // of this launch touches the new row, so the store needs no ordering.
   const int pos_new = L - 1;
-  const bool owner_cta = p.lens_before != nullptr && L > 0 && pos_new >= t0 && pos_new < t1;
+  const bool owner_cta = !KCH && p.lens_before != nullptr && L > 0 && pos_new >= t0 && pos_new < t1;
   const int t_end = owner_cta ? t1 - 1 : t1;  // tiles cover [t0, t_end)
 
-  // ---- score-mma A fragments: row r <-> (group r / GP, head r % GP) ----
+  // ---- score-mma A fragments: row r <-> (group r / GP, head r % GP); for
+  // axis-aware caches (KCH) every row r holds head r % GP over all channels,
+  // and the block's per-channel scales are multiplied in per tile ----
   const int g_lo = rho / GP, h_row = rho % GP;
   const int g_hi = g_lo + 8 / GP;
   const bool row_ok = h_row < G;
+  // channel of the score-mma k-slots 2jj, 2jj+1, 2jj+8, 2jj+9 of k-block kb
+  // (the order in which the code conversions deliver channels)
+  auto slot_channels = [](int kb, int jj, int (&dk)[4]) {
+    if constexpr (BITS == 4) {
+      const int base = 32 * (kb >> 1) + 8 * jj + 2 * (kb & 1);
+      dk[0] = base; dk[1] = base + 4; dk[2] = base + 1; dk[3] = base + 5;
+    } else {
+      const int base = 16 * kb + 4 * jj;
+      dk[0] = base; dk[1] = base + 1; dk[2] = base + 2; dk[3] = base + 3;
+    }
+  };
   uint32_t qa[C::KB][4];
 #pragma unroll
   for (int kb = 0; kb < C::KB; ++kb) {
     const int grp = (16 * kb) / C::GSZ;
     int dk[4];  // channel of k-slots 2j, 2j+1, 2j+8, 2j+9
-    if constexpr (BITS == 4) {
-      const int base = 32 * (kb >> 1) + 8 * j + 2 * (kb & 1);
-      dk[0] = base; dk[1] = base + 4; dk[2] = base + 1; dk[3] = base + 5;
-    } else {
-      const int base = 16 * kb + 4 * j;
-      dk[0] = base; dk[1] = base + 1; dk[2] = base + 2; dk[3] = base + 3;
-    }
+    slot_channels(kb, j, dk);
     const __half* qh = q_s + h_row * D;
-    const bool lo = row_ok && g_lo == grp;
-    const bool hi = C::HI && row_ok && g_hi == grp;
+    const bool lo = row_ok && (KCH || g_lo == grp);
+    const bool hi = row_ok && (KCH || (C::HI && g_hi == grp));
     const uint32_t v01 = pack_halves(qh[dk[0]], qh[dk[1]]);
     uint32_t v23 = pack_halves(qh[dk[2]], qh[dk[3]]);
     if constexpr (BITS == 4)  // slots 2j+8, 2j+9 meet the odd nibbles, held as 16c
@@ -312,8 +323,8 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
   // Per row (g, h): the sum of q_h over group g, and the offset that the
   // biased codes add, 1024 * (sum of the row's A entries); both by the same
   // mma against constant codes.
-  float qs_lo, qs_hi, off_lo, off_hi;
-  {
+  float qs_lo = 0.f, qs_hi = 0.f, off_lo = 0.f, off_hi = 0.f;
+  if constexpr (!KCH) {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float bia[4] = {0.f, 0.f, 0.f, 0.f};
     constexpr uint32_t kOnes = 0x3C003C00u;   // fp16 (1, 1)
@@ -350,7 +361,20 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
   float m_ref = -INFINITY, l_run = 0.f;
 
   // ---- this warp's tiles ----
-  const int ntiles = (t_end > t0) ? (t_end - t0 + kTT - 1) / kTT : 0;
+  // KCH: sinks [0, kS) and the residual window [kr0, L) are fp16 and handled
+  // after the loop; the tiles are the quantized blocks' 32-token tiles
+  // (anchored at kS) whose first token lies in [t0, t1).
+  int kS = 0, kr0 = 0, qbase = t0, ntiles;
+  if constexpr (KCH) {
+    kS = min(geo.sink, L);
+    kr0 = kS + ((L - kS) / geo.g) * geo.g;
+    const int m_lo = t0 <= kS ? 0 : (t0 - kS + kTT - 1) / kTT;
+    const int m_hi = min((kr0 - kS) / kTT, t1 <= kS ? 0 : (t1 - kS + kTT - 1) / kTT);
+    ntiles = max(0, m_hi - m_lo);
+    qbase = kS + kTT * m_lo;
+  } else {
+    ntiles = (t_end > t0) ? (t_end - t0 + kTT - 1) / kTT : 0;
+  }
   // the appending warp: one with the fewest tiles
   const bool owner = owner_cta && warp == ntiles % kWarps;  // warp-uniform
   const int nmine = (ntiles > warp) ? (ntiles - warp + kWarps - 1) / kWarps : 0;
@@ -369,8 +393,8 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
     const int stage = it % C::STAGES;
     bool unmapped = false;
     if (it < nmine) {
-      const int start = t0 + (warp + it * kWarps) * kTT;
-      const int n = min(kTT, t_end - start);
+      const int start = qbase + (warp + it * kWarps) * kTT;
+      const int n = KCH ? kTT : min(kTT, t_end - start);
       long long row = -1;  // this lane's token
       const uint32_t kc_s = wpipe_s + stage * C::STAGE, vc_s = kc_s + C::CODE_TILE;
       const uint32_t hd_s = vc_s + C::CODE_TILE;
@@ -409,12 +433,20 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
       const bool ok = row >= 0;
       const long long hoff = ok ? row * C::HDRB : 0;
       const uint32_t hdst = hd_s + lane * C::HDRB;
-      cp_async_small<C::HDRB>(hdst, ks_g + hoff, ok);
-      cp_async_small<C::HDRB>(hdst + 2 * C::HDR_TILE, vs_g + hoff, ok);
-      if constexpr (!SYM) {
-        cp_async_small<C::HDRB>(hdst + C::HDR_TILE, kz_g + hoff, ok);
-        cp_async_small<C::HDRB>(hdst + 3 * C::HDR_TILE, vz_g + hoff, ok);
+      if constexpr (KCH) {
+        // the block's K scales then zeros, 8 channels per 16-byte chunk
+        const long long hb = ((((long long)b * geo.Hkv + kvh) * (geo.slots / geo.g)) +
+                              (start - geo.sink) / geo.g) * D;
+        if (lane < D / 4) {
+          const int w = lane / (D / 8), c = lane % (D / 8);
+          cp_async16(hd_s + w * 2 * D + c * 16, (w ? kz_g : ks_g) + (hb + c * 8) * 2, true);
+        }
+      } else {
+        cp_async_small<C::HDRB>(hdst, ks_g + hoff, ok);
+        if constexpr (!SYM) cp_async_small<C::HDRB>(hdst + C::HDR_TILE, kz_g + hoff, ok);
       }
+      cp_async_small<C::HDRB>(hdst + C::KHB, vs_g + hoff, ok);
+      if constexpr (!SYM) cp_async_small<C::HDRB>(hdst + C::KHB + C::HDR_TILE, vz_g + hoff, ok);
     }
     cp_async_commit();  // one group per slot, empty past the end
     return unmapped;
@@ -428,7 +460,8 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
       if (SYM && (a & 1)) continue;  // no zero rows
-      const uint8_t* src = hsrc + a * C::HDR_TILE;
+      if (KCH && a < 2) continue;    // no per-token K header
+      const uint8_t* src = hsrc + (a < 2 ? a * C::HDR_TILE : C::KHB + (a - 2) * C::HDR_TILE);
       if constexpr (NG == 2) {
         r[a][0] = *reinterpret_cast<const uint32_t*>(src);
       } else if constexpr (NG == 4) {
@@ -445,14 +478,33 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
 #pragma unroll
     for (int g = 0; g < NG; ++g) {
       const int sh = (g & 1) * 16;
-      const unsigned short uk = (unsigned short)(r[0][g / 2] >> sh);
-      const unsigned short uz = SYM ? kSymZero : (unsigned short)(r[1][g / 2] >> sh);
-      ksz[g * C::KROW + lane] = make_float2(__half2float(__ushort_as_half(uk)) * p.scale_log2,
-                                            __half2float(__ushort_as_half(uz)));
+      if constexpr (!KCH) {
+        const unsigned short uk = (unsigned short)(r[0][g / 2] >> sh);
+        const unsigned short uz = SYM ? kSymZero : (unsigned short)(r[1][g / 2] >> sh);
+        ksz[g * C::KROW + lane] = make_float2(__half2float(__ushort_as_half(uk)) * p.scale_log2,
+                                              __half2float(__ushort_as_half(uz)));
+      }
       vs[g * C::VROW + lane] = (unsigned short)(r[2][g / 2] >> sh);
       vz[g * C::VROW + lane] = SYM ? kSymZero : (unsigned short)(r[3][g / 2] >> sh);
     }
     madd_of(buf)[lane] = ((bad >> lane) & 1u) ? -INFINITY : 0.f;
+    if constexpr (KCH) {
+      // the block's per-channel K scale and zero, reordered to [jj][kb][4]
+      // (k-slot order of lane group jj) so the score pass reads its slots
+      // with one 8-byte load per k-block
+      if (lane < 4 * C::KB) {
+        const int jj = lane & 3, kb = lane >> 2;
+        int dk[4];
+        slot_channels(kb, jj, dk);
+        const __half* blk = reinterpret_cast<const __half*>(wpipe + stg * C::STAGE + 2 * C::CODE_TILE);
+        __half* dst = reinterpret_cast<__half*>(ksz_of(buf)) + (jj * C::KB + kb) * 4;
+        *reinterpret_cast<uint2*>(dst) =
+            make_uint2(pack_halves(blk[dk[0]], blk[dk[1]]), pack_halves(blk[dk[2]], blk[dk[3]]));
+        *reinterpret_cast<uint2*>(dst + 4 * 4 * C::KB) =
+            make_uint2(pack_halves(blk[D + dk[0]], blk[D + dk[1]]),
+                       pack_halves(blk[D + dk[2]], blk[D + dk[3]]));
+      }
+    }
   };
 
   // scores of the tile's 4 n-tiles of 8 tokens (log2 units, masked)
@@ -460,6 +512,44 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
     const uint32_t kc_s = wpipe_s + stg * C::STAGE;
     const float2* ksz = ksz_of(buf);
     const float* madd = madd_of(buf);
+    // A operand: q as built above, or (KCH) q times the block's per-channel
+    // scale.  An fp16 product would lose 11 bits on every channel, so KCH
+    // carries it as hi + lo (lo = q s - hi by one fused rounding; the pair is
+    // exact to ~22 bits) and runs each score mma for both.  The accumulator
+    // starts at -(1024 sum(A) + sum(A z)), from mmas against B column 0 =
+    // 1024 and column 1 = z.
+    uint32_t Aop[C::KB][4];
+    uint32_t Alo[KCH ? C::KB : 1][2];
+    float kinit = 0.f;
+    if constexpr (KCH) {
+      const __half* sz = reinterpret_cast<const __half*>(ksz) + j * C::KB * 4;
+      float ci[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kb = 0; kb < C::KB; ++kb) {
+        const uint2 sv = *reinterpret_cast<const uint2*>(sz + kb * 4);
+        const uint2 zv = *reinterpret_cast<const uint2*>(sz + 4 * 4 * C::KB + kb * 4);
+        const __half2 h01 = __hmul2(u32_as_h2(qa[kb][0]), u32_as_h2(sv.x));
+        const __half2 h23 = __hmul2(u32_as_h2(qa[kb][2]), u32_as_h2(sv.y));
+        const uint32_t a01 = h2_as_u32(h01), a23 = h2_as_u32(h23);
+        Alo[kb][0] = h2_as_u32(__hfma2(u32_as_h2(qa[kb][0]), u32_as_h2(sv.x), __hneg2(h01)));
+        Alo[kb][1] = h2_as_u32(__hfma2(u32_as_h2(qa[kb][2]), u32_as_h2(sv.y), __hneg2(h23)));
+        Aop[kb][0] = a01; Aop[kb][1] = a01; Aop[kb][2] = a23; Aop[kb][3] = a23;
+        // slots 2j+8, 2j+9 meet the odd nibbles (held as 16c): their z is 16z
+        const uint32_t z23 = BITS == 4 ? h2_as_u32(__hmul2(u32_as_h2(zv.y), u32_as_h2(0x4C004C00u)))
+                                       : zv.y;
+        const uint32_t b0 = rho == 0 ? kH1024 : (rho == 1 ? zv.x : 0u);
+        const uint32_t b1 = rho == 0 ? kH1024 : (rho == 1 ? z23 : 0u);
+        mma16816(ci, a01, a01, a23, a23, b0, b1);
+        mma16816(ci, Alo[kb][0], Alo[kb][0], Alo[kb][1], Alo[kb][1], b0, b1);
+      }
+      // lane (rho, 0) holds columns 0 and 1 of row rho
+      kinit = __shfl_sync(0xffffffffu, -(ci[0] + ci[1]), rho << 2);
+    } else {
+#pragma unroll
+      for (int kb = 0; kb < C::KB; ++kb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) Aop[kb][e] = qa[kb][e];
+    }
 #pragma unroll
     for (int np = 0; np < 2; ++np) {
       uint32_t w[2][C::CHUNKS];
@@ -476,25 +566,39 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
         }
       }
       // the accumulators start at minus the offset of the biased codes
-      float acc[2][4] = {{-off_lo, -off_lo, -off_hi, -off_hi}, {-off_lo, -off_lo, -off_hi, -off_hi}};
+      float acc[2][4];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        acc[u][0] = acc[u][1] = KCH ? kinit : -off_lo;
+        acc[u][2] = acc[u][3] = KCH ? kinit : -off_hi;
+      }
 #pragma unroll
       for (int c = 0; c < C::CHUNKS; ++c) {
         if constexpr (BITS == 4) {
           uint32_t h0[4], h1[4];
           nib8_to_h2_biased(w[0][c], h0);
           nib8_to_h2_biased(w[1][c], h1);
-          mma16816(acc[0], qa[2 * c][0], qa[2 * c][1], qa[2 * c][2], qa[2 * c][3], h0[0], h0[1]);
-          mma16816(acc[1], qa[2 * c][0], qa[2 * c][1], qa[2 * c][2], qa[2 * c][3], h1[0], h1[1]);
-          mma16816(acc[0], qa[2 * c + 1][0], qa[2 * c + 1][1], qa[2 * c + 1][2],
-                   qa[2 * c + 1][3], h0[2], h0[3]);
-          mma16816(acc[1], qa[2 * c + 1][0], qa[2 * c + 1][1], qa[2 * c + 1][2],
-                   qa[2 * c + 1][3], h1[2], h1[3]);
+          mma16816(acc[0], Aop[2 * c][0], Aop[2 * c][1], Aop[2 * c][2], Aop[2 * c][3], h0[0], h0[1]);
+          mma16816(acc[1], Aop[2 * c][0], Aop[2 * c][1], Aop[2 * c][2], Aop[2 * c][3], h1[0], h1[1]);
+          mma16816(acc[0], Aop[2 * c + 1][0], Aop[2 * c + 1][1], Aop[2 * c + 1][2],
+                   Aop[2 * c + 1][3], h0[2], h0[3]);
+          mma16816(acc[1], Aop[2 * c + 1][0], Aop[2 * c + 1][1], Aop[2 * c + 1][2],
+                   Aop[2 * c + 1][3], h1[2], h1[3]);
+          if constexpr (KCH) {
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const uint32_t l01 = Alo[2 * c + e][0], l23 = Alo[2 * c + e][1];
+              mma16816(acc[0], l01, l01, l23, l23, h0[2 * e], h0[2 * e + 1]);
+              mma16816(acc[1], l01, l01, l23, l23, h1[2 * e], h1[2 * e + 1]);
+            }
+          }
         } else {
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const uint32_t h01 = byte2_to_h2_biased<0x4140>(w[u][c]);
             const uint32_t h23 = byte2_to_h2_biased<0x4342>(w[u][c]);
-            mma16816(acc[u], qa[c][0], qa[c][1], qa[c][2], qa[c][3], h01, h23);
+            mma16816(acc[u], Aop[c][0], Aop[c][1], Aop[c][2], Aop[c][3], h01, h23);
+            if constexpr (KCH) mma16816(acc[u], Alo[c][0], Alo[c][0], Alo[c][1], Alo[c][1], h01, h23);
           }
         }
       }
@@ -503,19 +607,26 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
       for (int u = 0; u < 2; ++u) {
         const int nt = 2 * np + u;
         const int ta = 8 * nt + 2 * j;
-        // (s*scale, z) of tokens ta and ta+1 in one 16-byte load
-        const float4 szl = *reinterpret_cast<const float4*>(ksz + g_lo_c * C::KROW + ta);
-        float va = szl.x * fmaf(-szl.y, qs_lo, acc[u][0]);
-        float vb = szl.z * fmaf(-szl.w, qs_lo, acc[u][1]);
-        if constexpr (C::HI) {
-          const float4 szh = *reinterpret_cast<const float4*>(ksz + g_hi_c * C::KROW + ta);
-          va = fmaf(szh.x, fmaf(-szh.y, qs_hi, acc[u][2]), va);
-          vb = fmaf(szh.z, fmaf(-szh.w, qs_hi, acc[u][3]), vb);
-        }
+        float va, vb;
+        if constexpr (KCH) {
+          // rows are heads and the scales are already in A
+          va = acc[u][0] * p.scale_log2;
+          vb = acc[u][1] * p.scale_log2;
+        } else {
+          // (s*scale, z) of tokens ta and ta+1 in one 16-byte load
+          const float4 szl = *reinterpret_cast<const float4*>(ksz + g_lo_c * C::KROW + ta);
+          va = szl.x * fmaf(-szl.y, qs_lo, acc[u][0]);
+          vb = szl.z * fmaf(-szl.w, qs_lo, acc[u][1]);
+          if constexpr (C::HI) {
+            const float4 szh = *reinterpret_cast<const float4*>(ksz + g_hi_c * C::KROW + ta);
+            va = fmaf(szh.x, fmaf(-szh.y, qs_hi, acc[u][2]), va);
+            vb = fmaf(szh.z, fmaf(-szh.w, qs_hi, acc[u][3]), vb);
+          }
 #pragma unroll
-        for (int s2 = 0; (1 << s2) < C::NGL; ++s2) {
-          va += __shfl_xor_sync(0xffffffffu, va, 4 * GP << s2);
-          vb += __shfl_xor_sync(0xffffffffu, vb, 4 * GP << s2);
+          for (int s2 = 0; (1 << s2) < C::NGL; ++s2) {
+            va += __shfl_xor_sync(0xffffffffu, va, 4 * GP << s2);
+            vb += __shfl_xor_sync(0xffffffffu, vb, 4 * GP << s2);
+          }
         }
         if (bad) {  // warp-uniform: only partial tiles and unmapped pages pay for the mask
           const float2 mk = *reinterpret_cast<const float2*>(madd + ta);
@@ -743,6 +854,64 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
     ml[(warp * GP + rho) * 2] = m_ref;
     ml[(warp * GP + rho) * 2 + 1] = l_run;
   }
+  // KCH: the fp16 tokens of this CTA's range (sinks, then the residual
+  // window), one token per warp at a time on CUDA cores, into a second set of
+  // per-warp partials
+  float* red2 = ml + kWarps * GP * 2;   // [warps][GP][D]
+  float* ml2 = red2 + kWarps * GP * D;  // [warps][GP][2]
+  if constexpr (KCH) {
+    constexpr int CPL = D / 32;         // channels per lane
+    const int ns = max(0, min(t1, kS) - t0);
+    const int rs = max(t0, kr0);
+    const int nw = ns + max(0, t1 - rs);
+    const long long wb = ((long long)b * geo.Hkv + kvh) * (geo.sink + geo.g);
+    float mh[GP], lh[GP], oh[GP][CPL];
+#pragma unroll
+    for (int h = 0; h < GP; ++h) {
+      mh[h] = -INFINITY;
+      lh[h] = 0.f;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) oh[h][c] = 0.f;
+    }
+    for (int i = warp; i < nw; i += kWarps) {
+      const int pos = i < ns ? t0 + i : rs + (i - ns);
+      const int slot = pos < kS ? pos : geo.sink + (pos - geo.sink) % geo.g;
+      const __half* kr = p.window[0] + (wb + slot) * D + lane * CPL;
+      const __half* vr = p.window[1] + (wb + slot) * D + lane * CPL;
+      float kf[CPL], vf[CPL];
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) {
+        kf[c] = __half2float(kr[c]);
+        vf[c] = __half2float(vr[c]);
+      }
+#pragma unroll
+      for (int h = 0; h < GP; ++h) {
+        if (h >= G) continue;
+        float part = 0.f;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) part = fmaf(__half2float(q_s[h * D + lane * CPL + c]), kf[c], part);
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o2);
+        const float sh = part * p.scale_log2;
+        const float mn = fmaxf(mh[h], sh);
+        const float a = mh[h] == -INFINITY ? 0.f : ex2(mh[h] - mn);
+        const float e = ex2(sh - mn);
+        lh[h] = fmaf(lh[h], a, e);
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) oh[h][c] = fmaf(oh[h][c], a, e * vf[c]);
+        mh[h] = mn;
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < GP; ++h) {
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) red2[(warp * GP + h) * D + lane * CPL + c] = oh[h][c];
+      if (lane == 0) {
+        ml2[(warp * GP + h) * 2] = mh[h];
+        ml2[(warp * GP + h) * 2 + 1] = lh[h];
+      }
+    }
+  }
   __syncthreads();
 
   const long long hq0 = (long long)b * p.Hq + (long long)kvh * G;
@@ -751,6 +920,10 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
     float M = -INFINITY;
 #pragma unroll
     for (int w2 = 0; w2 < kWarps; ++w2) M = fmaxf(M, ml[(w2 * GP + h) * 2]);
+    if constexpr (KCH) {
+#pragma unroll
+      for (int w2 = 0; w2 < kWarps; ++w2) M = fmaxf(M, ml2[(w2 * GP + h) * 2]);
+    }
     const float ms = owner_cta ? tok_s[h] : -INFINITY;  // the appended token's partial
     M = fmaxf(M, ms);
     float num = 0.f, den = 0.f;
@@ -760,6 +933,14 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
         const float f = exp2f(ml[(w2 * GP + h) * 2] - M);
         num = fmaf(f, red[(w2 * GP + h) * D + d], num);
         den = fmaf(f, ml[(w2 * GP + h) * 2 + 1], den);
+      }
+      if constexpr (KCH) {
+#pragma unroll
+        for (int w2 = 0; w2 < kWarps; ++w2) {
+          const float f = exp2f(ml2[(w2 * GP + h) * 2] - M);
+          num = fmaf(f, red2[(w2 * GP + h) * D + d], num);
+          den = fmaf(f, ml2[(w2 * GP + h) * 2 + 1], den);
+        }
       }
       if (owner_cta) {
         const float f = exp2f(ms - M);
@@ -780,30 +961,30 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP>::MIN_CTAS)
   }
 }
 
-template <int BITS, int D, int NG, int GP>
+template <int BITS, int D, int NG, int GP, bool KCH>
 size_t fast_smem_bytes() {
-  using C = Cfg<BITS, D, NG, GP>;
+  using C = Cfg<BITS, D, NG, GP, KCH>;
   const size_t pipe = (size_t)kWarps * C::WARP_BYTES;
   const size_t masks = ((kWarps * C::STAGES * 4 + 15) / 16) * 16;
   const size_t newtok = (D + GP) * sizeof(float);
-  const size_t merge = (size_t)kWarps * GP * (D + 2) * sizeof(float);
+  const size_t merge = (size_t)kWarps * GP * (D + 2) * sizeof(float) * (KCH ? 2 : 1);
   return ((GP * D * 2 + 127) / 128) * 128 + (pipe > merge ? pipe : merge) + masks + newtok;
 }
 
 // Launches the instantiation, or with ctas_per_sm != nullptr only reports
 // how many of its CTAs fit on one SM.
-template <int BITS, int D, int NG, int GP, bool SYM>
+template <int BITS, int D, int NG, int GP, bool SYM, bool KCH = false>
 cudaError_t launch_fast_inst(const DecodeParams& p, cudaStream_t stream, int* ctas_per_sm) {
-  const size_t smem = fast_smem_bytes<BITS, D, NG, GP>();
-  cudaError_t e = cudaFuncSetAttribute(decode_fast_kernel<BITS, D, NG, GP, SYM>,
+  const size_t smem = fast_smem_bytes<BITS, D, NG, GP, KCH>();
+  cudaError_t e = cudaFuncSetAttribute(decode_fast_kernel<BITS, D, NG, GP, SYM, KCH>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   if (ctas_per_sm) {
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        ctas_per_sm, decode_fast_kernel<BITS, D, NG, GP, SYM>, kWarps * 32, smem);
+        ctas_per_sm, decode_fast_kernel<BITS, D, NG, GP, SYM, KCH>, kWarps * 32, smem);
   }
   const dim3 grid(p.splits, p.geom.Hkv, p.batch);
-  decode_fast_kernel<BITS, D, NG, GP, SYM><<<grid, kWarps * 32, smem, stream>>>(p);
+  decode_fast_kernel<BITS, D, NG, GP, SYM, KCH><<<grid, kWarps * 32, smem, stream>>>(p);
   return cudaGetLastError();
 }
 

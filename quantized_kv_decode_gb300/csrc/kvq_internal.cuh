@@ -119,6 +119,10 @@ cudaError_t launch_decode_fast_int4_sym(const DecodeParams& p, int gp, cudaStrea
                                         bool* handled, int* occ);
 cudaError_t launch_decode_fast_int8_sym(const DecodeParams& p, int gp, cudaStream_t s,
                                         bool* handled, int* occ);
+cudaError_t launch_decode_fast_int4_kch(const DecodeParams& p, int gp, cudaStream_t s,
+                                        bool* handled, int* occ);
+cudaError_t launch_decode_fast_int8_kch(const DecodeParams& p, int gp, cudaStream_t s,
+                                        bool* handled, int* occ);
 cudaError_t launch_decode_fast_int8(const DecodeParams& p, int gp, cudaStream_t s, bool* handled,
                                     int* occ);
 int generic_ctas_per_sm(const DecodeParams& p);

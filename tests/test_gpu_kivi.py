@@ -118,6 +118,16 @@ def test_kivi_append_bit_exact_and_decode(bits, g, S, D, Hq, Hkv):
     _run(bits, g, S, D, Hq, Hkv, lens, chunks=[1, 7, 64, 3], seed=bits + g + S + D)
 
 
+@pytest.mark.parametrize("bits,g,S,D,Hq,Hkv", [
+    (4, 32, 4, 128, 32, 32), (4, 64, 2, 128, 8, 2), (8, 32, 0, 128, 16, 2), (4, 32, 8, 64, 14, 2)])
+@pytest.mark.parametrize("splits", [0, 5])
+def test_kivi_long_contexts(bits, g, S, D, Hq, Hkv, splits):
+    """Thousands of tokens: many blocks per warp, several splits, a residual
+    window of every fill (the tensor-core path for g a multiple of 32)."""
+    lens = [S + 40 * g + 17, 2051, S + 3 * g]
+    _run(bits, g, S, D, Hq, Hkv, lens, chunks=[2048, 1, 300], splits=splits, seed=bits * g + S)
+
+
 @pytest.mark.parametrize("chunks", [[1], [1000], [5, 11, 2]])
 def test_kivi_append_granularity_does_not_matter(chunks):
     """The same tokens appended one at a time, all at once, or in uneven
