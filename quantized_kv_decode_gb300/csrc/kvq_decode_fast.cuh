@@ -213,6 +213,19 @@ __device__ __forceinline__ float ex2(float x) {
 // o[0] = (1024+c0, 1024+c4), o[1] = (1024+16c1, 1024+16c5), o[2], o[3] likewise.
 __device__ __forceinline__ void nib8_to_h2_biased(uint32_t w, uint32_t (&o)[4]);
 
+// Programmatic dependent launch: let the next kernel of the stream begin its
+// launch, and wait for the previous one to complete (a no-op when the launch
+// did not allow overlap).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
+// Pull [p, p + bytes) into L2 (p and bytes multiples of 16).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
   return h2_as_u32(__floats2half2_rn(lo, hi));
 }
@@ -242,6 +255,35 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CT
   const int G = p.G;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int rho = lane >> 2, j = lane & 3;
+
+  // Launched with programmatic stream serialization: the next kernel of the
+  // stream may start launching now.  Until the previous kernel has completed
+  // (pdl_wait) nothing here reads or writes caller memory; it only warms L2
+  // with this warp's first tiles (dense caches, as if the sequence filled the
+  // cache).  Those bytes are read again after the wait, so a previous kernel
+  // that wrote the cache is still seen.
+  pdl_launch_dependents();
+  if constexpr (!KCH) {
+    if (geo.layout == KVQ_DENSE && lane < C::STAGES * 6) {
+      const int it = lane / 6, region = lane % 6;
+      const int t0g = split * p.chunk;
+      const int t1g = min(geo.slots, t0g + p.chunk);
+      const int start = t0g + (warp + it * kWarps) * kTT;
+      if (start < t1g && !(SYM && (region == 3 || region == 5))) {
+        const int n = min(kTT, t1g - start);
+        const long long row0 = ((long long)b * geo.Hkv + kvh) * geo.slots + start;
+        const int per = region < 2 ? C::ROWB : C::HDRB;
+        const void* base = region == 0 ? (const void*)p.codes[0] : region == 1 ? (const void*)p.codes[1]
+                         : region == 2 ? (const void*)p.scale[0] : region == 3 ? (const void*)p.zero[0]
+                         : region == 4 ? (const void*)p.scale[1] : (const void*)p.zero[1];
+        const uintptr_t a0 = reinterpret_cast<uintptr_t>(base) + (uintptr_t)(row0 * per);
+        const uintptr_t a1 = a0 + (uintptr_t)n * per;
+        const uintptr_t lo = a0 & ~(uintptr_t)15, hi = a1 & ~(uintptr_t)15;  // stay inside the array
+        if (hi > lo) prefetch_l2(reinterpret_cast<const void*>(lo), (uint32_t)(hi - lo));
+      }
+    }
+  }
+  pdl_wait();
 
   int L = seq_len_of(p, b);
   if (L < 0 || L > p.len_limit) {
@@ -983,9 +1025,20 @@ cudaError_t launch_fast_inst(const DecodeParams& p, cudaStream_t stream, int* ct
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
         ctas_per_sm, decode_fast_kernel<BITS, D, NG, GP, SYM, KCH>, kWarps * 32, smem);
   }
-  const dim3 grid(p.splits, p.geom.Hkv, p.batch);
-  decode_fast_kernel<BITS, D, NG, GP, SYM, KCH><<<grid, kWarps * 32, smem, stream>>>(p);
-  return cudaGetLastError();
+  // programmatic stream serialization: this launch may overlap the tail of the
+  // previous kernel in the stream; the kernel waits for it before using any
+  // caller data
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.splits, p.geom.Hkv, p.batch);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_fast_kernel<BITS, D, NG, GP, SYM, KCH>, p);
 }
 
 }  // namespace fast
