@@ -39,7 +39,8 @@ Readings of points the pages leave open (each is listed in the design doc):
   * a group holding inf/NaN is stored as s = z = 0, codes 0, flagged NONFINITE;
   * decode attention over an empty cache returns zeros.
 
-Pins (tests/test_oracle_pins.py): the axis-aware cache against the outlier
+Pins (tests/test_oracle_pins.py): INT2 and the NF4 levels against [KVQ]
+section 7 and [GIB]'s NF4 paragraph, the axis-aware cache against the outlier
 group of [KVQ] section 3 and its sink-window cost, the worked 8-value INT4
 group, its
 symmetric counterpart and the absmax level count of [SMU], the
@@ -203,17 +204,82 @@ def quantize_groups_symmetric(x16: np.ndarray, bits: int, group_size: int) -> di
     }
 
 
+def nf4_levels() -> np.ndarray:
+    """The 16 normal-quantile levels of the NF4 format ([GIB], the NF4
+    paragraph: levels placed at the quantiles of a normal distribution,
+    dense near zero and sparse in the tails).
+
+    Reading (the page gives no formula): level i is the (i + 1/2)/16
+    quantile of N(0, 1), divided by the outermost one so that the levels
+    span [-1, 1]; stored as fp16.
+    """
+    from scipy.special import ndtri
+    z = ndtri((np.arange(16) + 0.5) / 16.0)
+    return (z / z[-1]).astype(np.float16)
+
+
+def quantize_groups_nf4(x16: np.ndarray, group_size: int) -> dict:
+    """Block-scaled normal-quantile 4-bit quantization ([GIB], NF4).
+
+    Per group: s = max |x| (one fp16 scale, an fp16 value already), code =
+    the level nearest x / s (the quotient in fp32; ties to the lower code),
+    x_hat = level[code] * s.  A group of zeros stores s = 0 (no level is 0,
+    so any other s would not decode them to 0); a group holding inf/NaN
+    stores s = 0 and is flagged NONFINITE.  Codes are 0 wherever s = 0.
+    Returns the dict of quantize_groups with "zero" = None.
+    """
+    x16 = np.asarray(x16, dtype=np.float16)
+    D = x16.shape[-1]
+    if D % group_size:
+        raise ValueError("group_size must divide the last axis")
+    ng = D // group_size
+    xg = x16.reshape(x16.shape[:-1] + (ng, group_size)).astype(np.float64)
+    finite = np.isfinite(xg).all(axis=-1)
+    xg_safe = np.where(finite[..., None], xg, 0.0)
+    s16 = np.abs(xg_safe).max(axis=-1).astype(np.float16)      # exact: an fp16 value
+    lv = nf4_levels().astype(np.float32)
+    mids = (lv[:-1] + lv[1:]) / np.float32(2)                  # exact in fp32
+    s32 = s16.astype(np.float32)
+    live = s32 > 0
+    with np.errstate(invalid="ignore", divide="ignore"):
+        t = xg_safe.astype(np.float32) / np.where(live, s32, np.float32(1))[..., None]
+    codes = np.searchsorted(mids, t, side="left")               # number of midpoints below t
+    codes = np.where(live[..., None], codes, 0)
+    flags = np.where(finite, 0, NONFINITE).astype(np.uint32)
+    return {
+        "codes": codes.astype(np.uint8).reshape(x16.shape),
+        "scale": s16,
+        "zero": None,
+        "flags": flags,
+    }
+
+
+def dequantize_nf4(codes: np.ndarray, scale: np.ndarray, group_size: int) -> np.ndarray:
+    """x_hat = level[code] * s in fp64 ([GIB], NF4)."""
+    codes = np.asarray(codes)
+    D = codes.shape[-1]
+    ng = D // group_size
+    lv = nf4_levels().astype(np.float64)
+    qg = lv[codes.astype(np.int64)].reshape(codes.shape[:-1] + (ng, group_size))
+    s = np.asarray(scale, dtype=np.float16).astype(np.float64)[..., None]
+    return (qg * s).reshape(codes.shape)
+
+
 def pack_codes(codes: np.ndarray, bits: int) -> np.ndarray:
     """Pack codes into bytes ([KVQ] section 3 step 5, section 5).
 
+    INT2: four codes per byte, channel 4m + k in bits 2k, 2k + 1.
     INT4: two codes per byte, even channel in the low nibble.
     INT8: one code per byte.
     """
     codes = np.asarray(codes, dtype=np.uint8)
     if bits == 8:
         return codes.copy()
+    if bits == 2:
+        return (codes[..., 0::4] | (codes[..., 1::4] << 2) | (codes[..., 2::4] << 4) |
+                (codes[..., 3::4] << 6)).astype(np.uint8)
     if bits != 4:
-        raise ValueError("bits must be 4 or 8")
+        raise ValueError("bits must be 2, 4 or 8")
     even = codes[..., 0::2]
     odd = codes[..., 1::2]
     return (even | (odd << 4)).astype(np.uint8)
@@ -224,6 +290,10 @@ def unpack_codes(packed: np.ndarray, bits: int, D: int) -> np.ndarray:
     if bits == 8:
         return packed.copy()
     out = np.empty(packed.shape[:-1] + (D,), dtype=np.uint8)
+    if bits == 2:
+        for k in range(4):
+            out[..., k::4] = (packed >> (2 * k)) & 0x03
+        return out
     out[..., 0::2] = packed & 0x0F
     out[..., 1::2] = packed >> 4
     return out
@@ -425,7 +495,7 @@ def decode_attention(q16: np.ndarray, k_hat: np.ndarray, v_hat: np.ndarray,
 
 def kv_cache_bytes(layers: int, kv_heads: int, head_dim: int, tokens: int,
                    bits: int, group_size: int | None = None,
-                   symmetric: bool = False) -> int:
+                   symmetric: bool = False, nf4: bool = False) -> int:
     """Bytes of K+V cache for ``tokens`` tokens of one sequence.
 
     FP16 (bits == 16): 2 * layers * kv_heads * head_dim * 2 bytes per token.
@@ -436,5 +506,5 @@ def kv_cache_bytes(layers: int, kv_heads: int, head_dim: int, tokens: int,
     """
     per_vector = head_dim * bits // 8
     if bits != 16:
-        per_vector += (2 if symmetric else 4) * (head_dim // group_size)
+        per_vector += (2 if (symmetric or nf4) else 4) * (head_dim // group_size)
     return 2 * layers * kv_heads * per_vector * tokens

@@ -200,6 +200,112 @@ def test_symmetric_special_groups():
 
 
 # ---------------------------------------------------------------------------
+# Lower-bit and non-uniform levels: "What actually happens when you quantize a
+# KV cache", section 3 step 7 ("2-bit cliff"); "Gör inference billig", NF4
+# ---------------------------------------------------------------------------
+
+def test_int2_groups(golden):
+    """Four codes and three steps per group: s = range / 3 (rounded up),
+    every code in 0..3, at most four distinct decoded values, |x - x_hat|
+    <= s/2; the step is range/3 against range/15 at INT4 (5x coarser)."""
+    kv, _ = golden("kvq_int2.txt")
+    rng = np.random.default_rng(4)
+    x = f16(rng.standard_normal((200, 32)) * rng.uniform(0.01, 50, (200, 1)))
+    r = O.quantize_groups(x, kv["bits"], 32)
+    xd = x.astype(np.float64)
+    rngs = xd.max(-1) - xd.min(-1)
+    s = r["scale"][:, 0].astype(np.float64)
+    assert (s * kv["steps"] >= rngs).all()
+    assert (s < rngs / kv["steps"] * (1 + 2 ** -10) + 1e-12).all()
+    assert r["codes"].max() == kv["codes"] - 1
+    xh = O.dequantize(r["codes"], r["scale"], r["zero"], 32)
+    assert max(len(set(row)) for row in xh.tolist()) <= kv["codes"]
+    assert (np.abs(xh - xd) <= s[:, None] / 2 + 1e-12).all()
+    s4 = O.quantize_groups(x, 4, 32)["scale"][:, 0].astype(np.float64)
+    ratio = np.median(s / s4)
+    assert abs(ratio - kv["int4_steps"] / kv["steps"]) < 0.05
+
+
+def test_int2_pack_unpack():
+    rng = np.random.default_rng(5)
+    c = rng.integers(0, 4, size=(7, 64)).astype(np.uint8)
+    p = O.pack_codes(c, 2)
+    assert p.shape == (7, 16)
+    assert int(p[0, 0]) == int(c[0, 0] | (c[0, 1] << 2) | (c[0, 2] << 4) | (c[0, 3] << 6))
+    assert np.array_equal(O.unpack_codes(p, 2, 64), c)
+
+
+def test_nf4_levels_shape(golden):
+    """Sixteen increasing levels spanning [-1, 1], symmetric about zero,
+    spaced most tightly near zero and widening toward the tails."""
+    kv, _ = golden("gib_nf4.txt")
+    lv = O.nf4_levels().astype(np.float64)
+    assert len(lv) == kv["levels"] == 2 ** kv["code_bits"]
+    assert lv[0] == -1.0 and lv[-1] == 1.0
+    assert np.array_equal(lv, -lv[::-1])
+    gaps = np.diff(lv)
+    assert (gaps > 0).all()
+    half = gaps[7:]                       # from the centre outward
+    assert (np.diff(half) > 0).all()
+
+
+def test_nf4_levels_are_normal_quantiles():
+    """Against empirical quantiles of normal samples (numpy's generator, not
+    the inverse CDF the oracle uses): level i / level 15 matches the
+    (i + 1/2)/16 sample quantile over the 31/32 sample quantile."""
+    x = np.random.default_rng(6).standard_normal(4_000_000)
+    qs = np.quantile(x, (np.arange(16) + 0.5) / 16)
+    emp = qs / qs[-1]
+    lv = O.nf4_levels().astype(np.float64)
+    assert np.abs(emp - lv).max() < 4e-3
+
+
+def test_nf4_bits_per_value(golden):
+    kv, _ = golden("gib_nf4.txt")
+    D = 128
+    for g, want in ((128, kv["group128_bits_per_weight"]), (64, kv["nf4_bits_per_weight"])):
+        b = O.kv_cache_bytes(1, 1, D, 1, 4, g, nf4=True)
+        assert b * 8 / (2 * D) == want
+
+
+def test_nf4_nearest_level_and_error():
+    """Each code is the level nearest x / s (brute force over all 16, ties
+    to the lower code); on Gaussian blocks NF4's mean squared error is below
+    that of the uniform absmax 4-bit grid at the same block size."""
+    rng = np.random.default_rng(7)
+    x = f16(rng.standard_normal((400, 64)))
+    r = O.quantize_groups_nf4(x, 64)
+    lv = O.nf4_levels().astype(np.float32)
+    s32 = r["scale"].astype(np.float32)
+    for i in range(0, 400, 7):
+        t = x[i].astype(np.float32) / s32[i, 0]
+        for k in range(64):
+            d = np.abs(lv.astype(np.float64) - float(t[k]))
+            assert int(r["codes"][i, k]) == int(np.argmin(d))
+    xd = x.astype(np.float64)
+    e_nf4 = np.mean((O.dequantize_nf4(r["codes"], r["scale"], 64) - xd) ** 2)
+    sym = O.quantize_groups_symmetric(x, 4, 64)
+    e_int4 = np.mean((O.dequantize(sym["codes"], sym["scale"], sym["zero"], 64) - xd) ** 2)
+    assert e_nf4 < e_int4
+    # the block's largest magnitude sits on a +-1 level and decodes exactly
+    idx = np.abs(xd).argmax(axis=1)
+    xh = O.dequantize_nf4(r["codes"], r["scale"], 64)
+    assert np.array_equal(xh[np.arange(400), idx], xd[np.arange(400), idx])
+
+
+def test_nf4_special_groups():
+    x = np.zeros((3, 16), dtype=np.float16)
+    x[1, 3] = np.float16(np.nan)
+    x[2, :] = np.float16(-0.75)
+    r = O.quantize_groups_nf4(x, 16)
+    assert float(r["scale"][0, 0]) == 0.0 and r["flags"][0, 0] == 0
+    assert float(r["scale"][1, 0]) == 0.0 and r["flags"][1, 0] == O.NONFINITE
+    xh = O.dequantize_nf4(r["codes"], r["scale"], 16)
+    assert (xh[:2] == 0).all()
+    assert (xh[2] == -0.75).all() and (r["codes"][2] == 0).all()
+
+
+# ---------------------------------------------------------------------------
 # Axis-aware (KIVI-style) cache: "What actually happens when you quantize a KV
 # cache", section 3 step 7 and section 7
 # ---------------------------------------------------------------------------
