@@ -37,6 +37,8 @@
  *
  * Cache layouts (one instance for K, one for V; the same shapes for both):
  *   row_bytes = head_dim * bits / 8;  groups = head_dim / group_size
+ *   codes: INT8 one per byte; INT4 two per byte, even channel in the low
+ *   nibble; INT2 four per byte, channel 4m + k in bits 2k and 2k + 1.
  *   DENSE  codes  [batch][num_kv_heads][capacity][row_bytes]       uint8
  *          scale  [batch][num_kv_heads][capacity][groups]          fp16
  *          zero   same shape as scale
@@ -48,7 +50,7 @@
  *          at offset p % page_size.  Pages may be shared by sequences.
  *   bits == 16 stores the fp16 vectors themselves in the codes arrays
  *   (row_bytes = 2 * head_dim) and uses no scale/zero arrays.
- *   symmetric == 1 uses no zero arrays (k_zero and v_zero are ignored).
+ *   symmetric == 1 and nf4 == 1 use no zero arrays (k_zero, v_zero ignored).
  *
  * Axis-aware caches (k_per_channel == 1; "What actually happens when you
  * quantize a KV cache", section 3 step 7 and section 7: K grouped per
@@ -94,7 +96,7 @@ typedef enum {
 typedef enum { KVQ_DENSE = 0, KVQ_PAGED = 1 } kvq_layout;
 
 typedef struct {
-  int32_t bits;               /* 4 or 8 (quantized), 16 (fp16 cache)          */
+  int32_t bits;               /* 2, 4 or 8 (quantized), 16 (fp16 cache)       */
   int32_t group_size;         /* channels per group, multiple of 8, divides
                                  head_dim; ignored when bits == 16            */
   int32_t num_kv_heads;       /* >= 1                                          */
@@ -112,6 +114,9 @@ typedef struct {
                                  group_size consecutive tokens, V per token,
                                  fp16 sinks and residual window (see below)   */
   int32_t sink_tokens;        /* k_per_channel only: leading tokens kept fp16 */
+  int32_t nf4;                /* 1: bits 4 coded as 16 normal-quantile levels
+                                 with one fp16 absmax scale per group and no
+                                 zero arrays (see kvq_append)                 */
 } kvq_cache_desc;
 
 typedef struct {              /* all device pointers, caller-owned             */
@@ -130,8 +135,8 @@ typedef struct {              /* all device pointers, caller-owned             *
  * Bytes of K+V cache that `tokens` positions of ONE sequence occupy in one
  * layer: 2 * num_kv_heads * tokens * (row_bytes + 4 * groups), i.e. codes
  * plus a 4-byte fp16 scale+zero header per group ("What actually happens
- * when you quantize a KV cache", section 5; a symmetric cache keeps only the
- * 2-byte scale; for bits == 16 the header is absent and this is
+ * when you quantize a KV cache", section 5; a symmetric or NF4 cache keeps
+ * only the 2-byte scale; for bits == 16 the header is absent and this is
  * 2 * kv_heads * head_dim * 2 bytes per token, the formula of
  * "Quantization & inference optimisation", "What the cache costs").  Host
  * arithmetic only.  Returns 0 for an invalid descriptor.
@@ -181,6 +186,14 @@ kvq_status kvq_cache_array_bytes(const kvq_cache_desc* desc, int32_t batch,
  * a/(2^(bits-1)-1) (s = 1 when a == 0); q = clamp(round-half-even(x/s),
  * -2^(bits-1), 2^(bits-1)-1) in fp32, stored as the code q + 2^(bits-1);
  * x_hat = (code - 2^(bits-1)) * s.  inf/NaN: s = 0, code 2^(bits-1), flagged.
+ *
+ * NF4 caches ("Gör inference billig", the NF4 paragraph: sixteen levels at
+ * the quantiles of a normal distribution, block scaling): level i is the
+ * (i + 1/2)/16 quantile of N(0, 1) divided by the outermost one, as fp16;
+ * per group s = max |x| (an fp16 value, exact); the code is the level
+ * nearest x/s (fp32 quotient, ties to the lower code); x_hat = level * s.
+ * A group of zeros stores s = 0 (no level is 0); inf/NaN: s = 0, flagged;
+ * codes are 0 where s = 0.
  *
  * Axis-aware caches: a token at a sink position or in the residual window is
  * stored as fp16.  When a token completes block j, the block is quantized

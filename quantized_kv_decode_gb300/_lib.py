@@ -43,6 +43,7 @@ class kvq_cache_desc(Structure):
         ("symmetric", c_int32),
         ("k_per_channel", c_int32),
         ("sink_tokens", c_int32),
+        ("nf4", c_int32),
     ]
 
 

@@ -29,10 +29,11 @@ def _stream(stream) -> int | None:
 def make_desc(bits: int, group_size: int, num_kv_heads: int, head_dim: int,
               layout: int = KVQ_DENSE, capacity: int = 0, num_pages: int = 0,
               max_blocks_per_seq: int = 0, symmetric: bool = False,
-              k_per_channel: bool = False, sink_tokens: int = 0) -> kvq_cache_desc:
+              k_per_channel: bool = False, sink_tokens: int = 0,
+              nf4: bool = False) -> kvq_cache_desc:
     return kvq_cache_desc(bits, group_size, num_kv_heads, head_dim, layout, capacity,
                           num_pages, max_blocks_per_seq, int(bool(symmetric)),
-                          int(bool(k_per_channel)), int(sink_tokens))
+                          int(bool(k_per_channel)), int(sink_tokens), int(bool(nf4)))
 
 
 def kvq_cache_bytes(desc: kvq_cache_desc, tokens: int) -> int:
@@ -98,7 +99,7 @@ class KVCache:
         else:
             ng = D // desc.group_size
             hdr = lambda: torch.zeros(lead + (ng,), dtype=torch.float16, device=device)
-        zero = (lambda: None) if desc.symmetric else hdr
+        zero = (lambda: None) if (desc.symmetric or desc.nf4) else hdr
         if desc.k_per_channel:
             # K: one scale + zero per channel for each block of g tokens
             g = desc.group_size

@@ -21,7 +21,7 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 // Validates a cache descriptor; fills `g` on success.
 kvq_status check_desc(const kvq_cache_desc* d, CacheGeom* g) {
   if (!d) return KVQ_ERR_INVALID_ARG;
-  if (d->bits != 4 && d->bits != 8 && d->bits != 16) return KVQ_ERR_INVALID_ARG;
+  if (d->bits != 2 && d->bits != 4 && d->bits != 8 && d->bits != 16) return KVQ_ERR_INVALID_ARG;
   if (d->head_dim <= 0 || d->head_dim % 8 || d->num_kv_heads <= 0) return KVQ_ERR_INVALID_ARG;
   if (d->bits != 16) {
     if (d->group_size < 8 || d->group_size % 8 || d->head_dim % d->group_size)
@@ -30,8 +30,11 @@ kvq_status check_desc(const kvq_cache_desc* d, CacheGeom* g) {
   if (d->symmetric != 0 && d->symmetric != 1) return KVQ_ERR_INVALID_ARG;
   if (d->symmetric && d->bits == 16) return KVQ_ERR_INVALID_ARG;
   if (d->k_per_channel != 0 && d->k_per_channel != 1) return KVQ_ERR_INVALID_ARG;
+  if (d->nf4 != 0 && d->nf4 != 1) return KVQ_ERR_INVALID_ARG;
+  if (d->nf4 && (d->bits != 4 || d->symmetric || d->k_per_channel)) return KVQ_ERR_INVALID_ARG;
   if (d->k_per_channel) {
-    if (d->bits == 16 || d->symmetric || d->sink_tokens < 0) return KVQ_ERR_INVALID_ARG;
+    if (d->bits == 16 || d->bits == 2 || d->symmetric || d->sink_tokens < 0)
+      return KVQ_ERR_INVALID_ARG;
     if (d->layout == KVQ_DENSE &&
         (d->capacity % d->group_size || d->sink_tokens >= d->capacity))
       return KVQ_ERR_INVALID_ARG;
@@ -61,6 +64,7 @@ kvq_status check_desc(const kvq_cache_desc* d, CacheGeom* g) {
     g->sym = d->symmetric;
     g->kch = d->k_per_channel;
     g->sink = d->k_per_channel ? d->sink_tokens : 0;
+    g->nf4 = d->nf4;
     g->block_table = nullptr;
   }
   // the kernels are built for these head sizes; byte accounting takes any
@@ -75,7 +79,8 @@ kvq_status check_cache(const kvq_cache_desc* d, const kvq_cache* c) {
   if (d->bits != 16) {
     if (!c->k_scale || !c->v_scale || !aligned(c->k_scale) || !aligned(c->v_scale))
       return KVQ_ERR_INVALID_ARG;
-    if (!d->symmetric && (!c->k_zero || !c->v_zero || !aligned(c->k_zero) || !aligned(c->v_zero)))
+    if (!d->symmetric && !d->nf4 &&
+        (!c->k_zero || !c->v_zero || !aligned(c->k_zero) || !aligned(c->v_zero)))
       return KVQ_ERR_INVALID_ARG;
   }
   if (d->layout == KVQ_PAGED && (!c->block_table || !aligned(c->block_table)))
@@ -155,7 +160,7 @@ kvq_status make_plan(const kvq_cache_desc* desc, const CacheGeom& geom, int32_t 
   const int G = num_q_heads / desc->num_kv_heads;
   int occ = 0;
   plan->fast = false;
-  if (desc->bits != 16 && G <= 8) {
+  if ((desc->bits == 4 || desc->bits == 8) && !desc->nf4 && G <= 8) {
     int gp = 1;
     while (gp < G) gp <<= 1;
     plan->gp = gp;
@@ -187,6 +192,37 @@ kvq_status make_plan(const kvq_cache_desc* desc, const CacheGeom& geom, int32_t 
 }
 
 kvq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
+
+// NF4 levels: the (i + 1/2)/16 quantiles of N(0, 1) divided by the outermost
+// one, rounded to fp16 ("Gör inference billig", NF4: the sixteen levels sit
+// at the quantiles of a normal distribution).  Each quantile solves
+// Phi(x) = p, Phi(x) = erfc(-x / sqrt 2) / 2, by bisection to double
+// precision.  Computed once.
+struct Nf4Table {
+  float level[16];
+  float mid[16];
+};
+
+const Nf4Table& nf4_table() {
+  static const Nf4Table t = [] {
+    Nf4Table r{};
+    double z[16];
+    for (int i = 0; i < 16; ++i) {
+      const double p = (i + 0.5) / 16.0;
+      double lo = -10.0, hi = 10.0;
+      for (int it = 0; it < 200; ++it) {
+        const double m = 0.5 * (lo + hi);
+        if (0.5 * erfc(-m / sqrt(2.0)) < p) lo = m; else hi = m;
+      }
+      z[i] = 0.5 * (lo + hi);
+    }
+    for (int i = 0; i < 16; ++i) r.level[i] = __half2float(__double2half(z[i] / z[15]));
+    for (int i = 0; i < 15; ++i) r.mid[i] = (r.level[i] + r.level[i + 1]) * 0.5f;
+    r.mid[15] = INFINITY;
+    return r;
+  }();
+  return t;
+}
 
 }  // namespace
 
@@ -223,7 +259,8 @@ size_t kvq_cache_bytes(const kvq_cache_desc* desc, int64_t tokens) {
     const int64_t per_block = 2LL * g.g * g.row_bytes + 4LL * g.D + 4LL * g.g * g.ngroups;
     return (size_t)(g.Hkv * (2LL * 2 * g.D * fp16_rows + nb * per_block));
   }
-  const int64_t per_vector = g.row_bytes + (g.bits == 16 ? 0 : (g.sym ? 2LL : 4LL) * g.ngroups);
+  const int64_t per_vector =
+      g.row_bytes + (g.bits == 16 ? 0 : ((g.sym || g.nf4) ? 2LL : 4LL) * g.ngroups);
   return (size_t)(2LL * g.Hkv * tokens * per_vector);
 }
 
@@ -273,6 +310,7 @@ kvq_status kvq_append(const kvq_cache_desc* desc, const kvq_cache* cache, int32_
   p.src[1] = reinterpret_cast<const __half*>(v_new);
   p.window[0] = reinterpret_cast<__half*>(cache->k_window);
   p.window[1] = reinterpret_cast<__half*>(cache->v_window);
+  if (p.geom.nf4) memcpy(p.nf4_mid, nf4_table().mid, sizeof(p.nf4_mid));
   p.seq_lens_before = seq_lens_before;
   p.status = dev_status;
   p.batch = batch;
@@ -351,6 +389,7 @@ kvq_status decode_impl(const kvq_cache_desc* desc, const kvq_cache* cache, int32
   p.new_kv[1] = reinterpret_cast<const __half*>(v_new);
   p.window[0] = reinterpret_cast<const __half*>(cache->k_window);
   p.window[1] = reinterpret_cast<const __half*>(cache->v_window);
+  if (p.geom.nf4) memcpy(p.nf4_level, nf4_table().level, sizeof(p.nf4_level));
   p.out = reinterpret_cast<__half*>(out);
   p.ws_o = nullptr;
   p.ws_ml = nullptr;
@@ -387,6 +426,7 @@ kvq_status decode_impl(const kvq_cache_desc* desc, const kvq_cache* cache, int32
     a.src[1] = p.new_kv[1];
     a.window[0] = reinterpret_cast<__half*>(cache->k_window);
     a.window[1] = reinterpret_cast<__half*>(cache->v_window);
+    if (a.geom.nf4) memcpy(a.nf4_mid, nf4_table().mid, sizeof(a.nf4_mid));
     a.seq_lens_before = lens_before;
     a.status = dev_status;
     a.batch = batch;
@@ -394,7 +434,7 @@ kvq_status decode_impl(const kvq_cache_desc* desc, const kvq_cache* cache, int32
     return launch_append(a, s);
   };
   if (fused && desc->k_per_channel) e = append_first();
-  if (e == cudaSuccess && desc->bits != 16 && G <= 8) {
+  if (e == cudaSuccess && (desc->bits == 4 || desc->bits == 8) && !desc->nf4 && G <= 8) {
     if (desc->bits == 4) e = launch_decode_fast_int4(p, plan.gp, s, &handled, nullptr);
     else e = launch_decode_fast_int8(p, plan.gp, s, &handled, nullptr);
   }

@@ -12,8 +12,10 @@
 namespace kvq {
 namespace {
 
-template <int BITS, bool SYM>
+// KIND: 0 asymmetric, 1 symmetric, 2 NF4 (BITS 4)
+template <int BITS, int KIND>
 __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
+  constexpr bool SYM = KIND == 1;
   const CacheGeom& c = p.geom;
   const int which = blockIdx.y;  // 0: K, 1: V
   const int chunks = c.D / 8;    // 8-channel chunks per vector
@@ -55,7 +57,8 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
     const int sub = ch % tpg;          // this thread's place in its group
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (live) v = __ldg(reinterpret_cast<const uint4*>(src) + ch);
-    const Quant8 qz = quantize8<BITS, SYM>(v, tpg);  // every lane: the group uses shuffles
+    // every lane: the group uses shuffles
+    const Quant8 qz = KIND == 2 ? quantize8_nf4(v, tpg, p.nf4_mid) : quantize8<BITS, SYM>(v, tpg);
     if (!live) return;
     if (row < 0) {
       if (ch == 0 && p.status) atomicOr(p.status, flags);
@@ -65,7 +68,9 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
     const uint32_t w0 = qz.w0, w1 = qz.w1;
     const __half s_h = qz.s, z_h = qz.z;
     uint8_t* dst = p.codes[which] + row * c.row_bytes + (long long)ch * 8 * BITS / 8;
-    if constexpr (BITS == 4) {
+    if constexpr (BITS == 2) {
+      *reinterpret_cast<uint16_t*>(dst) = (uint16_t)w0;
+    } else if constexpr (BITS == 4) {
       *reinterpret_cast<uint32_t*>(dst) = w0;
     } else {
       *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);
@@ -73,7 +78,7 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
     if (sub == 0) {
       const long long h_idx = row * c.ngroups + ch / tpg;
       p.scale[which][h_idx] = s_h;
-      if constexpr (!SYM) p.zero[which][h_idx] = z_h;
+      if constexpr (KIND == 0) p.zero[which][h_idx] = z_h;
       if (flags && p.status) atomicOr(p.status, flags);
     }
   }
@@ -88,12 +93,16 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
   if (n_units == 0) return cudaSuccess;
   const dim3 block(256);
   const dim3 grid((unsigned)((n_units + 255) / 256), 2);
-  switch (c.bits * 2 + (c.sym ? 1 : 0)) {
-    case 8:  append_kernel<4, false><<<grid, block, 0, stream>>>(p); break;
-    case 9:  append_kernel<4, true><<<grid, block, 0, stream>>>(p); break;
-    case 16: append_kernel<8, false><<<grid, block, 0, stream>>>(p); break;
-    case 17: append_kernel<8, true><<<grid, block, 0, stream>>>(p); break;
-    default: append_kernel<16, false><<<grid, block, 0, stream>>>(p); break;
+  const int kind = c.nf4 ? 2 : (c.sym ? 1 : 0);
+  switch (c.bits * 4 + kind) {
+    case 8:  append_kernel<2, 0><<<grid, block, 0, stream>>>(p); break;
+    case 9:  append_kernel<2, 1><<<grid, block, 0, stream>>>(p); break;
+    case 16: append_kernel<4, 0><<<grid, block, 0, stream>>>(p); break;
+    case 17: append_kernel<4, 1><<<grid, block, 0, stream>>>(p); break;
+    case 18: append_kernel<4, 2><<<grid, block, 0, stream>>>(p); break;
+    case 32: append_kernel<8, 0><<<grid, block, 0, stream>>>(p); break;
+    case 33: append_kernel<8, 1><<<grid, block, 0, stream>>>(p); break;
+    default: append_kernel<16, 0><<<grid, block, 0, stream>>>(p); break;
   }
   return cudaGetLastError();
 }

@@ -22,24 +22,28 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kTile = 64;
 
+// nf4_level: the NF4 level table, or null for uniform codes
 template <int BITS>
 __device__ __forceinline__ float dequant(const uint8_t* codes, const __half* scale,
                                          const __half* zero, const CacheGeom& c,
-                                         long long row, int d) {
+                                         long long row, int d, const float* nf4_level) {
   if constexpr (BITS == 16) {
     return __half2float(reinterpret_cast<const __half*>(codes + row * c.row_bytes)[d]);
   } else {
     const uint8_t* r = codes + row * c.row_bytes;
-    float q;
-    if constexpr (BITS == 4) {
+    int q;
+    if constexpr (BITS == 2) {
+      q = (r[d >> 2] >> (2 * (d & 3))) & 3;
+    } else if constexpr (BITS == 4) {
       const uint8_t byte = r[d >> 1];
-      q = (float)((d & 1) ? (byte >> 4) : (byte & 15));
+      q = (d & 1) ? (byte >> 4) : (byte & 15);
     } else {
-      q = (float)r[d];
+      q = r[d];
     }
     const long long h = row * c.ngroups + d / c.g;
+    if (nf4_level) return nf4_level[q] * __half2float(scale[h]);
     const float z = c.sym ? (float)(1 << (BITS - 1)) : __half2float(zero[h]);
-    return (q - z) * __half2float(scale[h]);
+    return ((float)q - z) * __half2float(scale[h]);
   }
 }
 
@@ -64,7 +68,8 @@ __device__ __forceinline__ float load_kv(const DecodeParams& p, int which, int b
       }
     }
   }
-  return dequant<BITS>(p.codes[which], p.scale[which], p.zero[which], c, row, d);
+  return dequant<BITS>(p.codes[which], p.scale[which], p.zero[which], c, row, d,
+                       c.nf4 ? p.nf4_level : nullptr);
 }
 
 template <int BITS>
@@ -231,6 +236,11 @@ cudaError_t launch_decode_generic(const DecodeParams& p, cudaStream_t stream) {
   const dim3 grid(p.splits, p.geom.Hkv, p.batch);
   cudaError_t e = cudaSuccess;
   switch (p.geom.bits) {
+    case 2:
+      e = cudaFuncSetAttribute(decode_generic_kernel<2>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e == cudaSuccess) decode_generic_kernel<2><<<grid, kThreads, smem, stream>>>(p);
+      break;
     case 4:
       e = cudaFuncSetAttribute(decode_generic_kernel<4>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -264,6 +274,7 @@ int generic_ctas_per_sm(const DecodeParams& p) {
   int n = 0;
   cudaError_t e = cudaErrorInvalidValue;
   switch (p.geom.bits) {
+    case 2: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_generic_kernel<2>, kThreads, smem); break;
     case 4: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_generic_kernel<4>, kThreads, smem); break;
     case 8: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_generic_kernel<8>, kThreads, smem); break;
     default: e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_generic_kernel<16>, kThreads, smem); break;

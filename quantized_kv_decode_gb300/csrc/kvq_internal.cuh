@@ -30,6 +30,7 @@ struct CacheGeom {
   int32_t sym;         // 1: symmetric codes (offset 2^(bits-1)), no zero arrays
   int32_t kch;         // 1: axis-aware cache (K per channel, fp16 sinks + residual)
   int32_t sink;        // axis-aware: fp16 sink tokens
+  int32_t nf4;         // 1: 4-bit codes index the normal-quantile levels, no zero arrays
   const int32_t* block_table;
 };
 
@@ -65,6 +66,7 @@ struct AppendParams {
   __half* zero[2];
   const __half* src[2];  // k_new, v_new: [batch][num_new][Hkv][D]
   __half* window[2];     // axis-aware caches: fp16 sinks + residual, K and V
+  float nf4_mid[16];     // NF4: midpoints between consecutive levels (15 used)
   const int32_t* seq_lens_before;
   uint32_t* status;
   int32_t batch;
@@ -94,6 +96,7 @@ struct DecodeParams {
   const int32_t* lens_before;
   const __half* new_kv[2];
   const __half* window[2];  // axis-aware caches: fp16 sinks + residual, K and V
+  float nf4_level[16];      // NF4: the 16 levels (fp16 values as fp32)
 };
 
 // Tokens to attend over for sequence b (-1 for a length that cannot be formed).

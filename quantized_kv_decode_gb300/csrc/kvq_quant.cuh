@@ -96,7 +96,7 @@ __device__ __forceinline__ uint32_t group_encode(float x, const GroupParams& gp)
 
 // One lane's share of a group: 8 channels.
 struct Quant8 {
-  uint32_t w0, w1;  // packed codes: INT4 -> w0 (4 bytes), INT8 -> w0, w1 (8 bytes)
+  uint32_t w0, w1;  // packed codes: INT2 -> w0 (2 bytes), INT4 -> w0 (4 bytes), INT8 -> w0, w1
   __half s, z;      // the group's scale and zero-point
   uint32_t flags;   // KVQ_FLAG_ZERO_CLAMPED / KVQ_FLAG_NONFINITE
 };
@@ -152,7 +152,9 @@ __device__ __forceinline__ Quant8 quantize8(const uint4 v, int tpg) {
       float t = 0.f;
       if (finite) t = fminf(fmaxf(rintf(__fdiv_rn(__half2float(h[k]), sf)), (float)-HALF), (float)(HALF - 1));
       const uint32_t q = (uint32_t)(int)(t + (float)HALF);
-      if constexpr (BITS == 4) {
+      if constexpr (BITS == 2) {
+        r.w0 |= q << (2 * k);
+      } else if constexpr (BITS == 4) {
         r.w0 |= q << (4 * k);
       } else {
         if (k < 4) r.w0 |= q << (8 * k);
@@ -168,11 +170,53 @@ __device__ __forceinline__ Quant8 quantize8(const uint4 v, int tpg) {
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const uint32_t q = group_encode<BITS>(__half2float(h[k]), gp);
-    if constexpr (BITS == 4) {
+    if constexpr (BITS == 2) {
+      r.w0 |= q << (2 * k);  // channel 4m + j -> bits 2j of byte m
+    } else if constexpr (BITS == 4) {
       r.w0 |= q << (4 * k);  // channel 2m -> low nibble of byte m
     } else {
       if (k < 4) r.w0 |= q << (8 * k);
       else       r.w1 |= q << (8 * (k - 4));
+    }
+  }
+  return r;
+}
+
+// NF4 ("Gör inference billig", NF4: sixteen normal-quantile levels with a
+// block absmax scale).  s = max |x| over the group (an fp16 value, exact);
+// code = number of level midpoints (`mid`, fp32, increasing) below x/s, i.e.
+// the nearest level with ties to the lower one; a group of zeros or with
+// inf/NaN stores s = 0 and codes 0 (the latter flagged).  Same lane layout
+// and packing as quantize8<4>.
+__device__ __forceinline__ Quant8 quantize8_nf4(const uint4 v, int tpg, const float (&mid)[16]) {
+  const __half* h = reinterpret_cast<const __half*>(&v);
+  float a = 0.f;
+  bool finite = true;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float f = __half2float(h[k]);
+    finite = finite && isfinite(f);
+    a = fmaxf(a, fabsf(f));
+  }
+  for (int o = 1; o < tpg; o <<= 1) {
+    a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    finite = (__shfl_xor_sync(0xffffffffu, (int)finite, o) != 0) && finite;
+  }
+  Quant8 r;
+  r.flags = finite ? 0u : KVQ_FLAG_NONFINITE;
+  const bool live = finite && a > 0.f;
+  r.s = live ? __float2half_rn(a) : __ushort_as_half(0);
+  r.z = __ushort_as_half(0);
+  r.w0 = 0;
+  r.w1 = 0;
+  if (live) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float t = __fdiv_rn(__half2float(h[k]), a);
+      uint32_t q = 0;
+#pragma unroll
+      for (int i = 0; i < 15; ++i) q += (mid[i] < t) ? 1u : 0u;
+      r.w0 |= q << (4 * k);
     }
   }
   return r;

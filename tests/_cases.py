@@ -33,6 +33,7 @@ class Case:
     seed: int = 0
     spare_slots: int = 0      # extra dense capacity beyond max(lens)+1
     symmetric: bool = False   # absmax codes, scale only
+    nf4: bool = False         # normal-quantile levels (bits 4), scale only
 
 
 def make_inputs(c: Case):
@@ -69,11 +70,13 @@ def run_gpu(c: Case, inp, num_splits=0, repeat=1, fused=False):
     Lctx = inp["Lctx"]
     cap = Lctx + 1 + c.spare_slots
     if c.layout == "dense":
-        desc = K.make_desc(c.bits, c.g, c.Hkv, c.D, K.KVQ_DENSE, cap, symmetric=c.symmetric)
+        desc = K.make_desc(c.bits, c.g, c.Hkv, c.D, K.KVQ_DENSE, cap, symmetric=c.symmetric,
+                           nf4=c.nf4)
         cache = K.KVCache.allocate(desc, c.B, dev)
     else:
         desc = K.make_desc(c.bits, c.g, c.Hkv, c.D, K.KVQ_PAGED, c.page_size,
-                           inp["num_pages"], inp["table"].shape[1], symmetric=c.symmetric)
+                           inp["num_pages"], inp["table"].shape[1], symmetric=c.symmetric,
+                           nf4=c.nf4)
         cache = K.KVCache.allocate(desc, c.B, dev, torch.from_numpy(inp["table"]))
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     zeros = torch.zeros(c.B, dtype=torch.int32, device=dev)
@@ -116,9 +119,13 @@ def oracle_step(c: Case, inp):
                 hat[b, :, :L + 1] = rows.astype(np.float64)
                 ref_codes[(which, b)] = dict(raw=rows)
                 continue
-            quantize = O.quantize_groups_symmetric if c.symmetric else O.quantize_groups
-            r = quantize(rows, c.bits, c.g)
-            hat[b, :, :L + 1] = O.dequantize(r["codes"], r["scale"], r["zero"], c.g)
+            if c.nf4:
+                r = O.quantize_groups_nf4(rows, c.g)
+                hat[b, :, :L + 1] = O.dequantize_nf4(r["codes"], r["scale"], c.g)
+            else:
+                quantize = O.quantize_groups_symmetric if c.symmetric else O.quantize_groups
+                r = quantize(rows, c.bits, c.g)
+                hat[b, :, :L + 1] = O.dequantize(r["codes"], r["scale"], r["zero"], c.g)
             ref_codes[(which, b)] = dict(packed=O.pack_codes(r["codes"], c.bits),
                                          scale=r["scale"], zero=r["zero"], flags=r["flags"])
     out = O.decode_attention(inp["q"], k_hat, v_hat, lens + 1)
@@ -138,8 +145,8 @@ def gpu_codes(run, c: Case, inp, which, b):
     out["packed"] = np.stack(rows)
     for name in ("scale", "zero"):
         arr = getattr(cache, f"{which}_{name}")
-        if arr is None:     # symmetric: the zero-point is the fixed code offset
-            out[name] = np.full_like(out["scale"], 1 << (c.bits - 1))
+        if arr is None:     # symmetric: the zero-point is the fixed code offset; NF4: none
+            out[name] = None if c.nf4 else np.full_like(out["scale"], 1 << (c.bits - 1))
             continue
         t = arr.cpu().numpy()
         out[name] = np.stack([logical_rows(t, c, inp["table"], b, h, L) for h in range(c.Hkv)])

@@ -78,7 +78,7 @@ def test_cache_array_bytes(K):
 
 
 @pytest.mark.parametrize("field,value", [
-    ("bits", 5), ("bits", 2), ("group_size", 12), ("group_size", 0), ("group_size", 48),
+    ("bits", 5), ("bits", 3), ("group_size", 12), ("group_size", 0), ("group_size", 48),
     ("num_kv_heads", 0), ("layout", 3), ("capacity", 0), ("head_dim", 100)])
 def test_invalid_descriptor_rejected(K, field, value):
     d = K.make_desc(4, 32, 8, 128, K.KVQ_DENSE, 64)
@@ -179,3 +179,23 @@ def test_axis_aware_descriptor(K):
     assert K.kvq_cache_bytes(K.make_desc(4, 32, 8, 128, K.KVQ_DENSE, 48, k_per_channel=True), 1) == 0
     assert K.kvq_cache_bytes(K.make_desc(16, 0, 8, 128, K.KVQ_DENSE, 64, k_per_channel=True), 1) == 0
     assert K.kvq_cache_bytes(K.make_desc(4, 32, 8, 128, K.KVQ_DENSE, 64, sink_tokens=2), 1) == 0
+
+
+def test_lowbit_descriptors(K):
+    """INT2 packs four codes per byte; NF4 keeps a 2-byte scale per group and
+    no zero arrays; NF4 requires bits 4 and excludes the symmetric and
+    axis-aware options."""
+    import oracle as O
+    d2 = K.make_desc(2, 32, 8, 128, K.KVQ_DENSE, 64)
+    assert K.kvq_cache_bytes(d2, 1) == O.kv_cache_bytes(1, 8, 128, 1, 2, 32) == 2 * 8 * (32 + 16)
+    assert K.kvq_cache_array_bytes(d2, 1)[0] == 8 * 64 * 32
+    dn = K.make_desc(4, 64, 8, 128, K.KVQ_DENSE, 64, nf4=True)
+    assert K.kvq_cache_bytes(dn, 1) == O.kv_cache_bytes(1, 8, 128, 1, 4, 64, nf4=True)
+    for kw in (dict(bits=8), dict(bits=2), dict(symmetric=True)):
+        args = dict(bits=4, symmetric=False)
+        args.update(kw)
+        d = K.make_desc(args["bits"], 64, 8, 128, K.KVQ_DENSE, 64, symmetric=args["symmetric"], nf4=True)
+        assert K.kvq_cache_bytes(d, 1) == 0, kw
+    assert K.kvq_cache_bytes(K.make_desc(4, 64, 8, 128, K.KVQ_DENSE, 64, k_per_channel=True,
+                                         nf4=True), 1) == 0
+    assert K.kvq_cache_bytes(K.make_desc(2, 32, 8, 128, K.KVQ_DENSE, 64, k_per_channel=True), 1) == 0
