@@ -90,12 +90,13 @@ def kivi_decode_bytes(w, bits, rows, sink):
     return kv + 2 * w.batch * w.num_q_heads * D * 2
 
 
-def decode_bytes(w, bits, rows, fused=True, symmetric=False):
+def decode_bytes(w, bits, rows, fused=True, symmetric=False, group_size=None):
     """Algorithmic bytes of one step call.  Decode alone: `rows` cache rows
     (codes + scale/zero, K and V) read, q read, out written.  Fused append:
     rows - 1 cache rows read, the new row written, the new fp16 K/V read."""
     D = w.head_dim
-    per_row = D * bits // 8 + (0 if bits == 16 else (2 if symmetric else 4) * (D // w.group_size))
+    g = group_size or w.group_size
+    per_row = D * bits // 8 + (0 if bits == 16 else (2 if symmetric else 4) * (D // g))
     kv = 2 * w.batch * w.num_kv_heads * rows * per_row
     if fused:
         kv += 2 * w.batch * w.num_kv_heads * D * 2
@@ -234,16 +235,18 @@ def run_reference(args):
 # GPU arm
 # ---------------------------------------------------------------------------
 
-def build_layers(w, bits, layers, dev, seed, torch, K, synth, symmetric=False, kivi_sink=None):
+def build_layers(w, bits, layers, dev, seed, torch, K, synth, symmetric=False, kivi_sink=None,
+                 nf4=False, group_size=None):
     """Populate one cache per layer with device-drawn fp16 K/V; per-layer
     step inputs q, k_new, v_new.  kivi_sink: an axis-aware cache with that
-    many fp16 sink tokens."""
+    many fp16 sink tokens; nf4: normal-quantile levels."""
     import numpy as np
-    align = w.group_size if kivi_sink is not None else 16
+    g = group_size or w.group_size
+    align = g if kivi_sink is not None else 16
     cap = ((w.ctx[0] + 1 + align - 1) // align) * align
-    desc = K.make_desc(bits, w.group_size if bits != 16 else 0, w.num_kv_heads, w.head_dim,
+    desc = K.make_desc(bits, g if bits != 16 else 0, w.num_kv_heads, w.head_dim,
                        K.KVQ_DENSE, cap, symmetric=symmetric, k_per_channel=kivi_sink is not None,
-                       sink_tokens=kivi_sink or 0)
+                       sink_tokens=kivi_sink or 0, nf4=nf4)
     zeros = torch.zeros(w.batch, dtype=torch.int32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     caches, qs, kns, vns, host_slices = [], [], [], [], None
@@ -304,17 +307,23 @@ def run_gpu_arm(args):
     results = {}
     # formats: the headline asymmetric cache first, then the comparators
     kivi_sink = 4
-    formats = [(bits, False, None)]
+    nf4_group = 64  # the NF4 block size of the weight-quantization page
+    formats = [(bits, False, None, False, None)]
     if not args.no_symmetric:
-        formats.append((bits, True, None))
+        formats.append((bits, True, None, False, None))
     if not args.no_kivi:
-        formats.append((bits, False, kivi_sink))
+        formats.append((bits, False, kivi_sink, False, None))
+    if not args.no_lowbit:
+        formats.append((4, False, None, True, nf4_group))
+        formats.append((2, False, None, False, None))
     if args.fp16_comparator:
-        formats.append((16, False, None))
-    for fmt, sym, ksink in formats:
+        formats.append((16, False, None, False, None))
+    for fmt, sym, ksink, nf4, fgroup in formats:
         desc, caches, qs, kns, vns, host_slices = build_layers(
-            w, fmt, layers, dev, seed, torch, K, synth, symmetric=sym, kivi_sink=ksink)
-        key = "sym" if sym else ("kivi" if ksink is not None else fmt)
+            w, fmt, layers, dev, seed, torch, K, synth, symmetric=sym, kivi_sink=ksink, nf4=nf4,
+            group_size=fgroup)
+        key = ("sym" if sym else "kivi" if ksink is not None else "nf4" if nf4 else
+               "int2" if fmt == 2 else fmt)
         stream = torch.cuda.Stream(device=dev)
         lens_before = torch.full((w.batch,), w.ctx[0], dtype=torch.int32, device=dev)
         lens = lens_before + 1
@@ -432,7 +441,8 @@ def run_gpu_arm(args):
             e2e=job_throughput(tokens, world, e2e_ms), h2d=h2d, d2h=d2h, call_ms=call_ms,
             splits=splits,
             bytes=(kivi_decode_bytes(w, fmt, rows, ksink) if ksink is not None else
-                   decode_bytes(w, fmt, rows, not args.separate_append, sym)), clocks=clk,
+                   decode_bytes(w, fmt, rows, not args.separate_append, sym or nf4, fgroup)),
+            clocks=clk,
             host_slices=host_slices, out0=outs[0][:1].float().cpu().numpy(),
             launches=args.steps * layers * ((2 if args.separate_append else 1) +
                                             (1 if splits > 1 else 0)))
@@ -487,6 +497,19 @@ def run_gpu_arm(args):
             "what": f"the same step over axis-aware INT4 caches: K per channel over blocks of "
                     f"{w.group_size} tokens, V per token, {kivi_sink} fp16 sink tokens and the fp16 "
                     f"residual window; the step call is the append kernels + decode"}
+    for key, what in (("nf4", f"NF4-style caches: 4-bit codes indexing 16 normal-quantile levels, "
+                               f"one fp16 absmax scale per {nf4_group} channels; CUDA-core decode "
+                               f"kernel (no tensor-core path for lookup codes)"),
+                      ("int2", f"asymmetric INT2 g{w.group_size} caches (four codes per byte); "
+                               f"CUDA-core decode kernel")):
+        if key in results:
+            f = results[key]
+            line[f"{key}_cache"] = {
+                "value": f["value"], "unit": UNIT, "ms_per_step": f["ms_per_step"],
+                "achieved_gbs": f["bytes"] / (f["call_ms"] / 1e3) / 1e9,
+                "frac": f["bytes"] / (f["call_ms"] / 1e3) / 1e9 / peak,
+                "bytes_per_launch": f["bytes"], "avg_launch_us": f["call_ms"] * 1e3,
+                "e2e": f["e2e"], "speedup_vs_asymmetric": f["value"] / r["value"], "what": what}
     if 16 in results:
         f = results[16]
         line["fp16_cache"] = {
@@ -559,6 +582,8 @@ def main():
                     help="skip the symmetric-cache comparator")
     ap.add_argument("--no-kivi", action="store_true",
                     help="skip the axis-aware-cache comparator")
+    ap.add_argument("--no-lowbit", action="store_true",
+                    help="skip the NF4 and INT2 comparators")
     ap.add_argument("--separate-append", action="store_true",
                     help="append and attend in two calls instead of the fused call")
     args = ap.parse_args()
