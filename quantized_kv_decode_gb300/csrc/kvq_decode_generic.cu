@@ -229,7 +229,21 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
 
 }  // namespace
 
+namespace {
+// the CUDA-core kernel of kvq_decode_cc.cuh for every cache except the
+// axis-aware ones, which read per element through load_kv (kernel above)
+cudaError_t launch_cc(const DecodeParams& p, cudaStream_t stream, int* ctas_per_sm) {
+  switch (p.geom.bits) {
+    case 2: return launch_decode_cc_b2(p, stream, ctas_per_sm);
+    case 4: return launch_decode_cc_b4(p, stream, ctas_per_sm);
+    case 8: return launch_decode_cc_b8(p, stream, ctas_per_sm);
+    default: return launch_decode_cc_b16(p, stream, ctas_per_sm);
+  }
+}
+}  // namespace
+
 cudaError_t launch_decode_generic(const DecodeParams& p, cudaStream_t stream) {
+  if (!p.geom.kch) return launch_cc(p, stream, nullptr);
   const int G = p.G, D = p.geom.D;
   const size_t smem = sizeof(float) * (2 * G * D + G * kTile + 3 * G + 1) +
                       sizeof(long long) * (kTile + 1);
@@ -268,6 +282,10 @@ cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream) {
 }
 
 int generic_ctas_per_sm(const DecodeParams& p) {
+  if (!p.geom.kch) {
+    int n = 0;
+    return launch_cc(p, nullptr, &n) == cudaSuccess ? n : 0;
+  }
   const int G = p.G, D = p.geom.D;
   const size_t smem = sizeof(float) * (2 * G * D + G * kTile + 3 * G + 1) +
                       sizeof(long long) * (kTile + 1);

@@ -113,6 +113,10 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_append_kivi(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_decode_generic(const DecodeParams& p, cudaStream_t stream);
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream);
+cudaError_t launch_decode_cc_b2(const DecodeParams& p, cudaStream_t stream, int* ctas_per_sm);
+cudaError_t launch_decode_cc_b4(const DecodeParams& p, cudaStream_t stream, int* ctas_per_sm);
+cudaError_t launch_decode_cc_b8(const DecodeParams& p, cudaStream_t stream, int* ctas_per_sm);
+cudaError_t launch_decode_cc_b16(const DecodeParams& p, cudaStream_t stream, int* ctas_per_sm);
 // Tensor-core kernel for INT4/INT8 caches; *handled is false when the shape
 // (head_dim, groups, padded heads per KV head `gp`) has no instantiation.
 // With occ != nullptr nothing is launched: *occ receives the CTAs per SM.
