@@ -183,3 +183,44 @@ def test_kivi_descriptor_limits():
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     assert_close(out.cpu().numpy(), _oracle_out(q16.cpu().numpy(), k16, v16, [64], 4, 32, 4))
+
+
+def test_kivi_fullsize_mha7b():
+    """The 7B-class workload (batch 8 x 4096 cached tokens, 32 heads, head_dim
+    128, INT4 g32, 4 sinks) in the benchmark's configuration: one populating
+    append, one fused step; sampled units checked against the oracle."""
+    import torch
+    import quantized_kv_decode_gb300 as K
+    w = synth.WORKLOADS["mha7b"]
+    B, Hq, Hkv, D, g, S, L = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, 32, 4, w.ctx[0]
+    dev = "cuda"
+    rng = synth.rng_for(w.seed)
+    outl = synth.outlier_channels(rng, Hkv, D)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(1234)
+    k, v = synth.device_kv(gen, B, L + 1, Hkv, D, outl, dev)
+    q = torch.randn((B, Hq, D), generator=gen, device=dev).half()
+    cap = ((L + 1 + g - 1) // g) * g
+    desc = K.make_desc(4, g, Hkv, D, K.KVQ_DENSE, cap, k_per_channel=True, sink_tokens=S)
+    cache = K.KVCache.allocate(desc, B, dev)
+    st = torch.zeros(1, dtype=torch.int32, device=dev)
+    K.kvq_append(cache, k[:, :L].contiguous(), v[:, :L].contiguous(),
+                 torch.zeros(B, dtype=torch.int32, device=dev), st)
+    lens = torch.full((B,), L, dtype=torch.int32, device=dev)
+    out = K.kvq_append_decode_attn(cache, k[:, L].contiguous(), v[:, L].contiguous(), q, lens,
+                                   L + 1, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    G = Hq // Hkv
+    for b, kvh in ((0, 0), (B - 1, Hkv - 1), (3, 17)):
+        kk = k[b, :, kvh].cpu().numpy()[None]           # [1][L+1][D]
+        vv = v[b, :, kvh].cpu().numpy()[None]
+        r = O.kivi_quantize(kk, vv, 4, g, S)
+        S_, r0 = r["S"], r["r0"]
+        assert np.array_equal(cache.k_codes[b, kvh, S_:r0].cpu().numpy(),
+                              O.pack_codes(r["k_codes"][0], 4))
+        assert np.array_equal(cache.k_scale[b, kvh, :r["nb"]].cpu().numpy().view(np.uint16),
+                              r["k_scale"][0].view(np.uint16))
+        qh = q[b, kvh * G:(kvh + 1) * G].float().cpu().numpy().astype(np.float64)
+        want = O.attend(qh, r["k_hat"][0], r["v_hat"][0], 1.0 / np.sqrt(D))
+        assert_close(out[b, kvh * G:(kvh + 1) * G].float().cpu().numpy(), want)
