@@ -249,6 +249,12 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CT
   // SYM: symmetric caches, no zero arrays; every zero-point is 2^(BITS-1)
   constexpr unsigned short kSymZero = BITS == 4 ? 0x4800u : 0x5800u;  // fp16 8, 128
   using C = Cfg<BITS, D, NG, GP, KCH>;
+  // Token-rows layout (one query head per KV head): the score mma takes the
+  // codes as A (rows = 16 tokens) and q as B (columns = groups), half the
+  // mmas of the (group, head)-rows layout, which would leave 16 - NG rows
+  // empty.  The scores are then moved into the lanes the softmax and the V
+  // side expect.
+  constexpr bool TQ = !KCH && GP == 1;
   extern __shared__ __align__(128) uint8_t smem[];
   const CacheGeom& geo = p.geom;
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
@@ -366,7 +372,23 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CT
   // biased codes add, 1024 * (sum of the row's A entries); both by the same
   // mma against constant codes.
   float qs_lo = 0.f, qs_hi = 0.f, off_lo = 0.f, off_hi = 0.f;
-  if constexpr (!KCH) {
+  if constexpr (TQ) {
+    // B = q: per column (group) 2j and 2j+1 of this lane, the sum of q over
+    // the group and the biased codes' offset 1024 * (sum of the column)
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float bia[4] = {0.f, 0.f, 0.f, 0.f};
+    constexpr uint32_t kOnes = 0x3C003C00u;
+    constexpr uint32_t kHi = BITS == 4 ? 0x4C004C00u : 0x3C003C00u;  // x16 undoes q/16 in odd slots
+#pragma unroll
+    for (int kb = 0; kb < C::KB; ++kb) {
+      mma16816(acc, kOnes, kOnes, kHi, kHi, qa[kb][0], qa[kb][2]);
+      mma16816(bia, kH1024, kH1024, kH1024, kH1024, qa[kb][0], qa[kb][2]);
+    }
+    qs_lo = acc[0];   // column 2j
+    qs_hi = acc[1];   // column 2j + 1
+    off_lo = bia[0];
+    off_hi = bia[1];
+  } else if constexpr (!KCH) {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float bia[4] = {0.f, 0.f, 0.f, 0.f};
     constexpr uint32_t kOnes = 0x3C003C00u;   // fp16 (1, 1)
@@ -523,8 +545,10 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CT
       if constexpr (!KCH) {
         const unsigned short uk = (unsigned short)(r[0][g / 2] >> sh);
         const unsigned short uz = SYM ? kSymZero : (unsigned short)(r[1][g / 2] >> sh);
-        ksz[g * C::KROW + lane] = make_float2(__half2float(__ushort_as_half(uk)) * p.scale_log2,
-                                              __half2float(__ushort_as_half(uz)));
+        const float2 kv = make_float2(__half2float(__ushort_as_half(uk)) * p.scale_log2,
+                                      __half2float(__ushort_as_half(uz)));
+        if constexpr (TQ) ksz[lane * NG + g] = kv;   // [token][group]
+        else ksz[g * C::KROW + lane] = kv;           // [group][token]
       }
       vs[g * C::VROW + lane] = (unsigned short)(r[2][g / 2] >> sh);
       vz[g * C::VROW + lane] = SYM ? kSymZero : (unsigned short)(r[3][g / 2] >> sh);
@@ -592,6 +616,74 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CT
 #pragma unroll
         for (int e = 0; e < 4; ++e) Aop[kb][e] = qa[kb][e];
     }
+    if constexpr (TQ) {
+      float s4[4];  // this lane's tokens rho + 8i, i = 0..3
+#pragma unroll
+      for (int np = 0; np < 2; ++np) {
+        uint32_t w[2][C::CHUNKS];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int tok = 8 * (2 * np + u) + (lane & 7);
+          if constexpr (C::CHUNKS == 2) {
+            ldsm_x2(kc_s + C::at(tok, (lane >> 3) & 1), w[u][0], w[u][1]);
+          } else {
+#pragma unroll
+            for (int c4 = 0; c4 < C::CHUNKS; c4 += 4)
+              ldsm_x4(kc_s + C::at(tok, c4 + (lane >> 3)), w[u][c4], w[u][c4 + 1], w[u][c4 + 2],
+                      w[u][c4 + 3]);
+          }
+        }
+        // rows: tokens rho (octet 2np) and rho + 8 (octet 2np + 1); two
+        // accumulator chains (even / odd k-blocks)
+        float acc[2][4] = {{-off_lo, -off_hi, -off_lo, -off_hi}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+        for (int c = 0; c < C::CHUNKS; ++c) {
+          if constexpr (BITS == 4) {
+            uint32_t h0[4], h1[4];
+            nib8_to_h2_biased(w[0][c], h0);
+            nib8_to_h2_biased(w[1][c], h1);
+            mma16816(acc[0], h0[0], h1[0], h0[1], h1[1], qa[2 * c][0], qa[2 * c][2]);
+            mma16816(acc[1], h0[2], h1[2], h0[3], h1[3], qa[2 * c + 1][0], qa[2 * c + 1][2]);
+          } else {
+            const uint32_t a0 = byte2_to_h2_biased<0x4140>(w[0][c]);
+            const uint32_t a1 = byte2_to_h2_biased<0x4140>(w[1][c]);
+            const uint32_t a2 = byte2_to_h2_biased<0x4342>(w[0][c]);
+            const uint32_t a3 = byte2_to_h2_biased<0x4342>(w[1][c]);
+            mma16816(acc[c & 1], a0, a1, a2, a3, qa[c][0], qa[c][2]);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          // columns 2j, 2j+1 = groups 2j, 2j+1: s (sum q c - z sum q), then
+          // the groups of the other lanes of this token
+          float v = 0.f;
+          if (2 * j < NG) {
+            const int t = 16 * np + 8 * i + rho;
+            const float4 sz = *reinterpret_cast<const float4*>(ksz + t * NG + 2 * j);
+            v = sz.x * fmaf(-sz.y, qs_lo, acc[0][2 * i] + acc[1][2 * i]);
+            if (2 * j + 1 < NG) v = fmaf(sz.z, fmaf(-sz.w, qs_hi, acc[0][2 * i + 1] + acc[1][2 * i + 1]), v);
+          }
+          v += __shfl_xor_sync(0xffffffffu, v, 1);
+          v += __shfl_xor_sync(0xffffffffu, v, 2);
+          s4[2 * np + i] = v;
+        }
+      }
+      // into the softmax layout: token 8 nt + 2j + e of this lane lives in
+      // lane 4 (2j + e) as s4[nt]
+#pragma unroll
+      for (int nt = 0; nt < 4; ++nt) {
+        const int ta = 8 * nt + 2 * j;
+        float va = __shfl_sync(0xffffffffu, s4[nt], (2 * j) << 2);
+        float vb = __shfl_sync(0xffffffffu, s4[nt], (2 * j + 1) << 2);
+        if (bad) {  // warp-uniform
+          const float2 mk = *reinterpret_cast<const float2*>(madd + ta);
+          va += mk.x;
+          vb += mk.y;
+        }
+        sc[nt][0] = va + hmask;
+        sc[nt][1] = vb + hmask;
+      }
+    } else {
 #pragma unroll
     for (int np = 0; np < 2; ++np) {
       uint32_t w[2][C::CHUNKS];
@@ -679,6 +771,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CT
         sc[nt][1] = vb + hmask;
       }
     }
+    }  // (group, head)-rows layout
   };
 
   // online softmax over the tile; pp = fp16 probabilities of this lane's tokens
