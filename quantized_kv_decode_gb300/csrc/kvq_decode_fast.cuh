@@ -663,8 +663,9 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CT
             v = sz.x * fmaf(-sz.y, qs_lo, acc[0][2 * i] + acc[1][2 * i]);
             if (2 * j + 1 < NG) v = fmaf(sz.z, fmaf(-sz.w, qs_hi, acc[0][2 * i + 1] + acc[1][2 * i + 1]), v);
           }
-          v += __shfl_xor_sync(0xffffffffu, v, 1);
-          v += __shfl_xor_sync(0xffffffffu, v, 2);
+          // lane (rho, 0) must end with all groups: it is the one read below
+          if constexpr (NG > 2) v += __shfl_xor_sync(0xffffffffu, v, 1);
+          if constexpr (NG > 4) v += __shfl_xor_sync(0xffffffffu, v, 2);
           s4[2 * np + i] = v;
         }
       }
