@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CT
   // mmas of the (group, head)-rows layout, which would leave 16 - NG rows
   // empty.  The scores are then moved into the lanes the softmax and the V
   // side expect.
-  constexpr bool TQ = !KCH && GP == 1;
+  constexpr bool TQ = GP == 1;
   extern __shared__ __align__(128) uint8_t smem[];
   const CacheGeom& geo = p.geom;
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
@@ -585,9 +585,33 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CT
     // starts at -(1024 sum(A) + sum(A z)), from mmas against B column 0 =
     // 1024 and column 1 = z.
     uint32_t Aop[C::KB][4];
-    uint32_t Alo[KCH ? C::KB : 1][2];
-    float kinit = 0.f;
-    if constexpr (KCH) {
+    uint32_t Alo[(KCH && !TQ) ? C::KB : 1][2];
+    uint32_t Bq[(KCH && TQ) ? C::KB : 1][2];
+    float kinit = 0.f, kci0 = 0.f, kci1 = 0.f;
+    if constexpr (KCH && TQ) {
+      // token rows: B column 0 = q s (hi), column 1 = its lo part, so one
+      // mma per k-block carries both; the starts -(1024 sum B + sum z B) of
+      // both columns come from mmas with A = 1024 and A = z (every row)
+      const __half* sz = reinterpret_cast<const __half*>(ksz) + j * C::KB * 4;
+      float ci[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int kb = 0; kb < C::KB; ++kb) {
+        const uint2 sv = *reinterpret_cast<const uint2*>(sz + kb * 4);
+        const uint2 zv = *reinterpret_cast<const uint2*>(sz + 4 * 4 * C::KB + kb * 4);
+        const __half2 h01 = __hmul2(u32_as_h2(qa[kb][0]), u32_as_h2(sv.x));
+        const __half2 h23 = __hmul2(u32_as_h2(qa[kb][2]), u32_as_h2(sv.y));
+        const uint32_t l01 = h2_as_u32(__hfma2(u32_as_h2(qa[kb][0]), u32_as_h2(sv.x), __hneg2(h01)));
+        const uint32_t l23 = h2_as_u32(__hfma2(u32_as_h2(qa[kb][2]), u32_as_h2(sv.y), __hneg2(h23)));
+        Bq[kb][0] = rho == 0 ? h2_as_u32(h01) : (rho == 1 ? l01 : 0u);
+        Bq[kb][1] = rho == 0 ? h2_as_u32(h23) : (rho == 1 ? l23 : 0u);
+        const uint32_t z23 = BITS == 4 ? h2_as_u32(__hmul2(u32_as_h2(zv.y), u32_as_h2(0x4C004C00u)))
+                                       : zv.y;
+        mma16816(ci, kH1024, kH1024, kH1024, kH1024, Bq[kb][0], Bq[kb][1]);
+        mma16816(ci, zv.x, zv.x, z23, z23, Bq[kb][0], Bq[kb][1]);
+      }
+      kci0 = -ci[0];  // column 2j
+      kci1 = -ci[1];  // column 2j + 1
+    } else if constexpr (KCH) {
       const __half* sz = reinterpret_cast<const __half*>(ksz) + j * C::KB * 4;
       float ci[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -635,21 +659,26 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CT
         }
         // rows: tokens rho (octet 2np) and rho + 8 (octet 2np + 1); two
         // accumulator chains (even / odd k-blocks)
-        float acc[2][4] = {{-off_lo, -off_hi, -off_lo, -off_hi}, {0.f, 0.f, 0.f, 0.f}};
+        const float c0 = KCH ? kci0 : -off_lo, c1 = KCH ? kci1 : -off_hi;
+        float acc[2][4] = {{c0, c1, c0, c1}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
         for (int c = 0; c < C::CHUNKS; ++c) {
           if constexpr (BITS == 4) {
             uint32_t h0[4], h1[4];
             nib8_to_h2_biased(w[0][c], h0);
             nib8_to_h2_biased(w[1][c], h1);
-            mma16816(acc[0], h0[0], h1[0], h0[1], h1[1], qa[2 * c][0], qa[2 * c][2]);
-            mma16816(acc[1], h0[2], h1[2], h0[3], h1[3], qa[2 * c + 1][0], qa[2 * c + 1][2]);
+            const uint32_t b00 = KCH ? Bq[2 * c][0] : qa[2 * c][0];
+            const uint32_t b01 = KCH ? Bq[2 * c][1] : qa[2 * c][2];
+            const uint32_t b10 = KCH ? Bq[2 * c + 1][0] : qa[2 * c + 1][0];
+            const uint32_t b11 = KCH ? Bq[2 * c + 1][1] : qa[2 * c + 1][2];
+            mma16816(acc[0], h0[0], h1[0], h0[1], h1[1], b00, b01);
+            mma16816(acc[1], h0[2], h1[2], h0[3], h1[3], b10, b11);
           } else {
             const uint32_t a0 = byte2_to_h2_biased<0x4140>(w[0][c]);
             const uint32_t a1 = byte2_to_h2_biased<0x4140>(w[1][c]);
             const uint32_t a2 = byte2_to_h2_biased<0x4342>(w[0][c]);
             const uint32_t a3 = byte2_to_h2_biased<0x4342>(w[1][c]);
-            mma16816(acc[c & 1], a0, a1, a2, a3, qa[c][0], qa[c][2]);
+            mma16816(acc[c & 1], a0, a1, a2, a3, KCH ? Bq[c][0] : qa[c][0], KCH ? Bq[c][1] : qa[c][2]);
           }
         }
 #pragma unroll
@@ -657,15 +686,19 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CT
           // columns 2j, 2j+1 = groups 2j, 2j+1: s (sum q c - z sum q), then
           // the groups of the other lanes of this token
           float v = 0.f;
-          if (2 * j < NG) {
+          if constexpr (KCH) {
+            // lane (rho, 0): column 0 (hi) + column 1 (lo); scales already in q
+            v = ((acc[0][2 * i] + acc[1][2 * i]) + (acc[0][2 * i + 1] + acc[1][2 * i + 1])) *
+                p.scale_log2;
+          } else if (2 * j < NG) {
             const int t = 16 * np + 8 * i + rho;
             const float4 sz = *reinterpret_cast<const float4*>(ksz + t * NG + 2 * j);
             v = sz.x * fmaf(-sz.y, qs_lo, acc[0][2 * i] + acc[1][2 * i]);
             if (2 * j + 1 < NG) v = fmaf(sz.z, fmaf(-sz.w, qs_hi, acc[0][2 * i + 1] + acc[1][2 * i + 1]), v);
           }
           // lane (rho, 0) must end with all groups: it is the one read below
-          if constexpr (NG > 2) v += __shfl_xor_sync(0xffffffffu, v, 1);
-          if constexpr (NG > 4) v += __shfl_xor_sync(0xffffffffu, v, 2);
+          if constexpr (!KCH && NG > 2) v += __shfl_xor_sync(0xffffffffu, v, 1);
+          if constexpr (!KCH && NG > 4) v += __shfl_xor_sync(0xffffffffu, v, 2);
           s4[2 * np + i] = v;
         }
       }
