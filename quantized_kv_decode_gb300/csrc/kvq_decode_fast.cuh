@@ -249,12 +249,12 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CT
   // SYM: symmetric caches, no zero arrays; every zero-point is 2^(BITS-1)
   constexpr unsigned short kSymZero = BITS == 4 ? 0x4800u : 0x5800u;  // fp16 8, 128
   using C = Cfg<BITS, D, NG, GP, KCH>;
-  // Token-rows layout (one query head per KV head): the score mma takes the
-  // codes as A (rows = 16 tokens) and q as B (columns = groups), half the
-  // mmas of the (group, head)-rows layout, which would leave 16 - NG rows
-  // empty.  The scores are then moved into the lanes the softmax and the V
-  // side expect.
-  constexpr bool TQ = GP == 1;
+  // Token-rows layout, whenever the (group, head) pairs fill at most 8 rows
+  // of the (group, head)-rows layout: the score mma takes the codes as A
+  // (rows = 16 tokens) and q as B (columns = (group, head) pairs), half the
+  // mmas.  The scores are then moved into the lanes the softmax and the V
+  // side expect.  Axis-aware caches use it for one query head per KV head.
+  constexpr bool TQ = GP == 1 || (!KCH && GP <= 4 && NG * GP <= 8);
   extern __shared__ __align__(128) uint8_t smem[];
   const CacheGeom& geo = p.geom;
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
@@ -690,25 +690,46 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CT
             // lane (rho, 0): column 0 (hi) + column 1 (lo); scales already in q
             v = ((acc[0][2 * i] + acc[1][2 * i]) + (acc[0][2 * i + 1] + acc[1][2 * i + 1])) *
                 p.scale_log2;
-          } else if (2 * j < NG) {
-            const int t = 16 * np + 8 * i + rho;
-            const float4 sz = *reinterpret_cast<const float4*>(ksz + t * NG + 2 * j);
-            v = sz.x * fmaf(-sz.y, qs_lo, acc[0][2 * i] + acc[1][2 * i]);
-            if (2 * j + 1 < NG) v = fmaf(sz.z, fmaf(-sz.w, qs_hi, acc[0][2 * i + 1] + acc[1][2 * i + 1]), v);
+          } else if constexpr (GP == 1) {
+            if (2 * j < NG) {
+              const int t = 16 * np + 8 * i + rho;
+              const float4 sz = *reinterpret_cast<const float4*>(ksz + t * NG + 2 * j);
+              v = sz.x * fmaf(-sz.y, qs_lo, acc[0][2 * i] + acc[1][2 * i]);
+              if (2 * j + 1 < NG)
+                v = fmaf(sz.z, fmaf(-sz.w, qs_hi, acc[0][2 * i + 1] + acc[1][2 * i + 1]), v);
+            }
+            // lane (rho, 0) must end with all groups: it is the one read below
+            if constexpr (NG > 2) v += __shfl_xor_sync(0xffffffffu, v, 1);
+            if constexpr (NG > 4) v += __shfl_xor_sync(0xffffffffu, v, 2);
+          } else {
+            // columns 2j, 2j+1 = heads 2j % GP and the next one, both of group
+            // 2j / GP.  Lane j keeps one head, (j / (GP/2)) & 1 of its pair,
+            // and sends the other to lane j ^ (GP/2), which holds the same
+            // heads of another group and keeps the other one; GP = 2 then
+            // adds the remaining groups' lanes.
+            float v0 = 0.f, v1 = 0.f;
+            if (2 * j < NG * GP) {
+              const int t = 16 * np + 8 * i + rho;
+              const float2 sz = ksz[t * NG + (2 * j) / GP];
+              v0 = sz.x * fmaf(-sz.y, qs_lo, acc[0][2 * i] + acc[1][2 * i]);
+              v1 = sz.x * fmaf(-sz.y, qs_hi, acc[0][2 * i + 1] + acc[1][2 * i + 1]);
+            }
+            const bool sel = (j / (GP / 2)) & 1;
+            v = (sel ? v1 : v0) + __shfl_xor_sync(0xffffffffu, sel ? v0 : v1, GP / 2);
+            if constexpr (GP == 2 && NG > 2) v += __shfl_xor_sync(0xffffffffu, v, 2);
           }
-          // lane (rho, 0) must end with all groups: it is the one read below
-          if constexpr (!KCH && NG > 2) v += __shfl_xor_sync(0xffffffffu, v, 1);
-          if constexpr (!KCH && NG > 4) v += __shfl_xor_sync(0xffffffffu, v, 2);
           s4[2 * np + i] = v;
         }
       }
-      // into the softmax layout: token 8 nt + 2j + e of this lane lives in
-      // lane 4 (2j + e) as s4[nt]
+      // into the softmax layout: token 8 nt + 2j + e of this lane's head
+      // h_lane lives as s4[nt] in lane 4 (2j + e) + jsrc, the lane that kept
+      // that head
+      const int jsrc = (h_lane >> 1) + (h_lane & 1) * (GP / 2);
 #pragma unroll
       for (int nt = 0; nt < 4; ++nt) {
         const int ta = 8 * nt + 2 * j;
-        float va = __shfl_sync(0xffffffffu, s4[nt], (2 * j) << 2);
-        float vb = __shfl_sync(0xffffffffu, s4[nt], (2 * j + 1) << 2);
+        float va = __shfl_sync(0xffffffffu, s4[nt], ((2 * j) << 2) | jsrc);
+        float vb = __shfl_sync(0xffffffffu, s4[nt], ((2 * j + 1) << 2) | jsrc);
         if (bad) {  // warp-uniform
           const float2 mk = *reinterpret_cast<const float2*>(madd + ta);
           va += mk.x;

@@ -109,3 +109,43 @@ def test_unmapped_page_flags_block_table():
     o = out.cpu().numpy()
     assert np.array_equal(o[0].view(np.uint16), run["out"][0].view(np.uint16))
     assert np.isfinite(o[1].astype(np.float32)).all()
+
+
+@pytest.mark.parametrize("bits,g,D,Hq,Hkv,sym", [
+    (4, 32, 128, 4, 2, False),    # 2 heads x 4 groups: 8 score columns, two group-sum levels
+    (4, 64, 128, 4, 2, False),    # 2 heads x 2 groups
+    (4, 64, 128, 12, 4, False),   # 3 heads padded to 4, x 2 groups
+    (4, 64, 128, 16, 4, True),    # 4 heads x 2 groups, symmetric codes
+    (8, 64, 128, 16, 4, False),   # INT8, 4 heads x 2 groups
+    (8, 32, 128, 8, 4, True),     # INT8 symmetric, 2 heads x 4 groups
+    (8, 32, 64, 8, 4, False),     # INT8 head_dim 64, 2 heads x 2 groups
+    (4, 32, 64, 16, 4, False),    # head_dim 64, 4 heads x 2 groups
+    (4, 32, 64, 6, 2, False),     # head_dim 64, 3 heads padded to 4
+])
+def test_token_rows_gqa(bits, g, D, Hq, Hkv, sym):
+    """GQA shapes whose (group, head) pairs fit 8 score columns take the
+    token-rows score layout: ragged lengths around the 32-token tile (0, 31,
+    32, 33 cached tokens), several splits, and the fused step."""
+    rng = np.random.default_rng(bits * 7 + g + D + Hq)
+    lens = np.array([0, 31, 32, 33, int(rng.integers(300, 700))])
+    c = Case(B=5, Hq=Hq, Hkv=Hkv, D=D, bits=bits, g=g, lens=lens, seed=int(lens.sum()) % 97,
+             symmetric=sym)
+    for s in (0, 1, 3):
+        _check(c, num_splits=s)
+    inp = make_inputs(c)
+    run = run_gpu(c, inp, num_splits=2, fused=True)
+    ref, _ = oracle_step(c, inp)
+    assert run["status"] == 0
+    assert_close(run["out"], ref)
+
+
+def test_token_rows_gqa_paged_matches_dense():
+    """The token-rows GQA layout over a paged cache gives the dense result
+    bit for bit."""
+    lens = np.array([130, 1, 64, 47, 300])
+    dense = Case(B=5, Hq=16, Hkv=4, D=128, bits=4, g=64, lens=lens, seed=23)
+    paged = Case(B=5, Hq=16, Hkv=4, D=128, bits=4, g=64, lens=lens, seed=23, layout="paged",
+                 page_size=16)
+    rd, _ = _check(dense, num_splits=2)
+    rp, _ = _check(paged, num_splits=2)
+    assert np.array_equal(rd["out"].view(np.uint16), rp["out"].view(np.uint16))
