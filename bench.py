@@ -491,6 +491,8 @@ def run_gpu_arm(args):
 
     r = results[bits]
     peak, peak_kind = measured_peaks()
+    workloads = (run_workloads(dev, torch, K, synth, peak, args.steps)
+                 if world == 1 and not args.no_workloads else None)
     achieved = r["bytes"] / (r["call_ms"] / 1e3) / 1e9
     traffic = load_profiled_traffic()
     line = {
@@ -561,6 +563,8 @@ def run_gpu_arm(args):
                              "K/V (decode only, no append), per layer call"},
             "speedup_int4_vs_fp16_sdpa_per_call": f["sdpa_ms"] / r["call_ms"],
             "speedup_int4_vs_fp16_library_step": r["value"] / f["value"]}
+    if workloads:
+        line["workloads"] = workloads
     if world == 1 and not args.no_cpu_baseline:
         s = oracle_sample_setup(w, bits, None, kv=r["host_slices"])
         ref = oracle_step(w, bits, s)
@@ -577,6 +581,105 @@ def run_gpu_arm(args):
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+def run_workloads(dev, torch, K, synth, peak, steps):
+    """The other workloads of the build, one fused step call per layer cache
+    (append the step's token, then attend), timed in a CUDA graph over enough
+    layer caches to exceed L2.  Ragged lengths and paged block tables follow
+    the seeded recipe of each workload; a paged sequence maps exactly the
+    pages its rows need."""
+    import numpy as np
+    plan = [("gqa_mix", 4, 8), ("long", 4, 8), ("long", 8, 6), ("paged", 4, 12)]
+    out = {}
+    for name, bits, layers in plan:
+        w = synth.WORKLOADS[name]
+        rng = synth.rng_for(w.seed)
+        lens = synth.context_lengths(rng, w.batch, *w.ctx)
+        B, Hq, Hkv, D, g = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim, w.group_size
+        Lmax = int(lens.max())
+        status = torch.zeros(1, dtype=torch.int32, device=dev)
+        if w.layout == "paged":
+            table, num_pages = synth.block_table(rng, lens + 1, w.page_size)
+            desc = K.make_desc(bits, g, Hkv, D, K.KVQ_PAGED, w.page_size, num_pages,
+                               table.shape[1])
+            bt = torch.from_numpy(table)
+        else:
+            desc = K.make_desc(bits, g, Hkv, D, K.KVQ_DENSE, ((Lmax + 1 + 15) // 16) * 16)
+            bt = None
+        caches, qs, kns, vns = [], [], [], []
+        for l in range(layers):
+            gen = torch.Generator(device=dev)
+            gen.manual_seed(w.seed * 100003 + l)
+            outl = synth.outlier_channels(np.random.default_rng(w.seed * 100003 + l), Hkv, D)
+            cache = K.KVCache.allocate(desc, B, dev, block_table=bt)
+            if bt is None:
+                k, v = synth.device_kv(gen, B, Lmax, Hkv, D, outl, dev)
+                K.kvq_append(cache, k, v, torch.zeros(B, dtype=torch.int32, device=dev), status)
+                del k, v
+            else:
+                zero1 = torch.zeros(1, dtype=torch.int32, device=dev)
+                for b in range(B):  # each sequence fills only its own pages
+                    view = K.KVCache(desc, 1, cache.k_codes, cache.v_codes, cache.k_scale,
+                                     cache.k_zero, cache.v_scale, cache.v_zero,
+                                     cache.block_table[b:b + 1])
+                    k, v = synth.device_kv(gen, 1, int(lens[b]), Hkv, D, outl, dev)
+                    K.kvq_append(view, k, v, zero1, status)
+                del k, v
+            caches.append(cache)
+            kn, vn = synth.device_kv(gen, B, 1, Hkv, D, outl, dev)
+            kns.append(kn[:, 0])
+            vns.append(vn[:, 0])
+            qs.append(torch.randn((B, Hq, D), generator=gen, device=dev).half())
+        torch.cuda.synchronize()
+        if int(status.item()) != 0:
+            raise RuntimeError(f"{name}: populate flagged status {int(status.item()):#x}")
+        lens_before = torch.from_numpy(lens).to(dev)
+        rows = Lmax + 1
+        splits = K.kvq_decode_num_splits(desc, B, Hq, rows, 0)
+        ws = torch.empty(max(16, K.kvq_decode_workspace_size(desc, B, Hq, rows, 0)),
+                         dtype=torch.uint8, device=dev)
+        outs = [torch.empty_like(q) for q in qs]
+        stream = torch.cuda.Stream(device=dev)
+
+        def step():
+            for l in range(layers):
+                K.kvq_append_decode_attn(caches[l], kns[l], vns[l], qs[l], lens_before, rows,
+                                         outs[l], ws, status, stream=stream)
+
+        with torch.cuda.stream(stream):
+            step()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                graph.replay()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        reps = max(3, steps // 2)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if int(status.item()) != 0:
+            raise RuntimeError(f"{name}: device status {int(status.item()):#x}")
+        call_s = e0.elapsed_time(e1) / 1e3 / (reps * layers)
+        per_row = D * bits // 8 + 4 * (D // g)
+        nbytes = (2 * Hkv * int((lens + 1).sum()) * per_row + 2 * B * Hkv * D * 2 +
+                  2 * B * Hq * D * 2)
+        out[f"{name}_int{bits}"] = {
+            "what": f"{w.note}; INT{bits} group {g}; fused append + decode per layer cache",
+            "layers": layers, "splits": splits, "avg_launch_us": call_s * 1e6,
+            "tokens_per_s": B / call_s, "bytes_per_launch": nbytes,
+            "achieved_gbs": nbytes / call_s / 1e9, "frac": nbytes / call_s / 1e9 / peak}
+        del caches, graph, ws, outs
+        torch.cuda.empty_cache()
+    return out
 
 
 def reduce_max_over_ranks(x, world, device):
@@ -629,6 +732,8 @@ def main():
                     help="skip the axis-aware-cache comparator")
     ap.add_argument("--no-lowbit", action="store_true",
                     help="skip the NF4 and INT2 comparators")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the GQA-mix, long-context and paged workloads")
     ap.add_argument("--separate-append", action="store_true",
                     help="append and attend in two calls instead of the fused call")
     args = ap.parse_args()

@@ -152,6 +152,7 @@ int32_t choose_splits(int64_t units, int64_t max_len, int32_t requested, int cta
 struct Plan {
   bool fast = false;
   int gp = 1;
+  int occ = 0;  // tensor-core kernel: resident CTAs per SM
   int32_t splits = 0;
 };
 
@@ -164,7 +165,7 @@ kvq_status make_plan(const kvq_cache_desc* desc, const CacheGeom& geom, int32_t 
     int gp = 1;
     while (gp < G) gp <<= 1;
     plan->gp = gp;
-    if (requested > 0) {
+    if (requested > 0) {  // no device query: the occupancy is looked up at launch if needed
       plan->splits = choose_splits((int64_t)batch * desc->num_kv_heads, max_seq_len, requested, 0);
       return KVQ_OK;
     }
@@ -176,6 +177,7 @@ kvq_status make_plan(const kvq_cache_desc* desc, const CacheGeom& geom, int32_t 
                                     : launch_decode_fast_int8(probe, gp, nullptr, &handled, &occ);
     if (handled && e != cudaSuccess) return KVQ_ERR_CUDA;
     plan->fast = handled;
+    if (handled) plan->occ = occ;
   }
   if (requested > 0) {
     plan->splits = choose_splits((int64_t)batch * desc->num_kv_heads, max_seq_len, requested, 0);
@@ -405,6 +407,23 @@ kvq_status decode_impl(const kvq_cache_desc* desc, const kvq_cache* cache, int32
   p.len_limit = (int32_t)std::min<int64_t>(cap, max_seq_len);
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)desc->head_dim);
   p.scale_log2 = scale * 1.4426950408889634f;
+  // more CTAs than fit at once: start the longest sequences first, so that
+  // the last wave holds short ones
+  const bool fast_shape = (desc->bits == 4 || desc->bits == 8) && !desc->nf4 && G <= 8;
+  int occ = plan.occ;
+  if (fast_shape && occ == 0 && batch > 1 && batch <= kLongestFirstMaxBatch) {
+    DecodeParams probe{};
+    probe.geom = p.geom;
+    probe.G = G;
+    bool fast = false;
+    const cudaError_t pe = desc->bits == 4
+        ? launch_decode_fast_int4(probe, plan.gp, nullptr, &fast, &occ)
+        : launch_decode_fast_int8(probe, plan.gp, nullptr, &fast, &occ);
+    if (fast && pe != cudaSuccess) return KVQ_ERR_CUDA;
+    if (!fast) occ = 0;
+  }
+  p.longest_first = fast_shape && occ > 0 && batch > 1 && batch <= kLongestFirstMaxBatch &&
+                    (int64_t)splits * desc->num_kv_heads * batch > (int64_t)sm_count() * occ;
 
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaSuccess;

@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CT
   constexpr bool TQ = GP == 1 || (!KCH && GP <= 4 && NG * GP <= 8);
   extern __shared__ __align__(128) uint8_t smem[];
   const CacheGeom& geo = p.geom;
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int split = blockIdx.x, kvh = blockIdx.y;
   const int G = p.G;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int rho = lane >> 2, j = lane & 3;
@@ -270,7 +270,8 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CT
   // that wrote the cache is still seen.
   pdl_launch_dependents();
   if constexpr (!KCH) {
-    if (geo.layout == KVQ_DENSE && lane < C::STAGES * 6) {
+    if (!p.longest_first && geo.layout == KVQ_DENSE && lane < C::STAGES * 6) {
+      const int b = blockIdx.z;
       const int it = lane / 6, region = lane % 6;
       const int t0g = split * p.chunk;
       const int t1g = min(geo.slots, t0g + p.chunk);
@@ -291,6 +292,8 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CT
   }
   pdl_wait();
 
+  const int b = p.longest_first ? longest_first_seq(p, blockIdx.z, reinterpret_cast<int*>(smem))
+                                : (int)blockIdx.z;
   int L = seq_len_of(p, b);
   if (L < 0 || L > p.len_limit) {
     if (threadIdx.x == 0 && split == 0 && kvh == 0 && p.status) atomicOr(p.status, KVQ_FLAG_SEQ_LEN);

@@ -97,6 +97,10 @@ struct DecodeParams {
   const __half* new_kv[2];
   const __half* window[2];  // axis-aware caches: fp16 sinks + residual, K and V
   float nf4_level[16];      // NF4: the 16 levels (fp16 values as fp32)
+  // Tensor-core kernel: grid index z is a rank in the longest-first order of
+  // the batch instead of the sequence index (set for grids of more than one
+  // wave, so that the longest sequences start first)
+  int32_t longest_first;
 };
 
 // Tokens to attend over for sequence b (-1 for a length that cannot be formed).
@@ -106,6 +110,31 @@ __device__ __forceinline__ int seq_len_of(const DecodeParams& p, int b) {
     return (x < 0 || x == 0x7fffffff) ? -1 : x + 1;
   }
   return __ldg(p.seq_lens + b);
+}
+
+// The sequence of rank r when the batch is ordered by attended length,
+// longest first, ties by index (the keys are distinct, so the ranks are a
+// permutation).  Every thread of the CTA calls it; `scratch` is shared memory
+// for batch + 1 ints, free again on return.
+constexpr int kLongestFirstMaxBatch = 128;
+__device__ __forceinline__ int longest_first_seq(const DecodeParams& p, int r, int* scratch) {
+  const int B = p.batch;
+  for (int i = threadIdx.x; i < B; i += blockDim.x) scratch[i] = seq_len_of(p, i);
+  __syncthreads();
+  for (int c = threadIdx.x; c < B; c += blockDim.x) {
+    const int Lc = scratch[c];
+    int rank = 0;
+#pragma unroll 8
+    for (int i = 0; i < B; ++i) {
+      const int Li = scratch[i];
+      rank += (Li > Lc) | ((Li == Lc) & (i < c));
+    }
+    if (rank == r) scratch[B] = c;
+  }
+  __syncthreads();
+  const int b = scratch[B];
+  __syncthreads();
+  return b;
 }
 
 // Launchers (return a CUDA error code; the caller maps it to kvq_status).

@@ -149,3 +149,29 @@ def test_token_rows_gqa_paged_matches_dense():
     rd, _ = _check(dense, num_splits=2)
     rp, _ = _check(paged, num_splits=2)
     assert np.array_equal(rd["out"].view(np.uint16), rp["out"].view(np.uint16))
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,D,g,layout,fused", [
+    (40, 16, 8, 128, 32, "dense", False),    # 320 CTAs: more than one wave of the SMs
+    (40, 32, 8, 128, 64, "dense", True),     # fused append, token-rows GQA
+    (120, 28, 4, 64, 32, "paged", False),    # 7 heads per KV head, 16-token pages
+    (160, 4, 2, 64, 32, "dense", False),     # a batch above the longest-first cap
+])
+def test_multiwave_ragged_batches(B, Hq, Hkv, D, g, layout, fused):
+    """Grids larger than one wave run the batch longest sequence first (grid
+    index z is a rank in that order).  Every sequence must still get its own
+    output: ragged lengths with ties, an empty context and the longest
+    sequence last in the batch."""
+    rng = np.random.default_rng(B + Hq + D)
+    lens = rng.integers(0, 400, size=B)
+    lens[:5] = 17                                # ties broken by index
+    lens[5] = 0
+    lens[-1] = 450                               # the longest sequence sits last
+    c = Case(B=B, Hq=Hq, Hkv=Hkv, D=D, bits=4, g=g, lens=lens, seed=B % 89, layout=layout,
+             page_size=16)
+    inp = make_inputs(c)
+    ref, _ = oracle_step(c, inp)
+    for s in (0, 1):
+        run = run_gpu(c, inp, num_splits=s, fused=fused)
+        assert run["status"] == 0
+        assert_close(run["out"], ref)
