@@ -15,6 +15,8 @@ namespace {
 // KIND: 0 asymmetric, 1 symmetric, 2 NF4 (BITS 4)
 template <int BITS, int KIND>
 __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
   constexpr bool SYM = KIND == 1;
   const CacheGeom& c = p.geom;
   const int which = blockIdx.y;  // 0: K, 1: V
@@ -95,16 +97,15 @@ cudaError_t launch_append(const AppendParams& p, cudaStream_t stream) {
   const dim3 grid((unsigned)((n_units + 255) / 256), 2);
   const int kind = c.nf4 ? 2 : (c.sym ? 1 : 0);
   switch (c.bits * 4 + kind) {
-    case 8:  append_kernel<2, 0><<<grid, block, 0, stream>>>(p); break;
-    case 9:  append_kernel<2, 1><<<grid, block, 0, stream>>>(p); break;
-    case 16: append_kernel<4, 0><<<grid, block, 0, stream>>>(p); break;
-    case 17: append_kernel<4, 1><<<grid, block, 0, stream>>>(p); break;
-    case 18: append_kernel<4, 2><<<grid, block, 0, stream>>>(p); break;
-    case 32: append_kernel<8, 0><<<grid, block, 0, stream>>>(p); break;
-    case 33: append_kernel<8, 1><<<grid, block, 0, stream>>>(p); break;
-    default: append_kernel<16, 0><<<grid, block, 0, stream>>>(p); break;
+    case 8:  return launch_pdl(append_kernel<2, 0>, grid, block, 0, stream, p);
+    case 9:  return launch_pdl(append_kernel<2, 1>, grid, block, 0, stream, p);
+    case 16: return launch_pdl(append_kernel<4, 0>, grid, block, 0, stream, p);
+    case 17: return launch_pdl(append_kernel<4, 1>, grid, block, 0, stream, p);
+    case 18: return launch_pdl(append_kernel<4, 2>, grid, block, 0, stream, p);
+    case 32: return launch_pdl(append_kernel<8, 0>, grid, block, 0, stream, p);
+    case 33: return launch_pdl(append_kernel<8, 1>, grid, block, 0, stream, p);
+    default: return launch_pdl(append_kernel<16, 0>, grid, block, 0, stream, p);
   }
-  return cudaGetLastError();
 }
 
 }  // namespace kvq

@@ -38,6 +38,8 @@ __device__ __forceinline__ const __half* token_src(const AppendParams& p, int wh
 
 template <int BITS>
 __global__ void __launch_bounds__(kBlockThreads) kivi_block_kernel(const AppendParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
   const CacheGeom& c = p.geom;
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int S = c.sink, g = c.g, D = c.D;
@@ -116,6 +118,8 @@ __global__ void __launch_bounds__(kBlockThreads) kivi_block_kernel(const AppendP
 // Sinks and the residual window left after this append: one thread per
 // 16-byte chunk of a new token's K and V.
 __global__ void __launch_bounds__(256) kivi_window_kernel(const AppendParams p) {
+  pdl_launch_dependents();
+  pdl_wait();  // the block kernel reads the slots written here
   const CacheGeom& c = p.geom;
   const int chunks = c.D / 8;
   const long long units = (long long)p.batch * p.num_new * c.Hkv * chunks;
@@ -154,13 +158,11 @@ cudaError_t launch_append_kivi(const AppendParams& p, cudaStream_t stream) {
   // every later one it reaches
   const long long nblk = (long long)(p.num_new + c.g - 1) / c.g + 1;
   const dim3 grid1((unsigned)nblk, c.Hkv, p.batch);
-  if (c.bits == 4) kivi_block_kernel<4><<<grid1, kBlockThreads, 0, stream>>>(p);
-  else kivi_block_kernel<8><<<grid1, kBlockThreads, 0, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = c.bits == 4 ? launch_pdl(kivi_block_kernel<4>, grid1, dim3(kBlockThreads), 0, stream, p)
+                              : launch_pdl(kivi_block_kernel<8>, grid1, dim3(kBlockThreads), 0, stream, p);
   if (e != cudaSuccess) return e;
   const long long units = (long long)p.batch * p.num_new * c.Hkv * (c.D / 8);
-  kivi_window_kernel<<<(unsigned)((units + 255) / 256), 256, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kivi_window_kernel, dim3((unsigned)((units + 255) / 256)), dim3(256), 0, stream, p);
 }
 
 }  // namespace kvq

@@ -213,14 +213,6 @@ __device__ __forceinline__ float ex2(float x) {
 // o[0] = (1024+c0, 1024+c4), o[1] = (1024+16c1, 1024+16c5), o[2], o[3] likewise.
 __device__ __forceinline__ void nib8_to_h2_biased(uint32_t w, uint32_t (&o)[4]);
 
-// Programmatic dependent launch: let the next kernel of the stream begin its
-// launch, and wait for the previous one to complete (a no-op when the launch
-// did not allow overlap).
-__device__ __forceinline__ void pdl_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
-
 // Pull [p, p + bytes) into L2 (p and bytes multiples of 16).
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(p), "r"(bytes) : "memory");
@@ -266,8 +258,9 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CT
   // stream may start launching now.  Until the previous kernel has completed
   // (pdl_wait) nothing here reads or writes caller memory; it only warms L2
   // with this warp's first tiles (dense caches, as if the sequence filled the
-  // cache).  Those bytes are read again after the wait, so a previous kernel
-  // that wrote the cache is still seen.
+  // cache), the CTA's q rows and the new token's K/V rows.  Those bytes are
+  // read again after the wait, so a previous kernel that wrote them is still
+  // seen.
   pdl_launch_dependents();
   if constexpr (!KCH) {
     if (!p.longest_first && geo.layout == KVQ_DENSE && lane < C::STAGES * 6) {
@@ -289,6 +282,20 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CT
         if (hi > lo) prefetch_l2(reinterpret_cast<const void*>(lo), (uint32_t)(hi - lo));
       }
     }
+  }
+  // the CTA's q rows and, for the fused step, the new token's K and V rows
+  if (!p.longest_first && warp == 1 && lane < 3) {
+    const int b = blockIdx.z;
+    const void* src = nullptr;
+    uint32_t bytes = 0;
+    if (lane == 0) {
+      src = p.q + ((long long)b * p.Hq + (long long)kvh * G) * D;
+      bytes = (uint32_t)(G * D * 2);
+    } else if (p.lens_before != nullptr) {
+      src = p.new_kv[lane - 1] + ((long long)b * geo.Hkv + kvh) * D;
+      bytes = (uint32_t)(D * 2);
+    }
+    if (src != nullptr && (reinterpret_cast<uintptr_t>(src) & 15) == 0) prefetch_l2(src, bytes);
   }
   pdl_wait();
 

@@ -74,6 +74,8 @@ __device__ __forceinline__ float load_kv(const DecodeParams& p, int which, int b
 
 template <int BITS>
 __global__ void __launch_bounds__(kThreads) decode_generic_kernel(const DecodeParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
   extern __shared__ float smem[];
   const CacheGeom& c = p.geom;
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
@@ -205,6 +207,8 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(const DecodePa
 // that hold tokens of sequence b.  One CTA per (b, h), one thread per
 // channel; the loop rescales as it goes so that every load is independent.
 __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
+  pdl_launch_dependents();
+  pdl_wait();  // the partials of the decode kernel before it
   const long long rowid = blockIdx.x;  // b * Hq + h
   const int b = (int)(rowid / p.Hq);
   const int D = p.geom.D;
@@ -253,32 +257,30 @@ cudaError_t launch_decode_generic(const DecodeParams& p, cudaStream_t stream) {
     case 2:
       e = cudaFuncSetAttribute(decode_generic_kernel<2>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) decode_generic_kernel<2><<<grid, kThreads, smem, stream>>>(p);
+      if (e == cudaSuccess) e = launch_pdl(decode_generic_kernel<2>, grid, dim3(kThreads), smem, stream, p);
       break;
     case 4:
       e = cudaFuncSetAttribute(decode_generic_kernel<4>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) decode_generic_kernel<4><<<grid, kThreads, smem, stream>>>(p);
+      if (e == cudaSuccess) e = launch_pdl(decode_generic_kernel<4>, grid, dim3(kThreads), smem, stream, p);
       break;
     case 8:
       e = cudaFuncSetAttribute(decode_generic_kernel<8>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) decode_generic_kernel<8><<<grid, kThreads, smem, stream>>>(p);
+      if (e == cudaSuccess) e = launch_pdl(decode_generic_kernel<8>, grid, dim3(kThreads), smem, stream, p);
       break;
     default:
       e = cudaFuncSetAttribute(decode_generic_kernel<16>,
                                cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e == cudaSuccess) decode_generic_kernel<16><<<grid, kThreads, smem, stream>>>(p);
+      if (e == cudaSuccess) e = launch_pdl(decode_generic_kernel<16>, grid, dim3(kThreads), smem, stream, p);
       break;
   }
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  return e;
 }
 
 cudaError_t launch_merge(const DecodeParams& p, cudaStream_t stream) {
   const long long rows = (long long)p.batch * p.Hq;
-  merge_kernel<<<(unsigned)rows, p.geom.D, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(merge_kernel, dim3((unsigned)rows), dim3(p.geom.D), 0, stream, p);
 }
 
 int generic_ctas_per_sm(const DecodeParams& p) {

@@ -137,6 +137,32 @@ __device__ __forceinline__ int longest_first_seq(const DecodeParams& p, int r, i
   return b;
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with programmatic stream serialization: the next kernel of the stream may
+// start launching once all CTAs have passed pdl_launch_dependents, and each
+// kernel reads or writes caller memory only after pdl_wait, which returns
+// when the previous kernel has completed and its writes are visible.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
+template <typename Params>
+cudaError_t launch_pdl(void (*kernel)(Params), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, const Params& p) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
 // Launchers (return a CUDA error code; the caller maps it to kvq_status).
 cudaError_t launch_append(const AppendParams& p, cudaStream_t stream);
 cudaError_t launch_append_kivi(const AppendParams& p, cudaStream_t stream);
