@@ -137,8 +137,9 @@ __device__ __forceinline__ int longest_first_seq(const DecodeParams& p, int r, i
   return b;
 }
 
-// Programmatic dependent launch.  Every kernel of the library is launched
-// with programmatic stream serialization: the next kernel of the stream may
+// Programmatic dependent launch.  The library's kernels (all but the
+// CUDA-core decode kernel) are launched with programmatic stream
+// serialization: the next kernel of the stream may
 // start launching once all CTAs have passed pdl_launch_dependents, and each
 // kernel reads or writes caller memory only after pdl_wait, which returns
 // when the previous kernel has completed and its writes are visible.
