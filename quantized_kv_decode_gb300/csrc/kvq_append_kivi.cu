@@ -10,13 +10,14 @@
 // section 4 (group_params / group_encode / quantize8 in kvq_quant.cuh), so a
 // K group here is exactly a per-token group with its axis turned.
 //
-// One append is two launches in stream order:
+// An append of several tokens is two launches in stream order:
 //  1. kivi_block_kernel: every block that this append completes is
 //     quantized, reading the tokens already in the residual window and the
 //     new ones;
 //  2. kivi_window_kernel: sink tokens and the tokens left in the (new)
 //     residual window are written to their fp16 slots.  It runs second
 //     because its slots may be the ones launch 1 reads.
+// A one-token append (the decode step) is one launch, kivi_step_kernel.
 #include "kvq_quant.cuh"
 
 namespace kvq {
@@ -36,25 +37,14 @@ __device__ __forceinline__ const __half* token_src(const AppendParams& p, int wh
   return p.src[which] + (((long long)b * p.num_new + (q - p0)) * c.Hkv + kvh) * c.D;
 }
 
+// Quantizes block j (positions [start, start + g)) of sequence b, KV head
+// kvh, whose tokens before p0 sit in the residual window and the rest in the
+// caller's input.  Every thread of the CTA calls it.
 template <int BITS>
-__global__ void __launch_bounds__(kBlockThreads) kivi_block_kernel(const AppendParams p) {
-  pdl_launch_dependents();
-  pdl_wait();
+__device__ void quantize_block(const AppendParams& p, int b, int kvh, int j, long long start,
+                               int p0) {
   const CacheGeom& c = p.geom;
-  const int kvh = blockIdx.y, b = blockIdx.z;
-  const int S = c.sink, g = c.g, D = c.D;
-  const int p0 = __ldg(p.seq_lens_before + b);
-  const int n = p.num_new;
-  if (p0 < 0) return;  // flagged by the window kernel
-  // the block holding the first new token (or block 0), then the next ones
-  const int j = (p0 <= S ? 0 : (p0 - S) / g) + blockIdx.x;
-  const long long start = (long long)S + (long long)j * g;
-  const long long end = start + g - 1;               // last position of the block
-  if (end < p0 || end > (long long)p0 + n - 1) return;  // not completed by this append
-  if (end >= c.slots) {
-    if (threadIdx.x == 0 && p.status) atomicOr(p.status, KVQ_FLAG_SEQ_LEN);
-    return;
-  }
+  const int g = c.g, D = c.D;
   const long long bh = (long long)b * c.Hkv + kvh;
   uint32_t flags = 0;
 
@@ -115,6 +105,58 @@ __global__ void __launch_bounds__(kBlockThreads) kivi_block_kernel(const AppendP
   if (flags && p.status) atomicOr(p.status, flags);
 }
 
+template <int BITS>
+__global__ void __launch_bounds__(kBlockThreads) kivi_block_kernel(const AppendParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const CacheGeom& c = p.geom;
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int S = c.sink, g = c.g;
+  const int p0 = __ldg(p.seq_lens_before + b);
+  const int n = p.num_new;
+  if (p0 < 0) return;  // flagged by the window kernel
+  // the block holding the first new token (or block 0), then the next ones
+  const int j = (p0 <= S ? 0 : (p0 - S) / g) + blockIdx.x;
+  const long long start = (long long)S + (long long)j * g;
+  const long long end = start + g - 1;               // last position of the block
+  if (end < p0 || end > (long long)p0 + n - 1) return;  // not completed by this append
+  if (end >= c.slots) {
+    if (threadIdx.x == 0 && p.status) atomicOr(p.status, KVQ_FLAG_SEQ_LEN);
+    return;
+  }
+  quantize_block<BITS>(p, b, kvh, j, start, p0);
+}
+
+// One-token append in one launch, one CTA per (KV head, sequence): the token
+// either completes its block (quantized here, window rows read) or goes to
+// its fp16 slot (a sink or the residual ring).  The two never meet within a
+// sequence, so no second launch is needed to order them.
+template <int BITS>
+__global__ void __launch_bounds__(kBlockThreads) kivi_step_kernel(const AppendParams p) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const CacheGeom& c = p.geom;
+  const int kvh = blockIdx.y, b = blockIdx.z;
+  const int p0 = __ldg(p.seq_lens_before + b);
+  if (p0 < 0 || p0 >= c.slots) {
+    if (threadIdx.x == 0 && kvh == 0 && p.status) atomicOr(p.status, KVQ_FLAG_SEQ_LEN);
+    return;
+  }
+  const int slot = window_slot(c, p0 + 1, p0);
+  if (slot < 0) {  // p0 ends its block
+    const int j = (p0 - c.sink) / c.g;
+    quantize_block<BITS>(p, b, kvh, j, (long long)c.sink + (long long)j * c.g, p0);
+    return;
+  }
+  const long long bh = (long long)b * c.Hkv + kvh;
+  const int chunks = c.D / 8;
+  if (threadIdx.x < 2 * chunks) {
+    const int which = threadIdx.x / chunks, ch = threadIdx.x % chunks;
+    *(reinterpret_cast<uint4*>(p.window[which] + (bh * (c.sink + c.g) + slot) * c.D) + ch) =
+        *(reinterpret_cast<const uint4*>(p.src[which] + bh * c.D) + ch);
+  }
+}
+
 // Sinks and the residual window left after this append: one thread per
 // 16-byte chunk of a new token's K and V.
 __global__ void __launch_bounds__(256) kivi_window_kernel(const AppendParams p) {
@@ -156,6 +198,11 @@ cudaError_t launch_append_kivi(const AppendParams& p, cudaStream_t stream) {
   if (p.batch == 0 || p.num_new == 0) return cudaSuccess;
   // blocks one append can complete: the one holding its first token and
   // every later one it reaches
+  if (p.num_new == 1) {
+    const dim3 grid(1, c.Hkv, p.batch);
+    return c.bits == 4 ? launch_pdl(kivi_step_kernel<4>, grid, dim3(kBlockThreads), 0, stream, p)
+                       : launch_pdl(kivi_step_kernel<8>, grid, dim3(kBlockThreads), 0, stream, p);
+  }
   const long long nblk = (long long)(p.num_new + c.g - 1) / c.g + 1;
   const dim3 grid1((unsigned)nblk, c.Hkv, p.batch);
   cudaError_t e = c.bits == 4 ? launch_pdl(kivi_block_kernel<4>, grid1, dim3(kBlockThreads), 0, stream, p)

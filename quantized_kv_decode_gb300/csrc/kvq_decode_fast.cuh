@@ -283,17 +283,23 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CT
       }
     }
   }
-  // the CTA's q rows and, for the fused step, the new token's K and V rows
-  if (!p.longest_first && warp == 1 && lane < 3) {
+  // the CTA's q rows, for the fused step the new token's K and V rows, and
+  // for axis-aware caches the unit's fp16 rows (sinks and residual window)
+  if (!p.longest_first && warp == 1 && lane < 5) {
     const int b = blockIdx.z;
     const void* src = nullptr;
     uint32_t bytes = 0;
     if (lane == 0) {
       src = p.q + ((long long)b * p.Hq + (long long)kvh * G) * D;
       bytes = (uint32_t)(G * D * 2);
-    } else if (p.lens_before != nullptr) {
-      src = p.new_kv[lane - 1] + ((long long)b * geo.Hkv + kvh) * D;
-      bytes = (uint32_t)(D * 2);
+    } else if (lane < 3) {
+      if (p.lens_before != nullptr) {
+        src = p.new_kv[lane - 1] + ((long long)b * geo.Hkv + kvh) * D;
+        bytes = (uint32_t)(D * 2);
+      }
+    } else if (KCH) {
+      src = p.window[lane - 3] + ((long long)b * geo.Hkv + kvh) * (geo.sink + geo.g) * D;
+      bytes = (uint32_t)((geo.sink + geo.g) * D * 2);
     }
     if (src != nullptr && (reinterpret_cast<uintptr_t>(src) & 15) == 0) prefetch_l2(src, bytes);
   }
@@ -1073,33 +1079,72 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CT
 #pragma unroll
       for (int c = 0; c < CPL; ++c) oh[h][c] = 0.f;
     }
-    for (int i = warp; i < nw; i += kWarps) {
-      const int pos = i < ns ? t0 + i : rs + (i - ns);
-      const int slot = pos < kS ? pos : geo.sink + (pos - geo.sink) % geo.g;
-      const __half* kr = p.window[0] + (wb + slot) * D + lane * CPL;
-      const __half* vr = p.window[1] + (wb + slot) * D + lane * CPL;
-      float kf[CPL], vf[CPL];
+    // this warp's rows i = warp, warp + 4, ...: loaded WB at a time, then used
+    constexpr int WB = 8;
+    constexpr int WPR = CPL / 2;  // 32-bit words of a lane's channels in one row
+    for (int i0 = warp; i0 < nw; i0 += kWarps * WB) {
+      uint32_t kw[WB][WPR], vw[WB][WPR];
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) {
-        kf[c] = __half2float(kr[c]);
-        vf[c] = __half2float(vr[c]);
+      for (int k = 0; k < WB; ++k) {
+        const int i = min(i0 + k * kWarps, nw - 1);  // past the end: a row that exists, unused
+        const int pos = i < ns ? t0 + i : rs + (i - ns);
+        const int slot = pos < kS ? pos : geo.sink + (pos - geo.sink) % geo.g;
+        const uint32_t* kr = reinterpret_cast<const uint32_t*>(p.window[0] + (wb + slot) * D) + lane * WPR;
+        const uint32_t* vr = reinterpret_cast<const uint32_t*>(p.window[1] + (wb + slot) * D) + lane * WPR;
+#pragma unroll
+        for (int c = 0; c < WPR; ++c) {
+          kw[k][c] = kr[c];
+          vw[k][c] = vr[c];
+        }
       }
+      // scores of the batch's rows (independent, so their reductions
+      // overlap), then one online-softmax update per head
+      const int nb = min(WB, (nw - i0 + kWarps - 1) / kWarps);  // live rows of the batch
 #pragma unroll
       for (int h = 0; h < GP; ++h) {
         if (h >= G) continue;
-        float part = 0.f;
+        float qh[CPL];
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) part = fmaf(__half2float(q_s[h * D + lane * CPL + c]), kf[c], part);
+        for (int c = 0; c < CPL; ++c) qh[c] = __half2float(q_s[h * D + lane * CPL + c]);
+        float sc[WB];
 #pragma unroll
-        for (int o2 = 16; o2 > 0; o2 >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o2);
-        const float sh = part * p.scale_log2;
-        const float mn = fmaxf(mh[h], sh);
-        const float a = mh[h] == -INFINITY ? 0.f : ex2(mh[h] - mn);
-        const float e = ex2(sh - mn);
-        lh[h] = fmaf(lh[h], a, e);
+        for (int k = 0; k < WB; ++k) {
+          float part = 0.f;
 #pragma unroll
-        for (int c = 0; c < CPL; ++c) oh[h][c] = fmaf(oh[h][c], a, e * vf[c]);
-        mh[h] = mn;
+          for (int c = 0; c < WPR; ++c) {
+            const float2 kx = __half22float2(u32_as_h2(kw[k][c]));
+            part = fmaf(qh[2 * c], kx.x, part);
+            part = fmaf(qh[2 * c + 1], kx.y, part);
+          }
+          sc[k] = part;
+        }
+#pragma unroll
+        for (int o2 = 16; o2 > 0; o2 >>= 1) {
+#pragma unroll
+          for (int k = 0; k < WB; ++k) sc[k] += __shfl_xor_sync(0xffffffffu, sc[k], o2);
+        }
+        float mx = mh[h];
+#pragma unroll
+        for (int k = 0; k < WB; ++k) {
+          sc[k] = k < nb ? sc[k] * p.scale_log2 : -INFINITY;
+          mx = fmaxf(mx, sc[k]);
+        }
+        const float a = mh[h] == -INFINITY ? 0.f : ex2(mh[h] - mx);
+        lh[h] *= a;
+#pragma unroll
+        for (int c = 0; c < CPL; ++c) oh[h][c] *= a;
+#pragma unroll
+        for (int k = 0; k < WB; ++k) {
+          const float e = ex2(sc[k] - mx);  // 0 for the rows past the end
+          lh[h] += e;
+#pragma unroll
+          for (int c = 0; c < WPR; ++c) {
+            const float2 vx = __half22float2(u32_as_h2(vw[k][c]));
+            oh[h][2 * c] = fmaf(e, vx.x, oh[h][2 * c]);
+            oh[h][2 * c + 1] = fmaf(e, vx.y, oh[h][2 * c + 1]);
+          }
+        }
+        mh[h] = mx;
       }
     }
 #pragma unroll
