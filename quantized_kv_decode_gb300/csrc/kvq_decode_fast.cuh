@@ -71,6 +71,11 @@ struct Cfg {
   static constexpr int STAGES = STAGES_FIT > 5 ? 5 : (STAGES_FIT < 2 ? 2 : STAGES_FIT);
   static constexpr int WARP_BYTES = STAGES * STAGE + 2 * XHDR;
   static constexpr int MIN_CTAS = 2;
+  // One query head per KV head (per-token caches): a fifth warp does the
+  // fused step's append (quantize, store, one-token partial) next to the four
+  // streaming warps instead of in front of one of them's tiles.
+  static constexpr bool AW = !KCH && GP == 1;
+  static constexpr int THREADS = kWarps * 32 + (AW ? 32 : 0);
   static constexpr int NTV = (NG * GP + 7) / 8;           // V-mma n-tiles: columns (group, head)
   static constexpr int NGL = (NG < 8 / GP) ? NG : 8 / GP;  // groups in accumulator rows 0..7
   static constexpr bool HI = NG * GP > 8;                   // rows 8..15 in use
@@ -236,7 +241,7 @@ __device__ __forceinline__ uint32_t pack_halves(__half lo, __half hi) {
 constexpr float kSlack = 4.f;
 
 template <int BITS, int D, int NG, int GP, bool SYM, bool KCH>
-__global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CTAS)
+__global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, D, NG, GP, KCH>::MIN_CTAS)
     decode_fast_kernel(const DecodeParams p) {
   // SYM: symmetric caches, no zero arrays; every zero-point is 2^(BITS-1)
   constexpr unsigned short kSymZero = BITS == 4 ? 0x4800u : 0x5800u;  // fp16 8, 128
@@ -263,7 +268,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CT
   // seen.
   pdl_launch_dependents();
   if constexpr (!KCH) {
-    if (!p.longest_first && geo.layout == KVQ_DENSE && lane < C::STAGES * 6) {
+    if (!p.longest_first && geo.layout == KVQ_DENSE && warp < kWarps && lane < C::STAGES * 6) {
       const int b = blockIdx.z;
       const int it = lane / 6, region = lane % 6;
       const int t0g = split * p.chunk;
@@ -334,7 +339,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CT
   auto madd_of = [&](int buf) { return reinterpret_cast<float*>(vzx_of(buf) + NG * C::VROW); };
 
   const __half* qg = p.q + ((long long)b * p.Hq + (long long)kvh * G) * D;
-  for (int i = threadIdx.x; i < GP * D; i += kWarps * 32)
+  for (int i = threadIdx.x; i < GP * D; i += blockDim.x)
     q_s[i] = (i < G * D) ? qg[i] : __float2half_rn(0.f);
 
   __syncthreads();
@@ -456,8 +461,9 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CT
     ntiles = (t_end > t0) ? (t_end - t0 + kTT - 1) / kTT : 0;
   }
   // the appending warp: one with the fewest tiles
-  const bool owner = owner_cta && warp == ntiles % kWarps;  // warp-uniform
-  const int nmine = (ntiles > warp) ? (ntiles - warp + kWarps - 1) / kWarps : 0;
+  // (the append warp when the CTA has one)
+  const bool owner = owner_cta && warp == (C::AW ? kWarps : ntiles % kWarps);  // warp-uniform
+  const int nmine = (warp < kWarps && ntiles > warp) ? (ntiles - warp + kWarps - 1) / kWarps : 0;
   const uint8_t* kc_g = p.codes[0];
   const uint8_t* vc_g = p.codes[1];
   const uint8_t* ks_g = reinterpret_cast<const uint8_t*>(p.scale[0]);
@@ -1048,7 +1054,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CT
     for (int e = 0; e < 2; ++e) {
       const int col = 8 * t + 2 * j + e;  // (group col / GP, head col % GP)
       const int h = col % GP;
-      if (col / GP == g && h < G) {
+      if (col / GP == g && h < G && warp < kWarps) {
         const float corr = e ? corr1 : corr0;
         float* dst = red + (warp * GP + h) * D;
         dst[d0] = o[m][e] - corr;
@@ -1056,7 +1062,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CT
       }
     }
   }
-  if (j == 0 && rho < GP) {
+  if (j == 0 && rho < GP && warp < kWarps) {
     ml[(warp * GP + rho) * 2] = m_ref;
     ml[(warp * GP + rho) * 2 + 1] = l_run;
   }
@@ -1160,7 +1166,7 @@ __global__ void __launch_bounds__(kWarps * 32, Cfg<BITS, D, NG, GP, KCH>::MIN_CT
   __syncthreads();
 
   const long long hq0 = (long long)b * p.Hq + (long long)kvh * G;
-  for (int i = threadIdx.x; i < G * D; i += kWarps * 32) {
+  for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
     const int h = i / D, d = i - h * D;
     float M = -INFINITY;
 #pragma unroll
@@ -1226,14 +1232,15 @@ cudaError_t launch_fast_inst(const DecodeParams& p, cudaStream_t stream, int* ct
   if (e != cudaSuccess) return e;
   if (ctas_per_sm) {
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        ctas_per_sm, decode_fast_kernel<BITS, D, NG, GP, SYM, KCH>, kWarps * 32, smem);
+        ctas_per_sm, decode_fast_kernel<BITS, D, NG, GP, SYM, KCH>, Cfg<BITS, D, NG, GP, KCH>::THREADS, smem);
   }
   // programmatic stream serialization: this launch may overlap the tail of the
   // previous kernel in the stream; the kernel waits for it before using any
   // caller data
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.splits, p.geom.Hkv, p.batch);
-  cfg.blockDim = dim3(kWarps * 32);
+  // the append warp only runs in the fused step
+  cfg.blockDim = dim3(p.lens_before != nullptr ? Cfg<BITS, D, NG, GP, KCH>::THREADS : kWarps * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
