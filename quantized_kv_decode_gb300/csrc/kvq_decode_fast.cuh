@@ -71,10 +71,12 @@ struct Cfg {
   static constexpr int STAGES = STAGES_FIT > 5 ? 5 : (STAGES_FIT < 2 ? 2 : STAGES_FIT);
   static constexpr int WARP_BYTES = STAGES * STAGE + 2 * XHDR;
   static constexpr int MIN_CTAS = 2;
-  // One query head per KV head (per-token caches): a fifth warp does the
-  // fused step's append (quantize, store, one-token partial) next to the four
-  // streaming warps instead of in front of one of them's tiles.
-  static constexpr bool AW = !KCH && GP == 1;
+  // Per-token caches with one query head per KV head, or INT4 token-rows
+  // GQA shapes: a fifth warp does the fused step's append (quantize, store,
+  // one-token partial) next to the four streaming warps instead of in front
+  // of one of them's tiles.  (The other shapes need more registers than 160
+  // threads leave for two CTAs per SM.)
+  static constexpr bool AW = !KCH && (GP == 1 || (BITS == 4 && NG * GP <= 8));
   static constexpr int THREADS = kWarps * 32 + (AW ? 32 : 0);
   static constexpr int NTV = (NG * GP + 7) / 8;           // V-mma n-tiles: columns (group, head)
   static constexpr int NGL = (NG < 8 / GP) ? NG : 8 / GP;  // groups in accumulator rows 0..7
