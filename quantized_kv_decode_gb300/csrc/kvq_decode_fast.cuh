@@ -898,46 +898,20 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
     const uint32_t vc_s = wpipe_s + stg * C::STAGE + C::CODE_TILE;
     const __half* vsx = vsx_of(buf);
     const __half* vzx = vzx_of(buf);
+    // B[token][(g, h)] = p_h(token) * s_g(token); this lane's column per n-tile
+    uint32_t bt[2][C::NTV][2];
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
       const int tk = 16 * ks + 2 * j;  // this lane's tokens: tk, tk+1, tk+8, tk+9
       const uint32_t plo = pp[2 * ks], phi = pp[2 * ks + 1];
-      // B[token][(g, h)] = p_h(token) * s_g(token); this lane's column per n-tile
-      uint32_t bt[C::NTV][2];
 #pragma unroll
       for (int t = 0; t < C::NTV; ++t) {
         const int g = min(gcol[t], NG - 1);
         const uint32_t slo = *reinterpret_cast<const uint32_t*>(vsx + g * C::VROW + tk);
         const uint32_t shi = *reinterpret_cast<const uint32_t*>(vsx + g * C::VROW + tk + 8);
         const bool live = gcol[t] < NG;
-        bt[t][0] = live ? h2_as_u32(__hmul2(u32_as_h2(plo), u32_as_h2(slo))) : 0u;
-        bt[t][1] = live ? h2_as_u32(__hmul2(u32_as_h2(phi), u32_as_h2(shi))) : 0u;
-      }
-      // V codes, transposed: per chunk, lo = tokens 0-7 of the k-step, hi = tokens 8-15
-#pragma unroll
-      for (int c = 0; c < C::CHUNKS; c += 2) {
-        uint32_t xlo0, xhi0, xlo1, xhi1;
-        const int m = lane >> 3;
-        const int tok = 16 * ks + ((m & 1) << 3) + (lane & 7);
-        ldsm_x4_t(vc_s + C::at(tok, c + (m >> 1)), xlo0, xhi0, xlo1, xhi1);
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const uint32_t xlo = cc ? xlo1 : xlo0, xhi = cc ? xhi1 : xhi0;
-          const int chunk = c + cc;
-          const int t = ((chunk * C::DPC) / C::GSZ) * GP / 8;  // n-tile of the chunk's group
-          if constexpr (BITS == 4) {
-            uint32_t lo[4], hi[4];
-            nib8_to_h2(xlo, lo);
-            nib8_to_h2(xhi, hi);
-            // channel of lo[e] = chunk*32 + 4*rho + e; m-tile (chunk, pp) rows: e = 2pp, 2pp+1
-            mma16816(o[2 * chunk], lo[0], lo[1], hi[0], hi[1], bt[t][0], bt[t][1]);
-            mma16816(o[2 * chunk + 1], lo[2], lo[3], hi[2], hi[3], bt[t][0], bt[t][1]);
-          } else {
-            const uint32_t l0 = byte2_to_h2<0x4240>(xlo), l1 = byte2_to_h2<0x4341>(xlo);
-            const uint32_t h0 = byte2_to_h2<0x4240>(xhi), h1 = byte2_to_h2<0x4341>(xhi);
-            mma16816(o[chunk], l0, l1, h0, h1, bt[t][0], bt[t][1]);
-          }
-        }
+        bt[ks][t][0] = live ? h2_as_u32(__hmul2(u32_as_h2(plo), u32_as_h2(slo))) : 0u;
+        bt[ks][t][1] = live ? h2_as_u32(__hmul2(u32_as_h2(phi), u32_as_h2(shi))) : 0u;
       }
       // zero-points: A rows = groups r, A[r][token] = z_r(token); the entries
       // with r equal to the column's group are the ones used
@@ -945,7 +919,73 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
       const uint32_t zlo = rho < NG ? *reinterpret_cast<const uint32_t*>(vzx + gz * C::VROW + tk) : 0u;
       const uint32_t zhi = rho < NG ? *reinterpret_cast<const uint32_t*>(vzx + gz * C::VROW + tk + 8) : 0u;
 #pragma unroll
-      for (int t = 0; t < C::NTV; ++t) mma16816(cz[t], zlo, 0u, zhi, 0u, bt[t][0], bt[t][1]);
+      for (int t = 0; t < C::NTV; ++t) mma16816(cz[t], zlo, 0u, zhi, 0u, bt[ks][t][0], bt[ks][t][1]);
+    }
+    if constexpr (BITS == 4) {
+      // The codes stay biased (1024 + c; odd nibbles 1024 + 16c, whose rows
+      // accumulate in x16 units until the end).  Per n-tile, -1024 sum_t B
+      // (every row) is the offset they add over this tile; it goes into each
+      // m-tile's accumulator before the tile's mmas, so no accumulator
+      // carries more than one tile's offset.
+      constexpr uint32_t kHm1024 = 0xE400E400u;  // fp16 (-1024, -1024)
+      float nb[C::NTV][4];
+#pragma unroll
+      for (int t = 0; t < C::NTV; ++t) {
+        nb[t][0] = nb[t][1] = nb[t][2] = nb[t][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks)
+          mma16816(nb[t], kHm1024, kHm1024, kHm1024, kHm1024, bt[ks][t][0], bt[ks][t][1]);
+      }
+#pragma unroll
+      for (int c = 0; c < C::CHUNKS; c += 2) {
+        // V codes, transposed: per chunk, lo = tokens 0-7 of the k-step, hi = tokens 8-15
+        uint32_t x[2][4];
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+          const int m = lane >> 3;
+          const int tok = 16 * ks + ((m & 1) << 3) + (lane & 7);
+          ldsm_x4_t(vc_s + C::at(tok, c + (m >> 1)), x[ks][0], x[ks][1], x[ks][2], x[ks][3]);
+        }
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int chunk = c + cc;
+          const int t = ((chunk * C::DPC) / C::GSZ) * GP / 8;  // n-tile of the chunk's group
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            o[2 * chunk][e] += nb[t][e];
+            o[2 * chunk + 1][e] += nb[t][e];
+          }
+#pragma unroll
+          for (int ks = 0; ks < 2; ++ks) {
+            uint32_t lo[4], hi[4];
+            nib8_to_h2_biased(x[ks][2 * cc], lo);
+            nib8_to_h2_biased(x[ks][2 * cc + 1], hi);
+            // channel of lo[e] = chunk*32 + 4*rho + e; m-tile (chunk, pp) rows: e = 2pp, 2pp+1
+            mma16816(o[2 * chunk], lo[0], lo[1], hi[0], hi[1], bt[ks][t][0], bt[ks][t][1]);
+            mma16816(o[2 * chunk + 1], lo[2], lo[3], hi[2], hi[3], bt[ks][t][0], bt[ks][t][1]);
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+#pragma unroll
+        for (int c = 0; c < C::CHUNKS; c += 2) {
+          uint32_t xlo0, xhi0, xlo1, xhi1;
+          const int m = lane >> 3;
+          const int tok = 16 * ks + ((m & 1) << 3) + (lane & 7);
+          ldsm_x4_t(vc_s + C::at(tok, c + (m >> 1)), xlo0, xhi0, xlo1, xhi1);
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc) {
+            const uint32_t xlo = cc ? xlo1 : xlo0, xhi = cc ? xhi1 : xhi0;
+            const int chunk = c + cc;
+            const int t = ((chunk * C::DPC) / C::GSZ) * GP / 8;
+            const uint32_t l0 = byte2_to_h2<0x4240>(xlo), l1 = byte2_to_h2<0x4341>(xlo);
+            const uint32_t h0 = byte2_to_h2<0x4240>(xhi), h1 = byte2_to_h2<0x4341>(xhi);
+            mma16816(o[chunk], l0, l1, h0, h1, bt[ks][t][0], bt[ks][t][1]);
+          }
+        }
+      }
     }
   };
 
@@ -1060,7 +1100,7 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
         const float corr = e ? corr1 : corr0;
         float* dst = red + (warp * GP + h) * D;
         dst[d0] = o[m][e] - corr;
-        dst[d0 + 1] = o[m][2 + e] - corr;
+        dst[d0 + 1] = o[m][2 + e] * (BITS == 4 ? 0.0625f : 1.f) - corr;  // INT4: odd rows in x16 units
       }
     }
   }
