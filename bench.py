@@ -331,7 +331,12 @@ def run_gpu_arm(args):
         ws_bytes = K.kvq_decode_workspace_size(desc, w.batch, w.num_q_heads, rows, 0)
         ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
         status = torch.zeros(1, dtype=torch.int32, device=dev)
-        outs = [torch.empty_like(q) for q in qs]
+        # per-layer step inputs and outputs as views of buffers contiguous
+        # across layers
+        q_all, k_all, v_all = torch.stack(qs), torch.stack(kns), torch.stack(vns)
+        qs, kns, vns = list(q_all.unbind(0)), list(k_all.unbind(0)), list(v_all.unbind(0))
+        o_all = torch.empty_like(q_all)
+        outs = list(o_all.unbind(0))
 
         kn1 = [k[:, 0] for k in kns]   # [B][Hkv][D] views of the step's new K/V
         vn1 = [v[:, 0] for v in vns]
@@ -437,21 +442,21 @@ def run_gpu_arm(args):
             raise RuntimeError(f"device status {int(status.item()):#x}")
 
         # end to end: inputs from pinned host memory, outputs back, per step
-        h_q = [q.cpu().pin_memory() for q in qs]
-        h_k = [k.cpu().pin_memory() for k in kns]
-        h_v = [v.cpu().pin_memory() for v in vns]
-        h_o = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
-        h2d = sum(t.numel() * t.element_size() for t in h_q + h_k + h_v)
-        d2h = sum(t.numel() * t.element_size() for t in h_o)
+        h_q = q_all.cpu().pin_memory()
+        h_k = k_all.cpu().pin_memory()
+        h_v = v_all.cpu().pin_memory()
+        h_o = torch.empty(o_all.shape, dtype=o_all.dtype, pin_memory=True)
+        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v))
+        d2h = h_o.numel() * h_o.element_size()
 
+        # The step's inputs and outputs are contiguous across layers, so a
+        # step moves them with four copies: q, k and v in, out back.
         def e2e_step():
-            for l in range(layers):
-                qs[l].copy_(h_q[l], non_blocking=True)
-                kns[l].copy_(h_k[l], non_blocking=True)
-                vns[l].copy_(h_v[l], non_blocking=True)
+            q_all.copy_(h_q, non_blocking=True)
+            k_all.copy_(h_k, non_blocking=True)
+            v_all.copy_(h_v, non_blocking=True)
             graph.replay()
-            for l in range(layers):
-                h_o[l].copy_(outs[l], non_blocking=True)
+            h_o.copy_(o_all, non_blocking=True)
 
         with torch.cuda.stream(stream):
             for _ in range(2):
