@@ -158,10 +158,9 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
 __device__ __forceinline__ uint32_t h2_as_u32(__half2 h) { return *reinterpret_cast<uint32_t*>(&h); }
 __device__ __forceinline__ __half2 u32_as_h2(uint32_t u) { return *reinterpret_cast<__half2*>(&u); }
 
-// fp16 bit patterns: 1024, 1/16, -64 in both halves
+// fp16 bit patterns: 1024 and 1/16 in both halves
 constexpr uint32_t kH1024 = 0x64006400u;
 constexpr uint32_t kH1_16 = 0x2C002C00u;
-constexpr uint32_t kHm64 = 0xD400D400u;
 
 // (a & b) | c in one LOP3
 __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
@@ -171,20 +170,12 @@ __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
 }
 
 // Eight 4-bit codes of one 32-bit word (code k in bits 4k..4k+3) to four
-// fp16 pairs: o[0] = (c0, c4), o[1] = (c1, c5), o[2] = (c2, c6), o[3] = (c3, c7).
-// (0x6400 | c) is the fp16 value 1024 + c; (0x6400 | 16c) is 1024 + 16c.
-__device__ __forceinline__ void nib8_to_h2(uint32_t w, uint32_t (&o)[4]) {
-  const uint32_t w2 = w >> 8;
-  const uint32_t a = and_or(w, 0x000F000Fu, kH1024);
-  const uint32_t b = and_or(w, 0x00F000F0u, kH1024);
-  const uint32_t c = and_or(w2, 0x000F000Fu, kH1024);
-  const uint32_t d = and_or(w2, 0x00F000F0u, kH1024);
-  o[0] = h2_as_u32(__hsub2(u32_as_h2(a), u32_as_h2(kH1024)));
-  o[1] = h2_as_u32(__hfma2(u32_as_h2(b), u32_as_h2(kH1_16), u32_as_h2(kHm64)));
-  o[2] = h2_as_u32(__hsub2(u32_as_h2(c), u32_as_h2(kH1024)));
-  o[3] = h2_as_u32(__hfma2(u32_as_h2(d), u32_as_h2(kH1_16), u32_as_h2(kHm64)));
-}
-
+// biased fp16 pairs: (0x6400 | c) is the fp16 value 1024 + c, (0x6400 | 16c)
+// is 1024 + 16c; o[0] = (1024+c0, 1024+c4), o[1] = (1024+16c1, 1024+16c5),
+// o[2] = (1024+c2, 1024+c6), o[3] = (1024+16c3, 1024+16c7).  Both
+// contractions keep the offset: the scores remove it through the
+// accumulator's starting value (the x16 undone by q/16 in the matching
+// slots), the weighted V through a per-tile offset mma and x16 rows.
 __device__ __forceinline__ void nib8_to_h2_biased(uint32_t w, uint32_t (&o)[4]) {
   const uint32_t w2 = w >> 8;
   o[0] = and_or(w, 0x000F000Fu, kH1024);
@@ -213,12 +204,6 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
   return y;
 }
-
-// Score-side code conversion: the +1024 offset stays in (it is removed
-// exactly by the accumulator's starting value), and the x16 of the odd
-// nibbles is undone by q/16 in the matching A slots.
-// o[0] = (1024+c0, 1024+c4), o[1] = (1024+16c1, 1024+16c5), o[2], o[3] likewise.
-__device__ __forceinline__ void nib8_to_h2_biased(uint32_t w, uint32_t (&o)[4]);
 
 // Pull [p, p + bytes) into L2 (p and bytes multiples of 16).
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
