@@ -26,7 +26,7 @@ the decision in fp32, the precision the GPU kernel uses, as required for a
 bit-exact comparison.  A test pins the fp32 decision to the exact rational
 decision on randomised groups.
 
-Readings of points the pages leave open (each is listed in the design doc):
+Readings of points the pages leave open:
   * the fp16 scale is rounded UP from (max-min)/(2^b-1), the only rounding
     under which the pages' bound |x - x_hat| <= s/2 holds for every element;
   * round() is round-half-to-even, the convention of the pages' numpy/torch
@@ -162,7 +162,7 @@ def quantize_groups_symmetric(x16: np.ndarray, bits: int, group_size: int) -> di
         q     = clamp(round(x / scale), -qmax - 1, qmax)
         x_hat = q * scale
 
-    Readings (listed in the design doc): the fp16 scale is rounded up (as in the
+    Readings: the fp16 scale is rounded up (as in the
     asymmetric quantizer) so that no element is clipped; an all-zero group
     takes s = 1 (the page's clamp_min(1e-12) scale is not an fp16 value);
     the signed q is stored as the code q + 2^(b-1), which makes the grid the
