@@ -190,6 +190,14 @@ kvq_status make_plan(const kvq_cache_desc* desc, const CacheGeom& geom, int32_t 
     occ = generic_ctas_per_sm(probe);
   }
   plan->splits = choose_splits((int64_t)batch * desc->num_kv_heads, max_seq_len, 0, occ);
+  // More units than one wave holds, and the tensor-core kernel takes them
+  // longest first: whole sequences in that order balance better than splits
+  // of them, which the model above prices as if every sequence were
+  // max_seq_len long (the paged small-model batch: 47.8 us with one split,
+  // 53.7 us with two).
+  if (plan->fast && batch > 1 && batch <= kLongestFirstMaxBatch &&
+      (int64_t)batch * desc->num_kv_heads >= (int64_t)sm_count() * occ)
+    plan->splits = 1;
   return plan->splits > 0 ? KVQ_OK : KVQ_ERR_CUDA;
 }
 

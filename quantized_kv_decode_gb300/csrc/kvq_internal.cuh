@@ -112,27 +112,73 @@ __device__ __forceinline__ int seq_len_of(const DecodeParams& p, int b) {
   return __ldg(p.seq_lens + b);
 }
 
-// The sequence of rank r when the batch is ordered by attended length,
-// longest first, ties by index (the keys are distinct, so the ranks are a
-// permutation).  Every thread of the CTA calls it; `scratch` is shared memory
-// for batch + 1 ints, free again on return.
-constexpr int kLongestFirstMaxBatch = 128;
+// The sequence of rank r in a longest-first order of the batch: sequences
+// are put in 128 buckets of attended length (an unusable length counts as 0),
+// the buckets taken longest first and a bucket's sequences by index, so the
+// ranks are a permutation.  O(batch) per CTA: a histogram, a scan of the
+// buckets by one warp, and a ballot search for the r-th sequence of its
+// bucket.  Every thread of the CTA calls it; `scratch` is shared memory for
+// 132 ints and batch bytes, free again on return.
+constexpr int kLongestFirstMaxBatch = 4096;
+constexpr int kOrderBuckets = 128;
 __device__ __forceinline__ int longest_first_seq(const DecodeParams& p, int r, int* scratch) {
   const int B = p.batch;
-  for (int i = threadIdx.x; i < B; i += blockDim.x) scratch[i] = seq_len_of(p, i);
+  int* hist = scratch;               // [kOrderBuckets]
+  int* res = scratch + kOrderBuckets;  // bucket of rank r, rank within it, sequence
+  uint8_t* bkt = reinterpret_cast<uint8_t*>(scratch + kOrderBuckets + 4);  // [B]
+  for (int i = threadIdx.x; i < kOrderBuckets; i += blockDim.x) hist[i] = 0;
   __syncthreads();
-  for (int c = threadIdx.x; c < B; c += blockDim.x) {
-    const int Lc = scratch[c];
-    int rank = 0;
-#pragma unroll 8
-    for (int i = 0; i < B; ++i) {
-      const int Li = scratch[i];
-      rank += (Li > Lc) | ((Li == Lc) & (i < c));
-    }
-    if (rank == r) scratch[B] = c;
+  const long long span = (long long)max(p.len_limit, 0) + 1;
+  for (int i = threadIdx.x; i < B; i += blockDim.x) {
+    const int L = seq_len_of(p, i);
+    const int Lc = (L < 0 || L > p.len_limit) ? 0 : L;
+    const int k = (int)((long long)Lc * kOrderBuckets / span);
+    bkt[i] = (uint8_t)k;
+    atomicAdd(hist + k, 1);
   }
   __syncthreads();
-  const int b = scratch[B];
+  const int lane = threadIdx.x & 31;
+  if (threadIdx.x < 32) {
+    // lane l holds buckets 127 - 4l ... 124 - 4l (longest first)
+    int cnt[4], sum = 0;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      cnt[e] = hist[kOrderBuckets - 1 - (4 * lane + e)];
+      sum += cnt[e];
+    }
+    int inc = sum;
+#pragma unroll
+    for (int o2 = 1; o2 < 32; o2 <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, inc, o2);
+      if (lane >= o2) inc += y;
+    }
+    int before = inc - sum;  // sequences in longer buckets
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      if (r >= before && r < before + cnt[e]) {
+        res[0] = kOrderBuckets - 1 - (4 * lane + e);
+        res[1] = r - before;
+      }
+      before += cnt[e];
+    }
+    __syncwarp();
+    const int kz = res[0];
+    int k = res[1];
+    for (int base = 0; base < B; base += 32) {  // the k-th sequence of bucket kz
+      const int i = base + lane;
+      const unsigned m = __ballot_sync(0xffffffffu, i < B && bkt[i] == kz);
+      const int n = __popc(m);
+      if (k < n) {  // warp-uniform
+        unsigned mm = m;
+        for (int t = 0; t < k; ++t) mm &= mm - 1;
+        if (lane == 0) res[2] = base + __ffs(mm) - 1;
+        break;
+      }
+      k -= n;
+    }
+  }
+  __syncthreads();
+  const int b = res[2];
   __syncthreads();
   return b;
 }

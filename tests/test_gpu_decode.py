@@ -155,7 +155,7 @@ def test_token_rows_gqa_paged_matches_dense():
     (40, 16, 8, 128, 32, "dense", False),    # 320 CTAs: more than one wave of the SMs
     (40, 32, 8, 128, 64, "dense", True),     # fused append, token-rows GQA
     (120, 28, 4, 64, 32, "paged", False),    # 7 heads per KV head, 16-token pages
-    (160, 4, 2, 64, 32, "dense", False),     # a batch above the longest-first cap
+    (160, 4, 2, 64, 32, "dense", False),     # 160 sequences, one or two per length bucket
 ])
 def test_multiwave_ragged_batches(B, Hq, Hkv, D, g, layout, fused):
     """Grids larger than one wave run the batch longest sequence first (grid
