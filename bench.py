@@ -540,8 +540,8 @@ def run_gpu_arm(args):
                     f"{w.group_size} tokens, V per token, {kivi_sink} fp16 sink tokens and the fp16 "
                     f"residual window; the step call is the append kernels + decode"}
     for key, what in (("nf4", f"NF4-style caches: 4-bit codes indexing 16 normal-quantile levels, "
-                               f"one fp16 absmax scale per {nf4_group} channels; CUDA-core decode "
-                               f"kernel (no tensor-core path for lookup codes)"),
+                               f"one fp16 absmax scale per {nf4_group} channels; tensor-core decode "
+                               f"kernel, codes to fp16 levels by a byte-permute lookup"),
                       ("int2", f"asymmetric INT2 g{w.group_size} caches (four codes per byte); "
                                f"CUDA-core decode kernel")):
         if key in results:

@@ -147,6 +147,48 @@ int32_t choose_splits(int64_t units, int64_t max_len, int32_t requested, int cta
   return (int32_t)ceil_div(L, split_chunk(L, (int32_t)s));
 }
 
+// NF4 levels: the (i + 1/2)/16 quantiles of N(0, 1) divided by the outermost
+// one, rounded to fp16 ("Gör inference billig", NF4: the sixteen levels sit
+// at the quantiles of a normal distribution).  Each quantile solves
+// Phi(x) = p, Phi(x) = erfc(-x / sqrt 2) / 2, by bisection to double
+// precision.  Computed once.
+struct Nf4Table {
+  float level[16];
+  float mid[16];
+  bool symmetric;  // level[15 - i] == -level[i]: the tensor-core kernel's sign-magnitude lookup
+};
+
+const Nf4Table& nf4_table() {
+  static const Nf4Table t = [] {
+    Nf4Table r{};
+    double z[16];
+    for (int i = 0; i < 16; ++i) {
+      const double p = (i + 0.5) / 16.0;
+      double lo = -10.0, hi = 10.0;
+      for (int it = 0; it < 200; ++it) {
+        const double m = 0.5 * (lo + hi);
+        if (0.5 * erfc(-m / sqrt(2.0)) < p) lo = m; else hi = m;
+      }
+      z[i] = 0.5 * (lo + hi);
+    }
+    for (int i = 0; i < 16; ++i) r.level[i] = __half2float(__double2half(z[i] / z[15]));
+    for (int i = 0; i < 15; ++i) r.mid[i] = (r.level[i] + r.level[i + 1]) * 0.5f;
+    r.mid[15] = INFINITY;
+    r.symmetric = true;
+    for (int i = 0; i < 8; ++i) r.symmetric = r.symmetric && r.level[15 - i] == -r.level[i];
+    return r;
+  }();
+  return t;
+}
+
+// Formats and shapes with a tensor-core kernel: INT4 / INT8 codes (NF4 as
+// INT4 with a level lookup) and at most 8 query heads per KV head.
+bool fast_format(const kvq_cache_desc* desc, int G) {
+  if (G > 8) return false;
+  if (desc->nf4) return nf4_table().symmetric;
+  return desc->bits == 4 || desc->bits == 8;
+}
+
 // Which decode kernel runs for a descriptor and query-head count: the
 // tensor-core kernel when an instantiation exists, else the generic one.
 struct Plan {
@@ -161,7 +203,7 @@ kvq_status make_plan(const kvq_cache_desc* desc, const CacheGeom& geom, int32_t 
   const int G = num_q_heads / desc->num_kv_heads;
   int occ = 0;
   plan->fast = false;
-  if ((desc->bits == 4 || desc->bits == 8) && !desc->nf4 && G <= 8) {
+  if (fast_format(desc, G)) {
     int gp = 1;
     while (gp < G) gp <<= 1;
     plan->gp = gp;
@@ -203,36 +245,6 @@ kvq_status make_plan(const kvq_cache_desc* desc, const CacheGeom& geom, int32_t 
 
 kvq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
 
-// NF4 levels: the (i + 1/2)/16 quantiles of N(0, 1) divided by the outermost
-// one, rounded to fp16 ("Gör inference billig", NF4: the sixteen levels sit
-// at the quantiles of a normal distribution).  Each quantile solves
-// Phi(x) = p, Phi(x) = erfc(-x / sqrt 2) / 2, by bisection to double
-// precision.  Computed once.
-struct Nf4Table {
-  float level[16];
-  float mid[16];
-};
-
-const Nf4Table& nf4_table() {
-  static const Nf4Table t = [] {
-    Nf4Table r{};
-    double z[16];
-    for (int i = 0; i < 16; ++i) {
-      const double p = (i + 0.5) / 16.0;
-      double lo = -10.0, hi = 10.0;
-      for (int it = 0; it < 200; ++it) {
-        const double m = 0.5 * (lo + hi);
-        if (0.5 * erfc(-m / sqrt(2.0)) < p) lo = m; else hi = m;
-      }
-      z[i] = 0.5 * (lo + hi);
-    }
-    for (int i = 0; i < 16; ++i) r.level[i] = __half2float(__double2half(z[i] / z[15]));
-    for (int i = 0; i < 15; ++i) r.mid[i] = (r.level[i] + r.level[i + 1]) * 0.5f;
-    r.mid[15] = INFINITY;
-    return r;
-  }();
-  return t;
-}
 
 }  // namespace
 
@@ -417,7 +429,7 @@ kvq_status decode_impl(const kvq_cache_desc* desc, const kvq_cache* cache, int32
   p.scale_log2 = scale * 1.4426950408889634f;
   // more CTAs than fit at once: start the longest sequences first, so that
   // the last wave holds short ones
-  const bool fast_shape = (desc->bits == 4 || desc->bits == 8) && !desc->nf4 && G <= 8;
+  const bool fast_shape = fast_format(desc, G);
   int occ = plan.occ;
   if (fast_shape && occ == 0 && batch > 1 && batch <= kLongestFirstMaxBatch) {
     DecodeParams probe{};
@@ -461,7 +473,7 @@ kvq_status decode_impl(const kvq_cache_desc* desc, const kvq_cache* cache, int32
     return launch_append(a, s);
   };
   if (fused && desc->k_per_channel) e = append_first();
-  if (e == cudaSuccess && (desc->bits == 4 || desc->bits == 8) && !desc->nf4 && G <= 8) {
+  if (e == cudaSuccess && fast_format(desc, G)) {
     if (desc->bits == 4) e = launch_decode_fast_int4(p, plan.gp, s, &handled, nullptr);
     else e = launch_decode_fast_int8(p, plan.gp, s, &handled, nullptr);
   }

@@ -184,6 +184,33 @@ __device__ __forceinline__ void nib8_to_h2_biased(uint32_t w, uint32_t (&o)[4]) 
   o[3] = and_or(w2, 0x00F000F0u, kH1024);
 }
 
+// NF4 codes of one 32-bit word to their fp16 levels, in the pairing of
+// nib8_to_h2_biased: o[0] = (lv(c0), lv(c4)), o[1] = (lv(c1), lv(c5)), ...
+// The 16 levels are symmetric, lv(15 - c) = -lv(c), so a code picks one of
+// 8 magnitudes (c - 8 for c >= 8, 7 - c below) and a sign.  lut holds the
+// magnitudes' fp16 bytes: lut[0] / lut[1] the low bytes of magnitudes 0-3 /
+// 4-7, lut[2] / lut[3] the high bytes; byte permutes do the lookup.
+__device__ __forceinline__ void nib8_to_h2_nf4(uint32_t w, uint32_t (&o)[4],
+                                               const uint32_t (&lut)[4]) {
+  const uint32_t neg = ((w >> 3) & 0x11111111u) ^ 0x11111111u;  // per code: 1 if lv < 0
+  const uint32_t idx = (w ^ ((neg << 3) - neg)) & 0x77777777u;    // magnitude index
+  const uint32_t s01 = __byte_perm(idx, 0u, 0x0020u);  // selectors (c0, c1, c4, c5)
+  const uint32_t s23 = __byte_perm(idx, 0u, 0x0031u);  // selectors (c2, c3, c6, c7)
+  const uint32_t pl = __byte_perm(lut[0], lut[1], s01), ph = __byte_perm(lut[2], lut[3], s01);
+  const uint32_t ql = __byte_perm(lut[0], lut[1], s23), qh = __byte_perm(lut[2], lut[3], s23);
+  o[0] = __byte_perm(pl, ph, 0x6240u) ^ ((neg & 0x00010001u) << 15);
+  o[1] = __byte_perm(pl, ph, 0x7351u) ^ ((neg & 0x00100010u) << 11);
+  o[2] = __byte_perm(ql, qh, 0x6240u) ^ ((neg & 0x01000100u) << 7);
+  o[3] = __byte_perm(ql, qh, 0x7351u) ^ ((neg & 0x10001000u) << 3);
+}
+
+// The 4-bit conversion of a kernel instance: biased codes, or NF4 levels.
+template <bool NF>
+__device__ __forceinline__ void nib8_to_h2(uint32_t w, uint32_t (&o)[4], const uint32_t (&lut)[4]) {
+  if constexpr (NF) nib8_to_h2_nf4(w, o, lut);
+  else nib8_to_h2_biased(w, o);
+}
+
 // Four 8-bit codes (byte k = code k) to fp16 pairs 1024 + c (score side).
 template <uint32_t SEL>
 __device__ __forceinline__ uint32_t byte2_to_h2_biased(uint32_t w) {
@@ -227,11 +254,24 @@ __device__ __forceinline__ uint32_t pack_halves(__half lo, __half hi) {
 // bounded by 2^kSlack.
 constexpr float kSlack = 4.f;
 
-template <int BITS, int D, int NG, int GP, bool SYM, bool KCH>
+template <int BITS, int D, int NG, int GP, bool SYM, bool KCH, bool NF = false>
 __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, D, NG, GP, KCH>::MIN_CTAS)
     decode_fast_kernel(const DecodeParams p) {
-  // SYM: symmetric caches, no zero arrays; every zero-point is 2^(BITS-1)
-  constexpr unsigned short kSymZero = BITS == 4 ? 0x4800u : 0x5800u;  // fp16 8, 128
+  // SYM: symmetric caches, no zero arrays; every zero-point is 2^(BITS-1).
+  // NF: NF4 codes (with SYM: scale only), which stand for normal-quantile
+  // levels; no offset to remove and no zero-point.
+  static_assert(!NF || (BITS == 4 && SYM && !KCH), "NF4: 4-bit, scale-only, per-token");
+  constexpr unsigned short kSymZero = NF ? 0u : (BITS == 4 ? 0x4800u : 0x5800u);  // fp16 0, 8, 128
+  // NF4: the 8 level magnitudes as fp16 bytes (see nib8_to_h2_nf4)
+  uint32_t lut[4] = {0u, 0u, 0u, 0u};
+  if constexpr (NF) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const uint32_t hb = __half_as_ushort(__float2half_rn(p.nf4_level[8 + k]));
+      lut[k >> 2] |= (hb & 0xFFu) << (8 * (k & 3));
+      lut[2 + (k >> 2)] |= (hb >> 8) << (8 * (k & 3));
+    }
+  }
   using C = Cfg<BITS, D, NG, GP, KCH>;
   // Token-rows layout, whenever the (group, head) pairs fill at most 8 rows
   // of the (group, head)-rows layout: the score mma takes the codes as A
@@ -369,7 +409,7 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
     const bool hi = row_ok && (KCH || (C::HI && g_hi == grp));
     const uint32_t v01 = pack_halves(qh[dk[0]], qh[dk[1]]);
     uint32_t v23 = pack_halves(qh[dk[2]], qh[dk[3]]);
-    if constexpr (BITS == 4)  // slots 2j+8, 2j+9 meet the odd nibbles, held as 16c
+    if constexpr (BITS == 4 && !NF)  // slots 2j+8, 2j+9 meet the odd nibbles, held as 16c
       v23 = h2_as_u32(__hmul2(u32_as_h2(v23), u32_as_h2(kH1_16)));
     qa[kb][0] = lo ? v01 : 0u;
     qa[kb][1] = hi ? v01 : 0u;
@@ -386,11 +426,11 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     float bia[4] = {0.f, 0.f, 0.f, 0.f};
     constexpr uint32_t kOnes = 0x3C003C00u;
-    constexpr uint32_t kHi = BITS == 4 ? 0x4C004C00u : 0x3C003C00u;  // x16 undoes q/16 in odd slots
+    constexpr uint32_t kHi = (BITS == 4 && !NF) ? 0x4C004C00u : 0x3C003C00u;  // x16 undoes q/16 in odd slots
 #pragma unroll
     for (int kb = 0; kb < C::KB; ++kb) {
       mma16816(acc, kOnes, kOnes, kHi, kHi, qa[kb][0], qa[kb][2]);
-      mma16816(bia, kH1024, kH1024, kH1024, kH1024, qa[kb][0], qa[kb][2]);
+      if constexpr (!NF) mma16816(bia, kH1024, kH1024, kH1024, kH1024, qa[kb][0], qa[kb][2]);
     }
     qs_lo = acc[0];   // column 2j
     qs_hi = acc[1];   // column 2j + 1
@@ -404,8 +444,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
 #pragma unroll
     for (int kb = 0; kb < C::KB; ++kb) {
       mma16816(acc, qa[kb][0], qa[kb][1], qa[kb][2], qa[kb][3], kOnes,
-               BITS == 4 ? kSixteen : kOnes);
-      mma16816(bia, qa[kb][0], qa[kb][1], qa[kb][2], qa[kb][3], kH1024, kH1024);
+               (BITS == 4 && !NF) ? kSixteen : kOnes);
+      if constexpr (!NF) mma16816(bia, qa[kb][0], qa[kb][1], qa[kb][2], qa[kb][3], kH1024, kH1024);
     }
     qs_lo = acc[0];
     qs_hi = acc[2];
@@ -674,8 +714,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
         for (int c = 0; c < C::CHUNKS; ++c) {
           if constexpr (BITS == 4) {
             uint32_t h0[4], h1[4];
-            nib8_to_h2_biased(w[0][c], h0);
-            nib8_to_h2_biased(w[1][c], h1);
+            nib8_to_h2<NF>(w[0][c], h0, lut);
+            nib8_to_h2<NF>(w[1][c], h1, lut);
             const uint32_t b00 = KCH ? Bq[2 * c][0] : qa[2 * c][0];
             const uint32_t b01 = KCH ? Bq[2 * c][1] : qa[2 * c][2];
             const uint32_t b10 = KCH ? Bq[2 * c + 1][0] : qa[2 * c + 1][0];
@@ -774,8 +814,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
       for (int c = 0; c < C::CHUNKS; ++c) {
         if constexpr (BITS == 4) {
           uint32_t h0[4], h1[4];
-          nib8_to_h2_biased(w[0][c], h0);
-          nib8_to_h2_biased(w[1][c], h1);
+          nib8_to_h2<NF>(w[0][c], h0, lut);
+          nib8_to_h2<NF>(w[1][c], h1, lut);
           mma16816(acc[0], Aop[2 * c][0], Aop[2 * c][1], Aop[2 * c][2], Aop[2 * c][3], h0[0], h0[1]);
           mma16816(acc[1], Aop[2 * c][0], Aop[2 * c][1], Aop[2 * c][2], Aop[2 * c][3], h1[0], h1[1]);
           mma16816(acc[0], Aop[2 * c + 1][0], Aop[2 * c + 1][1], Aop[2 * c + 1][2],
@@ -903,8 +943,10 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
       const int gz = min(rho, NG - 1);
       const uint32_t zlo = rho < NG ? *reinterpret_cast<const uint32_t*>(vzx + gz * C::VROW + tk) : 0u;
       const uint32_t zhi = rho < NG ? *reinterpret_cast<const uint32_t*>(vzx + gz * C::VROW + tk + 8) : 0u;
+      if constexpr (!NF) {  // NF4 has no zero-point
 #pragma unroll
-      for (int t = 0; t < C::NTV; ++t) mma16816(cz[t], zlo, 0u, zhi, 0u, bt[ks][t][0], bt[ks][t][1]);
+        for (int t = 0; t < C::NTV; ++t) mma16816(cz[t], zlo, 0u, zhi, 0u, bt[ks][t][0], bt[ks][t][1]);
+      }
     }
     if constexpr (BITS == 4) {
       // The codes stay biased (1024 + c; odd nibbles 1024 + 16c, whose rows
@@ -913,13 +955,16 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
       // m-tile's accumulator before the tile's mmas, so no accumulator
       // carries more than one tile's offset.
       constexpr uint32_t kHm1024 = 0xE400E400u;  // fp16 (-1024, -1024)
+      // (NF4 levels carry no offset.)
       float nb[C::NTV][4];
 #pragma unroll
       for (int t = 0; t < C::NTV; ++t) {
         nb[t][0] = nb[t][1] = nb[t][2] = nb[t][3] = 0.f;
+        if constexpr (!NF) {
 #pragma unroll
-        for (int ks = 0; ks < 2; ++ks)
-          mma16816(nb[t], kHm1024, kHm1024, kHm1024, kHm1024, bt[ks][t][0], bt[ks][t][1]);
+          for (int ks = 0; ks < 2; ++ks)
+            mma16816(nb[t], kHm1024, kHm1024, kHm1024, kHm1024, bt[ks][t][0], bt[ks][t][1]);
+        }
       }
 #pragma unroll
       for (int c = 0; c < C::CHUNKS; c += 2) {
@@ -935,16 +980,18 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
         for (int cc = 0; cc < 2; ++cc) {
           const int chunk = c + cc;
           const int t = ((chunk * C::DPC) / C::GSZ) * GP / 8;  // n-tile of the chunk's group
+          if constexpr (!NF) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            o[2 * chunk][e] += nb[t][e];
-            o[2 * chunk + 1][e] += nb[t][e];
+            for (int e = 0; e < 4; ++e) {
+              o[2 * chunk][e] += nb[t][e];
+              o[2 * chunk + 1][e] += nb[t][e];
+            }
           }
 #pragma unroll
           for (int ks = 0; ks < 2; ++ks) {
             uint32_t lo[4], hi[4];
-            nib8_to_h2_biased(x[ks][2 * cc], lo);
-            nib8_to_h2_biased(x[ks][2 * cc + 1], hi);
+            nib8_to_h2<NF>(x[ks][2 * cc], lo, lut);
+            nib8_to_h2<NF>(x[ks][2 * cc + 1], hi, lut);
             // channel of lo[e] = chunk*32 + 4*rho + e; m-tile (chunk, pp) rows: e = 2pp, 2pp+1
             mma16816(o[2 * chunk], lo[0], lo[1], hi[0], hi[1], bt[ks][t][0], bt[ks][t][1]);
             mma16816(o[2 * chunk + 1], lo[2], lo[3], hi[2], hi[3], bt[ks][t][0], bt[ks][t][1]);
@@ -989,7 +1036,16 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
     if (which < 2)
       v = __ldg(reinterpret_cast<const uint4*>(p.new_kv[which] + ((long long)b * geo.Hkv + kvh) * D) + ch);
-    const Quant8 qz = quantize8<BITS, SYM>(v, C::GSZ / 8);
+    Quant8 qz;
+    if constexpr (NF) {
+      float mid[16];  // the level midpoints, as the host computes them
+#pragma unroll
+      for (int i = 0; i < 15; ++i) mid[i] = __fmul_rn(__fadd_rn(p.nf4_level[i], p.nf4_level[i + 1]), 0.5f);
+      mid[15] = INFINITY;
+      qz = quantize8_nf4(v, C::GSZ / 8, mid);
+    } else {
+      qz = quantize8<BITS, SYM>(v, C::GSZ / 8);
+    }
     if (which < 2 && nrow >= 0) {
       uint8_t* gcodes = const_cast<uint8_t*>(p.codes[which]) + nrow * C::ROWB + ch * BITS;
       if constexpr (BITS == 4) *reinterpret_cast<uint32_t*>(gcodes) = qz.w0;
@@ -1008,7 +1064,14 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
     for (int k = 0; k < 8; ++k) {
       const uint32_t code = BITS == 4 ? (qz.w0 >> (4 * k)) & 0xFu
                                       : ((k < 4 ? qz.w0 : qz.w1) >> (8 * (k & 3))) & 0xFFu;
-      xh[k] = ((float)code - zf) * sf;
+      if constexpr (NF) {
+        float lv = 0.f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) lv = code == (uint32_t)i ? p.nf4_level[i] : lv;
+        xh[k] = lv * sf;
+      } else {
+        xh[k] = ((float)code - zf) * sf;
+      }
     }
     if (which == 1) {
 #pragma unroll
@@ -1085,7 +1148,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
         const float corr = e ? corr1 : corr0;
         float* dst = red + (warp * GP + h) * D;
         dst[d0] = o[m][e] - corr;
-        dst[d0 + 1] = o[m][2 + e] * (BITS == 4 ? 0.0625f : 1.f) - corr;  // INT4: odd rows in x16 units
+        // biased INT4: odd rows in x16 units
+        dst[d0 + 1] = o[m][2 + e] * ((BITS == 4 && !NF) ? 0.0625f : 1.f) - corr;
       }
     }
   }
@@ -1251,15 +1315,15 @@ size_t fast_smem_bytes() {
 
 // Launches the instantiation, or with ctas_per_sm != nullptr only reports
 // how many of its CTAs fit on one SM.
-template <int BITS, int D, int NG, int GP, bool SYM, bool KCH = false>
+template <int BITS, int D, int NG, int GP, bool SYM, bool KCH = false, bool NF = false>
 cudaError_t launch_fast_inst(const DecodeParams& p, cudaStream_t stream, int* ctas_per_sm) {
   const size_t smem = fast_smem_bytes<BITS, D, NG, GP, KCH>();
-  cudaError_t e = cudaFuncSetAttribute(decode_fast_kernel<BITS, D, NG, GP, SYM, KCH>,
+  cudaError_t e = cudaFuncSetAttribute(decode_fast_kernel<BITS, D, NG, GP, SYM, KCH, NF>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   if (ctas_per_sm) {
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        ctas_per_sm, decode_fast_kernel<BITS, D, NG, GP, SYM, KCH>, Cfg<BITS, D, NG, GP, KCH>::THREADS, smem);
+        ctas_per_sm, decode_fast_kernel<BITS, D, NG, GP, SYM, KCH, NF>, Cfg<BITS, D, NG, GP, KCH>::THREADS, smem);
   }
   // programmatic stream serialization: this launch may overlap the tail of the
   // previous kernel in the stream; the kernel waits for it before using any
@@ -1275,7 +1339,7 @@ cudaError_t launch_fast_inst(const DecodeParams& p, cudaStream_t stream, int* ct
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_fast_kernel<BITS, D, NG, GP, SYM, KCH>, p);
+  return cudaLaunchKernelEx(&cfg, decode_fast_kernel<BITS, D, NG, GP, SYM, KCH, NF>, p);
 }
 
 }  // namespace fast

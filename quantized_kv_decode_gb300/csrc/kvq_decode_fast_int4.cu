@@ -23,7 +23,7 @@ static cudaError_t by_gp4(const DecodeParams& p, int gp, cudaStream_t s, bool* h
 cudaError_t launch_decode_fast_int4(const DecodeParams& p, int gp, cudaStream_t s,
                                     bool* handled, int* occ) {
   *handled = false;
-  if (p.geom.nf4) return cudaSuccess;  // lookup codes: the generic kernel
+  if (p.geom.nf4) return launch_decode_fast_nf4(p, gp, s, handled, occ);
   if (p.geom.sym) return launch_decode_fast_int4_sym(p, gp, s, handled, occ);
   if (p.geom.kch) return launch_decode_fast_int4_kch(p, gp, s, handled, occ);
   const int D = p.geom.D, NG = p.geom.ngroups;

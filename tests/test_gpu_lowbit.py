@@ -3,7 +3,9 @@
 INT2 packs four codes per byte (asymmetric and symmetric grids); NF4 codes
 index sixteen normal-quantile levels with one absmax scale per group.  Codes
 and scales must equal the oracle's bit for bit; decode attention (the CUDA-
-core kernel serves both formats) must match the oracle's attention over the
+core kernel serves INT2; NF4 runs on the tensor-core kernel for head_dim 64
+/ 128 with 2 or 4 groups per head and up to 8 query heads per KV head, on
+the CUDA-core kernel otherwise) must match the oracle's attention over the
 dequantized cache within the decode tolerance (max |err| <= 2e-3, relative
 L2 <= 1e-3).  The oracle's own pins state the accuracy these formats lose.
 """
@@ -44,7 +46,8 @@ def test_int2(sym, g, D, Hq, Hkv):
     _check(c, 3, fused=True)
 
 
-@pytest.mark.parametrize("g,D,Hq,Hkv", [(64, 128, 8, 2), (32, 128, 4, 4), (64, 64, 14, 2), (128, 256, 2, 1)])
+@pytest.mark.parametrize("g,D,Hq,Hkv", [(64, 128, 8, 2), (32, 128, 4, 4), (64, 64, 14, 2), (128, 256, 2, 1),
+                                        (32, 64, 16, 2), (32, 128, 6, 2), (32, 128, 16, 2)])
 def test_nf4(g, D, Hq, Hkv):
     rng = np.random.default_rng(g * 3 + D + Hq)
     lens = rng.integers(1, 700, size=3)
@@ -52,6 +55,14 @@ def test_nf4(g, D, Hq, Hkv):
     c = Case(B=3, Hq=Hq, Hkv=Hkv, D=D, bits=4, g=g, lens=lens, seed=int(lens.sum()) + 9, nf4=True)
     _check(c, 0)
     _check(c, 2, fused=True)
+
+
+def test_nf4_long_multiwave():
+    """Tensor-core NF4: several tiles per warp, a ragged tail, one and four splits."""
+    lens = np.array([4095, 1, 2048, 33, 3001, 32])
+    c = Case(B=6, Hq=32, Hkv=8, D=128, bits=4, g=32, lens=lens, seed=4242, nf4=True)
+    _check(c, 1, fused=True)
+    _check(c, 4)
 
 
 def test_nf4_paged():
