@@ -543,7 +543,7 @@ def run_gpu_arm(args):
                                f"one fp16 absmax scale per {nf4_group} channels; tensor-core decode "
                                f"kernel, codes to fp16 levels by a byte-permute lookup"),
                       ("int2", f"asymmetric INT2 g{w.group_size} caches (four codes per byte); "
-                               f"CUDA-core decode kernel")):
+                               f"tensor-core decode kernel")):
         if key in results:
             f = results[key]
             line[f"{key}_cache"] = {

@@ -181,12 +181,20 @@ const Nf4Table& nf4_table() {
   return t;
 }
 
-// Formats and shapes with a tensor-core kernel: INT4 / INT8 codes (NF4 as
-// INT4 with a level lookup) and at most 8 query heads per KV head.
+// Formats and shapes that may have a tensor-core kernel: INT2 / INT4 / INT8
+// codes (NF4 as INT4 with a level lookup) and at most 8 query heads per KV
+// head.  The launchers report the shapes they take (`handled`).
 bool fast_format(const kvq_cache_desc* desc, int G) {
   if (G > 8) return false;
   if (desc->nf4) return nf4_table().symmetric;
-  return desc->bits == 4 || desc->bits == 8;
+  return desc->bits == 2 || desc->bits == 4 || desc->bits == 8;
+}
+
+cudaError_t launch_decode_fast(const DecodeParams& p, int bits, int gp, cudaStream_t s,
+                               bool* handled, int* occ) {
+  if (bits == 2) return launch_decode_fast_int2(p, gp, s, handled, occ);
+  if (bits == 4) return launch_decode_fast_int4(p, gp, s, handled, occ);
+  return launch_decode_fast_int8(p, gp, s, handled, occ);
 }
 
 // Which decode kernel runs for a descriptor and query-head count: the
@@ -215,8 +223,7 @@ kvq_status make_plan(const kvq_cache_desc* desc, const CacheGeom& geom, int32_t 
     probe.geom = geom;
     probe.G = G;
     bool handled = false;
-    cudaError_t e = desc->bits == 4 ? launch_decode_fast_int4(probe, gp, nullptr, &handled, &occ)
-                                    : launch_decode_fast_int8(probe, gp, nullptr, &handled, &occ);
+    cudaError_t e = launch_decode_fast(probe, desc->bits, gp, nullptr, &handled, &occ);
     if (handled && e != cudaSuccess) return KVQ_ERR_CUDA;
     plan->fast = handled;
     if (handled) plan->occ = occ;
@@ -436,9 +443,7 @@ kvq_status decode_impl(const kvq_cache_desc* desc, const kvq_cache* cache, int32
     probe.geom = p.geom;
     probe.G = G;
     bool fast = false;
-    const cudaError_t pe = desc->bits == 4
-        ? launch_decode_fast_int4(probe, plan.gp, nullptr, &fast, &occ)
-        : launch_decode_fast_int8(probe, plan.gp, nullptr, &fast, &occ);
+    const cudaError_t pe = launch_decode_fast(probe, desc->bits, plan.gp, nullptr, &fast, &occ);
     if (fast && pe != cudaSuccess) return KVQ_ERR_CUDA;
     if (!fast) occ = 0;
   }
@@ -474,8 +479,7 @@ kvq_status decode_impl(const kvq_cache_desc* desc, const kvq_cache* cache, int32
   };
   if (fused && desc->k_per_channel) e = append_first();
   if (e == cudaSuccess && fast_format(desc, G)) {
-    if (desc->bits == 4) e = launch_decode_fast_int4(p, plan.gp, s, &handled, nullptr);
-    else e = launch_decode_fast_int8(p, plan.gp, s, &handled, nullptr);
+    e = launch_decode_fast(p, desc->bits, plan.gp, s, &handled, nullptr);
   }
   if (e == cudaSuccess && !handled) {
     if (fused && !appended) e = append_first();

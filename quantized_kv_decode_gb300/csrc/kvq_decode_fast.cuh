@@ -81,9 +81,13 @@ struct Cfg {
   static constexpr int NTV = (NG * GP + 7) / 8;           // V-mma n-tiles: columns (group, head)
   static constexpr int NGL = (NG < 8 / GP) ? NG : 8 / GP;  // groups in accumulator rows 0..7
   static constexpr bool HI = NG * GP > 8;                   // rows 8..15 in use
-  static_assert(BITS == 4 || BITS == 8, "bits");
+  static_assert(BITS == 2 || BITS == 4 || BITS == 8, "bits");
+  static_assert(BITS != 2 || !KCH, "INT2: per-token caches only");
+  // INT2: a 16-byte chunk spans 64 channels; a chunk of more than one group
+  // needs all its (group, head) columns in one V-mma n-tile
+  static_assert(BITS != 2 || GSZ % DPC == 0 || NG * GP <= 8, "INT2 groups");
   static_assert(ROWB == 32 || ROWB == 64 || ROWB == 128, "code row size");
-  static_assert(GSZ % DPC == 0, "a 16-byte chunk must lie inside one group");
+  static_assert(BITS == 2 || GSZ % DPC == 0, "a 16-byte chunk must lie inside one group");
   static_assert(NG * GP <= 16, "groups x padded heads must fit 16 rows");
   static_assert(HDRB == 4 || HDRB == 8 || HDRB == 16, "header row size");
   static_assert(2 * GP * (D + 2) * 4 <= WARP_BYTES, "the CTA merge reuses the pipeline region");
@@ -204,6 +208,25 @@ __device__ __forceinline__ void nib8_to_h2_nf4(uint32_t w, uint32_t (&o)[4],
   o[3] = __byte_perm(ql, qh, 0x7351u) ^ ((neg & 0x10001000u) << 3);
 }
 
+// Sixteen 2-bit codes (byte m = codes 4m .. 4m+3, code 4m + f in bits 2f of
+// byte m) to fp16 pairs 1024 + 4^f c, f = k & 3, by the same and-or as
+// nib8_to_h2_biased: o[k] = (code at byte k>>2, field f; the same field of
+// byte 2 + (k>>2)).  The factor 4^f is undone on the other operand (score
+// side) or at the end (value side).
+__device__ __forceinline__ void crumb16_to_h2_biased(uint32_t w, uint32_t (&o)[8]) {
+  const uint32_t w2 = w >> 8;
+#pragma unroll
+  for (int f = 0; f < 4; ++f) {
+    o[f] = and_or(w, 0x00030003u << (2 * f), kH1024);
+    o[4 + f] = and_or(w2, 0x00030003u << (2 * f), kH1024);
+  }
+}
+
+// A biased fp16 pair 1024 + x back to x (exact for the codes' x < 1024).
+__device__ __forceinline__ uint32_t unbias(uint32_t x) {
+  return h2_as_u32(__hsub2(u32_as_h2(x), u32_as_h2(kH1024)));
+}
+
 // The 4-bit conversion of a kernel instance: biased codes, or NF4 levels.
 template <bool NF>
 __device__ __forceinline__ void nib8_to_h2(uint32_t w, uint32_t (&o)[4], const uint32_t (&lut)[4]) {
@@ -221,8 +244,7 @@ __device__ __forceinline__ uint32_t byte2_to_h2_biased(uint32_t w) {
 // sel 0x4140 -> (c0, c1), 0x4342 -> (c2, c3), 0x4240 -> (c0, c2), 0x4341 -> (c1, c3).
 template <uint32_t SEL>
 __device__ __forceinline__ uint32_t byte2_to_h2(uint32_t w) {
-  const uint32_t x = __byte_perm(w, 0x64646464u, SEL);
-  return h2_as_u32(__hsub2(u32_as_h2(x), u32_as_h2(kH1024)));
+  return unbias(__byte_perm(w, 0x64646464u, SEL));
 }
 
 // 2^x by the SFU (flush-to-zero; 2^-inf = 0)
@@ -261,7 +283,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
   // NF: NF4 codes (with SYM: scale only), which stand for normal-quantile
   // levels; no offset to remove and no zero-point.
   static_assert(!NF || (BITS == 4 && SYM && !KCH), "NF4: 4-bit, scale-only, per-token");
-  constexpr unsigned short kSymZero = NF ? 0u : (BITS == 4 ? 0x4800u : 0x5800u);  // fp16 0, 8, 128
+  constexpr unsigned short kSymZero =
+      NF ? 0u : (BITS == 2 ? 0x4000u : (BITS == 4 ? 0x4800u : 0x5800u));  // fp16 0, 2, 8, 128
   // NF4: the 8 level magnitudes as fp16 bytes (see nib8_to_h2_nf4)
   uint32_t lut[4] = {0u, 0u, 0u, 0u};
   if constexpr (NF) {
@@ -390,7 +413,12 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
   // channel of the score-mma k-slots 2jj, 2jj+1, 2jj+8, 2jj+9 of k-block kb
   // (the order in which the code conversions deliver channels)
   auto slot_channels = [](int kb, int jj, int (&dk)[4]) {
-    if constexpr (BITS == 4) {
+    if constexpr (BITS == 2) {
+      // k-block kb = 4 c + i of chunk c takes conversion outputs 2i, 2i+1
+      const int i = kb & 3;
+      const int x = 64 * (kb >> 2) + 16 * jj + 4 * (i >> 1) + 2 * (i & 1);
+      dk[0] = x; dk[1] = x + 8; dk[2] = x + 1; dk[3] = x + 9;
+    } else if constexpr (BITS == 4) {
       const int base = 32 * (kb >> 1) + 8 * jj + 2 * (kb & 1);
       dk[0] = base; dk[1] = base + 4; dk[2] = base + 1; dk[3] = base + 5;
     } else {
@@ -401,18 +429,23 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
   uint32_t qa[C::KB][4];
 #pragma unroll
   for (int kb = 0; kb < C::KB; ++kb) {
-    const int grp = (16 * kb) / C::GSZ;
     int dk[4];  // channel of k-slots 2j, 2j+1, 2j+8, 2j+9
     slot_channels(kb, j, dk);
+    const int grp = dk[0] / C::GSZ;  // the four lie in one group
     const __half* qh = q_s + h_row * D;
     const bool lo = row_ok && (KCH || g_lo == grp);
     const bool hi = row_ok && (KCH || (C::HI && g_hi == grp));
     const uint32_t v01 = pack_halves(qh[dk[0]], qh[dk[1]]);
     uint32_t v23 = pack_halves(qh[dk[2]], qh[dk[3]]);
+    uint32_t v01s = v01;
     if constexpr (BITS == 4 && !NF)  // slots 2j+8, 2j+9 meet the odd nibbles, held as 16c
       v23 = h2_as_u32(__hmul2(u32_as_h2(v23), u32_as_h2(kH1_16)));
-    qa[kb][0] = lo ? v01 : 0u;
-    qa[kb][1] = hi ? v01 : 0u;
+    if constexpr (BITS == 2) {  // slots meet codes held as 4^f c: f = 2 (kb & 1), + 1 for 2j+8, 2j+9
+      v01s = h2_as_u32(__hmul2(u32_as_h2(v01), u32_as_h2((kb & 1) ? kH1_16 : 0x3C003C00u)));
+      v23 = h2_as_u32(__hmul2(u32_as_h2(v23), u32_as_h2((kb & 1) ? 0x24002400u : 0x34003400u)));
+    }
+    qa[kb][0] = lo ? v01s : 0u;
+    qa[kb][1] = hi ? v01s : 0u;
     qa[kb][2] = lo ? v23 : 0u;
     qa[kb][3] = hi ? v23 : 0u;
   }
@@ -429,7 +462,10 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
     constexpr uint32_t kHi = (BITS == 4 && !NF) ? 0x4C004C00u : 0x3C003C00u;  // x16 undoes q/16 in odd slots
 #pragma unroll
     for (int kb = 0; kb < C::KB; ++kb) {
-      mma16816(acc, kOnes, kOnes, kHi, kHi, qa[kb][0], qa[kb][2]);
+      // INT2: 4^f undoes the slots' 4^-f (1, 4 or 16, 64)
+      const uint32_t ulo = BITS == 2 ? ((kb & 1) ? 0x4C004C00u : kOnes) : kOnes;
+      const uint32_t uhi = BITS == 2 ? ((kb & 1) ? 0x54005400u : 0x44004400u) : kHi;
+      mma16816(acc, ulo, ulo, uhi, uhi, qa[kb][0], qa[kb][2]);
       if constexpr (!NF) mma16816(bia, kH1024, kH1024, kH1024, kH1024, qa[kb][0], qa[kb][2]);
     }
     qs_lo = acc[0];   // column 2j
@@ -443,8 +479,10 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
     constexpr uint32_t kSixteen = 0x4C004C00u;  // fp16 (16, 16)
 #pragma unroll
     for (int kb = 0; kb < C::KB; ++kb) {
-      mma16816(acc, qa[kb][0], qa[kb][1], qa[kb][2], qa[kb][3], kOnes,
-               (BITS == 4 && !NF) ? kSixteen : kOnes);
+      const uint32_t ulo = BITS == 2 ? ((kb & 1) ? kSixteen : kOnes) : kOnes;
+      const uint32_t uhi = BITS == 2 ? ((kb & 1) ? 0x54005400u : 0x44004400u)
+                                     : ((BITS == 4 && !NF) ? kSixteen : kOnes);
+      mma16816(acc, qa[kb][0], qa[kb][1], qa[kb][2], qa[kb][3], ulo, uhi);
       if constexpr (!NF) mma16816(bia, qa[kb][0], qa[kb][1], qa[kb][2], qa[kb][3], kH1024, kH1024);
     }
     qs_lo = acc[0];
@@ -712,7 +750,16 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
         float acc[2][4] = {{c0, c1, c0, c1}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
         for (int c = 0; c < C::CHUNKS; ++c) {
-          if constexpr (BITS == 4) {
+          if constexpr (BITS == 2) {
+            // a chunk of 64 channels: k-blocks 4c .. 4c+3
+            uint32_t h0[8], h1[8];
+            crumb16_to_h2_biased(w[0][c], h0);
+            crumb16_to_h2_biased(w[1][c], h1);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              mma16816(acc[i & 1], h0[2 * i], h1[2 * i], h0[2 * i + 1], h1[2 * i + 1],
+                       qa[4 * c + i][0], qa[4 * c + i][2]);
+          } else if constexpr (BITS == 4) {
             uint32_t h0[4], h1[4];
             nib8_to_h2<NF>(w[0][c], h0, lut);
             nib8_to_h2<NF>(w[1][c], h1, lut);
@@ -812,7 +859,17 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
       }
 #pragma unroll
       for (int c = 0; c < C::CHUNKS; ++c) {
-        if constexpr (BITS == 4) {
+        if constexpr (BITS == 2) {
+          uint32_t h0[8], h1[8];
+          crumb16_to_h2_biased(w[0][c], h0);
+          crumb16_to_h2_biased(w[1][c], h1);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int kb = 4 * c + i;
+            mma16816(acc[0], Aop[kb][0], Aop[kb][1], Aop[kb][2], Aop[kb][3], h0[2 * i], h0[2 * i + 1]);
+            mma16816(acc[1], Aop[kb][0], Aop[kb][1], Aop[kb][2], Aop[kb][3], h1[2 * i], h1[2 * i + 1]);
+          }
+        } else if constexpr (BITS == 4) {
           uint32_t h0[4], h1[4];
           nib8_to_h2<NF>(w[0][c], h0, lut);
           nib8_to_h2<NF>(w[1][c], h1, lut);
@@ -948,9 +1005,10 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
         for (int t = 0; t < C::NTV; ++t) mma16816(cz[t], zlo, 0u, zhi, 0u, bt[ks][t][0], bt[ks][t][1]);
       }
     }
-    if constexpr (BITS == 4) {
+    if constexpr (BITS <= 4) {
       // The codes stay biased (1024 + c; odd nibbles 1024 + 16c, whose rows
-      // accumulate in x16 units until the end).  Per n-tile, -1024 sum_t B
+      // accumulate in x16 units until the end; INT2: 1024 + 4^f c, rows in
+      // 4^f units).  Per n-tile, -1024 sum_t B
       // (every row) is the offset they add over this tile; it goes into each
       // m-tile's accumulator before the tile's mmas, so no accumulator
       // carries more than one tile's offset.
@@ -960,7 +1018,7 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
 #pragma unroll
       for (int t = 0; t < C::NTV; ++t) {
         nb[t][0] = nb[t][1] = nb[t][2] = nb[t][3] = 0.f;
-        if constexpr (!NF) {
+        if constexpr (!NF && BITS == 4) {
 #pragma unroll
           for (int ks = 0; ks < 2; ++ks)
             mma16816(nb[t], kHm1024, kHm1024, kHm1024, kHm1024, bt[ks][t][0], bt[ks][t][1]);
@@ -979,7 +1037,29 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
           const int chunk = c + cc;
-          const int t = ((chunk * C::DPC) / C::GSZ) * GP / 8;  // n-tile of the chunk's group
+          // n-tile of the chunk's group (INT2 chunks of several groups: one n-tile)
+          const int t = C::NTV == 1 ? 0 : ((chunk * C::DPC) / C::GSZ) * GP / 8;
+          if constexpr (BITS == 2) {
+            // m-tile 4 chunk + f: rows rho / rho + 8 = channels 64 chunk + 8 rho + f / + 4 + f.
+            // The codes lose their bias in fp16 (exact) rather than through
+            // an offset term: for field 0 the 1024 would be ~700x the signal
+            // (codes 0..3), and the accumulator's rounding of it would show.
+#pragma unroll
+            for (int ks = 0; ks < 2; ++ks) {
+              uint32_t lo[8], hi[8];
+              crumb16_to_h2_biased(x[ks][2 * cc], lo);
+              crumb16_to_h2_biased(x[ks][2 * cc + 1], hi);
+#pragma unroll
+              for (int r = 0; r < 8; ++r) {
+                lo[r] = unbias(lo[r]);
+                hi[r] = unbias(hi[r]);
+              }
+#pragma unroll
+              for (int f = 0; f < 4; ++f)
+                mma16816(o[4 * chunk + f], lo[f], lo[4 + f], hi[f], hi[4 + f], bt[ks][t][0], bt[ks][t][1]);
+            }
+            continue;
+          }
           if constexpr (!NF) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -1048,7 +1128,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
     }
     if (which < 2 && nrow >= 0) {
       uint8_t* gcodes = const_cast<uint8_t*>(p.codes[which]) + nrow * C::ROWB + ch * BITS;
-      if constexpr (BITS == 4) *reinterpret_cast<uint32_t*>(gcodes) = qz.w0;
+      if constexpr (BITS == 2) *reinterpret_cast<uint16_t*>(gcodes) = (uint16_t)qz.w0;
+      else if constexpr (BITS == 4) *reinterpret_cast<uint32_t*>(gcodes) = qz.w0;
       else *reinterpret_cast<uint2*>(gcodes) = make_uint2(qz.w0, qz.w1);
       if (ch % (C::GSZ / 8) == 0) {
         const int g = ch / (C::GSZ / 8);
@@ -1062,7 +1143,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
     float xh[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
-      const uint32_t code = BITS == 4 ? (qz.w0 >> (4 * k)) & 0xFu
+      const uint32_t code = BITS == 2 ? (qz.w0 >> (2 * k)) & 0x3u
+                          : BITS == 4 ? (qz.w0 >> (4 * k)) & 0xFu
                                       : ((k < 4 ? qz.w0 : qz.w1) >> (8 * (k & 3))) & 0xFFu;
       if constexpr (NF) {
         float lv = 0.f;
@@ -1132,10 +1214,20 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
   float* ml = red + kWarps * GP * D;                            // [warps][GP][2]
 #pragma unroll
   for (int m = 0; m < C::MT; ++m) {
-    int d0;
-    if constexpr (BITS == 4) d0 = 32 * (m >> 1) + 4 * rho + 2 * (m & 1);
-    else d0 = 16 * m + 2 * rho;
-    const int g = ((BITS == 4 ? (m >> 1) : m) * C::DPC) / C::GSZ;  // group of the m-tile's chunk
+    // rows rho / rho + 8 of m-tile m: channels d0 / d0 + d1, held in units
+    // of 1 / fac (the biased INT4 and INT2 codes' field weights)
+    int d0, d1 = 1;
+    float fac = 1.f;
+    if constexpr (BITS == 2) {
+      d0 = 64 * (m >> 2) + 8 * rho + (m & 3);
+      d1 = 4;
+      fac = (m & 3) == 0 ? 1.f : (m & 3) == 1 ? 0.25f : (m & 3) == 2 ? 0.0625f : 0.015625f;
+    } else if constexpr (BITS == 4) {
+      d0 = 32 * (m >> 1) + 4 * rho + 2 * (m & 1);
+    } else {
+      d0 = 16 * m + 2 * rho;
+    }
+    const int g = d0 / C::GSZ;  // group of the lane's rows
     const int t = g * GP / 8;
     // o[channel][(g, h)] -= cz[g][(g, h)]: row g of the correction lives in lanes 4g + j
     const float corr0 = __shfl_sync(0xffffffffu, cz[t][0], (g << 2) + j);
@@ -1147,9 +1239,14 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
       if (col / GP == g && h < G && warp < kWarps) {
         const float corr = e ? corr1 : corr0;
         float* dst = red + (warp * GP + h) * D;
-        dst[d0] = o[m][e] - corr;
-        // biased INT4: odd rows in x16 units
-        dst[d0 + 1] = o[m][2 + e] * ((BITS == 4 && !NF) ? 0.0625f : 1.f) - corr;
+        if constexpr (BITS == 2) {
+          dst[d0] = o[m][e] * fac - corr;
+          dst[d0 + d1] = o[m][2 + e] * fac - corr;
+        } else {
+          dst[d0] = o[m][e] - corr;
+          // biased INT4: odd rows in x16 units
+          dst[d0 + 1] = o[m][2 + e] * ((BITS == 4 && !NF) ? 0.0625f : 1.f) - corr;
+        }
       }
     }
   }

@@ -226,6 +226,9 @@ cudaError_t launch_decode_fast_int4(const DecodeParams& p, int gp, cudaStream_t 
                                     int* occ);
 cudaError_t launch_decode_fast_int4_sym(const DecodeParams& p, int gp, cudaStream_t s,
                                         bool* handled, int* occ);
+// INT2 caches, head_dim 128
+cudaError_t launch_decode_fast_int2(const DecodeParams& p, int gp, cudaStream_t s, bool* handled,
+                                    int* occ);
 // NF4 caches (with a symmetric level table: the caller checks it)
 cudaError_t launch_decode_fast_nf4(const DecodeParams& p, int gp, cudaStream_t s, bool* handled,
                                    int* occ);

@@ -3,9 +3,10 @@
 INT2 packs four codes per byte (asymmetric and symmetric grids); NF4 codes
 index sixteen normal-quantile levels with one absmax scale per group.  Codes
 and scales must equal the oracle's bit for bit; decode attention (the CUDA-
-core kernel serves INT2; NF4 runs on the tensor-core kernel for head_dim 64
-/ 128 with 2 or 4 groups per head and up to 8 query heads per KV head, on
-the CUDA-core kernel otherwise) must match the oracle's attention over the
+tensor-core kernel takes INT2 at head_dim 128 with groups of 16, 32 or 64
+channels, and NF4 at head_dim 64 / 128 with 2 or 4 groups per head, for up
+to 8 query heads per KV head (g16 / g32 INT2: 8 / 4 (group, head) columns);
+the CUDA-core kernel serves the other shapes) must match the oracle's attention over the
 dequantized cache within the decode tolerance (max |err| <= 2e-3, relative
 L2 <= 1e-3).  The oracle's own pins state the accuracy these formats lose.
 """
@@ -36,7 +37,9 @@ def _check(c, splits=0, fused=False):
 
 
 @pytest.mark.parametrize("sym", [False, True])
-@pytest.mark.parametrize("g,D,Hq,Hkv", [(32, 128, 8, 2), (16, 64, 4, 4), (64, 128, 4, 1)])
+@pytest.mark.parametrize("g,D,Hq,Hkv", [(32, 128, 8, 2), (16, 64, 4, 4), (64, 128, 4, 1),
+                                        (32, 128, 4, 4), (16, 128, 8, 8), (32, 128, 16, 8),
+                                        (64, 128, 16, 2), (64, 128, 6, 2)])
 def test_int2(sym, g, D, Hq, Hkv):
     rng = np.random.default_rng(g + D + Hq + int(sym))
     lens = rng.integers(1, 600, size=3)
@@ -55,6 +58,23 @@ def test_nf4(g, D, Hq, Hkv):
     c = Case(B=3, Hq=Hq, Hkv=Hkv, D=D, bits=4, g=g, lens=lens, seed=int(lens.sum()) + 9, nf4=True)
     _check(c, 0)
     _check(c, 2, fused=True)
+
+
+@pytest.mark.parametrize("g", [16, 32, 64])
+def test_int2_long_multiwave(g):
+    """Tensor-core INT2: several tiles per warp, ragged tails, one and four splits."""
+    lens = np.array([4095, 1, 2048, 33, 3001, 32])
+    c = Case(B=6, Hq=8, Hkv=8, D=128, bits=2, g=g, lens=lens, seed=4343 + g)
+    _check(c, 1, fused=True)
+    _check(c, 4)
+
+
+def test_int2_paged():
+    lens = np.array([130, 0, 64, 47, 300])
+    c = Case(B=5, Hq=8, Hkv=2, D=128, bits=2, g=64, lens=lens, seed=78, layout="paged",
+             page_size=16, symmetric=True)
+    _check(c, 2)
+    _check(c, 0, fused=True)
 
 
 def test_nf4_long_multiwave():
