@@ -188,24 +188,36 @@ __device__ __forceinline__ void nib8_to_h2_biased(uint32_t w, uint32_t (&o)[4]) 
   o[3] = and_or(w2, 0x00F000F0u, kH1024);
 }
 
+// prmt.b32 in its default mode: a selector nibble with bit 3 set gives its
+// output byte the sign (bit 7) of the selected byte, replicated.
+__device__ __forceinline__ uint32_t prmt_b32(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
 // NF4 codes of one 32-bit word to their fp16 levels, in the pairing of
 // nib8_to_h2_biased: o[0] = (lv(c0), lv(c4)), o[1] = (lv(c1), lv(c5)), ...
-// The 16 levels are symmetric, lv(15 - c) = -lv(c), so a code picks one of
-// 8 magnitudes (c - 8 for c >= 8, 7 - c below) and a sign.  lut holds the
-// magnitudes' fp16 bytes: lut[0] / lut[1] the low bytes of magnitudes 0-3 /
-// 4-7, lut[2] / lut[3] the high bytes; byte permutes do the lookup.
+// The 16 levels are antisymmetric, lv(15 - c) = -lv(c), so a code picks one
+// of 8 magnitudes (c - 8 for c >= 8, 7 - c below) and a sign.  lut holds
+// the magnitudes' fp16 bytes: lut[0] / lut[1] the low bytes of magnitudes
+// 0-3 / 4-7, lut[2] / lut[3] the high bytes; byte permutes do the lookup,
+// and sign-replicating permutes of the codes' bit 3 set the sign bits.
 __device__ __forceinline__ void nib8_to_h2_nf4(uint32_t w, uint32_t (&o)[4],
                                                const uint32_t (&lut)[4]) {
-  const uint32_t neg = ((w >> 3) & 0x11111111u) ^ 0x11111111u;  // per code: 1 if lv < 0
-  const uint32_t idx = (w ^ ((neg << 3) - neg)) & 0x77777777u;    // magnitude index
-  const uint32_t s01 = __byte_perm(idx, 0u, 0x0020u);  // selectors (c0, c1, c4, c5)
-  const uint32_t s23 = __byte_perm(idx, 0u, 0x0031u);  // selectors (c2, c3, c6, c7)
-  const uint32_t pl = __byte_perm(lut[0], lut[1], s01), ph = __byte_perm(lut[2], lut[3], s01);
-  const uint32_t ql = __byte_perm(lut[0], lut[1], s23), qh = __byte_perm(lut[2], lut[3], s23);
-  o[0] = __byte_perm(pl, ph, 0x6240u) ^ ((neg & 0x00010001u) << 15);
-  o[1] = __byte_perm(pl, ph, 0x7351u) ^ ((neg & 0x00100010u) << 11);
-  o[2] = __byte_perm(ql, qh, 0x6240u) ^ ((neg & 0x01000100u) << 7);
-  o[3] = __byte_perm(ql, qh, 0x7351u) ^ ((neg & 0x10001000u) << 3);
+  const uint32_t S = ~w & 0x88888888u;                         // per code: bit 3 set iff lv < 0
+  const uint32_t idx = (w ^ (S - (S >> 3))) & 0x77777777u;      // magnitude index
+  const uint32_t S4 = S << 4;  // the flags of even codes at their byte's bit 7
+  const uint32_t s01 = prmt_b32(idx, 0u, 0x0020u);  // selectors (c0, c1, c4, c5)
+  const uint32_t s23 = prmt_b32(idx, 0u, 0x0031u);  // selectors (c2, c3, c6, c7)
+  const uint32_t pl = prmt_b32(lut[0], lut[1], s01);
+  const uint32_t ql = prmt_b32(lut[0], lut[1], s23);
+  const uint32_t ph = prmt_b32(lut[2], lut[3], s01) | (prmt_b32(S4, S, 0xEAC8u) & 0x80808080u);
+  const uint32_t qh = prmt_b32(lut[2], lut[3], s23) | (prmt_b32(S4, S, 0xFBD9u) & 0x80808080u);
+  o[0] = prmt_b32(pl, ph, 0x6240u);
+  o[1] = prmt_b32(pl, ph, 0x7351u);
+  o[2] = prmt_b32(ql, qh, 0x6240u);
+  o[3] = prmt_b32(ql, qh, 0x7351u);
 }
 
 // Sixteen 2-bit codes (byte m = codes 4m .. 4m+3, code 4m + f in bits 2f of
