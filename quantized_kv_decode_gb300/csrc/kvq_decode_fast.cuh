@@ -188,6 +188,18 @@ __device__ __forceinline__ void nib8_to_h2_biased(uint32_t w, uint32_t (&o)[4]) 
   o[3] = and_or(w2, 0x00F000F0u, kH1024);
 }
 
+// The same codes as exact fp16 subnormals: with no exponent bits the half
+// (c) is c * 2^-24 and (16c) is 16c * 2^-24, so the contractions carry no
+// offset; the 2^24 goes into a scale on the other side of each contraction.
+// Tensor cores take fp16 subnormal inputs at full precision.
+__device__ __forceinline__ void nib8_to_h2_sub(uint32_t w, uint32_t (&o)[4]) {
+  const uint32_t w2 = w >> 8;
+  o[0] = w & 0x000F000Fu;
+  o[1] = w & 0x00F000F0u;
+  o[2] = w2 & 0x000F000Fu;
+  o[3] = w2 & 0x00F000F0u;
+}
+
 // prmt.b32 in its default mode: a selector nibble with bit 3 set gives its
 // output byte the sign (bit 7) of the selected byte, replicated.
 __device__ __forceinline__ uint32_t prmt_b32(uint32_t a, uint32_t b, uint32_t sel) {
@@ -234,29 +246,50 @@ __device__ __forceinline__ void crumb16_to_h2_biased(uint32_t w, uint32_t (&o)[8
   }
 }
 
+// crumb16_to_h2_biased's codes as fp16 subnormals 4^f c * 2^-24.
+__device__ __forceinline__ void crumb16_to_h2_sub(uint32_t w, uint32_t (&o)[8]) {
+  const uint32_t w2 = w >> 8;
+#pragma unroll
+  for (int f = 0; f < 4; ++f) {
+    o[f] = w & (0x00030003u << (2 * f));
+    o[4 + f] = w2 & (0x00030003u << (2 * f));
+  }
+}
+
+template <bool SUB>
+__device__ __forceinline__ void crumb16_to_h2(uint32_t w, uint32_t (&o)[8]) {
+  if constexpr (SUB) crumb16_to_h2_sub(w, o);
+  else crumb16_to_h2_biased(w, o);
+}
+
 // A biased fp16 pair 1024 + x back to x (exact for the codes' x < 1024).
 __device__ __forceinline__ uint32_t unbias(uint32_t x) {
   return h2_as_u32(__hsub2(u32_as_h2(x), u32_as_h2(kH1024)));
 }
 
-// The 4-bit conversion of a kernel instance: biased codes, or NF4 levels.
-template <bool NF>
+// The 4-bit conversion of a kernel instance: NF4 levels, subnormal codes or
+// biased codes.
+template <bool NF, bool SUB>
 __device__ __forceinline__ void nib8_to_h2(uint32_t w, uint32_t (&o)[4], const uint32_t (&lut)[4]) {
   if constexpr (NF) nib8_to_h2_nf4(w, o, lut);
+  else if constexpr (SUB) nib8_to_h2_sub(w, o);
   else nib8_to_h2_biased(w, o);
 }
 
-// Four 8-bit codes (byte k = code k) to fp16 pairs 1024 + c (score side).
-template <uint32_t SEL>
+// Four 8-bit codes (byte k = code k) to fp16 pairs 1024 + c (score side),
+// or (SUB) the subnormals c * 2^-24.
+template <uint32_t SEL, bool SUB = false>
 __device__ __forceinline__ uint32_t byte2_to_h2_biased(uint32_t w) {
-  return __byte_perm(w, 0x64646464u, SEL);
+  return __byte_perm(w, SUB ? 0u : 0x64646464u, SEL);
 }
 
 // Four 8-bit codes (byte k = code k) to fp16 pairs per the selectors:
 // sel 0x4140 -> (c0, c1), 0x4342 -> (c2, c3), 0x4240 -> (c0, c2), 0x4341 -> (c1, c3).
-template <uint32_t SEL>
+// (SUB: the subnormals c * 2^-24, no subtraction.)
+template <uint32_t SEL, bool SUB = false>
 __device__ __forceinline__ uint32_t byte2_to_h2(uint32_t w) {
-  return unbias(__byte_perm(w, 0x64646464u, SEL));
+  if constexpr (SUB) return __byte_perm(w, 0u, SEL);
+  else return unbias(__byte_perm(w, 0x64646464u, SEL));
 }
 
 // 2^x by the SFU (flush-to-zero; 2^-inf = 0)
@@ -297,6 +330,13 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
   static_assert(!NF || (BITS == 4 && SYM && !KCH), "NF4: 4-bit, scale-only, per-token");
   constexpr unsigned short kSymZero =
       NF ? 0u : (BITS == 2 ? 0x4000u : (BITS == 4 ? 0x4800u : 0x5800u));  // fp16 0, 2, 8, 128
+  // Per-token integer codes enter the tensor cores as fp16 subnormals (code *
+  // 2^-24, see nib8_to_h2_sub): no offsets to cancel.  kSub restores the
+  // scale: the K scales in the header scratch, the q sums of the zero-point
+  // term and the final rows carry it.  Axis-aware caches keep biased codes.
+  constexpr bool SUBN = !KCH && !NF;
+  constexpr float kSub = SUBN ? 16777216.f : 1.f;  // 2^24
+  const float kscale = p.scale_log2 * kSub;  // K scale factor of the header scratch
   // NF4: the 8 level magnitudes as fp16 bytes (see nib8_to_h2_nf4)
   uint32_t lut[4] = {0u, 0u, 0u, 0u};
   if constexpr (NF) {
@@ -478,7 +518,7 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
       const uint32_t ulo = BITS == 2 ? ((kb & 1) ? 0x4C004C00u : kOnes) : kOnes;
       const uint32_t uhi = BITS == 2 ? ((kb & 1) ? 0x54005400u : 0x44004400u) : kHi;
       mma16816(acc, ulo, ulo, uhi, uhi, qa[kb][0], qa[kb][2]);
-      if constexpr (!NF) mma16816(bia, kH1024, kH1024, kH1024, kH1024, qa[kb][0], qa[kb][2]);
+      if constexpr (!NF && !SUBN) mma16816(bia, kH1024, kH1024, kH1024, kH1024, qa[kb][0], qa[kb][2]);
     }
     qs_lo = acc[0];   // column 2j
     qs_hi = acc[1];   // column 2j + 1
@@ -495,13 +535,17 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
       const uint32_t uhi = BITS == 2 ? ((kb & 1) ? 0x54005400u : 0x44004400u)
                                      : ((BITS == 4 && !NF) ? kSixteen : kOnes);
       mma16816(acc, qa[kb][0], qa[kb][1], qa[kb][2], qa[kb][3], ulo, uhi);
-      if constexpr (!NF) mma16816(bia, qa[kb][0], qa[kb][1], qa[kb][2], qa[kb][3], kH1024, kH1024);
+      if constexpr (!NF && !SUBN) mma16816(bia, qa[kb][0], qa[kb][1], qa[kb][2], qa[kb][3], kH1024, kH1024);
     }
     qs_lo = acc[0];
     qs_hi = acc[2];
     off_lo = bia[0];
     off_hi = bia[2];
   }
+  // subnormal codes: the score accumulators carry 2^-24 sum q c, so the
+  // zero-point term's q sums do too (the header's K scales carry 2^24)
+  qs_lo *= 1.f / kSub;
+  qs_hi *= 1.f / kSub;
   const int g_lo_c = min(g_lo, NG - 1), g_hi_c = min(g_hi, NG - 1);
   // After the group sum, lane rho holds the scores of head rho % GP; lanes of
   // a head beyond G read a row of -inf as their token mask.
@@ -644,7 +688,7 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
       if constexpr (!KCH) {
         const unsigned short uk = (unsigned short)(r[0][g / 2] >> sh);
         const unsigned short uz = SYM ? kSymZero : (unsigned short)(r[1][g / 2] >> sh);
-        const float2 kv = make_float2(__half2float(__ushort_as_half(uk)) * p.scale_log2,
+        const float2 kv = make_float2(__half2float(__ushort_as_half(uk)) * kscale,
                                       __half2float(__ushort_as_half(uz)));
         if constexpr (TQ) ksz[lane * NG + g] = kv;   // [token][group]
         else ksz[g * C::KROW + lane] = kv;           // [group][token]
@@ -765,16 +809,16 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
           if constexpr (BITS == 2) {
             // a chunk of 64 channels: k-blocks 4c .. 4c+3
             uint32_t h0[8], h1[8];
-            crumb16_to_h2_biased(w[0][c], h0);
-            crumb16_to_h2_biased(w[1][c], h1);
+            crumb16_to_h2<SUBN>(w[0][c], h0);
+            crumb16_to_h2<SUBN>(w[1][c], h1);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               mma16816(acc[i & 1], h0[2 * i], h1[2 * i], h0[2 * i + 1], h1[2 * i + 1],
                        qa[4 * c + i][0], qa[4 * c + i][2]);
           } else if constexpr (BITS == 4) {
             uint32_t h0[4], h1[4];
-            nib8_to_h2<NF>(w[0][c], h0, lut);
-            nib8_to_h2<NF>(w[1][c], h1, lut);
+            nib8_to_h2<NF, SUBN>(w[0][c], h0, lut);
+            nib8_to_h2<NF, SUBN>(w[1][c], h1, lut);
             const uint32_t b00 = KCH ? Bq[2 * c][0] : qa[2 * c][0];
             const uint32_t b01 = KCH ? Bq[2 * c][1] : qa[2 * c][2];
             const uint32_t b10 = KCH ? Bq[2 * c + 1][0] : qa[2 * c + 1][0];
@@ -782,10 +826,10 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
             mma16816(acc[0], h0[0], h1[0], h0[1], h1[1], b00, b01);
             mma16816(acc[1], h0[2], h1[2], h0[3], h1[3], b10, b11);
           } else {
-            const uint32_t a0 = byte2_to_h2_biased<0x4140>(w[0][c]);
-            const uint32_t a1 = byte2_to_h2_biased<0x4140>(w[1][c]);
-            const uint32_t a2 = byte2_to_h2_biased<0x4342>(w[0][c]);
-            const uint32_t a3 = byte2_to_h2_biased<0x4342>(w[1][c]);
+            const uint32_t a0 = byte2_to_h2_biased<0x4140, SUBN>(w[0][c]);
+            const uint32_t a1 = byte2_to_h2_biased<0x4140, SUBN>(w[1][c]);
+            const uint32_t a2 = byte2_to_h2_biased<0x4342, SUBN>(w[0][c]);
+            const uint32_t a3 = byte2_to_h2_biased<0x4342, SUBN>(w[1][c]);
             mma16816(acc[c & 1], a0, a1, a2, a3, KCH ? Bq[c][0] : qa[c][0], KCH ? Bq[c][1] : qa[c][2]);
           }
         }
@@ -873,8 +917,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
       for (int c = 0; c < C::CHUNKS; ++c) {
         if constexpr (BITS == 2) {
           uint32_t h0[8], h1[8];
-          crumb16_to_h2_biased(w[0][c], h0);
-          crumb16_to_h2_biased(w[1][c], h1);
+          crumb16_to_h2<SUBN>(w[0][c], h0);
+          crumb16_to_h2<SUBN>(w[1][c], h1);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int kb = 4 * c + i;
@@ -883,8 +927,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
           }
         } else if constexpr (BITS == 4) {
           uint32_t h0[4], h1[4];
-          nib8_to_h2<NF>(w[0][c], h0, lut);
-          nib8_to_h2<NF>(w[1][c], h1, lut);
+          nib8_to_h2<NF, SUBN>(w[0][c], h0, lut);
+          nib8_to_h2<NF, SUBN>(w[1][c], h1, lut);
           mma16816(acc[0], Aop[2 * c][0], Aop[2 * c][1], Aop[2 * c][2], Aop[2 * c][3], h0[0], h0[1]);
           mma16816(acc[1], Aop[2 * c][0], Aop[2 * c][1], Aop[2 * c][2], Aop[2 * c][3], h1[0], h1[1]);
           mma16816(acc[0], Aop[2 * c + 1][0], Aop[2 * c + 1][1], Aop[2 * c + 1][2],
@@ -902,8 +946,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
         } else {
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const uint32_t h01 = byte2_to_h2_biased<0x4140>(w[u][c]);
-            const uint32_t h23 = byte2_to_h2_biased<0x4342>(w[u][c]);
+            const uint32_t h01 = byte2_to_h2_biased<0x4140, SUBN>(w[u][c]);
+            const uint32_t h23 = byte2_to_h2_biased<0x4342, SUBN>(w[u][c]);
             mma16816(acc[u], Aop[c][0], Aop[c][1], Aop[c][2], Aop[c][3], h01, h23);
             if constexpr (KCH) mma16816(acc[u], Alo[c][0], Alo[c][0], Alo[c][1], Alo[c][1], h01, h23);
           }
@@ -1030,7 +1074,7 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
 #pragma unroll
       for (int t = 0; t < C::NTV; ++t) {
         nb[t][0] = nb[t][1] = nb[t][2] = nb[t][3] = 0.f;
-        if constexpr (!NF && BITS == 4) {
+        if constexpr (!NF && !SUBN && BITS == 4) {
 #pragma unroll
           for (int ks = 0; ks < 2; ++ks)
             mma16816(nb[t], kHm1024, kHm1024, kHm1024, kHm1024, bt[ks][t][0], bt[ks][t][1]);
@@ -1059,12 +1103,14 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
 #pragma unroll
             for (int ks = 0; ks < 2; ++ks) {
               uint32_t lo[8], hi[8];
-              crumb16_to_h2_biased(x[ks][2 * cc], lo);
-              crumb16_to_h2_biased(x[ks][2 * cc + 1], hi);
+              crumb16_to_h2<SUBN>(x[ks][2 * cc], lo);
+              crumb16_to_h2<SUBN>(x[ks][2 * cc + 1], hi);
+              if constexpr (!SUBN) {
 #pragma unroll
-              for (int r = 0; r < 8; ++r) {
-                lo[r] = unbias(lo[r]);
-                hi[r] = unbias(hi[r]);
+                for (int r = 0; r < 8; ++r) {
+                  lo[r] = unbias(lo[r]);
+                  hi[r] = unbias(hi[r]);
+                }
               }
 #pragma unroll
               for (int f = 0; f < 4; ++f)
@@ -1072,7 +1118,7 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
             }
             continue;
           }
-          if constexpr (!NF) {
+          if constexpr (!NF && !SUBN) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               o[2 * chunk][e] += nb[t][e];
@@ -1082,8 +1128,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
 #pragma unroll
           for (int ks = 0; ks < 2; ++ks) {
             uint32_t lo[4], hi[4];
-            nib8_to_h2<NF>(x[ks][2 * cc], lo, lut);
-            nib8_to_h2<NF>(x[ks][2 * cc + 1], hi, lut);
+            nib8_to_h2<NF, SUBN>(x[ks][2 * cc], lo, lut);
+            nib8_to_h2<NF, SUBN>(x[ks][2 * cc + 1], hi, lut);
             // channel of lo[e] = chunk*32 + 4*rho + e; m-tile (chunk, pp) rows: e = 2pp, 2pp+1
             mma16816(o[2 * chunk], lo[0], lo[1], hi[0], hi[1], bt[ks][t][0], bt[ks][t][1]);
             mma16816(o[2 * chunk + 1], lo[2], lo[3], hi[2], hi[3], bt[ks][t][0], bt[ks][t][1]);
@@ -1104,8 +1150,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
             const uint32_t xlo = cc ? xlo1 : xlo0, xhi = cc ? xhi1 : xhi0;
             const int chunk = c + cc;
             const int t = ((chunk * C::DPC) / C::GSZ) * GP / 8;
-            const uint32_t l0 = byte2_to_h2<0x4240>(xlo), l1 = byte2_to_h2<0x4341>(xlo);
-            const uint32_t h0 = byte2_to_h2<0x4240>(xhi), h1 = byte2_to_h2<0x4341>(xhi);
+            const uint32_t l0 = byte2_to_h2<0x4240, SUBN>(xlo), l1 = byte2_to_h2<0x4341, SUBN>(xlo);
+            const uint32_t h0 = byte2_to_h2<0x4240, SUBN>(xhi), h1 = byte2_to_h2<0x4341, SUBN>(xhi);
             mma16816(o[chunk], l0, l1, h0, h1, bt[ks][t][0], bt[ks][t][1]);
           }
         }
@@ -1227,7 +1273,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
 #pragma unroll
   for (int m = 0; m < C::MT; ++m) {
     // rows rho / rho + 8 of m-tile m: channels d0 / d0 + d1, held in units
-    // of 1 / fac (the biased INT4 and INT2 codes' field weights)
+    // of 1 / fac (the INT4 and INT2 codes' field weights) and, for
+    // subnormal codes, of 2^-24
     int d0, d1 = 1;
     float fac = 1.f;
     if constexpr (BITS == 2) {
@@ -1251,14 +1298,11 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
       if (col / GP == g && h < G && warp < kWarps) {
         const float corr = e ? corr1 : corr0;
         float* dst = red + (warp * GP + h) * D;
-        if constexpr (BITS == 2) {
-          dst[d0] = o[m][e] * fac - corr;
-          dst[d0 + d1] = o[m][2 + e] * fac - corr;
-        } else {
-          dst[d0] = o[m][e] - corr;
-          // biased INT4: odd rows in x16 units
-          dst[d0 + 1] = o[m][2 + e] * ((BITS == 4 && !NF) ? 0.0625f : 1.f) - corr;
-        }
+        // INT4 (not NF4): odd rows in x16 units
+        const float fe = (BITS == 2 ? fac : 1.f) * kSub;
+        const float fo = (BITS == 2 ? fac : ((BITS == 4 && !NF) ? 0.0625f : 1.f)) * kSub;
+        dst[d0] = o[m][e] * fe - corr;
+        dst[d0 + d1] = o[m][2 + e] * fo - corr;
       }
     }
   }
