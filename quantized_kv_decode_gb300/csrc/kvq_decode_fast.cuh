@@ -331,12 +331,16 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
   constexpr unsigned short kSymZero =
       NF ? 0u : (BITS == 2 ? 0x4000u : (BITS == 4 ? 0x4800u : 0x5800u));  // fp16 0, 2, 8, 128
   // Per-token integer codes enter the tensor cores as fp16 subnormals (code *
-  // 2^-24, see nib8_to_h2_sub): no offsets to cancel.  kSub restores the
-  // scale: the K scales in the header scratch, the q sums of the zero-point
-  // term and the final rows carry it.  Axis-aware caches keep biased codes.
-  constexpr bool SUBN = !KCH && !NF;
-  constexpr float kSub = SUBN ? 16777216.f : 1.f;  // 2^24
-  const float kscale = p.scale_log2 * kSub;  // K scale factor of the header scratch
+  // 2^-24, see nib8_to_h2_sub): no offsets to cancel.  kSubK / kSubV restore
+  // the scale: the K scales in the header scratch and the q sums of the
+  // zero-point term carry kSubK, the final rows kSubV.  Axis-aware caches
+  // keep biased K codes (their per-channel scales are in the B operand and
+  // the offset in the accumulator's start); their V is per token.
+  constexpr bool SUBK = !KCH && !NF;
+  constexpr bool SUBV = !NF;
+  constexpr float kSubK = SUBK ? 16777216.f : 1.f;  // 2^24
+  constexpr float kSubV = SUBV ? 16777216.f : 1.f;
+  const float kscale = p.scale_log2 * kSubK;  // K scale factor of the header scratch
   // NF4: the 8 level magnitudes as fp16 bytes (see nib8_to_h2_nf4)
   uint32_t lut[4] = {0u, 0u, 0u, 0u};
   if constexpr (NF) {
@@ -518,7 +522,7 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
       const uint32_t ulo = BITS == 2 ? ((kb & 1) ? 0x4C004C00u : kOnes) : kOnes;
       const uint32_t uhi = BITS == 2 ? ((kb & 1) ? 0x54005400u : 0x44004400u) : kHi;
       mma16816(acc, ulo, ulo, uhi, uhi, qa[kb][0], qa[kb][2]);
-      if constexpr (!NF && !SUBN) mma16816(bia, kH1024, kH1024, kH1024, kH1024, qa[kb][0], qa[kb][2]);
+      if constexpr (!NF && !SUBK) mma16816(bia, kH1024, kH1024, kH1024, kH1024, qa[kb][0], qa[kb][2]);
     }
     qs_lo = acc[0];   // column 2j
     qs_hi = acc[1];   // column 2j + 1
@@ -535,7 +539,7 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
       const uint32_t uhi = BITS == 2 ? ((kb & 1) ? 0x54005400u : 0x44004400u)
                                      : ((BITS == 4 && !NF) ? kSixteen : kOnes);
       mma16816(acc, qa[kb][0], qa[kb][1], qa[kb][2], qa[kb][3], ulo, uhi);
-      if constexpr (!NF && !SUBN) mma16816(bia, qa[kb][0], qa[kb][1], qa[kb][2], qa[kb][3], kH1024, kH1024);
+      if constexpr (!NF && !SUBK) mma16816(bia, qa[kb][0], qa[kb][1], qa[kb][2], qa[kb][3], kH1024, kH1024);
     }
     qs_lo = acc[0];
     qs_hi = acc[2];
@@ -544,8 +548,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
   }
   // subnormal codes: the score accumulators carry 2^-24 sum q c, so the
   // zero-point term's q sums do too (the header's K scales carry 2^24)
-  qs_lo *= 1.f / kSub;
-  qs_hi *= 1.f / kSub;
+  qs_lo *= 1.f / kSubK;
+  qs_hi *= 1.f / kSubK;
   const int g_lo_c = min(g_lo, NG - 1), g_hi_c = min(g_hi, NG - 1);
   // After the group sum, lane rho holds the scores of head rho % GP; lanes of
   // a head beyond G read a row of -inf as their token mask.
@@ -809,16 +813,16 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
           if constexpr (BITS == 2) {
             // a chunk of 64 channels: k-blocks 4c .. 4c+3
             uint32_t h0[8], h1[8];
-            crumb16_to_h2<SUBN>(w[0][c], h0);
-            crumb16_to_h2<SUBN>(w[1][c], h1);
+            crumb16_to_h2<SUBK>(w[0][c], h0);
+            crumb16_to_h2<SUBK>(w[1][c], h1);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               mma16816(acc[i & 1], h0[2 * i], h1[2 * i], h0[2 * i + 1], h1[2 * i + 1],
                        qa[4 * c + i][0], qa[4 * c + i][2]);
           } else if constexpr (BITS == 4) {
             uint32_t h0[4], h1[4];
-            nib8_to_h2<NF, SUBN>(w[0][c], h0, lut);
-            nib8_to_h2<NF, SUBN>(w[1][c], h1, lut);
+            nib8_to_h2<NF, SUBK>(w[0][c], h0, lut);
+            nib8_to_h2<NF, SUBK>(w[1][c], h1, lut);
             const uint32_t b00 = KCH ? Bq[2 * c][0] : qa[2 * c][0];
             const uint32_t b01 = KCH ? Bq[2 * c][1] : qa[2 * c][2];
             const uint32_t b10 = KCH ? Bq[2 * c + 1][0] : qa[2 * c + 1][0];
@@ -826,10 +830,10 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
             mma16816(acc[0], h0[0], h1[0], h0[1], h1[1], b00, b01);
             mma16816(acc[1], h0[2], h1[2], h0[3], h1[3], b10, b11);
           } else {
-            const uint32_t a0 = byte2_to_h2_biased<0x4140, SUBN>(w[0][c]);
-            const uint32_t a1 = byte2_to_h2_biased<0x4140, SUBN>(w[1][c]);
-            const uint32_t a2 = byte2_to_h2_biased<0x4342, SUBN>(w[0][c]);
-            const uint32_t a3 = byte2_to_h2_biased<0x4342, SUBN>(w[1][c]);
+            const uint32_t a0 = byte2_to_h2_biased<0x4140, SUBK>(w[0][c]);
+            const uint32_t a1 = byte2_to_h2_biased<0x4140, SUBK>(w[1][c]);
+            const uint32_t a2 = byte2_to_h2_biased<0x4342, SUBK>(w[0][c]);
+            const uint32_t a3 = byte2_to_h2_biased<0x4342, SUBK>(w[1][c]);
             mma16816(acc[c & 1], a0, a1, a2, a3, KCH ? Bq[c][0] : qa[c][0], KCH ? Bq[c][1] : qa[c][2]);
           }
         }
@@ -917,8 +921,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
       for (int c = 0; c < C::CHUNKS; ++c) {
         if constexpr (BITS == 2) {
           uint32_t h0[8], h1[8];
-          crumb16_to_h2<SUBN>(w[0][c], h0);
-          crumb16_to_h2<SUBN>(w[1][c], h1);
+          crumb16_to_h2<SUBK>(w[0][c], h0);
+          crumb16_to_h2<SUBK>(w[1][c], h1);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int kb = 4 * c + i;
@@ -927,8 +931,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
           }
         } else if constexpr (BITS == 4) {
           uint32_t h0[4], h1[4];
-          nib8_to_h2<NF, SUBN>(w[0][c], h0, lut);
-          nib8_to_h2<NF, SUBN>(w[1][c], h1, lut);
+          nib8_to_h2<NF, SUBK>(w[0][c], h0, lut);
+          nib8_to_h2<NF, SUBK>(w[1][c], h1, lut);
           mma16816(acc[0], Aop[2 * c][0], Aop[2 * c][1], Aop[2 * c][2], Aop[2 * c][3], h0[0], h0[1]);
           mma16816(acc[1], Aop[2 * c][0], Aop[2 * c][1], Aop[2 * c][2], Aop[2 * c][3], h1[0], h1[1]);
           mma16816(acc[0], Aop[2 * c + 1][0], Aop[2 * c + 1][1], Aop[2 * c + 1][2],
@@ -946,8 +950,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
         } else {
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
-            const uint32_t h01 = byte2_to_h2_biased<0x4140, SUBN>(w[u][c]);
-            const uint32_t h23 = byte2_to_h2_biased<0x4342, SUBN>(w[u][c]);
+            const uint32_t h01 = byte2_to_h2_biased<0x4140, SUBK>(w[u][c]);
+            const uint32_t h23 = byte2_to_h2_biased<0x4342, SUBK>(w[u][c]);
             mma16816(acc[u], Aop[c][0], Aop[c][1], Aop[c][2], Aop[c][3], h01, h23);
             if constexpr (KCH) mma16816(acc[u], Alo[c][0], Alo[c][0], Alo[c][1], Alo[c][1], h01, h23);
           }
@@ -1074,7 +1078,7 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
 #pragma unroll
       for (int t = 0; t < C::NTV; ++t) {
         nb[t][0] = nb[t][1] = nb[t][2] = nb[t][3] = 0.f;
-        if constexpr (!NF && !SUBN && BITS == 4) {
+        if constexpr (!NF && !SUBV && BITS == 4) {
 #pragma unroll
           for (int ks = 0; ks < 2; ++ks)
             mma16816(nb[t], kHm1024, kHm1024, kHm1024, kHm1024, bt[ks][t][0], bt[ks][t][1]);
@@ -1103,9 +1107,9 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
 #pragma unroll
             for (int ks = 0; ks < 2; ++ks) {
               uint32_t lo[8], hi[8];
-              crumb16_to_h2<SUBN>(x[ks][2 * cc], lo);
-              crumb16_to_h2<SUBN>(x[ks][2 * cc + 1], hi);
-              if constexpr (!SUBN) {
+              crumb16_to_h2<SUBV>(x[ks][2 * cc], lo);
+              crumb16_to_h2<SUBV>(x[ks][2 * cc + 1], hi);
+              if constexpr (!SUBV) {
 #pragma unroll
                 for (int r = 0; r < 8; ++r) {
                   lo[r] = unbias(lo[r]);
@@ -1118,7 +1122,7 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
             }
             continue;
           }
-          if constexpr (!NF && !SUBN) {
+          if constexpr (!NF && !SUBV) {
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               o[2 * chunk][e] += nb[t][e];
@@ -1128,8 +1132,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
 #pragma unroll
           for (int ks = 0; ks < 2; ++ks) {
             uint32_t lo[4], hi[4];
-            nib8_to_h2<NF, SUBN>(x[ks][2 * cc], lo, lut);
-            nib8_to_h2<NF, SUBN>(x[ks][2 * cc + 1], hi, lut);
+            nib8_to_h2<NF, SUBV>(x[ks][2 * cc], lo, lut);
+            nib8_to_h2<NF, SUBV>(x[ks][2 * cc + 1], hi, lut);
             // channel of lo[e] = chunk*32 + 4*rho + e; m-tile (chunk, pp) rows: e = 2pp, 2pp+1
             mma16816(o[2 * chunk], lo[0], lo[1], hi[0], hi[1], bt[ks][t][0], bt[ks][t][1]);
             mma16816(o[2 * chunk + 1], lo[2], lo[3], hi[2], hi[3], bt[ks][t][0], bt[ks][t][1]);
@@ -1150,8 +1154,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
             const uint32_t xlo = cc ? xlo1 : xlo0, xhi = cc ? xhi1 : xhi0;
             const int chunk = c + cc;
             const int t = ((chunk * C::DPC) / C::GSZ) * GP / 8;
-            const uint32_t l0 = byte2_to_h2<0x4240, SUBN>(xlo), l1 = byte2_to_h2<0x4341, SUBN>(xlo);
-            const uint32_t h0 = byte2_to_h2<0x4240, SUBN>(xhi), h1 = byte2_to_h2<0x4341, SUBN>(xhi);
+            const uint32_t l0 = byte2_to_h2<0x4240, SUBV>(xlo), l1 = byte2_to_h2<0x4341, SUBV>(xlo);
+            const uint32_t h0 = byte2_to_h2<0x4240, SUBV>(xhi), h1 = byte2_to_h2<0x4341, SUBV>(xhi);
             mma16816(o[chunk], l0, l1, h0, h1, bt[ks][t][0], bt[ks][t][1]);
           }
         }
@@ -1299,8 +1303,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
         const float corr = e ? corr1 : corr0;
         float* dst = red + (warp * GP + h) * D;
         // INT4 (not NF4): odd rows in x16 units
-        const float fe = (BITS == 2 ? fac : 1.f) * kSub;
-        const float fo = (BITS == 2 ? fac : ((BITS == 4 && !NF) ? 0.0625f : 1.f)) * kSub;
+        const float fe = (BITS == 2 ? fac : 1.f) * kSubV;
+        const float fo = (BITS == 2 ? fac : ((BITS == 4 && !NF) ? 0.0625f : 1.f)) * kSubV;
         dst[d0] = o[m][e] * fe - corr;
         dst[d0 + d1] = o[m][2 + e] * fo - corr;
       }
