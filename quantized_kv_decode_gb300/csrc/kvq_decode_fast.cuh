@@ -1,4 +1,5 @@
-// Tensor-core split-K decode attention over INT4/INT8 caches (sm_103a).
+// Tensor-core split-K decode attention over INT2/INT4/INT8 and NF4 caches
+// (sm_103a).
 //
 // What it computes is the decode step of "Quantization & inference
 // optimisation" ("Prefill, then decode": scores = K q / sqrt(d), softmax,
@@ -14,17 +15,20 @@
 //    conflicts.
 //  * Scores, mma.m16n8k16 (fp16 in, fp32 accumulate): A = q, one row per
 //    (group, head) pair, holding that head's channels of that group only;
-//    B = the codes of 8 tokens as fp16 1024 + c (one LOP3 per code pair; the
-//    1024 offset is removed exactly by starting the accumulator at
-//    -1024 * sum(A row)).  Row (g, h) of the accumulator is
-//    sum_{d in g} q_h[d] c[d]; the epilogue forms s_g (sum - z_g sum_{d in g}
-//    q_h[d]) in fp32 and adds the groups with warp shuffles.
+//    B = the codes of 8 tokens as exact fp16 subnormals c * 2^-24 (one AND
+//    per code pair).  Row (g, h) of the accumulator is 2^-24 sum_{d in g}
+//    q_h[d] c[d]; the epilogue forms s_g (sum - z_g sum_{d in g} q_h[d]) in
+//    fp32, with the 2^24 in its scale, and adds the groups with warp
+//    shuffles.  Token-rows shapes swap the operands (A = codes of 16
+//    tokens, B = q).  Axis-aware caches keep K codes biased, 1024 + c, and
+//    start the accumulator at minus the offset.
 //  * Online softmax per 32-token tile (log2 domain), rescaling only when a
 //    head's tile maximum exceeds its reference maximum by kSlack.
 //  * Weighted V, mma.m16n8k16: A = V codes transposed (ldmatrix.trans puts
-//    two tokens of one channel in each register), B = p * s_g per token and
-//    group (fp16); the zero-points enter through one extra mma per n-tile
-//    whose A rows hold z_g per token, subtracted once at the end.
+//    two tokens of one channel in each register) as subnormals (NF4: their
+//    levels), B = p * s_g per token and group (fp16); the zero-points enter
+//    through one extra mma per n-tile whose A rows hold z_g per token,
+//    subtracted once at the end.
 //  * The warps' (m, l, o) are merged in shared memory; the CTA writes the
 //    final row (one split) or its partial for the merge kernel.
 //  * Fused append (lens_before set): the CTA holding the new position
@@ -176,10 +180,9 @@ __device__ __forceinline__ uint32_t and_or(uint32_t a, uint32_t b, uint32_t c) {
 // Eight 4-bit codes of one 32-bit word (code k in bits 4k..4k+3) to four
 // biased fp16 pairs: (0x6400 | c) is the fp16 value 1024 + c, (0x6400 | 16c)
 // is 1024 + 16c; o[0] = (1024+c0, 1024+c4), o[1] = (1024+16c1, 1024+16c5),
-// o[2] = (1024+c2, 1024+c6), o[3] = (1024+16c3, 1024+16c7).  Both
-// contractions keep the offset: the scores remove it through the
-// accumulator's starting value (the x16 undone by q/16 in the matching
-// slots), the weighted V through a per-tile offset mma and x16 rows.
+// o[2] = (1024+c2, 1024+c6), o[3] = (1024+16c3, 1024+16c7).  The axis-aware
+// caches' K side uses them: the accumulator's starting value removes the
+// offset, and q/16 in the matching slots undoes the x16.
 __device__ __forceinline__ void nib8_to_h2_biased(uint32_t w, uint32_t (&o)[4]) {
   const uint32_t w2 = w >> 8;
   o[0] = and_or(w, 0x000F000Fu, kH1024);
@@ -233,20 +236,10 @@ __device__ __forceinline__ void nib8_to_h2_nf4(uint32_t w, uint32_t (&o)[4],
 }
 
 // Sixteen 2-bit codes (byte m = codes 4m .. 4m+3, code 4m + f in bits 2f of
-// byte m) to fp16 pairs 1024 + 4^f c, f = k & 3, by the same and-or as
-// nib8_to_h2_biased: o[k] = (code at byte k>>2, field f; the same field of
-// byte 2 + (k>>2)).  The factor 4^f is undone on the other operand (score
-// side) or at the end (value side).
-__device__ __forceinline__ void crumb16_to_h2_biased(uint32_t w, uint32_t (&o)[8]) {
-  const uint32_t w2 = w >> 8;
-#pragma unroll
-  for (int f = 0; f < 4; ++f) {
-    o[f] = and_or(w, 0x00030003u << (2 * f), kH1024);
-    o[4 + f] = and_or(w2, 0x00030003u << (2 * f), kH1024);
-  }
-}
-
-// crumb16_to_h2_biased's codes as fp16 subnormals 4^f c * 2^-24.
+// byte m) to fp16 subnormal pairs 4^f c * 2^-24, f = k & 3, one AND each:
+// o[k] = (code at byte k>>2, field f; the same field of byte 2 + (k>>2)).
+// The factor 4^f is undone on the other operand (score side) or at the end
+// (value side).
 __device__ __forceinline__ void crumb16_to_h2_sub(uint32_t w, uint32_t (&o)[8]) {
   const uint32_t w2 = w >> 8;
 #pragma unroll
@@ -256,19 +249,8 @@ __device__ __forceinline__ void crumb16_to_h2_sub(uint32_t w, uint32_t (&o)[8]) 
   }
 }
 
-template <bool SUB>
-__device__ __forceinline__ void crumb16_to_h2(uint32_t w, uint32_t (&o)[8]) {
-  if constexpr (SUB) crumb16_to_h2_sub(w, o);
-  else crumb16_to_h2_biased(w, o);
-}
-
-// A biased fp16 pair 1024 + x back to x (exact for the codes' x < 1024).
-__device__ __forceinline__ uint32_t unbias(uint32_t x) {
-  return h2_as_u32(__hsub2(u32_as_h2(x), u32_as_h2(kH1024)));
-}
-
 // The 4-bit conversion of a kernel instance: NF4 levels, subnormal codes or
-// biased codes.
+// (axis-aware K) biased codes.
 template <bool NF, bool SUB>
 __device__ __forceinline__ void nib8_to_h2(uint32_t w, uint32_t (&o)[4], const uint32_t (&lut)[4]) {
   if constexpr (NF) nib8_to_h2_nf4(w, o, lut);
@@ -283,13 +265,11 @@ __device__ __forceinline__ uint32_t byte2_to_h2_biased(uint32_t w) {
   return __byte_perm(w, SUB ? 0u : 0x64646464u, SEL);
 }
 
-// Four 8-bit codes (byte k = code k) to fp16 pairs per the selectors:
-// sel 0x4140 -> (c0, c1), 0x4342 -> (c2, c3), 0x4240 -> (c0, c2), 0x4341 -> (c1, c3).
-// (SUB: the subnormals c * 2^-24, no subtraction.)
-template <uint32_t SEL, bool SUB = false>
-__device__ __forceinline__ uint32_t byte2_to_h2(uint32_t w) {
-  if constexpr (SUB) return __byte_perm(w, 0u, SEL);
-  else return unbias(__byte_perm(w, 0x64646464u, SEL));
+// Four 8-bit codes (byte k = code k) to fp16 subnormal pairs c * 2^-24 per
+// the selectors: 0x4240 -> (c0, c2), 0x4341 -> (c1, c3) (value side).
+template <uint32_t SEL>
+__device__ __forceinline__ uint32_t byte2_to_h2_sub(uint32_t w) {
+  return __byte_perm(w, 0u, SEL);
 }
 
 // 2^x by the SFU (flush-to-zero; 2^-inf = 0)
@@ -330,16 +310,15 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
   static_assert(!NF || (BITS == 4 && SYM && !KCH), "NF4: 4-bit, scale-only, per-token");
   constexpr unsigned short kSymZero =
       NF ? 0u : (BITS == 2 ? 0x4000u : (BITS == 4 ? 0x4800u : 0x5800u));  // fp16 0, 2, 8, 128
-  // Per-token integer codes enter the tensor cores as fp16 subnormals (code *
-  // 2^-24, see nib8_to_h2_sub): no offsets to cancel.  kSubK / kSubV restore
-  // the scale: the K scales in the header scratch and the q sums of the
+  // Integer codes enter the tensor cores as fp16 subnormals (code * 2^-24,
+  // see nib8_to_h2_sub): no offsets to cancel.  kSubK / kSubV restore the
+  // scale: the K scales in the header scratch and the q sums of the
   // zero-point term carry kSubK, the final rows kSubV.  Axis-aware caches
   // keep biased K codes (their per-channel scales are in the B operand and
   // the offset in the accumulator's start); their V is per token.
   constexpr bool SUBK = !KCH && !NF;
-  constexpr bool SUBV = !NF;
   constexpr float kSubK = SUBK ? 16777216.f : 1.f;  // 2^24
-  constexpr float kSubV = SUBV ? 16777216.f : 1.f;
+  constexpr float kSubV = NF ? 1.f : 16777216.f;
   const float kscale = p.scale_log2 * kSubK;  // K scale factor of the header scratch
   // NF4: the 8 level magnitudes as fp16 bytes (see nib8_to_h2_nf4)
   uint32_t lut[4] = {0u, 0u, 0u, 0u};
@@ -505,15 +484,13 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
     qa[kb][2] = lo ? v23 : 0u;
     qa[kb][3] = hi ? v23 : 0u;
   }
-  // Per row (g, h): the sum of q_h over group g, and the offset that the
-  // biased codes add, 1024 * (sum of the row's A entries); both by the same
+  // Per row (g, h): the sum of q_h over group g (the zero-point term), by an
   // mma against constant codes.
-  float qs_lo = 0.f, qs_hi = 0.f, off_lo = 0.f, off_hi = 0.f;
+  float qs_lo = 0.f, qs_hi = 0.f;
   if constexpr (TQ) {
     // B = q: per column (group) 2j and 2j+1 of this lane, the sum of q over
-    // the group and the biased codes' offset 1024 * (sum of the column)
+    // the group
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    float bia[4] = {0.f, 0.f, 0.f, 0.f};
     constexpr uint32_t kOnes = 0x3C003C00u;
     constexpr uint32_t kHi = (BITS == 4 && !NF) ? 0x4C004C00u : 0x3C003C00u;  // x16 undoes q/16 in odd slots
 #pragma unroll
@@ -522,15 +499,11 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
       const uint32_t ulo = BITS == 2 ? ((kb & 1) ? 0x4C004C00u : kOnes) : kOnes;
       const uint32_t uhi = BITS == 2 ? ((kb & 1) ? 0x54005400u : 0x44004400u) : kHi;
       mma16816(acc, ulo, ulo, uhi, uhi, qa[kb][0], qa[kb][2]);
-      if constexpr (!NF && !SUBK) mma16816(bia, kH1024, kH1024, kH1024, kH1024, qa[kb][0], qa[kb][2]);
     }
     qs_lo = acc[0];   // column 2j
     qs_hi = acc[1];   // column 2j + 1
-    off_lo = bia[0];
-    off_hi = bia[1];
   } else if constexpr (!KCH) {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    float bia[4] = {0.f, 0.f, 0.f, 0.f};
     constexpr uint32_t kOnes = 0x3C003C00u;   // fp16 (1, 1)
     constexpr uint32_t kSixteen = 0x4C004C00u;  // fp16 (16, 16)
 #pragma unroll
@@ -539,12 +512,9 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
       const uint32_t uhi = BITS == 2 ? ((kb & 1) ? 0x54005400u : 0x44004400u)
                                      : ((BITS == 4 && !NF) ? kSixteen : kOnes);
       mma16816(acc, qa[kb][0], qa[kb][1], qa[kb][2], qa[kb][3], ulo, uhi);
-      if constexpr (!NF && !SUBK) mma16816(bia, qa[kb][0], qa[kb][1], qa[kb][2], qa[kb][3], kH1024, kH1024);
     }
     qs_lo = acc[0];
     qs_hi = acc[2];
-    off_lo = bia[0];
-    off_hi = bia[2];
   }
   // subnormal codes: the score accumulators carry 2^-24 sum q c, so the
   // zero-point term's q sums do too (the header's K scales carry 2^24)
@@ -806,15 +776,18 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
         }
         // rows: tokens rho (octet 2np) and rho + 8 (octet 2np + 1); two
         // accumulator chains (even / odd k-blocks)
-        const float c0 = KCH ? kci0 : -off_lo, c1 = KCH ? kci1 : -off_hi;
+        // (axis-aware: the biased codes' offset and the zero-point term).
+        // The others start at -0, which adds like +0; the build with +0
+        // measured 1.5 % slower on the 7B-class step.
+        const float c0 = KCH ? kci0 : -0.f, c1 = KCH ? kci1 : -0.f;
         float acc[2][4] = {{c0, c1, c0, c1}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
         for (int c = 0; c < C::CHUNKS; ++c) {
           if constexpr (BITS == 2) {
             // a chunk of 64 channels: k-blocks 4c .. 4c+3
             uint32_t h0[8], h1[8];
-            crumb16_to_h2<SUBK>(w[0][c], h0);
-            crumb16_to_h2<SUBK>(w[1][c], h1);
+            crumb16_to_h2_sub(w[0][c], h0);
+            crumb16_to_h2_sub(w[1][c], h1);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
               mma16816(acc[i & 1], h0[2 * i], h1[2 * i], h0[2 * i + 1], h1[2 * i + 1],
@@ -910,19 +883,21 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
                     w[u][c4 + 3]);
         }
       }
-      // the accumulators start at minus the offset of the biased codes
+      // axis-aware caches: the accumulators start at minus the biased
+      // codes' offset and the zero-point term; the others at -0 (as in the
+      // token-rows layout)
       float acc[2][4];
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
-        acc[u][0] = acc[u][1] = KCH ? kinit : -off_lo;
-        acc[u][2] = acc[u][3] = KCH ? kinit : -off_hi;
+        acc[u][0] = acc[u][1] = KCH ? kinit : -0.f;
+        acc[u][2] = acc[u][3] = KCH ? kinit : -0.f;
       }
 #pragma unroll
       for (int c = 0; c < C::CHUNKS; ++c) {
         if constexpr (BITS == 2) {
           uint32_t h0[8], h1[8];
-          crumb16_to_h2<SUBK>(w[0][c], h0);
-          crumb16_to_h2<SUBK>(w[1][c], h1);
+          crumb16_to_h2_sub(w[0][c], h0);
+          crumb16_to_h2_sub(w[1][c], h1);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const int kb = 4 * c + i;
@@ -1066,24 +1041,9 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
       }
     }
     if constexpr (BITS <= 4) {
-      // The codes stay biased (1024 + c; odd nibbles 1024 + 16c, whose rows
-      // accumulate in x16 units until the end; INT2: 1024 + 4^f c, rows in
-      // 4^f units).  Per n-tile, -1024 sum_t B
-      // (every row) is the offset they add over this tile; it goes into each
-      // m-tile's accumulator before the tile's mmas, so no accumulator
-      // carries more than one tile's offset.
-      constexpr uint32_t kHm1024 = 0xE400E400u;  // fp16 (-1024, -1024)
-      // (NF4 levels carry no offset.)
-      float nb[C::NTV][4];
-#pragma unroll
-      for (int t = 0; t < C::NTV; ++t) {
-        nb[t][0] = nb[t][1] = nb[t][2] = nb[t][3] = 0.f;
-        if constexpr (!NF && !SUBV && BITS == 4) {
-#pragma unroll
-          for (int ks = 0; ks < 2; ++ks)
-            mma16816(nb[t], kHm1024, kHm1024, kHm1024, kHm1024, bt[ks][t][0], bt[ks][t][1]);
-        }
-      }
+      // The codes are subnormals with no offset (INT4 odd nibbles 16c: their
+      // rows accumulate in x16 units until the end; INT2 4^f c: rows in 4^f
+      // units), or NF4 levels.
 #pragma unroll
       for (int c = 0; c < C::CHUNKS; c += 2) {
         // V codes, transposed: per chunk, lo = tokens 0-7 of the k-step, hi = tokens 8-15
@@ -1100,40 +1060,23 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
           // n-tile of the chunk's group (INT2 chunks of several groups: one n-tile)
           const int t = C::NTV == 1 ? 0 : ((chunk * C::DPC) / C::GSZ) * GP / 8;
           if constexpr (BITS == 2) {
-            // m-tile 4 chunk + f: rows rho / rho + 8 = channels 64 chunk + 8 rho + f / + 4 + f.
-            // The codes lose their bias in fp16 (exact) rather than through
-            // an offset term: for field 0 the 1024 would be ~700x the signal
-            // (codes 0..3), and the accumulator's rounding of it would show.
+            // m-tile 4 chunk + f: rows rho / rho + 8 = channels 64 chunk + 8 rho + f / + 4 + f
 #pragma unroll
             for (int ks = 0; ks < 2; ++ks) {
               uint32_t lo[8], hi[8];
-              crumb16_to_h2<SUBV>(x[ks][2 * cc], lo);
-              crumb16_to_h2<SUBV>(x[ks][2 * cc + 1], hi);
-              if constexpr (!SUBV) {
-#pragma unroll
-                for (int r = 0; r < 8; ++r) {
-                  lo[r] = unbias(lo[r]);
-                  hi[r] = unbias(hi[r]);
-                }
-              }
+              crumb16_to_h2_sub(x[ks][2 * cc], lo);
+              crumb16_to_h2_sub(x[ks][2 * cc + 1], hi);
 #pragma unroll
               for (int f = 0; f < 4; ++f)
                 mma16816(o[4 * chunk + f], lo[f], lo[4 + f], hi[f], hi[4 + f], bt[ks][t][0], bt[ks][t][1]);
             }
             continue;
           }
-          if constexpr (!NF && !SUBV) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              o[2 * chunk][e] += nb[t][e];
-              o[2 * chunk + 1][e] += nb[t][e];
-            }
-          }
 #pragma unroll
           for (int ks = 0; ks < 2; ++ks) {
             uint32_t lo[4], hi[4];
-            nib8_to_h2<NF, SUBV>(x[ks][2 * cc], lo, lut);
-            nib8_to_h2<NF, SUBV>(x[ks][2 * cc + 1], hi, lut);
+            nib8_to_h2<NF, true>(x[ks][2 * cc], lo, lut);
+            nib8_to_h2<NF, true>(x[ks][2 * cc + 1], hi, lut);
             // channel of lo[e] = chunk*32 + 4*rho + e; m-tile (chunk, pp) rows: e = 2pp, 2pp+1
             mma16816(o[2 * chunk], lo[0], lo[1], hi[0], hi[1], bt[ks][t][0], bt[ks][t][1]);
             mma16816(o[2 * chunk + 1], lo[2], lo[3], hi[2], hi[3], bt[ks][t][0], bt[ks][t][1]);
@@ -1154,8 +1097,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
             const uint32_t xlo = cc ? xlo1 : xlo0, xhi = cc ? xhi1 : xhi0;
             const int chunk = c + cc;
             const int t = ((chunk * C::DPC) / C::GSZ) * GP / 8;
-            const uint32_t l0 = byte2_to_h2<0x4240, SUBV>(xlo), l1 = byte2_to_h2<0x4341, SUBV>(xlo);
-            const uint32_t h0 = byte2_to_h2<0x4240, SUBV>(xhi), h1 = byte2_to_h2<0x4341, SUBV>(xhi);
+            const uint32_t l0 = byte2_to_h2_sub<0x4240>(xlo), l1 = byte2_to_h2_sub<0x4341>(xlo);
+            const uint32_t h0 = byte2_to_h2_sub<0x4240>(xhi), h1 = byte2_to_h2_sub<0x4341>(xhi);
             mma16816(o[chunk], l0, l1, h0, h1, bt[ks][t][0], bt[ks][t][1]);
           }
         }
