@@ -1,6 +1,7 @@
 // CUDA-core split-K decode attention for the shapes the tensor-core kernel
-// does not take: fp16 caches, INT2, NF4 codes, head_dim 256, more than 8
-// query heads per KV head, groups of 8/16 channels at INT4.
+// does not take: fp16 caches, head_dim 256, more than 8 query heads per KV
+// head, INT4 / NF4 with groups of 8/16 channels or one group per head, INT2
+// at head_dim 64 or with more (group, head) columns than one V-mma n-tile.
 //
 // What it computes is the decode step of "Quantization & inference
 // optimisation" ("Prefill, then decode": scores = K q / sqrt(d), softmax,
