@@ -274,11 +274,13 @@ kvq_status kvq_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache,
  * Cache contents and status flags are those of kvq_append (num_new = 1)
  * followed by kvq_decode_attn: the codes, scales and zero-points written are
  * bit-identical.  out is the same attention; it can differ from the two-call
- * result in fp32 rounding.  For bits 4 and 8 with at most 8 query heads per
- * KV head this is one kernel launch (plus the merge when split): the thread
- * block that owns the new position quantizes the token, stores it, and adds
- * its dequantized K/V to the attention directly.  Other shapes run the two
- * kernels in sequence.  Lengths are not modified.
+ * result in fp32 rounding.  For per-token caches that the tensor-core kernel
+ * takes (bits 4 and 8 and NF4 at head_dim 64 / 128, bits 2 at head_dim 128,
+ * at most 8 query heads per KV head) this is one kernel launch (plus the
+ * merge when split): the thread block that owns the new position quantizes
+ * the token, stores it, and adds its dequantized K/V to the attention
+ * directly.  Other shapes, and axis-aware caches, run the append kernels and
+ * the decode in sequence.  Lengths are not modified.
  */
 kvq_status kvq_append_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache,
                                   int32_t batch, int32_t num_q_heads,
