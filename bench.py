@@ -331,9 +331,16 @@ def run_gpu_arm(args):
         ws_bytes = K.kvq_decode_workspace_size(desc, w.batch, w.num_q_heads, rows, 0)
         ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=dev)
         status = torch.zeros(1, dtype=torch.int32, device=dev)
-        # per-layer step inputs and outputs as views of buffers contiguous
-        # across layers
-        q_all, k_all, v_all = torch.stack(qs), torch.stack(kns), torch.stack(vns)
+        # per-layer step inputs as views of one buffer (q, then k, then v of
+        # every layer), so that a step's inputs arrive in one copy; outputs
+        # contiguous across layers
+        q_st, k_st, v_st = torch.stack(qs), torch.stack(kns), torch.stack(vns)
+        in_all = torch.cat([q_st.reshape(-1), k_st.reshape(-1), v_st.reshape(-1)])
+        nq, nk = q_st.numel(), k_st.numel()
+        q_all = in_all[:nq].view(q_st.shape)
+        k_all = in_all[nq:nq + nk].view(k_st.shape)
+        v_all = in_all[nq + nk:].view(v_st.shape)
+        del q_st, k_st, v_st
         qs, kns, vns = list(q_all.unbind(0)), list(k_all.unbind(0)), list(v_all.unbind(0))
         o_all = torch.empty_like(q_all)
         outs = list(o_all.unbind(0))
@@ -442,19 +449,15 @@ def run_gpu_arm(args):
             raise RuntimeError(f"device status {int(status.item()):#x}")
 
         # end to end: inputs from pinned host memory, outputs back, per step
-        h_q = q_all.cpu().pin_memory()
-        h_k = k_all.cpu().pin_memory()
-        h_v = v_all.cpu().pin_memory()
+        h_in = in_all.cpu().pin_memory()
         h_o = torch.empty(o_all.shape, dtype=o_all.dtype, pin_memory=True)
-        h2d = sum(t.numel() * t.element_size() for t in (h_q, h_k, h_v))
+        h2d = h_in.numel() * h_in.element_size()
         d2h = h_o.numel() * h_o.element_size()
 
-        # The step's inputs and outputs are contiguous across layers, so a
-        # step moves them with four copies: q, k and v in, out back.
+        # The step's inputs (q, k, v of every layer) share one buffer and its
+        # outputs another, so a step moves them with two copies.
         def e2e_step():
-            q_all.copy_(h_q, non_blocking=True)
-            k_all.copy_(h_k, non_blocking=True)
-            v_all.copy_(h_v, non_blocking=True)
+            in_all.copy_(h_in, non_blocking=True)
             graph.replay()
             h_o.copy_(o_all, non_blocking=True)
 
