@@ -175,3 +175,24 @@ def test_multiwave_ragged_batches(B, Hq, Hkv, D, g, layout, fused):
         run = run_gpu(c, inp, num_splits=s, fused=fused)
         assert run["status"] == 0
         assert_close(run["out"], ref)
+
+
+@pytest.mark.parametrize("bits,g,sym,nf4", [(4, 32, False, False), (8, 32, False, False),
+                                            (2, 32, False, False), (4, 64, True, False),
+                                            (4, 64, False, True)])
+@pytest.mark.parametrize("k_mul,v_mul", [(8.0, 1.0), (0.05, 0.01)])
+def test_magnitudes(bits, g, sym, nf4, k_mul, v_mul):
+    """K and V far from N(0, 1): a sharp softmax (K x 8) and small, flat
+    inputs (K x 0.05, V x 0.01).  The tensor-core kernel carries the codes
+    as fp16 subnormals and the 2^24 in its scales; the outputs must still
+    match the oracle on the same codes within the decode tolerance."""
+    c = Case(B=2, Hq=8, Hkv=8, D=128, bits=bits, g=g, lens=np.array([1500, 333]),
+             seed=5150 + bits + g, symmetric=sym, nf4=nf4)
+    inp = make_inputs(c)
+    for key, mul in (("k_ctx", k_mul), ("k_new", k_mul), ("v_ctx", v_mul), ("v_new", v_mul)):
+        inp[key] = (inp[key].astype(np.float32) * mul).astype(np.float16)
+    for fused in (False, True):
+        run = run_gpu(c, inp, fused=fused)
+        ref, _ = oracle_step(c, inp)
+        assert run["status"] == 0
+        assert_close(run["out"], ref)
