@@ -126,7 +126,7 @@ class ClockSampler:
                 ident = str(self.dev)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", ident, f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -378,8 +378,17 @@ def run_gpu_arm(args):
 
         clocks = ClockSampler(dev.index)
         if key == bits:
+            # the sampler starts under load: untimed replays for --clock-preroll
+            # seconds, then the timed steps, with nvidia-smi sampling throughout
             clocks.start()
-            time.sleep(0.3)
+            t_end = time.time() + args.clock_preroll
+            with torch.cuda.stream(stream):
+                while time.time() < t_end:
+                    for _ in range(8):
+                        graph.replay()
+                    torch.cuda.current_stream().synchronize()
+            torch.cuda.synchronize()
+            barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):
@@ -726,7 +735,10 @@ def load_profiled_traffic():
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--clock-preroll", type=float, default=0.4,
+                    help="seconds of untimed step replays between starting the clock sampler "
+                         "and the timed steps (0 under a profiler)")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="kvq", choices=["kvq", "reference"])
     ap.add_argument("--layers", type=int, default=0)
