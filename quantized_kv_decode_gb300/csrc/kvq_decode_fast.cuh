@@ -194,7 +194,8 @@ __device__ __forceinline__ void nib8_to_h2_biased(uint32_t w, uint32_t (&o)[4]) 
 // The same codes as exact fp16 subnormals: with no exponent bits the half
 // (c) is c * 2^-24 and (16c) is 16c * 2^-24, so the contractions carry no
 // offset; the 2^24 goes into a scale on the other side of each contraction.
-// Tensor cores take fp16 subnormal inputs at full precision.
+// mma.sync takes fp16 subnormal operands without flushing them to zero; every
+// parity test of the tensor-core path depends on that.
 __device__ __forceinline__ void nib8_to_h2_sub(uint32_t w, uint32_t (&o)[4]) {
   const uint32_t w2 = w >> 8;
   o[0] = w & 0x000F000Fu;
@@ -313,10 +314,10 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
   // Integer codes enter the tensor cores as fp16 subnormals (code * 2^-24,
   // see nib8_to_h2_sub): no offsets to cancel.  kSubK / kSubV restore the
   // scale: the K scales in the header scratch and the q sums of the
-  // zero-point term carry kSubK, the final rows kSubV.  Axis-aware caches
-  // keep biased K codes (their per-channel scales are in the B operand and
-  // the offset in the accumulator's start); their V is per token.
-  constexpr bool SUBK = !KCH && !NF;
+  // zero-point term carry kSubK (axis-aware caches: the score epilogue),
+  // the final rows kSubV.  Axis-aware caches in the (group, head)-rows
+  // layout keep biased K codes, whose offset their accumulators start at.
+  constexpr bool SUBK = !NF && (!KCH || GP == 1);
   constexpr float kSubK = SUBK ? 16777216.f : 1.f;  // 2^24
   constexpr float kSubV = NF ? 1.f : 16777216.f;
   const float kscale = p.scale_log2 * kSubK;  // K scale factor of the header scratch
@@ -698,17 +699,18 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
     // A operand: q as built above, or (KCH) q times the block's per-channel
     // scale.  An fp16 product would lose 11 bits on every channel, so KCH
     // carries it as hi + lo (lo = q s - hi by one fused rounding; the pair is
-    // exact to ~22 bits) and runs each score mma for both.  The accumulator
-    // starts at -(1024 sum(A) + sum(A z)), from mmas against B column 0 =
-    // 1024 and column 1 = z.
+    // exact to ~22 bits) and runs each score mma for both.  The zero-point
+    // term -sum(A z) (and for biased codes the offset -1024 sum(A)) comes
+    // from mmas against constant codes: the accumulator's start, or with
+    // subnormal codes an add in the epilogue.
     uint32_t Aop[C::KB][4];
     uint32_t Alo[(KCH && !TQ) ? C::KB : 1][2];
     uint32_t Bq[(KCH && TQ) ? C::KB : 1][2];
     float kinit = 0.f, kci0 = 0.f, kci1 = 0.f;
     if constexpr (KCH && TQ) {
       // token rows: B column 0 = q s (hi), column 1 = its lo part, so one
-      // mma per k-block carries both; the starts -(1024 sum B + sum z B) of
-      // both columns come from mmas with A = 1024 and A = z (every row)
+      // mma per k-block carries both; -sum z B of both columns comes from
+      // mmas with A = z (every row)
       const __half* sz = reinterpret_cast<const __half*>(ksz) + j * C::KB * 4;
       float ci[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -723,7 +725,7 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
         Bq[kb][1] = rho == 0 ? h2_as_u32(h23) : (rho == 1 ? l23 : 0u);
         const uint32_t z23 = BITS == 4 ? h2_as_u32(__hmul2(u32_as_h2(zv.y), u32_as_h2(0x4C004C00u)))
                                        : zv.y;
-        mma16816(ci, kH1024, kH1024, kH1024, kH1024, Bq[kb][0], Bq[kb][1]);
+        if constexpr (!SUBK) mma16816(ci, kH1024, kH1024, kH1024, kH1024, Bq[kb][0], Bq[kb][1]);
         mma16816(ci, zv.x, zv.x, z23, z23, Bq[kb][0], Bq[kb][1]);
       }
       kci0 = -ci[0];  // column 2j
@@ -779,7 +781,7 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
         // (axis-aware: the biased codes' offset and the zero-point term).
         // The others start at -0, which adds like +0; the build with +0
         // measured 1.5 % slower on the 7B-class step.
-        const float c0 = KCH ? kci0 : -0.f, c1 = KCH ? kci1 : -0.f;
+        const float c0 = (KCH && !SUBK) ? kci0 : -0.f, c1 = (KCH && !SUBK) ? kci1 : -0.f;
         float acc[2][4] = {{c0, c1, c0, c1}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
         for (int c = 0; c < C::CHUNKS; ++c) {
@@ -816,9 +818,10 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
           // the groups of the other lanes of this token
           float v = 0.f;
           if constexpr (KCH) {
-            // lane (rho, 0): column 0 (hi) + column 1 (lo); scales already in q
-            v = ((acc[0][2 * i] + acc[1][2 * i]) + (acc[0][2 * i + 1] + acc[1][2 * i + 1])) *
-                p.scale_log2;
+            // lane (rho, 0): column 0 (hi) + column 1 (lo); scales already in
+            // q; subnormal codes: 2^-24 sum B c, and the zero-point term here
+            const float a = (acc[0][2 * i] + acc[1][2 * i]) + (acc[0][2 * i + 1] + acc[1][2 * i + 1]);
+            v = (SUBK ? fmaf(a, kSubK, kci0 + kci1) : a) * p.scale_log2;
           } else if constexpr (GP == 1) {
             if (2 * j < NG) {
               const int t = 16 * np + 8 * i + rho;
