@@ -252,7 +252,6 @@ kvq_status make_plan(const kvq_cache_desc* desc, const CacheGeom& geom, int32_t 
 
 kvq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
 
-
 }  // namespace
 
 size_t workspace_bytes(int64_t batch, int64_t Hq, int64_t D, int64_t splits) {
