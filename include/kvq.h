@@ -63,10 +63,21 @@
  *     per-token groups of g channels as in the default layout;
  *   the newest L - S - floor((L - S) / g) g tokens (fewer than g) form the
  *     fp16 residual window, slot S + (p - S) mod g.
- *   DENSE only; capacity must be a multiple of g and larger than S.
+ *   DENSE: capacity must be a multiple of g and larger than S.
  *          k_codes, v_codes  [batch][num_kv_heads][capacity][row_bytes]
  *          k_scale, k_zero   [batch][num_kv_heads][capacity / g][head_dim]
  *          v_scale, v_zero   [batch][num_kv_heads][capacity][head_dim / g]
+ *          k_window, v_window [batch][num_kv_heads][S + g][head_dim] fp16
+ *   PAGED: only the positions after the sinks are paged, by u = p - S:
+ *     position p >= S lives in page block_table[b][u / capacity] at row
+ *     u mod capacity, and block j's K headers in that page's row
+ *     j mod (capacity / g).  capacity (tokens per page) must be a multiple
+ *     of g, so that no block straddles two pages.  A sequence holds at most
+ *     S + capacity * max_blocks_per_seq positions.  The window stays per
+ *     sequence.
+ *          k_codes, v_codes  [num_pages][num_kv_heads][capacity][row_bytes]
+ *          k_scale, k_zero   [num_pages][num_kv_heads][capacity / g][head_dim]
+ *          v_scale, v_zero   [num_pages][num_kv_heads][capacity][head_dim / g]
  *          k_window, v_window [batch][num_kv_heads][S + g][head_dim] fp16
  */
 #ifndef KVQ_H
@@ -109,7 +120,7 @@ typedef struct {
   int32_t symmetric;          /* 0: asymmetric, fp16 scale + zero per group;
                                  1: symmetric, fp16 scale only, codes offset
                                  by 2^(bits-1); must be 0 when bits == 16     */
-  int32_t k_per_channel;      /* 1: axis-aware cache (DENSE, bits 4/8,
+  int32_t k_per_channel;      /* 1: axis-aware cache (bits 4/8,
                                  asymmetric): K grouped per channel over
                                  group_size consecutive tokens, V per token,
                                  fp16 sinks and residual window (see below)   */

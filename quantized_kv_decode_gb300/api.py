@@ -103,7 +103,8 @@ class KVCache:
         if desc.k_per_channel:
             # K: one scale + zero per channel for each block of g tokens
             g = desc.group_size
-            khdr = lambda: torch.zeros((batch, Hkv, desc.capacity // g, D), dtype=torch.float16,
+            # (paged: per page; the pages hold the tokens after the sinks)
+            khdr = lambda: torch.zeros((lead[0], Hkv, desc.capacity // g, D), dtype=torch.float16,
                                        device=device)
             win = lambda: torch.zeros((batch, Hkv, desc.sink_tokens + g, D), dtype=torch.float16,
                                       device=device)

@@ -38,6 +38,8 @@ kvq_status check_desc(const kvq_cache_desc* d, CacheGeom* g) {
     if (d->layout == KVQ_DENSE &&
         (d->capacity % d->group_size || d->sink_tokens >= d->capacity))
       return KVQ_ERR_INVALID_ARG;
+    // paged: pages of the quantized region hold whole blocks
+    if (d->layout == KVQ_PAGED && d->capacity % d->group_size) return KVQ_ERR_INVALID_ARG;
   } else if (d->sink_tokens != 0) {
     return KVQ_ERR_INVALID_ARG;
   }
@@ -46,7 +48,9 @@ kvq_status check_desc(const kvq_cache_desc* d, CacheGeom* g) {
   } else if (d->layout == KVQ_PAGED) {
     if (d->capacity <= 0 || d->capacity % 8 || d->num_pages <= 0 || d->max_blocks_per_seq <= 0)
       return KVQ_ERR_INVALID_ARG;
-    if ((int64_t)d->capacity * d->max_blocks_per_seq > INT32_MAX) return KVQ_ERR_INVALID_ARG;
+    if ((int64_t)d->capacity * d->max_blocks_per_seq + (d->k_per_channel ? d->sink_tokens : 0) >
+        INT32_MAX)
+      return KVQ_ERR_INVALID_ARG;
   } else {
     return KVQ_ERR_INVALID_ARG;
   }
@@ -69,7 +73,6 @@ kvq_status check_desc(const kvq_cache_desc* d, CacheGeom* g) {
   }
   // the kernels are built for these head sizes; byte accounting takes any
   if (d->head_dim != 64 && d->head_dim != 128 && d->head_dim != 256) return KVQ_ERR_UNSUPPORTED;
-  if (d->k_per_channel && d->layout != KVQ_DENSE) return KVQ_ERR_UNSUPPORTED;
   return KVQ_OK;
 }
 
@@ -186,6 +189,9 @@ const Nf4Table& nf4_table() {
 // head.  The launchers report the shapes they take (`handled`).
 bool fast_format(const kvq_cache_desc* desc, int G) {
   if (G > 8) return false;
+  // paged axis-aware caches: the per-element kernel (the tensor-core
+  // instances address dense axis-aware caches only)
+  if (desc->k_per_channel && desc->layout != KVQ_DENSE) return false;
   if (desc->nf4) return nf4_table().symmetric;
   return desc->bits == 2 || desc->bits == 4 || desc->bits == 8;
 }
@@ -428,8 +434,11 @@ kvq_status decode_impl(const kvq_cache_desc* desc, const kvq_cache* cache, int32
   p.G = G;
   p.splits = splits;
   p.chunk = split_chunk(max_seq_len, splits);
-  const int64_t cap = desc->layout == KVQ_DENSE ? (int64_t)desc->capacity
-                                                 : (int64_t)desc->capacity * desc->max_blocks_per_seq;
+  // (a paged axis-aware cache pages only the tokens after its sinks)
+  const int64_t cap = desc->layout == KVQ_DENSE
+                          ? (int64_t)desc->capacity
+                          : (int64_t)desc->capacity * desc->max_blocks_per_seq +
+                                (desc->k_per_channel ? desc->sink_tokens : 0);
   p.len_limit = (int32_t)std::min<int64_t>(cap, max_seq_len);
   const float scale = softmax_scale > 0.f ? softmax_scale : 1.0f / sqrtf((float)desc->head_dim);
   p.scale_log2 = scale * 1.4426950408889634f;

@@ -45,8 +45,8 @@ __device__ void quantize_block(const AppendParams& p, int b, int kvh, int j, lon
                                int p0) {
   const CacheGeom& c = p.geom;
   const int g = c.g, D = c.D;
-  const long long bh = (long long)b * c.Hkv + kvh;
   uint32_t flags = 0;
+  const long long hrow = kch_hdr(c, b, kvh, j);  // the block's K header row (x D)
 
   // ---- K: one group per channel over the block's g tokens ----
   constexpr int CPU = BITS == 4 ? 2 : 1;  // channels per code byte
@@ -65,9 +65,12 @@ __device__ void quantize_block(const AppendParams& p, int b, int kvh, int j, lon
       }
       gp[e] = group_params<BITS>(mn, mx, finite);
       flags |= gp[e].flags;
-      const long long hi = (bh * (c.slots / g) + j) * D + ch;
-      p.scale[0][hi] = gp[e].s;
-      p.zero[0][hi] = gp[e].z;
+      if (hrow >= 0) {
+        p.scale[0][hrow * D + ch] = gp[e].s;
+        p.zero[0][hrow * D + ch] = gp[e].z;
+      } else {
+        flags |= KVQ_FLAG_BLOCK_TABLE;
+      }
     }
     for (int t = 0; t < g; ++t) {
       const __half* src = token_src(p, 0, b, kvh, (int)start + t, p0);
@@ -75,7 +78,9 @@ __device__ void quantize_block(const AppendParams& p, int b, int kvh, int j, lon
 #pragma unroll
       for (int e = 0; e < CPU; ++e)
         byte |= group_encode<BITS>(__half2float(src[u * CPU + e]), gp[e]) << (4 * e);
-      p.codes[0][(bh * c.slots + start + t) * c.row_bytes + u] = (uint8_t)byte;
+      const long long row = kch_row(c, b, kvh, (int)start + t);
+      if (row >= 0) p.codes[0][row * c.row_bytes + u] = (uint8_t)byte;
+      else flags |= KVQ_FLAG_BLOCK_TABLE;
     }
   }
 
@@ -89,14 +94,19 @@ __device__ void quantize_block(const AppendParams& p, int b, int kvh, int j, lon
     const long long q = start + t;
     const uint4 v = *(reinterpret_cast<const uint4*>(token_src(p, 1, b, kvh, (int)q, p0)) + ch);
     const Quant8 qz = quantize8<BITS>(v, tpg);
-    uint8_t* dst = p.codes[1] + (bh * c.slots + q) * c.row_bytes + ch * BITS;
+    const long long row = kch_row(c, b, kvh, (int)q);
+    if (row < 0) {
+      flags |= KVQ_FLAG_BLOCK_TABLE;
+      continue;
+    }
+    uint8_t* dst = p.codes[1] + row * c.row_bytes + ch * BITS;
     if constexpr (BITS == 4) {
       *reinterpret_cast<uint32_t*>(dst) = qz.w0;
     } else {
       *reinterpret_cast<uint2*>(dst) = make_uint2(qz.w0, qz.w1);
     }
     if (ch % tpg == 0) {
-      const long long hi = (bh * c.slots + q) * c.ngroups + ch / tpg;
+      const long long hi = row * c.ngroups + ch / tpg;
       p.scale[1][hi] = qz.s;
       p.zero[1][hi] = qz.z;
       flags |= qz.flags;
@@ -120,7 +130,7 @@ __global__ void __launch_bounds__(kBlockThreads) kivi_block_kernel(const AppendP
   const long long start = (long long)S + (long long)j * g;
   const long long end = start + g - 1;               // last position of the block
   if (end < p0 || end > (long long)p0 + n - 1) return;  // not completed by this append
-  if (end >= c.slots) {
+  if (end >= kch_capacity(c)) {
     if (threadIdx.x == 0 && p.status) atomicOr(p.status, KVQ_FLAG_SEQ_LEN);
     return;
   }
@@ -138,7 +148,7 @@ __global__ void __launch_bounds__(kBlockThreads) kivi_step_kernel(const AppendPa
   const CacheGeom& c = p.geom;
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int p0 = __ldg(p.seq_lens_before + b);
-  if (p0 < 0 || p0 >= c.slots) {
+  if (p0 < 0 || p0 >= kch_capacity(c)) {
     if (threadIdx.x == 0 && kvh == 0 && p.status) atomicOr(p.status, KVQ_FLAG_SEQ_LEN);
     return;
   }
@@ -175,12 +185,12 @@ __global__ void __launch_bounds__(256) kivi_window_kernel(const AppendParams p) 
   const int b = (int)(r / p.num_new);
   const int p0 = __ldg(p.seq_lens_before + b);
   const long long q = (long long)p0 + t;
-  if (p0 < 0 || q >= c.slots) {
+  if (p0 < 0 || q >= kch_capacity(c)) {
     if (ch == 0 && kvh == 0 && p.status) atomicOr(p.status, KVQ_FLAG_SEQ_LEN);
     return;
   }
   // the cache holds min(p0 + num_new, capacity) tokens after this append
-  const int slot = window_slot(c, (int)min((long long)p0 + p.num_new, (long long)c.slots), (int)q);
+  const int slot = window_slot(c, (int)min((long long)p0 + p.num_new, kch_capacity(c)), (int)q);
   if (slot < 0) return;  // quantized by the block kernel
   const long long bh = (long long)b * c.Hkv + kvh;
   const long long src = (((long long)b * p.num_new + t) * c.Hkv + kvh) * c.D + ch * 8;

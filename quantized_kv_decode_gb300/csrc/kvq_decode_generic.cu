@@ -63,7 +63,7 @@ __device__ __forceinline__ float load_kv(const DecodeParams& p, int which, int b
         const uint8_t* r = p.codes[0] + row * c.row_bytes;
         const float q = BITS == 4 ? (float)((d & 1) ? (r[d >> 1] >> 4) : (r[d >> 1] & 15))
                                   : (float)r[d];
-        const long long h = (bh * (c.slots / c.g) + (pos - c.sink) / c.g) * c.D + d;
+        const long long h = kch_hdr(c, b, kvh, (pos - c.sink) / c.g) * c.D + d;
         return (q - __half2float(p.zero[0][h])) * __half2float(p.scale[0][h]);
       }
     }
@@ -116,7 +116,10 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(const DecodePa
 
     // scores: one warp per token, lanes across channels
     for (int j = warp; j < n; j += kThreads / 32) {
-      const long long row = token_row(c, b, kvh, ts + j);
+      // axis-aware caches: window positions read the fp16 window (any row
+      // >= 0 marks them live); the quantized ones map through kch_row
+      const long long row = !c.kch ? token_row(c, b, kvh, ts + j)
+                            : (window_slot(c, L, ts + j) >= 0 ? 0 : kch_row(c, b, kvh, ts + j));
       float part[kMaxGroupHeads];
 #pragma unroll
       for (int h = 0; h < kMaxGroupHeads; ++h) part[h] = 0.f;

@@ -44,6 +44,41 @@ __device__ __forceinline__ int window_slot(const CacheGeom& c, int L, int p) {
   return p >= r0 ? c.sink + (p - c.sink) % c.g : -1;
 }
 
+// Axis-aware caches.  Dense: a sequence's rows are positions 0 .. slots-1
+// (the sink and window positions unused) and its K block j has header row
+// j.  Paged: only the quantized region is paged, indexed by u = pos - sink;
+// a page holds `slots` rows (a multiple of g, so a block never straddles
+// pages), page i of sequence b is block_table[b][i], and a page's K header
+// rows are its slots / g blocks.
+// Code / V-header row of position pos >= sink (-1: unmapped page).
+__device__ __forceinline__ long long kch_row(const CacheGeom& c, int b, int kvh, int pos) {
+  if (c.layout == KVQ_DENSE) return ((long long)b * c.Hkv + kvh) * c.slots + pos;
+  const int u = pos - c.sink;
+  if (u < 0) return -1;
+  const int blk = u / c.slots;
+  if (blk >= c.max_blocks) return -1;
+  const int page = __ldg(c.block_table + (long long)b * c.max_blocks + blk);
+  if (page < 0 || page >= c.num_pages) return -1;
+  return ((long long)page * c.Hkv + kvh) * c.slots + (u - blk * c.slots);
+}
+
+// K header row of block j >= 0 (times D: the block's per-channel scales and
+// zeros); -1 for an unmapped page.
+__device__ __forceinline__ long long kch_hdr(const CacheGeom& c, int b, int kvh, int j) {
+  const int bpp = c.slots / c.g;  // blocks per sequence (dense) or per page
+  if (c.layout == KVQ_DENSE) return ((long long)b * c.Hkv + kvh) * bpp + j;
+  const int blk = j / bpp;
+  if (blk >= c.max_blocks) return -1;
+  const int page = __ldg(c.block_table + (long long)b * c.max_blocks + blk);
+  if (page < 0 || page >= c.num_pages) return -1;
+  return ((long long)page * c.Hkv + kvh) * bpp + (j - blk * bpp);
+}
+
+// Positions an axis-aware cache can hold per sequence.
+__device__ __forceinline__ long long kch_capacity(const CacheGeom& c) {
+  return c.layout == KVQ_DENSE ? (long long)c.slots : c.sink + (long long)c.slots * c.max_blocks;
+}
+
 // Row index of token `pos` of sequence `b`, KV head `kvh`, into the
 // [..][row_bytes] codes array and the [..][ngroups] header arrays;
 // -1 when the block table maps the token to no valid page.

@@ -172,6 +172,13 @@ def test_axis_aware_descriptor(K):
         codes, hdr = K.kvq_cache_array_bytes(d, 2)
         assert codes == 2 * H * 4 * g * D * bits // 8 and hdr == 2 * H * 4 * g * (D // g) * 2
     assert K.kvq_cache_window_bytes(K.make_desc(4, 32, 8, 128, K.KVQ_DENSE, 64), 3) == 0
+    # paged: pages of the quantized region hold whole blocks; the arrays are
+    # per page (K headers: page_size / g blocks of D channels per page)
+    pd = K.make_desc(4, 32, 8, 128, K.KVQ_PAGED, 64, 10, 4, k_per_channel=True, sink_tokens=4)
+    codes, hdr = K.kvq_cache_array_bytes(pd, 1)
+    assert codes == 10 * 8 * 64 * 64 and hdr == 10 * 8 * (64 // 32) * 128 * 2
+    assert K.kvq_cache_bytes(K.make_desc(4, 32, 8, 128, K.KVQ_PAGED, 48, 10, 4,
+                                         k_per_channel=True), 1) == 0
     bad = [dict(symmetric=True), dict(sink_tokens=-1), dict(sink_tokens=64)]
     for kw in bad:
         d = K.make_desc(4, 32, 8, 128, K.KVQ_DENSE, 64, k_per_channel=True, **kw)

@@ -27,11 +27,20 @@ def _seq_view(K, cache, b):
                      cache.k_window[sl], cache.v_window[sl])
 
 
-def _fill(K, cache, k, v, lens, chunks, st):
+def _paged_view(K, cache, b):
+    """A one-sequence view of a paged cache: the shared page pool, row b of
+    the block table and of the fp16 window."""
+    sl = slice(b, b + 1)
+    return K.KVCache(cache.desc, 1, cache.k_codes, cache.v_codes, cache.k_scale, cache.k_zero,
+                     cache.v_scale, cache.v_zero, cache.block_table[sl], cache.k_window[sl],
+                     cache.v_window[sl])
+
+
+def _fill(K, cache, k, v, lens, chunks, st, view_fn=None):
     """Append sequence b's first lens[b] tokens in pieces of the given sizes."""
     import torch
     for b, L in enumerate(lens):
-        view = _seq_view(K, cache, b)
+        view = (view_fn or _seq_view)(K, cache, b)
         pos, i = 0, 0
         while pos < L:
             n = min(chunks[i % len(chunks)], L - pos)
@@ -158,10 +167,11 @@ def test_kivi_fused_step_and_splits(splits):
 def test_kivi_descriptor_limits():
     import torch
     import quantized_kv_decode_gb300 as K
-    paged = K.make_desc(4, 32, 2, 128, K.KVQ_PAGED, 32, 10, 4, k_per_channel=True)
+    # paged: a page must hold whole blocks
+    paged = K.make_desc(4, 32, 2, 128, K.KVQ_PAGED, 48, 10, 4, k_per_channel=True)
     with pytest.raises(K.KVQError) as e:
         K.kvq_cache_array_bytes(paged, 1)
-    assert e.value.status == K.KVQ_ERR_UNSUPPORTED
+    assert e.value.status == K.KVQ_ERR_INVALID_ARG
     # appending past the capacity flags SEQ_LEN and writes nothing there
     desc = K.make_desc(4, 32, 2, 128, K.KVQ_DENSE, 64, k_per_channel=True, sink_tokens=4)
     cache = K.KVCache.allocate(desc, 1)
@@ -224,3 +234,77 @@ def test_kivi_fullsize_mha7b():
         qh = q[b, kvh * G:(kvh + 1) * G].float().cpu().numpy().astype(np.float64)
         want = O.attend(qh, r["k_hat"][0], r["v_hat"][0], 1.0 / np.sqrt(D))
         assert_close(out[b, kvh * G:(kvh + 1) * G].float().cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("bits,G,g", [(4, 1, 32), (8, 1, 32), (4, 4, 32), (4, 1, 16)])
+def test_kivi_paged_matches_dense(bits, G, g):
+    """Paged axis-aware caches: pages hold the tokens after the sinks, whole
+    blocks per page, scattered by a seeded block table.  Filled by the same
+    appends as a dense cache, the codes and headers agree with the dense
+    cache's (the same appends), the fused step and a decode agree with the
+    dense cache's outputs, and both match the oracle.  Paged axis-aware
+    caches decode on the per-element kernel; the dense ones here run the
+    tensor-core kernel (g = 32) or the same per-element kernel (g = 16)."""
+    import torch
+    import quantized_kv_decode_gb300 as K
+    S, D, Hkv, page = 4, 128, 2, 64
+    Hq = Hkv * G
+    lens = [700, 35, 1300, 4]
+    B, Lmax = len(lens), max(lens)
+    rng = synth.rng_for(77 + bits + G + g)
+    outl = synth.outlier_channels(rng, Hkv, D)
+    k16, v16 = synth.host_kv(rng, B, Lmax + 1, Hkv, D, outl)
+    q16 = synth.host_q(rng, B, Hq, D)
+    need = np.maximum(np.array(lens) + 1 - S, 1)   # quantized-region tokens after the step
+    # rows padded to 4 entries so that one sequence's row (a view) stays
+    # 16-byte aligned, as the ABI asks of every pointer
+    mb = -(-int(max(-(-need // page))) // 4) * 4
+    table, num_pages = synth.block_table(rng, need, page, max_blocks=mb, spare_pages=2)
+    cap = ((Lmax + 1 + g - 1) // g) * g + g
+    dd = K.make_desc(bits, g, Hkv, D, K.KVQ_DENSE, cap, k_per_channel=True, sink_tokens=S)
+    pd = K.make_desc(bits, g, Hkv, D, K.KVQ_PAGED, page, num_pages, table.shape[1],
+                     k_per_channel=True, sink_tokens=S)
+    dense = K.KVCache.allocate(dd, B)
+    paged = K.KVCache.allocate(pd, B, block_table=torch.from_numpy(table))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kt, vt = torch.from_numpy(k16).cuda(), torch.from_numpy(v16).cuda()
+    _fill(K, dense, kt, vt, lens, [37, 1, 64], st)
+    _fill(K, paged, kt, vt, lens, [37, 1, 64], st, view_fn=_paged_view)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    # the quantized rows and K block headers, gathered through the block table
+    arr = {n: (getattr(dense, n).cpu().numpy(), getattr(paged, n).cpu().numpy())
+           for n in ("k_codes", "v_codes", "v_scale", "v_zero", "k_scale", "k_zero", "k_window",
+                     "v_window")}
+    for bi, L in enumerate(lens):
+        nb = max(0, (L - S) // g)
+        u = np.arange(nb * g)
+        pg, off = table[bi, u // page], u % page
+        for n in ("k_codes", "v_codes", "v_scale", "v_zero"):
+            d, pgd = arr[n]
+            assert np.array_equal(d[bi, :, S:S + nb * g], np.transpose(pgd[pg, :, off], (1, 0, 2))), n
+        jb = np.arange(nb)
+        for n in ("k_scale", "k_zero"):
+            d, pgd = arr[n]
+            got = np.transpose(pgd[table[bi, jb * g // page], :, jb % (page // g)], (1, 0, 2))
+            assert np.array_equal(d[bi, :, :nb].view(np.uint16), got.view(np.uint16)), n
+        for n in ("k_window", "v_window"):
+            assert np.array_equal(arr[n][0][bi].view(np.uint16), arr[n][1][bi].view(np.uint16)), n
+    lb = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    kn = torch.stack([kt[b, L] for b, L in enumerate(lens)]).contiguous()   # [B][Hkv][D]
+    vn = torch.stack([vt[b, L] for b, L in enumerate(lens)]).contiguous()
+    q = torch.from_numpy(q16).cuda()
+    outs = []
+    for cache in (dense, paged):
+        o1 = K.kvq_append_decode_attn(cache, kn, vn, q, lb, Lmax + 1, dev_status=st)
+        o2 = K.kvq_decode_attn(cache, q, lb + 1, Lmax + 1, dev_status=st)
+        outs.append((o1, o2))
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    lens1 = [L + 1 for L in lens]
+    want = _oracle_out(q16, k16, v16, lens1, bits, g, S)
+    for (d1, d2), (p1, p2) in [(outs[0], outs[1])]:
+        if g == 16:  # the same kernel on both layouts: bit for bit
+            assert torch.equal(d1, p1) and torch.equal(d2, p2)
+        for o in (d1, d2, p1, p2):
+            assert_close(o.cpu().numpy(), want)
