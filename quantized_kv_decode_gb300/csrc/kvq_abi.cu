@@ -189,9 +189,6 @@ const Nf4Table& nf4_table() {
 // head.  The launchers report the shapes they take (`handled`).
 bool fast_format(const kvq_cache_desc* desc, int G) {
   if (G > 8) return false;
-  // paged axis-aware caches: the per-element kernel (the tensor-core
-  // instances address dense axis-aware caches only)
-  if (desc->k_per_channel && desc->layout != KVQ_DENSE) return false;
   if (desc->nf4) return nf4_table().symmetric;
   return desc->bits == 2 || desc->bits == 4 || desc->bits == 8;
 }

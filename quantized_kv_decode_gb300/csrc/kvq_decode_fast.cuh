@@ -302,13 +302,16 @@ __device__ __forceinline__ uint32_t pack_halves(__half lo, __half hi) {
 // bounded by 2^kSlack.
 constexpr float kSlack = 4.f;
 
-template <int BITS, int D, int NG, int GP, bool SYM, bool KCH, bool NF = false>
+template <int BITS, int D, int NG, int GP, bool SYM, bool KCH, bool NF = false, bool PG = false>
 __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, D, NG, GP, KCH>::MIN_CTAS)
     decode_fast_kernel(const DecodeParams p) {
   // SYM: symmetric caches, no zero arrays; every zero-point is 2^(BITS-1).
   // NF: NF4 codes (with SYM: scale only), which stand for normal-quantile
   // levels; no offset to remove and no zero-point.
   static_assert(!NF || (BITS == 4 && SYM && !KCH), "NF4: 4-bit, scale-only, per-token");
+  // PG: a paged axis-aware cache (kch_row / kch_hdr map its rows; the dense
+  // instances keep their own addressing)
+  static_assert(!PG || KCH, "PG: axis-aware caches");
   constexpr unsigned short kSymZero =
       NF ? 0u : (BITS == 2 ? 0x4000u : (BITS == 4 ? 0x4800u : 0x5800u));  // fp16 0, 2, 8, 128
   // Integer codes enter the tensor cores as fp16 subnormals (code * 2^-24,
@@ -595,7 +598,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
         }
       } else {
         if (lane < n) {
-          row = token_row(geo, b, kvh, start + lane);
+          if constexpr (PG) row = kch_row(geo, b, kvh, start + lane);
+          else row = token_row(geo, b, kvh, start + lane);
           unmapped = row < 0;
         }
 #pragma unroll
@@ -617,11 +621,20 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
       const uint32_t hdst = hd_s + lane * C::HDRB;
       if constexpr (KCH) {
         // the block's K scales then zeros, 8 channels per 16-byte chunk
-        const long long hb = ((((long long)b * geo.Hkv + kvh) * (geo.slots / geo.g)) +
-                              (start - geo.sink) / geo.g) * D;
-        if (lane < D / 4) {
-          const int w = lane / (D / 8), c = lane % (D / 8);
-          cp_async16(hd_s + w * 2 * D + c * 16, (w ? kz_g : ks_g) + (hb + c * 8) * 2, true);
+        if constexpr (PG) {
+          const long long hrow = kch_hdr(geo, b, kvh, (start - geo.sink) / geo.g);
+          const long long hb = hrow >= 0 ? hrow * D : 0;  // unmapped: zero-filled (rows masked)
+          if (lane < D / 4) {
+            const int w = lane / (D / 8), c = lane % (D / 8);
+            cp_async16(hd_s + w * 2 * D + c * 16, (w ? kz_g : ks_g) + (hb + c * 8) * 2, hrow >= 0);
+          }
+        } else {
+          const long long hb = ((((long long)b * geo.Hkv + kvh) * (geo.slots / geo.g)) +
+                                (start - geo.sink) / geo.g) * D;
+          if (lane < D / 4) {
+            const int w = lane / (D / 8), c = lane % (D / 8);
+            cp_async16(hd_s + w * 2 * D + c * 16, (w ? kz_g : ks_g) + (hb + c * 8) * 2, true);
+          }
         }
       } else {
         cp_async_small<C::HDRB>(hdst, ks_g + hoff, ok);
@@ -1418,15 +1431,16 @@ size_t fast_smem_bytes() {
 
 // Launches the instantiation, or with ctas_per_sm != nullptr only reports
 // how many of its CTAs fit on one SM.
-template <int BITS, int D, int NG, int GP, bool SYM, bool KCH = false, bool NF = false>
+template <int BITS, int D, int NG, int GP, bool SYM, bool KCH = false, bool NF = false,
+          bool PG = false>
 cudaError_t launch_fast_inst(const DecodeParams& p, cudaStream_t stream, int* ctas_per_sm) {
   const size_t smem = fast_smem_bytes<BITS, D, NG, GP, KCH>();
-  cudaError_t e = cudaFuncSetAttribute(decode_fast_kernel<BITS, D, NG, GP, SYM, KCH, NF>,
+  cudaError_t e = cudaFuncSetAttribute(decode_fast_kernel<BITS, D, NG, GP, SYM, KCH, NF, PG>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   if (ctas_per_sm) {
     return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        ctas_per_sm, decode_fast_kernel<BITS, D, NG, GP, SYM, KCH, NF>, Cfg<BITS, D, NG, GP, KCH>::THREADS, smem);
+        ctas_per_sm, decode_fast_kernel<BITS, D, NG, GP, SYM, KCH, NF, PG>, Cfg<BITS, D, NG, GP, KCH>::THREADS, smem);
   }
   // programmatic stream serialization: this launch may overlap the tail of the
   // previous kernel in the stream; the kernel waits for it before using any
@@ -1442,7 +1456,7 @@ cudaError_t launch_fast_inst(const DecodeParams& p, cudaStream_t stream, int* ct
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_fast_kernel<BITS, D, NG, GP, SYM, KCH, NF>, p);
+  return cudaLaunchKernelEx(&cfg, decode_fast_kernel<BITS, D, NG, GP, SYM, KCH, NF, PG>, p);
 }
 
 }  // namespace fast

@@ -25,7 +25,9 @@ cudaError_t launch_decode_fast_int8(const DecodeParams& p, int gp, cudaStream_t 
                                     bool* handled, int* occ) {
   *handled = false;
   if (p.geom.sym) return launch_decode_fast_int8_sym(p, gp, s, handled, occ);
-  if (p.geom.kch) return launch_decode_fast_int8_kch(p, gp, s, handled, occ);
+  if (p.geom.kch)
+    return p.geom.layout == KVQ_DENSE ? launch_decode_fast_int8_kch(p, gp, s, handled, occ)
+                                      : launch_decode_fast_int8_kch_paged(p, gp, s, handled, occ);
   const int D = p.geom.D, NG = p.geom.ngroups;
   if (D == 128 && NG == 2) return by_gp8<128, 2>(p, gp, s, handled, occ);
   if (D == 128 && NG == 4) return by_gp8<128, 4>(p, gp, s, handled, occ);

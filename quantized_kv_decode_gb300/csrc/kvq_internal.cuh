@@ -271,8 +271,14 @@ cudaError_t launch_decode_fast_int8_sym(const DecodeParams& p, int gp, cudaStrea
                                         bool* handled, int* occ);
 cudaError_t launch_decode_fast_int4_kch(const DecodeParams& p, int gp, cudaStream_t s,
                                         bool* handled, int* occ);
+// (paged axis-aware caches)
+cudaError_t launch_decode_fast_int4_kch_paged(const DecodeParams& p, int gp, cudaStream_t s,
+                                              bool* handled, int* occ);
 cudaError_t launch_decode_fast_int8_kch(const DecodeParams& p, int gp, cudaStream_t s,
                                         bool* handled, int* occ);
+// (paged axis-aware caches)
+cudaError_t launch_decode_fast_int8_kch_paged(const DecodeParams& p, int gp, cudaStream_t s,
+                                              bool* handled, int* occ);
 cudaError_t launch_decode_fast_int8(const DecodeParams& p, int gp, cudaStream_t s, bool* handled,
                                     int* occ);
 int generic_ctas_per_sm(const DecodeParams& p);

@@ -240,11 +240,11 @@ def test_kivi_fullsize_mha7b():
 def test_kivi_paged_matches_dense(bits, G, g):
     """Paged axis-aware caches: pages hold the tokens after the sinks, whole
     blocks per page, scattered by a seeded block table.  Filled by the same
-    appends as a dense cache, the codes and headers agree with the dense
-    cache's (the same appends), the fused step and a decode agree with the
-    dense cache's outputs, and both match the oracle.  Paged axis-aware
-    caches decode on the per-element kernel; the dense ones here run the
-    tensor-core kernel (g = 32) or the same per-element kernel (g = 16)."""
+    appends as a dense cache, the stored rows, block headers and window
+    agree with the dense cache's, the fused step and a decode give the dense
+    cache's outputs bit for bit (the same arithmetic: the tensor-core kernel's
+    paged instances for g = 32, the per-element kernel for g = 16), and both
+    match the oracle."""
     import torch
     import quantized_kv_decode_gb300 as K
     S, D, Hkv, page = 4, 128, 2, 64
@@ -303,8 +303,7 @@ def test_kivi_paged_matches_dense(bits, G, g):
     assert int(st.item()) == 0
     lens1 = [L + 1 for L in lens]
     want = _oracle_out(q16, k16, v16, lens1, bits, g, S)
-    for (d1, d2), (p1, p2) in [(outs[0], outs[1])]:
-        if g == 16:  # the same kernel on both layouts: bit for bit
-            assert torch.equal(d1, p1) and torch.equal(d2, p2)
-        for o in (d1, d2, p1, p2):
-            assert_close(o.cpu().numpy(), want)
+    (d1, d2), (p1, p2) = outs
+    assert torch.equal(d1, p1) and torch.equal(d2, p2)
+    for o in (d1, d2):
+        assert_close(o.cpu().numpy(), want)
