@@ -318,8 +318,11 @@ kvq_status kvq_append_decode_attn(const kvq_cache_desc* desc, const kvq_cache* c
  *
  *   - Set-up: the first call on each device, with that device current,
  *     looks up the array's device address (cudaGetSymbolAddress) and keeps
- *     it. This may load the library's device code on that device. Make that
- *     first call before any stream capture.
+ *     it with the identifier of the device's current context. This may load
+ *     the library's device code on that device. Make that first call before
+ *     any stream capture. A later call in a different context (after
+ *     cudaDeviceReset, say) looks the address up again, since the array then
+ *     lives elsewhere; make that call before any capture as well.
  *   - Size limit: when kvq_decode_workspace_size() for the same arguments
  *     exceeds KVQ_STATIC_WORKSPACE_BYTES, the call returns KVQ_ERR_WORKSPACE
  *     before any launch. Pass a smaller num_splits, or use kvq_decode_attn.

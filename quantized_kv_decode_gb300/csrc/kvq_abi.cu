@@ -1,14 +1,42 @@
 // Host side of the C ABI declared in include/kvq.h: argument validation,
 // cache geometry, split selection, workspace carving and kernel dispatch.
 // No function here allocates memory or synchronizes a stream.
+#include <cuda.h>  // driver types for the context identifier (no libcuda link)
 #include <math.h>
 #include <string.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "kvq_internal.cuh"
 
 namespace kvq {
+
+unsigned long long current_context_id() {
+  // cuCtxGetCurrent and cuCtxGetId, looked up once through the runtime
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(f);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext c = nullptr;
+  if (get_current(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+  unsigned long long id = 0;
+  if (get_id(c, &id) != CUDA_SUCCESS) return 0;
+  return id + 1;  // 0 stays "unknown"
+}
 
 namespace {
 

@@ -284,12 +284,10 @@ __global__ void __launch_bounds__(kWarps * 32) decode_cc_kernel(const DecodePara
 template <int BITS, int D, int GP>
 cudaError_t launch_cc_inst(const DecodeParams& p, cudaStream_t stream, int* ctas_per_sm) {
   const size_t smem = cc_smem_bytes<BITS, D, GP>();
-  cudaError_t e = cudaFuncSetAttribute(decode_cc_kernel<BITS, D, GP>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  if (ctas_per_sm)
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas_per_sm, decode_cc_kernel<BITS, D, GP>,
-                                                         kWarps * 32, smem);
+  static KernelSetup setup;  // the shared-memory attribute and occupancy, once per device
+  const cudaError_t e = setup_kernel(decode_cc_kernel<BITS, D, GP>, setup, kWarps * 32, smem,
+                                     ctas_per_sm);
+  if (e != cudaSuccess || ctas_per_sm) return e;
   const dim3 grid(p.splits, p.geom.Hkv, p.batch);
   // a plain launch: with programmatic serialization this kernel ran 2-7 %
   // slower (fp16, NF4 and INT2 caches on the 7B-class step)

@@ -1435,13 +1435,10 @@ template <int BITS, int D, int NG, int GP, bool SYM, bool KCH = false, bool NF =
           bool PG = false>
 cudaError_t launch_fast_inst(const DecodeParams& p, cudaStream_t stream, int* ctas_per_sm) {
   const size_t smem = fast_smem_bytes<BITS, D, NG, GP, KCH>();
-  cudaError_t e = cudaFuncSetAttribute(decode_fast_kernel<BITS, D, NG, GP, SYM, KCH, NF, PG>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  if (ctas_per_sm) {
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-        ctas_per_sm, decode_fast_kernel<BITS, D, NG, GP, SYM, KCH, NF, PG>, Cfg<BITS, D, NG, GP, KCH>::THREADS, smem);
-  }
+  static KernelSetup setup;  // the shared-memory attribute and occupancy, once per device
+  const cudaError_t e = setup_kernel(decode_fast_kernel<BITS, D, NG, GP, SYM, KCH, NF, PG>, setup,
+                                     Cfg<BITS, D, NG, GP, KCH>::THREADS, smem, ctas_per_sm);
+  if (e != cudaSuccess || ctas_per_sm) return e;
   // programmatic stream serialization: this launch may overlap the tail of the
   // previous kernel in the stream; the kernel waits for it before using any
   // caller data

@@ -15,7 +15,7 @@
 
 #include <cuda_runtime.h>
 
-#include "../../include/kvq.h"
+#include "kvq_internal.cuh"
 
 namespace {
 
@@ -24,26 +24,33 @@ namespace {
 // call, so nothing here has to start at zero and nothing is cleared.
 __device__ __align__(256) unsigned char g_split_scratch[KVQ_STATIC_WORKSPACE_BYTES];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
+struct ScratchAddress {
+  unsigned long long ctx;  // the context the address belongs to
+  void* ptr;
+};
+ScratchAddress g_scratch[kvq::kMaxDevices] = {};
 
 // Device address of g_split_scratch on the current device. It is looked up
-// once per device, with that device current, on the first call made there;
-// the lookup loads this library's device code on that device if the CUDA
-// runtime has not done so yet.
+// with that device current on the first call made there, which loads this
+// library's device code on that device if the CUDA runtime has not done so
+// yet, and again whenever the device's context has changed since (after a
+// cudaDeviceReset the module, and so the array, lives at a new address).
 kvq_status scratch_on_current_device(void** ptr) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return KVQ_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return KVQ_ERR_UNSUPPORTED;
+  if (dev < 0 || dev >= kvq::kMaxDevices) return KVQ_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_setup_mutex);
-  if (!g_scratch_ptr[dev]) {
+  const unsigned long long ctx = kvq::current_context_id();
+  if (!g_scratch[dev].ptr || ctx == 0 || g_scratch[dev].ctx != ctx) {
     void* p = nullptr;
     const cudaError_t e = cudaGetSymbolAddress(&p, g_split_scratch);
     if (e != cudaSuccess || p == nullptr) return KVQ_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
+    // (the lookup made the context current if it was not yet)
+    g_scratch[dev].ctx = kvq::current_context_id();
+    g_scratch[dev].ptr = p;
   }
-  *ptr = g_scratch_ptr[dev];
+  *ptr = g_scratch[dev].ptr;
   return KVQ_OK;
 }
 

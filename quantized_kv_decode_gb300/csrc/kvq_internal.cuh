@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/kvq.h"
 
 namespace kvq {
@@ -243,6 +245,52 @@ cudaError_t launch_pdl(void (*kernel)(Params), dim3 grid, dim3 block, size_t sme
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+// Devices whose one-time kernel set-up the library caches.
+constexpr int kMaxDevices = 64;
+
+// Identifier of the current thread's CUDA context (the driver never reuses
+// one), or 0 when none is current or it cannot be read.  Set-up that lives in
+// a context (kernel attributes, the address of a module symbol) is cached
+// together with this identifier and redone when it changes, e.g. after
+// cudaDeviceReset.
+unsigned long long current_context_id();
+
+// One-time set-up of a kernel whose dynamic shared memory has a fixed size:
+// the attribute that allows that size and the CTAs per SM it leaves, cached
+// per device (a function-local static per kernel instantiation).
+struct KernelSetup {
+  std::atomic<unsigned long long> ctx[kMaxDevices];
+  std::atomic<int> occ[kMaxDevices];
+};
+
+// Raises the kernel's dynamic shared-memory limit to `smem` and reports its
+// resident CTAs per SM for `threads` threads, once per device and context;
+// later calls read the cache.
+template <typename Kernel>
+cudaError_t setup_kernel(Kernel kernel, KernelSetup& s, int threads, size_t smem,
+                         int* ctas_per_sm) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long ctx = current_context_id();
+  const bool cached = ctx != 0 && dev >= 0 && dev < kMaxDevices;
+  if (cached && s.ctx[dev].load(std::memory_order_acquire) == ctx) {
+    if (ctas_per_sm) *ctas_per_sm = s.occ[dev].load(std::memory_order_relaxed);
+    return cudaSuccess;
+  }
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int n = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem);
+  if (e != cudaSuccess) return e;
+  if (cached) {
+    s.occ[dev].store(n, std::memory_order_relaxed);
+    s.ctx[dev].store(ctx, std::memory_order_release);
+  }
+  if (ctas_per_sm) *ctas_per_sm = n;
+  return cudaSuccess;
 }
 
 // Launchers (return a CUDA error code; the caller maps it to kvq_status).

@@ -61,9 +61,60 @@ def logical_rows(arr_np, c: Case, table, b, kvh, L):
     return arr_np[pages, kvh, pos % c.page_size]
 
 
+class Guarded:
+    """A device tensor housed inside a larger byte buffer whose PAD bytes on
+    either side (and any tail bytes up to the next 16) hold PATTERN, so that a
+    kernel writing outside the tensor is caught by intact()."""
+    PAD = 4096
+    PATTERN = 0xA5
+
+    def __init__(self, shape, dtype, device):
+        import torch
+        n = 1
+        for d in shape:
+            n *= int(d)
+        self.nbytes = n * torch.empty((), dtype=dtype).element_size()
+        span = (self.nbytes + 15) // 16 * 16
+        self.buf = torch.full((2 * self.PAD + span,), self.PATTERN, dtype=torch.uint8,
+                              device=device)
+        self.tensor = self.buf[self.PAD:self.PAD + self.nbytes].view(dtype).view(tuple(shape))
+        self.tensor.zero_()
+
+    def intact(self) -> bool:
+        return bool((self.buf[:self.PAD] == self.PATTERN).all()) and bool(
+            (self.buf[self.PAD + self.nbytes:] == self.PATTERN).all())
+
+
+CACHE_ARRAYS = ("k_codes", "v_codes", "k_scale", "k_zero", "v_scale", "v_zero", "k_window",
+                "v_window")
+
+
+def guarded_cache(cache):
+    """The same cache (descriptor, shapes, zeroed contents, block table) with
+    every array moved into a Guarded buffer; returns (cache, guards)."""
+    import quantized_kv_decode_gb300 as K
+    guards, arrays = {}, {}
+    for name in CACHE_ARRAYS:
+        t = getattr(cache, name)
+        if t is None:
+            arrays[name] = None
+            continue
+        g = Guarded(t.shape, t.dtype, t.device)
+        guards[name] = g
+        arrays[name] = g.tensor
+    return K.KVCache(cache.desc, cache.batch, block_table=cache.block_table, **arrays), guards
+
+
+def check_guards(guards: dict, where: str):
+    bad = [name for name, g in guards.items() if not g.intact()]
+    assert not bad, f"{where}: bytes written outside {bad}"
+
+
 def run_gpu(c: Case, inp, num_splits=0, repeat=1, fused=False):
     """fused: the step's token is appended by kvq_append_decode_attn in the
-    same call as the attention instead of a separate kvq_append."""
+    same call as the attention instead of a separate kvq_append.  Every cache
+    array, the output and the split workspace sit between guard bytes that
+    are checked after each call."""
     import torch
     import quantized_kv_decode_gb300 as K
     dev = "cuda"
@@ -78,25 +129,35 @@ def run_gpu(c: Case, inp, num_splits=0, repeat=1, fused=False):
                            inp["num_pages"], inp["table"].shape[1], symmetric=c.symmetric,
                            nf4=c.nf4)
         cache = K.KVCache.allocate(desc, c.B, dev, torch.from_numpy(inp["table"]))
+    cache, guards = guarded_cache(cache)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     zeros = torch.zeros(c.B, dtype=torch.int32, device=dev)
     K.kvq_append(cache, torch.from_numpy(inp["k_ctx"]).to(dev), torch.from_numpy(inp["v_ctx"]).to(dev),
                  zeros, status)
+    check_guards(guards, "populate")
     lens = torch.from_numpy(c.lens.astype(np.int32)).to(dev)
     k_new = torch.from_numpy(inp["k_new"]).to(dev)
     v_new = torch.from_numpy(inp["v_new"]).to(dev)
     if not fused:
         K.kvq_append(cache, k_new, v_new, lens, status)
+        check_guards(guards, "append")
     q = torch.from_numpy(inp["q"]).to(dev)
+    ws_bytes = K.kvq_decode_workspace_size(desc, c.B, c.Hq, Lctx + 1, num_splits)
+    if ws_bytes:
+        guards["workspace"] = Guarded((ws_bytes,), torch.uint8, dev)
+    ws = guards["workspace"].tensor if ws_bytes else None
     outs = []
     for _ in range(repeat):
+        guards["out"] = Guarded(q.shape, torch.float16, dev)
+        o = guards["out"].tensor
         if fused:
-            o = K.kvq_append_decode_attn(cache, k_new[:, 0].contiguous(), v_new[:, 0].contiguous(),
-                                         q, lens, Lctx + 1, dev_status=status,
-                                         num_splits=num_splits)
+            K.kvq_append_decode_attn(cache, k_new[:, 0].contiguous(), v_new[:, 0].contiguous(),
+                                     q, lens, Lctx + 1, out=o, workspace=ws, dev_status=status,
+                                     num_splits=num_splits)
         else:
-            o = K.kvq_decode_attn(cache, q, lens + 1, Lctx + 1, dev_status=status,
-                                  num_splits=num_splits)
+            K.kvq_decode_attn(cache, q, lens + 1, Lctx + 1, out=o, workspace=ws,
+                              dev_status=status, num_splits=num_splits)
+        check_guards(guards, "fused step" if fused else "decode")
         outs.append(o.cpu().numpy())
     torch.cuda.synchronize()
     return dict(out=outs[0], outs=outs, status=int(status.item()), cache=cache, desc=desc)
@@ -161,3 +222,42 @@ def assert_close(gpu, ref, tol_abs=TOL_MAX_ABS, tol_rel=TOL_REL_L2):
     rel = float(np.linalg.norm(gpu - ref)) / denom if denom > 0 else float(np.linalg.norm(gpu))
     assert max_abs <= tol_abs and rel <= tol_rel, f"max_abs={max_abs:.3e} rel_l2={rel:.3e}"
     return max_abs, rel
+
+
+def _quantize_any(x, bits, g, kind):
+    if kind == "sym":
+        return O.quantize_groups_symmetric(x, bits, g)
+    if kind == "nf4":
+        return O.quantize_groups_nf4(x, g)
+    return O.quantize_groups(x, bits, g)
+
+
+def _dequantize_any(r, g, kind):
+    if kind == "nf4":
+        return O.dequantize_nf4(r["codes"], r["scale"], g)
+    return O.dequantize(r["codes"], r["scale"], r["zero"], g)
+
+
+def check_units(job):
+    """Oracle check of some KV heads of one sequence (a process-pool job).
+
+    job: x_k, x_v fp16 [heads][L][D] (the rows the GPU quantized, the new one
+    last); got: {"k"/"v": (packed codes, scale, zero or None)} read back from
+    the GPU cache for those rows; q [heads][G][D]; out [heads][G][D] the
+    GPU's fp16 output rows; bits, g, kind.  Codes, scales and zeros must be
+    bit-identical to the oracle's; the output within the decode tolerance.
+    Returns (max_abs, rel_l2) per head."""
+    x_k, x_v, got, q, out, bits, g, kind, tag = job
+    hats = []
+    for which, x in (("k", x_k), ("v", x_v)):
+        ref = _quantize_any(x, bits, g, kind)
+        codes, scale, zero = got[which]
+        assert np.array_equal(codes, O.pack_codes(ref["codes"], bits)), (tag, which, "codes")
+        assert np.array_equal(scale.view(np.uint16), ref["scale"].view(np.uint16)), (tag, which)
+        if zero is not None:
+            assert np.array_equal(zero.view(np.uint16), ref["zero"].view(np.uint16)), (tag, which)
+        hats.append(_dequantize_any(ref, g, kind))
+    D = x_k.shape[-1]
+    return [assert_close(out[i], O.attend(q[i].astype(np.float64), hats[0][i], hats[1][i],
+                                          1.0 / np.sqrt(D)))
+            for i in range(x_k.shape[0])]

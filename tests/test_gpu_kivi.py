@@ -236,22 +236,56 @@ def test_kivi_fullsize_mha7b():
         assert_close(out[b, kvh * G:(kvh + 1) * G].float().cpu().numpy(), want)
 
 
-@pytest.mark.parametrize("bits,G,g", [(4, 1, 32), (8, 1, 32), (4, 4, 32), (4, 1, 16)])
-def test_kivi_paged_matches_dense(bits, G, g):
+def _paged_kivi_pair(K, bits, G, g, D, lens, seed):
+    """A dense and a paged axis-aware cache (4 sinks, 2 KV heads, 64-token
+    pages scattered by a seeded block table) filled by the same appends."""
+    import torch
+    S, Hkv, page = 4, 2, 64
+    Hq = Hkv * G
+    B, Lmax = len(lens), max(lens)
+    rng = synth.rng_for(seed)
+    outl = synth.outlier_channels(rng, Hkv, D)
+    k16, v16 = synth.host_kv(rng, B, Lmax + 1, Hkv, D, outl)
+    q16 = synth.host_q(rng, B, Hq, D)
+    need = np.maximum(np.array(lens) + 1 - S, 1)   # quantized-region tokens after the step
+    mb = -(-int(max(-(-need // page))) // 4) * 4
+    table, num_pages = synth.block_table(rng, need, page, max_blocks=mb, spare_pages=2)
+    cap = ((Lmax + 1 + g - 1) // g) * g + g
+    dd = K.make_desc(bits, g, Hkv, D, K.KVQ_DENSE, cap, k_per_channel=True, sink_tokens=S)
+    pd = K.make_desc(bits, g, Hkv, D, K.KVQ_PAGED, page, num_pages, table.shape[1],
+                     k_per_channel=True, sink_tokens=S)
+    dense = K.KVCache.allocate(dd, B)
+    paged = K.KVCache.allocate(pd, B, block_table=torch.from_numpy(table))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kt, vt = torch.from_numpy(k16).cuda(), torch.from_numpy(v16).cuda()
+    _fill(K, dense, kt, vt, lens, [37, 1, 64], st)
+    _fill(K, paged, kt, vt, lens, [37, 1, 64], st, view_fn=_paged_view)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    kn = torch.stack([kt[b, L] for b, L in enumerate(lens)]).contiguous()   # [B][Hkv][D]
+    vn = torch.stack([vt[b, L] for b, L in enumerate(lens)]).contiguous()
+    return dict(dense=dense, paged=paged, table=table, k16=k16, v16=v16, q16=q16, kn=kn, vn=vn,
+                S=S)
+
+
+@pytest.mark.parametrize("bits,G,g,D,splits", [
+    (4, 1, 32, 128, 0), (8, 1, 32, 128, 0), (4, 4, 32, 128, 0), (4, 1, 16, 128, 0),
+    (4, 7, 32, 64, 0), (4, 1, 32, 128, 3), (4, 4, 64, 128, 3)])
+def test_kivi_paged_matches_dense(bits, G, g, D, splits):
     """Paged axis-aware caches: pages hold the tokens after the sinks, whole
     blocks per page, scattered by a seeded block table.  Filled by the same
     appends as a dense cache, the stored rows, block headers and window
     agree with the dense cache's, the fused step and a decode give the dense
     cache's outputs bit for bit (the same arithmetic: the tensor-core kernel's
-    paged instances for g = 32, the per-element kernel for g = 16), and both
-    match the oracle."""
+    paged instances for g = 32 and 64, head_dim 64 and 128, one or several
+    splits; the per-element kernel for g = 16), and both match the oracle."""
     import torch
     import quantized_kv_decode_gb300 as K
-    S, D, Hkv, page = 4, 128, 2, 64
+    S, Hkv, page = 4, 2, 64
     Hq = Hkv * G
     lens = [700, 35, 1300, 4]
     B, Lmax = len(lens), max(lens)
-    rng = synth.rng_for(77 + bits + G + g)
+    rng = synth.rng_for(77 + bits + G + g + D + splits)
     outl = synth.outlier_channels(rng, Hkv, D)
     k16, v16 = synth.host_kv(rng, B, Lmax + 1, Hkv, D, outl)
     q16 = synth.host_q(rng, B, Hq, D)
@@ -296,8 +330,9 @@ def test_kivi_paged_matches_dense(bits, G, g):
     q = torch.from_numpy(q16).cuda()
     outs = []
     for cache in (dense, paged):
-        o1 = K.kvq_append_decode_attn(cache, kn, vn, q, lb, Lmax + 1, dev_status=st)
-        o2 = K.kvq_decode_attn(cache, q, lb + 1, Lmax + 1, dev_status=st)
+        o1 = K.kvq_append_decode_attn(cache, kn, vn, q, lb, Lmax + 1, dev_status=st,
+                                      num_splits=splits)
+        o2 = K.kvq_decode_attn(cache, q, lb + 1, Lmax + 1, dev_status=st, num_splits=splits)
         outs.append((o1, o2))
     torch.cuda.synchronize()
     assert int(st.item()) == 0
@@ -307,3 +342,30 @@ def test_kivi_paged_matches_dense(bits, G, g):
     assert torch.equal(d1, p1) and torch.equal(d2, p2)
     for o in (d1, d2):
         assert_close(o.cpu().numpy(), want)
+
+
+def test_kivi_paged_unmapped_page():
+    """A block-table entry of -1 inside one sequence's quantized region: the
+    decode flags KVQ_FLAG_BLOCK_TABLE and the other sequences' outputs are
+    still the dense cache's, bit for bit (tensor-core paged instance, INT4
+    g32, one and three splits)."""
+    import torch
+    import quantized_kv_decode_gb300 as K
+    lens = [700, 35, 1300, 260]
+    c = _paged_kivi_pair(K, 4, 1, 32, 128, lens, seed=91)
+    dense, paged, table = c["dense"], c["paged"], c["table"].copy()
+    table[2, 5] = -1      # rows 320-383 after the sinks of sequence 2: quantized blocks
+    bad = K.KVCache(paged.desc, paged.batch, paged.k_codes, paged.v_codes, paged.k_scale,
+                    paged.k_zero, paged.v_scale, paged.v_zero,
+                    torch.from_numpy(table).cuda(), paged.k_window, paged.v_window)
+    q = torch.from_numpy(c["q16"]).cuda()
+    lb1 = torch.tensor([L + 1 for L in lens], dtype=torch.int32, device="cuda")
+    for splits in (1, 3):
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        want = K.kvq_decode_attn(dense, q, lb1, max(lens) + 1, dev_status=st, num_splits=splits)
+        got = K.kvq_decode_attn(bad, q, lb1, max(lens) + 1, dev_status=st, num_splits=splits)
+        torch.cuda.synchronize()
+        assert int(st.item()) & K.KVQ_FLAG_BLOCK_TABLE
+        for b in (0, 1, 3):
+            assert torch.equal(got[b], want[b]), b
+        assert not bool(torch.isnan(got).any())

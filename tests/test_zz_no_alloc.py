@@ -5,9 +5,11 @@ workspace.
 It is called straight through the C ABI (ctypes, caller-made buffers only)
 and compared with kvq_decode_attn on the same inputs: two calls in a row
 must each agree within the decode tolerance (max |err| <= 2e-3, relative L2
-<= 1e-3).  The cases force several splits so that the static scratch is
+<= 1e-3), and the second call must leave the device's free memory as the
+first left it.  The cases force several splits so that the static scratch is
 really used.  A request whose workspace would exceed the array is rejected
-before any launch.  The file is named to be collected last and its tests also
+before any launch, and the planner's scratch for every benchmark workload
+fits the array.  The file is named to be collected last and its tests also
 pass alone in a fresh process.
 """
 import os
@@ -57,13 +59,18 @@ def test_static_scratch_matches_workspace_entry_point(case, splits):
     max_len = inp["Lctx"] + 1
     assert K.kvq_decode_workspace_size(cache.desc, case.B, case.Hq, max_len, splits) > 0
     status = torch.zeros(1, dtype=torch.int32, device=dev)
-    for _ in range(2):                                  # two calls in a row
-        out = torch.full_like(q, float("nan"))
+    outs = [torch.full_like(q, float("nan")) for _ in range(2)]
+    free = []
+    for out in outs:                                    # two calls in a row
         st = _call_static(K, cache, q, seq_lens, max_len, out, status, splits)
         assert st == K.KVQ_OK, K.kvq_status_string(st)
         torch.cuda.synchronize()
+        free.append(torch.cuda.mem_get_info()[0])
         assert int(status.item()) == 0
         assert_close(out.cpu().numpy(), ref["out"].astype(np.float64))
+    # after the first call (which may load the library's device code), a call
+    # takes no device memory: the free bytes the driver reports do not move
+    assert free[1] == free[0]
 
 
 def test_static_scratch_rejects_oversized_request():
@@ -90,3 +97,23 @@ def test_static_scratch_rejects_oversized_request():
     assert _call_static(K, cache, q, seq_lens, L, out, status, 0) == K.KVQ_OK
     torch.cuda.synchronize()
     assert not bool(torch.isnan(out).any())
+
+
+def test_static_scratch_covers_the_workloads():
+    """The planner's split scratch for each benchmark workload's full shape
+    (automatic split choice) fits the static array."""
+    import quantized_kv_decode_gb300 as K
+    from quantized_kv_decode_gb300 import synth
+    for name, bits in (("tiny", 4), ("mha7b", 4), ("mha7b", 16), ("gqa_mix", 4), ("long", 4),
+                       ("long", 8), ("paged", 4)):
+        w = synth.WORKLOADS[name]
+        L = w.ctx[1] + 1
+        if w.layout == "paged":
+            pages = -(-L // w.page_size)
+            desc = K.make_desc(bits, w.group_size, w.num_kv_heads, w.head_dim, K.KVQ_PAGED,
+                               w.page_size, pages * w.batch, pages)
+        else:
+            desc = K.make_desc(bits, w.group_size if bits != 16 else 0, w.num_kv_heads,
+                               w.head_dim, K.KVQ_DENSE, (L + 15) // 16 * 16)
+        need = K.kvq_decode_workspace_size(desc, w.batch, w.num_q_heads, L, 0)
+        assert need <= _static_bytes(), (name, bits, need)
