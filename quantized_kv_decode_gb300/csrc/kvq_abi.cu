@@ -480,6 +480,9 @@ kvq_status decode_impl(const kvq_cache_desc* desc, const kvq_cache* cache, int32
     if (fast && pe != cudaSuccess) return KVQ_ERR_CUDA;
     if (!fast) occ = 0;
   }
+  p.rows32 = desc->layout == KVQ_PAGED &&
+             (int64_t)desc->num_pages * desc->num_kv_heads * desc->capacity * p.geom.row_bytes <
+                 ((int64_t)1 << 31);
   p.longest_first = fast_shape && occ > 0 && batch > 1 && batch <= kLongestFirstMaxBatch &&
                     (int64_t)splits * desc->num_kv_heads * batch > (int64_t)sm_count() * occ;
 

@@ -571,6 +571,9 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
   const uint8_t* vz_g = reinterpret_cast<const uint8_t*>(p.zero[1]);
   const bool dense = geo.layout == KVQ_DENSE;
   const long long slab_row = ((long long)b * geo.Hkv + kvh) * geo.slots;  // dense only
+  const long long bt_row = (long long)b * geo.max_blocks;                 // paged only
+  const bool pg_pow2 = (geo.slots & (geo.slots - 1)) == 0;
+  const int pg_shift = __ffs(geo.slots) - 1;
   const uint32_t wpipe_s = smem_u32(wpipe);
 
   // issues tile `it` into its stage; returns true when a page was unmapped
@@ -592,6 +595,29 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
           const int tok = c / C::CHUNKS, part = c % C::CHUNKS;
           const bool ok = tok < n;
           const long long off = ok ? base + tok * C::ROWB + part * 16 : 0;
+          const uint32_t dst = C::at(tok, part);
+          cp_async16(kc_s + dst, kc_g + off, ok);
+          cp_async16(vc_s + dst, vc_g + off, ok);
+        }
+      } else if (!PG && p.rows32) {
+        // rows and byte offsets in 32 bits; pages of a power-of-two size by a
+        // shift
+        int row32 = -1;
+        if (lane < n) {
+          const int pos = start + lane;
+          const int blk = pg_pow2 ? pos >> pg_shift : pos / geo.slots;
+          const int pg = __ldg(geo.block_table + bt_row + blk);
+          if (pg >= 0 && pg < geo.num_pages) row32 = (pg * geo.Hkv + kvh) * geo.slots + (pos - blk * geo.slots);
+          unmapped = row32 < 0;
+        }
+        row = row32;
+#pragma unroll
+        for (int k = 0; k < C::CHUNKS; ++k) {
+          const int c = lane + 32 * k;
+          const int tok = c / C::CHUNKS, part = c % C::CHUNKS;
+          const int r = __shfl_sync(0xffffffffu, row32, tok);
+          const bool ok = r >= 0;
+          const uint32_t off = ok ? (uint32_t)r * C::ROWB + part * 16 : 0u;
           const uint32_t dst = C::at(tok, part);
           cp_async16(kc_s + dst, kc_g + off, ok);
           cp_async16(vc_s + dst, vc_g + off, ok);

@@ -138,6 +138,9 @@ struct DecodeParams {
   // the batch instead of the sequence index (set for grids of more than one
   // wave, so that the longest sequences start first)
   int32_t longest_first;
+  // Paged per-token caches whose code arrays hold fewer than 2^31 bytes: the
+  // tensor-core kernel forms token rows and byte offsets in 32 bits
+  int32_t rows32;
 };
 
 // Tokens to attend over for sequence b (-1 for a length that cannot be formed).
