@@ -290,8 +290,14 @@ kvq_status kvq_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache,
  * at most 8 query heads per KV head) this is one kernel launch (plus the
  * merge when split): the thread block that owns the new position quantizes
  * the token, stores it, and adds its dequantized K/V to the attention
- * directly.  Other shapes, and axis-aware caches, run the append kernels and
- * the decode in sequence.  Lengths are not modified.
+ * directly.  Axis-aware caches of those shapes (group_size a multiple of 32,
+ * bits 4 or 8) are one launch too when the call runs with one split: each
+ * thread block, which owns one (sequence, KV head), first quantizes the
+ * block its token completes (when it completes one) or reads the token from
+ * k_new / v_new where the window would hold it, and stores it to its fp16
+ * slot after attending.  Other shapes, and axis-aware caches split over the
+ * context, run the append kernels and the decode in sequence.  Lengths are
+ * not modified.
  */
 kvq_status kvq_append_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache,
                                   int32_t batch, int32_t num_q_heads,

@@ -513,11 +513,18 @@ kvq_status decode_impl(const kvq_cache_desc* desc, const kvq_cache* cache, int32
     a.num_new = 1;
     return launch_append(a, s);
   };
-  if (fused && desc->k_per_channel) e = append_first();
+  // axis-aware caches: with one split the tensor-core kernel appends in its
+  // own CTAs (each (sequence, KV head) has one); otherwise, and for shapes
+  // it does not take, the append kernel runs first
+  if (fused && desc->k_per_channel) {
+    if (splits == 1 && fast_shape) p.kch_append = 1;
+    else e = append_first();
+  }
   if (e == cudaSuccess && fast_format(desc, G)) {
     e = launch_decode_fast(p, desc->bits, plan.gp, s, &handled, nullptr);
   }
   if (e == cudaSuccess && !handled) {
+    p.kch_append = 0;
     if (fused && !appended) e = append_first();
     if (e == cudaSuccess) e = launch_decode_generic(p, s);
   }

@@ -18,101 +18,26 @@
 //     residual window are written to their fp16 slots.  It runs second
 //     because its slots may be the ones launch 1 reads.
 // A one-token append (the decode step) is one launch, kivi_step_kernel.
-#include "kvq_quant.cuh"
+#include "kvq_kivi.cuh"
 
 namespace kvq {
 namespace {
 
 constexpr int kBlockThreads = 128;
 
-// fp16 source of token q of sequence b, KV head kvh: the residual window for
-// tokens cached before this append, the caller's input otherwise
-__device__ __forceinline__ const __half* token_src(const AppendParams& p, int which, int b, int kvh,
-                                                   int q, int p0) {
-  const CacheGeom& c = p.geom;
-  if (q < p0) {
-    const long long bh = (long long)b * c.Hkv + kvh;
-    return p.window[which] + (bh * (c.sink + c.g) + c.sink + (q - c.sink) % c.g) * c.D;
+__device__ __forceinline__ KiviIO kivi_io(const AppendParams& p) {
+  KiviIO io;
+  io.geom = &p.geom;
+  for (int w = 0; w < 2; ++w) {
+    io.codes[w] = p.codes[w];
+    io.scale[w] = p.scale[w];
+    io.zero[w] = p.zero[w];
+    io.src[w] = p.src[w];
+    io.window[w] = p.window[w];
   }
-  return p.src[which] + (((long long)b * p.num_new + (q - p0)) * c.Hkv + kvh) * c.D;
-}
-
-// Quantizes block j (positions [start, start + g)) of sequence b, KV head
-// kvh, whose tokens before p0 sit in the residual window and the rest in the
-// caller's input.  Every thread of the CTA calls it.
-template <int BITS>
-__device__ void quantize_block(const AppendParams& p, int b, int kvh, int j, long long start,
-                               int p0) {
-  const CacheGeom& c = p.geom;
-  const int g = c.g, D = c.D;
-  uint32_t flags = 0;
-  const long long hrow = kch_hdr(c, b, kvh, j);  // the block's K header row (x D)
-
-  // ---- K: one group per channel over the block's g tokens ----
-  constexpr int CPU = BITS == 4 ? 2 : 1;  // channels per code byte
-  for (int u = threadIdx.x; u < D / CPU; u += blockDim.x) {
-    GroupParams gp[CPU];
-#pragma unroll
-    for (int e = 0; e < CPU; ++e) {
-      const int ch = u * CPU + e;
-      float mn = INFINITY, mx = -INFINITY;
-      bool finite = true;
-      for (int t = 0; t < g; ++t) {
-        const float x = __half2float(token_src(p, 0, b, kvh, (int)start + t, p0)[ch]);
-        finite = finite && isfinite(x);
-        mn = fminf(mn, x);
-        mx = fmaxf(mx, x);
-      }
-      gp[e] = group_params<BITS>(mn, mx, finite);
-      flags |= gp[e].flags;
-      if (hrow >= 0) {
-        p.scale[0][hrow * D + ch] = gp[e].s;
-        p.zero[0][hrow * D + ch] = gp[e].z;
-      } else {
-        flags |= KVQ_FLAG_BLOCK_TABLE;
-      }
-    }
-    for (int t = 0; t < g; ++t) {
-      const __half* src = token_src(p, 0, b, kvh, (int)start + t, p0);
-      uint32_t byte = 0;
-#pragma unroll
-      for (int e = 0; e < CPU; ++e)
-        byte |= group_encode<BITS>(__half2float(src[u * CPU + e]), gp[e]) << (4 * e);
-      const long long row = kch_row(c, b, kvh, (int)start + t);
-      if (row >= 0) p.codes[0][row * c.row_bytes + u] = (uint8_t)byte;
-      else flags |= KVQ_FLAG_BLOCK_TABLE;
-    }
-  }
-
-  // ---- V: per-token groups of g channels (quantize8 over 8-channel chunks) ----
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int chv = D / 8;               // chunks per token
-  const int tpw = 32 / chv;            // tokens per warp pass (D <= 256)
-  const int tpg = g / 8;               // lanes per group
-  for (int t0 = warp * tpw; t0 < g; t0 += (blockDim.x / 32) * tpw) {
-    const int t = t0 + lane / chv, ch = lane % chv;  // every lane is live: g % tpw == 0
-    const long long q = start + t;
-    const uint4 v = *(reinterpret_cast<const uint4*>(token_src(p, 1, b, kvh, (int)q, p0)) + ch);
-    const Quant8 qz = quantize8<BITS>(v, tpg);
-    const long long row = kch_row(c, b, kvh, (int)q);
-    if (row < 0) {
-      flags |= KVQ_FLAG_BLOCK_TABLE;
-      continue;
-    }
-    uint8_t* dst = p.codes[1] + row * c.row_bytes + ch * BITS;
-    if constexpr (BITS == 4) {
-      *reinterpret_cast<uint32_t*>(dst) = qz.w0;
-    } else {
-      *reinterpret_cast<uint2*>(dst) = make_uint2(qz.w0, qz.w1);
-    }
-    if (ch % tpg == 0) {
-      const long long hi = row * c.ngroups + ch / tpg;
-      p.scale[1][hi] = qz.s;
-      p.zero[1][hi] = qz.z;
-      flags |= qz.flags;
-    }
-  }
-  if (flags && p.status) atomicOr(p.status, flags);
+  io.status = p.status;
+  io.num_new = p.num_new;
+  return io;
 }
 
 template <int BITS>
@@ -134,7 +59,7 @@ __global__ void __launch_bounds__(kBlockThreads) kivi_block_kernel(const AppendP
     if (threadIdx.x == 0 && p.status) atomicOr(p.status, KVQ_FLAG_SEQ_LEN);
     return;
   }
-  quantize_block<BITS>(p, b, kvh, j, start, p0);
+  kivi_quantize_block<BITS>(kivi_io(p), b, kvh, j, start, p0);
 }
 
 // One-token append in one launch, one CTA per (KV head, sequence): the token
@@ -145,26 +70,8 @@ template <int BITS>
 __global__ void __launch_bounds__(kBlockThreads) kivi_step_kernel(const AppendParams p) {
   pdl_launch_dependents();
   pdl_wait();
-  const CacheGeom& c = p.geom;
   const int kvh = blockIdx.y, b = blockIdx.z;
-  const int p0 = __ldg(p.seq_lens_before + b);
-  if (p0 < 0 || p0 >= kch_capacity(c)) {
-    if (threadIdx.x == 0 && kvh == 0 && p.status) atomicOr(p.status, KVQ_FLAG_SEQ_LEN);
-    return;
-  }
-  const int slot = window_slot(c, p0 + 1, p0);
-  if (slot < 0) {  // p0 ends its block
-    const int j = (p0 - c.sink) / c.g;
-    quantize_block<BITS>(p, b, kvh, j, (long long)c.sink + (long long)j * c.g, p0);
-    return;
-  }
-  const long long bh = (long long)b * c.Hkv + kvh;
-  const int chunks = c.D / 8;
-  if (threadIdx.x < 2 * chunks) {
-    const int which = threadIdx.x / chunks, ch = threadIdx.x % chunks;
-    *(reinterpret_cast<uint4*>(p.window[which] + (bh * (c.sink + c.g) + slot) * c.D) + ch) =
-        *(reinterpret_cast<const uint4*>(p.src[which] + bh * c.D) + ch);
-  }
+  kivi_append_one<BITS>(kivi_io(p), b, kvh, __ldg(p.seq_lens_before + b));
 }
 
 // Sinks and the residual window left after this append: one thread per

@@ -36,7 +36,7 @@
 //    one more partial; its tiles stop before that position.
 #pragma once
 
-#include "kvq_quant.cuh"
+#include "kvq_kivi.cuh"
 
 namespace kvq {
 namespace fast {
@@ -430,6 +430,36 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
   const __half* qg = p.q + ((long long)b * p.Hq + (long long)kvh * G) * D;
   for (int i = threadIdx.x; i < GP * D; i += blockDim.x)
     q_s[i] = (i < G * D) ? qg[i] : __float2half_rn(0.f);
+  // Fused step on an axis-aware cache, one split: this CTA appends its
+  // unit's new token (position L - 1) with the append kernel's code, so that
+  // it reads the cache as the two-call step leaves it.  A token that
+  // completes its block has the block quantized here, before any tile is
+  // copied (the fence makes the codes visible to the L2-only copies); a token
+  // bound for an fp16 slot (a sink or the residual ring) is read from the
+  // input by the window pass and stored to its slot at the end.
+  int kch_slot = -1;  // the new token's window slot, or -1
+  if constexpr (KCH && BITS != 2) {
+    if (p.kch_append && L > 0) {
+      const int p0 = L - 1;
+      kch_slot = window_slot(geo, L, p0);
+      if (kch_slot < 0) {
+        KiviIO io;
+        io.geom = &geo;
+        for (int w = 0; w < 2; ++w) {
+          io.codes[w] = const_cast<uint8_t*>(p.codes[w]);
+          io.scale[w] = const_cast<__half*>(p.scale[w]);
+          io.zero[w] = const_cast<__half*>(p.zero[w]);
+          io.src[w] = p.new_kv[w];
+          io.window[w] = const_cast<__half*>(p.window[w]);
+        }
+        io.status = p.status;
+        io.num_new = 1;
+        const int j = (p0 - geo.sink) / geo.g;
+        kivi_quantize_block<BITS>(io, b, kvh, j, (long long)geo.sink + (long long)j * geo.g, p0);
+        __threadfence();
+      }
+    }
+  }
 
   __syncthreads();
 
@@ -1112,16 +1142,16 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
               for (int f = 0; f < 4; ++f)
                 mma16816(o[4 * chunk + f], lo[f], lo[4 + f], hi[f], hi[4 + f], bt[ks][t][0], bt[ks][t][1]);
             }
-            continue;
-          }
+          } else {
 #pragma unroll
-          for (int ks = 0; ks < 2; ++ks) {
-            uint32_t lo[4], hi[4];
-            nib8_to_h2<NF, true>(x[ks][2 * cc], lo, lut);
-            nib8_to_h2<NF, true>(x[ks][2 * cc + 1], hi, lut);
-            // channel of lo[e] = chunk*32 + 4*rho + e; m-tile (chunk, pp) rows: e = 2pp, 2pp+1
-            mma16816(o[2 * chunk], lo[0], lo[1], hi[0], hi[1], bt[ks][t][0], bt[ks][t][1]);
-            mma16816(o[2 * chunk + 1], lo[2], lo[3], hi[2], hi[3], bt[ks][t][0], bt[ks][t][1]);
+            for (int ks = 0; ks < 2; ++ks) {
+              uint32_t lo[4], hi[4];
+              nib8_to_h2<NF, true>(x[ks][2 * cc], lo, lut);
+              nib8_to_h2<NF, true>(x[ks][2 * cc + 1], hi, lut);
+              // channel of lo[e] = chunk*32 + 4*rho + e; m-tile (chunk, pp) rows: e = 2pp, 2pp+1
+              mma16816(o[2 * chunk], lo[0], lo[1], hi[0], hi[1], bt[ks][t][0], bt[ks][t][1]);
+              mma16816(o[2 * chunk + 1], lo[2], lo[3], hi[2], hi[3], bt[ks][t][0], bt[ks][t][1]);
+            }
           }
         }
       }
@@ -1328,8 +1358,12 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
         const int i = min(i0 + k * kWarps, nw - 1);  // past the end: a row that exists, unused
         const int pos = i < ns ? t0 + i : rs + (i - ns);
         const int slot = pos < kS ? pos : geo.sink + (pos - geo.sink) % geo.g;
-        const uint32_t* kr = reinterpret_cast<const uint32_t*>(p.window[0] + (wb + slot) * D) + lane * WPR;
-        const uint32_t* vr = reinterpret_cast<const uint32_t*>(p.window[1] + (wb + slot) * D) + lane * WPR;
+        // (the token this launch appends: from the input)
+        const bool fresh = kch_slot >= 0 && pos == L - 1;
+        const __half* kw0 = fresh ? p.new_kv[0] + ((long long)b * geo.Hkv + kvh) * D : p.window[0] + (wb + slot) * D;
+        const __half* vw0 = fresh ? p.new_kv[1] + ((long long)b * geo.Hkv + kvh) * D : p.window[1] + (wb + slot) * D;
+        const uint32_t* kr = reinterpret_cast<const uint32_t*>(kw0) + lane * WPR;
+        const uint32_t* vr = reinterpret_cast<const uint32_t*>(vw0) + lane * WPR;
 #pragma unroll
         for (int c = 0; c < WPR; ++c) {
           kw[k][c] = kr[c];
@@ -1385,6 +1419,12 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
         }
         mh[h] = mx;
       }
+    }
+    if (kch_slot >= 0 && warp == 0 && lane < D / 4) {  // the appended token's fp16 slot
+      const int which = lane / (D / 8), ch = lane % (D / 8);
+      const long long bh = (long long)b * geo.Hkv + kvh;
+      *(reinterpret_cast<uint4*>(const_cast<__half*>(p.window[which]) + (bh * (geo.sink + geo.g) + kch_slot) * D) + ch) =
+          *(reinterpret_cast<const uint4*>(p.new_kv[which] + bh * D) + ch);
     }
 #pragma unroll
     for (int h = 0; h < GP; ++h) {

@@ -141,6 +141,10 @@ struct DecodeParams {
   // Paged per-token caches whose code arrays hold fewer than 2^31 bytes: the
   // tensor-core kernel forms token rows and byte offsets in 32 bits
   int32_t rows32;
+  // Fused step on an axis-aware cache with one split: each CTA of the
+  // tensor-core kernel first appends its (sequence, KV head)'s new token
+  // (window slot, or the block it completes), then attends
+  int32_t kch_append;
 };
 
 // Tokens to attend over for sequence b (-1 for a length that cannot be formed).

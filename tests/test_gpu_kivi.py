@@ -369,3 +369,65 @@ def test_kivi_paged_unmapped_page():
         for b in (0, 1, 3):
             assert torch.equal(got[b], want[b]), b
         assert not bool(torch.isnan(got).any())
+
+
+@pytest.mark.parametrize("bits,g,S,D,Hq,Hkv,layout", [
+    (4, 32, 4, 128, 32, 32, "dense"), (4, 32, 4, 128, 8, 2, "dense"), (8, 32, 0, 128, 4, 4, "dense"),
+    (4, 64, 8, 128, 4, 1, "dense"), (4, 32, 3, 64, 14, 2, "dense"), (4, 32, 4, 128, 4, 4, "paged"),
+    (4, 16, 1, 128, 4, 2, "dense")])
+def test_kivi_one_launch_step_matches_two_calls(bits, g, S, D, Hq, Hkv, layout):
+    """With one split, kvq_append_decode_attn on an axis-aware cache appends
+    inside the decode launch (each (sequence, KV head) CTA writes its token's
+    window slot, or quantizes the block the token completes, before it
+    attends).  The cache it leaves and its output must be bit-identical to
+    kvq_append followed by kvq_decode_attn, for a token landing on a sink, in
+    the residual window, and completing a block (g = 16 runs the append and
+    generic kernels instead)."""
+    import torch
+    import quantized_kv_decode_gb300 as K
+    lens = [max(S - 1, 0), S + g - 1, S + 5, S + 3 * g - 1, 200]   # cached before the step
+    B, Lmax = len(lens), max(lens)
+    rng = synth.rng_for(501 + bits + g + S + D + Hq)
+    outl = synth.outlier_channels(rng, Hkv, D)
+    k16, v16 = synth.host_kv(rng, B, Lmax + 1, Hkv, D, outl)
+    q16 = synth.host_q(rng, B, Hq, D)
+    kt, vt = torch.from_numpy(k16).cuda(), torch.from_numpy(v16).cuda()
+    kn = torch.stack([kt[b, L] for b, L in enumerate(lens)]).contiguous()   # [B][Hkv][D]
+    vn = torch.stack([vt[b, L] for b, L in enumerate(lens)]).contiguous()
+    q = torch.from_numpy(q16).cuda()
+    lb = torch.tensor(lens, dtype=torch.int32, device="cuda")
+
+    def fresh():
+        if layout == "dense":
+            cap = ((Lmax + 1 + g - 1) // g) * g + g
+            desc = K.make_desc(bits, g, Hkv, D, K.KVQ_DENSE, cap, k_per_channel=True, sink_tokens=S)
+            cache = K.KVCache.allocate(desc, B)
+            view = _seq_view
+        else:
+            page = 64
+            need = np.maximum(np.array(lens) + 1 - S, 1)
+            mb = -(-int(max(-(-need // page))) // 4) * 4
+            table, num_pages = synth.block_table(synth.rng_for(9), need, page, max_blocks=mb,
+                                                 spare_pages=2)
+            desc = K.make_desc(bits, g, Hkv, D, K.KVQ_PAGED, page, num_pages, table.shape[1],
+                               k_per_channel=True, sink_tokens=S)
+            cache = K.KVCache.allocate(desc, B, block_table=torch.from_numpy(table))
+            view = _paged_view
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        _fill(K, cache, kt, vt, lens, [29, 1, 64], st, view_fn=view)
+        return cache, st
+
+    two, st2 = fresh()
+    K.kvq_append(two, kn[:, None].contiguous(), vn[:, None].contiguous(), lb, st2)
+    o2 = K.kvq_decode_attn(two, q, lb + 1, Lmax + 1, dev_status=st2, num_splits=1)
+    one, st1 = fresh()
+    o1 = K.kvq_append_decode_attn(one, kn, vn, q, lb, Lmax + 1, dev_status=st1, num_splits=1)
+    torch.cuda.synchronize()
+    assert int(st1.item()) == 0 and int(st2.item()) == 0
+    for name in ("k_codes", "v_codes", "k_scale", "k_zero", "v_scale", "v_zero", "k_window",
+                 "v_window"):
+        a, c = getattr(two, name), getattr(one, name)
+        assert torch.equal(a.view(torch.uint8), c.view(torch.uint8)), name
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    lens1 = [L + 1 for L in lens]
+    assert_close(o1.cpu().numpy(), _oracle_out(q16, k16, v16, lens1, bits, g, S))
