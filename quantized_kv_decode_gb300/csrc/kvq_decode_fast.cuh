@@ -409,6 +409,13 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
   const int t0 = split * p.chunk;
   const int t1 = min(L, t0 + p.chunk);
   if (p.splits > 1 && t0 >= L) return;  // the merge reads splits < ceil(L / chunk) only
+  // Longest-first grids learn their sequence only here: warm the new K/V
+  // rows a fused step's append reads while q is staged.
+  if (!KCH && p.longest_first && p.lens_before != nullptr && L > 0 && L - 1 >= t0 && L - 1 < t1 &&
+      threadIdx.x < 2) {
+    const __half* src = p.new_kv[threadIdx.x] + ((long long)b * geo.Hkv + kvh) * D;
+    if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) prefetch_l2(src, (uint32_t)(D * 2));
+  }
 
   // shared memory: [q fp16 GP x D][per warp: stages, header scratch][tile
   // masks][the appended token's partial: v_hat fp32 [D], scores fp32 [GP]]
@@ -591,8 +598,27 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
   }
   // the appending warp: one with the fewest tiles
   // (the append warp when the CTA has one)
-  const bool owner = owner_cta && warp == (C::AW ? kWarps : ntiles % kWarps);  // warp-uniform
-  const int nmine = (warp < kWarps && ntiles > warp) ? (ntiles - warp + kWarps - 1) / kWarps : 0;
+  const int owner_warp = C::AW ? kWarps : ntiles % kWarps;
+  const bool owner = owner_cta && warp == owner_warp;  // warp-uniform
+  // Tiles go round-robin over the streaming warps.  In a fused step's owner
+  // CTA without an append warp, the owner warp appends before it streams;
+  // the last kSpill tiles (or all, in a short range) then go round-robin
+  // over the other three warps only, so that the owner has about kSpill / 4
+  // fewer tiles to make up for the append's time, about four tiles' worth
+  // (a paged small-model CTA finished about 3 us later than with a
+  // decode-only call).
+  constexpr int kSpill = 12;
+  const int spill = (owner_cta && !C::AW) ? min(kSpill, ntiles) : 0;
+  const int nrr = ntiles - spill;  // tiles [0, nrr) round-robin over all streaming warps
+  int nmine = (warp < kWarps && nrr > warp) ? (nrr - warp + kWarps - 1) / kWarps : 0;
+  const int srank = warp - (warp > owner_warp ? 1 : 0);  // rank among the non-owner warps
+  if (spill && warp < kWarps && warp != owner_warp)
+    nmine += (spill - srank + kWarps - 2) / (kWarps - 1);
+  // the CTA tile this warp takes as its it-th
+  auto tile_of = [&](int it) {
+    const int r = nrr > warp ? (nrr - warp + kWarps - 1) / kWarps : 0;
+    return it < r ? warp + it * kWarps : nrr + srank + (it - r) * (kWarps - 1);
+  };
   const uint8_t* kc_g = p.codes[0];
   const uint8_t* vc_g = p.codes[1];
   const uint8_t* ks_g = reinterpret_cast<const uint8_t*>(p.scale[0]);
@@ -611,7 +637,7 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
     const int stage = it % C::STAGES;
     bool unmapped = false;
     if (it < nmine) {
-      const int start = qbase + (warp + it * kWarps) * kTT;
+      const int start = qbase + tile_of(it) * kTT;
       const int n = KCH ? kTT : min(kTT, t_end - start);
       long long row = -1;  // this lane's token
       const uint32_t kc_s = wpipe_s + stage * C::STAGE, vc_s = kc_s + C::CODE_TILE;
