@@ -650,12 +650,23 @@ def run_gpu_arm(args):
 
         e2e_ms = timed(e2e_eager_step)
         e2e_graph_ms = timed(e2e_step)
+        # host time to issue one call through the C ABI (validation, planning,
+        # launch), the calls enqueued back to back without waiting
+        torch.cuda.synchronize()
+        n_issue = 0
+        h0 = time.perf_counter()
+        for _ in range(max(1, min(args.steps, 10))):
+            for fn, a in eager_calls:
+                fn(*a)
+                n_issue += 1
+        host_us = (time.perf_counter() - h0) / n_issue * 1e6
+        torch.cuda.synchronize()
 
         tokens = w.batch * layers * args.steps  # per rank
         results[key] = dict(
             value=job_throughput(tokens, world, ms_total), ms_per_step=ms_total / args.steps,
             e2e=job_throughput(tokens, world, e2e_ms),
-            e2e_graph=job_throughput(tokens, world, e2e_graph_ms), h2d=h2d, d2h=d2h,
+            e2e_graph=job_throughput(tokens, world, e2e_graph_ms), host_us=host_us, h2d=h2d, d2h=d2h,
             call_ms=call_ms,
             splits=splits,
             bytes=(kivi_decode_bytes(w, fmt, rows, ksink) if ksink is not None else
@@ -700,7 +711,9 @@ def run_gpu_arm(args):
                     "whole model's attention (one token = one sequence through every layer)"},
         "e2e": {"value": r["e2e"], "unit": UNIT, "h2d_bytes_per_step": r["h2d"],
                 "d2h_bytes_per_step": r["d2h"],
-                "what": "eager C-ABI calls per layer, host copies in and out, per step"},
+                "host_us_per_call": r["host_us"],
+                "what": "eager C-ABI calls per layer, host copies in and out, per step; "
+                        "host_us_per_call: host time to issue one call through ctypes"},
         "e2e_graph": {"value": r["e2e_graph"], "unit": UNIT, "h2d_bytes_per_step": r["h2d"],
                       "d2h_bytes_per_step": r["d2h"],
                       "what": "the same with the step's calls replayed from a CUDA graph"},
