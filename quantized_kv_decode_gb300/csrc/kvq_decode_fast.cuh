@@ -340,7 +340,13 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
   // (rows = 16 tokens) and q as B (columns = (group, head) pairs), half the
   // mmas.  The scores are then moved into the lanes the softmax and the V
   // side expect.  Axis-aware caches use it for one query head per KV head.
-  constexpr bool TQ = GP == 1 || (!KCH && GP <= 4 && NG * GP <= 8);
+  // With 16 (group, head) pairs (TQ2: GP = 2 or 4) the columns span two
+  // n-tiles, each k-block's group lying in one of them, so a k-block still
+  // takes one mma per 16 tokens: n-tile 1 holds the pairs of rows 8..15.
+  constexpr bool TQ2 = !KCH && BITS != 2 && (GP == 2 || GP == 4) && NG * GP == 16;
+  constexpr bool TQ = GP == 1 || (!KCH && GP <= 4 && NG * GP <= 8) || TQ2;
+  // the q n-tile of k-block kb's group (TQ2), else 0
+  auto qtile = [](int kb) { return TQ2 ? ((kb * 16) / C::GSZ) / (8 / GP) : 0; };
   extern __shared__ __align__(128) uint8_t smem[];
   const CacheGeom& geo = p.geom;
   const int split = blockIdx.x, kvh = blockIdx.y;
@@ -527,11 +533,11 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
   }
   // Per row (g, h): the sum of q_h over group g (the zero-point term), by an
   // mma against constant codes.
-  float qs_lo = 0.f, qs_hi = 0.f;
+  float qs_lo = 0.f, qs_hi = 0.f, qs_lo1 = 0.f, qs_hi1 = 0.f;  // *1: TQ2's n-tile 1
   if constexpr (TQ) {
     // B = q: per column (group) 2j and 2j+1 of this lane, the sum of q over
     // the group
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc1[4] = {0.f, 0.f, 0.f, 0.f};
     constexpr uint32_t kOnes = 0x3C003C00u;
     constexpr uint32_t kHi = (BITS == 4 && !NF) ? 0x4C004C00u : 0x3C003C00u;  // x16 undoes q/16 in odd slots
 #pragma unroll
@@ -540,9 +546,12 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
       const uint32_t ulo = BITS == 2 ? ((kb & 1) ? 0x4C004C00u : kOnes) : kOnes;
       const uint32_t uhi = BITS == 2 ? ((kb & 1) ? 0x54005400u : 0x44004400u) : kHi;
       mma16816(acc, ulo, ulo, uhi, uhi, qa[kb][0], qa[kb][2]);
+      if constexpr (TQ2) mma16816(acc1, ulo, ulo, uhi, uhi, qa[kb][1], qa[kb][3]);
     }
     qs_lo = acc[0];   // column 2j
     qs_hi = acc[1];   // column 2j + 1
+    qs_lo1 = acc1[0];
+    qs_hi1 = acc1[1];
   } else if constexpr (!KCH) {
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     constexpr uint32_t kOnes = 0x3C003C00u;   // fp16 (1, 1)
@@ -561,6 +570,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
   // zero-point term's q sums do too (the header's K scales carry 2^24)
   qs_lo *= 1.f / kSubK;
   qs_hi *= 1.f / kSubK;
+  qs_lo1 *= 1.f / kSubK;
+  qs_hi1 *= 1.f / kSubK;
   const int g_lo_c = min(g_lo, NG - 1), g_hi_c = min(g_hi, NG - 1);
   // After the group sum, lane rho holds the scores of head rho % GP; lanes of
   // a head beyond G read a row of -inf as their token mask.
@@ -872,7 +883,7 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
           }
         }
         // rows: tokens rho (octet 2np) and rho + 8 (octet 2np + 1); two
-        // accumulator chains (even / odd k-blocks)
+        // accumulator chains (even / odd k-blocks; TQ2: the two n-tiles)
         // (axis-aware: the biased codes' offset and the zero-point term).
         // The others start at -0, which adds like +0; the build with +0
         // measured 1.5 % slower on the 7B-class step.
@@ -893,18 +904,29 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
             uint32_t h0[4], h1[4];
             nib8_to_h2<NF, SUBK>(w[0][c], h0, lut);
             nib8_to_h2<NF, SUBK>(w[1][c], h1, lut);
-            const uint32_t b00 = KCH ? Bq[2 * c][0] : qa[2 * c][0];
-            const uint32_t b01 = KCH ? Bq[2 * c][1] : qa[2 * c][2];
-            const uint32_t b10 = KCH ? Bq[2 * c + 1][0] : qa[2 * c + 1][0];
-            const uint32_t b11 = KCH ? Bq[2 * c + 1][1] : qa[2 * c + 1][2];
-            mma16816(acc[0], h0[0], h1[0], h0[1], h1[1], b00, b01);
-            mma16816(acc[1], h0[2], h1[2], h0[3], h1[3], b10, b11);
+            if constexpr (TQ2) {
+              const int t = qtile(2 * c);  // both k-blocks of the chunk: one group
+              mma16816(acc[t], h0[0], h1[0], h0[1], h1[1], qa[2 * c][t], qa[2 * c][2 + t]);
+              mma16816(acc[t], h0[2], h1[2], h0[3], h1[3], qa[2 * c + 1][t], qa[2 * c + 1][2 + t]);
+            } else {
+              const uint32_t b00 = KCH ? Bq[2 * c][0] : qa[2 * c][0];
+              const uint32_t b01 = KCH ? Bq[2 * c][1] : qa[2 * c][2];
+              const uint32_t b10 = KCH ? Bq[2 * c + 1][0] : qa[2 * c + 1][0];
+              const uint32_t b11 = KCH ? Bq[2 * c + 1][1] : qa[2 * c + 1][2];
+              mma16816(acc[0], h0[0], h1[0], h0[1], h1[1], b00, b01);
+              mma16816(acc[1], h0[2], h1[2], h0[3], h1[3], b10, b11);
+            }
           } else {
             const uint32_t a0 = byte2_to_h2_biased<0x4140, SUBK>(w[0][c]);
             const uint32_t a1 = byte2_to_h2_biased<0x4140, SUBK>(w[1][c]);
             const uint32_t a2 = byte2_to_h2_biased<0x4342, SUBK>(w[0][c]);
             const uint32_t a3 = byte2_to_h2_biased<0x4342, SUBK>(w[1][c]);
-            mma16816(acc[c & 1], a0, a1, a2, a3, KCH ? Bq[c][0] : qa[c][0], KCH ? Bq[c][1] : qa[c][2]);
+            if constexpr (TQ2) {
+              const int t = qtile(c);
+              mma16816(acc[t], a0, a1, a2, a3, qa[c][t], qa[c][2 + t]);
+            } else {
+              mma16816(acc[c & 1], a0, a1, a2, a3, KCH ? Bq[c][0] : qa[c][0], KCH ? Bq[c][1] : qa[c][2]);
+            }
           }
         }
 #pragma unroll
@@ -935,7 +957,17 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
             // heads of another group and keeps the other one; GP = 2 then
             // adds the remaining groups' lanes.
             float v0 = 0.f, v1 = 0.f;
-            if (2 * j < NG * GP) {
+            if constexpr (TQ2) {
+              // n-tile 0 holds this lane's columns for group (2j) / GP,
+              // n-tile 1 for group (2j) / GP + 8 / GP
+              const int t = 16 * np + 8 * i + rho;
+              const float2 sz0 = ksz[t * NG + (2 * j) / GP];
+              const float2 sz1 = ksz[t * NG + (2 * j) / GP + 8 / GP];
+              v0 = fmaf(sz1.x, fmaf(-sz1.y, qs_lo1, acc[1][2 * i]),
+                        sz0.x * fmaf(-sz0.y, qs_lo, acc[0][2 * i]));
+              v1 = fmaf(sz1.x, fmaf(-sz1.y, qs_hi1, acc[1][2 * i + 1]),
+                        sz0.x * fmaf(-sz0.y, qs_hi, acc[0][2 * i + 1]));
+            } else if (2 * j < NG * GP) {
               const int t = 16 * np + 8 * i + rho;
               const float2 sz = ksz[t * NG + (2 * j) / GP];
               v0 = sz.x * fmaf(-sz.y, qs_lo, acc[0][2 * i] + acc[1][2 * i]);

@@ -121,11 +121,17 @@ def test_unmapped_page_flags_block_table():
     (8, 32, 64, 8, 4, False),     # INT8 head_dim 64, 2 heads x 2 groups
     (4, 32, 64, 16, 4, False),    # head_dim 64, 4 heads x 2 groups
     (4, 32, 64, 6, 2, False),     # head_dim 64, 3 heads padded to 4
+    # 16 (group, head) columns over two q n-tiles
+    (4, 32, 128, 16, 4, False),   # 4 heads x 4 groups
+    (4, 32, 128, 12, 4, True),    # 3 heads padded to 4, x 4 groups, symmetric codes
+    (8, 32, 128, 16, 4, False),   # INT8, 4 heads x 4 groups
+    (8, 16, 128, 8, 4, False),    # INT8, 2 heads x 8 groups: three group-sum levels
+    (8, 16, 64, 16, 4, True),     # INT8 head_dim 64, 4 heads x 4 groups, symmetric
 ])
 def test_token_rows_gqa(bits, g, D, Hq, Hkv, sym):
-    """GQA shapes whose (group, head) pairs fit 8 score columns take the
-    token-rows score layout: ragged lengths around the 32-token tile (0, 31,
-    32, 33 cached tokens), several splits, and the fused step."""
+    """GQA shapes whose (group, head) pairs fit 8 or 16 score columns take
+    the token-rows score layout: ragged lengths around the 32-token tile (0,
+    31, 32, 33 cached tokens), several splits, and the fused step."""
     rng = np.random.default_rng(bits * 7 + g + D + Hq)
     lens = np.array([0, 31, 32, 33, int(rng.integers(300, 700))])
     c = Case(B=5, Hq=Hq, Hkv=Hkv, D=D, bits=bits, g=g, lens=lens, seed=int(lens.sum()) % 97,
