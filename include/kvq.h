@@ -103,6 +103,8 @@ typedef enum {
 #define KVQ_FLAG_BLOCK_TABLE  0x2u /* block-table entry outside [0,num_pages)  */
 #define KVQ_FLAG_ZERO_CLAMPED 0x4u /* zero-point outside +-2048, clamped       */
 #define KVQ_FLAG_NONFINITE    0x8u /* group held inf/NaN, stored as zeros      */
+#define KVQ_FLAG_OOB          0x10u /* debug builds: an access outside its array
+                                       was skipped (see kvq_debug_checks)      */
 
 typedef enum { KVQ_DENSE = 0, KVQ_PAGED = 1 } kvq_layout;
 
@@ -347,6 +349,62 @@ kvq_status kvq_decode_attn_static_ws(const kvq_cache_desc* desc, const kvq_cache
                                      int32_t max_seq_len, int32_t num_splits,
                                      float softmax_scale, uint16_t* out,
                                      uint32_t* dev_status, void* stream);
+
+/*
+ * Debug builds.  build(debug=True) in quantized_kv_decode_gb300/build.py
+ * compiles the same sources with KVQ_DEBUG defined into libkvq_debug.so,
+ * which exports the same entry points.  There each launch carries the byte
+ * extent of every caller array it may touch, derived on the host from the
+ * descriptor and the call's sizes:
+ *   cache arrays   kvq_cache_array_bytes(desc, batch) each (DENSE: the
+ *                  call's batch of sequences; PAGED: num_pages), the
+ *                  windows kvq_cache_window_bytes(desc, batch) each;
+ *   block_table    batch * max_blocks_per_seq int32;
+ *   q, out         batch * num_q_heads * head_dim fp16 each;
+ *   k_new, v_new   batch * num_new * num_kv_heads * head_dim fp16 each;
+ *   seq_lens / seq_lens_before   batch int32;
+ *   workspace      workspace_bytes (the static array for the
+ *                  _static_ws call).
+ * Every global load and store of the kernels first checks that its bytes lie
+ * inside the extent of the array it addresses.  An access that does not is
+ * skipped (a load yields zeros), and KVQ_FLAG_OOB is OR-ed into *dev_status
+ * (when dev_status is not NULL).  The checks cost time; results are otherwise
+ * those of the release library, which never sets KVQ_FLAG_OOB.
+ */
+
+/* 1 when the loaded library is a debug build (bounds checks compiled in). */
+int32_t kvq_debug_checks(void);
+
+/* The caller arrays a debug build checks, named for kvq_debug_shrink_extent. */
+typedef enum {
+  KVQ_ARRAY_K_CODES = 0,
+  KVQ_ARRAY_V_CODES = 1,
+  KVQ_ARRAY_K_SCALE = 2,
+  KVQ_ARRAY_K_ZERO = 3,
+  KVQ_ARRAY_V_SCALE = 4,
+  KVQ_ARRAY_V_ZERO = 5,
+  KVQ_ARRAY_K_WINDOW = 6,
+  KVQ_ARRAY_V_WINDOW = 7,
+  KVQ_ARRAY_BLOCK_TABLE = 8,
+  KVQ_ARRAY_Q = 9,
+  KVQ_ARRAY_K_NEW = 10,
+  KVQ_ARRAY_V_NEW = 11,
+  KVQ_ARRAY_SEQ_LENS = 12,   /* seq_lens or seq_lens_before */
+  KVQ_ARRAY_OUT = 13,
+  KVQ_ARRAY_WORKSPACE = 14,
+  KVQ_ARRAY_COUNT = 15
+} kvq_array;
+
+/*
+ * Tests the checks themselves (debug builds only; a release build returns
+ * KVQ_ERR_UNSUPPORTED).  Every later launch checks array `array` (a
+ * kvq_array) against an extent `bytes` shorter than the one the host derives
+ * (bytes = 0 restores it).  Accesses to the array's last `bytes` bytes are
+ * then skipped and flagged although they lie inside the caller's allocation.
+ * Process-wide host state; not safe to call while another thread launches.
+ * Returns KVQ_ERR_INVALID_ARG for an unknown array or bytes < 0.
+ */
+kvq_status kvq_debug_shrink_extent(int32_t array, int64_t bytes);
 
 /* Static, human-readable name of a status code. */
 const char* kvq_status_string(kvq_status status);

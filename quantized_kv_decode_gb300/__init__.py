@@ -5,7 +5,7 @@ this package is its thin Python binding plus a seeded synthetic-input module.
 Build the library with ``python -m quantized_kv_decode_gb300.build``.
 """
 from ._lib import (KVQ_DENSE, KVQ_ERR_CUDA, KVQ_ERR_INVALID_ARG, KVQ_ERR_UNSUPPORTED,  # noqa: F401
-                   KVQ_ERR_WORKSPACE, KVQ_FLAG_BLOCK_TABLE, KVQ_FLAG_NONFINITE,
+                   KVQ_ERR_WORKSPACE, KVQ_FLAG_BLOCK_TABLE, KVQ_FLAG_NONFINITE, KVQ_FLAG_OOB,
                    KVQ_FLAG_SEQ_LEN, KVQ_FLAG_ZERO_CLAMPED, KVQ_OK, KVQ_PAGED, KVQError,
                    kvq_cache, kvq_cache_desc, lib)
 

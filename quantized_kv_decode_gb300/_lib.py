@@ -25,6 +25,13 @@ KVQ_FLAG_SEQ_LEN = 0x1
 KVQ_FLAG_BLOCK_TABLE = 0x2
 KVQ_FLAG_ZERO_CLAMPED = 0x4
 KVQ_FLAG_NONFINITE = 0x8
+KVQ_FLAG_OOB = 0x10  # debug builds only: an access outside its array was skipped
+
+# kvq_array: the caller arrays a debug build checks
+(KVQ_ARRAY_K_CODES, KVQ_ARRAY_V_CODES, KVQ_ARRAY_K_SCALE, KVQ_ARRAY_K_ZERO, KVQ_ARRAY_V_SCALE,
+ KVQ_ARRAY_V_ZERO, KVQ_ARRAY_K_WINDOW, KVQ_ARRAY_V_WINDOW, KVQ_ARRAY_BLOCK_TABLE, KVQ_ARRAY_Q,
+ KVQ_ARRAY_K_NEW, KVQ_ARRAY_V_NEW, KVQ_ARRAY_SEQ_LENS, KVQ_ARRAY_OUT,
+ KVQ_ARRAY_WORKSPACE) = range(15)
 
 KVQ_DENSE = 0
 KVQ_PAGED = 1
@@ -91,25 +98,40 @@ SIGNATURES = {
     "kvq_decode_attn_static_ws": (c_int32, [POINTER(kvq_cache_desc), POINTER(kvq_cache), c_int32,
                                             c_int32, c_void_p, c_void_p, c_int32, c_int32,
                                             c_float, c_void_p, c_void_p, c_void_p]),
+    "kvq_debug_checks": (c_int32, []),
+    "kvq_debug_shrink_extent": (c_int32, [c_int32, c_int64]),
     "kvq_status_string": (ctypes.c_char_p, [c_int32]),
 }
+
+
+def load(path: str) -> ctypes.CDLL:
+    """A handle on the library at `path` with the C signatures attached."""
+    if not os.path.exists(path):
+        raise RuntimeError(
+            f"{os.path.basename(path)} is not built; run `python -m quantized_kv_decode_gb300.build` "
+            "(the library has no fallback path)")
+    handle = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(handle, name)
+        fn.restype = res
+        fn.argtypes = args
+    return handle
 
 
 def lib() -> ctypes.CDLL:
     """Load libkvq.so (once).  Raises if it has not been built."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(
-                "libkvq.so is not built; run `python -m quantized_kv_decode_gb300.build` "
-                "(the library has no fallback path)")
-        handle = ctypes.CDLL(LIB_PATH)
-        for name, (res, args) in SIGNATURES.items():
-            fn = getattr(handle, name)
-            fn.restype = res
-            fn.argtypes = args
-        _lib = handle
+        _lib = load(LIB_PATH)
     return _lib
+
+
+def use(handle: ctypes.CDLL | None) -> ctypes.CDLL | None:
+    """Route the binding's calls to `handle` (e.g. the debug build,
+    libkvq_debug.so); None returns to libkvq.so.  Returns the previous handle."""
+    global _lib
+    prev, _lib = _lib, handle
+    return prev
 
 
 def status_string(status: int) -> str:

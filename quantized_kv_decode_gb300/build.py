@@ -2,6 +2,9 @@
 
 Each .cu under csrc/ compiles to an object in parallel; the objects link into
 quantized_kv_decode_gb300/libkvq.so.  Run ``python -m quantized_kv_decode_gb300.build``.
+``--debug`` (build(debug=True)) compiles the same sources with KVQ_DEBUG into
+libkvq_debug.so: every global access of the kernels is checked against the
+extent of its array first (see kvq_debug_checks in include/kvq.h).
 """
 from __future__ import annotations
 
@@ -16,6 +19,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libkvq.so")
+BUILD_DEBUG = os.path.join(PKG, "_build_debug")
+LIB_DEBUG = os.path.join(PKG, "libkvq_debug.so")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
@@ -39,23 +44,27 @@ def _deps():
         [os.path.join(INCLUDE, "kvq.h"), os.path.abspath(__file__)]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(debug: bool = False) -> bool:
+    lib = LIB_DEBUG if debug else LIB
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(verbose: bool = False, force: bool = False, ptxas_info: bool = False) -> str:
-    """Compile csrc/*.cu into libkvq.so; returns the library path."""
-    if not force and up_to_date():
-        return LIB
+def build(verbose: bool = False, force: bool = False, ptxas_info: bool = False,
+          debug: bool = False) -> str:
+    """Compile csrc/*.cu into libkvq.so (debug: libkvq_debug.so, with the
+    bounds checks of KVQ_DEBUG); returns the library path."""
+    lib, bdir = (LIB_DEBUG, BUILD_DEBUG) if debug else (LIB, BUILD)
+    if not force and up_to_date(debug):
+        return lib
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
-    extra = ["-Xptxas", "-v"] if ptxas_info else []
+    os.makedirs(bdir, exist_ok=True)
+    extra = (["-Xptxas", "-v"] if ptxas_info else []) + (["-DKVQ_DEBUG"] if debug else [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(bdir, os.path.basename(src) + ".o")
         cmd = [nvcc, *NVCC_FLAGS, *extra, "-I", INCLUDE, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         return src, obj, r
@@ -68,15 +77,16 @@ def build(verbose: bool = False, force: bool = False, ptxas_info: bool = False) 
             sys.stderr.write(r.stdout + r.stderr)
         if r.returncode:
             raise RuntimeError(f"nvcc failed on {os.path.basename(src)}")
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc, ARCH, "-shared", "-o", tmp, *[o for _, o, _ in results]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode:
         sys.stderr.write(r.stdout + r.stderr)
-        raise RuntimeError("link of libkvq.so failed")
-    os.replace(tmp, LIB)
-    return LIB
+        raise RuntimeError(f"link of {os.path.basename(lib)} failed")
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(verbose=True, force="--force" in sys.argv, ptxas_info="--ptxas" in sys.argv))
+    print(build(verbose=True, force="--force" in sys.argv, ptxas_info="--ptxas" in sys.argv,
+                debug="--debug" in sys.argv))

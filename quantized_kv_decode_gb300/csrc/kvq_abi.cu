@@ -283,6 +283,55 @@ kvq_status make_plan(const kvq_cache_desc* desc, const CacheGeom& geom, int32_t 
 
 kvq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
 
+#ifdef KVQ_DEBUG
+// Bytes kvq_debug_shrink_extent takes off each array's extent.
+int64_t g_dbg_shrink[KVQ_ARRAY_COUNT] = {};
+
+void dbg_set(DbgExtents& x, int a, const void* base, size_t bytes) {
+  const unsigned long long lo = (unsigned long long)reinterpret_cast<uintptr_t>(base);
+  const size_t cut = std::min<size_t>((size_t)g_dbg_shrink[a], bytes);
+  x.lo[a] = lo;
+  x.hi[a] = base ? lo + (bytes - cut) : lo;
+}
+#endif
+
+// Debug builds: the extent of every caller array of a call (the sizes
+// kvq.h states for debug builds); nothing in a release build.
+void dbg_fill(CacheGeom& g, const kvq_cache_desc* desc, const kvq_cache* cache, int32_t batch,
+              int32_t num_q_heads, int32_t num_new, const void* q, const void* k_new,
+              const void* v_new, const void* lens, const void* out, const void* ws,
+              size_t ws_bytes, uint32_t* status) {
+#ifdef KVQ_DEBUG
+  DbgExtents& x = g.dbg;
+  memset(&x, 0, sizeof(x));
+  size_t cb = 0, hb = 0;
+  if (kvq_cache_array_bytes(desc, batch, &cb, &hb) != KVQ_OK) cb = hb = 0;
+  const size_t wb = kvq_cache_window_bytes(desc, batch);
+  dbg_set(x, KVQ_ARRAY_K_CODES, cache->k_codes, cb);
+  dbg_set(x, KVQ_ARRAY_V_CODES, cache->v_codes, cb);
+  dbg_set(x, KVQ_ARRAY_K_SCALE, cache->k_scale, hb);
+  dbg_set(x, KVQ_ARRAY_K_ZERO, cache->k_zero, hb);
+  dbg_set(x, KVQ_ARRAY_V_SCALE, cache->v_scale, hb);
+  dbg_set(x, KVQ_ARRAY_V_ZERO, cache->v_zero, hb);
+  dbg_set(x, KVQ_ARRAY_K_WINDOW, cache->k_window, wb);
+  dbg_set(x, KVQ_ARRAY_V_WINDOW, cache->v_window, wb);
+  dbg_set(x, KVQ_ARRAY_BLOCK_TABLE, cache->block_table,
+          desc->layout == KVQ_PAGED ? (size_t)batch * desc->max_blocks_per_seq * 4 : 0);
+  const size_t qb = (size_t)batch * num_q_heads * desc->head_dim * 2;
+  dbg_set(x, KVQ_ARRAY_Q, q, qb);
+  dbg_set(x, KVQ_ARRAY_OUT, out, qb);
+  const size_t nb = (size_t)batch * num_new * desc->num_kv_heads * desc->head_dim * 2;
+  dbg_set(x, KVQ_ARRAY_K_NEW, k_new, nb);
+  dbg_set(x, KVQ_ARRAY_V_NEW, v_new, nb);
+  dbg_set(x, KVQ_ARRAY_SEQ_LENS, lens, (size_t)batch * 4);
+  dbg_set(x, KVQ_ARRAY_WORKSPACE, ws, ws_bytes);
+  x.status = status;
+#else
+  (void)g, (void)desc, (void)cache, (void)batch, (void)num_q_heads, (void)num_new, (void)q;
+  (void)k_new, (void)v_new, (void)lens, (void)out, (void)ws, (void)ws_bytes, (void)status;
+#endif
+}
+
 }  // namespace
 
 size_t workspace_bytes(int64_t batch, int64_t Hq, int64_t D, int64_t splits) {
@@ -374,6 +423,8 @@ kvq_status kvq_append(const kvq_cache_desc* desc, const kvq_cache* cache, int32_
   p.status = dev_status;
   p.batch = batch;
   p.num_new = num_new;
+  dbg_fill(p.geom, desc, cache, batch, 0, num_new, nullptr, k_new, v_new, seq_lens_before,
+           nullptr, nullptr, 0, dev_status);
   return from_cuda(launch_append(p, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -454,6 +505,9 @@ kvq_status decode_impl(const kvq_cache_desc* desc, const kvq_cache* cache, int32
   p.ws_ml = nullptr;
   if (splits > 1) workspace_carve(workspace, batch, num_q_heads, desc->head_dim, splits, &p.ws_o, &p.ws_ml);
   p.status = dev_status;
+  dbg_fill(p.geom, desc, cache, batch, num_q_heads, fused ? 1 : 0, q, k_new, v_new,
+           fused ? (const void*)lens_before : (const void*)seq_lens, out,
+           splits > 1 ? workspace : nullptr, splits > 1 ? workspace_size : 0, dev_status);
   p.batch = batch;
   p.Hq = num_q_heads;
   p.G = G;
@@ -558,6 +612,25 @@ kvq_status kvq_append_decode_attn(const kvq_cache_desc* desc, const kvq_cache* c
   return decode_impl(desc, cache, batch, num_q_heads, q, nullptr, seq_lens_before, k_new, v_new,
                      max_seq_len, num_splits, softmax_scale, out, workspace, workspace_size,
                      dev_status, stream);
+}
+
+int32_t kvq_debug_checks(void) {
+#ifdef KVQ_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+kvq_status kvq_debug_shrink_extent(int32_t array, int64_t bytes) {
+#ifdef KVQ_DEBUG
+  if (array < 0 || array >= KVQ_ARRAY_COUNT || bytes < 0) return KVQ_ERR_INVALID_ARG;
+  g_dbg_shrink[array] = bytes;
+  return KVQ_OK;
+#else
+  (void)array, (void)bytes;
+  return KVQ_ERR_UNSUPPORTED;
+#endif
 }
 
 const char* kvq_status_string(kvq_status status) {

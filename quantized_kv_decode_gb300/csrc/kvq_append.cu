@@ -34,7 +34,8 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
   const int b = (int)(r / p.num_new);
 
   uint32_t flags = 0;
-  const int pos = __ldg(p.seq_lens_before + b) + t;
+  const int32_t* lp = p.seq_lens_before + b;
+  const int pos = KVQ_IN(c, KVQ_ARRAY_SEQ_LENS, lp, 4) ? __ldg(lp) + t : -1;
   const int limit = (c.layout == KVQ_DENSE) ? c.slots : c.max_blocks * c.slots;
   long long row = -1;
   if (pos < 0 || pos >= limit) {
@@ -44,6 +45,8 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
     if (row < 0) flags |= KVQ_FLAG_BLOCK_TABLE;
   }
   const __half* src = p.src[which] + (((long long)b * p.num_new + t) * c.Hkv + kvh) * c.D;
+  const int a_src = which ? KVQ_ARRAY_V_NEW : KVQ_ARRAY_K_NEW;
+  const int a_codes = which ? KVQ_ARRAY_V_CODES : KVQ_ARRAY_K_CODES;
 
   if constexpr (BITS == 16) {
     if (!live) return;
@@ -51,14 +54,17 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
       if (ch == 0 && p.status) atomicOr(p.status, flags);
       return;
     }
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(src) + ch);
-    *reinterpret_cast<uint4*>(p.codes[which] + row * c.row_bytes + ch * 16) = v;
+    const uint4* sp = reinterpret_cast<const uint4*>(src) + ch;
+    const uint4 v = KVQ_IN(c, a_src, sp, 16) ? __ldg(sp) : make_uint4(0u, 0u, 0u, 0u);
+    uint8_t* dst = p.codes[which] + row * c.row_bytes + ch * 16;
+    if (KVQ_IN(c, a_codes, dst, 16)) *reinterpret_cast<uint4*>(dst) = v;
     return;
   } else {
     const int tpg = c.g / 8;          // threads per group: 1, 2, 4, ..., 32
     const int sub = ch % tpg;          // this thread's place in its group
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (live) v = __ldg(reinterpret_cast<const uint4*>(src) + ch);
+    if (live && KVQ_IN(c, a_src, reinterpret_cast<const uint4*>(src) + ch, 16))
+      v = __ldg(reinterpret_cast<const uint4*>(src) + ch);
     // every lane: the group uses shuffles
     const Quant8 qz = KIND == 2 ? quantize8_nf4(v, tpg, p.nf4_mid) : quantize8<BITS, SYM>(v, tpg);
     if (!live) return;
@@ -70,17 +76,22 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendParams p) {
     const uint32_t w0 = qz.w0, w1 = qz.w1;
     const __half s_h = qz.s, z_h = qz.z;
     uint8_t* dst = p.codes[which] + row * c.row_bytes + (long long)ch * 8 * BITS / 8;
-    if constexpr (BITS == 2) {
-      *reinterpret_cast<uint16_t*>(dst) = (uint16_t)w0;
-    } else if constexpr (BITS == 4) {
-      *reinterpret_cast<uint32_t*>(dst) = w0;
-    } else {
-      *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);
+    if (KVQ_IN(c, a_codes, dst, BITS)) {
+      if constexpr (BITS == 2) {
+        *reinterpret_cast<uint16_t*>(dst) = (uint16_t)w0;
+      } else if constexpr (BITS == 4) {
+        *reinterpret_cast<uint32_t*>(dst) = w0;
+      } else {
+        *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);
+      }
     }
     if (sub == 0) {
       const long long h_idx = row * c.ngroups + ch / tpg;
-      p.scale[which][h_idx] = s_h;
-      if constexpr (KIND == 0) p.zero[which][h_idx] = z_h;
+      if (KVQ_IN(c, which ? KVQ_ARRAY_V_SCALE : KVQ_ARRAY_K_SCALE, p.scale[which] + h_idx, 2))
+        p.scale[which][h_idx] = s_h;
+      if constexpr (KIND == 0)
+        if (KVQ_IN(c, which ? KVQ_ARRAY_V_ZERO : KVQ_ARRAY_K_ZERO, p.zero[which] + h_idx, 2))
+          p.zero[which][h_idx] = z_h;
       if (flags && p.status) atomicOr(p.status, flags);
     }
   }

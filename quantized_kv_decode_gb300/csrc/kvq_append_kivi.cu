@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(kBlockThreads) kivi_block_kernel(const AppendP
   const CacheGeom& c = p.geom;
   const int kvh = blockIdx.y, b = blockIdx.z;
   const int S = c.sink, g = c.g;
-  const int p0 = __ldg(p.seq_lens_before + b);
+  const int p0 = checked_len(p.geom, p.seq_lens_before, b, -1);
   const int n = p.num_new;
   if (p0 < 0) return;  // flagged by the window kernel
   // the block holding the first new token (or block 0), then the next ones
@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(kBlockThreads) kivi_step_kernel(const AppendPa
   pdl_launch_dependents();
   pdl_wait();
   const int kvh = blockIdx.y, b = blockIdx.z;
-  kivi_append_one<BITS>(kivi_io(p), b, kvh, __ldg(p.seq_lens_before + b));
+  kivi_append_one<BITS>(kivi_io(p), b, kvh, checked_len(p.geom, p.seq_lens_before, b, -1));
 }
 
 // Sinks and the residual window left after this append: one thread per
@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(256) kivi_window_kernel(const AppendParams p) 
   r /= c.Hkv;
   const int t = (int)(r % p.num_new);
   const int b = (int)(r / p.num_new);
-  const int p0 = __ldg(p.seq_lens_before + b);
+  const int p0 = checked_len(p.geom, p.seq_lens_before, b, -1);
   const long long q = (long long)p0 + t;
   if (p0 < 0 || q >= kch_capacity(c)) {
     if (ch == 0 && kvh == 0 && p.status) atomicOr(p.status, KVQ_FLAG_SEQ_LEN);
@@ -103,9 +103,13 @@ __global__ void __launch_bounds__(256) kivi_window_kernel(const AppendParams p) 
   const long long src = (((long long)b * p.num_new + t) * c.Hkv + kvh) * c.D + ch * 8;
   const long long dst = (bh * (c.sink + c.g) + slot) * c.D + ch * 8;
 #pragma unroll
-  for (int which = 0; which < 2; ++which)
-    *reinterpret_cast<uint4*>(p.window[which] + dst) =
-        *reinterpret_cast<const uint4*>(p.src[which] + src);
+  for (int which = 0; which < 2; ++which) {
+    const __half* from = p.src[which] + src;
+    __half* to = p.window[which] + dst;
+    if (KVQ_IN(c, which ? KVQ_ARRAY_V_NEW : KVQ_ARRAY_K_NEW, from, 16) &&
+        KVQ_IN(c, which ? KVQ_ARRAY_V_WINDOW : KVQ_ARRAY_K_WINDOW, to, 16))
+      *reinterpret_cast<uint4*>(to) = *reinterpret_cast<const uint4*>(from);
+  }
 }
 
 }  // namespace

@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_cc_kernel(const DecodePara
 
   const __half* qg = p.q + ((long long)b * p.Hq + (long long)kvh * G) * D;
   for (int i = threadIdx.x; i < GP * D; i += kWarps * 32)
-    q_s[i] = (i < G * D) ? __half2float(qg[i]) : 0.f;
+    q_s[i] = (i < G * D && KVQ_IN(c, KVQ_ARRAY_Q, qg + i, 2)) ? __half2float(qg[i]) : 0.f;
   if (threadIdx.x < 16) lv_s[threadIdx.x] = c.nf4 ? p.nf4_level[threadIdx.x] : 0.f;
   __syncthreads();
 
@@ -135,10 +135,11 @@ __global__ void __launch_bounds__(kWarps * 32) decode_cc_kernel(const DecodePara
     for (int h = 0; h < GP; ++h) sc[h] = 0.f;
     if (row >= 0) {
       const uint4* kr = reinterpret_cast<const uint4*>(p.codes[0] + row * C::ROWB);
+      const bool k_ok = KVQ_IN(c, KVQ_ARRAY_K_CODES, kr, C::ROWB);
       if constexpr (BITS == 16) {
 #pragma unroll
         for (int ch = 0; ch < C::NCH; ++ch) {
-          const uint4 w = __ldg(kr + ch);
+          const uint4 w = k_ok ? __ldg(kr + ch) : make_uint4(0u, 0u, 0u, 0u);
           const __half* hv = reinterpret_cast<const __half*>(&w);
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
@@ -158,8 +159,11 @@ __global__ void __launch_bounds__(kWarps * 32) decode_cc_kernel(const DecodePara
         for (int h = 0; h < GP; ++h) acc[h] = 0.f;
         auto flush = [&]() {
           const long long hi = row * ngr + gcur;
-          const float s = __half2float(p.scale[0][hi]);
-          const float z = nf4 ? 0.f : (sym ? zsym : __half2float(p.zero[0][hi]));
+          const float s = KVQ_IN(c, KVQ_ARRAY_K_SCALE, p.scale[0] + hi, 2) ? __half2float(p.scale[0][hi]) : 0.f;
+          const float z = nf4 ? 0.f
+                        : (sym ? zsym
+                               : (KVQ_IN(c, KVQ_ARRAY_K_ZERO, p.zero[0] + hi, 2) ? __half2float(p.zero[0][hi])
+                                                                                 : 0.f));
 #pragma unroll
           for (int h = 0; h < GP; ++h) {
             sc[h] = fmaf(s, fmaf(-z, qg_s[h * ngr + gcur], acc[h]), sc[h]);
@@ -169,7 +173,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_cc_kernel(const DecodePara
         };
 #pragma unroll
         for (int ch = 0; ch < C::NCH; ++ch) {
-          const uint4 w = __ldg(kr + ch);
+          const uint4 w = k_ok ? __ldg(kr + ch) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
           for (int e = 0; e < C::EPC; ++e) {
             const int d = ch * C::EPC + e;
@@ -212,18 +216,22 @@ __global__ void __launch_bounds__(kWarps * 32) decode_cc_kernel(const DecodePara
       if (vr < 0) continue;  // warp-uniform
       float x[C::CPL];
       const uint8_t* rp = p.codes[1] + vr * C::ROWB;
+      const bool v_ok = KVQ_IN(c, KVQ_ARRAY_V_CODES, rp, C::ROWB);
       if constexpr (BITS == 16) {
         const __half* hv = reinterpret_cast<const __half*>(rp) + d0;
 #pragma unroll
-        for (int e = 0; e < C::CPL; ++e) x[e] = __half2float(hv[e]);
+        for (int e = 0; e < C::CPL; ++e) x[e] = v_ok ? __half2float(hv[e]) : 0.f;
       } else {
         const long long hi = vr * ngr + gv;
-        const float s = __half2float(p.scale[1][hi]);
-        const float z = nf4 ? 0.f : (sym ? zsym : __half2float(p.zero[1][hi]));
+        const float s = KVQ_IN(c, KVQ_ARRAY_V_SCALE, p.scale[1] + hi, 2) ? __half2float(p.scale[1][hi]) : 0.f;
+        const float z = nf4 ? 0.f
+                      : (sym ? zsym
+                             : (KVQ_IN(c, KVQ_ARRAY_V_ZERO, p.zero[1] + hi, 2) ? __half2float(p.zero[1][hi])
+                                                                               : 0.f));
 #pragma unroll
         for (int e = 0; e < C::CPL; ++e) {
           const int d = d0 + e;
-          const uint32_t byte = rp[(d * BITS) >> 3];
+          const uint32_t byte = v_ok ? rp[(d * BITS) >> 3] : 0u;
           const uint32_t q = (byte >> ((d * BITS) & 7)) & ((1u << BITS) - 1u);
           x[e] = nf4 ? lv_s[q] * s : ((float)q - z) * s;
         }
@@ -269,13 +277,17 @@ __global__ void __launch_bounds__(kWarps * 32) decode_cc_kernel(const DecodePara
       }
     }
     if (p.splits == 1) {
-      p.out[hq0 * D + i] = __float2half_rn(den > 0.f ? num / den : 0.f);
+      if (KVQ_IN(c, KVQ_ARRAY_OUT, p.out + hq0 * D + i, 2))
+        p.out[hq0 * D + i] = __float2half_rn(den > 0.f ? num / den : 0.f);
     } else {
-      p.ws_o[((hq0 + h) * p.splits + split) * D + d] = num;
+      float* w = p.ws_o + ((hq0 + h) * p.splits + split) * D + d;
+      if (KVQ_IN(c, KVQ_ARRAY_WORKSPACE, w, 4)) *w = num;
       if (d == 0) {
         float* mlo = p.ws_ml + ((hq0 + h) * p.splits + split) * 2;
-        mlo[0] = M;
-        mlo[1] = den;
+        if (KVQ_IN(c, KVQ_ARRAY_WORKSPACE, mlo, 8)) {
+          mlo[0] = M;
+          mlo[1] = den;
+        }
       }
     }
   }

@@ -379,7 +379,9 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
         const uintptr_t a0 = reinterpret_cast<uintptr_t>(base) + (uintptr_t)(row0 * per);
         const uintptr_t a1 = a0 + (uintptr_t)n * per;
         const uintptr_t lo = a0 & ~(uintptr_t)15, hi = a1 & ~(uintptr_t)15;  // stay inside the array
-        if (hi > lo) prefetch_l2(reinterpret_cast<const void*>(lo), (uint32_t)(hi - lo));
+        // (region r is kvq_array r: K / V codes, K scale / zero, V scale / zero)
+        if (hi > lo && KVQ_IN(geo, region, reinterpret_cast<const void*>(lo), hi - lo))
+          prefetch_l2(reinterpret_cast<const void*>(lo), (uint32_t)(hi - lo));
       }
     }
   }
@@ -389,6 +391,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
     const int b = blockIdx.z;
     const void* src = nullptr;
     uint32_t bytes = 0;
+    const int arr = lane == 0 ? KVQ_ARRAY_Q : lane < 3 ? KVQ_ARRAY_K_NEW + (lane - 1)
+                                                       : KVQ_ARRAY_K_WINDOW + (lane - 3);
     if (lane == 0) {
       src = p.q + ((long long)b * p.Hq + (long long)kvh * G) * D;
       bytes = (uint32_t)(G * D * 2);
@@ -401,7 +405,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
       src = p.window[lane - 3] + ((long long)b * geo.Hkv + kvh) * (geo.sink + geo.g) * D;
       bytes = (uint32_t)((geo.sink + geo.g) * D * 2);
     }
-    if (src != nullptr && (reinterpret_cast<uintptr_t>(src) & 15) == 0) prefetch_l2(src, bytes);
+    if (src != nullptr && (reinterpret_cast<uintptr_t>(src) & 15) == 0 && KVQ_IN(geo, arr, src, bytes))
+      prefetch_l2(src, bytes);
   }
   pdl_wait();
 
@@ -420,7 +425,9 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
   if (!KCH && p.longest_first && p.lens_before != nullptr && L > 0 && L - 1 >= t0 && L - 1 < t1 &&
       threadIdx.x < 2) {
     const __half* src = p.new_kv[threadIdx.x] + ((long long)b * geo.Hkv + kvh) * D;
-    if ((reinterpret_cast<uintptr_t>(src) & 15) == 0) prefetch_l2(src, (uint32_t)(D * 2));
+    if ((reinterpret_cast<uintptr_t>(src) & 15) == 0 &&
+        KVQ_IN(geo, KVQ_ARRAY_K_NEW + (int)threadIdx.x, src, D * 2))
+      prefetch_l2(src, (uint32_t)(D * 2));
   }
 
   // shared memory: [q fp16 GP x D][per warp: stages, header scratch][tile
@@ -442,7 +449,7 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
 
   const __half* qg = p.q + ((long long)b * p.Hq + (long long)kvh * G) * D;
   for (int i = threadIdx.x; i < GP * D; i += blockDim.x)
-    q_s[i] = (i < G * D) ? qg[i] : __float2half_rn(0.f);
+    q_s[i] = (i < G * D && KVQ_IN(geo, KVQ_ARRAY_Q, qg + i, 2)) ? qg[i] : __float2half_rn(0.f);
   // Fused step on an axis-aware cache, one split: this CTA appends its
   // unit's new token (position L - 1) with the append kernel's code, so that
   // it reads the cache as the two-call step leaves it.  A token that
@@ -663,8 +670,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
           const bool ok = tok < n;
           const long long off = ok ? base + tok * C::ROWB + part * 16 : 0;
           const uint32_t dst = C::at(tok, part);
-          cp_async16(kc_s + dst, kc_g + off, ok);
-          cp_async16(vc_s + dst, vc_g + off, ok);
+          cp_async16(kc_s + dst, kc_g + off, ok && KVQ_IN(geo, KVQ_ARRAY_K_CODES, kc_g + off, 16));
+          cp_async16(vc_s + dst, vc_g + off, ok && KVQ_IN(geo, KVQ_ARRAY_V_CODES, vc_g + off, 16));
         }
       } else if (!PG && p.rows32) {
         // rows and byte offsets in 32 bits; pages of a power-of-two size by a
@@ -673,7 +680,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
         if (lane < n) {
           const int pos = start + lane;
           const int blk = pg_pow2 ? pos >> pg_shift : pos / geo.slots;
-          const int pg = __ldg(geo.block_table + bt_row + blk);
+          const int32_t* bte = geo.block_table + bt_row + blk;
+          const int pg = KVQ_IN(geo, KVQ_ARRAY_BLOCK_TABLE, bte, 4) ? __ldg(bte) : -1;
           if (pg >= 0 && pg < geo.num_pages) row32 = (pg * geo.Hkv + kvh) * geo.slots + (pos - blk * geo.slots);
           unmapped = row32 < 0;
         }
@@ -686,8 +694,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
           const bool ok = r >= 0;
           const uint32_t off = ok ? (uint32_t)r * C::ROWB + part * 16 : 0u;
           const uint32_t dst = C::at(tok, part);
-          cp_async16(kc_s + dst, kc_g + off, ok);
-          cp_async16(vc_s + dst, vc_g + off, ok);
+          cp_async16(kc_s + dst, kc_g + off, ok && KVQ_IN(geo, KVQ_ARRAY_K_CODES, kc_g + off, 16));
+          cp_async16(vc_s + dst, vc_g + off, ok && KVQ_IN(geo, KVQ_ARRAY_V_CODES, vc_g + off, 16));
         }
       } else {
         if (lane < n) {
@@ -703,8 +711,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
           const bool ok = r >= 0;
           const long long off = ok ? r * C::ROWB + part * 16 : 0;
           const uint32_t dst = C::at(tok, part);
-          cp_async16(kc_s + dst, kc_g + off, ok);
-          cp_async16(vc_s + dst, vc_g + off, ok);
+          cp_async16(kc_s + dst, kc_g + off, ok && KVQ_IN(geo, KVQ_ARRAY_K_CODES, kc_g + off, 16));
+          cp_async16(vc_s + dst, vc_g + off, ok && KVQ_IN(geo, KVQ_ARRAY_V_CODES, vc_g + off, 16));
         }
       }
       const unsigned bad = __ballot_sync(0xffffffffu, row < 0);
@@ -719,22 +727,32 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
           const long long hb = hrow >= 0 ? hrow * D : 0;  // unmapped: zero-filled (rows masked)
           if (lane < D / 4) {
             const int w = lane / (D / 8), c = lane % (D / 8);
-            cp_async16(hd_s + w * 2 * D + c * 16, (w ? kz_g : ks_g) + (hb + c * 8) * 2, hrow >= 0);
+            const uint8_t* hsrc = (w ? kz_g : ks_g) + (hb + c * 8) * 2;
+            cp_async16(hd_s + w * 2 * D + c * 16, hsrc,
+                       hrow >= 0 && KVQ_IN(geo, w ? KVQ_ARRAY_K_ZERO : KVQ_ARRAY_K_SCALE, hsrc, 16));
           }
         } else {
           const long long hb = ((((long long)b * geo.Hkv + kvh) * (geo.slots / geo.g)) +
                                 (start - geo.sink) / geo.g) * D;
           if (lane < D / 4) {
             const int w = lane / (D / 8), c = lane % (D / 8);
-            cp_async16(hd_s + w * 2 * D + c * 16, (w ? kz_g : ks_g) + (hb + c * 8) * 2, true);
+            const uint8_t* hsrc = (w ? kz_g : ks_g) + (hb + c * 8) * 2;
+            cp_async16(hd_s + w * 2 * D + c * 16, hsrc,
+                       KVQ_IN(geo, w ? KVQ_ARRAY_K_ZERO : KVQ_ARRAY_K_SCALE, hsrc, 16));
           }
         }
       } else {
-        cp_async_small<C::HDRB>(hdst, ks_g + hoff, ok);
-        if constexpr (!SYM) cp_async_small<C::HDRB>(hdst + C::HDR_TILE, kz_g + hoff, ok);
+        cp_async_small<C::HDRB>(hdst, ks_g + hoff,
+                                ok && KVQ_IN(geo, KVQ_ARRAY_K_SCALE, ks_g + hoff, C::HDRB));
+        if constexpr (!SYM)
+          cp_async_small<C::HDRB>(hdst + C::HDR_TILE, kz_g + hoff,
+                                  ok && KVQ_IN(geo, KVQ_ARRAY_K_ZERO, kz_g + hoff, C::HDRB));
       }
-      cp_async_small<C::HDRB>(hdst + C::KHB, vs_g + hoff, ok);
-      if constexpr (!SYM) cp_async_small<C::HDRB>(hdst + C::KHB + C::HDR_TILE, vz_g + hoff, ok);
+      cp_async_small<C::HDRB>(hdst + C::KHB, vs_g + hoff,
+                              ok && KVQ_IN(geo, KVQ_ARRAY_V_SCALE, vs_g + hoff, C::HDRB));
+      if constexpr (!SYM)
+        cp_async_small<C::HDRB>(hdst + C::KHB + C::HDR_TILE, vz_g + hoff,
+                                ok && KVQ_IN(geo, KVQ_ARRAY_V_ZERO, vz_g + hoff, C::HDRB));
     }
     cp_async_commit();  // one group per slot, empty past the end
     return unmapped;
@@ -1249,8 +1267,10 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
     const long long nrow = token_row(geo, b, kvh, pos_new);
     if (nrow < 0 && lane == 0 && p.status) atomicOr(p.status, KVQ_FLAG_BLOCK_TABLE);
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (which < 2)
-      v = __ldg(reinterpret_cast<const uint4*>(p.new_kv[which] + ((long long)b * geo.Hkv + kvh) * D) + ch);
+    if (which < 2) {
+      const uint4* src = reinterpret_cast<const uint4*>(p.new_kv[which] + ((long long)b * geo.Hkv + kvh) * D) + ch;
+      if (KVQ_IN(geo, KVQ_ARRAY_K_NEW + which, src, 16)) v = __ldg(src);
+    }
     Quant8 qz;
     if constexpr (NF) {
       float mid[16];  // the level midpoints, as the host computes them
@@ -1263,13 +1283,19 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
     }
     if (which < 2 && nrow >= 0) {
       uint8_t* gcodes = const_cast<uint8_t*>(p.codes[which]) + nrow * C::ROWB + ch * BITS;
-      if constexpr (BITS == 2) *reinterpret_cast<uint16_t*>(gcodes) = (uint16_t)qz.w0;
-      else if constexpr (BITS == 4) *reinterpret_cast<uint32_t*>(gcodes) = qz.w0;
-      else *reinterpret_cast<uint2*>(gcodes) = make_uint2(qz.w0, qz.w1);
+      if (KVQ_IN(geo, KVQ_ARRAY_K_CODES + which, gcodes, BITS)) {
+        if constexpr (BITS == 2) *reinterpret_cast<uint16_t*>(gcodes) = (uint16_t)qz.w0;
+        else if constexpr (BITS == 4) *reinterpret_cast<uint32_t*>(gcodes) = qz.w0;
+        else *reinterpret_cast<uint2*>(gcodes) = make_uint2(qz.w0, qz.w1);
+      }
       if (ch % (C::GSZ / 8) == 0) {
         const int g = ch / (C::GSZ / 8);
-        const_cast<__half*>(p.scale[which])[nrow * NG + g] = qz.s;
-        if constexpr (!SYM) const_cast<__half*>(p.zero[which])[nrow * NG + g] = qz.z;
+        __half* sp = const_cast<__half*>(p.scale[which]) + nrow * NG + g;
+        if (KVQ_IN(geo, which ? KVQ_ARRAY_V_SCALE : KVQ_ARRAY_K_SCALE, sp, 2)) *sp = qz.s;
+        if constexpr (!SYM) {
+          __half* zp = const_cast<__half*>(p.zero[which]) + nrow * NG + g;
+          if (KVQ_IN(geo, which ? KVQ_ARRAY_V_ZERO : KVQ_ARRAY_K_ZERO, zp, 2)) *zp = qz.z;
+        }
       }
     }
     if (which < 2 && ch % (C::GSZ / 8) == 0 && qz.flags && p.status) atomicOr(p.status, qz.flags);
@@ -1422,10 +1448,12 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
         const __half* vw0 = fresh ? p.new_kv[1] + ((long long)b * geo.Hkv + kvh) * D : p.window[1] + (wb + slot) * D;
         const uint32_t* kr = reinterpret_cast<const uint32_t*>(kw0) + lane * WPR;
         const uint32_t* vr = reinterpret_cast<const uint32_t*>(vw0) + lane * WPR;
+        const bool k_ok = KVQ_IN(geo, fresh ? KVQ_ARRAY_K_NEW : KVQ_ARRAY_K_WINDOW, kr, 4 * WPR);
+        const bool v_ok = KVQ_IN(geo, fresh ? KVQ_ARRAY_V_NEW : KVQ_ARRAY_V_WINDOW, vr, 4 * WPR);
 #pragma unroll
         for (int c = 0; c < WPR; ++c) {
-          kw[k][c] = kr[c];
-          vw[k][c] = vr[c];
+          kw[k][c] = k_ok ? kr[c] : 0u;
+          vw[k][c] = v_ok ? vr[c] : 0u;
         }
       }
       // scores of the batch's rows (independent, so their reductions
@@ -1481,8 +1509,10 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
     if (kch_slot >= 0 && warp == 0 && lane < D / 4) {  // the appended token's fp16 slot
       const int which = lane / (D / 8), ch = lane % (D / 8);
       const long long bh = (long long)b * geo.Hkv + kvh;
-      *(reinterpret_cast<uint4*>(const_cast<__half*>(p.window[which]) + (bh * (geo.sink + geo.g) + kch_slot) * D) + ch) =
-          *(reinterpret_cast<const uint4*>(p.new_kv[which] + bh * D) + ch);
+      uint4* to = reinterpret_cast<uint4*>(const_cast<__half*>(p.window[which]) + (bh * (geo.sink + geo.g) + kch_slot) * D) + ch;
+      const uint4* from = reinterpret_cast<const uint4*>(p.new_kv[which] + bh * D) + ch;
+      if (KVQ_IN(geo, KVQ_ARRAY_K_NEW + which, from, 16) && KVQ_IN(geo, KVQ_ARRAY_K_WINDOW + which, to, 16))
+        *to = *from;
     }
 #pragma unroll
     for (int h = 0; h < GP; ++h) {
@@ -1531,13 +1561,17 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
       }
     }
     if (p.splits == 1) {
-      p.out[hq0 * D + i] = __float2half_rn(den > 0.f ? num / den : 0.f);
+      if (KVQ_IN(geo, KVQ_ARRAY_OUT, p.out + hq0 * D + i, 2))
+        p.out[hq0 * D + i] = __float2half_rn(den > 0.f ? num / den : 0.f);
     } else {
-      p.ws_o[((hq0 + h) * p.splits + split) * D + d] = num;
+      float* w = p.ws_o + ((hq0 + h) * p.splits + split) * D + d;
+      if (KVQ_IN(geo, KVQ_ARRAY_WORKSPACE, w, 4)) *w = num;
       if (d == 0) {
         float* mlo = p.ws_ml + ((hq0 + h) * p.splits + split) * 2;
-        mlo[0] = M;
-        mlo[1] = den;
+        if (KVQ_IN(geo, KVQ_ARRAY_WORKSPACE, mlo, 8)) {
+          mlo[0] = M;
+          mlo[1] = den;
+        }
       }
     }
   }

@@ -22,28 +22,41 @@ namespace {
 constexpr int kThreads = 128;
 constexpr int kTile = 64;
 
-// nf4_level: the NF4 level table, or null for uniform codes
+// A caller array element, or 0 when a debug build finds it outside the array
+template <typename T>
+__device__ __forceinline__ T checked_at(const CacheGeom& c, int a, const T* ptr) {
+  return KVQ_IN(c, a, ptr, sizeof(T)) ? *ptr : T(0);
+}
+__device__ __forceinline__ float checked_half(const CacheGeom& c, int a, const __half* ptr) {
+  return KVQ_IN(c, a, ptr, 2) ? __half2float(*ptr) : 0.f;
+}
+
+// K (which = 0) or V (which = 1); nf4_level: the NF4 level table, or null
+// for uniform codes
 template <int BITS>
-__device__ __forceinline__ float dequant(const uint8_t* codes, const __half* scale,
+__device__ __forceinline__ float dequant(int which, const uint8_t* codes, const __half* scale,
                                          const __half* zero, const CacheGeom& c,
                                          long long row, int d, const float* nf4_level) {
+  const int a_codes = which ? KVQ_ARRAY_V_CODES : KVQ_ARRAY_K_CODES;
   if constexpr (BITS == 16) {
-    return __half2float(reinterpret_cast<const __half*>(codes + row * c.row_bytes)[d]);
+    return checked_half(c, a_codes, reinterpret_cast<const __half*>(codes + row * c.row_bytes) + d);
   } else {
     const uint8_t* r = codes + row * c.row_bytes;
     int q;
     if constexpr (BITS == 2) {
-      q = (r[d >> 2] >> (2 * (d & 3))) & 3;
+      q = (checked_at(c, a_codes, r + (d >> 2)) >> (2 * (d & 3))) & 3;
     } else if constexpr (BITS == 4) {
-      const uint8_t byte = r[d >> 1];
+      const uint8_t byte = checked_at(c, a_codes, r + (d >> 1));
       q = (d & 1) ? (byte >> 4) : (byte & 15);
     } else {
-      q = r[d];
+      q = checked_at(c, a_codes, r + d);
     }
     const long long h = row * c.ngroups + d / c.g;
-    if (nf4_level) return nf4_level[q] * __half2float(scale[h]);
-    const float z = c.sym ? (float)(1 << (BITS - 1)) : __half2float(zero[h]);
-    return ((float)q - z) * __half2float(scale[h]);
+    const float s = checked_half(c, which ? KVQ_ARRAY_V_SCALE : KVQ_ARRAY_K_SCALE, scale + h);
+    if (nf4_level) return nf4_level[q] * s;
+    const float z = c.sym ? (float)(1 << (BITS - 1))
+                          : checked_half(c, which ? KVQ_ARRAY_V_ZERO : KVQ_ARRAY_K_ZERO, zero + h);
+    return ((float)q - z) * s;
   }
 }
 
@@ -58,17 +71,20 @@ __device__ __forceinline__ float load_kv(const DecodeParams& p, int which, int b
     if (c.kch) {
       const long long bh = (long long)b * c.Hkv + kvh;
       const int slot = window_slot(c, L, pos);
-      if (slot >= 0) return __half2float(p.window[which][(bh * (c.sink + c.g) + slot) * c.D + d]);
+      if (slot >= 0)
+        return checked_half(c, which ? KVQ_ARRAY_V_WINDOW : KVQ_ARRAY_K_WINDOW,
+                            p.window[which] + (bh * (c.sink + c.g) + slot) * c.D + d);
       if (which == 0) {
         const uint8_t* r = p.codes[0] + row * c.row_bytes;
-        const float q = BITS == 4 ? (float)((d & 1) ? (r[d >> 1] >> 4) : (r[d >> 1] & 15))
-                                  : (float)r[d];
+        const uint8_t byte = checked_at(c, KVQ_ARRAY_K_CODES, r + (BITS == 4 ? d >> 1 : d));
+        const float q = BITS == 4 ? (float)((d & 1) ? (byte >> 4) : (byte & 15)) : (float)byte;
         const long long h = kch_hdr(c, b, kvh, (pos - c.sink) / c.g) * c.D + d;
-        return (q - __half2float(p.zero[0][h])) * __half2float(p.scale[0][h]);
+        return (q - checked_half(c, KVQ_ARRAY_K_ZERO, p.zero[0] + h)) *
+               checked_half(c, KVQ_ARRAY_K_SCALE, p.scale[0] + h);
       }
     }
   }
-  return dequant<BITS>(p.codes[which], p.scale[which], p.zero[which], c, row, d,
+  return dequant<BITS>(which, p.codes[which], p.scale[which], p.zero[which], c, row, d,
                        c.nf4 ? p.nf4_level : nullptr);
 }
 
@@ -102,7 +118,7 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(const DecodePa
 
   const __half* qg = p.q + ((long long)b * p.Hq + (long long)kvh * G) * D;
   for (int i = tid; i < G * D; i += kThreads) {
-    q_s[i] = __half2float(qg[i]);
+    q_s[i] = checked_half(c, KVQ_ARRAY_Q, qg + i);
     o_s[i] = 0.f;
   }
   if (tid < G) {
@@ -191,17 +207,21 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(const DecodePa
     for (int i = tid; i < G * D; i += kThreads) {
       const int h = i / D;
       const float l = l_s[h];
-      p.out[hq0 * D + i] = __float2half_rn(l > 0.f ? o_s[i] / l : 0.f);
+      if (KVQ_IN(c, KVQ_ARRAY_OUT, p.out + hq0 * D + i, 2))
+        p.out[hq0 * D + i] = __float2half_rn(l > 0.f ? o_s[i] / l : 0.f);
     }
   } else {
     for (int i = tid; i < G * D; i += kThreads) {
       const int h = i / D, d = i - h * D;
-      p.ws_o[((hq0 + h) * p.splits + split) * D + d] = o_s[i];
+      float* w = p.ws_o + ((hq0 + h) * p.splits + split) * D + d;
+      if (KVQ_IN(c, KVQ_ARRAY_WORKSPACE, w, 4)) *w = o_s[i];
     }
     if (tid < G) {
       float* ml = p.ws_ml + ((hq0 + tid) * p.splits + split) * 2;
-      ml[0] = m_s[tid];
-      ml[1] = l_s[tid];
+      if (KVQ_IN(c, KVQ_ARRAY_WORKSPACE, ml, 8)) {
+        ml[0] = m_s[tid];
+        ml[1] = l_s[tid];
+      }
     }
   }
 }
@@ -223,6 +243,9 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
   float M = -INFINITY, num = 0.f, den = 0.f;
 #pragma unroll 4
   for (int s = 0; s < nv; ++s) {
+    if (!KVQ_IN(p.geom, KVQ_ARRAY_WORKSPACE, ml + 2 * s, 8) ||
+        !KVQ_IN(p.geom, KVQ_ARRAY_WORKSPACE, o + (long long)s * D, 4))
+      continue;
     const float m = ml[2 * s], l = ml[2 * s + 1], x = o[(long long)s * D];
     if (m == -INFINITY) continue;
     const float Mn = fmaxf(M, m);
@@ -231,7 +254,8 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
     den = fmaf(f, l, den * a);
     M = Mn;
   }
-  if (d < D) p.out[rowid * D + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
+  if (d < D && KVQ_IN(p.geom, KVQ_ARRAY_OUT, p.out + rowid * D + d, 2))
+    p.out[rowid * D + d] = __float2half_rn(den > 0.f ? num / den : 0.f);
 }
 
 }  // namespace

@@ -17,6 +17,42 @@ namespace kvq {
 constexpr int kChunkAlign = 64;
 constexpr int kMaxGroupHeads = 16;  // query heads per KV head handled per CTA
 
+// Debug builds (KVQ_DEBUG): the byte extent [lo, hi) of each caller array a
+// launch may touch, indexed by kvq_array, and the status word to flag.  The
+// host fills it from the descriptor and the call's sizes; it travels in the
+// cache geometry so that every kernel and helper that addresses a caller
+// array can check the access first.
+struct DbgExtents {
+  unsigned long long lo[KVQ_ARRAY_COUNT];
+  unsigned long long hi[KVQ_ARRAY_COUNT];
+  uint32_t* status;
+};
+
+// The kernels name K / V pairs and the prefetch regions by offset.
+static_assert(KVQ_ARRAY_V_CODES == KVQ_ARRAY_K_CODES + 1 && KVQ_ARRAY_K_SCALE == 2 &&
+                  KVQ_ARRAY_K_ZERO == 3 && KVQ_ARRAY_V_SCALE == 4 && KVQ_ARRAY_V_ZERO == 5 &&
+                  KVQ_ARRAY_V_WINDOW == KVQ_ARRAY_K_WINDOW + 1 &&
+                  KVQ_ARRAY_V_NEW == KVQ_ARRAY_K_NEW + 1,
+              "kvq_array order");
+
+#ifdef KVQ_DEBUG
+// True when the n bytes at ptr lie inside array a's extent; otherwise flags
+// KVQ_FLAG_OOB and returns false, and the caller skips the access.
+__device__ __forceinline__ bool dbg_in(const DbgExtents& x, int a, const void* ptr,
+                                       unsigned long long n) {
+  const unsigned long long u = (unsigned long long)reinterpret_cast<uintptr_t>(ptr);
+  if (u >= x.lo[a] && u + n <= x.hi[a]) return true;
+  if (x.status) atomicOr(x.status, KVQ_FLAG_OOB);
+  return false;
+}
+// KVQ_IN(geometry, kvq_array, pointer, bytes): may the access go ahead?
+#define KVQ_IN(geo, a, ptr, n) (::kvq::dbg_in((geo).dbg, (a), (ptr), (n)))
+#else
+// (release: no check; the array id and pointer are only named, so that
+// variables kept for the check count as used)
+#define KVQ_IN(geo, a, ptr, n) ((void)(a), (void)(ptr), true)
+#endif
+
 // Geometry of one cache (K and V share it).
 struct CacheGeom {
   int32_t bits;        // 4, 8 or 16
@@ -34,6 +70,9 @@ struct CacheGeom {
   int32_t sink;        // axis-aware: fp16 sink tokens
   int32_t nf4;         // 1: 4-bit codes index the normal-quantile levels, no zero arrays
   const int32_t* block_table;
+#ifdef KVQ_DEBUG
+  DbgExtents dbg;
+#endif
 };
 
 // Axis-aware caches: the window slot of position p, or -1 when p is stored
@@ -59,7 +98,8 @@ __device__ __forceinline__ long long kch_row(const CacheGeom& c, int b, int kvh,
   if (u < 0) return -1;
   const int blk = u / c.slots;
   if (blk >= c.max_blocks) return -1;
-  const int page = __ldg(c.block_table + (long long)b * c.max_blocks + blk);
+  const int32_t* e = c.block_table + (long long)b * c.max_blocks + blk;
+  const int page = KVQ_IN(c, KVQ_ARRAY_BLOCK_TABLE, e, 4) ? __ldg(e) : -1;
   if (page < 0 || page >= c.num_pages) return -1;
   return ((long long)page * c.Hkv + kvh) * c.slots + (u - blk * c.slots);
 }
@@ -71,7 +111,8 @@ __device__ __forceinline__ long long kch_hdr(const CacheGeom& c, int b, int kvh,
   if (c.layout == KVQ_DENSE) return ((long long)b * c.Hkv + kvh) * bpp + j;
   const int blk = j / bpp;
   if (blk >= c.max_blocks) return -1;
-  const int page = __ldg(c.block_table + (long long)b * c.max_blocks + blk);
+  const int32_t* e = c.block_table + (long long)b * c.max_blocks + blk;
+  const int page = KVQ_IN(c, KVQ_ARRAY_BLOCK_TABLE, e, 4) ? __ldg(e) : -1;
   if (page < 0 || page >= c.num_pages) return -1;
   return ((long long)page * c.Hkv + kvh) * bpp + (j - blk * bpp);
 }
@@ -91,7 +132,8 @@ __device__ __forceinline__ long long token_row(const CacheGeom& c, int b, int kv
   }
   const int blk = pos / c.slots;
   const int off = pos - blk * c.slots;
-  const int page = __ldg(c.block_table + (long long)b * c.max_blocks + blk);
+  const int32_t* e = c.block_table + (long long)b * c.max_blocks + blk;
+  const int page = KVQ_IN(c, KVQ_ARRAY_BLOCK_TABLE, e, 4) ? __ldg(e) : -1;
   if (page < 0 || page >= c.num_pages) return -1;
   return ((long long)page * c.Hkv + kvh) * c.slots + off;
 }
@@ -147,13 +189,19 @@ struct DecodeParams {
   int32_t kch_append;
 };
 
+// lens[b] (a length array of the call), or `bad` when a debug build finds the
+// read outside the array.
+__device__ __forceinline__ int checked_len(const CacheGeom& c, const int32_t* lens, int b, int bad) {
+  return KVQ_IN(c, KVQ_ARRAY_SEQ_LENS, lens + b, 4) ? __ldg(lens + b) : bad;
+}
+
 // Tokens to attend over for sequence b (-1 for a length that cannot be formed).
 __device__ __forceinline__ int seq_len_of(const DecodeParams& p, int b) {
   if (p.lens_before) {
-    const int x = __ldg(p.lens_before + b);
+    const int x = checked_len(p.geom, p.lens_before, b, -1);
     return (x < 0 || x == 0x7fffffff) ? -1 : x + 1;
   }
-  return __ldg(p.seq_lens + b);
+  return checked_len(p.geom, p.seq_lens, b, -1);
 }
 
 // The sequence of rank r in a longest-first order of the batch: sequences

@@ -42,6 +42,12 @@ __device__ __forceinline__ const __half* kivi_token_src(const KiviIO& io, int wh
   return io.src[which] + (((long long)b * io.num_new + (q - p0)) * c.Hkv + kvh) * c.D;
 }
 
+// The caller array kivi_token_src reads for token q (debug-build checks).
+__device__ __forceinline__ int kivi_src_array(int which, int q, int p0) {
+  return q < p0 ? (which ? KVQ_ARRAY_V_WINDOW : KVQ_ARRAY_K_WINDOW)
+                : (which ? KVQ_ARRAY_V_NEW : KVQ_ARRAY_K_NEW);
+}
+
 // Quantizes block j (positions [start, start + g)) of sequence b, KV head
 // kvh, whose tokens before p0 sit in the residual window and the rest in the
 // new input.  Every thread of the CTA calls it (any whole number of warps).
@@ -63,7 +69,9 @@ __device__ void kivi_quantize_block(const KiviIO& io, int b, int kvh, int j, lon
       float mn = INFINITY, mx = -INFINITY;
       bool finite = true;
       for (int t = 0; t < g; ++t) {
-        const float x = __half2float(kivi_token_src(io, 0, b, kvh, (int)start + t, p0)[ch]);
+        const __half* xp = kivi_token_src(io, 0, b, kvh, (int)start + t, p0) + ch;
+        const float x = KVQ_IN(c, kivi_src_array(0, (int)start + t, p0), xp, 2) ? __half2float(*xp)
+                                                                               : 0.f;
         finite = finite && isfinite(x);
         mn = fminf(mn, x);
         mx = fmaxf(mx, x);
@@ -71,21 +79,25 @@ __device__ void kivi_quantize_block(const KiviIO& io, int b, int kvh, int j, lon
       gp[e] = group_params<BITS>(mn, mx, finite);
       flags |= gp[e].flags;
       if (hrow >= 0) {
-        io.scale[0][hrow * D + ch] = gp[e].s;
-        io.zero[0][hrow * D + ch] = gp[e].z;
+        if (KVQ_IN(c, KVQ_ARRAY_K_SCALE, io.scale[0] + hrow * D + ch, 2))
+          io.scale[0][hrow * D + ch] = gp[e].s;
+        if (KVQ_IN(c, KVQ_ARRAY_K_ZERO, io.zero[0] + hrow * D + ch, 2))
+          io.zero[0][hrow * D + ch] = gp[e].z;
       } else {
         flags |= KVQ_FLAG_BLOCK_TABLE;
       }
     }
     for (int t = 0; t < g; ++t) {
-      const __half* src = kivi_token_src(io, 0, b, kvh, (int)start + t, p0);
+      const __half* src = kivi_token_src(io, 0, b, kvh, (int)start + t, p0) + u * CPU;
+      const bool src_ok = KVQ_IN(c, kivi_src_array(0, (int)start + t, p0), src, 2 * CPU);
       uint32_t byte = 0;
 #pragma unroll
       for (int e = 0; e < CPU; ++e)
-        byte |= group_encode<BITS>(__half2float(src[u * CPU + e]), gp[e]) << (4 * e);
+        byte |= group_encode<BITS>(src_ok ? __half2float(src[e]) : 0.f, gp[e]) << (4 * e);
       const long long row = kch_row(c, b, kvh, (int)start + t);
-      if (row >= 0) io.codes[0][row * c.row_bytes + u] = (uint8_t)byte;
-      else flags |= KVQ_FLAG_BLOCK_TABLE;
+      if (row < 0) flags |= KVQ_FLAG_BLOCK_TABLE;
+      else if (KVQ_IN(c, KVQ_ARRAY_K_CODES, io.codes[0] + row * c.row_bytes + u, 1))
+        io.codes[0][row * c.row_bytes + u] = (uint8_t)byte;
     }
   }
 
@@ -97,7 +109,8 @@ __device__ void kivi_quantize_block(const KiviIO& io, int b, int kvh, int j, lon
   for (int t0 = warp * tpw; t0 < g; t0 += (blockDim.x / 32) * tpw) {
     const int t = t0 + lane / chv, ch = lane % chv;  // every lane is live: g % tpw == 0
     const long long q = start + t;
-    const uint4 v = *(reinterpret_cast<const uint4*>(kivi_token_src(io, 1, b, kvh, (int)q, p0)) + ch);
+    const uint4* vp = reinterpret_cast<const uint4*>(kivi_token_src(io, 1, b, kvh, (int)q, p0)) + ch;
+    const uint4 v = KVQ_IN(c, kivi_src_array(1, (int)q, p0), vp, 16) ? *vp : make_uint4(0u, 0u, 0u, 0u);
     const Quant8 qz = quantize8<BITS>(v, tpg);
     const long long row = kch_row(c, b, kvh, (int)q);
     if (row < 0) {
@@ -105,15 +118,17 @@ __device__ void kivi_quantize_block(const KiviIO& io, int b, int kvh, int j, lon
       continue;
     }
     uint8_t* dst = io.codes[1] + row * c.row_bytes + ch * BITS;
-    if constexpr (BITS == 4) {
-      *reinterpret_cast<uint32_t*>(dst) = qz.w0;
-    } else {
-      *reinterpret_cast<uint2*>(dst) = make_uint2(qz.w0, qz.w1);
+    if (KVQ_IN(c, KVQ_ARRAY_V_CODES, dst, BITS)) {
+      if constexpr (BITS == 4) {
+        *reinterpret_cast<uint32_t*>(dst) = qz.w0;
+      } else {
+        *reinterpret_cast<uint2*>(dst) = make_uint2(qz.w0, qz.w1);
+      }
     }
     if (ch % tpg == 0) {
       const long long hi = row * c.ngroups + ch / tpg;
-      io.scale[1][hi] = qz.s;
-      io.zero[1][hi] = qz.z;
+      if (KVQ_IN(c, KVQ_ARRAY_V_SCALE, io.scale[1] + hi, 2)) io.scale[1][hi] = qz.s;
+      if (KVQ_IN(c, KVQ_ARRAY_V_ZERO, io.zero[1] + hi, 2)) io.zero[1][hi] = qz.z;
       flags |= qz.flags;
     }
   }
@@ -142,8 +157,11 @@ __device__ void kivi_append_one(const KiviIO& io, int b, int kvh, int p0) {
   const int chunks = c.D / 8;
   if (threadIdx.x < 2 * chunks) {
     const int which = threadIdx.x / chunks, ch = threadIdx.x % chunks;
-    *(reinterpret_cast<uint4*>(io.window[which] + (bh * (c.sink + c.g) + slot) * c.D) + ch) =
-        *(reinterpret_cast<const uint4*>(io.src[which] + bh * c.D) + ch);
+    uint4* to = reinterpret_cast<uint4*>(io.window[which] + (bh * (c.sink + c.g) + slot) * c.D) + ch;
+    const uint4* from = reinterpret_cast<const uint4*>(io.src[which] + bh * c.D) + ch;
+    if (KVQ_IN(c, which ? KVQ_ARRAY_V_NEW : KVQ_ARRAY_K_NEW, from, 16) &&
+        KVQ_IN(c, which ? KVQ_ARRAY_V_WINDOW : KVQ_ARRAY_K_WINDOW, to, 16))
+      *to = *from;
   }
 }
 

@@ -206,3 +206,17 @@ def test_lowbit_descriptors(K):
     assert K.kvq_cache_bytes(K.make_desc(4, 64, 8, 128, K.KVQ_DENSE, 64, k_per_channel=True,
                                          nf4=True), 1) == 0
     assert K.kvq_cache_bytes(K.make_desc(2, 32, 8, 128, K.KVQ_DENSE, 64, k_per_channel=True), 1) == 0
+
+
+def test_release_library_has_no_debug_checks(K):
+    """The release library reports no bounds checks and refuses the
+    debug-only extent control (host functions, no launch)."""
+    lib = K.lib()
+    assert lib.kvq_debug_checks() == 0
+    assert lib.kvq_debug_shrink_extent(K._lib.KVQ_ARRAY_K_CODES, 16) == K.KVQ_ERR_UNSUPPORTED
+    assert K._lib.KVQ_ARRAY_WORKSPACE == 14   # the header's kvq_array order
+    text = open(HEADER).read()
+    ids = dict((m.group(1), int(m.group(2)))
+               for m in re.finditer(r"(KVQ_ARRAY_\w+)\s*=\s*(\d+)", text))
+    assert ids == {n: getattr(K._lib, n) for n in ids if n != "KVQ_ARRAY_COUNT"} | \
+        {"KVQ_ARRAY_COUNT": 15}
