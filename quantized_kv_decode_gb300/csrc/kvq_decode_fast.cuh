@@ -297,6 +297,46 @@ __device__ __forceinline__ uint32_t pack_halves(__half lo, __half hi) {
 // The kernel
 // ---------------------------------------------------------------------------
 
+// Dynamic shared memory of an instance: q, the warps' pipelines (reused by
+// the CTA merge), the tile masks and the appended token's partial; NF4
+// instances then hold their score-side level table (kNfLutBytes, 16-byte
+// aligned).
+template <int BITS, int D, int NG, int GP, bool KCH>
+__host__ __device__ constexpr size_t fast_smem_bytes() {
+  using C = Cfg<BITS, D, NG, GP, KCH>;
+  const size_t pipe = (size_t)kWarps * C::WARP_BYTES;
+  const size_t masks = ((kWarps * C::STAGES * 4 + 15) / 16) * 16;
+  const size_t newtok = (D + GP) * sizeof(float);
+  const size_t merge = (size_t)kWarps * GP * (D + 2) * sizeof(float) * (KCH ? 2 : 1);
+  return ((GP * D * 2 + 127) / 128) * 128 + (pipe > merge ? pipe : merge) + masks + newtok;
+}
+
+// NF4 score side: a table of the fp16 level pairs of every code byte (low
+// nibble = even channel), one word per byte value, in kNfLutCopies copies
+// interleaved word by word so that lanes of different copies never share a
+// bank for the same byte value.
+constexpr int kNfLutCopies = 8;
+constexpr size_t kNfLutBytes = 256 * kNfLutCopies * 4;
+template <int BITS, int D, int NG, int GP, bool KCH>
+__host__ __device__ constexpr size_t nf_lut_offset() {
+  return (fast_smem_bytes<BITS, D, NG, GP, KCH>() + 15) / 16 * 16;
+}
+
+// NF4 codes of one 32-bit word to their fp16 levels through that table,
+// byte by byte: o[k] = (level(low nibble), level(high nibble)) of byte k.
+// lut_lane: shared-memory address of this lane's copy.
+__device__ __forceinline__ void nib8_to_h2_nf4_table(uint32_t w, uint32_t (&o)[4],
+                                                     uint32_t lut_lane) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    uint32_t byte;  // byte k of w, zero-extended
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(byte) : "r"(w), "r"(0x4440u + k));
+    // (the table is written before the barrier that precedes every tile,
+    // and w comes from a tile, so the load cannot move ahead of it)
+    asm("ld.shared.u32 %0, [%1];" : "=r"(o[k]) : "r"(lut_lane + byte * (uint32_t)(kNfLutCopies * 4)));
+  }
+}
+
 // Threshold (log2 units) by which a head's tile maximum may exceed the
 // reference maximum before the accumulators are rescaled; probabilities are
 // bounded by 2^kSlack.
@@ -324,7 +364,7 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
   constexpr float kSubK = SUBK ? 16777216.f : 1.f;  // 2^24
   constexpr float kSubV = NF ? 1.f : 16777216.f;
   const float kscale = p.scale_log2 * kSubK;  // K scale factor of the header scratch
-  // NF4: the 8 level magnitudes as fp16 bytes (see nib8_to_h2_nf4)
+  // NF4, value side: the 8 level magnitudes as fp16 bytes (see nib8_to_h2_nf4)
   uint32_t lut[4] = {0u, 0u, 0u, 0u};
   if constexpr (NF) {
 #pragma unroll
@@ -335,6 +375,19 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
     }
   }
   using C = Cfg<BITS, D, NG, GP, KCH>;
+  extern __shared__ __align__(128) uint8_t smem[];
+  // NF4: the score side's level table (see nib8_to_h2_nf4_table), built
+  // from the kernel's own parameters before the wait; the barrier after q is
+  // staged publishes it
+  uint32_t nf_lut_lane = 0u;
+  if constexpr (NF) {
+    uint32_t* t = reinterpret_cast<uint32_t*>(smem + nf_lut_offset<BITS, D, NG, GP, KCH>());
+    for (int i = threadIdx.x; i < 256 * kNfLutCopies; i += blockDim.x) {
+      const int v = i / kNfLutCopies;
+      t[i] = pack_halves(__float2half_rn(p.nf4_level[v & 15]), __float2half_rn(p.nf4_level[v >> 4]));
+    }
+    nf_lut_lane = smem_u32(t + (threadIdx.x & (kNfLutCopies - 1)));
+  }
   // Token-rows layout, whenever the (group, head) pairs fill at most 8 rows
   // of the (group, head)-rows layout: the score mma takes the codes as A
   // (rows = 16 tokens) and q as B (columns = (group, head) pairs), half the
@@ -347,7 +400,6 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
   constexpr bool TQ = GP == 1 || (!KCH && GP <= 4 && NG * GP <= 8) || TQ2;
   // the q n-tile of k-block kb's group (TQ2), else 0
   auto qtile = [](int kb) { return TQ2 ? ((kb * 16) / C::GSZ) / (8 / GP) : 0; };
-  extern __shared__ __align__(128) uint8_t smem[];
   const CacheGeom& geo = p.geom;
   const int split = blockIdx.x, kvh = blockIdx.y;
   const int G = p.G;
@@ -507,6 +559,10 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
       const int i = kb & 3;
       const int x = 64 * (kb >> 2) + 16 * jj + 4 * (i >> 1) + 2 * (i & 1);
       dk[0] = x; dk[1] = x + 8; dk[2] = x + 1; dk[3] = x + 9;
+    } else if constexpr (BITS == 4 && NF) {
+      // the table conversion: byte k of the lane's word holds channels 2k, 2k + 1
+      const int base = 32 * (kb >> 1) + 8 * jj + 4 * (kb & 1);
+      dk[0] = base; dk[1] = base + 1; dk[2] = base + 2; dk[3] = base + 3;
     } else if constexpr (BITS == 4) {
       const int base = 32 * (kb >> 1) + 8 * jj + 2 * (kb & 1);
       dk[0] = base; dk[1] = base + 4; dk[2] = base + 1; dk[3] = base + 5;
@@ -920,8 +976,13 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
                        qa[4 * c + i][0], qa[4 * c + i][2]);
           } else if constexpr (BITS == 4) {
             uint32_t h0[4], h1[4];
-            nib8_to_h2<NF, SUBK>(w[0][c], h0, lut);
-            nib8_to_h2<NF, SUBK>(w[1][c], h1, lut);
+            if constexpr (NF) {
+              nib8_to_h2_nf4_table(w[0][c], h0, nf_lut_lane);
+              nib8_to_h2_nf4_table(w[1][c], h1, nf_lut_lane);
+            } else {
+              nib8_to_h2<NF, SUBK>(w[0][c], h0, lut);
+              nib8_to_h2<NF, SUBK>(w[1][c], h1, lut);
+            }
             if constexpr (TQ2) {
               const int t = qtile(2 * c);  // both k-blocks of the chunk: one group
               mma16816(acc[t], h0[0], h1[0], h0[1], h1[1], qa[2 * c][t], qa[2 * c][2 + t]);
@@ -1054,8 +1115,13 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
           }
         } else if constexpr (BITS == 4) {
           uint32_t h0[4], h1[4];
-          nib8_to_h2<NF, SUBK>(w[0][c], h0, lut);
-          nib8_to_h2<NF, SUBK>(w[1][c], h1, lut);
+          if constexpr (NF) {
+            nib8_to_h2_nf4_table(w[0][c], h0, nf_lut_lane);
+            nib8_to_h2_nf4_table(w[1][c], h1, nf_lut_lane);
+          } else {
+            nib8_to_h2<NF, SUBK>(w[0][c], h0, lut);
+            nib8_to_h2<NF, SUBK>(w[1][c], h1, lut);
+          }
           mma16816(acc[0], Aop[2 * c][0], Aop[2 * c][1], Aop[2 * c][2], Aop[2 * c][3], h0[0], h0[1]);
           mma16816(acc[1], Aop[2 * c][0], Aop[2 * c][1], Aop[2 * c][2], Aop[2 * c][3], h1[0], h1[1]);
           mma16816(acc[0], Aop[2 * c + 1][0], Aop[2 * c + 1][1], Aop[2 * c + 1][2],
@@ -1577,22 +1643,13 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
   }
 }
 
-template <int BITS, int D, int NG, int GP, bool KCH>
-size_t fast_smem_bytes() {
-  using C = Cfg<BITS, D, NG, GP, KCH>;
-  const size_t pipe = (size_t)kWarps * C::WARP_BYTES;
-  const size_t masks = ((kWarps * C::STAGES * 4 + 15) / 16) * 16;
-  const size_t newtok = (D + GP) * sizeof(float);
-  const size_t merge = (size_t)kWarps * GP * (D + 2) * sizeof(float) * (KCH ? 2 : 1);
-  return ((GP * D * 2 + 127) / 128) * 128 + (pipe > merge ? pipe : merge) + masks + newtok;
-}
-
 // Launches the instantiation, or with ctas_per_sm != nullptr only reports
 // how many of its CTAs fit on one SM.
 template <int BITS, int D, int NG, int GP, bool SYM, bool KCH = false, bool NF = false,
           bool PG = false>
 cudaError_t launch_fast_inst(const DecodeParams& p, cudaStream_t stream, int* ctas_per_sm) {
-  const size_t smem = fast_smem_bytes<BITS, D, NG, GP, KCH>();
+  const size_t smem = NF ? nf_lut_offset<BITS, D, NG, GP, KCH>() + kNfLutBytes
+                          : fast_smem_bytes<BITS, D, NG, GP, KCH>();
   static KernelSetup setup;  // the shared-memory attribute and occupancy, once per device
   const cudaError_t e = setup_kernel(decode_fast_kernel<BITS, D, NG, GP, SYM, KCH, NF, PG>, setup,
                                      Cfg<BITS, D, NG, GP, KCH>::THREADS, smem, ctas_per_sm);
