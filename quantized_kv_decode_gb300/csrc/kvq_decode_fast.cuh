@@ -864,9 +864,12 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
         __half* dst = reinterpret_cast<__half*>(ksz_of(buf)) + (jj * C::KB + kb) * 4;
         *reinterpret_cast<uint2*>(dst) =
             make_uint2(pack_halves(blk[dk[0]], blk[dk[1]]), pack_halves(blk[dk[2]], blk[dk[3]]));
+        // (INT4: slots 2j+8, 2j+9 meet the odd nibbles, held as 16c: their
+        // zero-points are stored as 16z, exact in fp16)
+        const uint32_t z23 = pack_halves(blk[D + dk[2]], blk[D + dk[3]]);
         *reinterpret_cast<uint2*>(dst + 4 * 4 * C::KB) =
             make_uint2(pack_halves(blk[D + dk[0]], blk[D + dk[1]]),
-                       pack_halves(blk[D + dk[2]], blk[D + dk[3]]));
+                       BITS == 4 ? h2_as_u32(__hmul2(u32_as_h2(z23), u32_as_h2(0x4C004C00u))) : z23);
       }
     }
   };
@@ -890,7 +893,8 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
     if constexpr (KCH && TQ) {
       // token rows: B column 0 = q s (hi), column 1 = its lo part, so one
       // mma per k-block carries both; -sum z B of both columns comes from
-      // mmas with A = z (every row)
+      // mmas with A = z (every row).  Columns 2..7 repeat the hi part: their
+      // results are never read.
       const __half* sz = reinterpret_cast<const __half*>(ksz) + j * C::KB * 4;
       float ci[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -901,12 +905,10 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
         const __half2 h23 = __hmul2(u32_as_h2(qa[kb][2]), u32_as_h2(sv.y));
         const uint32_t l01 = h2_as_u32(__hfma2(u32_as_h2(qa[kb][0]), u32_as_h2(sv.x), __hneg2(h01)));
         const uint32_t l23 = h2_as_u32(__hfma2(u32_as_h2(qa[kb][2]), u32_as_h2(sv.y), __hneg2(h23)));
-        Bq[kb][0] = rho == 0 ? h2_as_u32(h01) : (rho == 1 ? l01 : 0u);
-        Bq[kb][1] = rho == 0 ? h2_as_u32(h23) : (rho == 1 ? l23 : 0u);
-        const uint32_t z23 = BITS == 4 ? h2_as_u32(__hmul2(u32_as_h2(zv.y), u32_as_h2(0x4C004C00u)))
-                                       : zv.y;
+        Bq[kb][0] = rho == 1 ? l01 : h2_as_u32(h01);
+        Bq[kb][1] = rho == 1 ? l23 : h2_as_u32(h23);
         if constexpr (!SUBK) mma16816(ci, kH1024, kH1024, kH1024, kH1024, Bq[kb][0], Bq[kb][1]);
-        mma16816(ci, zv.x, zv.x, z23, z23, Bq[kb][0], Bq[kb][1]);
+        mma16816(ci, zv.x, zv.x, zv.y, zv.y, Bq[kb][0], Bq[kb][1]);  // zv.y: 16z for INT4
       }
       kci0 = -ci[0];  // column 2j
       kci1 = -ci[1];  // column 2j + 1
@@ -923,11 +925,10 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
         Alo[kb][0] = h2_as_u32(__hfma2(u32_as_h2(qa[kb][0]), u32_as_h2(sv.x), __hneg2(h01)));
         Alo[kb][1] = h2_as_u32(__hfma2(u32_as_h2(qa[kb][2]), u32_as_h2(sv.y), __hneg2(h23)));
         Aop[kb][0] = a01; Aop[kb][1] = a01; Aop[kb][2] = a23; Aop[kb][3] = a23;
-        // slots 2j+8, 2j+9 meet the odd nibbles (held as 16c): their z is 16z
-        const uint32_t z23 = BITS == 4 ? h2_as_u32(__hmul2(u32_as_h2(zv.y), u32_as_h2(0x4C004C00u)))
-                                       : zv.y;
+        // (zv.y: slots 2j+8, 2j+9, which meet the odd nibbles held as 16c,
+        // carry 16z for INT4; the header pass stored them so)
         const uint32_t b0 = rho == 0 ? kH1024 : (rho == 1 ? zv.x : 0u);
-        const uint32_t b1 = rho == 0 ? kH1024 : (rho == 1 ? z23 : 0u);
+        const uint32_t b1 = rho == 0 ? kH1024 : (rho == 1 ? zv.y : 0u);
         mma16816(ci, a01, a01, a23, a23, b0, b1);
         mma16816(ci, Alo[kb][0], Alo[kb][0], Alo[kb][1], Alo[kb][1], b0, b1);
       }
