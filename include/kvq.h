@@ -28,7 +28,8 @@
  *     stream).  Work is enqueued asynchronously; nothing synchronizes.
  *   - Errors that the host can see (bad sizes, null pointers, unsupported
  *     shapes, too small a workspace) are returned synchronously and nothing
- *     is launched.  A failed launch returns KVQ_ERR_CUDA.
+ *     is launched.  A failed launch returns KVQ_ERR_CUDA (with KVQ_VERBOSE
+ *     set in the environment, the CUDA error's name also goes to stderr).
  *   - Errors that only the data reveals (a length beyond the cache, a bad
  *     block-table entry, a group the format cannot store) are OR-ed as
  *     KVQ_FLAG_* bits into *dev_status (a device uint32_t, may be NULL) and
@@ -85,6 +86,14 @@
 
 #include <stddef.h>
 #include <stdint.h>
+
+/* Every entry point below is exported from the shared library; the library
+ * is built with hidden default visibility, so nothing else is. */
+#if defined(__GNUC__)
+#define KVQ_API __attribute__((visibility("default")))
+#else
+#define KVQ_API
+#endif
 
 #ifdef __cplusplus
 extern "C" {
@@ -154,14 +163,14 @@ typedef struct {              /* all device pointers, caller-owned             *
  * "Quantization & inference optimisation", "What the cache costs").  Host
  * arithmetic only.  Returns 0 for an invalid descriptor.
  */
-size_t kvq_cache_bytes(const kvq_cache_desc* desc, int64_t tokens);
+KVQ_API size_t kvq_cache_bytes(const kvq_cache_desc* desc, int64_t tokens);
 
 /*
  * Bytes of each of k_window and v_window for `batch` sequences of an
  * axis-aware cache (batch * num_kv_heads * (sink_tokens + group_size) *
  * head_dim * 2); 0 for other caches or an invalid descriptor.
  */
-size_t kvq_cache_window_bytes(const kvq_cache_desc* desc, int32_t batch);
+KVQ_API size_t kvq_cache_window_bytes(const kvq_cache_desc* desc, int32_t batch);
 
 /*
  * Allocation sizes for one layer's cache: *codes_bytes for each of k_codes
@@ -170,7 +179,7 @@ size_t kvq_cache_window_bytes(const kvq_cache_desc* desc, int32_t batch);
  * cover `batch` sequences of `capacity` slots; PAGED sizes cover num_pages
  * pages (`batch` is ignored).
  */
-kvq_status kvq_cache_array_bytes(const kvq_cache_desc* desc, int32_t batch,
+KVQ_API kvq_status kvq_cache_array_bytes(const kvq_cache_desc* desc, int32_t batch,
                                  size_t* codes_bytes, size_t* header_bytes);
 
 /*
@@ -215,7 +224,7 @@ kvq_status kvq_cache_array_bytes(const kvq_cache_desc* desc, int32_t batch,
  * above.  The tokens that remain in the residual window are then written
  * to their slots.  One call is two kernel launches, in stream order.
  */
-kvq_status kvq_append(const kvq_cache_desc* desc, const kvq_cache* cache,
+KVQ_API kvq_status kvq_append(const kvq_cache_desc* desc, const kvq_cache* cache,
                       int32_t batch, int32_t num_new,
                       const uint16_t* k_new, const uint16_t* v_new,
                       const int32_t* seq_lens_before, uint32_t* dev_status,
@@ -227,7 +236,7 @@ kvq_status kvq_append(const kvq_cache_desc* desc, const kvq_cache* cache,
  * num_splits == 0 lets the library choose from the SM count of the current
  * device (needs a device; returns 0 if none is available).
  */
-int32_t kvq_decode_num_splits(const kvq_cache_desc* desc, int32_t batch,
+KVQ_API int32_t kvq_decode_num_splits(const kvq_cache_desc* desc, int32_t batch,
                               int32_t num_q_heads, int32_t max_seq_len,
                               int32_t num_splits);
 
@@ -235,7 +244,7 @@ int32_t kvq_decode_num_splits(const kvq_cache_desc* desc, int32_t batch,
  * Workspace bytes kvq_decode_attn needs for these arguments (0 when the
  * work runs in one split).  Same num_splits convention as above.
  */
-size_t kvq_decode_workspace_size(const kvq_cache_desc* desc, int32_t batch,
+KVQ_API size_t kvq_decode_workspace_size(const kvq_cache_desc* desc, int32_t batch,
                                  int32_t num_q_heads, int32_t max_seq_len,
                                  int32_t num_splits);
 
@@ -261,7 +270,7 @@ size_t kvq_decode_workspace_size(const kvq_cache_desc* desc, int32_t batch,
  * cache capacity) flags KVQ_FLAG_SEQ_LEN and yields a zero row; a token whose
  * page is unmapped flags KVQ_FLAG_BLOCK_TABLE and is left out.
  */
-kvq_status kvq_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache,
+KVQ_API kvq_status kvq_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache,
                            int32_t batch, int32_t num_q_heads,
                            const uint16_t* q, const int32_t* seq_lens,
                            int32_t max_seq_len, int32_t num_splits,
@@ -301,7 +310,7 @@ kvq_status kvq_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache,
  * context, run the append kernels and the decode in sequence.  Lengths are
  * not modified.
  */
-kvq_status kvq_append_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache,
+KVQ_API kvq_status kvq_append_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache,
                                   int32_t batch, int32_t num_q_heads,
                                   const uint16_t* k_new, const uint16_t* v_new,
                                   const uint16_t* q, const int32_t* seq_lens_before,
@@ -343,7 +352,7 @@ kvq_status kvq_append_decode_attn(const kvq_cache_desc* desc, const kvq_cache* c
  *     covers calls on different streams without ordering between them, and
  *     calls from several host threads. Calls on one stream are safe.
  */
-kvq_status kvq_decode_attn_static_ws(const kvq_cache_desc* desc, const kvq_cache* cache,
+KVQ_API kvq_status kvq_decode_attn_static_ws(const kvq_cache_desc* desc, const kvq_cache* cache,
                                      int32_t batch, int32_t num_q_heads,
                                      const uint16_t* q, const int32_t* seq_lens,
                                      int32_t max_seq_len, int32_t num_splits,
@@ -373,7 +382,7 @@ kvq_status kvq_decode_attn_static_ws(const kvq_cache_desc* desc, const kvq_cache
  */
 
 /* 1 when the loaded library is a debug build (bounds checks compiled in). */
-int32_t kvq_debug_checks(void);
+KVQ_API int32_t kvq_debug_checks(void);
 
 /* The caller arrays a debug build checks, named for kvq_debug_shrink_extent. */
 typedef enum {
@@ -404,10 +413,10 @@ typedef enum {
  * Process-wide host state; not safe to call while another thread launches.
  * Returns KVQ_ERR_INVALID_ARG for an unknown array or bytes < 0.
  */
-kvq_status kvq_debug_shrink_extent(int32_t array, int64_t bytes);
+KVQ_API kvq_status kvq_debug_shrink_extent(int32_t array, int64_t bytes);
 
 /* Static, human-readable name of a status code. */
-const char* kvq_status_string(kvq_status status);
+KVQ_API const char* kvq_status_string(kvq_status status);
 
 #ifdef __cplusplus
 }

@@ -24,8 +24,13 @@ LIB_DEBUG = os.path.join(PKG, "libkvq_debug.so")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 
 ARCH = "-gencode=arch=compute_103a,code=sm_103a"
+# Hidden default visibility: the library exports its C ABI (KVQ_API in
+# include/kvq.h) and nothing else, so that two builds loaded in one process
+# (release and debug) share no C++ symbol, in particular no function-local
+# static of a template (GCC would make those process-wide unique symbols).
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", ARCH, "-Xcompiler", "-fPIC",
-              "-Xcompiler", "-Wall", "--expt-relaxed-constexpr"]
+              "-Xcompiler", "-Wall", "-Xcompiler", "-fvisibility=hidden",
+              "--expt-relaxed-constexpr"]
 
 
 def _nvcc() -> str:

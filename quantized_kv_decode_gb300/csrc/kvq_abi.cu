@@ -3,6 +3,8 @@
 // No function here allocates memory or synchronizes a stream.
 #include <cuda.h>  // driver types for the context identifier (no libcuda link)
 #include <math.h>
+#include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <algorithm>
@@ -120,6 +122,15 @@ kvq_status check_cache(const kvq_cache_desc* d, const kvq_cache* c) {
       (!c->k_window || !c->v_window || !aligned(c->k_window) || !aligned(c->v_window)))
     return KVQ_ERR_INVALID_ARG;
   return KVQ_OK;
+}
+
+// A failed CUDA call maps to KVQ_ERR_CUDA; with KVQ_VERBOSE set in the
+// environment its name also goes to stderr.
+kvq_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return KVQ_OK;
+  static const bool verbose = getenv("KVQ_VERBOSE") != nullptr;
+  if (verbose) fprintf(stderr, "kvq: CUDA error %d (%s)\n", (int)e, cudaGetErrorName(e));
+  return KVQ_ERR_CUDA;
 }
 
 int sm_count() {
@@ -255,7 +266,7 @@ kvq_status make_plan(const kvq_cache_desc* desc, const CacheGeom& geom, int32_t 
     probe.G = G;
     bool handled = false;
     cudaError_t e = launch_decode_fast(probe, desc->bits, gp, nullptr, &handled, &occ);
-    if (handled && e != cudaSuccess) return KVQ_ERR_CUDA;
+    if (handled && e != cudaSuccess) return from_cuda(e);
     plan->fast = handled;
     if (handled) plan->occ = occ;
   }
@@ -281,7 +292,6 @@ kvq_status make_plan(const kvq_cache_desc* desc, const CacheGeom& geom, int32_t 
   return plan->splits > 0 ? KVQ_OK : KVQ_ERR_CUDA;
 }
 
-kvq_status from_cuda(cudaError_t e) { return e == cudaSuccess ? KVQ_OK : KVQ_ERR_CUDA; }
 
 #ifdef KVQ_DEBUG
 // Bytes kvq_debug_shrink_extent takes off each array's extent.
@@ -531,7 +541,7 @@ kvq_status decode_impl(const kvq_cache_desc* desc, const kvq_cache* cache, int32
     probe.G = G;
     bool fast = false;
     const cudaError_t pe = launch_decode_fast(probe, desc->bits, plan.gp, nullptr, &fast, &occ);
-    if (fast && pe != cudaSuccess) return KVQ_ERR_CUDA;
+    if (fast && pe != cudaSuccess) return from_cuda(pe);
     if (!fast) occ = 0;
   }
   p.rows32 = desc->layout == KVQ_PAGED &&

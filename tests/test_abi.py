@@ -42,6 +42,21 @@ def test_library_exports_every_declared_symbol(K):
     assert sorted(K._lib.SIGNATURES) == declared_functions()
 
 
+def test_library_exports_nothing_else(K):
+    """The library is built with hidden default visibility: its dynamic
+    symbol table holds the C ABI and nothing else, so two builds loaded in
+    one process (release and debug) share no C++ symbol."""
+    import shutil
+    import subprocess
+    nm = shutil.which("nm")
+    if nm is None:
+        pytest.skip("nm not available")
+    out = subprocess.run([nm, "-D", "--defined-only", K._lib.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    names = sorted(line.split()[-1] for line in out.splitlines() if line.strip())
+    assert names == declared_functions()
+
+
 def test_status_strings(K):
     for st in range(5):
         assert K.kvq_status_string(st).startswith("KVQ_")
