@@ -180,3 +180,33 @@ def _call_sizes(K, case, run, splits):
         "KVQ_ARRAY_WORKSPACE": K.kvq_decode_workspace_size(desc, case.B, case.Hq, lmax, splits),
         "KVQ_ARRAY_BLOCK_TABLE": case.B * desc.max_blocks_per_seq * 4,
     }
+
+
+def test_release_and_debug_builds_in_one_process(debug_lib):
+    """Both builds loaded in one process keep their own kernel set-up: calls
+    alternate between them (each library's first call on a shape sets its
+    own shared-memory attribute), every call succeeds, each build repeats
+    its own output bit for bit, and both match the reference run."""
+    import torch
+    import quantized_kv_decode_gb300 as K
+    from quantized_kv_decode_gb300 import _lib
+    release = _lib.load(_lib.LIB_PATH)
+    assert release.kvq_debug_checks() == 0
+    case = Case(B=3, Hq=12, Hkv=4, D=128, bits=4, g=32, lens=_lens(333, 7, 120), seed=31)
+    inp = make_inputs(case)
+    ref = run_gpu(case, inp)                        # debug library (the fixture routes to it)
+    q = torch.from_numpy(inp["q"]).cuda()
+    lens = torch.from_numpy(case.lens.astype(np.int32) + 1).cuda()
+    outs = []
+    for handle in (release, debug_lib, release, debug_lib):
+        prev = _lib.use(handle)
+        try:
+            st = torch.zeros(1, dtype=torch.int32, device="cuda")
+            outs.append(K.kvq_decode_attn(ref["cache"], q, lens, inp["Lctx"] + 1, dev_status=st))
+            torch.cuda.synchronize()
+            assert int(st.item()) == 0
+        finally:
+            _lib.use(prev)
+    assert torch.equal(outs[0], outs[2]) and torch.equal(outs[1], outs[3])
+    for o in outs[:2]:
+        assert_close(o.cpu().numpy(), ref["out"].astype(np.float64))
