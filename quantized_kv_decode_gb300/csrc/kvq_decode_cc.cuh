@@ -1,7 +1,8 @@
-// CUDA-core split-K decode attention for the shapes the tensor-core kernel
-// does not take: fp16 caches, head_dim 256, more than 8 query heads per KV
-// head, INT4 / NF4 with groups of 8/16 channels or one group per head, INT2
-// at head_dim 64 or with more (group, head) columns than one V-mma n-tile.
+// CUDA-core split-K decode attention for the shapes the tensor-core kernels
+// do not take: head_dim 256, more than 8 query heads per KV head (fp16
+// caches included), INT4 / NF4 with groups of 8/16 channels or one group per
+// head, INT2 at head_dim 64 or with more (group, head) columns than one
+// V-mma n-tile.
 //
 // What it computes is the decode step of "Quantization & inference
 // optimisation" ("Prefill, then decode": scores = K q / sqrt(d), softmax,

@@ -202,3 +202,27 @@ def test_magnitudes(bits, g, sym, nf4, k_mul, v_mul):
         ref, _ = oracle_step(c, inp)
         assert run["status"] == 0
         assert_close(run["out"], ref)
+
+
+@pytest.mark.parametrize("D,Hq,Hkv,layout", [
+    (128, 4, 4, "dense"),    # one query head per KV head
+    (128, 16, 4, "dense"),   # 4 heads per KV head
+    (64, 14, 2, "dense"),    # 7 heads padded to 8, head_dim 64
+    (128, 8, 2, "paged"),    # paged, 4 heads
+    (64, 6, 2, "paged"),     # paged, 3 heads padded to 4, head_dim 64
+])
+def test_fp16_tensor_core(D, Hq, Hkv, layout):
+    """fp16 caches on the tensor-core kernel (16-token tiles): lengths around
+    the tile (0, 15, 16, 17 cached tokens) and a longer one, one and several
+    splits, and the fused step (append kernel, then the decode)."""
+    rng = np.random.default_rng(D + Hq + Hkv)
+    lens = np.array([0, 15, 16, 17, int(rng.integers(300, 900))])
+    c = Case(B=5, Hq=Hq, Hkv=Hkv, D=D, bits=16, g=0, lens=lens, seed=int(lens.sum()) % 89,
+             layout=layout, page_size=16)
+    for s in (0, 1, 3):
+        _check(c, num_splits=s)
+    inp = make_inputs(c)
+    run = run_gpu(c, inp, num_splits=2, fused=True)
+    ref, _ = oracle_step(c, inp)
+    assert run["status"] == 0
+    assert_close(run["out"], ref)
