@@ -56,7 +56,8 @@ PATHS = [
     ("nf4", Case(B=2, Hq=8, Hkv=2, D=128, bits=4, g=64, lens=_lens(180, 20), seed=8, nf4=True), 0, True),
     ("int2", Case(B=2, Hq=4, Hkv=4, D=128, bits=2, g=32, lens=_lens(170, 9), seed=9), 0, True),
     ("cuda_core_g8", Case(B=2, Hq=8, Hkv=2, D=128, bits=4, g=8, lens=_lens(120, 40), seed=10), 2, False),
-    ("cuda_core_fp16", Case(B=2, Hq=4, Hkv=2, D=128, bits=16, g=0, lens=_lens(90, 33), seed=11), 0, True),
+    ("fp16_tensor_core", Case(B=2, Hq=4, Hkv=2, D=128, bits=16, g=0, lens=_lens(90, 33), seed=11), 0, True),
+    ("cuda_core_fp16_d256", Case(B=2, Hq=2, Hkv=1, D=256, bits=16, g=0, lens=_lens(60, 21), seed=13), 2, False),
     ("cuda_core_g16_heads", Case(B=2, Hq=32, Hkv=2, D=64, bits=8, g=32, lens=_lens(77, 140), seed=12), 0, False),
 ]
 
