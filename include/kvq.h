@@ -107,6 +107,10 @@ typedef enum {
   KVQ_ERR_CUDA = 4          /* a CUDA runtime call or launch failed          */
 } kvq_status;
 
+/* Largest batch of one decode call (and of one append on an axis-aware
+ * cache): the kernels take the sequence from a grid dimension. */
+#define KVQ_MAX_BATCH 65535
+
 /* Bits OR-ed into the caller's device status word. */
 #define KVQ_FLAG_SEQ_LEN      0x1u /* position/length outside the cache        */
 #define KVQ_FLAG_BLOCK_TABLE  0x2u /* block-table entry outside [0,num_pages)  */
@@ -223,6 +227,8 @@ KVQ_API kvq_status kvq_cache_array_bytes(const kvq_cache_desc* desc, int32_t bat
  * tokens, and each V token per group of g channels, with the formulas
  * above.  The tokens that remain in the residual window are then written
  * to their slots.  One call is two kernel launches, in stream order.
+ * Axis-aware caches take at most KVQ_MAX_BATCH sequences per call (larger:
+ * KVQ_ERR_UNSUPPORTED before any launch).
  */
 KVQ_API kvq_status kvq_append(const kvq_cache_desc* desc, const kvq_cache* cache,
                       int32_t batch, int32_t num_new,
@@ -268,7 +274,9 @@ KVQ_API size_t kvq_decode_workspace_size(const kvq_cache_desc* desc, int32_t bat
  * an online softmax over token tiles and, when split, a log-sum-exp merge of
  * the per-split partials.  A length below 0 or above min(max_seq_len,
  * cache capacity) flags KVQ_FLAG_SEQ_LEN and yields a zero row; a token whose
- * page is unmapped flags KVQ_FLAG_BLOCK_TABLE and is left out.
+ * page is unmapped flags KVQ_FLAG_BLOCK_TABLE and is left out.  batch is at
+ * most KVQ_MAX_BATCH (one grid row per sequence); a larger batch returns
+ * KVQ_ERR_UNSUPPORTED before any launch.
  */
 KVQ_API kvq_status kvq_decode_attn(const kvq_cache_desc* desc, const kvq_cache* cache,
                            int32_t batch, int32_t num_q_heads,

@@ -415,6 +415,7 @@ kvq_status kvq_append(const kvq_cache_desc* desc, const kvq_cache* cache, int32_
   if ((st = check_cache(desc, cache)) != KVQ_OK) return st;
   if (batch < 0 || num_new < 0) return KVQ_ERR_INVALID_ARG;
   if (batch == 0 || num_new == 0) return KVQ_OK;
+  if (desc->k_per_channel && batch > KVQ_MAX_BATCH) return KVQ_ERR_UNSUPPORTED;
   if (!k_new || !v_new || !seq_lens_before) return KVQ_ERR_INVALID_ARG;
   if (!aligned(k_new) || !aligned(v_new) || !aligned(seq_lens_before)) return KVQ_ERR_INVALID_ARG;
   p.geom.block_table = cache->block_table;
@@ -485,7 +486,7 @@ kvq_status decode_impl(const kvq_cache_desc* desc, const kvq_cache* cache, int32
   if (fused ? (!aligned(lens_before) || !aligned(k_new) || !aligned(v_new)) : !aligned(seq_lens))
     return KVQ_ERR_INVALID_ARG;
   const int G = num_q_heads / desc->num_kv_heads;
-  if (G > kMaxGroupHeads) return KVQ_ERR_UNSUPPORTED;
+  if (G > kMaxGroupHeads || batch > KVQ_MAX_BATCH) return KVQ_ERR_UNSUPPORTED;
 
   Plan plan;
   if ((st = make_plan(desc, p.geom, batch, num_q_heads, max_seq_len, num_splits, &plan)) != KVQ_OK)

@@ -133,6 +133,13 @@ def test_append_and_decode_validate_before_launch(K):
     # too many query heads per KV head for the kernels
     assert lib.kvq_decode_attn(byref(d), byref(fake), 1, 2 * 17, 16, 16, 64, 1, 0.0, 16, None,
                                0, None, None) == K.KVQ_ERR_UNSUPPORTED
+    # more sequences than a grid dimension holds
+    assert lib.kvq_decode_attn(byref(d), byref(fake), 65536, 2, 16, 16, 64, 1, 0.0, 16, None,
+                               0, None, None) == K.KVQ_ERR_UNSUPPORTED
+    kd = K.make_desc(4, 32, 2, 128, K.KVQ_DENSE, 64, k_per_channel=True, sink_tokens=4)
+    kfake = K.kvq_cache(16, 32, 48, 64, 80, 96, None, 112, 128)
+    assert lib.kvq_append(byref(kd), byref(kfake), 65536, 1, 16, 16, 16, None,
+                          None) == K.KVQ_ERR_UNSUPPORTED
     # explicit split count needs a workspace
     assert lib.kvq_decode_attn(byref(d), byref(fake), 1, 2, 16, 16, 640, 4, 0.0, 16, None, 0,
                                None, None) == K.KVQ_ERR_WORKSPACE
