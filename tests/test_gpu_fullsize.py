@@ -30,7 +30,7 @@ def _run(w, bits, n_samples=3, seed_offset=0, kind="asym", group_size=None):
     dev = "cuda"
     rng = synth.rng_for(w.seed + seed_offset)
     B, Hq, Hkv, D = w.batch, w.num_q_heads, w.num_kv_heads, w.head_dim
-    g = group_size or w.group_size
+    g = w.group_size if group_size is None else group_size
     opts = dict(symmetric=kind == "sym", nf4=kind == "nf4")
     lens = synth.context_lengths(rng, B, *w.ctx)            # cached tokens before the step
     Lmax = int(lens.max())
@@ -139,8 +139,9 @@ def test_fullsize_paged_int4():
 
 
 @pytest.mark.parametrize("kind,bits,g", [("sym", 4, None), ("nf4", 4, 64), ("asym", 2, None),
-                                         ("asym", 8, None)])
+                                         ("asym", 8, None), ("fp16", 16, 0)])
 def test_fullsize_mha7b_formats(kind, bits, g):
     """The 7B-class workload in the benchmark's launch configuration for the
-    comparator formats: symmetric INT4, NF4 g64, INT2, INT8."""
+    comparator formats: symmetric INT4, NF4 g64, INT2, INT8, and the fp16
+    cache (the tensor-core fp16 kernel)."""
     _run(synth.WORKLOADS["mha7b"], bits, n_samples=8, kind=kind, group_size=g)
