@@ -233,7 +233,7 @@ def test_lowbit_descriptors(K):
 def test_release_library_has_no_debug_checks(K):
     """The release library reports no bounds checks and refuses the
     debug-only extent control (host functions, no launch)."""
-    lib = K.lib()
+    lib = K._lib.load(K._lib.LIB_PATH)
     assert lib.kvq_debug_checks() == 0
     assert lib.kvq_debug_shrink_extent(K._lib.KVQ_ARRAY_K_CODES, 16) == K.KVQ_ERR_UNSUPPORTED
     assert K._lib.KVQ_ARRAY_WORKSPACE == 14   # the header's kvq_array order
