@@ -586,10 +586,12 @@ kvq_status decode_impl(const kvq_cache_desc* desc, const kvq_cache* cache, int32
     else e = append_first();
   }
   if (e == cudaSuccess && fast_format(desc, G)) {
+    p.merge_all = splits > 1;
     e = launch_decode_fast(p, desc->bits, plan.gp, s, &handled, nullptr);
   }
   if (e == cudaSuccess && !handled) {
     p.kch_append = 0;
+    p.merge_all = 0;
     if (fused && !appended) e = append_first();
     if (e == cudaSuccess) e = launch_decode_generic(p, s);
   }

@@ -489,7 +489,17 @@ __global__ void __launch_bounds__(Cfg<BITS, D, NG, GP, KCH>::THREADS, Cfg<BITS, 
   }
   const int t0 = split * p.chunk;
   const int t1 = min(L, t0 + p.chunk);
-  if (p.splits > 1 && t0 >= L) return;  // the merge reads splits < ceil(L / chunk) only
+  if (p.splits > 1 && t0 >= L) {
+    // no tokens in this split: the merge skips it by its m = -inf
+    if (p.merge_all && threadIdx.x < G) {
+      float* mlo = p.ws_ml + (((long long)b * p.Hq + (long long)kvh * G + threadIdx.x) * p.splits + split) * 2;
+      if (KVQ_IN(geo, KVQ_ARRAY_WORKSPACE, mlo, 8)) {
+        mlo[0] = -INFINITY;
+        mlo[1] = 0.f;
+      }
+    }
+    return;
+  }
   // Longest-first grids learn their sequence only here: warm the new K/V
   // rows a fused step's append reads while q is staged.
   if (!KCH && p.longest_first && p.lens_before != nullptr && L > 0 && L - 1 >= t0 && L - 1 < t1 &&

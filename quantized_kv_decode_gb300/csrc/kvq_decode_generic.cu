@@ -228,7 +228,14 @@ __global__ void __launch_bounds__(kThreads) decode_generic_kernel(const DecodePa
 
 // out[b][h] = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s over the splits
 // that hold tokens of sequence b.  One CTA per (b, h), one thread per
-// channel; the loop rescales as it goes so that every load is independent.
+// channel.  The splits go in batches of kMergeBatch whose loads are all
+// issued before any is used, then one rescale per batch, so a call pays
+// about one memory latency per batch (most calls: one batch).  After the
+// tensor-core kernel (merge_all) every split carries a partial or the
+// marker m = -inf, and the merge needs no length: a marked split's o is
+// loaded but not used.  After the others only the ceil(len / chunk) splits
+// that hold tokens are read.
+constexpr int kMergeBatch = 16;
 __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
   pdl_launch_dependents();
   pdl_wait();  // the partials of the decode kernel before it
@@ -236,22 +243,46 @@ __global__ void __launch_bounds__(256) merge_kernel(const DecodeParams p) {
   const int b = (int)(rowid / p.Hq);
   const int D = p.geom.D;
   const int d = threadIdx.x;
-  const int L = seq_len_of(p, b);
-  const int nv = (L <= 0 || L > p.len_limit) ? 0 : (L + p.chunk - 1) / p.chunk;
+  int nv = p.splits;
+  if (!p.merge_all) {
+    const int L = seq_len_of(p, b);
+    nv = (L <= 0 || L > p.len_limit) ? 0 : (L + p.chunk - 1) / p.chunk;
+  }
   const float* ml = p.ws_ml + rowid * p.splits * 2;
   const float* o = p.ws_o + rowid * p.splits * D + d;
   float M = -INFINITY, num = 0.f, den = 0.f;
-#pragma unroll 4
-  for (int s = 0; s < nv; ++s) {
-    if (!KVQ_IN(p.geom, KVQ_ARRAY_WORKSPACE, ml + 2 * s, 8) ||
-        !KVQ_IN(p.geom, KVQ_ARRAY_WORKSPACE, o + (long long)s * D, 4))
-      continue;
-    const float m = ml[2 * s], l = ml[2 * s + 1], x = o[(long long)s * D];
-    if (m == -INFINITY) continue;
-    const float Mn = fmaxf(M, m);
-    const float a = exp2f(M - Mn), f = exp2f(m - Mn);
-    num = fmaf(f, x, num * a);
-    den = fmaf(f, l, den * a);
+  for (int s0 = 0; s0 < nv; s0 += kMergeBatch) {
+    float m[kMergeBatch], l[kMergeBatch], x[kMergeBatch];
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) {
+      const int s = s0 + u;
+      m[u] = -INFINITY;
+      l[u] = 0.f;
+      x[u] = 0.f;
+      if (s < nv && KVQ_IN(p.geom, KVQ_ARRAY_WORKSPACE, ml + 2 * s, 8) &&
+          KVQ_IN(p.geom, KVQ_ARRAY_WORKSPACE, o + (long long)s * D, 4)) {
+        const float2 v = *reinterpret_cast<const float2*>(ml + 2 * s);
+        m[u] = v.x;
+        l[u] = v.y;
+        x[u] = o[(long long)s * D];  // loaded with m, l: one latency
+      }
+    }
+    float Mn = M;
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) Mn = fmaxf(Mn, m[u]);
+    if (Mn == -INFINITY) continue;
+    const float a = exp2f(M - Mn);  // 0 while nothing is merged yet
+    num *= a;
+    den *= a;
+#pragma unroll
+    for (int u = 0; u < kMergeBatch; ++u) {
+      // a split with no live token (or the marker) adds nothing; its o may
+      // be a stale value of any bits, so it is not multiplied in
+      if (m[u] == -INFINITY) continue;
+      const float f = exp2f(m[u] - Mn);
+      num = fmaf(f, x[u], num);
+      den = fmaf(f, l[u], den);
+    }
     M = Mn;
   }
   if (d < D && KVQ_IN(p.geom, KVQ_ARRAY_OUT, p.out + rowid * D + d, 2))

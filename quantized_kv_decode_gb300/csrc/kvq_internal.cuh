@@ -187,6 +187,10 @@ struct DecodeParams {
   // tensor-core kernel first appends its (sequence, KV head)'s new token
   // (window slot, or the block it completes), then attends
   int32_t kch_append;
+  // Split calls of the tensor-core kernel: every split CTA writes its
+  // partial, a split past the sequence's end the marker m = -inf, so the
+  // merge reads all splits without the lengths
+  int32_t merge_all;
 };
 
 // lens[b] (a length array of the call), or `bad` when a debug build finds the
