@@ -110,8 +110,9 @@ def check_guards(guards: dict, where: str):
     assert not bad, f"{where}: bytes written outside {bad}"
 
 
-def run_gpu(c: Case, inp, num_splits=0, repeat=1, fused=False):
-    """fused: the step's token is appended by kvq_append_decode_attn in the
+def run_gpu(c: Case, inp, num_splits=0, repeat=1, fused=False, ws_fill=None):
+    """ws_fill: a byte written over the whole split workspace before the calls
+    (its contents need no init).  fused: the step's token is appended by kvq_append_decode_attn in the
     same call as the attention instead of a separate kvq_append.  Every cache
     array, the output and the split workspace sit between guard bytes that
     are checked after each call."""
@@ -146,6 +147,8 @@ def run_gpu(c: Case, inp, num_splits=0, repeat=1, fused=False):
     if ws_bytes:
         guards["workspace"] = Guarded((ws_bytes,), torch.uint8, dev)
     ws = guards["workspace"].tensor if ws_bytes else None
+    if ws is not None and ws_fill is not None:
+        ws.fill_(ws_fill)
     outs = []
     for _ in range(repeat):
         guards["out"] = Guarded(q.shape, torch.float16, dev)

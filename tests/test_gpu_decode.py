@@ -226,3 +226,22 @@ def test_fp16_tensor_core(D, Hq, Hkv, layout):
     ref, _ = oracle_step(c, inp)
     assert run["status"] == 0
     assert_close(run["out"], ref)
+
+
+@pytest.mark.parametrize("g", [32, 8])  # tensor-core kernel (marked empty splits) / CUDA-core kernel
+@pytest.mark.parametrize("fused", [False, True])
+def test_split_workspace_needs_no_init(g, fused):
+    """Split calls over a workspace filled with NaN bytes, or with bytes of a
+    large finite float: sequences shorter than a split leave splits with no
+    tokens, whose workspace rows the merge must not use (after the
+    tensor-core kernel they carry the m = -inf marker and a stale o)."""
+    lens = np.array([300, 5, 64, 0, 1000, 33, 257, 129])
+    c = Case(B=8, Hq=8, Hkv=2, D=128, bits=4, g=g, lens=lens, seed=31)
+    inp = make_inputs(c)
+    ref, _ = oracle_step(c, inp)
+    for fill in (0xFF, 0x7F):
+        run = run_gpu(c, inp, num_splits=4, fused=fused, ws_fill=fill, repeat=2)
+        assert run["status"] == 0
+        for out in run["outs"]:
+            assert np.isfinite(out).all()
+            assert_close(out, ref)
