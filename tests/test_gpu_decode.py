@@ -245,3 +245,51 @@ def test_split_workspace_needs_no_init(g, fused):
         for out in run["outs"]:
             assert np.isfinite(out).all()
             assert_close(out, ref)
+
+
+@pytest.mark.parametrize("graph", [False, True])
+def test_split_merge_across_calls(graph):
+    """Split calls on one workspace (filled with NaN bytes first), with a new
+    q before every call, eagerly or replayed from one CUDA graph: partials
+    and empty-split markers left by the call before never leak into this
+    call's merge (each output against the oracle for its own q)."""
+    import torch
+    import quantized_kv_decode_gb300 as K
+    c = Case(B=3, Hq=8, Hkv=2, D=128, bits=4, g=32, lens=np.array([900, 40, 1500]), seed=41)
+    inp = make_inputs(c)
+    run = run_gpu(c, inp, num_splits=4)
+    cache, desc = run["cache"], run["desc"]
+    rows = inp["Lctx"] + 1
+    assert K.kvq_decode_num_splits(desc, c.B, c.Hq, rows, 4) == 4
+    lens1 = torch.from_numpy((c.lens + 1).astype(np.int32)).cuda()
+    q_buf = torch.empty((c.B, c.Hq, c.D), dtype=torch.float16, device="cuda")
+    out = torch.empty_like(q_buf)
+    ws = torch.full((K.kvq_decode_workspace_size(desc, c.B, c.Hq, rows, 4),), 0xFF,
+                    dtype=torch.uint8, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def call():
+        K.kvq_decode_attn(cache, q_buf, lens1, rows, out=out, workspace=ws, dev_status=status,
+                          num_splits=4, stream=stream)
+
+    rng = np.random.default_rng(5)
+    step = call
+    if graph:
+        with torch.cuda.stream(stream):
+            call()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            call()
+        step = g.replay
+    for _ in range(3):
+        q = synth.host_q(rng, c.B, c.Hq, c.D)
+        q_buf.copy_(torch.from_numpy(q))
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            step()
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        ref, _ = oracle_step(c, dict(inp, q=q))
+        assert_close(out.cpu().numpy(), ref)
