@@ -20,8 +20,9 @@
 namespace {
 
 // The split partials ([batch][heads][splits][head_dim] o, then m and l) of
-// one call. Every partial a merge reads is written earlier in the same
-// call, so nothing here has to start at zero and nothing is cleared.
+// one call. Every (m, l) a merge reads is written earlier in the same call,
+// and an o is used only when its split's m says it holds tokens, so nothing
+// here has to start at zero and nothing is cleared.
 __device__ __align__(256) unsigned char g_split_scratch[KVQ_STATIC_WORKSPACE_BYTES];
 
 std::mutex g_setup_mutex;
